@@ -1,0 +1,211 @@
+"""ctypes front end of the CPU oracle (``qvg_oracle.cpp``) -- test
+infrastructure only.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this module.  Arrays are numpy; bf16 tensors travel as
+their uint16 bit patterns.  Layouts are per head unit (``[N][D]`` rows); the
+tests reshape the CUDA library's ``[S][H][N][...]`` buffers to compare.
+"""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "qvg_oracle.cpp")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(force=False):
+    """Compile the oracle with g++ (-O2, no FMA contraction, no fast-math)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    cmd = ["g++", "-O2", "-std=c++17", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+           "-shared", "-o", _LIB + ".tmp", _SRC]
+    subprocess.check_call(cmd)
+    os.replace(_LIB + ".tmp", _LIB)
+    return _LIB
+
+
+P = ctypes.c_void_p
+I64 = ctypes.c_int64
+I32 = ctypes.c_int
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB)
+        L.or_to_bf16.argtypes = [ctypes.c_double]
+        L.or_to_bf16.restype = ctypes.c_uint16
+        L.or_to_f16.argtypes = [ctypes.c_float]
+        L.or_to_f16.restype = ctypes.c_uint16
+        L.or_f16_to_f32.argtypes = [ctypes.c_uint16]
+        L.or_f16_to_f32.restype = ctypes.c_float
+        L.or_kmeans_init.argtypes = [P, I64, I32, I32, P]
+        L.or_assign.argtypes = [P, I64, I32, P, I32, P, P]
+        L.or_update.argtypes = [P, I64, I32, P, I32, P, P]
+        L.or_fit.argtypes = [P, I64, I32, I32, I32, P, P, P]
+        L.or_prq_encode.argtypes = [P, I64, I32, P, P, I32, I32, P, P]
+        L.or_decode.argtypes = [P, P, P, P, I64, I32, I32, I32, P]
+        L.or_stream.argtypes = [P, I64, I32, I32, I32, I32, I32, I32, I32, P, P, P, P, P]
+        L.or_stream.restype = I32
+        L.or_coral_predict.argtypes = [P, I64, I32, I32, P, P, P, I32, P]
+        L.or_coral_encode_layer.argtypes = [P, P, I64, I32, I32, P, P, P, I32, P, I32, I32, P, P, P, P]
+        L.or_coral_decode_layer.argtypes = [P, I64, I32, I32, P, P, P, I32, P, I32, I32, P, P, P]
+        L.or_bits_per_element.argtypes = [I32, I32, I32, I32, I32, I64, I32]
+        L.or_bits_per_element.restype = ctypes.c_double
+        _lib = L
+    return _lib
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# ----------------------------------------------------------------- formats --
+
+def to_bf16(v):
+    return lib().or_to_bf16(float(v))
+
+
+def to_f16(v):
+    return lib().or_to_f16(float(np.float32(v)))
+
+
+def f16_to_f32(h):
+    return lib().or_f16_to_f32(int(h))
+
+
+# ------------------------------------------------------------------ k-means --
+
+def kmeans_init(x, C):
+    x = _c(x, np.uint16)
+    N, D = x.shape
+    cent = np.empty((C, D), np.uint16)
+    lib().or_kmeans_init(_p(x), N, D, C, _p(cent))
+    return cent
+
+
+def assign(x, cent, return_dist=False):
+    x = _c(x, np.uint16)
+    cent = _c(cent, np.uint16)
+    N, D = x.shape
+    ids = np.empty(N, np.int32)
+    dmin = np.empty(N, np.float64)
+    lib().or_assign(_p(x), N, D, _p(cent), cent.shape[0], _p(ids), _p(dmin))
+    return (ids, dmin) if return_dist else ids
+
+
+def update(x, ids, cent):
+    x = _c(x, np.uint16)
+    ids = _c(ids, np.int32)
+    out = _c(cent, np.uint16).copy()
+    N, D = x.shape
+    counts = np.empty(out.shape[0], np.int64)
+    lib().or_update(_p(x), N, D, _p(ids), out.shape[0], _p(out), _p(counts))
+    return out, counts
+
+
+def fit(x, C, T, warm=None):
+    x = _c(x, np.uint16)
+    N, D = x.shape
+    cent = np.empty((C, D), np.uint16)
+    ids = np.empty(N, np.int32)
+    w = None if warm is None else _c(warm, np.uint16)
+    lib().or_fit(_p(x), N, D, C, T, _p(w), _p(cent), _p(ids))
+    return cent, ids
+
+
+# --------------------------------------------------------------------- PRQ --
+
+def prq_encode(x, cent, ids, S, G):
+    """codes [S][N][D/16] uint32, meta [S][N][D/G] uint32 (lo = fp16 scale,
+    hi = fp16 zero)."""
+    x = _c(x, np.uint16)
+    N, D = x.shape
+    codes = np.empty((S, N, D // 16), np.uint32)
+    meta = np.empty((S, N, D // G), np.uint32)
+    c = None if cent is None else _c(cent, np.uint16)
+    i = None if ids is None else _c(ids, np.int32)
+    lib().or_prq_encode(_p(x), N, D, _p(c), _p(i), S, G, _p(codes), _p(meta))
+    return codes, meta
+
+
+def decode(codes, meta, ids, cent, G):
+    codes = _c(codes, np.uint32)
+    meta = _c(meta, np.uint32)
+    S, N, W = codes.shape
+    D = W * 16
+    out = np.empty((N, D), np.uint16)
+    c = None if cent is None else _c(cent, np.uint16)
+    i = None if ids is None else _c(ids, np.int32)
+    lib().or_decode(_p(codes), _p(meta), _p(i), _p(c), N, D, S, G, _p(out))
+    return out
+
+
+def stream(x, chunk, steps, refit_every, C, T, S, G):
+    x = _c(x, np.uint16)
+    D = x.shape[1]
+    Ntot = chunk * steps
+    versions = np.zeros((steps, C, D), np.uint16)
+    cver = np.empty(steps, np.int32)
+    ids = np.empty(Ntot, np.int32)
+    codes = np.empty((S, Ntot, D // 16), np.uint32)
+    meta = np.empty((S, Ntot, D // G), np.uint32)
+    nv = lib().or_stream(_p(x), chunk, steps, refit_every, D, C, T, S, G, _p(versions),
+                         _p(cver), _p(ids), _p(codes), _p(meta))
+    return versions[:nv], cver, ids, codes, meta
+
+
+# ------------------------------------------------------------------- Coral --
+
+def coral_predict(xh, B, U, W, H, D):
+    xh = _c(xh, np.uint16)
+    N = xh.shape[0]
+    R = U.shape[1]
+    pred = np.empty((N, H * D), np.float64)
+    lib().or_coral_predict(_p(xh), N, H, D, _p(_c(B, np.uint16)), _p(_c(U, np.uint16)),
+                           _p(_c(W, np.uint16)), R, _p(pred))
+    return pred
+
+
+def coral_encode_layer(xh_prev, x_next, B, U, W, H, D, S, G, pred_in=None):
+    x_next = _c(x_next, np.uint16)
+    N = x_next.shape[0]
+    R = 0 if U is None else U.shape[1]
+    codes = np.empty((S, H, N, D // 16), np.uint32)
+    meta = np.empty((S, H, N, D // G), np.uint32)
+    xh_next = np.empty((N, H * D), np.uint16)
+    pred_out = np.empty((N, H * D), np.float32)
+    xp = None if xh_prev is None else _c(xh_prev, np.uint16)
+    pi = None if pred_in is None else _c(pred_in, np.float32)
+    cv = (lambda a: None if a is None else _c(a, np.uint16))
+    lib().or_coral_encode_layer(_p(xp), _p(x_next), N, H, D, _p(cv(B)), _p(cv(U)), _p(cv(W)), R,
+                                _p(pi), S, G, _p(codes), _p(meta), _p(xh_next), _p(pred_out))
+    return codes, meta, xh_next, pred_out
+
+
+def coral_decode_layer(xh_prev, codes, meta, B, U, W, H, D, G, pred_in=None):
+    codes = _c(codes, np.uint32)
+    meta = _c(meta, np.uint32)
+    S, _, N, _ = codes.shape
+    R = 0 if U is None else U.shape[1]
+    xh_next = np.empty((N, H * D), np.uint16)
+    xp = None if xh_prev is None else _c(xh_prev, np.uint16)
+    pi = None if pred_in is None else _c(pred_in, np.float32)
+    cv = (lambda a: None if a is None else _c(a, np.uint16))
+    lib().or_coral_decode_layer(_p(xp), N, H, D, _p(cv(B)), _p(cv(U)), _p(cv(W)), R, _p(pi), S, G,
+                                _p(codes), _p(meta), _p(xh_next))
+    return xh_next
+
+
+def bits_per_element(S, b, G, C, D, N, V=1):
+    return lib().or_bits_per_element(S, b, G, C, D, N, V)
