@@ -1,0 +1,419 @@
+"""Throughput of the KV-cache codec on one B300 (or N independent replicas).
+
+One step = the whole hot path over one Wan2.1-1.3B-shaped cache: for each of
+the 30 layers and both K and V (token-major [32760][12][128] bf16), the
+per-head k-means fit (C=256, 4 Lloyd iterations), the 2-stage 2-bit PRQ
+encode and the decode back to bf16.  value = bf16 KV bytes processed per
+second (6.04 GB per step), inputs resident in HBM; every layer's input
+(201 MB) is larger than L2.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--config wan|large|stream|coral|tiny]
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KV-cache 2-bit encode/decode GB/s of bf16 KV; % of B300 HBM peak"
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p["hbm_gbs"], p["bf16_tflops"], p["bf16_tflops_sustained"], "measured"
+    except Exception:
+        return 6400.0, 1800.0, 1400.0, "fallback"
+
+
+def source_hash(*files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel, src_files):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's
+    source has not changed since it was captured; else None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)
+        e = t[kernel]
+        if e["source_hash"] != source_hash(*src_files):
+            return None
+        return e["dram_bytes_per_launch"]
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            p = [x.strip() for x in ln.split(",")]
+            if len(p) < 8:
+                continue
+            try:
+                sm.append(float(p[0]))
+                mx = float(p[1])
+            except ValueError:
+                continue
+            for name, v in zip(names, p[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------- workload --
+
+def workload(name):
+    from synth import workloads as WL
+    return WL.SHORT[name]
+
+
+class QvgStep:
+    """Device buffers and the launch sequence of one step of the QVG path."""
+
+    def __init__(self, Q, wl, layers):
+        import torch
+        from synth import gpu as SG
+        self.Q, self.wl, self.L = Q, wl, layers
+        H, D, N = wl.heads, wl.head_dim, wl.tokens
+        self.cfg = Q.config(H, D, wl.clusters, wl.lloyd_iters, wl.stages, wl.group_size)
+        self.x = [[SG.mixture_layer_gpu(wl, l, t, layout="nhd") for t in (0, 1)] for l in range(layers)]
+        self.enc = [[Q.alloc_encoded(self.cfg, N) for _ in (0, 1)] for _ in range(layers)]
+        self.ws = Q.alloc_workspace(self.cfg, N)
+        self.out = [torch.empty((N, H, D), dtype=torch.int16, device="cuda") for _ in range(2)]
+        self.N, self.H, self.D = N, H, D
+        self.bytes_per_step = 2 * layers * N * H * D * 2
+
+    def fit(self, l, t):
+        e, N, D, H = self.enc[l][t], self.N, self.D, self.H
+        self.Q.qvg_fit_centroids(self.cfg, self.x[l][t], N, D, H * D, None, e["centroids"], e["ids"], N, 0, self.ws)
+
+    def assign(self, l, t):
+        e, N, D, H = self.enc[l][t], self.N, self.D, self.H
+        self.Q.qvg_assign(self.cfg, self.x[l][t], N, D, H * D, e["centroids"], e["ids"], N, 0, self.ws)
+
+    def encode(self, l, t):
+        e, N, D, H = self.enc[l][t], self.N, self.D, self.H
+        self.Q.qvg_encode(self.cfg, self.x[l][t], N, D, H * D, e["centroids"], 0, e["codes"], e["meta"], e["ids"],
+                          N, 0, self.ws)
+
+    def decode(self, l, t):
+        e, N, D, H = self.enc[l][t], self.N, self.D, self.H
+        self.Q.qvg_decode(self.cfg, e["codes"], e["meta"], e["ids"], e["centroids"], N, 0, N, self.out[t], D, H * D)
+
+    def step(self):
+        for l in range(self.L):
+            for t in (0, 1):
+                self.fit(l, t)
+                self.encode(l, t)
+                self.decode(l, t)
+
+    def compressed_bytes(self):
+        cb, mb, ib, xb = self.Q.qvg_encoded_bytes(self.cfg, self.N, 1)
+        return cb + mb + ib + xb
+
+
+def time_fn(fn, reps, stream=None):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s)
+    for _ in range(reps):
+        fn()
+    b.record(s)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps / 1e3
+
+
+def kernel_rooflines(st, peaks, reps=3):
+    """Average per-launch time of each kernel family over all 60 (layer,
+    tensor) units, and its algorithmic bytes or flops per launch."""
+    hbm, tf_burst, tf_sus, kind = peaks
+    wl, L = st.wl, st.L
+    elems = st.N * st.H * st.D                      # one tensor of one layer
+    S, G, C, D = wl.stages, wl.group_size, wl.clusters, wl.head_dim
+    code_b = S * (2 / 8 + 4 / G)                    # code + meta bytes per element
+    id_b = 1 / D
+    units = [(l, t) for l in range(L) for t in (0, 1)]
+
+    def over_units(f):
+        return lambda: [f(l, t) for (l, t) in units]
+
+    t_dec = time_fn(over_units(st.decode), reps) / len(units)
+    t_enc = time_fn(over_units(st.encode), reps) / len(units)
+    t_asg = time_fn(over_units(st.assign), reps) / len(units)
+    t_fit = time_fn(over_units(st.fit), 1) / len(units)
+    dec_bytes = elems * (code_b + id_b + 2)
+    enc_bytes = elems * (2 + id_b + code_b)
+    asg_flops = 2.0 * C * elems                     # token-by-centroid distance GEMM
+    out = {
+        "decode": {"bound": "hbm", "achieved": dec_bytes / t_dec / 1e9, "peak": hbm, "unit": "GB/s",
+                   "time_us": t_dec * 1e6, "algorithmic_bytes": dec_bytes},
+        "encode": {"bound": "hbm", "achieved": enc_bytes / t_enc / 1e9, "peak": hbm, "unit": "GB/s",
+                   "time_us": t_enc * 1e6, "algorithmic_bytes": enc_bytes},
+        "assign": {"bound": "tensor", "achieved": asg_flops / t_asg / 1e12, "peak": tf_burst, "unit": "TFLOP/s",
+                   "time_us": t_asg * 1e6, "algorithmic_flops": asg_flops},
+        "fit": {"bound": "tensor", "achieved": wl.lloyd_iters * asg_flops / t_fit / 1e12, "peak": tf_sus,
+                "unit": "TFLOP/s", "time_us": t_fit * 1e6},
+    }
+    for v in out.values():
+        v["frac"] = v["achieved"] / v["peak"]
+        v["peak_kind"] = kind
+    out["decode"]["bf16_gbs"] = elems * 2 / t_dec / 1e9
+    out["encode"]["bf16_gbs"] = elems * 2 / t_enc / 1e9
+    return out
+
+
+# ------------------------------------------------------------ CPU oracle --
+
+def _oracle_unit(args):
+    name, layer, tensor, head = args
+    import time as _t
+    from oracle import oracle as O
+    from synth import synth as SY
+    wl = workload(name)
+    x = SY.mixture_unit(wl, layer, tensor, head)
+    t0 = _t.perf_counter()
+    cent, ids = O.fit(x, wl.clusters, wl.lloyd_iters)
+    codes, meta = O.prq_encode(x, cent, ids, wl.stages, wl.group_size)
+    O.decode(codes, meta, ids, cent, wl.group_size)
+    return _t.perf_counter() - t0, x.size * 2
+
+
+def cpu_baseline(name, max_units=None):
+    """The oracle as it stands on this host's cores: one (layer, tensor, head)
+    unit per worker process, all units in parallel; throughput = bf16 bytes of
+    the units / wall time."""
+    import multiprocessing as mp
+    from oracle import oracle as O
+    O.build()
+    wl = workload(name)
+    cores = os.cpu_count() or 1
+    n = min(cores, 8 if max_units is None else max_units)
+    units = [(name, (i * 7) % wl.layers, i % 2, (i * 5) % wl.heads) for i in range(n)]
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(n) as pool:
+        res = pool.map(_oracle_unit, units)
+    wall = max(r[0] for r in res)
+    nbytes = sum(r[1] for r in res)
+    return {"value": nbytes / wall / 1e9, "unit": "GB/s", "cores": n, "kind": "oracle",
+            "sample": f"{n} (layer, tensor, head) units of {wl.name} ({wl.tokens} tokens x {wl.head_dim}), "
+                      f"fit T={wl.lloyd_iters} + encode + decode, one unit per process, all concurrent; "
+                      f"slowest unit {wall:.1f} s (timed inside the worker, generation excluded)"}
+
+
+# ------------------------------------------------------------------ main --
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    name = args.config
+    wl = workload(name)
+    t0 = time.perf_counter()
+    per_step = []
+    for _ in range(args.warmup):
+        cpu_baseline(name, max_units=2)
+    for _ in range(args.steps):
+        per_step.append(cpu_baseline(name, max_units=2))
+    wall = time.perf_counter() - t0
+    v = statistics.median(p["value"] for p in per_step)
+    cb = dict(per_step[-1])
+    cb["value"] = v
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall / max(1, args.steps + args.warmup) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64/f32",
+            "data": "synthetic", "config": config_block(wl, args),
+            "cpu_baseline": cb, "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def config_block(wl, args):
+    return {"workload": f"{wl.name}: {wl.layers} layers x {wl.heads} heads x head_dim {wl.head_dim} x {wl.tokens} "
+                        f"tokens, K and V bf16 token-major; C={wl.clusters} T={wl.lloyd_iters} S={wl.stages} "
+                        f"b=2 G={wl.group_size}",
+            "layers": wl.layers, "heads": wl.heads, "head_dim": wl.head_dim, "tokens": wl.tokens,
+            "clusters": wl.clusters, "lloyd_iters": wl.lloyd_iters, "stages": wl.stages, "group_size": wl.group_size,
+            "l2": "inputs larger than L2 (one layer's K or V is %.0f MB)" % (wl.tokens * wl.heads * wl.head_dim * 2 / 1e6),
+            "parallelism": f"replicas x{args.gpus}"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="wan", choices=["wan", "large"])
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    import __graft_entry__ as GE
+    GE.build()
+    import kv_cache_quantization_means_b300 as Q
+    Q.load()
+    wl = workload(args.config)
+    peaks = load_peaks()
+    layers = wl.layers if args.config == "wan" else 2
+    st = QvgStep(Q, wl, layers)
+    torch.cuda.synchronize()
+
+    graph = None
+    if not args.no_graph:
+        st.step()                                   # eager warm-up (sets kernel attributes)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            st.step()
+        run = graph.replay
+    else:
+        run = st.step
+    for _ in range(args.warmup):
+        run()
+    torch.cuda.synchronize()
+    barrier()
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        barrier()
+        s = torch.cuda.current_stream()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        for _ in range(args.steps):
+            run()
+        b.record(s)
+        torch.cuda.synchronize()
+        barrier()
+    t = a.elapsed_time(b) / 1e3 / args.steps
+    if world > 1:
+        tt = torch.tensor([t], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t = tt.item()
+    value = st.bytes_per_step * world / t / 1e9
+    launches_per_step = 2 * layers * (1 + wl.lloyd_iters * 4 + 2)
+
+    roof = kernel_rooflines(st, peaks)
+
+    # end to end through the C ABI with host buffers: pinned H2D of every
+    # layer's K/V, fit + encode + decode, D2H of the compressed stream
+    e2e = None
+    if not args.no_e2e:
+        host_x = [[st.x[l][t].cpu().pin_memory() for t in (0, 1)] for l in range(layers)]
+        host_out = [torch.empty(st.compressed_bytes(), dtype=torch.uint8).pin_memory() for _ in (0, 1)]
+
+        def e2e_step():
+            for l in range(layers):
+                for t in (0, 1):
+                    st.x[l][t].copy_(host_x[l][t], non_blocking=True)
+                    st.fit(l, t)
+                    st.encode(l, t)
+                    st.decode(l, t)
+                    e = st.enc[l][t]
+                    o = 0
+                    for k in ("codes", "meta", "ids", "centroids"):
+                        nb = e[k].numel() * e[k].element_size()
+                        host_out[t][o:o + nb].copy_(e[k].view(torch.uint8), non_blocking=True)
+                        o += nb
+        e2e_step()
+        te = time_fn(e2e_step, max(1, min(args.steps, 3)))
+        e2e = {"value": st.bytes_per_step * world / te / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": st.bytes_per_step, "d2h_bytes_per_step": 2 * layers * st.compressed_bytes()}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(args.config)
+
+    dom = max(("assign", "decode", "encode"), key=lambda k: roof[k]["time_us"])
+    src = {"assign": ["kv_cache_quantization_means_b300/csrc/kmeans.cu"],
+           "decode": ["kv_cache_quantization_means_b300/csrc/prq.cu"],
+           "encode": ["kv_cache_quantization_means_b300/csrc/prq.cu"]}
+    rl = {k: roof[dom][k] for k in ("bound", "achieved", "peak", "unit", "frac")}
+    rl["kernel"] = dom
+    rl["traffic"] = traffic_for(dom, src[dom])
+    rl["peak_kind"] = roof[dom]["peak_kind"]
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded mixture-of-Gaussians bf16 KV cache)",
+            "config": config_block(wl, args), "roofline": rl,
+            "kernels": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items()}
+                        for k, v in roof.items()},
+            "hbm_frac_of_nominal_8tbs": {k: roof[k]["achieved"] / 8000.0 for k in ("decode", "encode")},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk.summary(), "cuda_graph": graph is not None}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

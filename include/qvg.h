@@ -1,0 +1,223 @@
+/*
+ * qvg.h -- C ABI of the B300 KV-cache codec (libqvg.so).
+ *
+ * Two codecs for the key/value cache of an autoregressive video diffusion
+ * model, after the pages they come from:
+ *
+ *  - Quant VideoGen (QVG; gist.science explainer of arXiv 2602.02958,
+ *    "Sommario tecnico"): semantic-aware smoothing (sec. 2A: per-head k-means
+ *    along the sequence axis, subtraction of each token's centroid) followed
+ *    by progressive residual quantisation (sec. 2B: several stages of 2-bit
+ *    quantisation, each coding what the previous stages left; decoding
+ *    dequantises, sums the stages and adds the centroid back).  Centroid
+ *    caching (sec. 3) gives the streaming append call.
+ *  - Coral-KV (news items on the preprint, section "cross-layer
+ *    prediction"): layer l+1 is predicted from the reconstruction of layer l
+ *    by a block-diagonal-per-head plus global low-rank (block-DPLR) map and
+ *    only the prediction residual is quantised.
+ *
+ * Conventions for every call
+ *  - Pointers named x, centroids, codes, meta, ids, out, workspace, B, U, W,
+ *    xhat_* and pred are DEVICE pointers into caller-owned memory; the library
+ *    never allocates, frees or synchronises.  A qvg_config / qvg_cache /
+ *    coral_predictor struct itself lives in host memory.
+ *  - bf16 and fp16 values travel as their 16-bit patterns (qvg_bf16).
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and returns before it runs.  Calls are capturable in a CUDA graph
+ *    except qvg_append_chunk, whose host-side bookkeeping happens at call time.
+ *  - Arguments are validated on the host before anything is launched; a bad
+ *    argument returns QVG_ERR_INVALID_ARG (or QVG_ERR_UNSUPPORTED for a shape
+ *    outside the supported set, QVG_ERR_CAPACITY for a full cache) and
+ *    launches nothing.  A failed launch returns QVG_ERR_CUDA.  The message of
+ *    the last failure on the calling thread is qvg_last_error().  No C++
+ *    exception crosses this boundary.
+ *
+ * Supported shapes: head_dim D in {32, 64, 128, 256} (k-means: D <= 128);
+ * group_size G in {16, 32, 64, 128} dividing D; num_stages S in 1..4;
+ * bits = 2; num_clusters C in 0..256 (0 = no smoothing).  Pointers must be
+ * 16-byte aligned and strides multiples of 8 elements.
+ *
+ * Encoded layout of one (layer, tensor) with `capacity` token rows per head:
+ *   codes : uint32 [S][H][capacity][D/16]; element j of a row sits in word
+ *           j/16, bits 2*(j%16) .. 2*(j%16)+1 (least significant first).
+ *   meta  : uint32 [S][H][capacity][D/G]; low half = fp16 scale s, high half
+ *           = fp16 zero-point z of the group; a code q decodes to q*s + z.
+ *   ids   : uint8  [H][capacity] cluster of each token row (C > 0 only).
+ *   centroids : bf16 [V][H][C][D], V centroid-table versions (V = 1 unless
+ *           streaming).
+ * Compressed bits per element = S*2 + 32*S/G + [C > 0]*(8/D + 16*C*V/N).
+ */
+#ifndef QVG_H
+#define QVG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QVG_API __attribute__((visibility("default")))
+#else
+#define QVG_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t qvg_bf16;
+typedef void* qvg_stream;
+
+typedef enum {
+    QVG_OK = 0,
+    QVG_ERR_INVALID_ARG = 1,
+    QVG_ERR_UNSUPPORTED = 2,
+    QVG_ERR_CAPACITY = 3,
+    QVG_ERR_CUDA = 4,
+    QVG_ERR_TIMEOUT = 5
+} qvg_status;
+
+typedef struct {
+    int32_t num_heads;     /* H */
+    int32_t head_dim;      /* D */
+    int32_t num_clusters;  /* C, 0 = no smoothing */
+    int32_t lloyd_iters;   /* T, Lloyd iterations of qvg_fit_centroids */
+    int32_t num_stages;    /* S */
+    int32_t bits;          /* bits per code, must be 2 */
+    int32_t group_size;    /* G, elements per (scale, zero) along D */
+} qvg_config;
+
+/* Streaming cache of one (layer, tensor).  Device buffers are caller-owned;
+ * the counters are host-side state that qvg_append_chunk advances. */
+typedef struct {
+    uint32_t* codes;         /* [S][H][capacity][D/16] */
+    uint32_t* meta;          /* [S][H][capacity][D/G]  */
+    uint8_t* ids;            /* [H][capacity]          */
+    qvg_bf16* centroids;     /* [max_versions][H][C][D] */
+    int64_t* chunk_offset;   /* device [max_chunks + 1], first token of chunk i; [n_chunks] = n_used */
+    int32_t* chunk_version;  /* device [max_chunks], centroid version of chunk i */
+    int64_t capacity;        /* token rows per head */
+    int32_t max_versions;
+    int32_t max_chunks;      /* <= 4096 */
+    int64_t n_used;          /* tokens appended so far (host) */
+    int32_t n_versions;      /* centroid tables written so far (host) */
+    int32_t n_chunks;        /* chunks appended so far (host) */
+} qvg_cache;
+
+/* Block-DPLR predictor of layer l+1 from layer l (Coral-KV):
+ * pred[n][h*D+o] = sum_i B[h][o][i] x[n][h*D+i] + sum_r U[h*D+o][r] t[n][r],
+ * t[n][r] = sum_j W[j][r] x[n][j].  All bf16, device. */
+typedef struct {
+    const qvg_bf16* B;   /* [H][D][D] (out x in) */
+    const qvg_bf16* U;   /* [H*D][R] */
+    const qvg_bf16* W;   /* [H*D][R] */
+    int32_t rank;        /* R, 0 = block-diagonal only; R % 16 == 0, R <= 64 */
+} coral_predictor;
+
+/* Message of the last failed call on this thread ("" if none). */
+QVG_API const char* qvg_last_error(void);
+
+/* Library version string. */
+QVG_API const char* qvg_version(void);
+
+/* Bytes of each encoded buffer for `capacity` token rows and `n_versions`
+ * centroid tables (host only; any output pointer may be NULL).  Follows the
+ * layout above; ids and centroids are 0 when C = 0. */
+QVG_API qvg_status qvg_encoded_bytes(const qvg_config* cfg, int64_t capacity, int32_t n_versions,
+                             size_t* codes_bytes, size_t* meta_bytes, size_t* ids_bytes,
+                             size_t* centroid_bytes);
+
+/* Scratch bytes that qvg_fit_centroids / qvg_encode / qvg_update /
+ * qvg_append_chunk / coral_* need for `n_tokens` tokens (host only). */
+QVG_API qvg_status qvg_workspace_bytes(const qvg_config* cfg, int64_t n_tokens, size_t* bytes);
+
+/* SAS k-means (QVG sec. 2A items 1-2 and sec. 3): per head, T Lloyd iterations
+ * of (assign, update) on the n_tokens rows of x.  x is bf16 with logical
+ * layout [H][n_tokens][D]: row (h, n) starts at x + h*head_stride +
+ * n*token_stride (elements; D contiguous).  Initial centroids are
+ * warm_start ([H][C][D]) when non-NULL, else the tokens floor(j*n/C).
+ * Writes the last update's centroids ([H][C][D]) and the last assignment's
+ * ids to ids[h*capacity + tok_offset + n].  Assignment is the exact argmin of
+ * the squared Euclidean distance (lowest index on ties); an empty cluster
+ * keeps its centroid; a centroid is the exact mean of its tokens rounded to
+ * bf16.  Needs n_tokens >= 1 and C >= 1.  `workspace` (qvg_workspace_bytes)
+ * must not be shared with concurrent calls. */
+QVG_API qvg_status qvg_fit_centroids(const qvg_config* cfg, const qvg_bf16* x, int64_t n_tokens,
+                             int64_t head_stride, int64_t token_stride, const qvg_bf16* warm_start,
+                             qvg_bf16* centroids, uint8_t* ids, int64_t capacity, int64_t tok_offset,
+                             void* workspace, size_t workspace_bytes, qvg_stream stream);
+
+/* Assign step alone: ids[h*capacity + tok_offset + n] = argmin_j ||x - c_j||^2. */
+QVG_API qvg_status qvg_assign(const qvg_config* cfg, const qvg_bf16* x, int64_t n_tokens,
+                      int64_t head_stride, int64_t token_stride, const qvg_bf16* centroids,
+                      uint8_t* ids, int64_t capacity, int64_t tok_offset, void* workspace,
+                      size_t workspace_bytes, qvg_stream stream);
+
+/* Update step alone: centroids (in/out, [H][C][D]) <- mean of their tokens
+ * under ids; empty clusters unchanged. */
+QVG_API qvg_status qvg_update(const qvg_config* cfg, const qvg_bf16* x, int64_t n_tokens,
+                      int64_t head_stride, int64_t token_stride, const uint8_t* ids,
+                      int64_t capacity, int64_t tok_offset, qvg_bf16* centroids, void* workspace,
+                      size_t workspace_bytes, qvg_stream stream);
+
+/* QVG encode (sec. 2A item 3 and sec. 2B items 1-2): per token row,
+ * r = x - c[id] in fp32 (r = x when C = 0), then for each stage and group of G
+ * channels s = fp16((max r - min r)/3), z = fp16(min r),
+ * q = clamp(rint((r - z) * fp32(1/s)), 0, 3) (0 when s = 0), r <- r - (q*s + z).
+ * Rows go to rows tok_offset .. tok_offset+n_tokens-1 of codes/meta/ids.
+ * assign = 0: ids are read from `ids` (e.g. written by qvg_fit_centroids);
+ * assign = 1: ids are first computed against `centroids` and written there. */
+QVG_API qvg_status qvg_encode(const qvg_config* cfg, const qvg_bf16* x, int64_t n_tokens,
+                      int64_t head_stride, int64_t token_stride, const qvg_bf16* centroids,
+                      int32_t assign, uint32_t* codes, uint32_t* meta, uint8_t* ids,
+                      int64_t capacity, int64_t tok_offset, void* workspace, size_t workspace_bytes,
+                      qvg_stream stream);
+
+/* QVG decode (sec. 2B item 3): rows [tok_begin, tok_end) of every head,
+ * x_hat = bf16(((c[id] + d_1) + d_2) + ...), d_s = q_s*s_s + z_s in fp32,
+ * written to out + h*out_head_stride + (n - tok_begin)*out_token_stride. */
+QVG_API qvg_status qvg_decode(const qvg_config* cfg, const uint32_t* codes, const uint32_t* meta,
+                      const uint8_t* ids, const qvg_bf16* centroids, int64_t capacity,
+                      int64_t tok_begin, int64_t tok_end, qvg_bf16* out, int64_t out_head_stride,
+                      int64_t out_token_stride, qvg_stream stream);
+
+/* Streaming append (centroid caching, QVG sec. 3): encodes n_new new tokens
+ * at row cache->n_used.  refit != 0: the chunk is fitted (T iterations,
+ * warm-started from the newest table, cold when there is none) and the result
+ * is pushed as a new table version; refit == 0: the chunk's tokens are
+ * assigned to the newest table.  Advances n_used, n_chunks (and n_versions).
+ * QVG_ERR_CAPACITY if rows, chunks or versions would overflow. */
+QVG_API qvg_status qvg_append_chunk(const qvg_config* cfg, qvg_cache* cache, const qvg_bf16* x,
+                            int64_t n_new, int64_t head_stride, int64_t token_stride,
+                            int32_t refit, void* workspace, size_t workspace_bytes,
+                            qvg_stream stream);
+
+/* Decode rows [tok_begin, tok_end) of a streaming cache, each chunk against
+ * its own centroid version. */
+QVG_API qvg_status qvg_decode_cache(const qvg_config* cfg, const qvg_cache* cache, int64_t tok_begin,
+                            int64_t tok_end, qvg_bf16* out, int64_t out_head_stride,
+                            int64_t out_token_stride, qvg_stream stream);
+
+/* Coral-KV closed-loop encode of one layer (cfg->num_clusters must be 0):
+ * pred = block-DPLR(xhat_prev) in fp32 (0 when xhat_prev is NULL: first
+ * layer), r = x_next - pred, PRQ-coded per head row into codes/meta
+ * ([S][H][n_tokens][...]), and xhat_next = bf16(((pred + d_1) + d_2) + ...)
+ * written for the next layer.  xhat_prev, x_next, xhat_next are token-major
+ * [n_tokens][H*D].  pred_out ([n_tokens][H*D] fp32) may be NULL; when given it
+ * receives the prediction (for staged checks). */
+QVG_API qvg_status coral_predict_encode(const qvg_config* cfg, const coral_predictor* pred,
+                                const qvg_bf16* xhat_prev, const qvg_bf16* x_next, int64_t n_tokens,
+                                uint32_t* codes, uint32_t* meta, qvg_bf16* xhat_next, float* pred_out,
+                                void* workspace, size_t workspace_bytes, qvg_stream stream);
+
+/* Decoder twin of coral_predict_encode: rebuilds xhat_next from xhat_prev,
+ * the predictor and the stored codes (bit-identical to the encoder's
+ * xhat_next). */
+QVG_API qvg_status coral_predict_decode(const qvg_config* cfg, const coral_predictor* pred,
+                                const qvg_bf16* xhat_prev, int64_t n_tokens, const uint32_t* codes,
+                                const uint32_t* meta, qvg_bf16* xhat_next, float* pred_out,
+                                void* workspace, size_t workspace_bytes, qvg_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QVG_H */

@@ -1,0 +1,462 @@
+// C ABI of the KV-cache codec: host-side validation, workspace carving and
+// launch sequencing.  Declarations and contracts: include/qvg.h.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+qvg_status fail(qvg_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+qvg_status ok() {
+    g_err[0] = '\0';
+    return QVG_OK;
+}
+
+qvg_status cuda_status(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return ok();
+    return fail(QVG_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+constexpr int kMaxChunks = 4096;   // chunk table is staged in shared memory by the decoder
+
+qvg_status check_config(const qvg_config* c, bool need_clusters) {
+    if (!c) return fail(QVG_ERR_INVALID_ARG, "config is NULL");
+    if (c->num_heads < 1) return fail(QVG_ERR_INVALID_ARG, "num_heads must be >= 1");
+    if (c->bits != 2) return fail(QVG_ERR_UNSUPPORTED, "bits must be 2 (got %d)", c->bits);
+    const int D = c->head_dim, G = c->group_size;
+    if (D != 32 && D != 64 && D != 128 && D != 256)
+        return fail(QVG_ERR_UNSUPPORTED, "head_dim must be 32, 64, 128 or 256 (got %d)", D);
+    if (G != 16 && G != 32 && G != 64 && G != 128)
+        return fail(QVG_ERR_UNSUPPORTED, "group_size must be 16, 32, 64 or 128 (got %d)", G);
+    if (G > D || D % G) return fail(QVG_ERR_INVALID_ARG, "group_size %d must divide head_dim %d", G, D);
+    if (c->num_stages < 1 || c->num_stages > qvg::kMaxStages)
+        return fail(QVG_ERR_UNSUPPORTED, "num_stages must be in 1..%d", qvg::kMaxStages);
+    if (c->num_clusters < 0 || c->num_clusters > qvg::kMaxClusters)
+        return fail(QVG_ERR_UNSUPPORTED, "num_clusters must be in 0..%d", qvg::kMaxClusters);
+    if (c->num_clusters > 0 && D > 128)
+        return fail(QVG_ERR_UNSUPPORTED, "k-means smoothing supports head_dim <= 128");
+    if (need_clusters && c->num_clusters < 1)
+        return fail(QVG_ERR_INVALID_ARG, "this call needs num_clusters >= 1");
+    return QVG_OK;
+}
+
+qvg_status check_input(const qvg_config* c, const void* x, int64_t n, int64_t hs, int64_t ts,
+                       const char* name) {
+    if (n < 0) return fail(QVG_ERR_INVALID_ARG, "%s: negative token count", name);
+    if (n == 0) return QVG_OK;
+    if (!x) return fail(QVG_ERR_INVALID_ARG, "%s is NULL", name);
+    if (!aligned16(x)) return fail(QVG_ERR_INVALID_ARG, "%s must be 16-byte aligned", name);
+    if (hs % 8 || ts % 8) return fail(QVG_ERR_INVALID_ARG, "%s strides must be multiples of 8 elements", name);
+    if (ts < c->head_dim && c->num_heads > 0 && hs < c->head_dim)
+        return fail(QVG_ERR_INVALID_ARG, "%s strides overlap rows", name);
+    if (hs < 0 || ts < 0) return fail(QVG_ERR_INVALID_ARG, "%s strides must be non-negative", name);
+    return QVG_OK;
+}
+
+qvg_status check_rows(int64_t cap, int64_t off, int64_t n) {
+    if (cap < 0 || off < 0 || n < 0) return fail(QVG_ERR_INVALID_ARG, "negative capacity/offset/count");
+    if (off + n > cap)
+        return fail(QVG_ERR_CAPACITY, "rows [%lld, %lld) exceed capacity %lld", (long long)off,
+                    (long long)(off + n), (long long)cap);
+    return QVG_OK;
+}
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+struct FitWorkspace {
+    int* counts;        // [H][C]
+    int* cursors;       // [H][C]
+    int* perm;          // [H][N]
+    long long* sum_hi;  // [H][C][D]
+    long long* sum_lo;  // [H][C][D]
+    unsigned long long* stats;  // [4]
+    size_t bytes;
+};
+
+FitWorkspace carve(const qvg_config* c, int64_t n, void* base) {
+    const size_t H = c->num_heads, C = c->num_clusters > 0 ? c->num_clusters : 1, D = c->head_dim;
+    FitWorkspace w{};
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = o;
+        o += align256(bytes);
+        return base ? (void*)((char*)base + at) : nullptr;
+    };
+    w.counts = (int*)take(sizeof(int) * H * C * 2);    // counts and cursors, contiguous
+    w.cursors = w.counts ? w.counts + H * C : nullptr;
+    w.perm = (int*)take(sizeof(int) * H * (size_t)(n > 0 ? n : 1));
+    w.sum_hi = (long long*)take(sizeof(long long) * H * C * D);
+    w.sum_lo = (long long*)take(sizeof(long long) * H * C * D);
+    w.stats = (unsigned long long*)take(sizeof(unsigned long long) * 4);
+    w.bytes = o;
+    return w;
+}
+
+qvg_status check_workspace(const qvg_config* c, int64_t n, void* ws, size_t ws_bytes, FitWorkspace* out) {
+    FitWorkspace need = carve(c, n, nullptr);
+    if (!ws) return fail(QVG_ERR_INVALID_ARG, "workspace is NULL (need %zu bytes)", need.bytes);
+    if (((uintptr_t)ws & 255u) != 0) return fail(QVG_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    if (ws_bytes < need.bytes)
+        return fail(QVG_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", ws_bytes, need.bytes);
+    *out = carve(c, n, ws);
+    return QVG_OK;
+}
+
+qvg::AssignArgs assign_args(const qvg_config* c, const qvg_bf16* x, int64_t n, int64_t hs, int64_t ts,
+                            const qvg_bf16* cent, uint8_t* ids, int64_t cap, int64_t off, int* counts,
+                            unsigned long long* stats) {
+    qvg::AssignArgs a;
+    a.x = x; a.head_stride = hs; a.token_stride = ts; a.n_tokens = n;
+    a.cent = cent; a.C = c->num_clusters;
+    a.ids = ids; a.cap = cap; a.tok_offset = off;
+    a.counts = counts; a.stats = stats;
+    return a;
+}
+
+qvg::UpdateArgs update_args(const qvg_config* c, const qvg_bf16* x, int64_t n, int64_t hs, int64_t ts,
+                            const uint8_t* ids, int64_t cap, int64_t off, const FitWorkspace& w,
+                            qvg_bf16* cent) {
+    qvg::UpdateArgs u;
+    u.x = x; u.head_stride = hs; u.token_stride = ts; u.n_tokens = n;
+    u.ids = ids; u.cap = cap; u.tok_offset = off;
+    u.H = c->num_heads; u.C = c->num_clusters;
+    u.counts = w.counts; u.cursors = w.cursors; u.perm = w.perm;
+    u.sum_hi = w.sum_hi; u.sum_lo = w.sum_lo; u.cent = cent;
+    return u;
+}
+
+// T Lloyd iterations (init already in `cent`).
+qvg_status lloyd(const qvg_config* c, const qvg_bf16* x, int64_t n, int64_t hs, int64_t ts,
+                 qvg_bf16* cent, uint8_t* ids, int64_t cap, int64_t off, const FitWorkspace& w,
+                 cudaStream_t s) {
+    const size_t H = c->num_heads, C = c->num_clusters, D = c->head_dim;
+    cudaError_t e = cudaMemsetAsync(w.sum_hi, 0, sizeof(long long) * H * C * D, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(w.sum_lo, 0, sizeof(long long) * H * C * D, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(w.stats, 0, sizeof(unsigned long long) * 4, s);
+    if (e != cudaSuccess) return cuda_status(e, "memset");
+    for (int t = 0; t < c->lloyd_iters; ++t) {
+        e = cudaMemsetAsync(w.counts, 0, sizeof(int) * H * C * 2, s);
+        if (e != cudaSuccess) return cuda_status(e, "memset");
+        e = qvg::launch_assign(c->head_dim, c->num_heads,
+                               assign_args(c, x, n, hs, ts, cent, ids, cap, off, w.counts, w.stats), s);
+        if (e != cudaSuccess) return cuda_status(e, "assign launch");
+        e = qvg::launch_update(c->head_dim, update_args(c, x, n, hs, ts, ids, cap, off, w, cent), s);
+        if (e != cudaSuccess) return cuda_status(e, "update launch");
+    }
+    return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* qvg_last_error(void) { return g_err; }
+
+const char* qvg_version(void) { return "qvg-b300 0.1 (sm_103a)"; }
+
+qvg_status qvg_encoded_bytes(const qvg_config* cfg, int64_t capacity, int32_t n_versions, size_t* codes_bytes,
+                             size_t* meta_bytes, size_t* ids_bytes, size_t* centroid_bytes) {
+    qvg_status st = check_config(cfg, false);
+    if (st) return st;
+    if (capacity < 0 || n_versions < 0) return fail(QVG_ERR_INVALID_ARG, "negative capacity or versions");
+    const size_t S = cfg->num_stages, H = cfg->num_heads, D = cfg->head_dim, G = cfg->group_size,
+                 C = cfg->num_clusters, N = (size_t)capacity;
+    if (codes_bytes) *codes_bytes = S * H * N * (D / 16) * 4;
+    if (meta_bytes) *meta_bytes = S * H * N * (D / G) * 4;
+    if (ids_bytes) *ids_bytes = C ? H * N : 0;
+    if (centroid_bytes) *centroid_bytes = C ? (size_t)n_versions * H * C * D * 2 : 0;
+    return ok();
+}
+
+qvg_status qvg_workspace_bytes(const qvg_config* cfg, int64_t n_tokens, size_t* bytes) {
+    qvg_status st = check_config(cfg, false);
+    if (st) return st;
+    if (!bytes || n_tokens < 0) return fail(QVG_ERR_INVALID_ARG, "bad arguments");
+    size_t b = carve(cfg, n_tokens, nullptr).bytes;
+    if (cfg->num_clusters == 0) {
+        // cross-layer predictor: low-rank projection t [N][64] fp32
+        size_t coral = align256(sizeof(float) * 64 * (size_t)(n_tokens > 0 ? n_tokens : 1));
+        if (coral > b) b = coral;
+    }
+    *bytes = b;
+    return ok();
+}
+
+qvg_status qvg_fit_centroids(const qvg_config* cfg, const qvg_bf16* x, int64_t n_tokens, int64_t head_stride,
+                             int64_t token_stride, const qvg_bf16* warm_start, qvg_bf16* centroids, uint8_t* ids,
+                             int64_t capacity, int64_t tok_offset, void* workspace, size_t workspace_bytes,
+                             qvg_stream stream) {
+    qvg_status st = check_config(cfg, true);
+    if (st) return st;
+    if (cfg->lloyd_iters < 1) return fail(QVG_ERR_INVALID_ARG, "lloyd_iters must be >= 1");
+    if (n_tokens < 1) return fail(QVG_ERR_INVALID_ARG, "fit needs n_tokens >= 1");
+    if ((st = check_input(cfg, x, n_tokens, head_stride, token_stride, "x"))) return st;
+    if (!centroids || !aligned16(centroids)) return fail(QVG_ERR_INVALID_ARG, "centroids NULL or unaligned");
+    if (warm_start && !aligned16(warm_start)) return fail(QVG_ERR_INVALID_ARG, "warm_start unaligned");
+    if (!ids) return fail(QVG_ERR_INVALID_ARG, "ids is NULL");
+    if ((st = check_rows(capacity, tok_offset, n_tokens))) return st;
+    FitWorkspace w;
+    if ((st = check_workspace(cfg, n_tokens, workspace, workspace_bytes, &w))) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = qvg::launch_kmeans_init(cfg->head_dim, x, head_stride, token_stride, n_tokens, warm_start,
+                                            cfg->num_heads, cfg->num_clusters, centroids, s);
+    if (e != cudaSuccess) return cuda_status(e, "init launch");
+    return lloyd(cfg, x, n_tokens, head_stride, token_stride, centroids, ids, capacity, tok_offset, w, s);
+}
+
+qvg_status qvg_assign(const qvg_config* cfg, const qvg_bf16* x, int64_t n_tokens, int64_t head_stride,
+                      int64_t token_stride, const qvg_bf16* centroids, uint8_t* ids, int64_t capacity,
+                      int64_t tok_offset, void* workspace, size_t workspace_bytes, qvg_stream stream) {
+    qvg_status st = check_config(cfg, true);
+    if (st) return st;
+    if ((st = check_input(cfg, x, n_tokens, head_stride, token_stride, "x"))) return st;
+    if (!centroids || !aligned16(centroids)) return fail(QVG_ERR_INVALID_ARG, "centroids NULL or unaligned");
+    if (!ids) return fail(QVG_ERR_INVALID_ARG, "ids is NULL");
+    if ((st = check_rows(capacity, tok_offset, n_tokens))) return st;
+    FitWorkspace w;
+    if ((st = check_workspace(cfg, n_tokens, workspace, workspace_bytes, &w))) return st;
+    cudaError_t e = qvg::launch_assign(
+        cfg->head_dim, cfg->num_heads,
+        assign_args(cfg, x, n_tokens, head_stride, token_stride, centroids, ids, capacity, tok_offset, nullptr,
+                    w.stats),
+        (cudaStream_t)stream);
+    return cuda_status(e, "assign launch");
+}
+
+qvg_status qvg_update(const qvg_config* cfg, const qvg_bf16* x, int64_t n_tokens, int64_t head_stride,
+                      int64_t token_stride, const uint8_t* ids, int64_t capacity, int64_t tok_offset,
+                      qvg_bf16* centroids, void* workspace, size_t workspace_bytes, qvg_stream stream) {
+    qvg_status st = check_config(cfg, true);
+    if (st) return st;
+    if ((st = check_input(cfg, x, n_tokens, head_stride, token_stride, "x"))) return st;
+    if (!centroids || !aligned16(centroids)) return fail(QVG_ERR_INVALID_ARG, "centroids NULL or unaligned");
+    if (!ids) return fail(QVG_ERR_INVALID_ARG, "ids is NULL");
+    if ((st = check_rows(capacity, tok_offset, n_tokens))) return st;
+    FitWorkspace w;
+    if ((st = check_workspace(cfg, n_tokens, workspace, workspace_bytes, &w))) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t H = cfg->num_heads, C = cfg->num_clusters, D = cfg->head_dim;
+    cudaError_t e = cudaMemsetAsync(w.counts, 0, sizeof(int) * H * C * 2, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(w.sum_hi, 0, sizeof(long long) * H * C * D, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(w.sum_lo, 0, sizeof(long long) * H * C * D, s);
+    if (e != cudaSuccess) return cuda_status(e, "memset");
+    qvg::UpdateArgs u = update_args(cfg, x, n_tokens, head_stride, token_stride, ids, capacity, tok_offset, w,
+                                    centroids);
+    e = qvg::launch_count(u, s);
+    if (e == cudaSuccess) e = qvg::launch_update(cfg->head_dim, u, s);
+    return cuda_status(e, "update launch");
+}
+
+qvg_status qvg_encode(const qvg_config* cfg, const qvg_bf16* x, int64_t n_tokens, int64_t head_stride,
+                      int64_t token_stride, const qvg_bf16* centroids, int32_t assign, uint32_t* codes, uint32_t* meta,
+                      uint8_t* ids, int64_t capacity, int64_t tok_offset, void* workspace, size_t workspace_bytes,
+                      qvg_stream stream) {
+    qvg_status st = check_config(cfg, false);
+    if (st) return st;
+    if ((st = check_input(cfg, x, n_tokens, head_stride, token_stride, "x"))) return st;
+    if (!codes || !meta) return fail(QVG_ERR_INVALID_ARG, "codes/meta is NULL");
+    if (!aligned16(codes) || !aligned16(meta)) return fail(QVG_ERR_INVALID_ARG, "codes/meta must be 16-byte aligned");
+    if ((st = check_rows(capacity, tok_offset, n_tokens))) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    const int C = cfg->num_clusters;
+    if (C > 0) {
+        if (!centroids || !aligned16(centroids)) return fail(QVG_ERR_INVALID_ARG, "centroids NULL or unaligned");
+        if (!ids) return fail(QVG_ERR_INVALID_ARG, "ids is NULL");
+        if (assign) {
+            FitWorkspace w;
+            if ((st = check_workspace(cfg, n_tokens, workspace, workspace_bytes, &w))) return st;
+            cudaError_t e = qvg::launch_assign(cfg->head_dim, cfg->num_heads,
+                                               assign_args(cfg, x, n_tokens, head_stride, token_stride, centroids,
+                                                           ids, capacity, tok_offset, nullptr, w.stats),
+                                               s);
+            if (e != cudaSuccess) return cuda_status(e, "assign launch");
+        }
+    }
+    qvg::EncodeArgs a;
+    a.x = x; a.head_stride = head_stride; a.token_stride = token_stride; a.n_tokens = n_tokens;
+    a.cent = C > 0 ? centroids : nullptr;
+    a.ids = C > 0 ? ids : nullptr;
+    a.codes = codes; a.meta = meta; a.cap = capacity; a.tok_offset = tok_offset;
+    a.H = cfg->num_heads; a.C = C; a.S = cfg->num_stages;
+    return cuda_status(qvg::launch_encode(cfg->head_dim, cfg->group_size, a, s), "encode launch");
+}
+
+static qvg_status decode_impl(const qvg_config* cfg, const uint32_t* codes, const uint32_t* meta, const uint8_t* ids,
+                              const qvg_bf16* centroids, const int64_t* chunk_offset, const int32_t* chunk_version,
+                              int n_chunks, int64_t capacity, int64_t tok_begin, int64_t tok_end, qvg_bf16* out,
+                              int64_t ohs, int64_t ots, cudaStream_t s) {
+    if (tok_begin < 0 || tok_end < tok_begin || tok_end > capacity)
+        return fail(QVG_ERR_INVALID_ARG, "token range [%lld, %lld) outside [0, %lld)", (long long)tok_begin,
+                    (long long)tok_end, (long long)capacity);
+    if (tok_end == tok_begin) return ok();
+    if (!codes || !meta || !out) return fail(QVG_ERR_INVALID_ARG, "codes/meta/out is NULL");
+    if (!aligned16(codes) || !aligned16(meta) || !aligned16(out))
+        return fail(QVG_ERR_INVALID_ARG, "codes/meta/out must be 16-byte aligned");
+    if (ohs % 8 || ots % 8 || ohs < 0 || ots < 0) return fail(QVG_ERR_INVALID_ARG, "out strides must be multiples of 8");
+    if (cfg->num_clusters > 0 && (!ids || !centroids || !aligned16(centroids)))
+        return fail(QVG_ERR_INVALID_ARG, "ids/centroids missing");
+    qvg::DecodeArgs a;
+    a.codes = codes; a.meta = meta; a.ids = ids; a.cent = centroids;
+    a.chunk_offset = chunk_offset; a.chunk_version = chunk_version; a.n_chunks = n_chunks;
+    a.cap = capacity; a.tok_begin = tok_begin; a.tok_end = tok_end;
+    a.out = out; a.out_head_stride = ohs; a.out_token_stride = ots;
+    a.H = cfg->num_heads; a.C = cfg->num_clusters; a.S = cfg->num_stages;
+    return cuda_status(qvg::launch_decode(cfg->head_dim, cfg->group_size, a, s), "decode launch");
+}
+
+qvg_status qvg_decode(const qvg_config* cfg, const uint32_t* codes, const uint32_t* meta, const uint8_t* ids,
+                      const qvg_bf16* centroids, int64_t capacity, int64_t tok_begin, int64_t tok_end, qvg_bf16* out,
+                      int64_t out_head_stride, int64_t out_token_stride, qvg_stream stream) {
+    qvg_status st = check_config(cfg, false);
+    if (st) return st;
+    return decode_impl(cfg, codes, meta, ids, centroids, nullptr, nullptr, 0, capacity, tok_begin, tok_end, out,
+                       out_head_stride, out_token_stride, (cudaStream_t)stream);
+}
+
+qvg_status qvg_append_chunk(const qvg_config* cfg, qvg_cache* cache, const qvg_bf16* x, int64_t n_new,
+                            int64_t head_stride, int64_t token_stride, int32_t refit, void* workspace,
+                            size_t workspace_bytes, qvg_stream stream) {
+    qvg_status st = check_config(cfg, true);
+    if (st) return st;
+    if (!cache) return fail(QVG_ERR_INVALID_ARG, "cache is NULL");
+    if (n_new < 1) return fail(QVG_ERR_INVALID_ARG, "append needs n_new >= 1");
+    if (!cache->codes || !cache->meta || !cache->ids || !cache->centroids || !cache->chunk_offset ||
+        !cache->chunk_version)
+        return fail(QVG_ERR_INVALID_ARG, "cache buffers missing");
+    if ((st = check_input(cfg, x, n_new, head_stride, token_stride, "x"))) return st;
+    if (cache->n_used < 0 || cache->n_chunks < 0 || cache->n_versions < 0)
+        return fail(QVG_ERR_INVALID_ARG, "corrupt cache counters");
+    if (cache->max_chunks > kMaxChunks)
+        return fail(QVG_ERR_UNSUPPORTED, "max_chunks must be <= %d", kMaxChunks);
+    if (cache->n_chunks >= cache->max_chunks) return fail(QVG_ERR_CAPACITY, "chunk table full (%d)", cache->max_chunks);
+    if (refit && cache->n_versions >= cache->max_versions)
+        return fail(QVG_ERR_CAPACITY, "centroid versions full (%d)", cache->max_versions);
+    if (!refit && cache->n_versions == 0)
+        return fail(QVG_ERR_INVALID_ARG, "first chunk must refit (no centroid table yet)");
+    if ((st = check_rows(cache->capacity, cache->n_used, n_new))) return st;
+    if (cfg->lloyd_iters < 1 && refit) return fail(QVG_ERR_INVALID_ARG, "lloyd_iters must be >= 1");
+    FitWorkspace w;
+    if ((st = check_workspace(cfg, n_new, workspace, workspace_bytes, &w))) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t table = (size_t)cfg->num_heads * cfg->num_clusters * cfg->head_dim;
+    int version = cache->n_versions - 1;
+    if (refit) {
+        version = cache->n_versions;
+        const qvg_bf16* warm = cache->n_versions ? cache->centroids + (size_t)(cache->n_versions - 1) * table : nullptr;
+        qvg_bf16* dst = cache->centroids + (size_t)version * table;
+        cudaError_t e = qvg::launch_kmeans_init(cfg->head_dim, x, head_stride, token_stride, n_new, warm,
+                                                cfg->num_heads, cfg->num_clusters, dst, s);
+        if (e != cudaSuccess) return cuda_status(e, "init launch");
+        if ((st = lloyd(cfg, x, n_new, head_stride, token_stride, dst, cache->ids, cache->capacity, cache->n_used, w,
+                        s)))
+            return st;
+    }
+    st = qvg_encode(cfg, x, n_new, head_stride, token_stride, cache->centroids + (size_t)version * table,
+                    refit ? 0 : 1, cache->codes, cache->meta, cache->ids, cache->capacity, cache->n_used, workspace,
+                    workspace_bytes, stream);
+    if (st) return st;
+    cudaError_t e = qvg::launch_set_chunk(cache->chunk_offset, cache->chunk_version, cache->n_chunks, cache->n_used,
+                                          cache->n_used + n_new, version, s);
+    if (e != cudaSuccess) return cuda_status(e, "chunk table launch");
+    cache->n_used += n_new;
+    cache->n_chunks += 1;
+    if (refit) cache->n_versions += 1;
+    return ok();
+}
+
+qvg_status qvg_decode_cache(const qvg_config* cfg, const qvg_cache* cache, int64_t tok_begin, int64_t tok_end,
+                            qvg_bf16* out, int64_t out_head_stride, int64_t out_token_stride, qvg_stream stream) {
+    qvg_status st = check_config(cfg, true);
+    if (st) return st;
+    if (!cache) return fail(QVG_ERR_INVALID_ARG, "cache is NULL");
+    if (tok_end > cache->n_used)
+        return fail(QVG_ERR_INVALID_ARG, "tok_end %lld beyond the %lld encoded rows", (long long)tok_end,
+                    (long long)cache->n_used);
+    if (tok_end > tok_begin && cache->n_chunks < 1) return fail(QVG_ERR_INVALID_ARG, "cache holds no chunk");
+    if (cache->n_chunks > kMaxChunks || cache->n_chunks > cache->max_chunks)
+        return fail(QVG_ERR_INVALID_ARG, "corrupt chunk count %d", cache->n_chunks);
+    return decode_impl(cfg, cache->codes, cache->meta, cache->ids, cache->centroids, cache->chunk_offset,
+                       cache->chunk_version, cache->n_chunks, cache->capacity, tok_begin, tok_end, out,
+                       out_head_stride, out_token_stride, (cudaStream_t)stream);
+}
+
+static qvg_status coral_common(const qvg_config* cfg, const coral_predictor* pred, const qvg_bf16* xhat_prev,
+                               int64_t n_tokens, void* workspace, size_t workspace_bytes) {
+    qvg_status st = check_config(cfg, false);
+    if (st) return st;
+    if (cfg->num_clusters != 0) return fail(QVG_ERR_INVALID_ARG, "cross-layer codec needs num_clusters == 0");
+    if (cfg->head_dim != 64 && cfg->head_dim != 128)
+        return fail(QVG_ERR_UNSUPPORTED, "cross-layer codec supports head_dim 64 or 128");
+    if (n_tokens < 0) return fail(QVG_ERR_INVALID_ARG, "negative token count");
+    if (xhat_prev) {
+        if (!pred || !pred->B) return fail(QVG_ERR_INVALID_ARG, "predictor missing");
+        if (pred->rank < 0 || pred->rank > 64 || pred->rank % 16)
+            return fail(QVG_ERR_UNSUPPORTED, "rank must be a multiple of 16 in 0..64");
+        if (pred->rank > 0 && (!pred->U || !pred->W)) return fail(QVG_ERR_INVALID_ARG, "U/W missing");
+        if (!aligned16(xhat_prev) || !aligned16(pred->B) || (pred->rank && (!aligned16(pred->U) || !aligned16(pred->W))))
+            return fail(QVG_ERR_INVALID_ARG, "predictor / xhat_prev must be 16-byte aligned");
+        size_t need = align256(sizeof(float) * 64 * (size_t)(n_tokens > 0 ? n_tokens : 1));
+        if (pred->rank > 0 && (!workspace || workspace_bytes < need))
+            return fail(QVG_ERR_INVALID_ARG, "workspace too small: need %zu bytes", need);
+    }
+    return QVG_OK;
+}
+
+qvg_status coral_predict_encode(const qvg_config* cfg, const coral_predictor* pred, const qvg_bf16* xhat_prev,
+                                const qvg_bf16* x_next, int64_t n_tokens, uint32_t* codes, uint32_t* meta,
+                                qvg_bf16* xhat_next, float* pred_out, void* workspace, size_t workspace_bytes,
+                                qvg_stream stream) {
+    qvg_status st = coral_common(cfg, pred, xhat_prev, n_tokens, workspace, workspace_bytes);
+    if (st) return st;
+    if (n_tokens == 0) return ok();
+    if (!x_next || !codes || !meta || !xhat_next) return fail(QVG_ERR_INVALID_ARG, "buffer is NULL");
+    if (!aligned16(x_next) || !aligned16(codes) || !aligned16(meta) || !aligned16(xhat_next) ||
+        !aligned16(pred_out))
+        return fail(QVG_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+    qvg::CoralArgs a{};
+    a.xprev = xhat_prev; a.xnext = x_next;
+    a.B = xhat_prev ? pred->B : nullptr; a.U = xhat_prev ? pred->U : nullptr; a.W = xhat_prev ? pred->W : nullptr;
+    a.R = xhat_prev ? pred->rank : 0;
+    a.n_tokens = n_tokens; a.H = cfg->num_heads; a.S = cfg->num_stages;
+    a.codes = codes; a.meta = meta; a.xhat = xhat_next; a.pred_out = pred_out;
+    a.lowrank = (float*)workspace;
+    return cuda_status(qvg::launch_coral(cfg->head_dim, cfg->group_size, true, a, (cudaStream_t)stream),
+                       "coral launch");
+}
+
+qvg_status coral_predict_decode(const qvg_config* cfg, const coral_predictor* pred, const qvg_bf16* xhat_prev,
+                                int64_t n_tokens, const uint32_t* codes, const uint32_t* meta, qvg_bf16* xhat_next,
+                                float* pred_out, void* workspace, size_t workspace_bytes, qvg_stream stream) {
+    qvg_status st = coral_common(cfg, pred, xhat_prev, n_tokens, workspace, workspace_bytes);
+    if (st) return st;
+    if (n_tokens == 0) return ok();
+    if (!codes || !meta || !xhat_next) return fail(QVG_ERR_INVALID_ARG, "buffer is NULL");
+    if (!aligned16(codes) || !aligned16(meta) || !aligned16(xhat_next) || !aligned16(pred_out))
+        return fail(QVG_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+    qvg::CoralArgs a{};
+    a.xprev = xhat_prev; a.xnext = nullptr;
+    a.B = xhat_prev ? pred->B : nullptr; a.U = xhat_prev ? pred->U : nullptr; a.W = xhat_prev ? pred->W : nullptr;
+    a.R = xhat_prev ? pred->rank : 0;
+    a.n_tokens = n_tokens; a.H = cfg->num_heads; a.S = cfg->num_stages;
+    a.codes = const_cast<uint32_t*>(codes); a.meta = const_cast<uint32_t*>(meta);
+    a.xhat = xhat_next; a.pred_out = pred_out;
+    a.lowrank = (float*)workspace;
+    return cuda_status(qvg::launch_coral(cfg->head_dim, cfg->group_size, false, a, (cudaStream_t)stream),
+                       "coral launch");
+}
+
+}  // extern "C"

@@ -1,0 +1,91 @@
+// Shared device helpers of the KV-cache codec kernels (sm_103a).
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/qvg.h"
+
+namespace qvg {
+
+constexpr int kMaxClusters = 256;
+constexpr int kMaxStages = 4;
+
+// ----------------------------------------------------------- conversions --
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+// Two fp32 -> packed bf16x2 (lo in the low half), round to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float f16_bits_to_f32(uint32_t h) {
+    return __half2float(__ushort_as_half((unsigned short)(h & 0xFFFF)));
+}
+
+// fp64 -> bf16 with a single round-to-nearest-even: truncate to fp32 and
+// make the fp32 sticky (round to odd), which then rounds correctly to the
+// 8-bit bf16 significand (fp32 carries 16 more bits).
+__device__ __forceinline__ uint16_t f64_to_bf16_rn(double v) {
+    float t = __double2float_rz(v);
+    uint32_t u = __float_as_uint(t);
+    if ((double)t != v) u |= 1u;
+    float f = __uint_as_float(u);
+    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// ------------------------------------------------------------- the quantiser
+
+struct GroupParams {
+    float s, z, inv;
+    uint32_t meta;   // low half fp16 scale, high half fp16 zero
+};
+
+// Scale / zero / reciprocal of one group from its fp32 min and max.
+__device__ __forceinline__ GroupParams group_params(float mn, float mx) {
+    GroupParams p;
+    float range = __fsub_rn(mx, mn);
+    float s32 = __fdiv_rn(range, 3.0f);
+    __half sh = __float2half_rn(s32);
+    __half zh = __float2half_rn(mn);
+    p.s = __half2float(sh);
+    p.z = __half2float(zh);
+    p.inv = (p.s != 0.0f) ? __frcp_rn(p.s) : 0.0f;
+    p.meta = (uint32_t)__half_as_ushort(sh) | ((uint32_t)__half_as_ushort(zh) << 16);
+    return p;
+}
+
+__device__ __forceinline__ uint32_t quant_code(float r, const GroupParams& p) {
+    float t = __fmul_rn(__fsub_rn(r, p.z), p.inv);
+    float q = rintf(t);
+    q = fminf(fmaxf(q, 0.0f), 3.0f);
+    return (uint32_t)q;
+}
+
+__device__ __forceinline__ float dequant(uint32_t q, float s, float z) {
+    return __fmaf_rn((float)q, s, z);
+}
+
+// --------------------------------------------------------------- memory ----
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void stg_v4_stream(void* p, uint4 v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+}  // namespace qvg

@@ -1,0 +1,89 @@
+// Internal launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace qvg {
+
+struct EncodeArgs {
+    const uint16_t* x;
+    int64_t head_stride, token_stride, n_tokens;
+    const uint16_t* cent;   // [H][C][D] or nullptr
+    const uint8_t* ids;     // [H][cap], rows tok_offset.. (C > 0)
+    uint32_t* codes;        // [S][H][cap][D/16]
+    uint32_t* meta;         // [S][H][cap][D/G]
+    int64_t cap, tok_offset;
+    int H, C, S;
+};
+
+struct DecodeArgs {
+    const uint32_t* codes;
+    const uint32_t* meta;
+    const uint8_t* ids;
+    const uint16_t* cent;         // version 0 table, [V][H][C][D]
+    const int64_t* chunk_offset;  // nullptr: single version
+    const int32_t* chunk_version;
+    int n_chunks;
+    int64_t cap, tok_begin, tok_end;
+    uint16_t* out;
+    int64_t out_head_stride, out_token_stride;
+    int H, C, S;
+};
+
+struct AssignArgs {
+    const uint16_t* x;
+    int64_t head_stride, token_stride, n_tokens;
+    const uint16_t* cent;   // [H][C][D]
+    int C;
+    uint8_t* ids;           // [H][cap]
+    int64_t cap, tok_offset;
+    int* counts;            // [H][C] or nullptr
+    unsigned long long* stats;  // [4] refinement counters or nullptr
+};
+
+struct UpdateArgs {
+    const uint16_t* x;
+    int64_t head_stride, token_stride, n_tokens;
+    const uint8_t* ids;
+    int64_t cap, tok_offset;
+    int H, C;
+    int* counts;            // [H][C]
+    int* cursors;           // [H][C]
+    int* perm;              // [H][n_tokens]
+    long long* sum_hi;      // [H][C][D]
+    long long* sum_lo;      // [H][C][D]
+    uint16_t* cent;         // [H][C][D] in/out
+};
+
+struct CoralArgs {
+    const uint16_t* xprev;   // [N][H*D] or nullptr
+    const uint16_t* xnext;   // [N][H*D] (encode) or nullptr (decode)
+    const uint16_t* B;       // [H][D][D]
+    const uint16_t* U;       // [H*D][R]
+    const uint16_t* W;       // [H*D][R]
+    int R;
+    int64_t n_tokens;
+    int H, S;
+    uint32_t* codes;         // [S][H][N][D/16]
+    uint32_t* meta;          // [S][H][N][D/G]
+    uint16_t* xhat;          // [N][H*D] out
+    float* pred_out;         // optional [N][H*D]
+    float* lowrank;          // workspace [N][R]
+};
+
+// Each launcher returns cudaSuccess or the launch error; shapes are
+// validated by the caller.
+cudaError_t launch_encode(int D, int G, const EncodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode(int D, int G, const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_kmeans_init(int D, const uint16_t* x, int64_t head_stride, int64_t token_stride,
+                               int64_t n_tokens, const uint16_t* warm, int H, int C, uint16_t* cent,
+                               cudaStream_t s);
+cudaError_t launch_assign(int D, int H, const AssignArgs& a, cudaStream_t s);
+cudaError_t launch_count(const UpdateArgs& a, cudaStream_t s);
+cudaError_t launch_update(int D, const UpdateArgs& a, cudaStream_t s);
+cudaError_t launch_set_chunk(int64_t* chunk_offset, int32_t* chunk_version, int idx, int64_t begin,
+                             int64_t end, int32_t version, cudaStream_t s);
+cudaError_t launch_coral(int D, int G, bool encode, const CoralArgs& a, cudaStream_t s);
+
+}  // namespace qvg

@@ -1,0 +1,214 @@
+"""Thin ctypes binding of libqvg.so (include/qvg.h): argument marshalling only.
+
+Every function has the C name and forwards to the C ABI; torch tensors supply
+device memory and the current CUDA stream.  Nothing here computes: a missing
+library raises, there is no fallback path.
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libqvg.so")
+
+QVG_OK, QVG_ERR_INVALID_ARG, QVG_ERR_UNSUPPORTED, QVG_ERR_CAPACITY, QVG_ERR_CUDA, QVG_ERR_TIMEOUT = range(6)
+
+EXPORTS = [
+    "qvg_last_error", "qvg_version", "qvg_encoded_bytes", "qvg_workspace_bytes", "qvg_fit_centroids",
+    "qvg_assign", "qvg_update", "qvg_encode", "qvg_decode", "qvg_append_chunk", "qvg_decode_cache",
+    "coral_predict_encode", "coral_predict_decode",
+]
+
+
+class QvgError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__(f"qvg status {status}: {msg}")
+        self.status = status
+
+
+class qvg_config(ctypes.Structure):
+    _fields_ = [("num_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("num_clusters", ctypes.c_int32), ("lloyd_iters", ctypes.c_int32),
+                ("num_stages", ctypes.c_int32), ("bits", ctypes.c_int32),
+                ("group_size", ctypes.c_int32)]
+
+
+class qvg_cache(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("meta", ctypes.c_void_p), ("ids", ctypes.c_void_p),
+                ("centroids", ctypes.c_void_p), ("chunk_offset", ctypes.c_void_p),
+                ("chunk_version", ctypes.c_void_p), ("capacity", ctypes.c_int64),
+                ("max_versions", ctypes.c_int32), ("max_chunks", ctypes.c_int32),
+                ("n_used", ctypes.c_int64), ("n_versions", ctypes.c_int32), ("n_chunks", ctypes.c_int32)]
+
+
+class coral_predictor(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_void_p), ("U", ctypes.c_void_p), ("W", ctypes.c_void_p),
+                ("rank", ctypes.c_int32)]
+
+
+_lib = None
+P, I64, I32, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+PCFG = ctypes.POINTER(qvg_config)
+PSZ = ctypes.POINTER(ctypes.c_size_t)
+
+
+def load(path=LIB_PATH):
+    """Load libqvg.so (built by ``build.py`` / ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with `python -m kv_cache_quantization_means_b300.build`")
+    L = ctypes.CDLL(path)
+    L.qvg_last_error.restype = ctypes.c_char_p
+    L.qvg_version.restype = ctypes.c_char_p
+    L.qvg_encoded_bytes.argtypes = [PCFG, I64, I32, PSZ, PSZ, PSZ, PSZ]
+    L.qvg_workspace_bytes.argtypes = [PCFG, I64, PSZ]
+    L.qvg_fit_centroids.argtypes = [PCFG, P, I64, I64, I64, P, P, P, I64, I64, P, SZ, P]
+    L.qvg_assign.argtypes = [PCFG, P, I64, I64, I64, P, P, I64, I64, P, SZ, P]
+    L.qvg_update.argtypes = [PCFG, P, I64, I64, I64, P, I64, I64, P, P, SZ, P]
+    L.qvg_encode.argtypes = [PCFG, P, I64, I64, I64, P, I32, P, P, P, I64, I64, P, SZ, P]
+    L.qvg_decode.argtypes = [PCFG, P, P, P, P, I64, I64, I64, P, I64, I64, P]
+    L.qvg_append_chunk.argtypes = [PCFG, ctypes.POINTER(qvg_cache), P, I64, I64, I64, I32, P, SZ, P]
+    L.qvg_decode_cache.argtypes = [PCFG, ctypes.POINTER(qvg_cache), I64, I64, P, I64, I64, P]
+    L.coral_predict_encode.argtypes = [PCFG, ctypes.POINTER(coral_predictor), P, P, I64, P, P, P, P, P, SZ, P]
+    L.coral_predict_decode.argtypes = [PCFG, ctypes.POINTER(coral_predictor), P, I64, P, P, P, P, P, SZ, P]
+    for name in EXPORTS[2:]:
+        getattr(L, name).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def _check(st):
+    if st != QVG_OK:
+        raise QvgError(st, load().qvg_last_error().decode())
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _nbytes(t):
+    return 0 if t is None else t.numel() * t.element_size()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def config(num_heads, head_dim, num_clusters, lloyd_iters, num_stages, group_size, bits=2):
+    return qvg_config(num_heads, head_dim, num_clusters, lloyd_iters, num_stages, bits, group_size)
+
+
+# ------------------------------------------------------------ the C calls --
+
+def qvg_version():
+    return load().qvg_version().decode()
+
+
+def qvg_encoded_bytes(cfg, capacity, n_versions=1):
+    out = [ctypes.c_size_t() for _ in range(4)]
+    _check(load().qvg_encoded_bytes(ctypes.byref(cfg), capacity, n_versions, *[ctypes.byref(o) for o in out]))
+    return tuple(o.value for o in out)
+
+
+def qvg_workspace_bytes(cfg, n_tokens):
+    b = ctypes.c_size_t()
+    _check(load().qvg_workspace_bytes(ctypes.byref(cfg), n_tokens, ctypes.byref(b)))
+    return b.value
+
+
+def qvg_fit_centroids(cfg, x, n_tokens, head_stride, token_stride, warm_start, centroids, ids, capacity,
+                      tok_offset, workspace, stream=None):
+    _check(load().qvg_fit_centroids(ctypes.byref(cfg), _ptr(x), n_tokens, head_stride, token_stride,
+                                    _ptr(warm_start), _ptr(centroids), _ptr(ids), capacity, tok_offset,
+                                    _ptr(workspace), _nbytes(workspace), _stream(stream)))
+
+
+def qvg_assign(cfg, x, n_tokens, head_stride, token_stride, centroids, ids, capacity, tok_offset, workspace,
+               stream=None):
+    _check(load().qvg_assign(ctypes.byref(cfg), _ptr(x), n_tokens, head_stride, token_stride, _ptr(centroids),
+                             _ptr(ids), capacity, tok_offset, _ptr(workspace), _nbytes(workspace), _stream(stream)))
+
+
+def qvg_update(cfg, x, n_tokens, head_stride, token_stride, ids, capacity, tok_offset, centroids, workspace,
+               stream=None):
+    _check(load().qvg_update(ctypes.byref(cfg), _ptr(x), n_tokens, head_stride, token_stride, _ptr(ids), capacity,
+                             tok_offset, _ptr(centroids), _ptr(workspace), _nbytes(workspace), _stream(stream)))
+
+
+def qvg_encode(cfg, x, n_tokens, head_stride, token_stride, centroids, assign, codes, meta, ids, capacity,
+               tok_offset, workspace=None, stream=None):
+    _check(load().qvg_encode(ctypes.byref(cfg), _ptr(x), n_tokens, head_stride, token_stride, _ptr(centroids),
+                             int(assign), _ptr(codes), _ptr(meta), _ptr(ids), capacity, tok_offset,
+                             _ptr(workspace), _nbytes(workspace), _stream(stream)))
+
+
+def qvg_decode(cfg, codes, meta, ids, centroids, capacity, tok_begin, tok_end, out, out_head_stride,
+               out_token_stride, stream=None):
+    _check(load().qvg_decode(ctypes.byref(cfg), _ptr(codes), _ptr(meta), _ptr(ids), _ptr(centroids), capacity,
+                             tok_begin, tok_end, _ptr(out), out_head_stride, out_token_stride, _stream(stream)))
+
+
+def qvg_append_chunk(cfg, cache, x, n_new, head_stride, token_stride, refit, workspace, stream=None):
+    _check(load().qvg_append_chunk(ctypes.byref(cfg), ctypes.byref(cache), _ptr(x), n_new, head_stride,
+                                   token_stride, int(refit), _ptr(workspace), _nbytes(workspace), _stream(stream)))
+
+
+def qvg_decode_cache(cfg, cache, tok_begin, tok_end, out, out_head_stride, out_token_stride, stream=None):
+    _check(load().qvg_decode_cache(ctypes.byref(cfg), ctypes.byref(cache), tok_begin, tok_end, _ptr(out),
+                                   out_head_stride, out_token_stride, _stream(stream)))
+
+
+def coral_predict_encode(cfg, pred, xhat_prev, x_next, n_tokens, codes, meta, xhat_next, pred_out=None,
+                         workspace=None, stream=None):
+    _check(load().coral_predict_encode(ctypes.byref(cfg), ctypes.byref(pred) if pred is not None else None,
+                                       _ptr(xhat_prev), _ptr(x_next), n_tokens, _ptr(codes), _ptr(meta),
+                                       _ptr(xhat_next), _ptr(pred_out), _ptr(workspace), _nbytes(workspace),
+                                       _stream(stream)))
+
+
+def coral_predict_decode(cfg, pred, xhat_prev, n_tokens, codes, meta, xhat_next, pred_out=None, workspace=None,
+                         stream=None):
+    _check(load().coral_predict_decode(ctypes.byref(cfg), ctypes.byref(pred) if pred is not None else None,
+                                       _ptr(xhat_prev), n_tokens, _ptr(codes), _ptr(meta), _ptr(xhat_next),
+                                       _ptr(pred_out), _ptr(workspace), _nbytes(workspace), _stream(stream)))
+
+
+# -------------------------------------------------- allocation conveniences --
+
+def alloc_encoded(cfg, capacity, n_versions=1, device="cuda"):
+    """Device buffers for one encoded (layer, tensor), sized by qvg_encoded_bytes."""
+    cb, mb, ib, xb = qvg_encoded_bytes(cfg, capacity, n_versions)
+    return {
+        "codes": torch.empty(cb // 4, dtype=torch.int32, device=device),
+        "meta": torch.empty(mb // 4, dtype=torch.int32, device=device),
+        "ids": torch.empty(max(ib, 1), dtype=torch.uint8, device=device),
+        "centroids": torch.empty(max(xb // 2, 8), dtype=torch.int16, device=device),
+    }
+
+
+def alloc_workspace(cfg, n_tokens, device="cuda"):
+    return torch.empty(qvg_workspace_bytes(cfg, n_tokens), dtype=torch.uint8, device=device)
+
+
+def make_cache(cfg, capacity, max_versions, max_chunks, device="cuda"):
+    """A streaming cache: device buffers (kept alive in the returned dict) and
+    the qvg_cache struct pointing at them."""
+    bufs = alloc_encoded(cfg, capacity, max_versions, device)
+    bufs["chunk_offset"] = torch.zeros(max_chunks + 1, dtype=torch.int64, device=device)
+    bufs["chunk_version"] = torch.zeros(max_chunks, dtype=torch.int32, device=device)
+    c = qvg_cache(codes=_ptr(bufs["codes"]), meta=_ptr(bufs["meta"]), ids=_ptr(bufs["ids"]),
+                  centroids=_ptr(bufs["centroids"]), chunk_offset=_ptr(bufs["chunk_offset"]),
+                  chunk_version=_ptr(bufs["chunk_version"]), capacity=capacity, max_versions=max_versions,
+                  max_chunks=max_chunks, n_used=0, n_versions=0, n_chunks=0)
+    return c, bufs

@@ -201,6 +201,10 @@ static void quantize_stage(float* r, int D, int G, uint32_t* codes, uint32_t* me
             if (v < mn) mn = v;
             if (v > mx) mx = v;
         }
+        // a zero extreme is taken as +0 (the sign of a zero minimum would
+        // otherwise depend on which equal element was seen first)
+        mn = mn + 0.0f;
+        mx = mx + 0.0f;
         float range = mx - mn;
         float s32 = range / 3.0f;
         uint16_t sh = to_f16(s32), zh = to_f16(mn);

@@ -1,0 +1,150 @@
+"""The C-ABI library loads, exports every symbol include/qvg.h declares, and
+rejects bad arguments on the host before launching anything (no GPU needed:
+every call here fails validation or is a host-only size query)."""
+import ctypes
+import os
+import re
+from fractions import Fraction
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def Q():
+    import kv_cache_quantization_means_b300 as Q
+    from kv_cache_quantization_means_b300 import build as B
+    B.build()
+    Q.load()
+    return Q
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "qvg.h")).read()
+    return sorted(set(re.findall(r"QVG_API\s+[\w\s\*]+?\b(\w+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for name in ["qvg_fit_centroids", "qvg_encode", "qvg_append_chunk", "qvg_decode", "coral_predict_encode"]:
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(Q):
+    lib = ctypes.CDLL(Q.qvg.LIB_PATH)
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    assert sorted(Q.EXPORTS) == declared_symbols()
+
+
+def test_version(Q):
+    assert "sm_103a" in Q.qvg_version()
+
+
+def cfg(Q, H=2, D=64, C=16, T=3, S=2, G=64, bits=2):
+    return Q.config(H, D, C, T, S, G, bits)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(bits=4), 2), (dict(D=48), 2), (dict(G=48), 2), (dict(D=64, G=128), 1), (dict(S=0), 2),
+    (dict(S=5), 2), (dict(C=300), 2), (dict(C=-1), 2), (dict(D=256, C=16), 2), (dict(H=0), 1),
+])
+def test_bad_configs_rejected(Q, kw, status):
+    with pytest.raises(Q.QvgError) as e:
+        Q.qvg_encoded_bytes(cfg(Q, **kw), 100)
+    assert e.value.status == status
+
+
+def test_encoded_bytes_closed_form(Q):
+    """Buffer sizes from the ABI equal the closed form S*b + 32*S/G + 8/D +
+    16*C*V/N bits per element."""
+    for (H, D, C, S, G, N, V) in [(2, 64, 16, 2, 64, 1560, 1), (12, 128, 256, 2, 64, 32760, 1),
+                                  (12, 128, 256, 2, 64, 187200, 5), (40, 128, 256, 3, 128, 81920, 1),
+                                  (16, 128, 0, 2, 64, 16384, 1)]:
+        c = Q.config(H, D, C, 1, S, G)
+        cb, mb, ib, xb = Q.qvg_encoded_bytes(c, N, V)
+        bits = Fraction(8 * (cb + mb + ib + xb), H * N * D)
+        want = Fraction(2 * S) + Fraction(32 * S, G) + ((Fraction(8, D) + Fraction(16 * C * V, N)) if C else 0)
+        assert bits == want
+
+
+def test_workspace_bytes_monotone(Q):
+    c = cfg(Q)
+    a, b = Q.qvg_workspace_bytes(c, 100), Q.qvg_workspace_bytes(c, 10000)
+    assert 0 < a < b and a % 256 == 0
+
+
+def _raw(Q):
+    return Q.load()
+
+
+def test_invalid_arguments_fail_before_launch(Q):
+    L = _raw(Q)
+    c = cfg(Q)
+    b = ctypes.byref(c)
+    # NULL input
+    assert L.qvg_encode(b, None, 10, 640, 64, None, 0, None, None, None, 10, 0, None, 0, None) == 1
+    # misaligned input pointer
+    assert L.qvg_encode(b, 8, 10, 640, 64, 16, 0, 16, 16, 16, 10, 0, None, 0, None) == 1
+    # strides not multiples of 8
+    assert L.qvg_encode(b, 16, 10, 644, 64, 16, 0, 16, 16, 16, 10, 0, None, 0, None) == 1
+    # rows beyond capacity
+    assert L.qvg_encode(b, 16, 10, 640, 64, 16, 0, 16, 16, 16, 15, 6, None, 0, None) == 3
+    # assign without workspace
+    assert L.qvg_encode(b, 16, 10, 640, 64, 16, 1, 16, 16, 16, 10, 0, None, 0, None) == 1
+    # workspace too small / unaligned
+    assert L.qvg_fit_centroids(b, 16, 10, 640, 64, None, 16, 16, 10, 0, 256, 16, None) == 1
+    assert L.qvg_fit_centroids(b, 16, 10, 640, 64, None, 16, 16, 10, 0, 264, 1 << 30, None) == 1
+    # fit with no tokens / no clusters
+    assert L.qvg_fit_centroids(b, 16, 0, 640, 64, None, 16, 16, 10, 0, 256, 1 << 30, None) == 1
+    c0 = cfg(Q, C=0)
+    assert L.qvg_fit_centroids(ctypes.byref(c0), 16, 10, 640, 64, None, 16, 16, 10, 0, 256, 1 << 30, None) == 1
+    # decode range outside capacity
+    assert L.qvg_decode(b, 16, 16, 16, 16, 10, 5, 11, 16, 640, 64, None) == 1
+    assert L.qvg_decode(b, 16, 16, 16, 16, 10, 6, 5, 16, 640, 64, None) == 1
+    # the message names the problem
+    assert L.qvg_decode(b, 16, 16, 16, 16, 10, 5, 11, 16, 640, 64, None) == 1
+    assert b"outside" in L.qvg_last_error()
+    assert L.qvg_encode(b, 16, 10, 640, 64, 16, 0, 16, 16, 16, 15, 6, None, 0, None) == 3
+    assert b"capacity" in L.qvg_last_error()
+
+
+def test_empty_calls_are_no_ops(Q):
+    L = _raw(Q)
+    c = cfg(Q)
+    b = ctypes.byref(c)
+    # empty decode range and empty encode return OK without touching the GPU
+    assert L.qvg_decode(b, 16, 16, 16, 16, 10, 4, 4, 16, 640, 64, None) == 0
+    c0 = cfg(Q, C=0)
+    assert L.qvg_encode(ctypes.byref(c0), None, 0, 0, 0, None, 0, 16, 16, None, 0, 0, None, 0, None) == 0
+
+
+def test_append_chunk_capacity_checks(Q):
+    L = _raw(Q)
+    c = cfg(Q)
+    cache = Q.qvg.qvg_cache(codes=16, meta=16, ids=16, centroids=16, chunk_offset=16, chunk_version=16,
+                            capacity=100, max_versions=1, max_chunks=2, n_used=0, n_versions=0, n_chunks=0)
+    cp = ctypes.byref(cache)
+    # first chunk must refit
+    assert L.qvg_append_chunk(ctypes.byref(c), cp, 16, 50, 6400, 64, 0, 256, 1 << 30, None) == 1
+    # overflowing rows
+    assert L.qvg_append_chunk(ctypes.byref(c), cp, 16, 150, 9600, 64, 1, 256, 1 << 30, None) == 3
+    cache.n_versions, cache.n_chunks, cache.n_used = 1, 2, 60
+    assert L.qvg_append_chunk(ctypes.byref(c), cp, 16, 10, 640, 64, 0, 256, 1 << 30, None) == 3   # chunks full
+    cache.n_chunks = 1
+    assert L.qvg_append_chunk(ctypes.byref(c), cp, 16, 10, 640, 64, 1, 256, 1 << 30, None) == 3   # versions full
+    assert cache.n_used == 60 and cache.n_chunks == 1   # failed calls change nothing
+
+
+def test_coral_argument_checks(Q):
+    L = _raw(Q)
+    c = Q.config(4, 128, 0, 0, 2, 64)
+    pred = Q.qvg.coral_predictor(B=16, U=16, W=16, rank=24)
+    args = (ctypes.byref(c), ctypes.byref(pred), 16, 16, 10, 16, 16, 16, None, 256, 1 << 20, None)
+    assert L.coral_predict_encode(*args) == 2          # rank not a multiple of 16
+    pred.rank = 32
+    assert L.coral_predict_encode(ctypes.byref(c), ctypes.byref(pred), 16, 16, 10, 16, 16, 16, None, 256, 8,
+                                  None) == 1         # workspace too small
+    cq = Q.config(4, 128, 16, 1, 2, 64)
+    assert L.coral_predict_encode(ctypes.byref(cq), *args[1:]) == 1   # clusters must be 0

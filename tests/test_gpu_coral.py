@@ -1,0 +1,127 @@
+"""GPU parity of the Coral-KV cross-layer codec.
+
+The prediction is a tensor-core fp32 contraction, so it is compared with the
+oracle's fp64 prediction within an accumulation bound; every integer decision
+after it is then checked bit-exactly by driving the oracle's quantiser with
+the GPU's own fp32 prediction (staged parity).  Encoder and decoder
+reconstructions must be bit-identical.  The closed-loop chain over several
+layers is also run on both sides independently and compared in relative MSE.
+"""
+import numpy as np
+import pytest
+import torch
+
+from synth import synth as SY
+from synth import workloads as WL
+from gpu_helpers import to_dev, u16, u32
+
+pytestmark = pytest.mark.gpu
+
+GAMMA = 2.0 ** -13
+
+
+def pred_bound(xh, B, U, W, H, D):
+    f = lambda a: np.abs(SY.bf16_bits_to_f32(a).astype(np.float64))
+    x = f(xh).reshape(-1, H, D)
+    blk = np.einsum("hoi,nhi->nho", f(B), x).reshape(x.shape[0], H * D)
+    t_abs = x.reshape(x.shape[0], H * D) @ f(W)
+    low = t_abs @ f(U).T
+    return GAMMA * (blk + low) + 1e-6
+
+
+def gpu_layer(qvg, cfg, pred, xprev_dev, xnext_dev, N, encode=True, codes=None, meta=None):
+    H, D, S, G = cfg.num_heads, cfg.head_dim, cfg.num_stages, cfg.group_size
+    if encode:
+        codes = torch.full((S * H * N * D // 16,), -1, dtype=torch.int32, device="cuda")
+        meta = torch.full((S * H * N * D // G,), -1, dtype=torch.int32, device="cuda")
+    xh = torch.full((N, H * D), -1, dtype=torch.int16, device="cuda")
+    pout = torch.empty((N, H * D), dtype=torch.float32, device="cuda")
+    ws = qvg.alloc_workspace(cfg, N)
+    if encode:
+        qvg.coral_predict_encode(cfg, pred, xprev_dev, xnext_dev, N, codes, meta, xh, pout, ws)
+    else:
+        qvg.coral_predict_decode(cfg, pred, xprev_dev, N, codes, meta, xh, pout, ws)
+    torch.cuda.synchronize()
+    return codes, meta, xh, pout
+
+
+def predictor(qvg, B, U, W):
+    dev = [to_dev(a) for a in (B, U, W)]
+    p = qvg.qvg.coral_predictor(B=dev[0].data_ptr(), U=dev[1].data_ptr(), W=dev[2].data_ptr(), rank=U.shape[1])
+    return p, dev
+
+
+@pytest.mark.parametrize("N,R", [(300, 32), (64, 16), (129, 0)])
+def test_coral_chain_staged_parity(qvg, oracle, N, R):
+    wl = WL.CORAL
+    H, D, S, G, L = 4, wl.head_dim, wl.stages, wl.group_size, 4
+    small = WL.Workload(**{**wl.__dict__, "heads": H, "tokens": N, "layers": L, "rank": max(R, 16)})
+    xs = SY.coral_layers(small, SY.K_TENSOR, 0, N)              # [L][N][H*D]
+    cfg = qvg.config(H, D, 0, 0, S, G)
+    # layer 0: plain PRQ, bit-exact
+    codes, meta, xh, _ = gpu_layer(qvg, cfg, None, None, to_dev(xs[0]), N)
+    oc, om, oxh, _ = oracle.coral_encode_layer(None, xs[0], None, None, None, H, D, S, G)
+    np.testing.assert_array_equal(u32(codes).reshape(oc.shape), oc)
+    np.testing.assert_array_equal(u32(meta).reshape(om.shape), om)
+    np.testing.assert_array_equal(u16(xh), oxh)
+    prev = u16(xh)
+    for l in range(L - 1):
+        B, U, W = SY.coral_predictor(small, l)
+        if R == 0:
+            U = np.zeros((H * D, 0), np.uint16)
+            W = U
+        pred, keep = predictor(qvg, B, U, W)
+        codes, meta, xh, pout = gpu_layer(qvg, cfg, pred, to_dev(prev), to_dev(xs[l + 1]), N)
+        gp = pout.cpu().numpy()
+        # 1. prediction within the fp32 accumulation bound of the fp64 value
+        p64 = oracle.coral_predict(prev, B, U if R else np.zeros((H * D, 16), np.uint16),
+                                   W if R else np.zeros((H * D, 16), np.uint16), H, D)
+        bound = pred_bound(prev, B, U if R else np.zeros((H * D, 1), np.uint16),
+                           W if R else np.zeros((H * D, 1), np.uint16), H, D)
+        assert np.all(np.abs(gp - p64) <= bound), np.max(np.abs(gp - p64) / bound)
+        # 2. quantiser and reconstruction bit-exact given the GPU's prediction
+        oc, om, oxh, _ = oracle.coral_encode_layer(prev, xs[l + 1], B, U, W, H, D, S, G, pred_in=gp)
+        np.testing.assert_array_equal(u32(codes).reshape(oc.shape), oc)
+        np.testing.assert_array_equal(u32(meta).reshape(om.shape), om)
+        np.testing.assert_array_equal(u16(xh), oxh)
+        # 3. the decoder rebuilds the encoder's reconstruction exactly
+        _, _, dxh, dp = gpu_layer(qvg, cfg, pred, to_dev(prev), None, N, encode=False, codes=codes, meta=meta)
+        np.testing.assert_array_equal(u16(dxh), u16(xh))
+        np.testing.assert_array_equal(dp.cpu().numpy(), gp)
+        prev = u16(xh)
+
+
+def test_coral_closed_loop_end_to_end(qvg, oracle):
+    """Both sides run the whole chain on their own; reconstructions agree in
+    relative MSE within 1% at every layer.  At the first predicted layer the
+    codes are identical except where the fp32 and fp64 predictions straddle a
+    rounding boundary; after that a single differing code changes the next
+    prediction of its whole token (the low-rank term mixes all heads), so the
+    two chains are compared in quality only -- their per-layer exactness is
+    the staged test above."""
+    wl = WL.CORAL
+    H, D, S, G, L, N = 16, wl.head_dim, wl.stages, wl.group_size, 6, 256
+    small = WL.Workload(**{**wl.__dict__, "tokens": N, "layers": L})
+    xs = SY.coral_layers(small, SY.V_TENSOR, 0, N)
+    cfg = qvg.config(H, D, 0, 0, S, G)
+    g_prev = o_prev = None
+    total = diff = 0
+    for l in range(L):
+        if l == 0:
+            codes, meta, xh, _ = gpu_layer(qvg, cfg, None, None, to_dev(xs[0]), N)
+            oc, om, oxh, _ = oracle.coral_encode_layer(None, xs[0], None, None, None, H, D, S, G)
+        else:
+            B, U, W = SY.coral_predictor(small, l - 1)
+            pred, keep = predictor(qvg, B, U, W)
+            codes, meta, xh, _ = gpu_layer(qvg, cfg, pred, to_dev(g_prev), to_dev(xs[l]), N)
+            oc, om, oxh, _ = oracle.coral_encode_layer(o_prev, xs[l], B, U, W, H, D, S, G)
+        gc = u32(codes).reshape(oc.shape)
+        if l <= 1:
+            total += gc.size
+            diff += int(np.sum(gc != oc))
+        g_prev, o_prev = u16(xh), oxh
+        x = SY.bf16_bits_to_f32(xs[l]).astype(np.float64)
+        eg = np.mean((SY.bf16_bits_to_f32(g_prev) - x) ** 2)
+        eo = np.mean((SY.bf16_bits_to_f32(o_prev) - x) ** 2)
+        assert abs(eg - eo) <= 0.01 * eo, (l, eg, eo)
+    assert diff <= 1e-3 * total, (diff, total)

@@ -1,0 +1,192 @@
+"""GPU parity of the QVG path (k-means fit, assign, update, PRQ encode and
+decode) against the CPU oracle, element by element, through the C ABI.
+
+Integer outputs (ids, codes, meta words) and bf16 outputs (centroids,
+reconstructions) must be bit-exact: the CUDA path takes every decision in the
+arithmetic the oracle uses (exact argmin, exact cluster sums, fp32 quantiser).
+"""
+import numpy as np
+import pytest
+import torch
+
+from synth import synth as SY
+from synth import workloads as WL
+from gpu_helpers import Encoded, run_fit_encode_decode, to_dev, u16
+
+pytestmark = pytest.mark.gpu
+
+
+def mixture(rng, N, D, M=8, spread=1.0, noise=0.1):
+    centres = rng.standard_normal((M, D)) * spread
+    lab = rng.integers(0, M, N)
+    return SY.f64_to_bf16_bits(centres[lab] + noise * rng.standard_normal((N, D)))
+
+
+def check_unit(oracle, xh, enc, dec, h, C, T, S, G, offset=0, n=None, warm=None):
+    n = xh.shape[0] if n is None else n
+    sl = slice(offset, offset + n)
+    if C > 0:
+        oc, oi = oracle.fit(xh, C, T, warm=warm)
+        np.testing.assert_array_equal(enc.centroids()[0, h], oc, err_msg=f"centroids head {h}")
+        np.testing.assert_array_equal(enc.ids()[h, sl], oi, err_msg=f"ids head {h}")
+    else:
+        oc, oi = None, None
+    rc, rm = oracle.prq_encode(xh, oc, oi, S, G)
+    np.testing.assert_array_equal(enc.codes()[:, h, sl], rc, err_msg=f"codes head {h}")
+    np.testing.assert_array_equal(enc.meta()[:, h, sl], rm, err_msg=f"meta head {h}")
+    np.testing.assert_array_equal(dec[h], oracle.decode(rc, rm, oi, oc, G), err_msg=f"decode head {h}")
+
+
+@pytest.mark.parametrize("tensor", [SY.K_TENSOR, SY.V_TENSOR])
+def test_tiny_workload_bit_exact(qvg, oracle, tensor):
+    wl = WL.TINY
+    H, D, N = wl.heads, wl.head_dim, wl.tokens
+    xb = SY.mixture_layer(wl, 0, tensor)
+    cfg = qvg.config(H, D, wl.clusters, wl.lloyd_iters, wl.stages, wl.group_size)
+    enc, dec = run_fit_encode_decode(qvg, cfg, to_dev(xb), N, N * D, D)
+    for h in range(H):
+        check_unit(oracle, xb[h], enc, dec, h, wl.clusters, wl.lloyd_iters, wl.stages, wl.group_size)
+
+
+@pytest.mark.parametrize("D,G,S,C", [
+    (64, 64, 1, 0), (128, 64, 2, 0), (128, 128, 3, 0), (128, 16, 4, 0), (256, 128, 2, 0), (32, 16, 2, 0),
+    (32, 32, 1, 5), (64, 32, 2, 16), (128, 64, 2, 256), (128, 128, 3, 100), (64, 16, 4, 64), (128, 32, 1, 1),
+])
+def test_shape_variants_bit_exact(qvg, oracle, D, G, S, C):
+    rng = np.random.default_rng(D * 7 + G + S * 3 + C)
+    H, N, T = 3, 777, 2                      # ragged: not a multiple of any tile
+    xb = np.stack([mixture(rng, N, D, M=12, spread=1.5, noise=0.2) for _ in range(H)])
+    cfg = qvg.config(H, D, C, T, S, G)
+    enc, dec = run_fit_encode_decode(qvg, cfg, to_dev(xb), N, N * D, D)
+    for h in range(H):
+        check_unit(oracle, xb[h], enc, dec, h, C, T, S, G)
+
+
+def test_token_major_layout_offsets_and_subrange_decode(qvg, oracle):
+    """[N][H][D] input (head_stride = D, token_stride = H*D), rows written at an
+    offset inside a larger buffer, and a decode of a sub-range."""
+    rng = np.random.default_rng(11)
+    H, D, N, C, T, S, G = 4, 128, 1000, 32, 2, 2, 64
+    xb = np.stack([mixture(rng, N, D, M=20) for _ in range(H)])          # [H][N][D]
+    xt = np.ascontiguousarray(xb.transpose(1, 0, 2))                    # [N][H][D]
+    cfg = qvg.config(H, D, C, T, S, G)
+    off, cap = 300, 1500
+    enc, dec = run_fit_encode_decode(qvg, cfg, to_dev(xt), N, D, H * D, capacity=cap, offset=off,
+                                     decode_range=(off + 100, off + 617))
+    for h in range(H):
+        oc, oi = oracle.fit(xb[h], C, T)
+        np.testing.assert_array_equal(enc.centroids()[0, h], oc)
+        np.testing.assert_array_equal(enc.ids()[h, off:off + N], oi)
+        rc, rm = oracle.prq_encode(xb[h], oc, oi, S, G)
+        np.testing.assert_array_equal(enc.codes()[:, h, off:off + N], rc)
+        np.testing.assert_array_equal(enc.meta()[:, h, off:off + N], rm)
+        np.testing.assert_array_equal(dec[h], oracle.decode(rc, rm, oi, oc, G)[100:617])
+    # rows outside [off, off + N) were not touched
+    assert np.all(enc.codes()[:, :, :off] == 0xFFFFFFFF) and np.all(enc.codes()[:, :, off + N:] == 0xFFFFFFFF)
+    assert np.all(enc.ids()[:, :off] == 255)
+
+
+def test_staged_assign_and_update(qvg, oracle):
+    """assign given the oracle's centroids, update given the oracle's ids."""
+    rng = np.random.default_rng(12)
+    H, D, N, C = 2, 128, 3000, 256
+    xb = np.stack([mixture(rng, N, D, M=64, spread=1.0, noise=0.15) for _ in range(H)])
+    cent = np.stack([oracle.kmeans_init(xb[h], C) for h in range(H)])
+    cfg = qvg.config(H, D, C, 1, 2, 64)
+    x = to_dev(xb)
+    ids = torch.full((H * N,), 255, dtype=torch.uint8, device="cuda")
+    ws = qvg.alloc_workspace(cfg, N)
+    qvg.qvg_assign(cfg, x, N, N * D, D, to_dev(cent), ids, N, 0, ws)
+    torch.cuda.synchronize()
+    gids = ids.cpu().numpy().reshape(H, N).astype(np.int32)
+    for h in range(H):
+        np.testing.assert_array_equal(gids[h], oracle.assign(xb[h], cent[h]))
+    # update with the oracle's ids of the next-to-initial centroids
+    oids = np.stack([oracle.assign(xb[h], cent[h]) for h in range(H)])
+    c_dev = to_dev(cent)
+    qvg.qvg_update(cfg, x, N, N * D, D, to_dev(oids.astype(np.uint8)), N, 0, c_dev, ws)
+    torch.cuda.synchronize()
+    got = u16(c_dev).reshape(H, C, D)
+    for h in range(H):
+        want, counts = oracle.update(xb[h], oids[h], cent[h])
+        np.testing.assert_array_equal(got[h], want)
+
+
+def test_ties_and_degenerate_inputs(qvg, oracle):
+    """Exact duplicate tokens (ties at distance 0 between equal centroids),
+    fewer tokens than clusters (duplicate initial centroids), constant rows
+    (zero scale) and a single token."""
+    rng = np.random.default_rng(13)
+    D, G, S = 64, 32, 2
+    base = mixture(rng, 40, D, M=3)
+    cases = [
+        np.concatenate([base, base, base[:7]]),                        # duplicates
+        base[:5],                                                        # N < C
+        np.tile(SY.f64_to_bf16_bits(np.full((1, D), 0.75)), (50, 1)),   # constant rows
+        base[:1],                                                        # one token
+    ]
+    for k, xh in enumerate(cases):
+        N = xh.shape[0]
+        for C in (1, 8):
+            cfg = qvg.config(1, D, C, 3, S, G)
+            enc, dec = run_fit_encode_decode(qvg, cfg, to_dev(xh[None]), N, N * D, D)
+            check_unit(oracle, xh, enc, dec, 0, C, 3, S, G)
+
+
+def test_outlier_and_wide_range_values(qvg, oracle):
+    """Large outlier channels, tiny magnitudes and exact zeros."""
+    rng = np.random.default_rng(14)
+    H, D, N, C, S, G = 2, 128, 900, 16, 3, 64
+    x = rng.standard_normal((H, N, D))
+    x[:, :, 3] *= 60.0
+    x[:, :, 100] *= 1e-7
+    x[:, ::7, 50] = 0.0
+    xb = SY.f64_to_bf16_bits(x)
+    cfg = qvg.config(H, D, C, 3, S, G)
+    enc, dec = run_fit_encode_decode(qvg, cfg, to_dev(xb), N, N * D, D)
+    for h in range(H):
+        check_unit(oracle, xb[h], enc, dec, h, C, 3, S, G)
+
+
+def test_warm_start_fit(qvg, oracle):
+    rng = np.random.default_rng(15)
+    H, D, N, C, T = 2, 64, 1200, 16, 2
+    xb = np.stack([mixture(rng, N, D, M=16) for _ in range(H)])
+    warm = np.stack([SY.f64_to_bf16_bits(rng.standard_normal((C, D))) for _ in range(H)])
+    cfg = qvg.config(H, D, C, T, 2, 64)
+    enc, dec = run_fit_encode_decode(qvg, cfg, to_dev(xb), N, N * D, D, warm=to_dev(warm))
+    for h in range(H):
+        check_unit(oracle, xb[h], enc, dec, h, C, T, 2, 64, warm=warm[h])
+
+
+def test_encode_with_device_assign(qvg, oracle):
+    """qvg_encode(assign=1): ids computed on the fly against given centroids."""
+    rng = np.random.default_rng(16)
+    H, D, N, C, S, G = 3, 128, 2049, 64, 2, 64
+    xb = np.stack([mixture(rng, N, D, M=30) for _ in range(H)])
+    cent = np.stack([oracle.fit(xb[h][:500], C, 2)[0] for h in range(H)])
+    cfg = qvg.config(H, D, C, 2, S, G)
+    enc = Encoded(qvg, cfg, N)
+    ws = qvg.alloc_workspace(cfg, N)
+    enc["centroids"][: cent.size].copy_(to_dev(cent.reshape(-1)))
+    qvg.qvg_encode(cfg, to_dev(xb), N, N * D, D, enc["centroids"], 1, enc["codes"], enc["meta"], enc["ids"], N, 0,
+                   ws)
+    torch.cuda.synchronize()
+    for h in range(H):
+        oi = oracle.assign(xb[h], cent[h])
+        np.testing.assert_array_equal(enc.ids()[h], oi)
+        rc, rm = oracle.prq_encode(xb[h], cent[h], oi, S, G)
+        np.testing.assert_array_equal(enc.codes()[:, h], rc)
+        np.testing.assert_array_equal(enc.meta()[:, h], rm)
+
+
+def test_repeated_calls_are_deterministic(qvg):
+    wl = WL.TINY
+    H, D, N = wl.heads, wl.head_dim, wl.tokens
+    x = to_dev(SY.mixture_layer(wl, 0, 0))
+    cfg = qvg.config(H, D, wl.clusters, wl.lloyd_iters, wl.stages, wl.group_size)
+    runs = [run_fit_encode_decode(qvg, cfg, x, N, N * D, D) for _ in range(3)]
+    for enc, dec in runs[1:]:
+        assert np.array_equal(enc.codes(), runs[0][0].codes())
+        assert np.array_equal(enc.centroids(), runs[0][0].centroids())
+        assert np.array_equal(dec, runs[0][1])
