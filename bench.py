@@ -147,6 +147,10 @@ class QvgStep:
         self.Q.qvg_encode(self.cfg, self.x[l][t], N, D, H * D, e["centroids"], 0, e["codes"], e["meta"], e["ids"],
                           N, 0, self.ws)
 
+    def update(self, l, t):
+        e, N, D, H = self.enc[l][t], self.N, self.D, self.H
+        self.Q.qvg_update(self.cfg, self.x[l][t], N, D, H * D, e["ids"], N, 0, e["centroids"], self.ws)
+
     def decode(self, l, t):
         e, N, D, H = self.enc[l][t], self.N, self.D, self.H
         self.Q.qvg_decode(self.cfg, e["codes"], e["meta"], e["ids"], e["centroids"], N, 0, N, self.out[t], D, H * D)
@@ -176,9 +180,23 @@ def time_fn(fn, reps, stream=None):
     return a.elapsed_time(b) / reps / 1e3
 
 
+def graph_time(fn, reps):
+    """Device time of fn() per call: fn is captured once in a CUDA graph and
+    the graph is replayed, so host-side launch cost does not enter."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    g.replay()
+    torch.cuda.synchronize()
+    return time_fn(g.replay, reps)
+
+
 def kernel_rooflines(st, peaks, reps=3):
-    """Average per-launch time of each kernel family over all 60 (layer,
-    tensor) units, and its algorithmic bytes or flops per launch."""
+    """Average per-launch device time of each kernel family over all
+    (layer, tensor) units, and its algorithmic bytes or flops per launch."""
     hbm, tf_burst, tf_sus, kind = peaks
     wl, L = st.wl, st.L
     elems = st.N * st.H * st.D                      # one tensor of one layer
@@ -190,13 +208,15 @@ def kernel_rooflines(st, peaks, reps=3):
     def over_units(f):
         return lambda: [f(l, t) for (l, t) in units]
 
-    t_dec = time_fn(over_units(st.decode), reps) / len(units)
-    t_enc = time_fn(over_units(st.encode), reps) / len(units)
-    t_asg = time_fn(over_units(st.assign), reps) / len(units)
-    t_fit = time_fn(over_units(st.fit), 1) / len(units)
+    t_dec = graph_time(over_units(st.decode), reps) / len(units)
+    t_enc = graph_time(over_units(st.encode), reps) / len(units)
+    t_asg = graph_time(over_units(st.assign), reps) / len(units)
+    t_upd = graph_time(over_units(st.update), reps) / len(units)
+    t_fit = graph_time(over_units(st.fit), 1) / len(units)
     dec_bytes = elems * (code_b + id_b + 2)
     enc_bytes = elems * (2 + id_b + code_b)
     asg_flops = 2.0 * C * elems                     # token-by-centroid distance GEMM
+    upd_bytes = elems * (2 + id_b)                  # reads every token once (plus ids)
     out = {
         "decode": {"bound": "hbm", "achieved": dec_bytes / t_dec / 1e9, "peak": hbm, "unit": "GB/s",
                    "time_us": t_dec * 1e6, "algorithmic_bytes": dec_bytes},
@@ -204,6 +224,8 @@ def kernel_rooflines(st, peaks, reps=3):
                    "time_us": t_enc * 1e6, "algorithmic_bytes": enc_bytes},
         "assign": {"bound": "tensor", "achieved": asg_flops / t_asg / 1e12, "peak": tf_burst, "unit": "TFLOP/s",
                    "time_us": t_asg * 1e6, "algorithmic_flops": asg_flops},
+        "update": {"bound": "hbm", "achieved": upd_bytes / t_upd / 1e9, "peak": hbm, "unit": "GB/s",
+                   "time_us": t_upd * 1e6, "algorithmic_bytes": upd_bytes},
         "fit": {"bound": "tensor", "achieved": wl.lloyd_iters * asg_flops / t_fit / 1e12, "peak": tf_sus,
                 "unit": "TFLOP/s", "time_us": t_fit * 1e6},
     }

@@ -129,6 +129,16 @@ QVG_API qvg_status qvg_encoded_bytes(const qvg_config* cfg, int64_t capacity, in
  * qvg_append_chunk / coral_* need for `n_tokens` tokens (host only). */
 QVG_API qvg_status qvg_workspace_bytes(const qvg_config* cfg, int64_t n_tokens, size_t* bytes);
 
+/* Diagnostics of the last k-means call (fit, assign, update, append) that
+ * used `workspace`: out[0] = token rows the tensor-core screen could not
+ * decide and re-ranked exactly, out[1] = those among them whose nearest
+ * centroid was settled by the fp64 squared distance, out[2] = 0,
+ * out[3] = error word (0 = none; 0x7E000000 = a kernel gave up waiting on an
+ * internal barrier and its ids are not valid).  Copies from the device and
+ * waits for `stream`; out is host memory. */
+QVG_API qvg_status qvg_fit_stats(const qvg_config* cfg, int64_t n_tokens, const void* workspace,
+                         size_t workspace_bytes, uint64_t* out, qvg_stream stream);
+
 /* SAS k-means (QVG sec. 2A items 1-2 and sec. 3): per head, T Lloyd iterations
  * of (assign, update) on the n_tokens rows of x.  x is bf16 with logical
  * layout [H][n_tokens][D]: row (h, n) starts at x + h*head_stride +

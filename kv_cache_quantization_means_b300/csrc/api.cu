@@ -79,28 +79,33 @@ size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct FitWorkspace {
     int* counts;        // [H][C]
-    int* cursors;       // [H][C]
+    int* first_piece;   // [H][C]
+    int* npieces;       // [H]
     int* perm;          // [H][N]
-    long long* sum_hi;  // [H][C][D]
-    long long* sum_lo;  // [H][C][D]
+    int4* pieces;       // [H][max_pieces]
+    void* partials;     // [H][max_pieces][D] 16-byte exact sums
     unsigned long long* stats;  // [4]
+    int max_pieces;
     size_t bytes;
 };
 
 FitWorkspace carve(const qvg_config* c, int64_t n, void* base) {
     const size_t H = c->num_heads, C = c->num_clusters > 0 ? c->num_clusters : 1, D = c->head_dim;
+    const size_t N = (size_t)(n > 0 ? n : 1);
     FitWorkspace w{};
+    w.max_pieces = (int)((N + qvg::kPieceTokens - 1) / qvg::kPieceTokens + C);
     size_t o = 0;
     auto take = [&](size_t bytes) {
         size_t at = o;
         o += align256(bytes);
         return base ? (void*)((char*)base + at) : nullptr;
     };
-    w.counts = (int*)take(sizeof(int) * H * C * 2);    // counts and cursors, contiguous
-    w.cursors = w.counts ? w.counts + H * C : nullptr;
-    w.perm = (int*)take(sizeof(int) * H * (size_t)(n > 0 ? n : 1));
-    w.sum_hi = (long long*)take(sizeof(long long) * H * C * D);
-    w.sum_lo = (long long*)take(sizeof(long long) * H * C * D);
+    w.counts = (int*)take(sizeof(int) * H * C);
+    w.first_piece = (int*)take(sizeof(int) * H * C);
+    w.npieces = (int*)take(sizeof(int) * H);
+    w.perm = (int*)take(sizeof(int) * H * N);
+    w.pieces = (int4*)take(sizeof(int4) * H * (size_t)w.max_pieces);
+    w.partials = take((size_t)16 * H * (size_t)w.max_pieces * D);
     w.stats = (unsigned long long*)take(sizeof(unsigned long long) * 4);
     w.bytes = o;
     return w;
@@ -124,6 +129,7 @@ qvg::AssignArgs assign_args(const qvg_config* c, const qvg_bf16* x, int64_t n, i
     a.cent = cent; a.C = c->num_clusters;
     a.ids = ids; a.cap = cap; a.tok_offset = off;
     a.counts = counts; a.stats = stats;
+    a.err = stats ? reinterpret_cast<uint32_t*>(stats + 3) : nullptr;
     return a;
 }
 
@@ -134,8 +140,9 @@ qvg::UpdateArgs update_args(const qvg_config* c, const qvg_bf16* x, int64_t n, i
     u.x = x; u.head_stride = hs; u.token_stride = ts; u.n_tokens = n;
     u.ids = ids; u.cap = cap; u.tok_offset = off;
     u.H = c->num_heads; u.C = c->num_clusters;
-    u.counts = w.counts; u.cursors = w.cursors; u.perm = w.perm;
-    u.sum_hi = w.sum_hi; u.sum_lo = w.sum_lo; u.cent = cent;
+    u.max_pieces = w.max_pieces;
+    u.counts = w.counts; u.first_piece = w.first_piece; u.npieces = w.npieces;
+    u.perm = w.perm; u.pieces = w.pieces; u.partials = w.partials; u.cent = cent;
     return u;
 }
 
@@ -143,16 +150,11 @@ qvg::UpdateArgs update_args(const qvg_config* c, const qvg_bf16* x, int64_t n, i
 qvg_status lloyd(const qvg_config* c, const qvg_bf16* x, int64_t n, int64_t hs, int64_t ts,
                  qvg_bf16* cent, uint8_t* ids, int64_t cap, int64_t off, const FitWorkspace& w,
                  cudaStream_t s) {
-    const size_t H = c->num_heads, C = c->num_clusters, D = c->head_dim;
-    cudaError_t e = cudaMemsetAsync(w.sum_hi, 0, sizeof(long long) * H * C * D, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(w.sum_lo, 0, sizeof(long long) * H * C * D, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(w.stats, 0, sizeof(unsigned long long) * 4, s);
+    cudaError_t e = cudaMemsetAsync(w.stats, 0, sizeof(unsigned long long) * 4, s);
     if (e != cudaSuccess) return cuda_status(e, "memset");
     for (int t = 0; t < c->lloyd_iters; ++t) {
-        e = cudaMemsetAsync(w.counts, 0, sizeof(int) * H * C * 2, s);
-        if (e != cudaSuccess) return cuda_status(e, "memset");
         e = qvg::launch_assign(c->head_dim, c->num_heads,
-                               assign_args(c, x, n, hs, ts, cent, ids, cap, off, w.counts, w.stats), s);
+                               assign_args(c, x, n, hs, ts, cent, ids, cap, off, nullptr, w.stats), s);
         if (e != cudaSuccess) return cuda_status(e, "assign launch");
         e = qvg::launch_update(c->head_dim, update_args(c, x, n, hs, ts, ids, cap, off, w, cent), s);
         if (e != cudaSuccess) return cuda_status(e, "update launch");
@@ -196,6 +198,22 @@ qvg_status qvg_workspace_bytes(const qvg_config* cfg, int64_t n_tokens, size_t* 
     return ok();
 }
 
+qvg_status qvg_fit_stats(const qvg_config* cfg, int64_t n_tokens, const void* workspace, size_t workspace_bytes,
+                         uint64_t* out, qvg_stream stream) {
+    qvg_status st = check_config(cfg, true);
+    if (st) return st;
+    if (!out) return fail(QVG_ERR_INVALID_ARG, "out is NULL");
+    if (n_tokens < 0) return fail(QVG_ERR_INVALID_ARG, "negative token count");
+    FitWorkspace w;
+    if ((st = check_workspace(cfg, n_tokens, const_cast<void*>(workspace), workspace_bytes, &w))) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaMemcpyAsync(out, w.stats, sizeof(unsigned long long) * 4, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_status(e, "stats copy");
+    out[3] &= 0xFFFFFFFFull;
+    return ok();
+}
+
 qvg_status qvg_fit_centroids(const qvg_config* cfg, const qvg_bf16* x, int64_t n_tokens, int64_t head_stride,
                              int64_t token_stride, const qvg_bf16* warm_start, qvg_bf16* centroids, uint8_t* ids,
                              int64_t capacity, int64_t tok_offset, void* workspace, size_t workspace_bytes,
@@ -229,7 +247,9 @@ qvg_status qvg_assign(const qvg_config* cfg, const qvg_bf16* x, int64_t n_tokens
     if ((st = check_rows(capacity, tok_offset, n_tokens))) return st;
     FitWorkspace w;
     if ((st = check_workspace(cfg, n_tokens, workspace, workspace_bytes, &w))) return st;
-    cudaError_t e = qvg::launch_assign(
+    cudaError_t e = cudaMemsetAsync(w.stats, 0, sizeof(unsigned long long) * 4, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_status(e, "memset");
+    e = qvg::launch_assign(
         cfg->head_dim, cfg->num_heads,
         assign_args(cfg, x, n_tokens, head_stride, token_stride, centroids, ids, capacity, tok_offset, nullptr,
                     w.stats),
@@ -249,15 +269,9 @@ qvg_status qvg_update(const qvg_config* cfg, const qvg_bf16* x, int64_t n_tokens
     FitWorkspace w;
     if ((st = check_workspace(cfg, n_tokens, workspace, workspace_bytes, &w))) return st;
     cudaStream_t s = (cudaStream_t)stream;
-    const size_t H = cfg->num_heads, C = cfg->num_clusters, D = cfg->head_dim;
-    cudaError_t e = cudaMemsetAsync(w.counts, 0, sizeof(int) * H * C * 2, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(w.sum_hi, 0, sizeof(long long) * H * C * D, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(w.sum_lo, 0, sizeof(long long) * H * C * D, s);
-    if (e != cudaSuccess) return cuda_status(e, "memset");
     qvg::UpdateArgs u = update_args(cfg, x, n_tokens, head_stride, token_stride, ids, capacity, tok_offset, w,
                                     centroids);
-    e = qvg::launch_count(u, s);
-    if (e == cudaSuccess) e = qvg::launch_update(cfg->head_dim, u, s);
+    cudaError_t e = qvg::launch_update(cfg->head_dim, u, s);
     return cuda_status(e, "update launch");
 }
 
@@ -279,7 +293,9 @@ qvg_status qvg_encode(const qvg_config* cfg, const qvg_bf16* x, int64_t n_tokens
         if (assign) {
             FitWorkspace w;
             if ((st = check_workspace(cfg, n_tokens, workspace, workspace_bytes, &w))) return st;
-            cudaError_t e = qvg::launch_assign(cfg->head_dim, cfg->num_heads,
+            cudaError_t e = cudaMemsetAsync(w.stats, 0, sizeof(unsigned long long) * 4, s);
+            if (e != cudaSuccess) return cuda_status(e, "memset");
+            e = qvg::launch_assign(cfg->head_dim, cfg->num_heads,
                                                assign_args(cfg, x, n_tokens, head_stride, token_stride, centroids,
                                                            ids, capacity, tok_offset, nullptr, w.stats),
                                                s);

@@ -1,0 +1,640 @@
+// k-means assign step on the 5th-generation tensor cores (sm_103a).
+//
+// Quant VideoGen explainer, Sommario tecnico sec. 2A item 1: every token is
+// grouped with its nearest centroid (squared Euclidean distance, lowest index
+// on ties).  Per head, the distances of a 128-token tile to all C centroids
+// are ranked through the score ||c_j||^2 - 2<x, c_j>, whose dot products are
+// one [128 x D] x [D x C] bf16 GEMM with fp32 accumulation in tensor memory.
+//
+// One persistent CTA per SM works through a contiguous range of one head's
+// token tiles with warp-specialised roles:
+//   warp 0    TMA producer: token tiles (128 rows x 64 channels per copy,
+//             128-byte swizzle) into a 3-stage shared-memory ring;
+//   warp 1    MMA issuer: tcgen05.mma (M = 128, N = C rounded up to 64,
+//             K = 16 per instruction) into one of two TMEM accumulators;
+//             also owns the TMEM allocation;
+//   warps 2-9 epilogue: each reads half of the accumulator columns of its
+//             32-row TMEM lane quadrant (tcgen05.ld), in two passes:
+//               A. the minimum score of the row,
+//               B. the bitmask of centroids whose score is within 2E of it,
+//             E being a bound on the screen's error.  A row with one
+//             candidate is decided; the others are re-ranked over their
+//             candidates with direct fp32 distances (relative error bound)
+//             and, when those cannot separate, with the squared distance in
+//             fp64 summed in channel order, exactly as the plain definition.
+// Centroids (K-major, 128-byte swizzle) and their squared norms stay in
+// shared memory for the whole CTA.  Every wait on an mbarrier is bounded: on
+// expiry the kernel records an error code, lets the other roles drain and
+// returns after freeing its tensor memory.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace qvg {
+
+namespace {
+
+constexpr int kTile = 128;                 // tokens per tile = UMMA M
+constexpr int kStages = 3;                 // token tiles in flight
+constexpr int kEpiWarps = 8;
+constexpr int kTcThreads = 64 + 32 * kEpiWarps;
+constexpr int kAtomBytes = kTile * 128;    // one 64-channel slab of a tile
+constexpr uint32_t kErrTimeout = 0x7E000000u;
+
+// Screen error bound, relative to ||x|| ||c||max and ||c||max^2: the dot
+// products are sums of exact bf16 x bf16 products accumulated in fp32 (a
+// sequential sum of 128 terms rounded to nearest errs by at most 2^-17 of the
+// sum of magnitudes); the bound allows 4x that, plus the fp32 rounding of the
+// norms and of the score.
+constexpr float kScreenXC = 0x1p-15f;
+constexpr float kScreenCC = 0x1p-16f;
+// Relative error bound of a direct fp32 sum of D <= 128 squared differences
+// ((D + 2) * 2^-24 < 2^-16.9), with a 3.7x margin.
+constexpr float kDirectRel = 0x1p-15f;
+constexpr float kDirectAbs = 1e-35f;
+
+struct TcArgs {
+    const uint16_t* cent;    // [H][C][D]
+    int C, Cpad;
+    uint8_t* ids;            // [H][cap]
+    int64_t cap, tok_offset, n_tokens;
+    int tiles_per_head, ctas_per_head;
+    int head_inner;              // tensor map dims are (D, H, N) rather than (D, N, H)
+    unsigned long long* stats;   // [4] or null
+    uint32_t* err;               // or null
+};
+
+// ------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits for the phase of parity `parity` to complete; gives up after about
+// two seconds and returns false.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try(bar, parity)) return true;
+        if ((it & 255u) == 0 && global_ns() - t0 > 2000000000ull) return false;
+    }
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                            int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory"); }
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFFu);          // start address
+    d |= (uint64_t)1u << 16;                         // leading byte offset (unused with this swizzle)
+    d |= (uint64_t)(1024u >> 4) << 32;               // stride byte offset
+    d |= (uint64_t)1u << 46;                         // descriptor version
+    d |= (uint64_t)2u << 61;                         // 128-byte swizzle
+    return d;
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(da), "l"(db), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* v) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+          "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+          "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ----------------------------------------------------- shared memory map
+
+struct alignas(16) RowX {      // per tile row, exchanged between the two column halves
+    float bmin[2];
+    float xn[2];
+    int cnt[2];
+    int idx[2];
+};
+
+struct Layout {
+    uint32_t b_off, x_off, cn_off, row_off, mask_off, flag_off, bar_off, misc_off, total;
+};
+
+__host__ __device__ inline Layout make_layout(int D, int Cpad) {
+    Layout L;
+    const int nA = D / 64;
+    uint32_t o = 0;
+    L.b_off = o;    o += (uint32_t)nA * Cpad * 128;
+    L.x_off = o;    o += (uint32_t)kStages * nA * kAtomBytes;
+    L.cn_off = o;   o += (uint32_t)Cpad * 4;
+    L.row_off = o;  o += (uint32_t)kTile * sizeof(RowX);
+    L.mask_off = o; o += (uint32_t)kTile * (Cpad / 32) * 4;
+    L.flag_off = o; o += (uint32_t)kTile * 4 + 16;
+    L.bar_off = o;  o += (uint32_t)(2 * kStages + 4) * 8;
+    L.misc_off = o; o += 32;
+    L.total = o + 1024;            // slack for 1024-byte alignment of the base
+    return L;
+}
+
+// Byte offset of channel i of row r inside a K-major, 128-byte-swizzled
+// operand whose 64-channel slabs are `slab` bytes apart.
+__device__ __forceinline__ uint32_t sw_off(int r, int i, uint32_t slab) {
+    const int atom = i >> 6, cc = (i >> 3) & 7;
+    return (uint32_t)atom * slab + (uint32_t)r * 128u + (uint32_t)((cc ^ (r & 7)) << 4) + (uint32_t)((i & 7) << 1);
+}
+
+template <int D>
+__device__ double canonical_dist_smem(const uint8_t* xs, int row, const uint8_t* cs, int j, uint32_t cslab) {
+    double acc = 0.0;
+    for (int i = 0; i < D; ++i) {
+        const float xv = bf16f(*reinterpret_cast<const uint16_t*>(xs + sw_off(row, i, kAtomBytes)));
+        const float cv = bf16f(*reinterpret_cast<const uint16_t*>(cs + sw_off(j, i, cslab)));
+        const double df = __dsub_rn((double)xv, (double)cv);
+        acc = __dadd_rn(acc, __dmul_rn(df, df));
+    }
+    return acc;
+}
+
+// Direct fp32 squared distance, 4 (D = 128) or 2 (D = 64) channels per lane.
+template <int D>
+__device__ __forceinline__ float warp_dist(const uint8_t* xs, int row, const uint8_t* cs, int j, uint32_t cslab,
+                                           int lane) {
+    constexpr int CPL = D / 32;
+    const int i0 = lane * CPL;
+    float acc = 0.0f;
+    if (CPL == 4) {
+        const uint2 xv = *reinterpret_cast<const uint2*>(xs + sw_off(row, i0, kAtomBytes));
+        const uint2 cv = *reinterpret_cast<const uint2*>(cs + sw_off(j, i0, cslab));
+        float d;
+        d = __fsub_rn(bf16_lo(xv.x), bf16_lo(cv.x)); acc = __fmaf_rn(d, d, acc);
+        d = __fsub_rn(bf16_hi(xv.x), bf16_hi(cv.x)); acc = __fmaf_rn(d, d, acc);
+        d = __fsub_rn(bf16_lo(xv.y), bf16_lo(cv.y)); acc = __fmaf_rn(d, d, acc);
+        d = __fsub_rn(bf16_hi(xv.y), bf16_hi(cv.y)); acc = __fmaf_rn(d, d, acc);
+    } else {
+        const uint32_t xv = *reinterpret_cast<const uint32_t*>(xs + sw_off(row, i0, kAtomBytes));
+        const uint32_t cv = *reinterpret_cast<const uint32_t*>(cs + sw_off(j, i0, cslab));
+        float d;
+        d = __fsub_rn(bf16_lo(xv), bf16_lo(cv)); acc = __fmaf_rn(d, d, acc);
+        d = __fsub_rn(bf16_hi(xv), bf16_hi(cv)); acc = __fmaf_rn(d, d, acc);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    return acc;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    kmeans_assign_tc_kernel(const __grid_constant__ CUtensorMap tmap, TcArgs a) {
+    constexpr int nA = D / 64;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    const int Cpad = a.Cpad, C = a.C;
+    const Layout L = make_layout(D, Cpad);
+    uint8_t* Bs = base + L.b_off;
+    uint8_t* Xs = base + L.x_off;
+    float* cn = reinterpret_cast<float*>(base + L.cn_off);
+    RowX* rx = reinterpret_cast<RowX*>(base + L.row_off);
+    uint32_t* maskw = reinterpret_cast<uint32_t*>(base + L.mask_off);
+    int* flag_rows = reinterpret_cast<int*>(base + L.flag_off);
+    int* nflag = flag_rows + kTile;
+    const uint32_t bar0 = smem_u32(base + L.bar_off);
+    const uint32_t full_bar = bar0, empty_bar = bar0 + 8 * kStages, tfull_bar = bar0 + 16 * kStages,
+                   tempty_bar = tfull_bar + 16;
+    // [0] tmem base, [1] abort (producer / MMA), [2] cmax2 bits, [3] abort (epilogue)
+    uint32_t* misc = reinterpret_cast<uint32_t*>(base + L.misc_off);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int h = blockIdx.x / a.ctas_per_head, part = blockIdx.x % a.ctas_per_head;
+    const int t_begin = (int)((int64_t)part * a.tiles_per_head / a.ctas_per_head);
+    const int t_end = (int)((int64_t)(part + 1) * a.tiles_per_head / a.ctas_per_head);
+    const int n_tiles = t_end - t_begin;
+    const uint32_t cslab = (uint32_t)Cpad * 128u;
+    const uint32_t acc_cols = (uint32_t)Cpad;
+    uint32_t alloc_cols = 32;
+    while (alloc_cols < 2u * acc_cols) alloc_cols <<= 1;
+
+    // ---- set-up: barriers, tensor memory, centroids and their norms
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full_bar + 8 * s, 1);
+            mbar_init(empty_bar + 8 * s, kEpiWarps);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar + 8 * b, 1);
+            mbar_init(tempty_bar + 8 * b, kEpiWarps);
+        }
+        misc[1] = 0;
+        misc[2] = 0;
+        misc[3] = 0;
+        *nflag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(misc)),
+                     "r"(alloc_cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    const uint16_t* cg = a.cent + (int64_t)h * C * D;
+    for (int v = tid; v < Cpad * (D / 8); v += kTcThreads) {
+        const int j = v / (D / 8), k = v % (D / 8);
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if (j < C) val = __ldg(reinterpret_cast<const uint4*>(cg + (int64_t)j * D) + k);
+        *reinterpret_cast<uint4*>(Bs + sw_off(j, k * 8, cslab)) = val;
+    }
+    for (int j = warp; j < Cpad; j += kTcThreads / 32) {
+        float s = 0.0f;
+        if (j < C) {
+            for (int i = lane; i < D; i += 32) {
+                const float c = bf16f(cg[(int64_t)j * D + i]);
+                s = __fmaf_rn(c, c, s);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        }
+        if (lane == 0) {
+            cn[j] = j < C ? s : INFINITY;
+            if (j < C) atomicMax(misc + 2, __float_as_uint(s));
+        }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+    const float cm2 = __uint_as_float(misc[2]);
+    const float cm = sqrtf(cm2);
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int armed = 0;
+            for (int i = 0; i < n_tiles; ++i) {
+                const int s = i % kStages;
+                const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+                if (!mbar_wait(empty_bar + 8 * s, ph ^ 1u)) { atomicExch(misc + 1, 1u); break; }
+                if (*(volatile uint32_t*)(misc + 1)) break;
+                mbar_arrive_tx(full_bar + 8 * s, (uint32_t)(nA * kAtomBytes));
+                const int tok0 = (t_begin + i) * kTile;
+                for (int at = 0; at < nA; ++at) {
+                    const uint32_t dst = smem_u32(Xs + (size_t)(s * nA + at) * kAtomBytes);
+                    if (a.head_inner) tma_load_3d(dst, &tmap, full_bar + 8 * s, at * 64, h, tok0);
+                    else tma_load_3d(dst, &tmap, full_bar + 8 * s, at * 64, tok0, h);
+                }
+                armed = i + 1;
+            }
+            // drain: every copy this thread issued has landed before exit
+            for (int i = armed - kStages > 0 ? armed - kStages : 0; i < armed; ++i)
+                mbar_wait(full_bar + 8 * (i % kStages), (uint32_t)(i / kStages) & 1u);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(Cpad >> 3) << 17) |
+                                   ((uint32_t)(kTile >> 4) << 24);
+            int issued = 0;
+            for (int i = 0; i < n_tiles; ++i) {
+                const int s = i % kStages, acc = i & 1;
+                const uint32_t ph = (uint32_t)(i / kStages) & 1u, aph = (uint32_t)(i >> 1) & 1u;
+                if (!mbar_wait(tempty_bar + 8 * acc, aph ^ 1u)) { atomicExch(misc + 1, 1u); break; }
+                if (!mbar_wait(full_bar + 8 * s, ph)) { atomicExch(misc + 1, 1u); break; }
+                if (*(volatile uint32_t*)(misc + 1)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + (uint32_t)acc * acc_cols;
+                for (int at = 0; at < nA; ++at)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint64_t da = sw128_desc(smem_u32(Xs + (size_t)(s * nA + at) * kAtomBytes) + 32u * k);
+                        const uint64_t db = sw128_desc(smem_u32(Bs + (size_t)at * cslab) + 32u * k);
+                        umma_bf16(d_tmem, da, db, idesc, (at | k) != 0 ? 1u : 0u);
+                    }
+                umma_commit(tfull_bar + 8 * acc);
+                issued = i + 1;
+            }
+            // drain: the last accumulators are complete before tensor memory is freed
+            for (int i = issued - 2 > 0 ? issued - 2 : 0; i < issued; ++i)
+                mbar_wait(tfull_bar + 8 * (i & 1), (uint32_t)(i >> 1) & 1u);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue
+        const int e = warp - 2;
+        const int q = warp & 3;                 // TMEM lane quadrant of this warp
+        const int half = e >> 2;                // which half of the columns
+        const int row = q * 32 + lane;          // tile row = TMEM lane
+        const int ncols = Cpad / 2, nch = ncols / 32;
+        const int col0 = half * ncols;
+        unsigned long long n_flag = 0, n_fp64 = 0;
+        for (int i = 0; i < n_tiles; ++i) {
+            const int s = i % kStages, acc = i & 1;
+            const uint32_t ph = (uint32_t)(i / kStages) & 1u, aph = (uint32_t)(i >> 1) & 1u;
+            // the abort flag is written only before and read only after the
+            // same barrier, so every epilogue warp takes the same branch
+            if (!mbar_wait(tfull_bar + 8 * acc, aph) || !mbar_wait(full_bar + 8 * s, ph)) atomicExch(misc + 3, 1u);
+            epi_sync();
+            if (*(volatile uint32_t*)(misc + 3)) break;
+            tc_fence_after();
+            const uint8_t* xs = Xs + (size_t)s * nA * kAtomBytes;
+            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * acc_cols + (uint32_t)col0;
+            // pass A: minimum score over this half
+            float bmin = INFINITY;
+            {
+                uint32_t v[32];
+                for (int c = 0; c < nch; ++c) {
+                    tmem_ld32(taddr + 32u * c, v);
+                    tmem_wait_ld();
+                    const float* cnc = cn + col0 + 32 * c;
+#pragma unroll
+                    for (int jj = 0; jj < 32; jj += 2) {
+                        const float2 sc = f2_fma(make_float2(__uint_as_float(v[jj]), __uint_as_float(v[jj + 1])),
+                                                 make_float2(-2.0f, -2.0f), make_float2(cnc[jj], cnc[jj + 1]));
+                        bmin = fmin3(bmin, sc.x, sc.y);
+                    }
+                }
+            }
+            // partial ||x||^2 of this row: half 0 takes the first D/2 channels
+            float xn = 0.0f;
+            for (int i8 = half * (D / 16); i8 < (half + 1) * (D / 16); ++i8) {
+                const uint4 w = *reinterpret_cast<const uint4*>(xs + sw_off(row, i8 * 8, kAtomBytes));
+                float f[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                              bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+#pragma unroll
+                for (int k = 0; k < 8; ++k) xn = __fmaf_rn(f[k], f[k], xn);
+            }
+            rx[row].bmin[half] = bmin;
+            rx[row].xn[half] = xn;
+            epi_sync();
+            const float b1 = fminf(rx[row].bmin[0], rx[row].bmin[1]);
+            const float xnt = rx[row].xn[0] + rx[row].xn[1];
+            const float E = 1.01f * (kScreenXC * sqrtf(xnt) * cm + kScreenCC * cm2) + 1e-30f;
+            const float thr = b1 + 2.0f * E;
+            // pass B: candidates within 2E of the minimum
+            int cnt = 0, first = -1;
+            {
+                uint32_t v[32];
+                for (int c = 0; c < nch; ++c) {
+                    tmem_ld32(taddr + 32u * c, v);
+                    tmem_wait_ld();
+                    const float* cnc = cn + col0 + 32 * c;
+                    uint32_t m = 0;
+#pragma unroll
+                    for (int jj = 0; jj < 32; jj += 2) {
+                        const float2 sc = f2_fma(make_float2(__uint_as_float(v[jj]), __uint_as_float(v[jj + 1])),
+                                                 make_float2(-2.0f, -2.0f), make_float2(cnc[jj], cnc[jj + 1]));
+                        if (sc.x <= thr) m |= 1u << jj;
+                        if (sc.y <= thr) m |= 2u << jj;
+                    }
+                    maskw[row * (Cpad / 32) + half * nch + c] = m;
+                    if (m && first < 0) first = col0 + 32 * c + __ffs(m) - 1;
+                    cnt += __popc(m);
+                }
+            }
+            // accumulator drained: hand it back to the MMA issuer
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar + 8 * acc);
+            rx[row].cnt[half] = cnt;
+            rx[row].idx[half] = first;
+            epi_sync();
+            const int64_t tok = (int64_t)(t_begin + i) * kTile + row;
+            if (half == 0 && tok < a.n_tokens) {
+                const int c0 = rx[row].cnt[0], c1 = rx[row].cnt[1];
+                if (c0 + c1 == 1) {
+                    a.ids[(int64_t)h * a.cap + a.tok_offset + tok] = (uint8_t)(c0 ? rx[row].idx[0] : rx[row].idx[1]);
+                } else {
+                    flag_rows[atomicAdd(nflag, 1)] = row;
+                }
+            }
+            epi_sync();
+            // refine undecided rows: one warp per row over its candidates
+            const int nf = *nflag;
+            for (int f = e; f < nf; f += kEpiWarps) {
+                const int r = flag_rows[f];
+                const uint32_t* mw = maskw + r * (Cpad / 32);
+                float dmin = INFINITY;
+                for (int w = 0; w < Cpad / 32; ++w)
+                    for (uint32_t m = mw[w]; m; m &= m - 1) {
+                        const int j = 32 * w + __ffs(m) - 1;
+                        dmin = fminf(dmin, warp_dist<D>(xs, r, Bs, j, cslab, lane));
+                    }
+                const float emin = kDirectRel * dmin + kDirectAbs;
+                int nsurv = 0, best = -1;
+                double cbest = INFINITY;
+                for (int w = 0; w < Cpad / 32; ++w)
+                    for (uint32_t m = mw[w]; m; m &= m - 1) {
+                        const int j = 32 * w + __ffs(m) - 1;
+                        const float d = warp_dist<D>(xs, r, Bs, j, cslab, lane);
+                        if (d - (kDirectRel * d + kDirectAbs) <= dmin + emin) {
+                            ++nsurv;
+                            if (best < 0) best = j;
+                        }
+                    }
+                if (nsurv > 1) {
+                    // several survivors: the plain fp64 distance decides (ties -> lowest j)
+                    best = -1;
+                    for (int w = 0; w < Cpad / 32; ++w)
+                        for (uint32_t m = mw[w]; m; m &= m - 1) {
+                            const int j = 32 * w + __ffs(m) - 1;
+                            const float d = warp_dist<D>(xs, r, Bs, j, cslab, lane);
+                            if (d - (kDirectRel * d + kDirectAbs) > dmin + emin) continue;
+                            double cd = 0.0;
+                            if (lane == 0) cd = canonical_dist_smem<D>(xs, r, Bs, j, cslab);
+                            cd = __shfl_sync(0xffffffffu, cd, 0);
+                            if (cd < cbest) { cbest = cd; best = j; }
+                        }
+                    ++n_fp64;
+                }
+                const int64_t tk = (int64_t)(t_begin + i) * kTile + r;
+                if (lane == 0 && tk < a.n_tokens && best >= 0)
+                    a.ids[(int64_t)h * a.cap + a.tok_offset + tk] = (uint8_t)best;
+                ++n_flag;
+            }
+            epi_sync();
+            if (e == 0 && lane == 0) *nflag = 0;
+            // the token tile is no longer read
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_bar + 8 * s);
+        }
+        if (a.stats && lane == 0 && (n_flag | n_fp64)) {
+            atomicAdd(a.stats, n_flag);
+            atomicAdd(a.stats + 1, n_fp64);
+        }
+    }
+
+    // ---- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && (misc[1] | misc[3]) && a.err) atomicExch(a.err, kErrTimeout);
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(alloc_cols) : "memory");
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+int sm_count() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 148;
+    }
+    return n;
+}
+
+// CTAs per head: balance the tiles of all heads over the SMs, counting about
+// two tiles of set-up per CTA.
+int ctas_per_head(int H, int tiles) {
+    const int sms = sm_count();
+    int best_k = 1;
+    int64_t best = INT64_MAX;
+    for (int k = 1; k <= tiles; ++k) {
+        const int64_t waves = ((int64_t)H * k + sms - 1) / sms;
+        const int64_t span = waves * ((tiles + k - 1) / k + 2);
+        if (span < best) { best = span; best_k = k; }
+        if ((int64_t)H * k > 8 * (int64_t)sms) break;
+    }
+    return best_k;
+}
+
+template <int D>
+cudaError_t assign_tc_d(int H, const AssignArgs& a, bool* launched, cudaStream_t s) {
+    *launched = false;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return cudaSuccess;
+    // dims innermost first; the token and head dimensions in stride order
+    const bool head_inner = a.head_stride <= a.token_stride;
+    cuuint64_t dims[3], strides[2];
+    cuuint32_t box[3], estr[3] = {1, 1, 1};
+    dims[0] = (cuuint64_t)D;
+    if (head_inner) {
+        dims[1] = (cuuint64_t)H; dims[2] = (cuuint64_t)a.n_tokens;
+        strides[0] = (cuuint64_t)a.head_stride * 2; strides[1] = (cuuint64_t)a.token_stride * 2;
+        box[0] = 64; box[1] = 1; box[2] = kTile;
+    } else {
+        dims[1] = (cuuint64_t)a.n_tokens; dims[2] = (cuuint64_t)H;
+        strides[0] = (cuuint64_t)a.token_stride * 2; strides[1] = (cuuint64_t)a.head_stride * 2;
+        box[0] = 64; box[1] = kTile; box[2] = 1;
+    }
+    if (H == 1) {
+        // a single head: any head stride will do
+        if (head_inner) strides[0] = (cuuint64_t)D * 2;
+        else strides[1] = strides[0] * (cuuint64_t)a.n_tokens;
+    }
+    CUtensorMap map;
+    const CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(a.x), dims, strides, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaSuccess;   // layout not expressible: caller falls back
+    TcArgs t;
+    t.cent = a.cent; t.C = a.C; t.Cpad = (a.C + 63) / 64 * 64;
+    t.ids = a.ids; t.cap = a.cap; t.tok_offset = a.tok_offset; t.n_tokens = a.n_tokens;
+    t.tiles_per_head = (int)((a.n_tokens + kTile - 1) / kTile);
+    t.head_inner = head_inner ? 1 : 0;
+    t.ctas_per_head = ctas_per_head(H, t.tiles_per_head);
+    t.stats = a.stats;
+    t.err = a.err;
+    const Layout L = make_layout(D, t.Cpad);
+    // at least 116 KB so that one CTA (and one TMEM allocation) lives per SM
+    const size_t smem = L.total < 118784u ? 118784u : L.total;
+    cudaError_t e = cudaFuncSetAttribute(kmeans_assign_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    kmeans_assign_tc_kernel<D><<<(unsigned)(H * t.ctas_per_head), kTcThreads, smem, s>>>(map, t);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) *launched = true;
+    return e;
+}
+
+}  // namespace
+
+cudaError_t launch_assign_tc(int D, int H, const AssignArgs& a, bool* launched, cudaStream_t s) {
+    *launched = false;
+    if (a.n_tokens == 0 || a.C < 1) return cudaSuccess;
+    if ((reinterpret_cast<uintptr_t>(a.x) & 15u) || (a.head_stride % 8) || (a.token_stride % 8)) return cudaSuccess;
+    if (a.n_tokens > (int64_t)INT32_MAX - kTile) return cudaSuccess;
+    switch (D) {
+        case 64: return assign_tc_d<64>(H, a, launched, s);
+        case 128: return assign_tc_d<128>(H, a, launched, s);
+        default: return cudaSuccess;
+    }
+}
+
+}  // namespace qvg

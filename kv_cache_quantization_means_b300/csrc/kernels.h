@@ -40,7 +40,10 @@ struct AssignArgs {
     int64_t cap, tok_offset;
     int* counts;            // [H][C] or nullptr
     unsigned long long* stats;  // [4] refinement counters or nullptr
+    uint32_t* err;              // error code of a kernel that gave up a wait, or nullptr
 };
+
+constexpr int kPieceTokens = 64;   // tokens per exact partial sum of the update
 
 struct UpdateArgs {
     const uint16_t* x;
@@ -48,11 +51,13 @@ struct UpdateArgs {
     const uint8_t* ids;
     int64_t cap, tok_offset;
     int H, C;
-    int* counts;            // [H][C]
-    int* cursors;           // [H][C]
-    int* perm;              // [H][n_tokens]
-    long long* sum_hi;      // [H][C][D]
-    long long* sum_lo;      // [H][C][D]
+    int max_pieces;         // per head: ceil(n_tokens / kPieceTokens) + C
+    int* counts;            // [H][C] tokens per cluster
+    int* first_piece;       // [H][C] index of the cluster's first piece
+    int* npieces;           // [H]
+    int* perm;              // [H][n_tokens] token indices sorted by cluster
+    int4* pieces;           // [H][max_pieces]: first sorted position, length, cluster, only piece?
+    void* partials;         // [H][max_pieces][D] exact 128-bit sums (units 2^-52)
     uint16_t* cent;         // [H][C][D] in/out
 };
 
@@ -80,7 +85,9 @@ cudaError_t launch_kmeans_init(int D, const uint16_t* x, int64_t head_stride, in
                                int64_t n_tokens, const uint16_t* warm, int H, int C, uint16_t* cent,
                                cudaStream_t s);
 cudaError_t launch_assign(int D, int H, const AssignArgs& a, cudaStream_t s);
-cudaError_t launch_count(const UpdateArgs& a, cudaStream_t s);
+// tcgen05 assign; sets *launched = false (and returns cudaSuccess) when the
+// shape or layout is outside what it handles, so the caller can fall back.
+cudaError_t launch_assign_tc(int D, int H, const AssignArgs& a, bool* launched, cudaStream_t s);
 cudaError_t launch_update(int D, const UpdateArgs& a, cudaStream_t s);
 cudaError_t launch_set_chunk(int64_t* chunk_offset, int32_t* chunk_version, int idx, int64_t begin,
                              int64_t end, int32_t version, cudaStream_t s);

@@ -24,6 +24,7 @@
 // in magnitude.
 #include "common.cuh"
 #include "kernels.h"
+#include "exact_mean.cuh"
 
 namespace qvg {
 
@@ -354,94 +355,114 @@ __global__ void kmeans_init_kernel(const uint16_t* x, int64_t head_stride, int64
         reinterpret_cast<uint4*>(dst)[k] = __ldg(reinterpret_cast<const uint4*>(src) + k);
 }
 
-// Histogram of ids per head.
-__global__ void kmeans_count_kernel(UpdateArgs a) {
-    __shared__ int hist[kMaxClusters];
-    const int h = blockIdx.y;
-    for (int j = threadIdx.x; j < a.C; j += blockDim.x) hist[j] = 0;
-    __syncthreads();
+// ------------------------------------------------------------- update ---
+//
+// 1. sort: one CTA per head builds a stable counting sort of its tokens by
+//    cluster (perm), the cluster sizes and a table of pieces: runs of at most
+//    kPieceTokens sorted positions of one cluster.  Each warp histograms a
+//    contiguous token range with __match_any_sync (one writer per distinct
+//    id), so neither the counts nor the order depend on scheduling.
+// 2. sum: one warp per piece gathers its rows and forms their exact sum
+//    (fixed-point windows); the only piece of a cluster is turned into the
+//    centroid directly, other pieces store their exact partial.
+// 3. mean: clusters with several pieces add their partials in piece order
+//    and round the mean.  Integer sums make the result independent of any
+//    order; no atomic operation is used.
+
+constexpr int kSortThreads = 1024;
+constexpr int kSortWarps = kSortThreads / 32;
+
+__global__ void __launch_bounds__(kSortThreads) kmeans_sort_kernel(UpdateArgs a) {
+    __shared__ int hist[kSortWarps][kMaxClusters];
+    __shared__ int cnt_s[kMaxClusters];
+    __shared__ int off_s[kMaxClusters];
+    __shared__ int pfirst_s[kMaxClusters + 1];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int h = blockIdx.x, C = a.C;
+    const int64_t N = a.n_tokens;
     const uint8_t* idh = a.ids + (int64_t)h * a.cap + a.tok_offset;
-    for (int64_t n = (int64_t)blockIdx.x * blockDim.x * 8 + threadIdx.x;
-         n < a.n_tokens && n < (int64_t)(blockIdx.x + 1) * blockDim.x * 8; n += blockDim.x)
-        atomicAdd(&hist[min((int)idh[n], a.C - 1)], 1);
+    for (int i = tid; i < kSortWarps * kMaxClusters; i += kSortThreads) (&hist[0][0])[i] = 0;
     __syncthreads();
-    for (int j = threadIdx.x; j < a.C; j += blockDim.x)
-        if (hist[j]) atomicAdd(a.counts + (size_t)h * a.C + j, hist[j]);
-}
-
-constexpr int kScatterTokens = 2048;
-
-// Counting sort of token indices by cluster: perm[h][offset[j] + k] = the
-// k-th token of cluster j (order inside a cluster is immaterial: the sums are
-// exact integers).  Each CTA reserves one contiguous range per cluster.
-__global__ void kmeans_scatter_kernel(UpdateArgs a) {
-    __shared__ int offs[kMaxClusters];
-    __shared__ int local[kMaxClusters];
-    __shared__ int base[kMaxClusters];
-    const int h = blockIdx.y, tid = threadIdx.x;
-    const int C = a.C;
-    // exclusive scan of counts[h][*] by warp 0
-    if (tid < 32) {
-        constexpr int kPerLane = kMaxClusters / 32;
-        int v[kPerLane], tot = 0;
+    const int64_t w0 = (int64_t)warp * N / kSortWarps, w1 = (int64_t)(warp + 1) * N / kSortWarps;
+    for (int64_t b = w0; b < w1; b += 32) {
+        const int64_t n = b + lane;
+        const int id = n < w1 ? min((int)idh[n], C - 1) : -1;
+        const unsigned m = __match_any_sync(0xffffffffu, id);
+        if (id >= 0 && lane == __ffs(m) - 1) hist[warp][id] += __popc(m);
+    }
+    __syncthreads();
+    for (int j = tid; j < C; j += kSortThreads) {
+        int tot = 0;
+        for (int w = 0; w < kSortWarps; ++w) tot += hist[w][j];
+        cnt_s[j] = tot;
+        a.counts[(int64_t)h * C + j] = tot;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // exclusive scans of the counts and of the piece counts, 8 clusters per lane
+        constexpr int kPer = kMaxClusters / 32;
+        int c[kPer], pc[kPer], sc = 0, sp = 0;
 #pragma unroll
-        for (int k = 0; k < kPerLane; ++k) {
-            const int j = tid * kPerLane + k;
-            v[k] = j < C ? a.counts[(size_t)h * C + j] : 0;
-            tot += v[k];
+        for (int k = 0; k < kPer; ++k) {
+            const int j = lane * kPer + k;
+            c[k] = j < C ? cnt_s[j] : 0;
+            pc[k] = (c[k] + kPieceTokens - 1) / kPieceTokens;
+            sc += c[k];
+            sp += pc[k];
         }
-        int inc = tot;
+        int ic = sc, ip = sp;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            int u = __shfl_up_sync(0xffffffffu, inc, o);
-            if (tid >= o) inc += u;
+            const int uc = __shfl_up_sync(0xffffffffu, ic, o), up = __shfl_up_sync(0xffffffffu, ip, o);
+            if (lane >= o) { ic += uc; ip += up; }
         }
-        int run = inc - tot;
+        int rc = ic - sc, rp = ip - sp;
 #pragma unroll
-        for (int k = 0; k < kPerLane; ++k) {
-            const int j = tid * kPerLane + k;
-            if (j < kMaxClusters) offs[j] = run;
-            run += v[k];
+        for (int k = 0; k < kPer; ++k) {
+            const int j = lane * kPer + k;
+            if (j < C) { off_s[j] = rc; pfirst_s[j] = rp; }
+            rc += c[k];
+            rp += pc[k];
         }
-    }
-    for (int j = tid; j < kMaxClusters; j += blockDim.x) local[j] = 0;
-    __syncthreads();
-    const uint8_t* idh = a.ids + (int64_t)h * a.cap + a.tok_offset;
-    const int64_t t0 = (int64_t)blockIdx.x * kScatterTokens;
-    const int64_t t1 = min(t0 + kScatterTokens, a.n_tokens);
-    for (int64_t n = t0 + tid; n < t1; n += blockDim.x) atomicAdd(&local[min((int)idh[n], C - 1)], 1);
-    __syncthreads();
-    for (int j = tid; j < C; j += blockDim.x) {
-        base[j] = local[j] ? offs[j] + atomicAdd(a.cursors + (size_t)h * C + j, local[j]) : 0;
-        local[j] = 0;
+        if (lane == 31) pfirst_s[C] = rp;
     }
     __syncthreads();
-    int* ph = a.perm + (int64_t)h * a.n_tokens;
-    for (int64_t n = t0 + tid; n < t1; n += blockDim.x) {
-        const int j = min((int)idh[n], C - 1);
-        ph[base[j] + atomicAdd(&local[j], 1)] = (int)n;
+    int4* ph = a.pieces + (int64_t)h * a.max_pieces;
+    for (int j = tid; j < C; j += kSortThreads) {
+        int run = off_s[j];
+        for (int w = 0; w < kSortWarps; ++w) {
+            const int t = hist[w][j];
+            hist[w][j] = run;
+            run += t;
+        }
+        const int cnt = cnt_s[j], np = (cnt + kPieceTokens - 1) / kPieceTokens;
+        for (int p = 0; p < np; ++p)
+            ph[pfirst_s[j] + p] = make_int4(off_s[j] + p * kPieceTokens, min(kPieceTokens, cnt - p * kPieceTokens), j,
+                                            np == 1 ? 1 : 0);
+        a.first_piece[(int64_t)h * C + j] = pfirst_s[j];
+    }
+    if (tid == 0) a.npieces[h] = pfirst_s[C];
+    __syncthreads();
+    int* perm = a.perm + (int64_t)h * N;
+    const unsigned lt = (1u << lane) - 1u;
+    for (int64_t b = w0; b < w1; b += 32) {
+        const int64_t n = b + lane;
+        const int id = n < w1 ? min((int)idh[n], C - 1) : -1;
+        const unsigned m = __match_any_sync(0xffffffffu, id);
+        if (id >= 0) perm[hist[warp][id] + __popc(m & lt)] = (int)n;
+        __syncwarp();
+        if (id >= 0 && lane == __ffs(m) - 1) hist[warp][id] += __popc(m);
+        __syncwarp();
     }
 }
-
-// bf16 bits -> exact fixed-point parts (units 2^-36 and 2^-75).
-__device__ __forceinline__ void fixed_add(uint32_t b, long long& hi, long long& lo) {
-    uint32_t e = (b >> 7) & 0xFFu;
-    long long m = (long long)((b & 0x7Fu) | (e ? 0x80u : 0u));
-    if (e == 0) e = 1;
-    if (b & 0x8000u) m = -m;
-    if (e >= 98) hi += m * (1ll << min(e - 98u, 54u));   // |x| >= 2^26 is outside the exact range
-    else if (e >= 59) lo += m * (1ll << (e - 59));
-}
-
-constexpr int kSumPositions = 64;    // sorted positions per warp
 
 template <int DPL>
 __device__ __forceinline__ void load_lane_channels(const uint16_t* p, uint32_t* v) {
     if constexpr (DPL == 4) {
-        uint2 w = *reinterpret_cast<const uint2*>(p);
+        const uint2 w = *reinterpret_cast<const uint2*>(p);
         v[0] = w.x & 0xFFFFu; v[1] = w.x >> 16; v[2] = w.y & 0xFFFFu; v[3] = w.y >> 16;
     } else if constexpr (DPL == 2) {
-        uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
         v[0] = w & 0xFFFFu; v[1] = w >> 16;
     } else {
         v[0] = *p;
@@ -450,76 +471,82 @@ __device__ __forceinline__ void load_lane_channels(const uint16_t* p, uint32_t* 
 
 template <int D>
 __global__ void __launch_bounds__(kThreads) kmeans_sum_kernel(UpdateArgs a) {
-    constexpr int DPL = D / 32;          // channels per lane
+    constexpr int DPL = D / 32;   // channels per lane
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int h = blockIdx.y;
-    const int64_t p0 = ((int64_t)blockIdx.x * (kThreads / 32) + warp) * kSumPositions;
-    if (p0 >= a.n_tokens) return;
-    const int64_t p1 = min(p0 + kSumPositions, a.n_tokens);
-    const int* ph = a.perm + (int64_t)h * a.n_tokens;
-    const uint8_t* idh = a.ids + (int64_t)h * a.cap + a.tok_offset;
+    const int p = blockIdx.x * (kThreads / 32) + warp;
+    if (p >= a.npieces[h]) return;
+    const int4 pc = a.pieces[(int64_t)h * a.max_pieces + p];
+    const int start = pc.x, len = pc.y, j = pc.z;
+    const int* ph = a.perm + (int64_t)h * a.n_tokens + start;
     const uint16_t* xh = a.x + (int64_t)h * a.head_stride + lane * DPL;
-    long long hi[DPL], lo[DPL];
+    int w1[DPL], w2[DPL], w3[DPL];
 #pragma unroll
-    for (int k = 0; k < DPL; ++k) hi[k] = lo[k] = 0;
-    int cur = -1;
-    auto flush = [&](int j) {
-        long long* sh = a.sum_hi + ((size_t)h * a.C + j) * D + lane * DPL;
-        long long* sl = a.sum_lo + ((size_t)h * a.C + j) * D + lane * DPL;
-#pragma unroll
-        for (int k = 0; k < DPL; ++k) {
-            if (hi[k]) atomicAdd(reinterpret_cast<unsigned long long*>(sh + k), (unsigned long long)hi[k]);
-            if (lo[k]) atomicAdd(reinterpret_cast<unsigned long long*>(sl + k), (unsigned long long)lo[k]);
-            hi[k] = lo[k] = 0;
-        }
-    };
-    for (int64_t pb = p0; pb < p1; pb += 32) {
-        const int cnt = (int)min((int64_t)32, p1 - pb);
-        int myn = 0, myj = 0;
-        if (lane < cnt) {
-            myn = ph[pb + lane];
-            myj = min((int)idh[myn], a.C - 1);
-        }
-        for (int k0 = 0; k0 < cnt; k0 += 8) {
+    for (int d = 0; d < DPL; ++d) w1[d] = w2[d] = w3[d] = 0;
+    float amax = 0.0f;
+    for (int k0 = 0; k0 < len; k0 += 32) {
+        const int cnt = min(32, len - k0);
+        const int myn = lane < cnt ? ph[k0 + lane] : 0;
+        for (int u0 = 0; u0 < cnt; u0 += 8) {
             uint32_t v[8][DPL];
-            int jj[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                const int k = k0 + u;
-                const int n = __shfl_sync(0xffffffffu, myn, k & 31);
-                jj[u] = __shfl_sync(0xffffffffu, myj, k & 31);
-                if (k < cnt) load_lane_channels<DPL>(xh + (int64_t)n * a.token_stride, v[u]);
-            }
+                const int n = __shfl_sync(0xffffffffu, myn, (u0 + u) & 31);
+                if (u0 + u < cnt) load_lane_channels<DPL>(xh + (int64_t)n * a.token_stride, v[u]);
+                else {
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                if (k0 + u >= cnt) break;
-                if (jj[u] != cur) {
-                    if (cur >= 0) flush(cur);
-                    cur = jj[u];
+                    for (int d = 0; d < DPL; ++d) v[u][d] = 0;
                 }
-#pragma unroll
-                for (int d = 0; d < DPL; ++d) fixed_add(v[u][d], hi[d], lo[d]);
             }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+#pragma unroll
+                for (int d = 0; d < DPL; ++d) {
+                    const float xf = bf16f((uint16_t)v[u][d]);
+                    amax = fmaxf(amax, fabsf(xf));
+                    window_add(xf, w1[d], w2[d], w3[d]);
+                }
         }
     }
-    if (cur >= 0) flush(cur);
+    i128 tot[DPL];
+    if (__any_sync(0xffffffffu, !(amax < kWinMax))) {
+        // a value outside the first window: redo the piece with 128-bit sums
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) tot[d] = 0;
+        for (int k = 0; k < len; ++k) {
+            uint32_t v[DPL];
+            load_lane_channels<DPL>(xh + (int64_t)ph[k] * a.token_stride, v);
+#pragma unroll
+            for (int d = 0; d < DPL; ++d) tot[d] += bf16_to_i128_units(v[d]);
+        }
+    } else {
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) tot[d] = windows_to_i128(w1[d], w2[d], w3[d]);
+    }
+    if (pc.w) {
+        uint16_t* cr = a.cent + ((int64_t)h * a.C + j) * D + lane * DPL;
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) cr[d] = mean_bf16_bits(tot[d], (uint32_t)len);
+    } else {
+        i128* pr = reinterpret_cast<i128*>(a.partials) + ((int64_t)h * a.max_pieces + p) * D + lane * DPL;
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) pr[d] = tot[d];
+    }
 }
 
-// Exact sum -> fp64 -> mean -> bf16; empty clusters keep their centroid.
-// Also clears the accumulators for the next iteration.
-__global__ void kmeans_mean_kernel(UpdateArgs a, int D) {
-    const int hj = blockIdx.x;                  // h * C + j
-    const int cnt = a.counts[hj];
+// Clusters made of several pieces: add the partials in piece order, round.
+template <int D>
+__global__ void kmeans_mean_kernel(UpdateArgs a) {
+    const int j = blockIdx.x, h = blockIdx.y;
+    const int cnt = a.counts[(int64_t)h * a.C + j];
+    const int np = (cnt + kPieceTokens - 1) / kPieceTokens;
+    if (np <= 1) return;
+    const int first = a.first_piece[(int64_t)h * a.C + j];
+    const i128* pr = reinterpret_cast<const i128*>(a.partials) + ((int64_t)h * a.max_pieces + first) * D;
     for (int d = threadIdx.x; d < D; d += blockDim.x) {
-        const size_t i = (size_t)hj * D + d;
-        const long long hi = a.sum_hi[i], lo = a.sum_lo[i];
-        if (cnt > 0) {
-            double s = __dadd_rn(__dmul_rn(__ll2double_rn(hi), 0x1p-36),
-                                 __dmul_rn(__ll2double_rn(lo), 0x1p-75));
-            a.cent[i] = f64_to_bf16_rn(__ddiv_rn(s, (double)cnt));
-        }
-        a.sum_hi[i] = 0;
-        a.sum_lo[i] = 0;
+        i128 s = 0;
+        for (int p = 0; p < np; ++p) s += pr[(int64_t)p * D + d];
+        a.cent[((int64_t)h * a.C + j) * D + d] = mean_bf16_bits(s, (uint32_t)cnt);
     }
 }
 
@@ -551,12 +578,10 @@ cudaError_t assign_d(int H, const AssignArgs& a, cudaStream_t s) {
 template <int D>
 cudaError_t update_d(const UpdateArgs& a, cudaStream_t s) {
     if (a.n_tokens == 0) return cudaSuccess;
-    dim3 g1((unsigned)((a.n_tokens + kScatterTokens - 1) / kScatterTokens), (unsigned)a.H);
-    kmeans_scatter_kernel<<<g1, kThreads, 0, s>>>(a);
-    const int64_t per_cta = (int64_t)(kThreads / 32) * kSumPositions;
-    dim3 g2((unsigned)((a.n_tokens + per_cta - 1) / per_cta), (unsigned)a.H);
+    kmeans_sort_kernel<<<(unsigned)a.H, kSortThreads, 0, s>>>(a);
+    dim3 g2((unsigned)((a.max_pieces + kThreads / 32 - 1) / (kThreads / 32)), (unsigned)a.H);
     kmeans_sum_kernel<D><<<g2, kThreads, 0, s>>>(a);
-    kmeans_mean_kernel<<<(unsigned)(a.H * a.C), D < 128 ? D : 128, 0, s>>>(a, D);
+    kmeans_mean_kernel<D><<<dim3((unsigned)a.C, (unsigned)a.H), D, 0, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -571,19 +596,15 @@ cudaError_t launch_kmeans_init(int D, const uint16_t* x, int64_t head_stride, in
 }
 
 cudaError_t launch_assign(int D, int H, const AssignArgs& a, cudaStream_t s) {
+    bool launched = false;
+    const cudaError_t e = launch_assign_tc(D, H, a, &launched, s);
+    if (e != cudaSuccess || launched) return e;
     switch (D) {
         case 32: return assign_d<32>(H, a, s);
         case 64: return assign_d<64>(H, a, s);
         case 128: return assign_d<128>(H, a, s);
         default: return cudaErrorInvalidValue;
     }
-}
-
-cudaError_t launch_count(const UpdateArgs& a, cudaStream_t s) {
-    if (a.n_tokens == 0) return cudaSuccess;
-    const int64_t per = 256 * 8;
-    kmeans_count_kernel<<<dim3((unsigned)((a.n_tokens + per - 1) / per), (unsigned)a.H), 256, 0, s>>>(a);
-    return cudaGetLastError();
 }
 
 cudaError_t launch_update(int D, const UpdateArgs& a, cudaStream_t s) {

@@ -4,118 +4,116 @@
 // token's centroid) and sec. 2B items 1-3 (re-quantise the residual stage by
 // stage; decode = dequantise, sum the stages, add the centroid back).
 //
-// Both kernels are HBM-streaming: one lane owns 8 consecutive channels of a
-// token row (one 16-byte bf16 vector), D/8 lanes cover a row, a warp covers
-// 32/(D/8) rows per step and 16 rows in all.  Group min/max are warp-shuffle
-// reductions over the G/8 lanes of a group; each lane packs its 8 2-bit codes
-// into one 16-bit half of a code word, so a warp's code store is contiguous.
+// Both kernels stream HBM.  A thread owns 16 consecutive channels of a token
+// row (two 16-byte bf16 vectors, one 32-bit code word per stage); D/16 lanes
+// cover a row and a warp covers 32/(D/16) rows at a time.  Group min/max are
+// warp-shuffle reductions over the G/16 lanes of a group.  Every load of a
+// row is issued before any of its arithmetic (the encoder also prefetches
+// the next row), so each warp keeps several rows of HBM traffic in flight.
 #include "common.cuh"
 #include "kernels.h"
+#include "prq16.cuh"
 
 namespace qvg {
 
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kRowsPerWarp = 16;
+constexpr int kEncRowsPerThread = 4;   // encoder: rows per thread (pipelined)
+constexpr int kDecRowsPerThread = 2;   // decoder: rows per thread (loads hoisted)
 
 template <int D>
-struct RowMap {
-    static constexpr int LPR = D / 8;           // lanes per row
-    static constexpr int RPS = 32 / LPR;        // rows per warp step
-    static constexpr int STEPS = kRowsPerWarp / RPS;
-    static constexpr int ROWS_PER_CTA = kRowsPerWarp * (kThreads / 32);
+struct Map16 {
+    static constexpr int TPR = D / 16;                   // threads per row
+    static constexpr int RPW = 32 / TPR;                 // rows per warp step
+    static constexpr int RPS = RPW * (kThreads / 32);    // rows per CTA step
 };
 
-__device__ __forceinline__ void unpack8(const uint4& v, float* f) {
-    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
-    f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
-    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
-    f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
-}
-
 template <int D, int G, bool HAS_C>
-__global__ void __launch_bounds__(kThreads) prq_encode_kernel(EncodeArgs a) {
-    using M = RowMap<D>;
-    constexpr int LPG = G / 8;
+__global__ void __launch_bounds__(kThreads, 4) prq_encode_kernel(EncodeArgs a) {
+    using M = Map16<D>;
+    constexpr int TPG = G / 16;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int sub = lane % M::LPR, rw = lane / M::LPR;
+    const int t = lane % M::TPR;
     const int h = blockIdx.y;
-    const int64_t row0 = (int64_t)blockIdx.x * M::ROWS_PER_CTA + (int64_t)warp * kRowsPerWarp + rw;
+    // rows of this thread: base + k * RPS, k < kEncRowsPerThread
+    const int64_t base = (int64_t)blockIdx.x * M::RPS * kEncRowsPerThread + (int64_t)warp * M::RPW + lane / M::TPR;
 
-    const uint16_t* xh = a.x + (int64_t)h * a.head_stride + sub * 8;
+    const uint16_t* xh = a.x + (int64_t)h * a.head_stride + t * 16;
     const uint8_t* idh = HAS_C ? a.ids + (int64_t)h * a.cap + a.tok_offset : nullptr;
-    const uint16_t* ch = HAS_C ? a.cent + (int64_t)h * a.C * D + sub * 8 : nullptr;
-    uint16_t* codes16 = reinterpret_cast<uint16_t*>(a.codes);
+    const uint16_t* ch = HAS_C ? a.cent + (int64_t)h * a.C * D + t * 16 : nullptr;
+    const int64_t stage_rows = (int64_t)a.H * a.cap;
+    const int64_t row0 = (int64_t)h * a.cap + a.tok_offset;
 
-    // Register double-buffering of the next row's input.
-    uint4 xv = make_uint4(0, 0, 0, 0);
-    int idv = 0;
-    if (row0 < a.n_tokens) {
-        xv = ldg_nc_v4(xh + row0 * a.token_stride);
-        if (HAS_C) idv = idh[row0];
+    uint4 xa = make_uint4(0, 0, 0, 0), xb = xa, ca = xa, cb = xa;
+    if (base < a.n_tokens) {
+        const uint16_t* p = xh + base * a.token_stride;
+        xa = ldg_nc_v4(p);
+        xb = ldg_nc_v4(p + 8);
+        if (HAS_C) {
+            const int id = min((int)idh[base], a.C - 1);
+            ca = __ldg(reinterpret_cast<const uint4*>(ch + (int64_t)id * D));
+            cb = __ldg(reinterpret_cast<const uint4*>(ch + (int64_t)id * D + 8));
+        }
     }
 #pragma unroll 1
-    for (int st = 0; st < M::STEPS; ++st) {
-        const int64_t n = row0 + (int64_t)st * M::RPS;
+    for (int k = 0; k < kEncRowsPerThread; ++k) {
+        const int64_t n = base + (int64_t)k * M::RPS;
         const bool valid = n < a.n_tokens;
+        // prefetch the next row of this thread
         const int64_t nn = n + M::RPS;
-        uint4 xnext = make_uint4(0, 0, 0, 0);
-        int idnext = 0;
-        if (st + 1 < M::STEPS && nn < a.n_tokens) {
-            xnext = ldg_nc_v4(xh + nn * a.token_stride);
-            if (HAS_C) idnext = idh[nn];
+        uint4 nxa = make_uint4(0, 0, 0, 0), nxb = nxa;
+        int nid = 0;
+        const bool nvalid = (k + 1 < kEncRowsPerThread) && nn < a.n_tokens;
+        if (nvalid) {
+            const uint16_t* p = xh + nn * a.token_stride;
+            nxa = ldg_nc_v4(p);
+            nxb = ldg_nc_v4(p + 8);
+            if (HAS_C) nid = min((int)idh[nn], a.C - 1);
         }
-        float r[8];
-        unpack8(xv, r);
+        float r[16];
+        unpack16(xa, xb, r);
         if (HAS_C) {
-            uint4 cv = valid ? __ldg(reinterpret_cast<const uint4*>(ch + (int64_t)min(idv, a.C - 1) * D))
-                             : make_uint4(0, 0, 0, 0);
-            float c[8];
-            unpack8(cv, c);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) r[i] = __fsub_rn(r[i], c[i]);
+            float c[16];
+            unpack16(ca, cb, c);
+            sub16(r, c);
         }
-        const int64_t rowoff = (int64_t)h * a.cap + a.tok_offset + n;
+        const int64_t row = row0 + n;
         for (int s = 0; s < a.S; ++s) {
-            float mn = r[0], mx = r[0];
-#pragma unroll
-            for (int i = 1; i < 8; ++i) { mn = fminf(mn, r[i]); mx = fmaxf(mx, r[i]); }
-#pragma unroll
-            for (int off = 1; off < LPG; off <<= 1) {
-                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            }
-            // a zero extreme is taken as +0 so the stored bits do not depend
-            // on the reduction order
-            mn = __fadd_rn(mn, 0.0f);
-            mx = __fadd_rn(mx, 0.0f);
-            const GroupParams p = group_params(mn, mx);
-            uint32_t code = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                uint32_t q = quant_code(r[i], p);
-                code |= q << (2 * i);
-                if (s + 1 < a.S) r[i] = __fsub_rn(r[i], dequant(q, p.s, p.z));
-            }
+            uint32_t meta;
+            const uint32_t code = quant_stage16<TPG>(r, s + 1 < a.S, nullptr, meta);
             if (valid) {
-                const int64_t srow = (int64_t)s * a.H * a.cap + rowoff;
-                codes16[srow * (D / 8) + sub] = (uint16_t)code;
-                if (sub % LPG == 0) a.meta[srow * (D / G) + sub / LPG] = p.meta;
+                const int64_t srow = (int64_t)s * stage_rows + row;
+                a.codes[srow * (D / 16) + t] = code;
+                if (t % TPG == 0) a.meta[srow * (D / G) + t / TPG] = meta;
             }
         }
-        xv = xnext;
-        idv = idnext;
+        xa = nxa;
+        xb = nxb;
+        if (HAS_C && nvalid) {
+            ca = __ldg(reinterpret_cast<const uint4*>(ch + (int64_t)nid * D));
+            cb = __ldg(reinterpret_cast<const uint4*>(ch + (int64_t)nid * D + 8));
+        }
     }
+}
+
+// Centroid version of token n: the last chunk whose first token is <= n.
+__device__ __forceinline__ int chunk_of(const int64_t* offs, int n_chunks, int64_t n) {
+    int lo = 0, hi = n_chunks - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (offs[mid] <= n) lo = mid; else hi = mid - 1;
+    }
+    return lo;
 }
 
 template <int D, int G, bool HAS_C, bool VERSIONED>
-__global__ void __launch_bounds__(kThreads) prq_decode_kernel(DecodeArgs a) {
-    using M = RowMap<D>;
-    constexpr int LPG = G / 8;
+__global__ void __launch_bounds__(kThreads, 4) prq_decode_kernel(DecodeArgs a) {
+    using M = Map16<D>;
+    constexpr int NR = kDecRowsPerThread;
     extern __shared__ int64_t chunk_smem[];   // VERSIONED: offsets[n_chunks + 1], versions[n_chunks]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int sub = lane % M::LPR, rw = lane / M::LPR;
+    const int t = lane % M::TPR;
     const int h = blockIdx.y;
     if (VERSIONED) {
         int32_t* vers = reinterpret_cast<int32_t*>(chunk_smem + a.n_chunks + 1);
@@ -124,58 +122,69 @@ __global__ void __launch_bounds__(kThreads) prq_decode_kernel(DecodeArgs a) {
         __syncthreads();
     }
     const int64_t n_rows = a.tok_end - a.tok_begin;
-    const int64_t row0 = (int64_t)blockIdx.x * M::ROWS_PER_CTA + (int64_t)warp * kRowsPerWarp + rw;
-    const uint16_t* codes16 = reinterpret_cast<const uint16_t*>(a.codes);
-    const int64_t stage_stride = (int64_t)a.H * a.cap;
-    const int64_t version_stride = (int64_t)a.H * a.C * D;
+    const int64_t base = (int64_t)blockIdx.x * M::RPS * NR + (int64_t)warp * M::RPW + lane / M::TPR;
+    const int64_t stage_rows = (int64_t)a.H * a.cap;
+    constexpr int WPR = D / 16, MPR = D / G;
+    const int mi = (t * 16) / G;
 
-#pragma unroll 1
-    for (int st = 0; st < M::STEPS; ++st) {
-        const int64_t i = row0 + (int64_t)st * M::RPS;
-        if (i >= n_rows) break;
-        const int64_t n = a.tok_begin + i;
-        const int64_t row = (int64_t)h * a.cap + n;
-        float acc[8];
+    int64_t ii[NR];
+    bool ok[NR];
+    int id[NR];
+    uint32_t code[NR][kMaxStages], meta[NR][kMaxStages];
+#pragma unroll
+    for (int k = 0; k < NR; ++k) {
+        ii[k] = base + (int64_t)k * M::RPS;
+        ok[k] = ii[k] < n_rows;
+        const int64_t row = (int64_t)h * a.cap + a.tok_begin + ii[k];
+        id[k] = 0;
+        if (HAS_C && ok[k]) id[k] = a.ids[row];
+#pragma unroll
+        for (int s = 0; s < kMaxStages; ++s) {
+            code[k][s] = 0;
+            meta[k][s] = 0;
+            if (s < a.S && ok[k]) {
+                const int64_t srow = (int64_t)s * stage_rows + row;
+                code[k][s] = __ldg(a.codes + srow * WPR + t);
+                meta[k][s] = __ldg(a.meta + srow * MPR + mi);
+            }
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < NR; ++k) {
+        if (!ok[k]) continue;
+        float acc[16];
         if (HAS_C) {
             const uint16_t* cbase = a.cent;
             if (VERSIONED) {
                 const int32_t* vers = reinterpret_cast<const int32_t*>(chunk_smem + a.n_chunks + 1);
-                int lo = 0, hi = a.n_chunks - 1;     // last chunk whose offset <= n
-                while (lo < hi) {
-                    int mid = (lo + hi + 1) >> 1;
-                    if (chunk_smem[mid] <= n) lo = mid; else hi = mid - 1;
-                }
-                cbase += (int64_t)vers[lo] * version_stride;
+                const int c = chunk_of(chunk_smem, a.n_chunks, a.tok_begin + ii[k]);
+                cbase += (int64_t)vers[c] * a.H * a.C * D;
             }
-            const int id = min((int)a.ids[row], a.C - 1);
-            uint4 cv = __ldg(reinterpret_cast<const uint4*>(cbase + ((int64_t)h * a.C + id) * D + sub * 8));
-            unpack8(cv, acc);
+            const uint16_t* cr = cbase + ((int64_t)h * a.C + min(id[k], a.C - 1)) * D + t * 16;
+            const uint4 c0 = __ldg(reinterpret_cast<const uint4*>(cr));
+            const uint4 c1 = __ldg(reinterpret_cast<const uint4*>(cr + 8));
+            unpack16(c0, c1, acc);
         } else {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) acc[k] = 0.0f;
+            for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
         }
-        for (int s = 0; s < a.S; ++s) {
-            const int64_t srow = (int64_t)s * stage_stride + row;
-            const uint32_t code = codes16[srow * (D / 8) + sub];
-            const uint32_t m = __ldg(a.meta + srow * (D / G) + sub / LPG);
-            const float sc = f16_bits_to_f32(m), z = f16_bits_to_f32(m >> 16);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) acc[k] = __fadd_rn(acc[k], dequant((code >> (2 * k)) & 3u, sc, z));
-        }
-        uint4 o;
-        o.x = pack_bf16x2(acc[0], acc[1]);
-        o.y = pack_bf16x2(acc[2], acc[3]);
-        o.z = pack_bf16x2(acc[4], acc[5]);
-        o.w = pack_bf16x2(acc[6], acc[7]);
-        stg_v4_stream(a.out + (int64_t)h * a.out_head_stride + i * a.out_token_stride + sub * 8, o);
+        for (int s = 0; s < kMaxStages; ++s)
+            if (s < a.S) dequant_add16(acc, code[k][s], meta[k][s]);
+        uint4 o0, o1;
+        pack16_bf16(acc, o0, o1);
+        uint16_t* op = a.out + (int64_t)h * a.out_head_stride + ii[k] * a.out_token_stride + t * 16;
+        stg_v4_stream(op, o0);
+        stg_v4_stream(op + 8, o1);
     }
 }
 
 template <int D, int G>
 cudaError_t encode_dg(const EncodeArgs& a, cudaStream_t s) {
-    using M = RowMap<D>;
+    using M = Map16<D>;
     if (a.n_tokens == 0) return cudaSuccess;
-    dim3 grid((unsigned)((a.n_tokens + M::ROWS_PER_CTA - 1) / M::ROWS_PER_CTA), (unsigned)a.H);
+    const int64_t rows_per_cta = (int64_t)M::RPS * kEncRowsPerThread;
+    dim3 grid((unsigned)((a.n_tokens + rows_per_cta - 1) / rows_per_cta), (unsigned)a.H);
     if (a.C > 0) prq_encode_kernel<D, G, true><<<grid, kThreads, 0, s>>>(a);
     else prq_encode_kernel<D, G, false><<<grid, kThreads, 0, s>>>(a);
     return cudaGetLastError();
@@ -183,12 +192,13 @@ cudaError_t encode_dg(const EncodeArgs& a, cudaStream_t s) {
 
 template <int D, int G>
 cudaError_t decode_dg(const DecodeArgs& a, cudaStream_t s) {
-    using M = RowMap<D>;
+    using M = Map16<D>;
     const int64_t rows = a.tok_end - a.tok_begin;
     if (rows <= 0) return cudaSuccess;
-    dim3 grid((unsigned)((rows + M::ROWS_PER_CTA - 1) / M::ROWS_PER_CTA), (unsigned)a.H);
+    const int64_t rows_per_cta = (int64_t)M::RPS * kDecRowsPerThread;
+    dim3 grid((unsigned)((rows + rows_per_cta - 1) / rows_per_cta), (unsigned)a.H);
     if (a.C > 0 && a.chunk_offset) {
-        size_t smem = sizeof(int64_t) * (a.n_chunks + 1) + sizeof(int32_t) * a.n_chunks;
+        const size_t smem = sizeof(int64_t) * (a.n_chunks + 1) + sizeof(int32_t) * a.n_chunks;
         prq_decode_kernel<D, G, true, true><<<grid, kThreads, smem, s>>>(a);
     } else if (a.C > 0) {
         prq_decode_kernel<D, G, true, false><<<grid, kThreads, 0, s>>>(a);

@@ -1,0 +1,135 @@
+// One thread's share of progressive residual quantisation: 16 consecutive
+// channels of a token row (Quant VideoGen explainer, Sommario tecnico
+// sec. 2B: each stage re-quantises what the previous stages left; decoding
+// dequantises and sums the stages onto the centroid).
+//
+// Arithmetic per element and stage (identical, operation for operation, to
+// the plain statement of the quantiser):
+//   t = (r - z) * inv            two IEEE single operations
+//   q = clamp(rint(t), 0, 3)     computed as rint(clamp(t, 0, 3)), which is
+//                                the same integer because 0 and 3 are
+//                                integers; rint by adding and subtracting
+//                                1.5 * 2^23, whose IEEE sum rounds to an
+//                                integer with ties to even
+//   d = fma(q, s, z)             q*s is exact, so this is q*s + z rounded once
+//   r = r - d
+// The 16 2-bit codes go to one 32-bit word, element k at bits 2k, 2k+1.
+#pragma once
+
+#include "common.cuh"
+
+namespace qvg {
+
+constexpr float kRintMagic = 12582912.0f;   // 1.5 * 2^23
+constexpr uint32_t kQMagicBits = 0x4B000000u;  // bit pattern of 2^23
+
+__device__ __forceinline__ void unpack16(const uint4& lo, const uint4& hi, float* f) {
+    f[0] = bf16_lo(lo.x); f[1] = bf16_hi(lo.x);
+    f[2] = bf16_lo(lo.y); f[3] = bf16_hi(lo.y);
+    f[4] = bf16_lo(lo.z); f[5] = bf16_hi(lo.z);
+    f[6] = bf16_lo(lo.w); f[7] = bf16_hi(lo.w);
+    f[8] = bf16_lo(hi.x); f[9] = bf16_hi(hi.x);
+    f[10] = bf16_lo(hi.y); f[11] = bf16_hi(hi.y);
+    f[12] = bf16_lo(hi.z); f[13] = bf16_hi(hi.z);
+    f[14] = bf16_lo(hi.w); f[15] = bf16_hi(hi.w);
+}
+
+__device__ __forceinline__ void pack16_bf16(const float* f, uint4& lo, uint4& hi) {
+    lo.x = pack_bf16x2(f[0], f[1]);   lo.y = pack_bf16x2(f[2], f[3]);
+    lo.z = pack_bf16x2(f[4], f[5]);   lo.w = pack_bf16x2(f[6], f[7]);
+    hi.x = pack_bf16x2(f[8], f[9]);   hi.y = pack_bf16x2(f[10], f[11]);
+    hi.z = pack_bf16x2(f[12], f[13]); hi.w = pack_bf16x2(f[14], f[15]);
+}
+
+// r[i] -= c[i] (fp32, exact for bf16 operands of close magnitude, one
+// rounding otherwise).
+__device__ __forceinline__ void sub16(float* r, const float* c) {
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+        float2 d = f2_sub(make_float2(r[i], r[i + 1]), make_float2(c[i], c[i + 1]));
+        r[i] = d.x; r[i + 1] = d.y;
+    }
+}
+
+// One stage over the thread's 16 channels; the group spans TPG = G/16
+// consecutive lanes (all 32 lanes must call this together).  Returns the code
+// word; `meta` receives the group's (scale, zero) word.  When `update` the
+// residual is replaced by what the stage leaves; `acc` (may be null) gets the
+// dequantised values added.
+template <int TPG>
+__device__ __forceinline__ uint32_t quant_stage16(float* r, bool update, float* acc, uint32_t& meta) {
+    float mn = fmin3(r[0], r[1], r[2]), mx = fmax3(r[0], r[1], r[2]);
+#pragma unroll
+    for (int i = 3; i < 15; i += 2) {
+        mn = fmin3(mn, r[i], r[i + 1]);
+        mx = fmax3(mx, r[i], r[i + 1]);
+    }
+    mn = fminf(mn, r[15]);
+    mx = fmaxf(mx, r[15]);
+#pragma unroll
+    for (int off = 1; off < TPG; off <<= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    }
+    // a zero extreme is taken as +0 so the stored bits do not depend on the
+    // order in which equal extremes are met
+    mn = __fadd_rn(mn, 0.0f);
+    mx = __fadd_rn(mx, 0.0f);
+    const GroupParams p = group_params(mn, mx);
+    meta = p.meta;
+    const float2 z2 = make_float2(p.z, p.z), inv2 = make_float2(p.inv, p.inv);
+    const float2 s2 = make_float2(p.s, p.s), m2 = make_float2(kRintMagic, kRintMagic);
+    uint32_t vb[16];
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+        float2 t = f2_mul(f2_sub(make_float2(r[i], r[i + 1]), z2), inv2);
+        t.x = fminf(fmaxf(t.x, 0.0f), 3.0f);
+        t.y = fminf(fmaxf(t.y, 0.0f), 3.0f);
+        const float2 v = f2_add(t, m2);             // 1.5*2^23 + q exactly
+        vb[i] = __float_as_uint(v.x);
+        vb[i + 1] = __float_as_uint(v.y);
+        if (update || acc) {
+            const float2 q = f2_sub(v, m2);
+            const float2 d = f2_fma(q, s2, z2);
+            if (update) {
+                const float2 nr = f2_sub(make_float2(r[i], r[i + 1]), d);
+                r[i] = nr.x; r[i + 1] = nr.y;
+            }
+            if (acc) {
+                const float2 na = f2_add(make_float2(acc[i], acc[i + 1]), d);
+                acc[i] = na.x; acc[i + 1] = na.y;
+            }
+        }
+    }
+    // the low byte of vb[k] is q_k; gather bytes {q_j, q_{j+4}, q_{j+8}, q_{j+12}}
+    // into W_j, then interleave the four words two bits apart
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t lo = prmt(vb[j], vb[j + 4], 0x0040u);
+        const uint32_t hi = prmt(vb[j + 8], vb[j + 12], 0x0040u);
+        w[j] = prmt(lo, hi, 0x5410u);
+    }
+    return w[0] | (w[1] << 2) | (w[2] << 4) | (w[3] << 6);
+}
+
+// acc[k] += q_k * s + z for the 16 codes of `code` (element k at bits 2k).
+__device__ __forceinline__ void dequant_add16(float* acc, uint32_t code, uint32_t meta) {
+    const float s = f16_bits_to_f32(meta), z = f16_bits_to_f32(meta >> 16);
+    const float2 s2 = make_float2(s, s), z2 = make_float2(z, z);
+    const float2 b2 = make_float2(8388608.0f, 8388608.0f);
+    uint32_t t[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) t[i] = (code >> (2 * i)) & 0x03030303u;   // byte j = q_{4j+i}
+#pragma unroll
+    for (int k = 0; k < 16; k += 2) {
+        const uint32_t ba = prmt(t[k & 3], kQMagicBits, 0x7650u | (uint32_t)(k >> 2));
+        const uint32_t bb = prmt(t[(k + 1) & 3], kQMagicBits, 0x7650u | (uint32_t)((k + 1) >> 2));
+        const float2 q = f2_sub(make_float2(__uint_as_float(ba), __uint_as_float(bb)), b2);
+        const float2 d = f2_fma(q, s2, z2);
+        const float2 na = f2_add(make_float2(acc[k], acc[k + 1]), d);
+        acc[k] = na.x; acc[k + 1] = na.y;
+    }
+}
+
+}  // namespace qvg

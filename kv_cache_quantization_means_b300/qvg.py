@@ -15,7 +15,8 @@ LIB_PATH = os.path.join(_HERE, "libqvg.so")
 QVG_OK, QVG_ERR_INVALID_ARG, QVG_ERR_UNSUPPORTED, QVG_ERR_CAPACITY, QVG_ERR_CUDA, QVG_ERR_TIMEOUT = range(6)
 
 EXPORTS = [
-    "qvg_last_error", "qvg_version", "qvg_encoded_bytes", "qvg_workspace_bytes", "qvg_fit_centroids",
+    "qvg_last_error", "qvg_version", "qvg_encoded_bytes", "qvg_workspace_bytes", "qvg_fit_stats",
+    "qvg_fit_centroids",
     "qvg_assign", "qvg_update", "qvg_encode", "qvg_decode", "qvg_append_chunk", "qvg_decode_cache",
     "coral_predict_encode", "coral_predict_decode",
 ]
@@ -65,6 +66,7 @@ def load(path=LIB_PATH):
     L.qvg_version.restype = ctypes.c_char_p
     L.qvg_encoded_bytes.argtypes = [PCFG, I64, I32, PSZ, PSZ, PSZ, PSZ]
     L.qvg_workspace_bytes.argtypes = [PCFG, I64, PSZ]
+    L.qvg_fit_stats.argtypes = [PCFG, I64, P, SZ, ctypes.POINTER(ctypes.c_uint64), P]
     L.qvg_fit_centroids.argtypes = [PCFG, P, I64, I64, I64, P, P, P, I64, I64, P, SZ, P]
     L.qvg_assign.argtypes = [PCFG, P, I64, I64, I64, P, P, I64, I64, P, SZ, P]
     L.qvg_update.argtypes = [PCFG, P, I64, I64, I64, P, I64, I64, P, P, SZ, P]
@@ -125,6 +127,13 @@ def qvg_workspace_bytes(cfg, n_tokens):
     b = ctypes.c_size_t()
     _check(load().qvg_workspace_bytes(ctypes.byref(cfg), n_tokens, ctypes.byref(b)))
     return b.value
+
+
+def qvg_fit_stats(cfg, n_tokens, workspace, stream=None):
+    out = (ctypes.c_uint64 * 4)()
+    _check(load().qvg_fit_stats(ctypes.byref(cfg), n_tokens, _ptr(workspace), _nbytes(workspace), out,
+                                _stream(stream)))
+    return tuple(int(v) for v in out)
 
 
 def qvg_fit_centroids(cfg, x, n_tokens, head_stride, token_stride, warm_start, centroids, ids, capacity,

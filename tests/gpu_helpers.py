@@ -64,6 +64,7 @@ def run_fit_encode_decode(Q, cfg, x_dev, n, head_stride, token_stride, capacity=
     if cfg.num_clusters > 0:
         Q.qvg_fit_centroids(cfg, x_dev, n, head_stride, token_stride, warm, enc["centroids"], enc["ids"], cap,
                             offset, ws)
+        assert Q.qvg_fit_stats(cfg, n, ws)[3] == 0, "a k-means kernel gave up a wait"
     Q.qvg_encode(cfg, x_dev, n, head_stride, token_stride, enc["centroids"], 0, enc["codes"], enc["meta"],
                  enc["ids"], cap, offset, ws)
     b, e = decode_range if decode_range else (offset, offset + n)

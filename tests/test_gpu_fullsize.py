@@ -30,6 +30,10 @@ def run_layer(qvg, wl, tensor, layer=0):
     enc = Encoded(qvg, cfg, N)
     ws = qvg.alloc_workspace(cfg, N)
     qvg.qvg_fit_centroids(cfg, x, N, D, H * D, None, enc["centroids"], enc["ids"], N, 0, ws)
+    stats = qvg.qvg_fit_stats(cfg, N, ws)
+    assert stats[3] == 0, "a k-means kernel gave up a wait"
+    print(f"\n{wl.name} tensor {tensor}: {wl.lloyd_iters} Lloyd assigns re-ranked {stats[0]} of {wl.lloyd_iters * H * N} rows exactly "
+          f"({stats[0] / (wl.lloyd_iters * H * N):.4f}), {stats[1]} settled in fp64")
     qvg.qvg_encode(cfg, x, N, D, H * D, enc["centroids"], 0, enc["codes"], enc["meta"], enc["ids"], N, 0, ws)
     out = torch.empty((N, H, D), dtype=torch.int16, device="cuda")
     qvg.qvg_decode(cfg, enc["codes"], enc["meta"], enc["ids"], enc["centroids"], N, 0, N, out, D, H * D)
