@@ -167,6 +167,99 @@ class QvgStep:
         return cb + mb + ib + xb
 
 
+class CoralStep:
+    """Cross-layer closed loop of the Coral-KV workload (24 layers x 16 heads x
+    128 x 16,384 tokens, K and V): per tensor, layer 0 is PRQ-coded, then for
+    each l the block-DPLR prediction from the reconstructed layer l is
+    subtracted from layer l+1 and the residual PRQ-coded (encoder), and the
+    chain is decoded back (decoder)."""
+
+    def __init__(self, Q, wl, layers):
+        import torch
+        from synth import gpu as SG
+        self.Q, self.wl, self.L = Q, wl, layers
+        H, D, N, S, G = wl.heads, wl.head_dim, wl.tokens, wl.stages, wl.group_size
+        self.cfg = Q.config(H, D, 0, 0, S, G)
+        self.N, self.H, self.D, self.HD = N, H, D, H * D
+        self.x = [SG.coral_chain_gpu(wl, t, n_layers=layers) for t in (0, 1)]        # [L][N][HD]
+        self.preds = []
+        for l in range(layers - 1):
+            B, U, W = SG.coral_predictor_device(wl, l)
+            self.preds.append(Q.qvg.coral_predictor(B=B.data_ptr(), U=U.data_ptr(), W=W.data_ptr(), rank=wl.rank))
+        self.codes = [[torch.empty(S * H * N * D // 16, dtype=torch.int32, device="cuda") for _ in range(layers)]
+                      for _ in (0, 1)]
+        self.meta = [[torch.empty(S * H * N * D // G, dtype=torch.int32, device="cuda") for _ in range(layers)]
+                     for _ in (0, 1)]
+        self.xh = [torch.empty((layers, N, H * D), dtype=torch.int16, device="cuda") for _ in (0, 1)]
+        self.dec = [torch.empty((layers, N, H * D), dtype=torch.int16, device="cuda") for _ in (0, 1)]
+        self.ws = Q.alloc_workspace(self.cfg, N)
+        self.bytes_per_step = 2 * layers * N * H * D * 2
+        self.launches_per_step = 2 * (1 + 2 * (layers - 1)) * 2
+
+    def encode(self, t, l):
+        prev = None if l == 0 else self.xh[t][l - 1]
+        pred = None if l == 0 else self.preds[l - 1]
+        self.Q.coral_predict_encode(self.cfg, pred, prev, self.x[t][l], self.N, self.codes[t][l], self.meta[t][l],
+                                    self.xh[t][l], None, self.ws)
+
+    def decode(self, t, l):
+        prev = None if l == 0 else self.dec[t][l - 1]
+        pred = None if l == 0 else self.preds[l - 1]
+        self.Q.coral_predict_decode(self.cfg, pred, prev, self.N, self.codes[t][l], self.meta[t][l],
+                                    self.dec[t][l], None, self.ws)
+
+    def step(self):
+        for t in (0, 1):
+            for l in range(self.L):
+                self.encode(t, l)
+            for l in range(self.L):
+                self.decode(t, l)
+
+
+class StreamStep:
+    """Streaming rollout on the Wan2.1 shape (30 layers x 12 heads x 128): 40
+    steps, each appending a 3-frame chunk of 4680 tokens per layer and tensor
+    (a warm-started refit every 8th chunk, assign-only otherwise) and then
+    decoding the whole history of every layer, layer by layer, into one
+    reused bf16 buffer.  One bench step = the whole rollout."""
+
+    def __init__(self, Q, wl, layers):
+        import torch
+        from synth import gpu as SG
+        self.Q, self.wl, self.L = Q, wl, layers
+        H, D, N = wl.heads, wl.head_dim, wl.tokens
+        self.cfg = Q.config(H, D, wl.clusters, wl.lloyd_iters, wl.stages, wl.group_size)
+        self.N, self.H, self.D = N, H, D
+        self.chunk, self.steps, self.every = wl.chunk_tokens, wl.steps, wl.refit_every
+        self.x = [[SG.mixture_layer_gpu(wl, l, t, layout="nhd") for t in (0, 1)] for l in range(layers)]
+        vmax = (self.steps + self.every - 1) // self.every
+        self.caches = [[Q.make_cache(self.cfg, N, vmax, self.steps) for _ in (0, 1)] for _ in range(layers)]
+        self.ws = Q.alloc_workspace(self.cfg, self.chunk)
+        self.out = torch.empty((N, H, D), dtype=torch.int16, device="cuda")
+        per_tok = H * D * 2
+        self.enc_bytes = 2 * layers * N * per_tok
+        self.dec_bytes = 2 * layers * per_tok * self.chunk * sum(range(1, self.steps + 1))
+        self.bytes_per_step = self.enc_bytes + self.dec_bytes
+
+    def reset(self):
+        for row in self.caches:
+            for c, _ in row:
+                c.n_used = 0
+                c.n_versions = 0
+                c.n_chunks = 0
+
+    def step(self):
+        self.reset()
+        H, D, ch = self.H, self.D, self.chunk
+        for k in range(self.steps):
+            for l in range(self.L):
+                for t in (0, 1):
+                    c, _ = self.caches[l][t]
+                    xs = self.x[l][t][k * ch:(k + 1) * ch]
+                    self.Q.qvg_append_chunk(self.cfg, c, xs, ch, D, H * D, k % self.every == 0, self.ws)
+                    self.Q.qvg_decode_cache(self.cfg, c, 0, c.n_used, self.out, D, H * D)
+
+
 def time_fn(fn, reps, stream=None):
     import torch
     s = torch.cuda.current_stream() if stream is None else stream
@@ -312,13 +405,60 @@ def config_block(wl, args):
             "parallelism": f"replicas x{args.gpus}"}
 
 
+def run_aux(args, Q, wl, peaks, world, rank, local):
+    """Bench line of the cross-layer (coral) or streaming (stream) workload:
+    whole step captured in one CUDA graph, device-timed; the roofline is that
+    of the step's dominant kernel family."""
+    import torch
+    hbm = peaks[0]
+    if args.config == "coral":
+        st = CoralStep(Q, wl, wl.layers)
+    else:
+        st = StreamStep(Q, wl, wl.layers)
+    st.step()
+    torch.cuda.synchronize()
+    t_step = graph_time(st.step, max(1, args.steps))
+    if args.config == "coral":
+        L, n = st.L, st.N * st.HD
+        t_dec = graph_time(lambda: [st.decode(t, l) for t in (0, 1) for l in range(L)], 3) / (2 * L)
+        dec_bytes = n * (2 + wl.stages * (2 / 8 + 4 / wl.group_size) + 2)   # read x_hat_l, codes+meta; write x_hat_l+1
+        dom = {"kernel": "coral decode (low-rank + predict/decode per layer)", "bound": "hbm",
+               "achieved": dec_bytes / t_dec / 1e9, "peak": hbm, "unit": "GB/s", "time_us": t_dec * 1e6}
+        cfgb = {"workload": f"{wl.name}: {wl.layers} layers x {wl.heads} heads x head_dim {wl.head_dim} x {wl.tokens} "
+                            f"tokens, K and V, closed-loop block-DPLR (rank {wl.rank}) + PRQ S={wl.stages} G={wl.group_size}, "
+                            "encode chain + decode chain"}
+    else:
+        c = st.caches[-1][-1][0]
+        lens = [st.chunk * (k + 1) for k in range(st.steps)]
+        t_dec = graph_time(lambda: [Q.qvg_decode_cache(st.cfg, c, 0, n, st.out, st.D, st.H * st.D) for n in lens], 3)
+        el = sum(lens) * st.H * st.D
+        b = el * (wl.stages * (2 / 8 + 4 / wl.group_size) + 1 / wl.head_dim + 2)
+        dom = {"kernel": "prq_decode (versioned history decode)", "bound": "hbm", "achieved": b / t_dec / 1e9,
+               "peak": hbm, "unit": "GB/s", "time_us": t_dec / st.steps * 1e6}
+        cfgb = {"workload": f"{wl.name}: {wl.layers} layers x {wl.heads} heads x head_dim {wl.head_dim}; {wl.steps} steps "
+                            f"of {wl.chunk_tokens}-token chunks (refit every {wl.refit_every}, C={wl.clusters} "
+                            f"T={wl.lloyd_iters}), full-history decode of every layer per step; value counts bf16 bytes "
+                            f"encoded ({st.enc_bytes / 1e9:.1f} GB) + decoded ({st.dec_bytes / 1e9:.1f} GB)"}
+    dom["frac"] = dom["achieved"] / dom["peak"]
+    dom["traffic"] = None
+    dom["peak_kind"] = peaks[3]
+    value = st.bytes_per_step * world / t_step / 1e9
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": cfgb, "roofline": dom,
+            "cpu_baseline": None, "e2e": None, "cuda_graph": True}
+    if rank == 0:
+        print(json.dumps(line))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="wan", choices=["wan", "large"])
+    ap.add_argument("--config", default="wan", choices=["wan", "large", "coral", "stream"])
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -345,6 +485,8 @@ def main():
     Q.load()
     wl = workload(args.config)
     peaks = load_peaks()
+    if args.config in ("coral", "stream"):
+        return run_aux(args, Q, wl, peaks, world, rank, local)
     layers = wl.layers if args.config == "wan" else 2
     st = QvgStep(Q, wl, layers)
     torch.cuda.synchronize()

@@ -242,6 +242,29 @@ __device__ __forceinline__ float warp_dist(const uint8_t* xs, int row, const uin
     return acc;
 }
 
+// Squared distance in fp64, channels split over the warp.  Every term is
+// rounded at most once and the sum of n = D non-negative terms errs by at
+// most about (n + 1) * 2^-53 of the total, in any order; so two such
+// distances further apart than 2^-42 of the larger compare the same way as
+// the channel-order sums of the plain definition.
+template <int D>
+__device__ __forceinline__ double warp_dist_f64(const uint8_t* xs, int row, const uint8_t* cs, int j, uint32_t cslab,
+                                                int lane) {
+    constexpr int CPL = D / 32;
+    const int i0 = lane * CPL;
+    double acc = 0.0;
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) {
+        const double xv = (double)bf16f(*reinterpret_cast<const uint16_t*>(xs + sw_off(row, i0 + k, kAtomBytes)));
+        const double cv = (double)bf16f(*reinterpret_cast<const uint16_t*>(cs + sw_off(j, i0 + k, cslab)));
+        const double df = __dsub_rn(xv, cv);
+        acc = __dadd_rn(acc, __dmul_rn(df, df));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc = __dadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
+    return acc;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
     kmeans_assign_tc_kernel(const __grid_constant__ CUtensorMap tmap, TcArgs a) {
@@ -297,22 +320,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     const uint16_t* cg = a.cent + (int64_t)h * C * D;
-    for (int v = tid; v < Cpad * (D / 8); v += kTcThreads) {
-        const int j = v / (D / 8), k = v % (D / 8);
-        uint4 val = make_uint4(0, 0, 0, 0);
-        if (j < C) val = __ldg(reinterpret_cast<const uint4*>(cg + (int64_t)j * D) + k);
-        *reinterpret_cast<uint4*>(Bs + sw_off(j, k * 8, cslab)) = val;
-    }
-    for (int j = warp; j < Cpad; j += kTcThreads / 32) {
-        float s = 0.0f;
-        if (j < C) {
-            for (int i = lane; i < D; i += 32) {
-                const float c = bf16f(cg[(int64_t)j * D + i]);
-                s = __fmaf_rn(c, c, s);
+    {
+        // centroids -> swizzled shared memory, four independent 16-byte loads in flight per thread
+        constexpr int kBatch = 4;
+        const int total = Cpad * (D / 8);
+        for (int v0 = tid; v0 < total; v0 += kTcThreads * kBatch) {
+            uint4 val[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int v = v0 + u * kTcThreads;
+                const int j = v / (D / 8), k = v % (D / 8);
+                val[u] = make_uint4(0, 0, 0, 0);
+                if (v < total && j < C) val[u] = __ldg(reinterpret_cast<const uint4*>(cg + (int64_t)j * D) + k);
             }
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            for (int u = 0; u < kBatch; ++u) {
+                const int v = v0 + u * kTcThreads;
+                if (v < total) *reinterpret_cast<uint4*>(Bs + sw_off(v / (D / 8), (v % (D / 8)) * 8, cslab)) = val[u];
+            }
         }
+    }
+    __syncthreads();
+    // squared norms from shared memory, one warp per centroid
+    for (int j = warp; j < Cpad; j += kTcThreads / 32) {
+        float s = 0.0f;
+        for (int i = lane * 2; i < D; i += 64) {
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(Bs + sw_off(j, i, cslab));
+            const float c0 = bf16_lo(w), c1 = bf16_hi(w);
+            s = __fmaf_rn(c0, c0, s);
+            s = __fmaf_rn(c1, c1, s);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
         if (lane == 0) {
             cn[j] = j < C ? s : INFINITY;
             if (j < C) atomicMax(misc + 2, __float_as_uint(s));
@@ -386,7 +425,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int row = q * 32 + lane;          // tile row = TMEM lane
         const int ncols = Cpad / 2, nch = ncols / 32;
         const int col0 = half * ncols;
-        unsigned long long n_flag = 0, n_fp64 = 0;
+        unsigned long long n_flag = 0, n_fp64 = 0, n_seq = 0;
         for (int i = 0; i < n_tiles; ++i) {
             const int s = i % kStages, acc = i & 1;
             const uint32_t ph = (uint32_t)(i / kStages) & 1u, aph = (uint32_t)(i >> 1) & 1u;
@@ -492,18 +531,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         }
                     }
                 if (nsurv > 1) {
-                    // several survivors: the plain fp64 distance decides (ties -> lowest j)
+                    // several survivors: fp64 distances decide; candidates within
+                    // 2^-42 of the best are settled by the channel-order fp64 sum
+                    // of the plain definition (ties -> lowest j)
                     best = -1;
+                    double dbest = INFINITY;
                     for (int w = 0; w < Cpad / 32; ++w)
                         for (uint32_t m = mw[w]; m; m &= m - 1) {
                             const int j = 32 * w + __ffs(m) - 1;
                             const float d = warp_dist<D>(xs, r, Bs, j, cslab, lane);
                             if (d - (kDirectRel * d + kDirectAbs) > dmin + emin) continue;
-                            double cd = 0.0;
-                            if (lane == 0) cd = canonical_dist_smem<D>(xs, r, Bs, j, cslab);
-                            cd = __shfl_sync(0xffffffffu, cd, 0);
-                            if (cd < cbest) { cbest = cd; best = j; }
+                            const double dp = warp_dist_f64<D>(xs, r, Bs, j, cslab, lane);
+                            if (dp < dbest) { dbest = dp; best = j; }
                         }
+                    bool near = false;
+                    for (int w = 0; w < Cpad / 32 && !near; ++w)
+                        for (uint32_t m = mw[w]; m; m &= m - 1) {
+                            const int j = 32 * w + __ffs(m) - 1;
+                            if (j == best) continue;
+                            const float d = warp_dist<D>(xs, r, Bs, j, cslab, lane);
+                            if (d - (kDirectRel * d + kDirectAbs) > dmin + emin) continue;
+                            const double dp = warp_dist_f64<D>(xs, r, Bs, j, cslab, lane);
+                            if (dp - dbest <= 0x1p-42 * fmax(dp, dbest) + 1e-300) { near = true; break; }
+                        }
+                    if (near) {
+                        best = -1;
+                        for (int w = 0; w < Cpad / 32; ++w)
+                            for (uint32_t m = mw[w]; m; m &= m - 1) {
+                                const int j = 32 * w + __ffs(m) - 1;
+                                const float d = warp_dist<D>(xs, r, Bs, j, cslab, lane);
+                                if (d - (kDirectRel * d + kDirectAbs) > dmin + emin) continue;
+                                const double dp = warp_dist_f64<D>(xs, r, Bs, j, cslab, lane);
+                                if (dp - dbest > 0x1p-42 * fmax(dp, dbest) + 1e-300) continue;
+                                double cd = 0.0;
+                                if (lane == 0) cd = canonical_dist_smem<D>(xs, r, Bs, j, cslab);
+                                cd = __shfl_sync(0xffffffffu, cd, 0);
+                                if (cd < cbest) { cbest = cd; best = j; }
+                            }
+                        ++n_seq;
+                    }
                     ++n_fp64;
                 }
                 const int64_t tk = (int64_t)(t_begin + i) * kTile + r;
@@ -517,9 +583,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(empty_bar + 8 * s);
         }
-        if (a.stats && lane == 0 && (n_flag | n_fp64)) {
+        if (a.stats && lane == 0 && (n_flag | n_fp64 | n_seq)) {
             atomicAdd(a.stats, n_flag);
             atomicAdd(a.stats + 1, n_fp64);
+            atomicAdd(a.stats + 2, n_seq);
         }
     }
 

@@ -372,8 +372,11 @@ __global__ void kmeans_init_kernel(const uint16_t* x, int64_t head_stride, int64
 constexpr int kSortThreads = 1024;
 constexpr int kSortWarps = kSortThreads / 32;
 
+constexpr int kSortStage = 8192;    // ids staged in shared memory per round
+
 __global__ void __launch_bounds__(kSortThreads) kmeans_sort_kernel(UpdateArgs a) {
     __shared__ int hist[kSortWarps][kMaxClusters];
+    __shared__ __align__(16) uint8_t ids_s[kSortStage];
     __shared__ int cnt_s[kMaxClusters];
     __shared__ int off_s[kMaxClusters];
     __shared__ int pfirst_s[kMaxClusters + 1];
@@ -383,14 +386,22 @@ __global__ void __launch_bounds__(kSortThreads) kmeans_sort_kernel(UpdateArgs a)
     const uint8_t* idh = a.ids + (int64_t)h * a.cap + a.tok_offset;
     for (int i = tid; i < kSortWarps * kMaxClusters; i += kSortThreads) (&hist[0][0])[i] = 0;
     __syncthreads();
-    const int64_t w0 = (int64_t)warp * N / kSortWarps, w1 = (int64_t)(warp + 1) * N / kSortWarps;
-    for (int64_t b = w0; b < w1; b += 32) {
-        const int64_t n = b + lane;
-        const int id = n < w1 ? min((int)idh[n], C - 1) : -1;
-        const unsigned m = __match_any_sync(0xffffffffu, id);
-        if (id >= 0 && lane == __ffs(m) - 1) hist[warp][id] += __popc(m);
+    // Tokens are taken in rounds of kSortStage staged in shared memory; within
+    // a round warp w owns a contiguous slice.  A cluster's positions follow
+    // (warp, round, token) order: fixed, whatever the scheduling.
+    for (int64_t r0 = 0; r0 < N; r0 += kSortStage) {
+        const int rn = (int)min((int64_t)kSortStage, N - r0);
+        for (int i = tid; i < rn; i += kSortThreads) ids_s[i] = idh[r0 + i];
+        __syncthreads();
+        const int w0 = warp * rn / kSortWarps, w1 = (warp + 1) * rn / kSortWarps;
+        for (int b = w0; b < w1; b += 32) {
+            const int n = b + lane;
+            const int id = n < w1 ? min((int)ids_s[n], C - 1) : -1;
+            const unsigned m = __match_any_sync(0xffffffffu, id);
+            if (id >= 0 && lane == __ffs(m) - 1) hist[warp][id] += __popc(m);
+        }
+        __syncthreads();
     }
-    __syncthreads();
     for (int j = tid; j < C; j += kSortThreads) {
         int tot = 0;
         for (int w = 0; w < kSortWarps; ++w) tot += hist[w][j];
@@ -445,92 +456,111 @@ __global__ void __launch_bounds__(kSortThreads) kmeans_sort_kernel(UpdateArgs a)
     __syncthreads();
     int* perm = a.perm + (int64_t)h * N;
     const unsigned lt = (1u << lane) - 1u;
-    for (int64_t b = w0; b < w1; b += 32) {
-        const int64_t n = b + lane;
-        const int id = n < w1 ? min((int)idh[n], C - 1) : -1;
-        const unsigned m = __match_any_sync(0xffffffffu, id);
-        if (id >= 0) perm[hist[warp][id] + __popc(m & lt)] = (int)n;
-        __syncwarp();
-        if (id >= 0 && lane == __ffs(m) - 1) hist[warp][id] += __popc(m);
-        __syncwarp();
+    for (int64_t r0 = 0; r0 < N; r0 += kSortStage) {
+        const int rn = (int)min((int64_t)kSortStage, N - r0);
+        for (int i = tid; i < rn; i += kSortThreads) ids_s[i] = idh[r0 + i];
+        __syncthreads();
+        const int w0 = warp * rn / kSortWarps, w1 = (warp + 1) * rn / kSortWarps;
+        for (int b = w0; b < w1; b += 32) {
+            const int n = b + lane;
+            const int id = n < w1 ? min((int)ids_s[n], C - 1) : -1;
+            const unsigned m = __match_any_sync(0xffffffffu, id);
+            if (id >= 0) perm[hist[warp][id] + __popc(m & lt)] = (int)(r0 + n);
+            __syncwarp();
+            if (id >= 0 && lane == __ffs(m) - 1) hist[warp][id] += __popc(m);
+            __syncwarp();
+        }
+        __syncthreads();
     }
 }
 
-template <int DPL>
-__device__ __forceinline__ void load_lane_channels(const uint16_t* p, uint32_t* v) {
-    if constexpr (DPL == 4) {
-        const uint2 w = *reinterpret_cast<const uint2*>(p);
-        v[0] = w.x & 0xFFFFu; v[1] = w.x >> 16; v[2] = w.y & 0xFFFFu; v[3] = w.y >> 16;
-    } else if constexpr (DPL == 2) {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
-        v[0] = w & 0xFFFFu; v[1] = w >> 16;
-    } else {
-        v[0] = *p;
-    }
+__device__ __forceinline__ i128 shfl_xor_i128(i128 v, int mask) {
+    const uint64_t lo = (uint64_t)v, hi = (uint64_t)((u128)v >> 64);
+    const uint64_t olo = __shfl_xor_sync(0xffffffffu, lo, mask), ohi = __shfl_xor_sync(0xffffffffu, hi, mask);
+    return (i128)(((u128)ohi << 64) | (u128)olo);
 }
+
+// One warp per piece.  A lane owns 8 consecutive channels of one row slot;
+// D/8 lanes cover a row, so each 16-byte load instruction of the warp fetches
+// 32/(D/8) rows, and kSumBatch of them are in flight before any arithmetic.
+// Row slots are reduced at the end (integer additions: exact, any order).
+constexpr int kSumBatch = 8;
 
 template <int D>
 __global__ void __launch_bounds__(kThreads) kmeans_sum_kernel(UpdateArgs a) {
-    constexpr int DPL = D / 32;   // channels per lane
+    constexpr int LPR = D / 8, RPI = 32 / LPR;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int sub = lane % LPR, slot = lane / LPR;
     const int h = blockIdx.y;
     const int p = blockIdx.x * (kThreads / 32) + warp;
     if (p >= a.npieces[h]) return;
     const int4 pc = a.pieces[(int64_t)h * a.max_pieces + p];
     const int start = pc.x, len = pc.y, j = pc.z;
     const int* ph = a.perm + (int64_t)h * a.n_tokens + start;
-    const uint16_t* xh = a.x + (int64_t)h * a.head_stride + lane * DPL;
-    int w1[DPL], w2[DPL], w3[DPL];
+    const uint16_t* xh = a.x + (int64_t)h * a.head_stride + sub * 8;
+    int w1[8], w2[8], w3[8];
 #pragma unroll
-    for (int d = 0; d < DPL; ++d) w1[d] = w2[d] = w3[d] = 0;
+    for (int d = 0; d < 8; ++d) w1[d] = w2[d] = w3[d] = 0;
     float amax = 0.0f;
     for (int k0 = 0; k0 < len; k0 += 32) {
         const int cnt = min(32, len - k0);
         const int myn = lane < cnt ? ph[k0 + lane] : 0;
-        for (int u0 = 0; u0 < cnt; u0 += 8) {
-            uint32_t v[8][DPL];
+        for (int u0 = 0; u0 < cnt; u0 += RPI * kSumBatch) {
+            uint4 v[kSumBatch];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int n = __shfl_sync(0xffffffffu, myn, (u0 + u) & 31);
-                if (u0 + u < cnt) load_lane_channels<DPL>(xh + (int64_t)n * a.token_stride, v[u]);
-                else {
-#pragma unroll
-                    for (int d = 0; d < DPL; ++d) v[u][d] = 0;
-                }
+            for (int u = 0; u < kSumBatch; ++u) {
+                const int idx = u0 + u * RPI + slot;
+                const int n = __shfl_sync(0xffffffffu, myn, idx & 31);
+                v[u] = idx < cnt ? ldg_nc_v4(xh + (int64_t)n * a.token_stride) : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
+            for (int u = 0; u < kSumBatch; ++u) {
+                const uint32_t wv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
-                for (int d = 0; d < DPL; ++d) {
-                    const float xf = bf16f((uint16_t)v[u][d]);
-                    amax = fmaxf(amax, fabsf(xf));
-                    window_add(xf, w1[d], w2[d], w3[d]);
+                for (int q = 0; q < 4; ++q) {
+                    const float lo = bf16_lo(wv[q]), hi = bf16_hi(wv[q]);
+                    amax = fmax3(amax, fabsf(lo), fabsf(hi));
+                    window_add(lo, w1[2 * q], w2[2 * q], w3[2 * q]);
+                    window_add(hi, w1[2 * q + 1], w2[2 * q + 1], w3[2 * q + 1]);
                 }
+            }
         }
     }
-    i128 tot[DPL];
+    i128 tot[8];
     if (__any_sync(0xffffffffu, !(amax < kWinMax))) {
         // a value outside the first window: redo the piece with 128-bit sums
 #pragma unroll
-        for (int d = 0; d < DPL; ++d) tot[d] = 0;
-        for (int k = 0; k < len; ++k) {
-            uint32_t v[DPL];
-            load_lane_channels<DPL>(xh + (int64_t)ph[k] * a.token_stride, v);
+        for (int d = 0; d < 8; ++d) tot[d] = 0;
+        for (int k = slot; k < len; k += RPI) {
+            const uint4 v = ldg_nc_v4(xh + (int64_t)ph[k] * a.token_stride);
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int d = 0; d < DPL; ++d) tot[d] += bf16_to_i128_units(v[d]);
+            for (int q = 0; q < 4; ++q) {
+                tot[2 * q] += bf16_to_i128_units(wv[q] & 0xFFFFu);
+                tot[2 * q + 1] += bf16_to_i128_units(wv[q] >> 16);
+            }
         }
     } else {
 #pragma unroll
-        for (int d = 0; d < DPL; ++d) tot[d] = windows_to_i128(w1[d], w2[d], w3[d]);
+        for (int d = 0; d < 8; ++d) tot[d] = windows_to_i128(w1[d], w2[d], w3[d]);
     }
+#pragma unroll
+    for (int o = LPR; o < 32; o <<= 1)
+#pragma unroll
+        for (int d = 0; d < 8; ++d) tot[d] += shfl_xor_i128(tot[d], o);
+    if (slot != 0) return;
     if (pc.w) {
-        uint16_t* cr = a.cent + ((int64_t)h * a.C + j) * D + lane * DPL;
+        uint16_t r[8];
 #pragma unroll
-        for (int d = 0; d < DPL; ++d) cr[d] = mean_bf16_bits(tot[d], (uint32_t)len);
+        for (int d = 0; d < 8; ++d) r[d] = mean_bf16_bits(tot[d], (uint32_t)len);
+        uint4 o;
+        o.x = r[0] | ((uint32_t)r[1] << 16); o.y = r[2] | ((uint32_t)r[3] << 16);
+        o.z = r[4] | ((uint32_t)r[5] << 16); o.w = r[6] | ((uint32_t)r[7] << 16);
+        *reinterpret_cast<uint4*>(a.cent + ((int64_t)h * a.C + j) * D + sub * 8) = o;
     } else {
-        i128* pr = reinterpret_cast<i128*>(a.partials) + ((int64_t)h * a.max_pieces + p) * D + lane * DPL;
+        i128* pr = reinterpret_cast<i128*>(a.partials) + ((int64_t)h * a.max_pieces + p) * D + sub * 8;
 #pragma unroll
-        for (int d = 0; d < DPL; ++d) pr[d] = tot[d];
+        for (int d = 0; d < 8; ++d) pr[d] = tot[d];
     }
 }
 
