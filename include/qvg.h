@@ -132,7 +132,7 @@ QVG_API qvg_status qvg_workspace_bytes(const qvg_config* cfg, int64_t n_tokens, 
 /* Diagnostics of the last k-means call (fit, assign, update, append) that
  * used `workspace`: out[0] = token rows the tensor-core screen could not
  * decide and re-ranked exactly, out[1] = those among them whose nearest
- * centroid was settled by fp64 squared distances, out[2] = those among
+ * centroid was settled by exact squared distances, out[2] = those among
  * them that needed the channel-order fp64 sum (near-exact ties),
  * out[3] = error word (0 = none; 0x7E000000 = a kernel gave up waiting on an
  * internal barrier and its ids are not valid).  Copies from the device and

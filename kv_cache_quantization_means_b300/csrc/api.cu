@@ -85,7 +85,8 @@ struct FitWorkspace {
     int4* pieces;       // [H][max_pieces]
     void* partials;     // [H][max_pieces][D] 16-byte exact sums
     unsigned long long* stats;  // [4]
-    int max_pieces;
+    int* blockhist;     // [H][n_blocks][C]
+    int max_pieces, n_blocks;
     size_t bytes;
 };
 
@@ -107,6 +108,8 @@ FitWorkspace carve(const qvg_config* c, int64_t n, void* base) {
     w.pieces = (int4*)take(sizeof(int4) * H * (size_t)w.max_pieces);
     w.partials = take((size_t)16 * H * (size_t)w.max_pieces * D);
     w.stats = (unsigned long long*)take(sizeof(unsigned long long) * 4);
+    w.n_blocks = (int)((N + qvg::kSortBlock - 1) / qvg::kSortBlock);
+    w.blockhist = (int*)take(sizeof(int) * H * (size_t)w.n_blocks * C);
     w.bytes = o;
     return w;
 }
@@ -141,6 +144,7 @@ qvg::UpdateArgs update_args(const qvg_config* c, const qvg_bf16* x, int64_t n, i
     u.ids = ids; u.cap = cap; u.tok_offset = off;
     u.H = c->num_heads; u.C = c->num_clusters;
     u.max_pieces = w.max_pieces;
+    u.n_blocks = w.n_blocks; u.blockhist = w.blockhist;
     u.counts = w.counts; u.first_piece = w.first_piece; u.npieces = w.npieces;
     u.perm = w.perm; u.pieces = w.pieces; u.partials = w.partials; u.cent = cent;
     return u;

@@ -86,12 +86,15 @@ __device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes) {
                  : "memory");
 }
 
+// One bounded probe; the thread may be suspended (up to ~0.1 ms) until the
+// phase completes, so a waiting warp does not spin on the issue slots.
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(100000u)
         : "memory");
     return ok != 0;
 }
@@ -109,7 +112,7 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     const uint64_t t0 = global_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try(bar, parity)) return true;
-        if ((it & 255u) == 0 && global_ns() - t0 > 2000000000ull) return false;
+        if ((it & 15u) == 0 && global_ns() - t0 > 2000000000ull) return false;
     }
 }
 
@@ -169,11 +172,13 @@ __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.
 
 // ----------------------------------------------------- shared memory map
 
-struct alignas(16) RowX {      // per tile row, exchanged between the two column halves
-    float bmin[2];
-    float xn[2];
-    int cnt[2];
-    int idx[2];
+// Per tile row, exchanged between the two column halves (structure of
+// arrays: consecutive rows are consecutive words, no bank conflicts).
+struct RowX {
+    float bmin[2][kTile];
+    float xn[2][kTile];
+    int cnt[2][kTile];
+    int idx[2][kTile];
 };
 
 struct Layout {
@@ -187,7 +192,7 @@ __host__ __device__ inline Layout make_layout(int D, int Cpad) {
     L.b_off = o;    o += (uint32_t)nA * Cpad * 128;
     L.x_off = o;    o += (uint32_t)kStages * nA * kAtomBytes;
     L.cn_off = o;   o += (uint32_t)Cpad * 4;
-    L.row_off = o;  o += (uint32_t)kTile * sizeof(RowX);
+    L.row_off = o;  o += (uint32_t)sizeof(RowX);
     L.mask_off = o; o += (uint32_t)kTile * (Cpad / 32) * 4;
     L.flag_off = o; o += (uint32_t)kTile * 4 + 16;
     L.bar_off = o;  o += (uint32_t)(2 * kStages + 4) * 8;
@@ -242,26 +247,43 @@ __device__ __forceinline__ float warp_dist(const uint8_t* xs, int row, const uin
     return acc;
 }
 
-// Squared distance in fp64, channels split over the warp.  Every term is
-// rounded at most once and the sum of n = D non-negative terms errs by at
-// most about (n + 1) * 2^-53 of the total, in any order; so two such
-// distances further apart than 2^-42 of the larger compare the same way as
-// the channel-order sums of the plain definition.
+typedef __int128 i128;
+
+// bf16 value in units of 2^-30, exact for 2^-23 <= |x| < 2^16 and for 0
+// (|value| < 2^46, so a difference squared and summed over 128 channels stays
+// below 2^101); `ok` is cleared for a value outside that range.
+__device__ __forceinline__ int64_t bf16_fixed30(uint32_t b, bool& ok) {
+    const int e = (int)((b >> 7) & 0xFFu);
+    const int64_t m = (int64_t)((b & 0x7Fu) | 0x80u);
+    if (e == 0 && (b & 0x7Fu) == 0) return 0;                  // +-0
+    if (e < 104 || e > 142) { ok = false; return 0; }
+    const int64_t v = m << (e - 104);                          // x = m * 2^(e-134)
+    return (b & 0x8000u) ? -v : v;
+}
+
+// Exact squared distance in units of 2^-60, channels split over the warp;
+// `ok` is false (on every lane) when a value lies outside the exact range.
 template <int D>
-__device__ __forceinline__ double warp_dist_f64(const uint8_t* xs, int row, const uint8_t* cs, int j, uint32_t cslab,
-                                                int lane) {
+__device__ __forceinline__ i128 warp_dist_exact(const uint8_t* xs, int row, const uint8_t* cs, int j, uint32_t cslab,
+                                                int lane, bool& ok) {
     constexpr int CPL = D / 32;
     const int i0 = lane * CPL;
-    double acc = 0.0;
+    bool good = true;
+    i128 acc = 0;
 #pragma unroll
     for (int k = 0; k < CPL; ++k) {
-        const double xv = (double)bf16f(*reinterpret_cast<const uint16_t*>(xs + sw_off(row, i0 + k, kAtomBytes)));
-        const double cv = (double)bf16f(*reinterpret_cast<const uint16_t*>(cs + sw_off(j, i0 + k, cslab)));
-        const double df = __dsub_rn(xv, cv);
-        acc = __dadd_rn(acc, __dmul_rn(df, df));
+        const uint32_t xb = *reinterpret_cast<const uint16_t*>(xs + sw_off(row, i0 + k, kAtomBytes));
+        const uint32_t cb = *reinterpret_cast<const uint16_t*>(cs + sw_off(j, i0 + k, cslab));
+        const int64_t df = bf16_fixed30(xb, good) - bf16_fixed30(cb, good);
+        acc += (i128)df * (i128)df;
     }
+    ok = __all_sync(0xffffffffu, good);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc = __dadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
+    for (int o = 16; o > 0; o >>= 1) {
+        const uint64_t lo = (uint64_t)acc, hi = (uint64_t)((unsigned __int128)acc >> 64);
+        const uint64_t olo = __shfl_xor_sync(0xffffffffu, lo, o), ohi = __shfl_xor_sync(0xffffffffu, hi, o);
+        acc += (i128)(((unsigned __int128)ohi << 64) | (unsigned __int128)olo);
+    }
     return acc;
 }
 
@@ -276,7 +298,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint8_t* Bs = base + L.b_off;
     uint8_t* Xs = base + L.x_off;
     float* cn = reinterpret_cast<float*>(base + L.cn_off);
-    RowX* rx = reinterpret_cast<RowX*>(base + L.row_off);
+    RowX& rx = *reinterpret_cast<RowX*>(base + L.row_off);
     uint32_t* maskw = reinterpret_cast<uint32_t*>(base + L.mask_off);
     int* flag_rows = reinterpret_cast<int*>(base + L.flag_off);
     int* nflag = flag_rows + kTile;
@@ -437,21 +459,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc_fence_after();
             const uint8_t* xs = Xs + (size_t)s * nA * kAtomBytes;
             const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * acc_cols + (uint32_t)col0;
-            // pass A: minimum score over this half
-            float bmin = INFINITY;
+            // pass A: minimum score over this half (two 32-column chunks per
+            // TMEM wait, four independent running minima)
+            float bmin;
             {
-                uint32_t v[32];
-                for (int c = 0; c < nch; ++c) {
-                    tmem_ld32(taddr + 32u * c, v);
+                uint32_t v[2][32];
+                float m4[4] = {INFINITY, INFINITY, INFINITY, INFINITY};
+                for (int c = 0; c < nch; c += 2) {
+                    tmem_ld32(taddr + 32u * c, v[0]);
+                    if (c + 1 < nch) tmem_ld32(taddr + 32u * (c + 1), v[1]);
                     tmem_wait_ld();
-                    const float* cnc = cn + col0 + 32 * c;
 #pragma unroll
-                    for (int jj = 0; jj < 32; jj += 2) {
-                        const float2 sc = f2_fma(make_float2(__uint_as_float(v[jj]), __uint_as_float(v[jj + 1])),
-                                                 make_float2(-2.0f, -2.0f), make_float2(cnc[jj], cnc[jj + 1]));
-                        bmin = fmin3(bmin, sc.x, sc.y);
+                    for (int cc = 0; cc < 2; ++cc) {
+                        if (c + cc >= nch) break;
+                        const float* cnc = cn + col0 + 32 * (c + cc);
+#pragma unroll
+                        for (int jj = 0; jj < 32; jj += 4) {
+                            const float4 cq = *reinterpret_cast<const float4*>(cnc + jj);
+                            const float2 s0 = f2_fma(make_float2(__uint_as_float(v[cc][jj]), __uint_as_float(v[cc][jj + 1])),
+                                                     make_float2(-2.0f, -2.0f), make_float2(cq.x, cq.y));
+                            const float2 s1 = f2_fma(make_float2(__uint_as_float(v[cc][jj + 2]), __uint_as_float(v[cc][jj + 3])),
+                                                     make_float2(-2.0f, -2.0f), make_float2(cq.z, cq.w));
+                            const int k = (jj >> 2) & 3;
+                            m4[k] = fmin3(m4[k], s0.x, s0.y);
+                            m4[k ^ 2] = fmin3(m4[k ^ 2], s1.x, s1.y);
+                        }
                     }
                 }
+                bmin = fminf(fminf(m4[0], m4[1]), fminf(m4[2], m4[3]));
             }
             // partial ||x||^2 of this row: half 0 takes the first D/2 channels
             float xn = 0.0f;
@@ -462,46 +497,57 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int k = 0; k < 8; ++k) xn = __fmaf_rn(f[k], f[k], xn);
             }
-            rx[row].bmin[half] = bmin;
-            rx[row].xn[half] = xn;
+            rx.bmin[half][row] = bmin;
+            rx.xn[half][row] = xn;
             epi_sync();
-            const float b1 = fminf(rx[row].bmin[0], rx[row].bmin[1]);
-            const float xnt = rx[row].xn[0] + rx[row].xn[1];
+            const float b1 = fminf(rx.bmin[0][row], rx.bmin[1][row]);
+            const float xnt = rx.xn[0][row] + rx.xn[1][row];
             const float E = 1.01f * (kScreenXC * sqrtf(xnt) * cm + kScreenCC * cm2) + 1e-30f;
             const float thr = b1 + 2.0f * E;
             // pass B: candidates within 2E of the minimum
             int cnt = 0, first = -1;
             {
-                uint32_t v[32];
-                for (int c = 0; c < nch; ++c) {
-                    tmem_ld32(taddr + 32u * c, v);
+                uint32_t v[2][32];
+                for (int c = 0; c < nch; c += 2) {
+                    tmem_ld32(taddr + 32u * c, v[0]);
+                    if (c + 1 < nch) tmem_ld32(taddr + 32u * (c + 1), v[1]);
                     tmem_wait_ld();
-                    const float* cnc = cn + col0 + 32 * c;
-                    uint32_t m = 0;
 #pragma unroll
-                    for (int jj = 0; jj < 32; jj += 2) {
-                        const float2 sc = f2_fma(make_float2(__uint_as_float(v[jj]), __uint_as_float(v[jj + 1])),
-                                                 make_float2(-2.0f, -2.0f), make_float2(cnc[jj], cnc[jj + 1]));
-                        if (sc.x <= thr) m |= 1u << jj;
-                        if (sc.y <= thr) m |= 2u << jj;
+                    for (int cc = 0; cc < 2; ++cc) {
+                        if (c + cc >= nch) break;
+                        const float* cnc = cn + col0 + 32 * (c + cc);
+                        uint32_t me = 0, mo = 0;
+#pragma unroll
+                        for (int jj = 0; jj < 32; jj += 4) {
+                            const float4 cq = *reinterpret_cast<const float4*>(cnc + jj);
+                            const float2 s0 = f2_fma(make_float2(__uint_as_float(v[cc][jj]), __uint_as_float(v[cc][jj + 1])),
+                                                     make_float2(-2.0f, -2.0f), make_float2(cq.x, cq.y));
+                            const float2 s1 = f2_fma(make_float2(__uint_as_float(v[cc][jj + 2]), __uint_as_float(v[cc][jj + 3])),
+                                                     make_float2(-2.0f, -2.0f), make_float2(cq.z, cq.w));
+                            if (s0.x <= thr) me |= 1u << jj;
+                            if (s0.y <= thr) mo |= 2u << jj;
+                            if (s1.x <= thr) me |= 4u << jj;
+                            if (s1.y <= thr) mo |= 8u << jj;
+                        }
+                        const uint32_t m = me | mo;
+                        maskw[row * (Cpad / 32) + half * nch + c + cc] = m;
+                        if (m && first < 0) first = col0 + 32 * (c + cc) + __ffs(m) - 1;
+                        cnt += __popc(m);
                     }
-                    maskw[row * (Cpad / 32) + half * nch + c] = m;
-                    if (m && first < 0) first = col0 + 32 * c + __ffs(m) - 1;
-                    cnt += __popc(m);
                 }
             }
             // accumulator drained: hand it back to the MMA issuer
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar + 8 * acc);
-            rx[row].cnt[half] = cnt;
-            rx[row].idx[half] = first;
+            rx.cnt[half][row] = cnt;
+            rx.idx[half][row] = first;
             epi_sync();
             const int64_t tok = (int64_t)(t_begin + i) * kTile + row;
             if (half == 0 && tok < a.n_tokens) {
-                const int c0 = rx[row].cnt[0], c1 = rx[row].cnt[1];
+                const int c0 = rx.cnt[0][row], c1 = rx.cnt[1][row];
                 if (c0 + c1 == 1) {
-                    a.ids[(int64_t)h * a.cap + a.tok_offset + tok] = (uint8_t)(c0 ? rx[row].idx[0] : rx[row].idx[1]);
+                    a.ids[(int64_t)h * a.cap + a.tok_offset + tok] = (uint8_t)(c0 ? rx.idx[0][row] : rx.idx[1][row]);
                 } else {
                     flag_rows[atomicAdd(nflag, 1)] = row;
                 }
@@ -512,62 +558,78 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int f = e; f < nf; f += kEpiWarps) {
                 const int r = flag_rows[f];
                 const uint32_t* mw = maskw + r * (Cpad / 32);
-                float dmin = INFINITY;
-                for (int w = 0; w < Cpad / 32; ++w)
-                    for (uint32_t m = mw[w]; m; m &= m - 1) {
-                        const int j = 32 * w + __ffs(m) - 1;
-                        dmin = fminf(dmin, warp_dist<D>(xs, r, Bs, j, cslab, lane));
-                    }
-                const float emin = kDirectRel * dmin + kDirectAbs;
-                int nsurv = 0, best = -1;
-                double cbest = INFINITY;
+                // direct fp32 distances of every candidate; lane k keeps candidate k
+                float dmin = INFINITY, myd = INFINITY;
+                int ncand = 0, myj = -1;
                 for (int w = 0; w < Cpad / 32; ++w)
                     for (uint32_t m = mw[w]; m; m &= m - 1) {
                         const int j = 32 * w + __ffs(m) - 1;
                         const float d = warp_dist<D>(xs, r, Bs, j, cslab, lane);
-                        if (d - (kDirectRel * d + kDirectAbs) <= dmin + emin) {
-                            ++nsurv;
-                            if (best < 0) best = j;
+                        if (lane == (ncand & 31)) { myd = d; myj = j; }
+                        ++ncand;
+                        dmin = fminf(dmin, d);
+                    }
+                const float emin = kDirectRel * dmin + kDirectAbs;
+                // survivors: candidates whose distance may still be the smallest
+                unsigned sb = 0xffffffffu;
+                int best = -1;
+                if (ncand <= 32) {
+                    sb = __ballot_sync(0xffffffffu, myj >= 0 && myd - (kDirectRel * myd + kDirectAbs) <= dmin + emin);
+                    if (__popc(sb) == 1) best = __shfl_sync(0xffffffffu, myj, __ffs(sb) - 1);
+                }
+                auto surv_j = [&](int k) { return __shfl_sync(0xffffffffu, myj, k); };
+                if (best < 0) {
+                    // several survivors: exact squared distances decide (ties ->
+                    // lowest j).  Candidates within 2^-40 of the best -- or any
+                    // value outside the exact range -- are settled by the
+                    // channel-order fp64 sum of the plain definition.
+                    // Survivor list: lanes of sb, or (more than 32 candidates)
+                    // every candidate, re-filtered.
+                    const bool listed = ncand <= 32;
+                    int nlist = listed ? 32 : Cpad;
+                    i128 dbest = 0;
+                    bool exact = true, near = false;
+                    for (int k = 0; k < nlist && exact; ++k) {
+                        int j;
+                        if (listed) {
+                            if (!((sb >> k) & 1u)) continue;
+                            j = surv_j(k);
+                        } else {
+                            j = k;
+                            if (!((mw[j >> 5] >> (j & 31)) & 1u)) continue;
+                            const float d = warp_dist<D>(xs, r, Bs, j, cslab, lane);
+                            if (d - (kDirectRel * d + kDirectAbs) > dmin + emin) continue;
+                        }
+                        bool ok;
+                        const i128 de = warp_dist_exact<D>(xs, r, Bs, j, cslab, lane, ok);
+                        if (!ok) { exact = false; break; }
+                        if (best < 0 || de < dbest) {
+                            if (best >= 0 && dbest - de <= (dbest >> 40)) near = true;
+                            dbest = de;
+                            best = j;
+                        } else if (de - dbest <= (de >> 40)) {
+                            near = true;
                         }
                     }
-                if (nsurv > 1) {
-                    // several survivors: fp64 distances decide; candidates within
-                    // 2^-42 of the best are settled by the channel-order fp64 sum
-                    // of the plain definition (ties -> lowest j)
-                    best = -1;
-                    double dbest = INFINITY;
-                    for (int w = 0; w < Cpad / 32; ++w)
-                        for (uint32_t m = mw[w]; m; m &= m - 1) {
-                            const int j = 32 * w + __ffs(m) - 1;
-                            const float d = warp_dist<D>(xs, r, Bs, j, cslab, lane);
-                            if (d - (kDirectRel * d + kDirectAbs) > dmin + emin) continue;
-                            const double dp = warp_dist_f64<D>(xs, r, Bs, j, cslab, lane);
-                            if (dp < dbest) { dbest = dp; best = j; }
-                        }
-                    bool near = false;
-                    for (int w = 0; w < Cpad / 32 && !near; ++w)
-                        for (uint32_t m = mw[w]; m; m &= m - 1) {
-                            const int j = 32 * w + __ffs(m) - 1;
-                            if (j == best) continue;
-                            const float d = warp_dist<D>(xs, r, Bs, j, cslab, lane);
-                            if (d - (kDirectRel * d + kDirectAbs) > dmin + emin) continue;
-                            const double dp = warp_dist_f64<D>(xs, r, Bs, j, cslab, lane);
-                            if (dp - dbest <= 0x1p-42 * fmax(dp, dbest) + 1e-300) { near = true; break; }
-                        }
-                    if (near) {
+                    if (!exact || near) {
                         best = -1;
-                        for (int w = 0; w < Cpad / 32; ++w)
-                            for (uint32_t m = mw[w]; m; m &= m - 1) {
-                                const int j = 32 * w + __ffs(m) - 1;
+                        double cbest = INFINITY;
+                        for (int k = 0; k < nlist; ++k) {
+                            int j;
+                            if (listed) {
+                                if (!((sb >> k) & 1u)) continue;
+                                j = surv_j(k);
+                            } else {
+                                j = k;
+                                if (!((mw[j >> 5] >> (j & 31)) & 1u)) continue;
                                 const float d = warp_dist<D>(xs, r, Bs, j, cslab, lane);
                                 if (d - (kDirectRel * d + kDirectAbs) > dmin + emin) continue;
-                                const double dp = warp_dist_f64<D>(xs, r, Bs, j, cslab, lane);
-                                if (dp - dbest > 0x1p-42 * fmax(dp, dbest) + 1e-300) continue;
-                                double cd = 0.0;
-                                if (lane == 0) cd = canonical_dist_smem<D>(xs, r, Bs, j, cslab);
-                                cd = __shfl_sync(0xffffffffu, cd, 0);
-                                if (cd < cbest) { cbest = cd; best = j; }
                             }
+                            double cd = 0.0;
+                            if (lane == 0) cd = canonical_dist_smem<D>(xs, r, Bs, j, cslab);
+                            cd = __shfl_sync(0xffffffffu, cd, 0);
+                            if (cd < cbest) { cbest = cd; best = j; }
+                        }
                         ++n_seq;
                     }
                     ++n_fp64;

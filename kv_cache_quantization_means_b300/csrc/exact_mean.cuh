@@ -19,6 +19,8 @@
 
 #include <cstdint>
 
+#include "common.cuh"
+
 namespace qvg {
 
 constexpr float kWin1 = 49152.0f;                // 1.5 * 2^15 -> unit 2^-8
@@ -40,6 +42,22 @@ __device__ __forceinline__ void window_add(float x, int& a1, int& a2, int& a3) {
     const float r2 = __fsub_rn(r1, __fsub_rn(v2, kWin2));
     const float v3 = __fadd_rn(r2, kWin3);
     a3 += (int)(__float_as_uint(v3) - __float_as_uint(kWin3));
+}
+
+// The same for two values at once (packed fp32 pairs).
+__device__ __forceinline__ void window_add2(float2 x, int* a1, int* a2, int* a3) {
+    const float2 W1 = make_float2(kWin1, kWin1), W2 = make_float2(kWin2, kWin2), W3 = make_float2(kWin3, kWin3);
+    const float2 v1 = f2_add(x, W1);
+    a1[0] += (int)(__float_as_uint(v1.x) - __float_as_uint(kWin1));
+    a1[1] += (int)(__float_as_uint(v1.y) - __float_as_uint(kWin1));
+    const float2 r1 = f2_sub(x, f2_sub(v1, W1));
+    const float2 v2 = f2_add(r1, W2);
+    a2[0] += (int)(__float_as_uint(v2.x) - __float_as_uint(kWin2));
+    a2[1] += (int)(__float_as_uint(v2.y) - __float_as_uint(kWin2));
+    const float2 r2 = f2_sub(r1, f2_sub(v2, W2));
+    const float2 v3 = f2_add(r2, W3);
+    a3[0] += (int)(__float_as_uint(v3.x) - __float_as_uint(kWin3));
+    a3[1] += (int)(__float_as_uint(v3.y) - __float_as_uint(kWin3));
 }
 
 __device__ __forceinline__ i128 windows_to_i128(int a1, int a2, int a3) {

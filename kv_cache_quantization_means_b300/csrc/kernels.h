@@ -44,6 +44,7 @@ struct AssignArgs {
 };
 
 constexpr int kPieceTokens = 64;   // tokens per exact partial sum of the update
+constexpr int kSortBlock = 2048;   // tokens per block of the update's counting sort
 
 struct UpdateArgs {
     const uint16_t* x;
@@ -52,6 +53,8 @@ struct UpdateArgs {
     int64_t cap, tok_offset;
     int H, C;
     int max_pieces;         // per head: ceil(n_tokens / kPieceTokens) + C
+    int n_blocks;           // per head: ceil(n_tokens / kSortBlock) sort blocks
+    int* blockhist;         // [H][n_blocks][C] ids per cluster and sort block
     int* counts;            // [H][C] tokens per cluster
     int* first_piece;       // [H][C] index of the cluster's first piece
     int* npieces;           // [H]

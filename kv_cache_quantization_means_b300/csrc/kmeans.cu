@@ -357,11 +357,12 @@ __global__ void kmeans_init_kernel(const uint16_t* x, int64_t head_stride, int64
 
 // ------------------------------------------------------------- update ---
 //
-// 1. sort: one CTA per head builds a stable counting sort of its tokens by
-//    cluster (perm), the cluster sizes and a table of pieces: runs of at most
-//    kPieceTokens sorted positions of one cluster.  Each warp histograms a
-//    contiguous token range with __match_any_sync (one writer per distinct
-//    id), so neither the counts nor the order depend on scheduling.
+// 1. sort: per block of kSortBlock tokens a histogram of ids, then a stable
+//    counting sort of the tokens by cluster (perm), the cluster sizes and a
+//    table of pieces: runs of at most kPieceTokens sorted positions of one
+//    cluster.  Offsets come from the block histograms in a fixed order and
+//    ranks from __match_any_sync, so neither the counts nor the order depend
+//    on scheduling.
 // 2. sum: one warp per piece gathers its rows and forms their exact sum
 //    (fixed-point windows); the only piece of a cluster is turned into the
 //    centroid directly, other pieces store their exact partial.
@@ -369,108 +370,113 @@ __global__ void kmeans_init_kernel(const uint16_t* x, int64_t head_stride, int64
 //    and round the mean.  Integer sums make the result independent of any
 //    order; no atomic operation is used.
 
-constexpr int kSortThreads = 1024;
-constexpr int kSortWarps = kSortThreads / 32;
+constexpr int kSortWarps = kThreads / 32;
+constexpr int kSortPerWarp = kSortBlock / kSortWarps;
 
-constexpr int kSortStage = 8192;    // ids staged in shared memory per round
+// Exclusive scan of v over threads 0..kMaxClusters-1 of a 256-thread block;
+// returns the prefix, *total receives the sum.
+__device__ __forceinline__ int block_scan256(int v, int* warp_tot, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += u;
+    }
+    if (lane == 31) warp_tot[warp] = inc;
+    __syncthreads();
+    int before = 0, all = 0;
+    for (int w = 0; w < kThreads / 32; ++w) {
+        if (w < warp) before += warp_tot[w];
+        all += warp_tot[w];
+    }
+    __syncthreads();
+    *total = all;
+    return before + inc - v;
+}
 
-__global__ void __launch_bounds__(kSortThreads) kmeans_sort_kernel(UpdateArgs a) {
-    __shared__ int hist[kSortWarps][kMaxClusters];
-    __shared__ __align__(16) uint8_t ids_s[kSortStage];
-    __shared__ int cnt_s[kMaxClusters];
-    __shared__ int off_s[kMaxClusters];
-    __shared__ int pfirst_s[kMaxClusters + 1];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int h = blockIdx.x, C = a.C;
-    const int64_t N = a.n_tokens;
+// Histogram of the ids of one block of kSortBlock tokens.
+__global__ void __launch_bounds__(kThreads) kmeans_hist_kernel(UpdateArgs a) {
+    __shared__ int hist[kMaxClusters];
+    const int h = blockIdx.y, b = blockIdx.x, C = a.C;
+    for (int j = threadIdx.x; j < kMaxClusters; j += kThreads) hist[j] = 0;
+    __syncthreads();
     const uint8_t* idh = a.ids + (int64_t)h * a.cap + a.tok_offset;
-    for (int i = tid; i < kSortWarps * kMaxClusters; i += kSortThreads) (&hist[0][0])[i] = 0;
+    const int64_t n0 = (int64_t)b * kSortBlock, n1 = min(n0 + kSortBlock, a.n_tokens);
+    for (int64_t n = n0 + threadIdx.x; n < n1; n += kThreads) atomicAdd(&hist[min((int)idh[n], C - 1)], 1);
     __syncthreads();
-    // Tokens are taken in rounds of kSortStage staged in shared memory; within
-    // a round warp w owns a contiguous slice.  A cluster's positions follow
-    // (warp, round, token) order: fixed, whatever the scheduling.
-    for (int64_t r0 = 0; r0 < N; r0 += kSortStage) {
-        const int rn = (int)min((int64_t)kSortStage, N - r0);
-        for (int i = tid; i < rn; i += kSortThreads) ids_s[i] = idh[r0 + i];
-        __syncthreads();
-        const int w0 = warp * rn / kSortWarps, w1 = (warp + 1) * rn / kSortWarps;
-        for (int b = w0; b < w1; b += 32) {
-            const int n = b + lane;
-            const int id = n < w1 ? min((int)ids_s[n], C - 1) : -1;
-            const unsigned m = __match_any_sync(0xffffffffu, id);
-            if (id >= 0 && lane == __ffs(m) - 1) hist[warp][id] += __popc(m);
+    int* bh = a.blockhist + ((int64_t)h * a.n_blocks + b) * C;
+    for (int j = threadIdx.x; j < C; j += kThreads) bh[j] = hist[j];
+}
+
+// Stable counting sort, one block of kSortBlock tokens per CTA: the block's
+// first position for cluster j is (tokens of clusters < j) + (tokens of j in
+// earlier blocks), both from the block histograms in a fixed order; inside the
+// block, warp w's slice follows warps < w and a warp ranks equal ids with
+// __match_any_sync.  Block 0 of each head also writes the counts and the
+// table of pieces.
+__global__ void __launch_bounds__(kThreads) kmeans_scatter_kernel(UpdateArgs a) {
+    __shared__ int cur[kSortWarps][kMaxClusters];
+    __shared__ int warp_tot[kThreads / 32];
+    __shared__ __align__(16) uint8_t ids_s[kSortBlock];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int h = blockIdx.y, b = blockIdx.x, C = a.C;
+    const uint8_t* idh = a.ids + (int64_t)h * a.cap + a.tok_offset;
+    const int64_t n0 = (int64_t)b * kSortBlock;
+    const int nb = (int)min((int64_t)kSortBlock, a.n_tokens - n0);
+    for (int i = tid; i < nb; i += kThreads) ids_s[i] = idh[n0 + i];
+    for (int i = tid; i < kSortWarps * kMaxClusters; i += kThreads) (&cur[0][0])[i] = 0;
+    // totals and the part before this block, per cluster (thread j)
+    const int* bh = a.blockhist + (int64_t)h * a.n_blocks * C;
+    int total = 0, before = 0;
+    if (tid < C)
+        for (int bb = 0; bb < a.n_blocks; ++bb) {
+            const int v = bh[(int64_t)bb * C + tid];
+            total += v;
+            if (bb < b) before += v;
         }
-        __syncthreads();
+    int all;
+    const int off = block_scan256(tid < C ? total : 0, warp_tot, &all);   // also syncs ids_s / cur
+    const int np = (total + kPieceTokens - 1) / kPieceTokens;
+    int np_all;
+    const int pfirst = block_scan256(tid < C ? np : 0, warp_tot, &np_all);
+    if (b == 0 && tid < C) {
+        a.counts[(int64_t)h * C + tid] = total;
+        a.first_piece[(int64_t)h * C + tid] = pfirst;
+        int4* ph = a.pieces + (int64_t)h * a.max_pieces;
+        for (int p = 0; p < np; ++p)
+            ph[pfirst + p] = make_int4(off + p * kPieceTokens, min(kPieceTokens, total - p * kPieceTokens), tid,
+                                       np == 1 ? 1 : 0);
     }
-    for (int j = tid; j < C; j += kSortThreads) {
-        int tot = 0;
-        for (int w = 0; w < kSortWarps; ++w) tot += hist[w][j];
-        cnt_s[j] = tot;
-        a.counts[(int64_t)h * C + j] = tot;
+    if (b == 0 && tid == 0) a.npieces[h] = np_all;
+    // per-warp histograms of this block
+    const int w0 = warp * kSortPerWarp, w1 = min(w0 + kSortPerWarp, nb);
+    for (int bs = w0; bs < w1; bs += 32) {
+        const int n = bs + lane;
+        const int id = n < w1 ? min((int)ids_s[n], C - 1) : -1;
+        const unsigned m = __match_any_sync(0xffffffffu, id);
+        if (id >= 0 && lane == __ffs(m) - 1) cur[warp][id] += __popc(m);
     }
     __syncthreads();
-    if (warp == 0) {
-        // exclusive scans of the counts and of the piece counts, 8 clusters per lane
-        constexpr int kPer = kMaxClusters / 32;
-        int c[kPer], pc[kPer], sc = 0, sp = 0;
-#pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-            const int j = lane * kPer + k;
-            c[k] = j < C ? cnt_s[j] : 0;
-            pc[k] = (c[k] + kPieceTokens - 1) / kPieceTokens;
-            sc += c[k];
-            sp += pc[k];
-        }
-        int ic = sc, ip = sp;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int uc = __shfl_up_sync(0xffffffffu, ic, o), up = __shfl_up_sync(0xffffffffu, ip, o);
-            if (lane >= o) { ic += uc; ip += up; }
-        }
-        int rc = ic - sc, rp = ip - sp;
-#pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-            const int j = lane * kPer + k;
-            if (j < C) { off_s[j] = rc; pfirst_s[j] = rp; }
-            rc += c[k];
-            rp += pc[k];
-        }
-        if (lane == 31) pfirst_s[C] = rp;
-    }
-    __syncthreads();
-    int4* ph = a.pieces + (int64_t)h * a.max_pieces;
-    for (int j = tid; j < C; j += kSortThreads) {
-        int run = off_s[j];
+    if (tid < C) {
+        int run = off + before;
         for (int w = 0; w < kSortWarps; ++w) {
-            const int t = hist[w][j];
-            hist[w][j] = run;
+            const int t = cur[w][tid];
+            cur[w][tid] = run;
             run += t;
         }
-        const int cnt = cnt_s[j], np = (cnt + kPieceTokens - 1) / kPieceTokens;
-        for (int p = 0; p < np; ++p)
-            ph[pfirst_s[j] + p] = make_int4(off_s[j] + p * kPieceTokens, min(kPieceTokens, cnt - p * kPieceTokens), j,
-                                            np == 1 ? 1 : 0);
-        a.first_piece[(int64_t)h * C + j] = pfirst_s[j];
     }
-    if (tid == 0) a.npieces[h] = pfirst_s[C];
     __syncthreads();
-    int* perm = a.perm + (int64_t)h * N;
+    int* perm = a.perm + (int64_t)h * a.n_tokens;
     const unsigned lt = (1u << lane) - 1u;
-    for (int64_t r0 = 0; r0 < N; r0 += kSortStage) {
-        const int rn = (int)min((int64_t)kSortStage, N - r0);
-        for (int i = tid; i < rn; i += kSortThreads) ids_s[i] = idh[r0 + i];
-        __syncthreads();
-        const int w0 = warp * rn / kSortWarps, w1 = (warp + 1) * rn / kSortWarps;
-        for (int b = w0; b < w1; b += 32) {
-            const int n = b + lane;
-            const int id = n < w1 ? min((int)ids_s[n], C - 1) : -1;
-            const unsigned m = __match_any_sync(0xffffffffu, id);
-            if (id >= 0) perm[hist[warp][id] + __popc(m & lt)] = (int)(r0 + n);
-            __syncwarp();
-            if (id >= 0 && lane == __ffs(m) - 1) hist[warp][id] += __popc(m);
-            __syncwarp();
-        }
-        __syncthreads();
+    for (int bs = w0; bs < w1; bs += 32) {
+        const int n = bs + lane;
+        const int id = n < w1 ? min((int)ids_s[n], C - 1) : -1;
+        const unsigned m = __match_any_sync(0xffffffffu, id);
+        if (id >= 0) perm[cur[warp][id] + __popc(m & lt)] = (int)(n0 + n);
+        __syncwarp();
+        if (id >= 0 && lane == __ffs(m) - 1) cur[warp][id] += __popc(m);
+        __syncwarp();
     }
 }
 
@@ -484,10 +490,10 @@ __device__ __forceinline__ i128 shfl_xor_i128(i128 v, int mask) {
 // D/8 lanes cover a row, so each 16-byte load instruction of the warp fetches
 // 32/(D/8) rows, and kSumBatch of them are in flight before any arithmetic.
 // Row slots are reduced at the end (integer additions: exact, any order).
-constexpr int kSumBatch = 8;
+constexpr int kSumBatch = 4;
 
 template <int D>
-__global__ void __launch_bounds__(kThreads) kmeans_sum_kernel(UpdateArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) kmeans_sum_kernel(UpdateArgs a) {
     constexpr int LPR = D / 8, RPI = 32 / LPR;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int sub = lane % LPR, slot = lane / LPR;
@@ -520,8 +526,7 @@ __global__ void __launch_bounds__(kThreads) kmeans_sum_kernel(UpdateArgs a) {
                 for (int q = 0; q < 4; ++q) {
                     const float lo = bf16_lo(wv[q]), hi = bf16_hi(wv[q]);
                     amax = fmax3(amax, fabsf(lo), fabsf(hi));
-                    window_add(lo, w1[2 * q], w2[2 * q], w3[2 * q]);
-                    window_add(hi, w1[2 * q + 1], w2[2 * q + 1], w3[2 * q + 1]);
+                    window_add2(make_float2(lo, hi), w1 + 2 * q, w2 + 2 * q, w3 + 2 * q);
                 }
             }
         }
@@ -608,7 +613,9 @@ cudaError_t assign_d(int H, const AssignArgs& a, cudaStream_t s) {
 template <int D>
 cudaError_t update_d(const UpdateArgs& a, cudaStream_t s) {
     if (a.n_tokens == 0) return cudaSuccess;
-    kmeans_sort_kernel<<<(unsigned)a.H, kSortThreads, 0, s>>>(a);
+    dim3 g1((unsigned)a.n_blocks, (unsigned)a.H);
+    kmeans_hist_kernel<<<g1, kThreads, 0, s>>>(a);
+    kmeans_scatter_kernel<<<g1, kThreads, 0, s>>>(a);
     dim3 g2((unsigned)((a.max_pieces + kThreads / 32 - 1) / (kThreads / 32)), (unsigned)a.H);
     kmeans_sum_kernel<D><<<g2, kThreads, 0, s>>>(a);
     kmeans_mean_kernel<D><<<dim3((unsigned)a.C, (unsigned)a.H), D, 0, s>>>(a);
