@@ -219,6 +219,28 @@ QVG_API qvg_status coral_predict_encode(const qvg_config* cfg, const coral_predi
                                 uint32_t* codes, uint32_t* meta, qvg_bf16* xhat_next, float* pred_out,
                                 void* workspace, size_t workspace_bytes, qvg_stream stream);
 
+/* Allocation-free variant of coral_predict_encode.  The paper has no
+ * counterpart to this call: it is an interface convenience for callers that
+ * cannot allocate device memory or pass a workspace -- a runtime whose
+ * allocator owns all device memory, a plugin that must not grow the
+ * footprint, or code that cannot call cudaMalloc at the point of use.  Arguments and results are those
+ * of coral_predict_encode without the workspace: the low-rank scratch is a
+ * fixed 4 MiB device array inside this library (64 floats per token), which
+ * every GPU that loads the library keeps until the process exits.
+ *  - n_tokens must be <= 16384; larger returns QVG_ERR_CAPACITY, launching
+ *    nothing.  The call allocates and frees nothing.
+ *  - The first call on a device (with a previous layer) looks up the array's
+ *    device address on the current device; make that first call before any
+ *    stream capture.
+ *  - All calls share the one array: calls whose work can overlap on the GPU
+ *    (other streams, other host threads) race and must be serialised by the
+ *    caller.  The array needs no clearing: each call writes every value it
+ *    reads before reading it. */
+QVG_API qvg_status coral_predict_encode_static(const qvg_config* cfg, const coral_predictor* pred,
+                                       const qvg_bf16* xhat_prev, const qvg_bf16* x_next, int64_t n_tokens,
+                                       uint32_t* codes, uint32_t* meta, qvg_bf16* xhat_next, float* pred_out,
+                                       qvg_stream stream);
+
 /* Decoder twin of coral_predict_encode: rebuilds xhat_next from xhat_prev,
  * the predictor and the stored codes (bit-identical to the encoder's
  * xhat_next). */

@@ -3,6 +3,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -476,6 +477,79 @@ qvg_status coral_predict_decode(const qvg_config* cfg, const coral_predictor* pr
     a.xhat = xhat_next; a.pred_out = pred_out;
     a.lowrank = (float*)workspace;
     return cuda_status(qvg::launch_coral(cfg->head_dim, cfg->group_size, false, a, (cudaStream_t)stream),
+                       "coral launch");
+}
+
+// ------------------------------------------- allocation-free Coral encode
+//
+// Same computation as coral_predict_encode, for callers that cannot hand the
+// library a workspace: the low-rank projection t = xhat_prev W ([n_tokens]
+// x [rank] floats, the only scratch this call needs) lives in a file-scope
+// device array of fixed size that every GPU loading the library keeps until
+// the process exits.  Its device address is looked up once per device.
+
+}  // extern "C"
+
+namespace {
+
+constexpr size_t kStaticScratchFloats = (size_t)1 << 20;          // 4 MiB
+constexpr int64_t kStaticMaxTokens = (int64_t)(kStaticScratchFloats / 64);   // 64 floats per token (rank <= 64)
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) float g_coral_scratch[kStaticScratchFloats];
+
+std::mutex g_scratch_mu;
+float* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_coral_scratch on the current device (looked up with
+// that device current, once per device).
+qvg_status static_scratch(float** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(QVG_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_coral_scratch);
+        if (e != cudaSuccess) return cuda_status(e, "cudaGetSymbolAddress(scratch)");
+        g_scratch_ptr[dev] = static_cast<float*>(p);
+    }
+    *out = g_scratch_ptr[dev];
+    return QVG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+qvg_status coral_predict_encode_static(const qvg_config* cfg, const coral_predictor* pred,
+                                       const qvg_bf16* xhat_prev, const qvg_bf16* x_next, int64_t n_tokens,
+                                       uint32_t* codes, uint32_t* meta, qvg_bf16* xhat_next, float* pred_out,
+                                       qvg_stream stream) {
+    if (n_tokens > kStaticMaxTokens)
+        return fail(QVG_ERR_CAPACITY, "n_tokens %lld exceeds the %lld tokens the built-in scratch holds",
+                    (long long)n_tokens, (long long)kStaticMaxTokens);
+    float* scratch = nullptr;
+    qvg_status st = QVG_OK;
+    if (n_tokens > 0 && xhat_prev) {
+        if ((st = static_scratch(&scratch))) return st;
+    }
+    st = coral_common(cfg, pred, xhat_prev, n_tokens, scratch, kStaticScratchFloats * sizeof(float));
+    if (st) return st;
+    if (n_tokens == 0) return ok();
+    if (!x_next || !codes || !meta || !xhat_next) return fail(QVG_ERR_INVALID_ARG, "buffer is NULL");
+    if (!aligned16(x_next) || !aligned16(codes) || !aligned16(meta) || !aligned16(xhat_next) ||
+        !aligned16(pred_out))
+        return fail(QVG_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+    qvg::CoralArgs a{};
+    a.xprev = xhat_prev; a.xnext = x_next;
+    a.B = xhat_prev ? pred->B : nullptr; a.U = xhat_prev ? pred->U : nullptr; a.W = xhat_prev ? pred->W : nullptr;
+    a.R = xhat_prev ? pred->rank : 0;
+    a.n_tokens = n_tokens; a.H = cfg->num_heads; a.S = cfg->num_stages;
+    a.codes = codes; a.meta = meta; a.xhat = xhat_next; a.pred_out = pred_out;
+    a.lowrank = scratch;
+    return cuda_status(qvg::launch_coral(cfg->head_dim, cfg->group_size, true, a, (cudaStream_t)stream),
                        "coral launch");
 }
 

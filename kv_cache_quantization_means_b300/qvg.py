@@ -18,7 +18,7 @@ EXPORTS = [
     "qvg_last_error", "qvg_version", "qvg_encoded_bytes", "qvg_workspace_bytes", "qvg_fit_stats",
     "qvg_fit_centroids",
     "qvg_assign", "qvg_update", "qvg_encode", "qvg_decode", "qvg_append_chunk", "qvg_decode_cache",
-    "coral_predict_encode", "coral_predict_decode",
+    "coral_predict_encode", "coral_predict_decode", "coral_predict_encode_static",
 ]
 
 
@@ -75,6 +75,7 @@ def load(path=LIB_PATH):
     L.qvg_append_chunk.argtypes = [PCFG, ctypes.POINTER(qvg_cache), P, I64, I64, I64, I32, P, SZ, P]
     L.qvg_decode_cache.argtypes = [PCFG, ctypes.POINTER(qvg_cache), I64, I64, P, I64, I64, P]
     L.coral_predict_encode.argtypes = [PCFG, ctypes.POINTER(coral_predictor), P, P, I64, P, P, P, P, P, SZ, P]
+    L.coral_predict_encode_static.argtypes = [PCFG, ctypes.POINTER(coral_predictor), P, P, I64, P, P, P, P, P]
     L.coral_predict_decode.argtypes = [PCFG, ctypes.POINTER(coral_predictor), P, I64, P, P, P, P, P, SZ, P]
     for name in EXPORTS[2:]:
         getattr(L, name).restype = ctypes.c_int
@@ -184,6 +185,14 @@ def coral_predict_encode(cfg, pred, xhat_prev, x_next, n_tokens, codes, meta, xh
                                        _ptr(xhat_prev), _ptr(x_next), n_tokens, _ptr(codes), _ptr(meta),
                                        _ptr(xhat_next), _ptr(pred_out), _ptr(workspace), _nbytes(workspace),
                                        _stream(stream)))
+
+
+def coral_predict_encode_static(cfg, pred, xhat_prev, x_next, n_tokens, codes, meta, xhat_next, pred_out=None,
+                                stream=None):
+    """coral_predict_encode without a workspace (built-in fixed scratch)."""
+    _check(load().coral_predict_encode_static(ctypes.byref(cfg), ctypes.byref(pred) if pred is not None else None,
+                                              _ptr(xhat_prev), _ptr(x_next), n_tokens, _ptr(codes), _ptr(meta),
+                                              _ptr(xhat_next), _ptr(pred_out), _stream(stream)))
 
 
 def coral_predict_decode(cfg, pred, xhat_prev, n_tokens, codes, meta, xhat_next, pred_out=None, workspace=None,
