@@ -8,24 +8,30 @@
 //
 // One persistent CTA per SM works through a contiguous range of one head's
 // token tiles with warp-specialised roles:
-//   warp 0    TMA producer: token tiles (128 rows x 64 channels per copy,
-//             128-byte swizzle) into a 3-stage shared-memory ring;
-//   warp 1    MMA issuer: tcgen05.mma (M = 128, N = C rounded up to 64,
-//             K = 16 per instruction) into one of two TMEM accumulators;
-//             also owns the TMEM allocation;
-//   warps 2-9 epilogue: each reads half of the accumulator columns of its
-//             32-row TMEM lane quadrant (tcgen05.ld), in two passes:
-//               A. the minimum score of the row,
-//               B. the bitmask of centroids whose score is within 2E of it,
-//             E being a bound on the screen's error.  A row with one
-//             candidate is decided; the others are re-ranked over their
-//             candidates with direct fp32 distances (relative error bound)
-//             and, when those cannot separate, with the squared distance in
-//             fp64 summed in channel order, exactly as the plain definition.
-// Centroids (K-major, 128-byte swizzle) and their squared norms stay in
-// shared memory for the whole CTA.  Every wait on an mbarrier is bounded: on
-// expiry the kernel records an error code, lets the other roles drain and
-// returns after freeing its tensor memory.
+//   warp 0     TMA producer: token tiles (128 rows x 64 channels per copy,
+//              128-byte swizzle) into a ring of 2-3 shared-memory stages;
+//   warp 1     MMA issuer: tcgen05.mma (M = 128, N = C rounded up to 64,
+//              K = 16 per instruction) into one of two TMEM accumulators;
+//              also owns the TMEM allocation;
+//   warps 2-9  epilogue, two groups of four: group g takes the tiles that use
+//              accumulator g; a thread owns one tile row (its TMEM lane) and
+//              reads all of that row's columns (tcgen05.ld), so the groups and
+//              their warps never wait on one another.
+// The GEMM computes the score  <x, c_j> - ||c_j||^2 / 2  directly: one more
+// K = 16 block multiplies a constant ones column of the token side by
+// -||c_j||^2 / 2 split into three bf16 parts on the centroid side.  The
+// nearest centroid is the largest score.  The epilogue makes two passes:
+//   A. the row's largest score,
+//   B. the bitmask of centroids whose score is within 2E of it, E being a
+//      bound on the screen's error.
+// A row with one candidate is decided; the warp then re-ranks each of its
+// other rows over the row's candidates with direct fp32 distances (relative
+// error bound), then with exact squared distances in 128-bit integers, and
+// for near-exact ties with the squared distance in fp64 summed in channel
+// order, exactly as the plain definition.  Centroids (K-major, 128-byte
+// swizzle) stay in shared memory for the whole CTA.  Every wait is a bounded
+// wait on an mbarrier: on expiry the kernel records an error code, lets the
+// other roles drain and returns after freeing its tensor memory.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -37,8 +43,8 @@ namespace qvg {
 namespace {
 
 constexpr int kTile = 128;                 // tokens per tile = UMMA M
-constexpr int kStages = 3;                 // token tiles in flight
-constexpr int kEpiWarps = 8;
+constexpr int kMaxStages = 3;              // token tiles in flight (2 when shared memory is short)
+constexpr int kEpiWarps = 8;               // two groups of four
 constexpr int kTcThreads = 64 + 32 * kEpiWarps;
 constexpr int kAtomBytes = kTile * 128;    // one 64-channel slab of a tile
 constexpr uint32_t kErrTimeout = 0x7E000000u;
@@ -57,7 +63,7 @@ constexpr float kDirectAbs = 1e-35f;
 
 struct TcArgs {
     const uint16_t* cent;    // [H][C][D]
-    int C, Cpad;
+    int C, Cpad, stages;
     uint8_t* ids;            // [H][cap]
     int64_t cap, tok_offset, n_tokens;
     int tiles_per_head, ctas_per_head;
@@ -130,7 +136,6 @@ __device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory"); }
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
 // 128 bytes, 8-row groups 1024 bytes apart.
@@ -172,30 +177,22 @@ __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.
 
 // ----------------------------------------------------- shared memory map
 
-// Per tile row, exchanged between the two column halves (structure of
-// arrays: consecutive rows are consecutive words, no bank conflicts).
-struct RowX {
-    float bmin[2][kTile];
-    float xn[2][kTile];
-    int cnt[2][kTile];
-    int idx[2][kTile];
-};
-
 struct Layout {
-    uint32_t b_off, x_off, cn_off, row_off, mask_off, flag_off, bar_off, misc_off, total;
+    uint32_t b_off, bx_off, ax_off, x_off, bar_off, misc_off, total;
 };
 
-__host__ __device__ inline Layout make_layout(int D, int Cpad) {
+// Centroids (nA slabs of Cpad rows), the extra K block of the centroid side
+// (one slab of Cpad rows) and of the token side (one slab of 128 rows), the
+// token stages, then the barriers.
+__host__ __device__ inline Layout make_layout(int D, int Cpad, int stages) {
     Layout L;
     const int nA = D / 64;
     uint32_t o = 0;
     L.b_off = o;    o += (uint32_t)nA * Cpad * 128;
-    L.x_off = o;    o += (uint32_t)kStages * nA * kAtomBytes;
-    L.cn_off = o;   o += (uint32_t)Cpad * 4;
-    L.row_off = o;  o += (uint32_t)sizeof(RowX);
-    L.mask_off = o; o += (uint32_t)kTile * (Cpad / 32) * 4;
-    L.flag_off = o; o += (uint32_t)kTile * 4 + 16;
-    L.bar_off = o;  o += (uint32_t)(2 * kStages + 4) * 8;
+    L.bx_off = o;   o += (uint32_t)Cpad * 128;
+    L.ax_off = o;   o += (uint32_t)kAtomBytes;
+    L.x_off = o;    o += (uint32_t)stages * nA * kAtomBytes;
+    L.bar_off = o;  o += (uint32_t)(2 * kMaxStages + 4) * 8;
     L.misc_off = o; o += 32;
     L.total = o + 1024;            // slack for 1024-byte alignment of the base
     return L;
@@ -287,23 +284,26 @@ __device__ __forceinline__ i128 warp_dist_exact(const uint8_t* xs, int row, cons
     return acc;
 }
 
-template <int D>
+// bf16 bits of x, round to nearest even (x finite).
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+template <int D, int CP>
 __global__ void __launch_bounds__(kTcThreads, 1)
     kmeans_assign_tc_kernel(const __grid_constant__ CUtensorMap tmap, TcArgs a) {
     constexpr int nA = D / 64;
+    constexpr int Cpad = CP;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    const int Cpad = a.Cpad, C = a.C;
-    const Layout L = make_layout(D, Cpad);
-    uint8_t* Bs = base + L.b_off;
+    const int C = a.C, NS = a.stages;
+    const Layout L = make_layout(D, Cpad, NS);
+    uint8_t* Bs = base + L.b_off;     // centroids c_j
+    uint8_t* Bx = base + L.bx_off;    // -||c_j||^2 / 2 as three bf16 parts
+    uint8_t* Ax = base + L.ax_off;    // ones column block of the token side
     uint8_t* Xs = base + L.x_off;
-    float* cn = reinterpret_cast<float*>(base + L.cn_off);
-    RowX& rx = *reinterpret_cast<RowX*>(base + L.row_off);
-    uint32_t* maskw = reinterpret_cast<uint32_t*>(base + L.mask_off);
-    int* flag_rows = reinterpret_cast<int*>(base + L.flag_off);
-    int* nflag = flag_rows + kTile;
     const uint32_t bar0 = smem_u32(base + L.bar_off);
-    const uint32_t full_bar = bar0, empty_bar = bar0 + 8 * kStages, tfull_bar = bar0 + 16 * kStages,
+    const uint32_t full_bar = bar0, empty_bar = bar0 + 8 * kMaxStages, tfull_bar = bar0 + 16 * kMaxStages,
                    tempty_bar = tfull_bar + 16;
     // [0] tmem base, [1] abort (producer / MMA), [2] cmax2 bits, [3] abort (epilogue)
     uint32_t* misc = reinterpret_cast<uint32_t*>(base + L.misc_off);
@@ -320,18 +320,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     // ---- set-up: barriers, tensor memory, centroids and their norms
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(full_bar + 8 * s, 1);
-            mbar_init(empty_bar + 8 * s, kEpiWarps);
+        for (int st = 0; st < NS; ++st) {
+            mbar_init(full_bar + 8 * st, 1);
+            mbar_init(empty_bar + 8 * st, kEpiWarps / 2);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar + 8 * b, 1);
-            mbar_init(tempty_bar + 8 * b, kEpiWarps);
+            mbar_init(tempty_bar + 8 * b, kEpiWarps / 2);
         }
         misc[1] = 0;
         misc[2] = 0;
         misc[3] = 0;
-        *nflag = 0;
         fence_mbar_init();
     }
     __syncthreads();
@@ -361,22 +360,43 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (v < total) *reinterpret_cast<uint4*>(Bs + sw_off(v / (D / 8), (v % (D / 8)) * 8, cslab)) = val[u];
             }
         }
+        // the token side's extra block: 1 in channels 0..2, 0 elsewhere
+        for (int v = tid; v < kTile * 8; v += kTcThreads) {
+            const int r = v >> 3, k = v & 7;
+            uint4 w = make_uint4(0, 0, 0, 0);
+            if (k == 0) { w.x = 0x3F803F80u; w.y = 0x00003F80u; }
+            *reinterpret_cast<uint4*>(Ax + sw_off(r, k * 8, kAtomBytes)) = w;
+        }
     }
     __syncthreads();
-    // squared norms from shared memory, one warp per centroid
+    // -||c_j||^2 / 2 into the centroid side's extra block, one warp per centroid
     for (int j = warp; j < Cpad; j += kTcThreads / 32) {
-        float s = 0.0f;
+        float sq = 0.0f;
         for (int i = lane * 2; i < D; i += 64) {
             const uint32_t w = *reinterpret_cast<const uint32_t*>(Bs + sw_off(j, i, cslab));
             const float c0 = bf16_lo(w), c1 = bf16_hi(w);
-            s = __fmaf_rn(c0, c0, s);
-            s = __fmaf_rn(c1, c1, s);
+            sq = __fmaf_rn(c0, c0, sq);
+            sq = __fmaf_rn(c1, c1, sq);
         }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (lane == 0) {
-            cn[j] = j < C ? s : INFINITY;
-            if (j < C) atomicMax(misc + 2, __float_as_uint(s));
+        for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        if (lane < 8) {
+            uint4 w = make_uint4(0, 0, 0, 0);
+            if (lane == 0) {
+                if (j < C) {
+                    const float v = -0.5f * sq;              // exact scaling
+                    const uint16_t hi = f32_to_bf16_bits(v);
+                    const float r1 = __fsub_rn(v, bf16f(hi));
+                    const uint16_t mid = f32_to_bf16_bits(r1);
+                    const uint16_t lo = f32_to_bf16_bits(__fsub_rn(r1, bf16f(mid)));
+                    w.x = (uint32_t)hi | ((uint32_t)mid << 16);
+                    w.y = lo;
+                } else {
+                    w.x = 0xFB80u;                           // -2^120: never the largest score
+                }
+            }
+            *reinterpret_cast<uint4*>(Bx + sw_off(j, lane * 8, cslab)) = w;
+            if (lane == 0 && j < C) atomicMax(misc + 2, __float_as_uint(sq));
         }
     }
     fence_async_smem();
@@ -392,22 +412,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
             int armed = 0;
             for (int i = 0; i < n_tiles; ++i) {
-                const int s = i % kStages;
-                const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-                if (!mbar_wait(empty_bar + 8 * s, ph ^ 1u)) { atomicExch(misc + 1, 1u); break; }
+                const int st = i % NS;
+                const uint32_t ph = (uint32_t)(i / NS) & 1u;
+                if (!mbar_wait(empty_bar + 8 * st, ph ^ 1u)) { atomicExch(misc + 1, 1u); break; }
                 if (*(volatile uint32_t*)(misc + 1)) break;
-                mbar_arrive_tx(full_bar + 8 * s, (uint32_t)(nA * kAtomBytes));
+                mbar_arrive_tx(full_bar + 8 * st, (uint32_t)(nA * kAtomBytes));
                 const int tok0 = (t_begin + i) * kTile;
                 for (int at = 0; at < nA; ++at) {
-                    const uint32_t dst = smem_u32(Xs + (size_t)(s * nA + at) * kAtomBytes);
-                    if (a.head_inner) tma_load_3d(dst, &tmap, full_bar + 8 * s, at * 64, h, tok0);
-                    else tma_load_3d(dst, &tmap, full_bar + 8 * s, at * 64, tok0, h);
+                    const uint32_t dst = smem_u32(Xs + (size_t)(st * nA + at) * kAtomBytes);
+                    if (a.head_inner) tma_load_3d(dst, &tmap, full_bar + 8 * st, at * 64, h, tok0);
+                    else tma_load_3d(dst, &tmap, full_bar + 8 * st, at * 64, tok0, h);
                 }
                 armed = i + 1;
             }
             // drain: every copy this thread issued has landed before exit
-            for (int i = armed - kStages > 0 ? armed - kStages : 0; i < armed; ++i)
-                mbar_wait(full_bar + 8 * (i % kStages), (uint32_t)(i / kStages) & 1u);
+            for (int i = armed - NS > 0 ? armed - NS : 0; i < armed; ++i)
+                mbar_wait(full_bar + 8 * (i % NS), (uint32_t)(i / NS) & 1u);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -415,21 +435,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
             const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(Cpad >> 3) << 17) |
                                    ((uint32_t)(kTile >> 4) << 24);
+            const uint64_t dax = sw128_desc(smem_u32(Ax)), dbx = sw128_desc(smem_u32(Bx));
             int issued = 0;
             for (int i = 0; i < n_tiles; ++i) {
-                const int s = i % kStages, acc = i & 1;
-                const uint32_t ph = (uint32_t)(i / kStages) & 1u, aph = (uint32_t)(i >> 1) & 1u;
+                const int st = i % NS, acc = i & 1;
+                const uint32_t ph = (uint32_t)(i / NS) & 1u, aph = (uint32_t)(i >> 1) & 1u;
                 if (!mbar_wait(tempty_bar + 8 * acc, aph ^ 1u)) { atomicExch(misc + 1, 1u); break; }
-                if (!mbar_wait(full_bar + 8 * s, ph)) { atomicExch(misc + 1, 1u); break; }
+                if (!mbar_wait(full_bar + 8 * st, ph)) { atomicExch(misc + 1, 1u); break; }
                 if (*(volatile uint32_t*)(misc + 1)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + (uint32_t)acc * acc_cols;
+                umma_bf16(d_tmem, dax, dbx, idesc, 0u);      // -||c||^2 / 2 (overwrites)
                 for (int at = 0; at < nA; ++at)
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const uint64_t da = sw128_desc(smem_u32(Xs + (size_t)(s * nA + at) * kAtomBytes) + 32u * k);
+                        const uint64_t da = sw128_desc(smem_u32(Xs + (size_t)(st * nA + at) * kAtomBytes) + 32u * k);
                         const uint64_t db = sw128_desc(smem_u32(Bs + (size_t)at * cslab) + 32u * k);
-                        umma_bf16(d_tmem, da, db, idesc, (at | k) != 0 ? 1u : 0u);
+                        umma_bf16(d_tmem, da, db, idesc, 1u);
                     }
                 umma_commit(tfull_bar + 8 * acc);
                 issued = i + 1;
@@ -441,129 +463,117 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------ epilogue
-        const int e = warp - 2;
+        const int e = warp - 2;                 // 0..7
+        const int g = e >> 2;                   // group = accumulator it drains
         const int q = warp & 3;                 // TMEM lane quadrant of this warp
-        const int half = e >> 2;                // which half of the columns
         const int row = q * 32 + lane;          // tile row = TMEM lane
-        const int ncols = Cpad / 2, nch = ncols / 32;
-        const int col0 = half * ncols;
-        unsigned long long n_flag = 0, n_fp64 = 0, n_seq = 0;
-        for (int i = 0; i < n_tiles; ++i) {
-            const int s = i % kStages, acc = i & 1;
-            const uint32_t ph = (uint32_t)(i / kStages) & 1u, aph = (uint32_t)(i >> 1) & 1u;
-            // the abort flag is written only before and read only after the
-            // same barrier, so every epilogue warp takes the same branch
-            if (!mbar_wait(tfull_bar + 8 * acc, aph) || !mbar_wait(full_bar + 8 * s, ph)) atomicExch(misc + 3, 1u);
-            epi_sync();
-            if (*(volatile uint32_t*)(misc + 3)) break;
+        constexpr int NW = CP / 32;             // 32-column chunks = mask words
+        unsigned long long n_flag = 0, n_exact = 0, n_seq = 0;
+        for (int i = g; i < n_tiles; i += 2) {
+            const int st = i % NS;
+            const uint32_t ph = (uint32_t)(i / NS) & 1u, aph = (uint32_t)(i >> 1) & 1u;
+            if (!mbar_wait(tfull_bar + 8 * g, aph) || !mbar_wait(full_bar + 8 * st, ph)) {
+                atomicExch(misc + 3, 1u);
+                break;
+            }
             tc_fence_after();
-            const uint8_t* xs = Xs + (size_t)s * nA * kAtomBytes;
-            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * acc_cols + (uint32_t)col0;
-            // pass A: minimum score over this half (two 32-column chunks per
-            // TMEM wait, four independent running minima)
-            float bmin;
+            const uint8_t* xs = Xs + (size_t)st * nA * kAtomBytes;
+            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)g * acc_cols;
+            // ||x||^2 of this row (error bound of the screen)
+            float xnt;
+            {
+                float2 s2 = make_float2(0.0f, 0.0f), t2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+                for (int i8 = 0; i8 < D / 8; ++i8) {
+                    const uint4 w = *reinterpret_cast<const uint4*>(xs + sw_off(row, i8 * 8, kAtomBytes));
+                    const float2 f0 = make_float2(bf16_lo(w.x), bf16_hi(w.x)), f1 = make_float2(bf16_lo(w.y), bf16_hi(w.y));
+                    const float2 f2v = make_float2(bf16_lo(w.z), bf16_hi(w.z)), f3 = make_float2(bf16_lo(w.w), bf16_hi(w.w));
+                    s2 = f2_fma(f0, f0, s2);
+                    t2 = f2_fma(f1, f1, t2);
+                    s2 = f2_fma(f2v, f2v, s2);
+                    t2 = f2_fma(f3, f3, t2);
+                }
+                xnt = (s2.x + s2.y) + (t2.x + t2.y);
+            }
+            // pass A: the largest score of the row
+            float b1;
             {
                 uint32_t v[2][32];
-                float m4[4] = {INFINITY, INFINITY, INFINITY, INFINITY};
-                for (int c = 0; c < nch; c += 2) {
-                    tmem_ld32(taddr + 32u * c, v[0]);
-                    if (c + 1 < nch) tmem_ld32(taddr + 32u * (c + 1), v[1]);
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int c0 = 0; c0 < NW; c0 += 2) {
+                    tmem_ld32(taddr + 32u * c0, v[0]);
+                    if (c0 + 1 < NW) tmem_ld32(taddr + 32u * (c0 + 1), v[1]);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        if (c + cc >= nch) break;
-                        const float* cnc = cn + col0 + 32 * (c + cc);
+                    for (int c = 0; c < 2; ++c) {
+                        if (c0 + c < NW) {
 #pragma unroll
-                        for (int jj = 0; jj < 32; jj += 4) {
-                            const float4 cq = *reinterpret_cast<const float4*>(cnc + jj);
-                            const float2 s0 = f2_fma(make_float2(__uint_as_float(v[cc][jj]), __uint_as_float(v[cc][jj + 1])),
-                                                     make_float2(-2.0f, -2.0f), make_float2(cq.x, cq.y));
-                            const float2 s1 = f2_fma(make_float2(__uint_as_float(v[cc][jj + 2]), __uint_as_float(v[cc][jj + 3])),
-                                                     make_float2(-2.0f, -2.0f), make_float2(cq.z, cq.w));
-                            const int k = (jj >> 2) & 3;
-                            m4[k] = fmin3(m4[k], s0.x, s0.y);
-                            m4[k ^ 2] = fmin3(m4[k ^ 2], s1.x, s1.y);
+                            for (int jj = 0; jj < 32; jj += 8) {
+                                m4[0] = fmax3(m4[0], __uint_as_float(v[c][jj]), __uint_as_float(v[c][jj + 1]));
+                                m4[1] = fmax3(m4[1], __uint_as_float(v[c][jj + 2]), __uint_as_float(v[c][jj + 3]));
+                                m4[2] = fmax3(m4[2], __uint_as_float(v[c][jj + 4]), __uint_as_float(v[c][jj + 5]));
+                                m4[3] = fmax3(m4[3], __uint_as_float(v[c][jj + 6]), __uint_as_float(v[c][jj + 7]));
+                            }
                         }
                     }
                 }
-                bmin = fminf(fminf(m4[0], m4[1]), fminf(m4[2], m4[3]));
+                b1 = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
             }
-            // partial ||x||^2 of this row: half 0 takes the first D/2 channels
-            float xn = 0.0f;
-            for (int i8 = half * (D / 16); i8 < (half + 1) * (D / 16); ++i8) {
-                const uint4 w = *reinterpret_cast<const uint4*>(xs + sw_off(row, i8 * 8, kAtomBytes));
-                float f[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
-                              bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
-#pragma unroll
-                for (int k = 0; k < 8; ++k) xn = __fmaf_rn(f[k], f[k], xn);
-            }
-            rx.bmin[half][row] = bmin;
-            rx.xn[half][row] = xn;
-            epi_sync();
-            const float b1 = fminf(rx.bmin[0][row], rx.bmin[1][row]);
-            const float xnt = rx.xn[0][row] + rx.xn[1][row];
-            const float E = 1.01f * (kScreenXC * sqrtf(xnt) * cm + kScreenCC * cm2) + 1e-30f;
-            const float thr = b1 + 2.0f * E;
-            // pass B: candidates within 2E of the minimum
-            int cnt = 0, first = -1;
+            // bound on the error of a score (half the bound on ||c||^2 - 2<x, c>)
+            const float E = 0.5f * (1.01f * (kScreenXC * sqrtf(xnt) * cm + kScreenCC * cm2) + 1e-30f);
+            const float thr = b1 - 2.0f * E;
+            // pass B: candidates within 2E of the largest score
+            uint32_t mw[NW];
             {
                 uint32_t v[2][32];
-                for (int c = 0; c < nch; c += 2) {
-                    tmem_ld32(taddr + 32u * c, v[0]);
-                    if (c + 1 < nch) tmem_ld32(taddr + 32u * (c + 1), v[1]);
+#pragma unroll
+                for (int c0 = 0; c0 < NW; c0 += 2) {
+                    tmem_ld32(taddr + 32u * c0, v[0]);
+                    if (c0 + 1 < NW) tmem_ld32(taddr + 32u * (c0 + 1), v[1]);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        if (c + cc >= nch) break;
-                        const float* cnc = cn + col0 + 32 * (c + cc);
-                        uint32_t me = 0, mo = 0;
+                    for (int c = 0; c < 2; ++c) {
+                        if (c0 + c < NW) {
+                            uint32_t me = 0, mo = 0;
 #pragma unroll
-                        for (int jj = 0; jj < 32; jj += 4) {
-                            const float4 cq = *reinterpret_cast<const float4*>(cnc + jj);
-                            const float2 s0 = f2_fma(make_float2(__uint_as_float(v[cc][jj]), __uint_as_float(v[cc][jj + 1])),
-                                                     make_float2(-2.0f, -2.0f), make_float2(cq.x, cq.y));
-                            const float2 s1 = f2_fma(make_float2(__uint_as_float(v[cc][jj + 2]), __uint_as_float(v[cc][jj + 3])),
-                                                     make_float2(-2.0f, -2.0f), make_float2(cq.z, cq.w));
-                            if (s0.x <= thr) me |= 1u << jj;
-                            if (s0.y <= thr) mo |= 2u << jj;
-                            if (s1.x <= thr) me |= 4u << jj;
-                            if (s1.y <= thr) mo |= 8u << jj;
+                            for (int jj = 0; jj < 32; jj += 2) {
+                                if (__uint_as_float(v[c][jj]) >= thr) me |= 1u << jj;
+                                if (__uint_as_float(v[c][jj + 1]) >= thr) mo |= 2u << jj;
+                            }
+                            mw[c0 + c] = me | mo;
                         }
-                        const uint32_t m = me | mo;
-                        maskw[row * (Cpad / 32) + half * nch + c + cc] = m;
-                        if (m && first < 0) first = col0 + 32 * (c + cc) + __ffs(m) - 1;
-                        cnt += __popc(m);
                     }
                 }
             }
             // accumulator drained: hand it back to the MMA issuer
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar + 8 * acc);
-            rx.cnt[half][row] = cnt;
-            rx.idx[half][row] = first;
-            epi_sync();
-            const int64_t tok = (int64_t)(t_begin + i) * kTile + row;
-            if (half == 0 && tok < a.n_tokens) {
-                const int c0 = rx.cnt[0][row], c1 = rx.cnt[1][row];
-                if (c0 + c1 == 1) {
-                    a.ids[(int64_t)h * a.cap + a.tok_offset + tok] = (uint8_t)(c0 ? rx.idx[0][row] : rx.idx[1][row]);
-                } else {
-                    flag_rows[atomicAdd(nflag, 1)] = row;
-                }
+            if (lane == 0) mbar_arrive(tempty_bar + 8 * g);
+            int cnt = 0, first = -1;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                if (mw[w] && first < 0) first = 32 * w + __ffs(mw[w]) - 1;
+                cnt += __popc(mw[w]);
             }
-            epi_sync();
-            // refine undecided rows: one warp per row over its candidates
-            const int nf = *nflag;
-            for (int f = e; f < nf; f += kEpiWarps) {
-                const int r = flag_rows[f];
-                const uint32_t* mw = maskw + r * (Cpad / 32);
+            const int64_t tok = (int64_t)(t_begin + i) * kTile + row;
+            const bool valid = tok < a.n_tokens;
+            uint8_t* idrow = a.ids + (int64_t)h * a.cap + a.tok_offset;
+            if (valid && cnt == 1) idrow[tok] = (uint8_t)first;
+            // undecided rows of this warp, one at a time, all lanes on the row
+            for (unsigned und = __ballot_sync(0xffffffffu, valid && cnt != 1); und; und &= und - 1) {
+                const int src = __ffs(und) - 1;
+                const int r = q * 32 + src;
+                uint32_t m[NW];
+#pragma unroll
+                for (int w = 0; w < NW; ++w) m[w] = __shfl_sync(0xffffffffu, mw[w], src);
                 // direct fp32 distances of every candidate; lane k keeps candidate k
                 float dmin = INFINITY, myd = INFINITY;
                 int ncand = 0, myj = -1;
-                for (int w = 0; w < Cpad / 32; ++w)
-                    for (uint32_t m = mw[w]; m; m &= m - 1) {
-                        const int j = 32 * w + __ffs(m) - 1;
+#pragma unroll
+                for (int w = 0; w < NW; ++w)
+                    for (uint32_t mm = m[w]; mm; mm &= mm - 1) {
+                        const int j = 32 * w + __ffs(mm) - 1;
                         const float d = warp_dist<D>(xs, r, Bs, j, cslab, lane);
                         if (lane == (ncand & 31)) { myd = d; myj = j; }
                         ++ncand;
@@ -577,7 +587,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     sb = __ballot_sync(0xffffffffu, myj >= 0 && myd - (kDirectRel * myd + kDirectAbs) <= dmin + emin);
                     if (__popc(sb) == 1) best = __shfl_sync(0xffffffffu, myj, __ffs(sb) - 1);
                 }
-                auto surv_j = [&](int k) { return __shfl_sync(0xffffffffu, myj, k); };
                 if (best < 0) {
                     // several survivors: exact squared distances decide (ties ->
                     // lowest j).  Candidates within 2^-40 of the best -- or any
@@ -586,17 +595,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     // Survivor list: lanes of sb, or (more than 32 candidates)
                     // every candidate, re-filtered.
                     const bool listed = ncand <= 32;
-                    int nlist = listed ? 32 : Cpad;
+                    const int nlist = listed ? 32 : CP;
                     i128 dbest = 0;
                     bool exact = true, near = false;
                     for (int k = 0; k < nlist && exact; ++k) {
                         int j;
                         if (listed) {
                             if (!((sb >> k) & 1u)) continue;
-                            j = surv_j(k);
+                            j = __shfl_sync(0xffffffffu, myj, k);
                         } else {
                             j = k;
-                            if (!((mw[j >> 5] >> (j & 31)) & 1u)) continue;
+                            if (!((m[j >> 5] >> (j & 31)) & 1u)) continue;
                             const float d = warp_dist<D>(xs, r, Bs, j, cslab, lane);
                             if (d - (kDirectRel * d + kDirectAbs) > dmin + emin) continue;
                         }
@@ -618,10 +627,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             int j;
                             if (listed) {
                                 if (!((sb >> k) & 1u)) continue;
-                                j = surv_j(k);
+                                j = __shfl_sync(0xffffffffu, myj, k);
                             } else {
                                 j = k;
-                                if (!((mw[j >> 5] >> (j & 31)) & 1u)) continue;
+                                if (!((m[j >> 5] >> (j & 31)) & 1u)) continue;
                                 const float d = warp_dist<D>(xs, r, Bs, j, cslab, lane);
                                 if (d - (kDirectRel * d + kDirectAbs) > dmin + emin) continue;
                             }
@@ -632,22 +641,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         }
                         ++n_seq;
                     }
-                    ++n_fp64;
+                    ++n_exact;
                 }
-                const int64_t tk = (int64_t)(t_begin + i) * kTile + r;
-                if (lane == 0 && tk < a.n_tokens && best >= 0)
-                    a.ids[(int64_t)h * a.cap + a.tok_offset + tk] = (uint8_t)best;
+                if (lane == 0 && best >= 0) idrow[(int64_t)(t_begin + i) * kTile + r] = (uint8_t)best;
                 ++n_flag;
             }
-            epi_sync();
-            if (e == 0 && lane == 0) *nflag = 0;
-            // the token tile is no longer read
+            // the token tile is no longer read by this warp
             __syncwarp();
-            if (lane == 0) mbar_arrive(empty_bar + 8 * s);
+            if (lane == 0) mbar_arrive(empty_bar + 8 * st);
         }
-        if (a.stats && lane == 0 && (n_flag | n_fp64 | n_seq)) {
+        if (a.stats && lane == 0 && (n_flag | n_exact | n_seq)) {
             atomicAdd(a.stats, n_flag);
-            atomicAdd(a.stats + 1, n_fp64);
+            atomicAdd(a.stats + 1, n_exact);
             atomicAdd(a.stats + 2, n_seq);
         }
     }
@@ -740,13 +745,23 @@ cudaError_t assign_tc_d(int H, const AssignArgs& a, bool* launched, cudaStream_t
     t.ctas_per_head = ctas_per_head(H, t.tiles_per_head);
     t.stats = a.stats;
     t.err = a.err;
-    const Layout L = make_layout(D, t.Cpad);
+    // three token stages when they fit in shared memory, else two
+    t.stages = kMaxStages;
+    Layout L = make_layout(D, t.Cpad, t.stages);
+    if (L.total > 232448u) { t.stages = 2; L = make_layout(D, t.Cpad, t.stages); }
+    if (L.total > 232448u) return cudaSuccess;
     // at least 116 KB so that one CTA (and one TMEM allocation) lives per SM
     const size_t smem = L.total < 118784u ? 118784u : L.total;
-    cudaError_t e = cudaFuncSetAttribute(kmeans_assign_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    auto kern = kmeans_assign_tc_kernel<D, 256>;
+    switch (t.Cpad) {
+        case 64: kern = kmeans_assign_tc_kernel<D, 64>; break;
+        case 128: kern = kmeans_assign_tc_kernel<D, 128>; break;
+        case 192: kern = kmeans_assign_tc_kernel<D, 192>; break;
+        default: break;
+    }
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kmeans_assign_tc_kernel<D><<<(unsigned)(H * t.ctas_per_head), kTcThreads, smem, s>>>(map, t);
+    kern<<<(unsigned)(H * t.ctas_per_head), kTcThreads, smem, s>>>(map, t);
     e = cudaGetLastError();
     if (e == cudaSuccess) *launched = true;
     return e;

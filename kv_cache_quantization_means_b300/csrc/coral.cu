@@ -16,6 +16,7 @@
 //     bit for bit.
 #include "common.cuh"
 #include "kernels.h"
+#include "prq16.cuh"
 
 namespace qvg {
 
@@ -48,13 +49,6 @@ __device__ __forceinline__ void mma16816(float* d, const uint32_t* a, uint32_t b
         "{%8,%9}, {%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void unpack8(const uint4& v, float* f) {
-    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
-    f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
-    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
-    f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
 }
 
 // t[n][r] = sum_j xhat[n][j] W[j][r]; one CTA = 128 tokens x R, warps own 16 rows.
@@ -116,7 +110,6 @@ template <int D, int G, bool ENCODE>
 __global__ void __launch_bounds__(kThreads, 2) coral_predict_kernel(CoralArgs a) {
     constexpr int LDX = D + 8;           // bf16 rows
     constexpr int LDP = D + 4;           // fp32 prediction rows
-    constexpr int LPR = D / 8, RPS = 32 / LPR, LPG = G / 8;
     extern __shared__ __align__(16) unsigned char smem[];
     const int R = a.R, R2 = 2 * a.R, LDU = 2 * a.R + 8;
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem);          // [kTok][LDX]
@@ -203,83 +196,63 @@ __global__ void __launch_bounds__(kThreads, 2) coral_predict_kernel(CoralArgs a)
         __syncthreads();
     }
 
-    // ---- residual coding, one lane per 8 channels of a token row
-    const int sub = lane % LPR, rw = lane / LPR;
-    uint16_t* codes16 = reinterpret_cast<uint16_t*>(a.codes);
+    // ---- residual coding: a thread owns 16 consecutive channels of a token row
+    constexpr int TPR = D / 16, RPW = 32 / TPR, TPG = G / 16;
+    const int t = lane % TPR, rw = lane / TPR;
     const int64_t stage_stride = (int64_t)H * a.n_tokens;
-    for (int r0 = warp * RPS; r0 < kTok; r0 += (kThreads / 32) * RPS) {
+    for (int r0 = warp * RPW; r0 < kTok; r0 += (kThreads / 32) * RPW) {
         const int row = r0 + rw;
         const int64_t n = n0 + row;
         const bool valid = n < a.n_tokens;
-        float p[8];
+        float p[16];
         if (has_pred) {
-            const float4 p0 = *reinterpret_cast<const float4*>(ps + row * LDP + sub * 8);
-            const float4 p1 = *reinterpret_cast<const float4*>(ps + row * LDP + sub * 8 + 4);
-            p[0] = p0.x; p[1] = p0.y; p[2] = p0.z; p[3] = p0.w;
-            p[4] = p1.x; p[5] = p1.y; p[6] = p1.z; p[7] = p1.w;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float4 v = *reinterpret_cast<const float4*>(ps + row * LDP + t * 16 + 4 * k);
+                p[4 * k] = v.x; p[4 * k + 1] = v.y; p[4 * k + 2] = v.z; p[4 * k + 3] = v.w;
+            }
         } else {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) p[i] = 0.0f;
+            for (int i = 0; i < 16; ++i) p[i] = 0.0f;
         }
-        const int64_t elem = n * HD + h * D + sub * 8;
+        const int64_t elem = n * HD + h * D + t * 16;
         if (valid && a.pred_out) {
-            *reinterpret_cast<float4*>(a.pred_out + elem) = make_float4(p[0], p[1], p[2], p[3]);
-            *reinterpret_cast<float4*>(a.pred_out + elem + 4) = make_float4(p[4], p[5], p[6], p[7]);
-        }
-        float acc[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = p[i];
+            for (int k = 0; k < 4; ++k)
+                *reinterpret_cast<float4*>(a.pred_out + elem + 4 * k) =
+                    make_float4(p[4 * k], p[4 * k + 1], p[4 * k + 2], p[4 * k + 3]);
+        }
+        float acc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = p[i];
         const int64_t rowoff = (int64_t)h * a.n_tokens + n;
         if (ENCODE) {
-            float rr[8];
-            const uint4 xv = valid ? ldg_nc_v4(a.xnext + elem) : make_uint4(0, 0, 0, 0);
-            unpack8(xv, rr);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) rr[i] = __fsub_rn(rr[i], p[i]);
+            // every lane takes part in the group reductions; `valid` gates the stores only
+            float rr[16];
+            const uint4 x0 = valid ? ldg_nc_v4(a.xnext + elem) : make_uint4(0, 0, 0, 0);
+            const uint4 x1 = valid ? ldg_nc_v4(a.xnext + elem + 8) : make_uint4(0, 0, 0, 0);
+            unpack16(x0, x1, rr);
+            sub16(rr, p);
             for (int s = 0; s < a.S; ++s) {
-                float mn = rr[0], mx = rr[0];
-#pragma unroll
-                for (int i = 1; i < 8; ++i) { mn = fminf(mn, rr[i]); mx = fmaxf(mx, rr[i]); }
-#pragma unroll
-                for (int off = 1; off < LPG; off <<= 1) {
-                    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-                }
-                mn = __fadd_rn(mn, 0.0f);
-                mx = __fadd_rn(mx, 0.0f);
-                const GroupParams gp = group_params(mn, mx);
-                uint32_t code = 0;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint32_t qv = quant_code(rr[i], gp);
-                    code |= qv << (2 * i);
-                    const float d = dequant(qv, gp.s, gp.z);
-                    rr[i] = __fsub_rn(rr[i], d);
-                    acc[i] = __fadd_rn(acc[i], d);
-                }
+                uint32_t meta;
+                const uint32_t code = quant_stage16<TPG>(rr, s + 1 < a.S, acc, meta);
                 if (valid) {
                     const int64_t srow = (int64_t)s * stage_stride + rowoff;
-                    codes16[srow * (D / 8) + sub] = (uint16_t)code;
-                    if (sub % LPG == 0) a.meta[srow * (D / G) + sub / LPG] = gp.meta;
+                    a.codes[srow * (D / 16) + t] = code;
+                    if (t % TPG == 0) a.meta[srow * (D / G) + t / TPG] = meta;
                 }
             }
         } else if (valid) {
             for (int s = 0; s < a.S; ++s) {
                 const int64_t srow = (int64_t)s * stage_stride + rowoff;
-                const uint32_t code = codes16[srow * (D / 8) + sub];
-                const uint32_t m = __ldg(a.meta + srow * (D / G) + sub / LPG);
-                const float sc = f16_bits_to_f32(m), z = f16_bits_to_f32(m >> 16);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], dequant((code >> (2 * i)) & 3u, sc, z));
+                dequant_add16(acc, __ldg(a.codes + srow * (D / 16) + t), __ldg(a.meta + srow * (D / G) + (t * 16) / G));
             }
         }
         if (valid) {
-            uint4 o;
-            o.x = pack_bf16x2(acc[0], acc[1]);
-            o.y = pack_bf16x2(acc[2], acc[3]);
-            o.z = pack_bf16x2(acc[4], acc[5]);
-            o.w = pack_bf16x2(acc[6], acc[7]);
-            *reinterpret_cast<uint4*>(a.xhat + elem) = o;
+            uint4 o0, o1;
+            pack16_bf16(acc, o0, o1);
+            *reinterpret_cast<uint4*>(a.xhat + elem) = o0;
+            *reinterpret_cast<uint4*>(a.xhat + elem + 8) = o1;
         }
     }
 }

@@ -491,6 +491,7 @@ __device__ __forceinline__ i128 shfl_xor_i128(i128 v, int mask) {
 // 32/(D/8) rows, and kSumBatch of them are in flight before any arithmetic.
 // Row slots are reduced at the end (integer additions: exact, any order).
 constexpr int kSumBatch = 4;
+static_assert(kPieceTokens <= 64, "a warp holds a piece's token indices in two registers per lane");
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 3) kmeans_sum_kernel(UpdateArgs a) {
@@ -508,28 +509,36 @@ __global__ void __launch_bounds__(kThreads, 3) kmeans_sum_kernel(UpdateArgs a) {
 #pragma unroll
     for (int d = 0; d < 8; ++d) w1[d] = w2[d] = w3[d] = 0;
     float amax = 0.0f;
-    for (int k0 = 0; k0 < len; k0 += 32) {
-        const int cnt = min(32, len - k0);
-        const int myn = lane < cnt ? ph[k0 + lane] : 0;
-        for (int u0 = 0; u0 < cnt; u0 += RPI * kSumBatch) {
-            uint4 v[kSumBatch];
+    // the piece's token indices (len <= kPieceTokens = 64): lane k holds
+    // positions k and k + 32
+    const int pa = lane < len ? ph[lane] : 0, pb = lane + 32 < len ? ph[lane + 32] : 0;
+    constexpr int kStep = RPI * kSumBatch;   // rows per batch
+    auto load_batch = [&](int b0, uint4* v) {
 #pragma unroll
-            for (int u = 0; u < kSumBatch; ++u) {
-                const int idx = u0 + u * RPI + slot;
-                const int n = __shfl_sync(0xffffffffu, myn, idx & 31);
-                v[u] = idx < cnt ? ldg_nc_v4(xh + (int64_t)n * a.token_stride) : make_uint4(0, 0, 0, 0);
-            }
+        for (int u = 0; u < kSumBatch; ++u) {
+            const int idx = b0 + u * RPI + slot;
+            const int na = __shfl_sync(0xffffffffu, pa, idx & 31), nb = __shfl_sync(0xffffffffu, pb, idx & 31);
+            const int n = idx < 32 ? na : nb;
+            v[u] = idx < len ? ldg_nc_v4(xh + (int64_t)n * a.token_stride) : make_uint4(0, 0, 0, 0);
+        }
+    };
+    // two batches in flight: the next batch is loaded while this one is summed
+    uint4 cur[kSumBatch], nxt[kSumBatch];
+    load_batch(0, cur);
+    for (int b0 = 0; b0 < len; b0 += kStep) {
+        if (b0 + kStep < len) load_batch(b0 + kStep, nxt);
 #pragma unroll
-            for (int u = 0; u < kSumBatch; ++u) {
-                const uint32_t wv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        for (int u = 0; u < kSumBatch; ++u) {
+            const uint32_t wv[4] = {cur[u].x, cur[u].y, cur[u].z, cur[u].w};
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float lo = bf16_lo(wv[q]), hi = bf16_hi(wv[q]);
-                    amax = fmax3(amax, fabsf(lo), fabsf(hi));
-                    window_add2(make_float2(lo, hi), w1 + 2 * q, w2 + 2 * q, w3 + 2 * q);
-                }
+            for (int q = 0; q < 4; ++q) {
+                const float lo = bf16_lo(wv[q]), hi = bf16_hi(wv[q]);
+                amax = fmax3(amax, fabsf(lo), fabsf(hi));
+                window_add2(make_float2(lo, hi), w1 + 2 * q, w2 + 2 * q, w3 + 2 * q);
             }
         }
+#pragma unroll
+        for (int u = 0; u < kSumBatch; ++u) cur[u] = nxt[u];
     }
     i128 tot[8];
     if (__any_sync(0xffffffffu, !(amax < kWinMax))) {

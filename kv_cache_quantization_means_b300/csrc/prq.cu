@@ -4,12 +4,12 @@
 // token's centroid) and sec. 2B items 1-3 (re-quantise the residual stage by
 // stage; decode = dequantise, sum the stages, add the centroid back).
 //
-// Both kernels stream HBM.  A thread owns 16 consecutive channels of a token
-// row (two 16-byte bf16 vectors, one 32-bit code word per stage); D/16 lanes
-// cover a row and a warp covers 32/(D/16) rows at a time.  Group min/max are
-// warp-shuffle reductions over the G/16 lanes of a group.  Every load of a
-// row is issued before any of its arithmetic (the encoder also prefetches
-// the next row), so each warp keeps several rows of HBM traffic in flight.
+// Both kernels stream HBM.  A thread owns one quantisation group of a token
+// row (G channels; two threads share a group of 128), so the group's
+// min/max, scale, zero-point and reciprocal are formed once per group; its
+// CPT = min(G, 64) channels arrive as 16-byte bf16 vectors and its codes
+// leave as one vector store per stage.  Every load of a row is issued before
+// any of its arithmetic.
 #include "common.cuh"
 #include "kernels.h"
 #include "prq16.cuh"
@@ -19,80 +19,85 @@ namespace qvg {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kEncRowsPerThread = 4;   // encoder: rows per thread (pipelined)
-constexpr int kDecRowsPerThread = 2;   // decoder: rows per thread (loads hoisted)
 
-template <int D>
-struct Map16 {
-    static constexpr int TPR = D / 16;                   // threads per row
-    static constexpr int RPW = 32 / TPR;                 // rows per warp step
-    static constexpr int RPS = RPW * (kThreads / 32);    // rows per CTA step
+template <int D, int G>
+struct GMap {
+    static constexpr int CPT = G < 64 ? G : 64;   // channels per thread
+    static constexpr int TPG = G / CPT;           // threads per group (1 or 2)
+    static constexpr int TPR = D / CPT;           // threads per row
+    static constexpr int RPW = 32 / TPR;          // rows per warp
+    static constexpr int RPC = RPW * (kThreads / 32);
+    static constexpr int NV = CPT / 8;            // 16-byte bf16 vectors per thread
+    static constexpr int NW = CPT / 16;           // code words per thread and stage
 };
 
+// 16-byte load through L1 (a thread's consecutive vectors share sectors).
+__device__ __forceinline__ uint4 ldg_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+template <int NW>
+__device__ __forceinline__ void store_words(uint32_t* p, const uint32_t* w) {
+    if constexpr (NW == 4) *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+    else if constexpr (NW == 2) *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
+    else *p = w[0];
+}
+
+template <int NW>
+__device__ __forceinline__ void load_words(const uint32_t* p, uint32_t* w) {
+    if constexpr (NW == 4) {
+        const uint4 v = ldg_v4(p);
+        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+    } else if constexpr (NW == 2) {
+        const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
+        w[0] = v.x; w[1] = v.y;
+    } else {
+        w[0] = __ldg(p);
+    }
+}
+
 template <int D, int G, bool HAS_C>
-__global__ void __launch_bounds__(kThreads, 4) prq_encode_kernel(EncodeArgs a) {
-    using M = Map16<D>;
-    constexpr int TPG = G / 16;
+__global__ void __launch_bounds__(kThreads, 2) prq_encode_kernel(EncodeArgs a) {
+    using M = GMap<D, G>;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t = lane % M::TPR;
     const int h = blockIdx.y;
-    // rows of this thread: base + k * RPS, k < kEncRowsPerThread
-    const int64_t base = (int64_t)blockIdx.x * M::RPS * kEncRowsPerThread + (int64_t)warp * M::RPW + lane / M::TPR;
-
-    const uint16_t* xh = a.x + (int64_t)h * a.head_stride + t * 16;
-    const uint8_t* idh = HAS_C ? a.ids + (int64_t)h * a.cap + a.tok_offset : nullptr;
-    const uint16_t* ch = HAS_C ? a.cent + (int64_t)h * a.C * D + t * 16 : nullptr;
-    const int64_t stage_rows = (int64_t)a.H * a.cap;
-    const int64_t row0 = (int64_t)h * a.cap + a.tok_offset;
-
-    uint4 xa = make_uint4(0, 0, 0, 0), xb = xa, ca = xa, cb = xa;
-    if (base < a.n_tokens) {
-        const uint16_t* p = xh + base * a.token_stride;
-        xa = ldg_nc_v4(p);
-        xb = ldg_nc_v4(p + 8);
+    const int64_t n = (int64_t)blockIdx.x * M::RPC + (int64_t)warp * M::RPW + lane / M::TPR;
+    const bool valid = n < a.n_tokens;
+    // every lane takes part in the group reductions; `valid` gates memory only
+    float r[M::CPT];
+    {
+        uint4 xv[M::NV], cv[M::NV];
+        const uint16_t* xp = a.x + (int64_t)h * a.head_stride + (valid ? n : 0) * a.token_stride + t * M::CPT;
+#pragma unroll
+        for (int k = 0; k < M::NV; ++k) xv[k] = valid ? ldg_v4(xp + 8 * k) : make_uint4(0, 0, 0, 0);
         if (HAS_C) {
-            const int id = min((int)idh[base], a.C - 1);
-            ca = __ldg(reinterpret_cast<const uint4*>(ch + (int64_t)id * D));
-            cb = __ldg(reinterpret_cast<const uint4*>(ch + (int64_t)id * D + 8));
+            const int id = valid ? min((int)a.ids[(int64_t)h * a.cap + a.tok_offset + n], a.C - 1) : 0;
+            const uint16_t* cp = a.cent + ((int64_t)h * a.C + id) * D + t * M::CPT;
+#pragma unroll
+            for (int k = 0; k < M::NV; ++k) cv[k] = valid ? __ldg(reinterpret_cast<const uint4*>(cp + 8 * k)) : make_uint4(0, 0, 0, 0);
         }
-    }
-#pragma unroll 1
-    for (int k = 0; k < kEncRowsPerThread; ++k) {
-        const int64_t n = base + (int64_t)k * M::RPS;
-        const bool valid = n < a.n_tokens;
-        // prefetch the next row of this thread
-        const int64_t nn = n + M::RPS;
-        uint4 nxa = make_uint4(0, 0, 0, 0), nxb = nxa;
-        int nid = 0;
-        const bool nvalid = (k + 1 < kEncRowsPerThread) && nn < a.n_tokens;
-        if (nvalid) {
-            const uint16_t* p = xh + nn * a.token_stride;
-            nxa = ldg_nc_v4(p);
-            nxb = ldg_nc_v4(p + 8);
-            if (HAS_C) nid = min((int)idh[nn], a.C - 1);
-        }
-        float r[16];
-        unpack16(xa, xb, r);
-        if (HAS_C) {
+#pragma unroll
+        for (int k = 0; k < M::NV; k += 2) {
             float c[16];
-            unpack16(ca, cb, c);
-            sub16(r, c);
-        }
-        const int64_t row = row0 + n;
-        for (int s = 0; s < a.S; ++s) {
-            uint32_t meta;
-            const uint32_t code = quant_stage16<TPG>(r, s + 1 < a.S, nullptr, meta);
-            if (valid) {
-                const int64_t srow = (int64_t)s * stage_rows + row;
-                a.codes[srow * (D / 16) + t] = code;
-                if (t % TPG == 0) a.meta[srow * (D / G) + t / TPG] = meta;
+            unpack16(xv[k], xv[k + 1], r + 8 * k);
+            if (HAS_C) {
+                unpack16(cv[k], cv[k + 1], c);
+                sub16(r + 8 * k, c);
             }
         }
-        xa = nxa;
-        xb = nxb;
-        if (HAS_C && nvalid) {
-            ca = __ldg(reinterpret_cast<const uint4*>(ch + (int64_t)nid * D));
-            cb = __ldg(reinterpret_cast<const uint4*>(ch + (int64_t)nid * D + 8));
+    }
+    const int64_t row = (int64_t)h * a.cap + a.tok_offset + n;
+    const int64_t stage_rows = (int64_t)a.H * a.cap;
+    for (int s = 0; s < a.S; ++s) {
+        uint32_t code[M::NW], meta;
+        quant_stage<M::CPT, M::TPG>(r, s + 1 < a.S, nullptr, code, meta);
+        if (valid) {
+            const int64_t srow = (int64_t)s * stage_rows + row;
+            store_words<M::NW>(a.codes + srow * (D / 16) + t * M::NW, code);
+            if (t % M::TPG == 0) a.meta[srow * (D / G) + t / M::TPG] = meta;
         }
     }
 }
@@ -108,9 +113,8 @@ __device__ __forceinline__ int chunk_of(const int64_t* offs, int n_chunks, int64
 }
 
 template <int D, int G, bool HAS_C, bool VERSIONED>
-__global__ void __launch_bounds__(kThreads, 4) prq_decode_kernel(DecodeArgs a) {
-    using M = Map16<D>;
-    constexpr int NR = kDecRowsPerThread;
+__global__ void __launch_bounds__(kThreads, 2) prq_decode_kernel(DecodeArgs a) {
+    using M = GMap<D, G>;
     extern __shared__ int64_t chunk_smem[];   // VERSIONED: offsets[n_chunks + 1], versions[n_chunks]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t = lane % M::TPR;
@@ -121,70 +125,69 @@ __global__ void __launch_bounds__(kThreads, 4) prq_decode_kernel(DecodeArgs a) {
         for (int i = threadIdx.x; i < a.n_chunks; i += kThreads) vers[i] = a.chunk_version[i];
         __syncthreads();
     }
-    const int64_t n_rows = a.tok_end - a.tok_begin;
-    const int64_t base = (int64_t)blockIdx.x * M::RPS * NR + (int64_t)warp * M::RPW + lane / M::TPR;
+    const int64_t i = (int64_t)blockIdx.x * M::RPC + (int64_t)warp * M::RPW + lane / M::TPR;
+    if (i >= a.tok_end - a.tok_begin) return;
+    const int64_t n = a.tok_begin + i;
+    const int64_t row = (int64_t)h * a.cap + n;
     const int64_t stage_rows = (int64_t)a.H * a.cap;
-    constexpr int WPR = D / 16, MPR = D / G;
-    const int mi = (t * 16) / G;
-
-    int64_t ii[NR];
-    bool ok[NR];
-    int id[NR];
-    uint32_t code[NR][kMaxStages], meta[NR][kMaxStages];
+    // codes and scale/zero words of every stage, then the centroid
+    uint32_t code[kMaxStages][M::NW], meta[kMaxStages];
 #pragma unroll
-    for (int k = 0; k < NR; ++k) {
-        ii[k] = base + (int64_t)k * M::RPS;
-        ok[k] = ii[k] < n_rows;
-        const int64_t row = (int64_t)h * a.cap + a.tok_begin + ii[k];
-        id[k] = 0;
-        if (HAS_C && ok[k]) id[k] = a.ids[row];
-#pragma unroll
-        for (int s = 0; s < kMaxStages; ++s) {
-            code[k][s] = 0;
-            meta[k][s] = 0;
-            if (s < a.S && ok[k]) {
-                const int64_t srow = (int64_t)s * stage_rows + row;
-                code[k][s] = __ldg(a.codes + srow * WPR + t);
-                meta[k][s] = __ldg(a.meta + srow * MPR + mi);
-            }
+    for (int s = 0; s < kMaxStages; ++s) {
+        if (s < a.S) {
+            const int64_t srow = (int64_t)s * stage_rows + row;
+            load_words<M::NW>(a.codes + srow * (D / 16) + t * M::NW, code[s]);
+            meta[s] = __ldg(a.meta + srow * (D / G) + t / M::TPG);
         }
     }
+    // centroid row, then the output in runs of up to 32 channels (keeps the
+    // live registers down)
+    constexpr int HC = M::CPT < 32 ? M::CPT : 32;   // channels per run
+    const uint16_t* cp = nullptr;
+    if (HAS_C) {
+        const uint16_t* cbase = a.cent;
+        if (VERSIONED) {
+            const int32_t* vers = reinterpret_cast<const int32_t*>(chunk_smem + a.n_chunks + 1);
+            cbase += (int64_t)vers[chunk_of(chunk_smem, a.n_chunks, n)] * a.H * a.C * D;
+        }
+        const int id = min((int)a.ids[row], a.C - 1);
+        cp = cbase + ((int64_t)h * a.C + id) * D + t * M::CPT;
+    }
+    uint16_t* op = a.out + (int64_t)h * a.out_head_stride + i * a.out_token_stride + t * M::CPT;
 #pragma unroll
-    for (int k = 0; k < NR; ++k) {
-        if (!ok[k]) continue;
-        float acc[16];
+    for (int hc = 0; hc < M::CPT; hc += HC) {
+        float acc[HC];
         if (HAS_C) {
-            const uint16_t* cbase = a.cent;
-            if (VERSIONED) {
-                const int32_t* vers = reinterpret_cast<const int32_t*>(chunk_smem + a.n_chunks + 1);
-                const int c = chunk_of(chunk_smem, a.n_chunks, a.tok_begin + ii[k]);
-                cbase += (int64_t)vers[c] * a.H * a.C * D;
-            }
-            const uint16_t* cr = cbase + ((int64_t)h * a.C + min(id[k], a.C - 1)) * D + t * 16;
-            const uint4 c0 = __ldg(reinterpret_cast<const uint4*>(cr));
-            const uint4 c1 = __ldg(reinterpret_cast<const uint4*>(cr + 8));
-            unpack16(c0, c1, acc);
+            uint4 cv[HC / 8];
+#pragma unroll
+            for (int k = 0; k < HC / 8; ++k) cv[k] = __ldg(reinterpret_cast<const uint4*>(cp + hc + 8 * k));
+#pragma unroll
+            for (int k = 0; k < HC / 8; k += 2) unpack16(cv[k], cv[k + 1], acc + 8 * k);
         } else {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+            for (int k = 0; k < HC; ++k) acc[k] = 0.0f;
         }
 #pragma unroll
         for (int s = 0; s < kMaxStages; ++s)
-            if (s < a.S) dequant_add16(acc, code[k][s], meta[k][s]);
-        uint4 o0, o1;
-        pack16_bf16(acc, o0, o1);
-        uint16_t* op = a.out + (int64_t)h * a.out_head_stride + ii[k] * a.out_token_stride + t * 16;
-        stg_v4_stream(op, o0);
-        stg_v4_stream(op + 8, o1);
+            if (s < a.S) {
+#pragma unroll
+                for (int w = 0; w < HC / 16; ++w) dequant_add16(acc + 16 * w, code[s][hc / 16 + w], meta[s]);
+            }
+#pragma unroll
+        for (int k = 0; k < HC / 8; k += 2) {
+            uint4 o0, o1;
+            pack16_bf16(acc + 8 * k, o0, o1);
+            stg_v4_stream(op + hc + 8 * k, o0);
+            stg_v4_stream(op + hc + 8 * k + 8, o1);
+        }
     }
 }
 
 template <int D, int G>
 cudaError_t encode_dg(const EncodeArgs& a, cudaStream_t s) {
-    using M = Map16<D>;
+    using M = GMap<D, G>;
     if (a.n_tokens == 0) return cudaSuccess;
-    const int64_t rows_per_cta = (int64_t)M::RPS * kEncRowsPerThread;
-    dim3 grid((unsigned)((a.n_tokens + rows_per_cta - 1) / rows_per_cta), (unsigned)a.H);
+    dim3 grid((unsigned)((a.n_tokens + M::RPC - 1) / M::RPC), (unsigned)a.H);
     if (a.C > 0) prq_encode_kernel<D, G, true><<<grid, kThreads, 0, s>>>(a);
     else prq_encode_kernel<D, G, false><<<grid, kThreads, 0, s>>>(a);
     return cudaGetLastError();
@@ -192,11 +195,10 @@ cudaError_t encode_dg(const EncodeArgs& a, cudaStream_t s) {
 
 template <int D, int G>
 cudaError_t decode_dg(const DecodeArgs& a, cudaStream_t s) {
-    using M = Map16<D>;
+    using M = GMap<D, G>;
     const int64_t rows = a.tok_end - a.tok_begin;
     if (rows <= 0) return cudaSuccess;
-    const int64_t rows_per_cta = (int64_t)M::RPS * kDecRowsPerThread;
-    dim3 grid((unsigned)((rows + rows_per_cta - 1) / rows_per_cta), (unsigned)a.H);
+    dim3 grid((unsigned)((rows + M::RPC - 1) / M::RPC), (unsigned)a.H);
     if (a.C > 0 && a.chunk_offset) {
         const size_t smem = sizeof(int64_t) * (a.n_chunks + 1) + sizeof(int32_t) * a.n_chunks;
         prq_decode_kernel<D, G, true, true><<<grid, kThreads, smem, s>>>(a);

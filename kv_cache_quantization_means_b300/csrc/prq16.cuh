@@ -1,5 +1,5 @@
-// One thread's share of progressive residual quantisation: 16 consecutive
-// channels of a token row (Quant VideoGen explainer, Sommario tecnico
+// One thread's share of progressive residual quantisation: a run of
+// consecutive channels of a token row (Quant VideoGen explainer, Sommario tecnico
 // sec. 2B: each stage re-quantises what the previous stages left; decoding
 // dequantises and sums the stages onto the centroid).
 //
@@ -13,7 +13,7 @@
 //                                integer with ties to even
 //   d = fma(q, s, z)             q*s is exact, so this is q*s + z rounded once
 //   r = r - d
-// The 16 2-bit codes go to one 32-bit word, element k at bits 2k, 2k+1.
+// Every 16 2-bit codes go to one 32-bit word, element k at bits 2k, 2k+1.
 #pragma once
 
 #include "common.cuh"
@@ -51,21 +51,40 @@ __device__ __forceinline__ void sub16(float* r, const float* c) {
     }
 }
 
-// One stage over the thread's 16 channels; the group spans TPG = G/16
-// consecutive lanes (all 32 lanes must call this together).  Returns the code
-// word; `meta` receives the group's (scale, zero) word.  When `update` the
-// residual is replaced by what the stage leaves; `acc` (may be null) gets the
-// dequantised values added.
-template <int TPG>
-__device__ __forceinline__ uint32_t quant_stage16(float* r, bool update, float* acc, uint32_t& meta) {
-    float mn = fmin3(r[0], r[1], r[2]), mx = fmax3(r[0], r[1], r[2]);
+// Packs the low bytes of vb[0..15] (each a code q_k < 4) into one word,
+// element k at bits 2k: bytes {q_j, q_j+4, q_j+8, q_j+12} are gathered into
+// W_j, then the four words are interleaved two bits apart.
+__device__ __forceinline__ uint32_t pack_codes16(const uint32_t* vb) {
+    uint32_t w[4];
 #pragma unroll
-    for (int i = 3; i < 15; i += 2) {
-        mn = fmin3(mn, r[i], r[i + 1]);
-        mx = fmax3(mx, r[i], r[i + 1]);
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t lo = prmt(vb[j], vb[j + 4], 0x0040u);
+        const uint32_t hi = prmt(vb[j + 8], vb[j + 12], 0x0040u);
+        w[j] = prmt(lo, hi, 0x5410u);
     }
-    mn = fminf(mn, r[15]);
-    mx = fmaxf(mx, r[15]);
+    return w[0] | (w[1] << 2) | (w[2] << 4) | (w[3] << 6);
+}
+
+// One stage over the thread's CPT channels (a multiple of 16); the group of
+// G = CPT * TPG channels spans TPG consecutive lanes (TPG > 1: all 32 lanes
+// must call this together).  Writes CPT/16 code words to `codes`; `meta`
+// receives the group's (scale, zero) word.  When `update` the residual is
+// replaced by what the stage leaves; `acc` (may be null) gets the
+// dequantised values added.
+template <int CPT, int TPG>
+__device__ __forceinline__ void quant_stage(float* r, bool update, float* acc, uint32_t* codes, uint32_t& meta) {
+    float m0 = fmin3(r[0], r[1], r[2]), M0 = fmax3(r[0], r[1], r[2]);
+    float m1 = fmin3(r[3], r[4], r[5]), M1 = fmax3(r[3], r[4], r[5]);
+#pragma unroll
+    for (int i = 6; i + 3 < CPT; i += 4) {
+        m0 = fmin3(m0, r[i], r[i + 1]);
+        M0 = fmax3(M0, r[i], r[i + 1]);
+        m1 = fmin3(m1, r[i + 2], r[i + 3]);
+        M1 = fmax3(M1, r[i + 2], r[i + 3]);
+    }
+    // CPT % 4 == 0: the loop stops with r[CPT-2], r[CPT-1] left
+    float mn = fmin3(m0, m1, fminf(r[CPT - 2], r[CPT - 1]));
+    float mx = fmax3(M0, M1, fmaxf(r[CPT - 2], r[CPT - 1]));
 #pragma unroll
     for (int off = 1; off < TPG; off <<= 1) {
         mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
@@ -79,38 +98,41 @@ __device__ __forceinline__ uint32_t quant_stage16(float* r, bool update, float* 
     meta = p.meta;
     const float2 z2 = make_float2(p.z, p.z), inv2 = make_float2(p.inv, p.inv);
     const float2 s2 = make_float2(p.s, p.s), m2 = make_float2(kRintMagic, kRintMagic);
-    uint32_t vb[16];
 #pragma unroll
-    for (int i = 0; i < 16; i += 2) {
-        float2 t = f2_mul(f2_sub(make_float2(r[i], r[i + 1]), z2), inv2);
-        t.x = fminf(fmaxf(t.x, 0.0f), 3.0f);
-        t.y = fminf(fmaxf(t.y, 0.0f), 3.0f);
-        const float2 v = f2_add(t, m2);             // 1.5*2^23 + q exactly
-        vb[i] = __float_as_uint(v.x);
-        vb[i + 1] = __float_as_uint(v.y);
-        if (update || acc) {
-            const float2 q = f2_sub(v, m2);
-            const float2 d = f2_fma(q, s2, z2);
-            if (update) {
-                const float2 nr = f2_sub(make_float2(r[i], r[i + 1]), d);
-                r[i] = nr.x; r[i + 1] = nr.y;
-            }
-            if (acc) {
-                const float2 na = f2_add(make_float2(acc[i], acc[i + 1]), d);
-                acc[i] = na.x; acc[i + 1] = na.y;
+    for (int w = 0; w < CPT / 16; ++w) {
+        uint32_t vb[16];
+#pragma unroll
+        for (int k = 0; k < 16; k += 2) {
+            const int i = 16 * w + k;
+            float2 t = f2_mul(f2_sub(make_float2(r[i], r[i + 1]), z2), inv2);
+            t.x = fminf(fmaxf(t.x, 0.0f), 3.0f);
+            t.y = fminf(fmaxf(t.y, 0.0f), 3.0f);
+            const float2 v = f2_add(t, m2);             // 1.5*2^23 + q exactly
+            vb[k] = __float_as_uint(v.x);
+            vb[k + 1] = __float_as_uint(v.y);
+            if (update || acc) {
+                const float2 q = f2_sub(v, m2);
+                const float2 d = f2_fma(q, s2, z2);
+                if (update) {
+                    const float2 nr = f2_sub(make_float2(r[i], r[i + 1]), d);
+                    r[i] = nr.x; r[i + 1] = nr.y;
+                }
+                if (acc) {
+                    const float2 na = f2_add(make_float2(acc[i], acc[i + 1]), d);
+                    acc[i] = na.x; acc[i + 1] = na.y;
+                }
             }
         }
+        codes[w] = pack_codes16(vb);
     }
-    // the low byte of vb[k] is q_k; gather bytes {q_j, q_{j+4}, q_{j+8}, q_{j+12}}
-    // into W_j, then interleave the four words two bits apart
-    uint32_t w[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const uint32_t lo = prmt(vb[j], vb[j + 4], 0x0040u);
-        const uint32_t hi = prmt(vb[j + 8], vb[j + 12], 0x0040u);
-        w[j] = prmt(lo, hi, 0x5410u);
-    }
-    return w[0] | (w[1] << 2) | (w[2] << 4) | (w[3] << 6);
+}
+
+// 16-channel form (one code word).
+template <int TPG>
+__device__ __forceinline__ uint32_t quant_stage16(float* r, bool update, float* acc, uint32_t& meta) {
+    uint32_t c;
+    quant_stage<16, TPG>(r, update, acc, &c, meta);
+    return c;
 }
 
 // acc[k] += q_k * s + z for the 16 codes of `code` (element k at bits 2k).
