@@ -237,6 +237,11 @@ class StreamStep:
         self.ws = Q.alloc_workspace(self.cfg, self.chunk)
         self.out = torch.empty((N, H, D), dtype=torch.int16, device="cuda")
         per_tok = H * D * 2
+        # per (layer, tensor) and step: refit (init + T x 5 kernels) or assign, encode, chunk-table
+        # update, then the history decode
+        T = wl.lloyd_iters
+        self.launches_per_step = 2 * layers * sum((1 + 5 * T if k % self.every == 0 else 1) + 2 + 1
+                                                  for k in range(self.steps))
         self.enc_bytes = 2 * layers * N * per_tok
         self.dec_bytes = 2 * layers * per_tok * self.chunk * sum(range(1, self.steps + 1))
         self.bytes_per_step = self.enc_bytes + self.dec_bytes
@@ -446,7 +451,7 @@ def run_aux(args, Q, wl, peaks, world, rank, local):
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": cfgb, "roofline": dom,
-            "cpu_baseline": None, "e2e": None, "cuda_graph": True}
+            "cpu_baseline": None, "e2e": None, "gpu_launches": st.launches_per_step * args.steps, "cuda_graph": True}
     if rank == 0:
         print(json.dumps(line))
     return 0
@@ -522,7 +527,8 @@ def main():
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         t = tt.item()
     value = st.bytes_per_step * world / t / 1e9
-    launches_per_step = 2 * layers * (1 + wl.lloyd_iters * 4 + 2)
+    # per (layer, tensor): init + T x (assign, histogram, scatter, exact sum, mean) + encode + decode
+    launches_per_step = 2 * layers * (1 + wl.lloyd_iters * 5 + 2)
 
     roof = kernel_rooflines(st, peaks)
 

@@ -135,7 +135,10 @@ QVG_API qvg_status qvg_workspace_bytes(const qvg_config* cfg, int64_t n_tokens, 
  * centroid was settled by exact squared distances, out[2] = those among
  * them that needed the channel-order fp64 sum (near-exact ties),
  * out[3] = error word (0 = none; 0x7E000000 = a kernel gave up waiting on an
- * internal barrier and its ids are not valid).  Copies from the device and
+ * internal barrier and its ids are not valid).  With C = 0 (a Coral-KV
+ * configuration) out[0..2] are 0 and out[3] is the error word of the last
+ * coral_* call that used `workspace` (0x7E000000 = a tensor-core kernel gave
+ * up waiting and its outputs are not valid).  Copies from the device and
  * waits for `stream`; out is host memory. */
 QVG_API qvg_status qvg_fit_stats(const qvg_config* cfg, int64_t n_tokens, const void* workspace,
                          size_t workspace_bytes, uint64_t* out, qvg_stream stream);

@@ -125,6 +125,14 @@ qvg_status check_workspace(const qvg_config* c, int64_t n, void* ws, size_t ws_b
     return QVG_OK;
 }
 
+// Workspace of the cross-layer calls: the low-rank projection (fp32 [N][64])
+// or the tensor-core path's scratch, whichever is larger.
+size_t coral_ws_bytes(const qvg_config* c, int64_t n_tokens) {
+    const size_t lr = align256(sizeof(float) * 64 * (size_t)(n_tokens > 0 ? n_tokens : 1));
+    const size_t tc = qvg::coral_tc_scratch_bytes(c->num_heads, n_tokens);
+    return lr > tc ? lr : tc;
+}
+
 qvg::AssignArgs assign_args(const qvg_config* c, const qvg_bf16* x, int64_t n, int64_t hs, int64_t ts,
                             const qvg_bf16* cent, uint8_t* ids, int64_t cap, int64_t off, int* counts,
                             unsigned long long* stats) {
@@ -195,8 +203,7 @@ qvg_status qvg_workspace_bytes(const qvg_config* cfg, int64_t n_tokens, size_t* 
     if (!bytes || n_tokens < 0) return fail(QVG_ERR_INVALID_ARG, "bad arguments");
     size_t b = carve(cfg, n_tokens, nullptr).bytes;
     if (cfg->num_clusters == 0) {
-        // cross-layer predictor: low-rank projection t [N][64] fp32
-        size_t coral = align256(sizeof(float) * 64 * (size_t)(n_tokens > 0 ? n_tokens : 1));
+        size_t coral = coral_ws_bytes(cfg, n_tokens);
         if (coral > b) b = coral;
     }
     *bytes = b;
@@ -205,10 +212,24 @@ qvg_status qvg_workspace_bytes(const qvg_config* cfg, int64_t n_tokens, size_t* 
 
 qvg_status qvg_fit_stats(const qvg_config* cfg, int64_t n_tokens, const void* workspace, size_t workspace_bytes,
                          uint64_t* out, qvg_stream stream) {
-    qvg_status st = check_config(cfg, true);
+    qvg_status st = check_config(cfg, false);
     if (st) return st;
     if (!out) return fail(QVG_ERR_INVALID_ARG, "out is NULL");
     if (n_tokens < 0) return fail(QVG_ERR_INVALID_ARG, "negative token count");
+    if (cfg->num_clusters == 0) {
+        // cross-layer config: only the error word of the tensor-core path
+        const size_t tc = qvg::coral_tc_scratch_bytes(cfg->num_heads, n_tokens);
+        out[0] = out[1] = out[2] = out[3] = 0;
+        if (!workspace || workspace_bytes < tc) return ok();
+        uint32_t w = 0;
+        cudaStream_t s = (cudaStream_t)stream;
+        cudaError_t e = cudaMemcpyAsync(&w, static_cast<const char*>(workspace) + tc - 256, sizeof(w),
+                                        cudaMemcpyDeviceToHost, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return cuda_status(e, "stats copy");
+        out[3] = w;
+        return ok();
+    }
     FitWorkspace w;
     if ((st = check_workspace(cfg, n_tokens, const_cast<void*>(workspace), workspace_bytes, &w))) return st;
     cudaStream_t s = (cudaStream_t)stream;
@@ -415,6 +436,13 @@ qvg_status qvg_decode_cache(const qvg_config* cfg, const qvg_cache* cache, int64
                        out_head_stride, out_token_stride, (cudaStream_t)stream);
 }
 
+// Zeroes the error word of the tensor-core cross-layer path (the word sits at
+// the end of its scratch) when the workspace is large enough for that path.
+static void clear_coral_error(const qvg_config* cfg, int64_t n_tokens, void* ws, size_t ws_bytes, cudaStream_t s) {
+    const size_t tc = qvg::coral_tc_scratch_bytes(cfg->num_heads, n_tokens);
+    if (ws_bytes >= tc) cudaMemsetAsync(static_cast<char*>(ws) + tc - 256, 0, sizeof(uint32_t), s);
+}
+
 static qvg_status coral_common(const qvg_config* cfg, const coral_predictor* pred, const qvg_bf16* xhat_prev,
                                int64_t n_tokens, void* workspace, size_t workspace_bytes) {
     qvg_status st = check_config(cfg, false);
@@ -430,7 +458,7 @@ static qvg_status coral_common(const qvg_config* cfg, const coral_predictor* pre
         if (pred->rank > 0 && (!pred->U || !pred->W)) return fail(QVG_ERR_INVALID_ARG, "U/W missing");
         if (!aligned16(xhat_prev) || !aligned16(pred->B) || (pred->rank && (!aligned16(pred->U) || !aligned16(pred->W))))
             return fail(QVG_ERR_INVALID_ARG, "predictor / xhat_prev must be 16-byte aligned");
-        size_t need = align256(sizeof(float) * 64 * (size_t)(n_tokens > 0 ? n_tokens : 1));
+        const size_t need = coral_ws_bytes(cfg, n_tokens);
         if (pred->rank > 0 && (!workspace || workspace_bytes < need))
             return fail(QVG_ERR_INVALID_ARG, "workspace too small: need %zu bytes", need);
     }
@@ -455,6 +483,9 @@ qvg_status coral_predict_encode(const qvg_config* cfg, const coral_predictor* pr
     a.n_tokens = n_tokens; a.H = cfg->num_heads; a.S = cfg->num_stages;
     a.codes = codes; a.meta = meta; a.xhat = xhat_next; a.pred_out = pred_out;
     a.lowrank = (float*)workspace;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    if (workspace) clear_coral_error(cfg, n_tokens, workspace, workspace_bytes, (cudaStream_t)stream);
     return cuda_status(qvg::launch_coral(cfg->head_dim, cfg->group_size, true, a, (cudaStream_t)stream),
                        "coral launch");
 }
@@ -476,6 +507,9 @@ qvg_status coral_predict_decode(const qvg_config* cfg, const coral_predictor* pr
     a.codes = const_cast<uint32_t*>(codes); a.meta = const_cast<uint32_t*>(meta);
     a.xhat = xhat_next; a.pred_out = pred_out;
     a.lowrank = (float*)workspace;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    if (workspace) clear_coral_error(cfg, n_tokens, workspace, workspace_bytes, (cudaStream_t)stream);
     return cuda_status(qvg::launch_coral(cfg->head_dim, cfg->group_size, false, a, (cudaStream_t)stream),
                        "coral launch");
 }
@@ -549,6 +583,9 @@ qvg_status coral_predict_encode_static(const qvg_config* cfg, const coral_predic
     a.n_tokens = n_tokens; a.H = cfg->num_heads; a.S = cfg->num_stages;
     a.codes = codes; a.meta = meta; a.xhat = xhat_next; a.pred_out = pred_out;
     a.lowrank = scratch;
+    a.workspace = scratch;
+    a.workspace_bytes = kStaticScratchFloats * sizeof(float);
+    if (scratch) clear_coral_error(cfg, n_tokens, scratch, a.workspace_bytes, (cudaStream_t)stream);
     return cuda_status(qvg::launch_coral(cfg->head_dim, cfg->group_size, true, a, (cudaStream_t)stream),
                        "coral launch");
 }

@@ -269,6 +269,20 @@ size_t predict_smem(int D, int R) {
 template <int D, int G>
 cudaError_t coral_dg(bool encode, const CoralArgs& a, cudaStream_t s) {
     if (a.n_tokens == 0) return cudaSuccess;
+    if (a.xprev && a.workspace && a.workspace_bytes >= coral_tc_scratch_bytes(a.H, a.n_tokens)) {
+        // tensor-core path first; the kernels below serve every other shape
+        auto a256 = [](size_t v) { return (v + 255) & ~(size_t)255; };
+        const size_t N = (size_t)a.n_tokens, HD = (size_t)a.H * 128;
+        uint8_t* base = static_cast<uint8_t*>(a.workspace);
+        CoralTcScratch w;
+        w.t2 = reinterpret_cast<uint16_t*>(base);
+        w.wt = reinterpret_cast<uint16_t*>(base + a256(N * 64 * 2));
+        w.ud = reinterpret_cast<uint16_t*>(base + a256(N * 64 * 2) + a256(32 * HD * 2));
+        w.err = reinterpret_cast<uint32_t*>(base + coral_tc_scratch_bytes(a.H, a.n_tokens) - 256);
+        bool launched = false;
+        cudaError_t e = launch_coral_tc(D, G, encode, a, w, &launched, s);
+        if (e != cudaSuccess || launched) return e;
+    }
     const int HD = a.H * D;
     if (a.xprev && a.R > 0) {
         dim3 g((unsigned)((a.n_tokens + kLrTile - 1) / kLrTile));

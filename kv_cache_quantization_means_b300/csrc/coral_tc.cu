@@ -1,0 +1,501 @@
+// Coral-KV cross-layer prediction on the 5th-generation tensor cores (sm_103a).
+//
+// Coral-KV news items, section "cross-layer prediction": layer l+1 is
+// predicted from the reconstruction of layer l by a block-DPLR map -- a dense
+// D x D block per head plus one global rank-R term -- and only the residual
+// is quantised.  Per layer (one tensor, N tokens, H heads of D = 128, R = 32):
+//
+//  prep       Wt = W^T ([R][H*D]) and Ud = [U | U] ([H*D][2R]), bf16, so every
+//             GEMM operand is K-major with 128-byte rows.
+//  lowrank    t = xhat W: one CTA per 128-token tile streams the H*D/64
+//             channel slabs of xhat and Wt through TMA into shared memory;
+//             tcgen05.mma accumulates the [128 x 32] fp32 result in TMEM;
+//             the epilogue stores t as a bf16 pair (hi, lo = t - hi), i.e. a
+//             [128 x 64] K-major operand that keeps ~16 significant bits.
+//  predict    persistent CTAs over (token tile, head) items: TMA brings
+//             xhat_h (128 x 128), B_h (128 x 128), t (128 x 64) and Ud_h
+//             (128 x 64); 8 + 4 MMAs (K = 16) form
+//                 pred = xhat_h B_h^T + t_hi U_h^T + t_lo U_h^T
+//             in one of two TMEM accumulators; two epilogue groups of four
+//             warps drain them, a thread per token row, 32 channels (or one
+//             64-channel group) at a time: encode subtracts pred from x_{l+1}, runs the same
+//             per-thread PRQ stages as the other kernels and writes codes,
+//             scale/zero words and x_hat_{l+1} = bf16(((pred + d_1) + d_2)..);
+//             decode rebuilds x_hat_{l+1} from the codes.  Encoder and decoder
+//             run the identical prediction, so their reconstructions agree
+//             bit for bit.
+// Every wait is a bounded mbarrier wait; on expiry the kernel records an
+// error code, drains its own copies and MMAs and frees its tensor memory.
+#include "common.cuh"
+#include "kernels.h"
+#include "prq16.cuh"
+#include "tc_common.cuh"
+
+namespace qvg {
+
+namespace {
+
+constexpr int kT = 128;                 // tokens per tile (UMMA M)
+constexpr int kR = 32;                  // rank handled here
+constexpr int kDh = 128;                // head dim handled here
+constexpr int kSlab = kT * 128;         // one [128 x 64] bf16 operand slab, bytes
+constexpr uint32_t kErrTimeout = 0x7E000000u;
+
+// ------------------------------------------------------------------ prep
+
+__global__ void coral_prep_kernel(const uint16_t* W, const uint16_t* U, int HD, uint16_t* Wt, uint16_t* Ud) {
+    const int j = blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= HD) return;
+#pragma unroll 4
+    for (int r = 0; r < kR; ++r) {
+        Wt[(int64_t)r * HD + j] = W[(int64_t)j * kR + r];
+        const uint16_t u = U[(int64_t)j * kR + r];
+        Ud[(int64_t)j * 2 * kR + r] = u;
+        Ud[(int64_t)j * 2 * kR + kR + r] = u;
+    }
+}
+
+// --------------------------------------------------------------- lowrank
+
+constexpr int kLrStages = 4;
+constexpr int kLrThreads = 64 + 128;    // TMA warp, MMA warp, 4 epilogue warps
+
+struct LrArgs {
+    int64_t n_tokens;
+    int HD;
+    uint16_t* t2;          // [N][64] bf16: t_hi | t_lo
+    uint32_t* err;
+};
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+__global__ void __launch_bounds__(kLrThreads, 1)
+    coral_lowrank_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                            LrArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    constexpr int kWBytes = kR * 128;                   // Wt slab [32 x 64]
+    uint8_t* Xs = base;                                  // kLrStages x [128 x 64]
+    uint8_t* Ws = base + kLrStages * kSlab;              // kLrStages x [32 x 64]
+    const uint32_t bar0 = smem_u32(base + kLrStages * (kSlab + kWBytes));
+    const uint32_t full_bar = bar0, empty_bar = bar0 + 8 * kLrStages, done_bar = bar0 + 16 * kLrStages;
+    uint32_t* misc = reinterpret_cast<uint32_t*>(base + kLrStages * (kSlab + kWBytes) + 8 * (2 * kLrStages + 1));
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tok0 = blockIdx.x * kT;
+    const int nk = a.HD / 64;
+    if (tid == 0) {
+        for (int s = 0; s < kLrStages; ++s) {
+            mbar_init(full_bar + 8 * s, 1);
+            mbar_init(empty_bar + 8 * s, 1);
+        }
+        mbar_init(done_bar, 1);
+        misc[1] = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(misc)),
+                     "r"(32u)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+    if (warp == 0) {
+        if (lane == 0) {
+            int armed = 0;
+            for (int k = 0; k < nk; ++k) {
+                const int s = k % kLrStages;
+                if (!mbar_wait(empty_bar + 8 * s, ((uint32_t)(k / kLrStages) & 1u) ^ 1u)) { misc[1] = 1; break; }
+                mbar_arrive_tx(full_bar + 8 * s, (uint32_t)(kSlab + kWBytes));
+                tma_load_2d(smem_u32(Xs + (size_t)s * kSlab), &tm_x, full_bar + 8 * s, k * 64, tok0);
+                tma_load_2d(smem_u32(Ws + (size_t)s * kWBytes), &tm_w, full_bar + 8 * s, k * 64, 0);
+                armed = k + 1;
+            }
+            for (int k = armed - kLrStages > 0 ? armed - kLrStages : 0; k < armed; ++k)
+                mbar_wait(full_bar + 8 * (k % kLrStages), (uint32_t)(k / kLrStages) & 1u);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kR >> 3) << 17) |
+                                   ((uint32_t)(kT >> 4) << 24);
+            bool ok = true;
+            for (int k = 0; k < nk; ++k) {
+                const int s = k % kLrStages;
+                if (!mbar_wait(full_bar + 8 * s, (uint32_t)(k / kLrStages) & 1u)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    umma_bf16(tmem, sw128_desc(smem_u32(Xs + (size_t)s * kSlab) + 32u * kk),
+                              sw128_desc(smem_u32(Ws + (size_t)s * kWBytes) + 32u * kk), idesc,
+                              (k | kk) != 0 ? 1u : 0u);
+                umma_commit(empty_bar + 8 * s);          // stage free once these MMAs are done
+            }
+            if (ok) umma_commit(done_bar);
+            else misc[1] = 1;
+        }
+        __syncwarp();
+    } else {
+        const int q = warp & 3, row = q * 32 + lane;
+        const bool ok = mbar_wait(done_bar, 0);
+        if (!ok) misc[1] = 1;
+        tc_fence_after();
+        uint32_t v[32];
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16), v);
+        tmem_wait_ld();
+        const int64_t n = (int64_t)tok0 + row;
+        if (ok && n < a.n_tokens) {
+            uint32_t hw[16], lw[16];
+#pragma unroll
+            for (int r = 0; r < kR; r += 2) {
+                const float t0 = __uint_as_float(v[r]), t1 = __uint_as_float(v[r + 1]);
+                const __nv_bfloat162 hi = __floats2bfloat162_rn(t0, t1);
+                const float2 hf = __bfloat1622float2(hi);
+                const __nv_bfloat162 lo = __floats2bfloat162_rn(__fsub_rn(t0, hf.x), __fsub_rn(t1, hf.y));
+                hw[r / 2] = *reinterpret_cast<const uint32_t*>(&hi);
+                lw[r / 2] = *reinterpret_cast<const uint32_t*>(&lo);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(a.t2 + n * 2 * kR);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) dst[k] = make_uint4(hw[4 * k], hw[4 * k + 1], hw[4 * k + 2], hw[4 * k + 3]);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) dst[4 + k] = make_uint4(lw[4 * k], lw[4 * k + 1], lw[4 * k + 2], lw[4 * k + 3]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && misc[1] && a.err) atomicExch(a.err, kErrTimeout);
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(32u) : "memory");
+    }
+}
+
+// --------------------------------------------------------------- predict
+
+constexpr int kPrStages = 2;
+constexpr int kPrThreads = 64 + 256;    // TMA warp, MMA warp, two groups of four epilogue warps
+constexpr int kStageBytes = 2 * kSlab + 2 * kSlab + kSlab + kSlab;   // xhat_h, B_h, t2, Ud_h
+
+struct PrArgs {
+    int64_t n_tokens;
+    int H, S, tiles;
+    const uint16_t* xnext;   // [N][H*D] (encode) or null (decode)
+    uint32_t* codes;         // [S][H][N][D/16]
+    uint32_t* meta;          // [S][H][N][D/G]
+    uint16_t* xhat;          // [N][H*D] out
+    float* pred_out;         // optional [N][H*D]
+    uint32_t* err;
+};
+
+// 16-byte load through L1 (a thread's consecutive vectors share sectors).
+__device__ __forceinline__ uint4 ldg_v4_l1(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+template <int G, bool ENCODE>
+__global__ void __launch_bounds__(kPrThreads, 1)
+    coral_predict_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
+                            const __grid_constant__ CUtensorMap tm_t, const __grid_constant__ CUtensorMap tm_u,
+                            PrArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    const uint32_t bar0 = smem_u32(base + kPrStages * kStageBytes);
+    const uint32_t full_bar = bar0, empty_bar = bar0 + 8 * kPrStages, tfull_bar = bar0 + 16 * kPrStages,
+                   tempty_bar = tfull_bar + 16;
+    uint32_t* misc = reinterpret_cast<uint32_t*>(base + kPrStages * kStageBytes + 8 * (2 * kPrStages + 4));
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int H = a.H, HD = H * kDh;
+    const int n_items = a.tiles * H;
+    // this CTA's items: blockIdx.x, blockIdx.x + gridDim.x, ...
+    const int my_items = n_items > (int)blockIdx.x ? (n_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    if (tid == 0) {
+        for (int s = 0; s < kPrStages; ++s) {
+            mbar_init(full_bar + 8 * s, 1);
+            mbar_init(empty_bar + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar + 8 * b, 1);
+            mbar_init(tempty_bar + 8 * b, 4);
+        }
+        misc[1] = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(misc)),
+                     "r"(256u)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+    if (warp == 0) {
+        // ---------------------------------------------------- TMA producer
+        if (lane == 0) {
+            int armed = 0;
+            for (int i = 0; i < my_items; ++i) {
+                const int item = (int)blockIdx.x + i * (int)gridDim.x;
+                const int tile = item / H, h = item % H;
+                const int s = i % kPrStages;
+                if (!mbar_wait(empty_bar + 8 * s, ((uint32_t)(i / kPrStages) & 1u) ^ 1u)) { misc[1] = 1; break; }
+                uint8_t* st = base + (size_t)s * kStageBytes;
+                mbar_arrive_tx(full_bar + 8 * s, (uint32_t)kStageBytes);
+                const uint32_t fb = full_bar + 8 * s;
+                for (int at = 0; at < 2; ++at) {
+                    tma_load_2d(smem_u32(st + at * kSlab), &tm_x, fb, h * kDh + at * 64, tile * kT);
+                    tma_load_2d(smem_u32(st + (2 + at) * kSlab), &tm_b, fb, at * 64, h * kDh);
+                }
+                tma_load_2d(smem_u32(st + 4 * kSlab), &tm_t, fb, 0, tile * kT);
+                tma_load_2d(smem_u32(st + 5 * kSlab), &tm_u, fb, 0, h * kDh);
+                armed = i + 1;
+            }
+            for (int i = armed - kPrStages > 0 ? armed - kPrStages : 0; i < armed; ++i)
+                mbar_wait(full_bar + 8 * (i % kPrStages), (uint32_t)(i / kPrStages) & 1u);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kDh >> 3) << 17) |
+                                   ((uint32_t)(kT >> 4) << 24);
+            int issued = 0;
+            for (int i = 0; i < my_items; ++i) {
+                const int s = i % kPrStages, acc = i & 1;
+                if (!mbar_wait(tempty_bar + 8 * acc, ((uint32_t)(i >> 1) & 1u) ^ 1u)) { misc[1] = 1; break; }
+                if (!mbar_wait(full_bar + 8 * s, (uint32_t)(i / kPrStages) & 1u)) { misc[1] = 1; break; }
+                tc_fence_after();
+                const uint32_t st = smem_u32(base + (size_t)s * kStageBytes);
+                const uint32_t d = tmem + (uint32_t)acc * kDh;
+#pragma unroll
+                for (int at = 0; at < 2; ++at)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_bf16(d, sw128_desc(st + at * kSlab + 32u * kk), sw128_desc(st + (2 + at) * kSlab + 32u * kk),
+                                  idesc, (at | kk) != 0 ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    umma_bf16(d, sw128_desc(st + 4 * kSlab + 32u * kk), sw128_desc(st + 5 * kSlab + 32u * kk), idesc, 1u);
+                umma_commit(empty_bar + 8 * s);        // operands free once these MMAs are done
+                umma_commit(tfull_bar + 8 * acc);
+                issued = i + 1;
+            }
+            for (int i = issued - 2 > 0 ? issued - 2 : 0; i < issued; ++i)
+                mbar_wait(tfull_bar + 8 * (i & 1), (uint32_t)(i >> 1) & 1u);
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------- epilogue
+        constexpr int CPT = G < 32 ? 32 : G;      // channels per pass (whole groups, whole TMEM loads)
+        constexpr int GPP = CPT / G;              // groups per pass
+        const int e = warp - 2, g = e >> 2, q = warp & 3;
+        const int row = q * 32 + lane;
+        const int64_t stage_rows = (int64_t)H * a.n_tokens;
+        for (int i = g; i < my_items; i += 2) {
+            const int item = (int)blockIdx.x + i * (int)gridDim.x;
+            const int tile = item / H, h = item % H;
+            if (!mbar_wait(tfull_bar + 8 * g, (uint32_t)(i >> 1) & 1u)) { misc[1] = 1; break; }
+            tc_fence_after();
+            const int64_t n = (int64_t)tile * kT + row;
+            const bool valid = n < a.n_tokens;
+            const int64_t elem0 = n * HD + (int64_t)h * kDh;
+            const int64_t rowoff = (int64_t)h * a.n_tokens + n;
+#pragma unroll 1
+            for (int c = 0; c < kDh / CPT; ++c) {
+                const uint32_t tcol = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)g * kDh + (uint32_t)(c * CPT);
+                // this pass's codes and scale/zero words of every stage
+                uint32_t code[kMaxStages][CPT / 16], meta[kMaxStages][GPP];
+                if (ENCODE) {
+                    // residual r = x_{l+1} - pred, quantised stage by stage
+                    float r[CPT];
+#pragma unroll
+                    for (int k = 0; k < CPT / 32; ++k) {
+                        uint32_t v[32];
+                        tmem_ld32(tcol + 32u * k, v);
+                        uint4 xv[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            xv[u] = valid ? ldg_v4_l1(a.xnext + elem0 + c * CPT + 32 * k + 8 * u) : make_uint4(0, 0, 0, 0);
+                        tmem_wait_ld();
+                        float pk[32];
+#pragma unroll
+                        for (int jj = 0; jj < 32; ++jj) pk[jj] = __uint_as_float(v[jj]);
+                        if (valid && a.pred_out) {
+#pragma unroll
+                            for (int jj = 0; jj < 32; jj += 4)
+                                *reinterpret_cast<float4*>(a.pred_out + elem0 + c * CPT + 32 * k + jj) =
+                                    make_float4(pk[jj], pk[jj + 1], pk[jj + 2], pk[jj + 3]);
+                        }
+                        unpack16(xv[0], xv[1], r + 32 * k);
+                        unpack16(xv[2], xv[3], r + 32 * k + 16);
+                        sub16(r + 32 * k, pk);
+                        sub16(r + 32 * k + 16, pk + 16);
+                    }
+                    for (int s = 0; s < a.S; ++s) {
+#pragma unroll
+                        for (int gi = 0; gi < GPP; ++gi) {
+                            uint32_t cw[G / 16], m;
+                            quant_stage<G, 1>(r + gi * G, s + 1 < a.S, nullptr, cw, m);
+#pragma unroll
+                            for (int w = 0; w < G / 16; ++w) code[s][gi * (G / 16) + w] = cw[w];
+                            meta[s][gi] = m;
+                            if (valid) {
+                                const int64_t srow = (int64_t)s * stage_rows + rowoff;
+                                uint32_t* cp = a.codes + srow * (kDh / 16) + (c * CPT + gi * G) / 16;
+#pragma unroll
+                                for (int w = 0; w < G / 16; ++w) cp[w] = cw[w];
+                                a.meta[srow * (kDh / G) + (c * CPT) / G + gi] = m;
+                            }
+                        }
+                    }
+                } else if (valid) {
+                    for (int s = 0; s < a.S; ++s) {
+                        const int64_t srow = (int64_t)s * stage_rows + rowoff;
+                        const uint32_t* cp = a.codes + srow * (kDh / 16) + (c * CPT) / 16;
+                        if constexpr (CPT == 64) {
+                            const uint4 cw = ldg_v4_l1(cp);
+                            code[s][0] = cw.x; code[s][1] = cw.y;
+                            code[s][2] = cw.z; code[s][3] = cw.w;
+                        } else {
+                            const uint2 cw = __ldg(reinterpret_cast<const uint2*>(cp));
+                            code[s][0] = cw.x; code[s][1] = cw.y;
+                        }
+#pragma unroll
+                        for (int gi = 0; gi < GPP; ++gi)
+                            meta[s][gi] = __ldg(a.meta + srow * (kDh / G) + (c * CPT) / G + gi);
+                    }
+                }
+                // x_hat = ((pred + d_1) + d_2) + ..., identical in encoder and decoder
+                float acc[CPT];
+#pragma unroll
+                for (int k = 0; k < CPT / 32; ++k) {
+                    uint32_t v[32];
+                    tmem_ld32(tcol + 32u * k, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj) acc[32 * k + jj] = __uint_as_float(v[jj]);
+                }
+                if (!ENCODE && valid && a.pred_out) {
+#pragma unroll
+                    for (int jj = 0; jj < CPT; jj += 4)
+                        *reinterpret_cast<float4*>(a.pred_out + elem0 + c * CPT + jj) =
+                            make_float4(acc[jj], acc[jj + 1], acc[jj + 2], acc[jj + 3]);
+                }
+                for (int s = 0; s < a.S; ++s) {
+#pragma unroll
+                    for (int w = 0; w < CPT / 16; ++w)
+                        dequant_add16(acc + 16 * w, code[s][w], meta[s][(16 * w) / G]);
+                }
+                if (valid) {
+                    uint16_t* op = a.xhat + elem0 + c * CPT;
+#pragma unroll
+                    for (int k = 0; k < CPT; k += 16) {
+                        uint4 o0, o1;
+                        pack16_bf16(acc + k, o0, o1);
+                        *reinterpret_cast<uint4*>(op + k) = o0;
+                        *reinterpret_cast<uint4*>(op + k + 8) = o1;
+                    }
+                }
+            }
+            // accumulator drained
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar + 8 * g);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && misc[1] && a.err) atomicExch(a.err, kErrTimeout);
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256u) : "memory");
+    }
+}
+
+bool encode_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+               uint32_t box_inner, uint32_t box_outer) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int G>
+cudaError_t coral_tc_g(bool encode, const CoralArgs& a, const CoralTcScratch& w, bool* launched, cudaStream_t s) {
+    const int H = a.H, HD = H * kDh;
+    const int64_t N = a.n_tokens;
+    CUtensorMap tx, tw, tb, tt, tu;
+    if (!encode_2d(&tx, a.xprev, (uint64_t)HD, (uint64_t)N, (uint64_t)HD * 2, 64, kT)) return cudaSuccess;
+    if (!encode_2d(&tw, w.wt, (uint64_t)HD, (uint64_t)kR, (uint64_t)HD * 2, 64, kR)) return cudaSuccess;
+    if (!encode_2d(&tb, a.B, (uint64_t)kDh, (uint64_t)HD, (uint64_t)kDh * 2, 64, kT)) return cudaSuccess;
+    if (!encode_2d(&tt, w.t2, (uint64_t)(2 * kR), (uint64_t)N, (uint64_t)(4 * kR), 64, kT)) return cudaSuccess;
+    if (!encode_2d(&tu, w.ud, (uint64_t)(2 * kR), (uint64_t)HD, (uint64_t)(4 * kR), 64, kT)) return cudaSuccess;
+    coral_prep_kernel<<<(unsigned)((HD + 127) / 128), 128, 0, s>>>(a.W, a.U, HD, w.wt, w.ud);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int tiles = (int)((N + kT - 1) / kT);
+    const size_t lr_smem = (size_t)kLrStages * (kSlab + kR * 128) + 8 * (2 * kLrStages + 1) + 32 + 1024;
+    // at least 116 KB so that one CTA (and one TMEM allocation) lives per SM
+    const size_t lr_req = lr_smem < 118784 ? 118784 : lr_smem;
+    e = cudaFuncSetAttribute(coral_lowrank_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lr_req);
+    if (e != cudaSuccess) return e;
+    LrArgs la{N, HD, w.t2, w.err};
+    coral_lowrank_tc_kernel<<<(unsigned)tiles, kLrThreads, lr_req, s>>>(tx, tw, la);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const size_t pr_smem = (size_t)kPrStages * kStageBytes + 8 * (2 * kPrStages + 4) + 32 + 1024;
+    auto kern = encode ? coral_predict_tc_kernel<G, true> : coral_predict_tc_kernel<G, false>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pr_smem);
+    if (e != cudaSuccess) return e;
+    PrArgs pa;
+    pa.n_tokens = N; pa.H = H; pa.S = a.S; pa.tiles = tiles;
+    pa.xnext = a.xnext; pa.codes = a.codes; pa.meta = a.meta; pa.xhat = a.xhat; pa.pred_out = a.pred_out;
+    pa.err = w.err;
+    const int items = tiles * H;
+    const int grid = items < sm_count() ? items : sm_count();
+    kern<<<(unsigned)grid, kPrThreads, pr_smem, s>>>(tx, tb, tt, tu, pa);
+    if ((e = cudaGetLastError()) == cudaSuccess) *launched = true;
+    return e;
+}
+
+}  // namespace
+
+size_t coral_tc_scratch_bytes(int H, int64_t n_tokens) {
+    const size_t HD = (size_t)H * kDh, N = (size_t)(n_tokens > 0 ? n_tokens : 1);
+    auto a256 = [](size_t v) { return (v + 255) & ~(size_t)255; };
+    return a256(N * 2 * kR * 2) + a256((size_t)kR * HD * 2) + a256(HD * 2 * kR * 2) + 256;
+}
+
+cudaError_t launch_coral_tc(int D, int G, bool encode, const CoralArgs& a, const CoralTcScratch& w, bool* launched,
+                            cudaStream_t s) {
+    *launched = false;
+    if (D != kDh || a.R != kR || !a.xprev || a.n_tokens == 0) return cudaSuccess;
+    auto al = [](const void* p, uintptr_t m) { return (reinterpret_cast<uintptr_t>(p) & (m - 1)) == 0; };
+    if (!al(a.xprev, 16) || !al(a.B, 16) || !al(w.t2, 128) || !al(w.wt, 128) || !al(w.ud, 128)) return cudaSuccess;
+    // the epilogue moves 16-byte vectors of x_{l+1}, x_hat, codes and the prediction
+    if (!al(a.xnext, 16) || !al(a.xhat, 16) || !al(a.codes, 16) || !al(a.pred_out, 16)) return cudaSuccess;
+    switch (G) {
+        case 16: return coral_tc_g<16>(encode, a, w, launched, s);
+        case 32: return coral_tc_g<32>(encode, a, w, launched, s);
+        case 64: return coral_tc_g<64>(encode, a, w, launched, s);
+        default: return cudaSuccess;
+    }
+}
+
+}  // namespace qvg

@@ -14,7 +14,8 @@
 // The mean of a cluster is rounded as the plain definition does it: the
 // quotient of the exact sum by the count rounded to double precision (53
 // significant bits, nearest-even), then that double rounded to bf16
-// (nearest-even).  Both roundings are done on integers here.
+// (nearest-even).  Both roundings are decided with integer comparisons here
+// (valid for means of magnitude 2^-84 .. 2^16).
 #pragma once
 
 #include <cstdint>
@@ -82,43 +83,59 @@ __device__ __forceinline__ int clz128(u128 v) {
     return hi ? __clzll(hi) : 64 + __clzll(lo);
 }
 
-// bf16 bits of bf16_rn(f64_rn(I * 2^-52 / cnt)), cnt >= 1.
+// U * 2^sh compared with V * 2^sv (U, V unsigned 128-bit, shifts may be
+// negative); returns -1, 0 or 1.  Operands stay below 2^120.
+__device__ __forceinline__ int cmp_scaled(u128 U, int sh, u128 V, int sv) {
+    const int m = sh < sv ? sh : sv;
+    const u128 a = U << (sh - m), b = V << (sv - m);
+    return a > b ? 1 : (a < b ? -1 : 0);
+}
+
+// bf16 bits of bf16_rn(f64_rn(I * 2^-52 / cnt)), cnt >= 1, from one fp32
+// estimate and exact 128-bit comparisons (no division of the wide integer).
+// q = U * 2^-52 / cnt (U = |I|) lies in a
+// binade [2^ex, 2^(ex+1)) found from an fp32 estimate and confirmed exactly;
+// there the bf16 values are k * 2^(ex-7), k = 128..256, and the result is
+// one of the two neighbours of q.  With k0 = floor of the estimate of
+// q / 2^(ex-7) and mid = (2 k0 + 1) * 2^(ex-8) (when q lies near mid, k0 is
+// exact; otherwise either neighbouring midpoint is far), the side of q relative to mid
+// is the sign of  U - (2 k0 + 1) * cnt * 2^(ex + 44).  A q within half a
+// double ulp of mid (|q - mid| <= 2^(ex-53)) rounds to mid in double
+// precision first and then to the even neighbour.
 __device__ __forceinline__ uint16_t mean_bf16_bits(i128 I, uint32_t cnt) {
     if (I == 0) return 0;
     const bool neg = I < 0;
-    u128 U = neg ? (u128)(-I) : (u128)I;
+    const u128 U = neg ? (u128)(-I) : (u128)I;
     const int bl = 128 - clz128(U);
-    const int k = bl < 86 ? 86 - bl : 0;   // scale so the quotient has >= 54 bits
-    U <<= k;
-    // 128-bit by 32-bit long division, 32 bits at a time
-    uint64_t rem = 0;
-    u128 q = 0;
-#pragma unroll
-    for (int li = 3; li >= 0; --li) {
-        const uint64_t cur = (rem << 32) | (uint64_t)(uint32_t)(U >> (32 * li));
-        const uint64_t ql = cur / cnt;
-        rem = cur - ql * cnt;
-        q |= (u128)ql << (32 * li);
+    const int sh = bl > 24 ? bl - 24 : 0;
+    const float qf = __fdiv_rn((float)(uint32_t)(U >> sh), (float)cnt);   // q ~ qf * 2^(sh-52)
+    int ex;
+    frexpf(qf, &ex);                                   // qf in [2^(ex-1), 2^ex)
+    ex = ex - 1 + sh - 52;                             // estimated binade of q
+    // exact binade: 2^ex <= q < 2^(ex+1)  <=>  cnt * 2^(ex+52) <= U < cnt * 2^(ex+53)
+    if (cmp_scaled(U, 0, (u128)cnt, ex + 52) < 0) --ex;
+    else if (cmp_scaled(U, 0, (u128)cnt, ex + 53) >= 0) ++ex;
+    // k estimate of q / 2^(ex-7), in [128, 256)
+    const float kq = ldexpf(qf, sh - 52 - (ex - 7));
+    const int k0 = (int)floorf(kq);                  // q/2^(ex-7) lies within 2^-12 of kq
+    const u128 Mc = (u128)(uint32_t)(2 * k0 + 1) * (u128)cnt;
+    // side of q relative to mid: U vs Mc * 2^(ex - 8 + 52)
+    const int side = cmp_scaled(U, 0, Mc, ex + 44);
+    // tie: |U - Mc * 2^(ex+44)| <= cnt * 2^(ex-1)   (both sides times 2^52)
+    bool tie;
+    {
+        const int m = (ex - 1) < 0 ? (ex - 1) : 0;     // common unit 2^m (m <= 0)
+        const u128 a = U << (0 - m), b = Mc << (ex + 44 - m);
+        const u128 d = a > b ? a - b : b - a;
+        tie = d <= ((u128)cnt << (ex - 1 - m));
     }
-    // first rounding: to 53 significant bits, nearest-even, remainder sticky
-    int sh = (128 - clz128(q)) - 53;
-    const u128 low = q & (((u128)1 << sh) - 1);
-    const u128 half = (u128)1 << (sh - 1);
-    uint64_t q53 = (uint64_t)(q >> sh);
-    if (low > half || (low == half && (rem != 0 || (q53 & 1)))) ++q53;
-    if (q53 >> 53) { q53 >>= 1; ++sh; }
-    // second rounding: the double to 8 significant bits, nearest-even
-    const uint64_t low2 = q53 & ((1ull << 45) - 1);
-    uint32_t m8 = (uint32_t)(q53 >> 45);
-    int sh2 = 45;
-    if (low2 > (1ull << 44) || (low2 == (1ull << 44) && (m8 & 1))) ++m8;
-    if (m8 == 256) { m8 = 128; ++sh2; }
-    // value = m8 * 2^(sh + sh2 - 52 - k), m8 in [128, 255]
-    const int E = 7 + sh + sh2 - 52 - k;
+    int k = (tie || side == 0) ? ((k0 & 1) ? k0 + 1 : k0) : (side > 0 ? k0 + 1 : k0);
+    int e = ex;
+    if (k >= 256) { k >>= 1; ++e; }
     uint32_t bits;
-    if (E + 127 >= 255) bits = 0x7F80u;          // outside the supported range
-    else if (E + 127 <= 0) bits = 0u;
-    else bits = ((uint32_t)(E + 127) << 7) | (m8 & 0x7Fu);
+    if (e + 127 >= 255) bits = 0x7F80u;
+    else if (e + 127 <= 0) bits = 0u;
+    else bits = ((uint32_t)(e + 127) << 7) | ((uint32_t)k & 0x7Fu);
     return (uint16_t)(bits | (neg ? 0x8000u : 0u));
 }
 

@@ -78,7 +78,21 @@ struct CoralArgs {
     uint16_t* xhat;          // [N][H*D] out
     float* pred_out;         // optional [N][H*D]
     float* lowrank;          // workspace [N][R]
+    void* workspace;         // the whole workspace (tensor-core path)
+    size_t workspace_bytes;
 };
+
+// Scratch of the tensor-core cross-layer path, carved from the workspace.
+struct CoralTcScratch {
+    uint16_t* t2;      // [N][64] bf16: low-rank projection as (hi, lo) pairs
+    uint16_t* wt;      // [32][H*D] bf16: W transposed
+    uint16_t* ud;      // [H*D][64] bf16: [U | U]
+    uint32_t* err;     // error word (0 = none)
+};
+
+// Bytes of CoralTcScratch for H heads of 128 and n_tokens tokens (including
+// the error word at the end).
+size_t coral_tc_scratch_bytes(int H, int64_t n_tokens);
 
 // Each launcher returns cudaSuccess or the launch error; shapes are
 // validated by the caller.
@@ -95,5 +109,9 @@ cudaError_t launch_update(int D, const UpdateArgs& a, cudaStream_t s);
 cudaError_t launch_set_chunk(int64_t* chunk_offset, int32_t* chunk_version, int idx, int64_t begin,
                              int64_t end, int32_t version, cudaStream_t s);
 cudaError_t launch_coral(int D, int G, bool encode, const CoralArgs& a, cudaStream_t s);
+// tcgen05 cross-layer path (D = 128, rank 32, G <= 64, a previous layer);
+// *launched = false (cudaSuccess) when outside that set.
+cudaError_t launch_coral_tc(int D, int G, bool encode, const CoralArgs& a, const CoralTcScratch& w, bool* launched,
+                            cudaStream_t s);
 
 }  // namespace qvg

@@ -554,14 +554,23 @@ __global__ void __launch_bounds__(kThreads, 3) kmeans_sum_kernel(UpdateArgs a) {
                 tot[2 * q + 1] += bf16_to_i128_units(wv[q] >> 16);
             }
         }
+#pragma unroll
+        for (int o = LPR; o < 32; o <<= 1)
+#pragma unroll
+            for (int d = 0; d < 8; ++d) tot[d] += shfl_xor_i128(tot[d], o);
     } else {
+        // row slots first, in int32 (at most kPieceTokens terms of <= 2^22 each)
+#pragma unroll
+        for (int o = LPR; o < 32; o <<= 1)
+#pragma unroll
+            for (int d = 0; d < 8; ++d) {
+                w1[d] += __shfl_xor_sync(0xffffffffu, w1[d], o);
+                w2[d] += __shfl_xor_sync(0xffffffffu, w2[d], o);
+                w3[d] += __shfl_xor_sync(0xffffffffu, w3[d], o);
+            }
 #pragma unroll
         for (int d = 0; d < 8; ++d) tot[d] = windows_to_i128(w1[d], w2[d], w3[d]);
     }
-#pragma unroll
-    for (int o = LPR; o < 32; o <<= 1)
-#pragma unroll
-        for (int d = 0; d < 8; ++d) tot[d] += shfl_xor_i128(tot[d], o);
     if (slot != 0) return;
     if (pc.w) {
         uint16_t r[8];

@@ -4,12 +4,14 @@
 // token's centroid) and sec. 2B items 1-3 (re-quantise the residual stage by
 // stage; decode = dequantise, sum the stages, add the centroid back).
 //
-// Both kernels stream HBM.  A thread owns one quantisation group of a token
-// row (G channels; two threads share a group of 128), so the group's
-// min/max, scale, zero-point and reciprocal are formed once per group; its
-// CPT = min(G, 64) channels arrive as 16-byte bf16 vectors and its codes
-// leave as one vector store per stage.  Every load of a row is issued before
-// any of its arithmetic.
+// Both kernels stream HBM.  In the encoder a thread owns one quantisation
+// group of a token row (G channels; two threads share a group of 128), so the
+// group's min/max, scale, zero-point and reciprocal are formed once per
+// group; its CPT = min(G, 64) channels arrive as 16-byte bf16 vectors and its
+// codes leave as one vector store per stage.  In the write-heavy decoder a
+// thread owns 16 consecutive channels, so a warp's stores cover whole
+// contiguous row segments.  Every load of a row is issued before any of its
+// arithmetic.
 #include "common.cuh"
 #include "kernels.h"
 #include "prq16.cuh"
@@ -20,9 +22,20 @@ namespace {
 
 constexpr int kThreads = 256;
 
+constexpr int kDecRowsPerThread = 2;   // decoder: rows per thread (loads hoisted)
+
+// Decoder mapping: a thread owns 16 consecutive channels (one code word per
+// stage), so each warp store instruction writes whole contiguous row segments.
+template <int D>
+struct Map16 {
+    static constexpr int TPR = D / 16;                   // threads per row
+    static constexpr int RPW = 32 / TPR;                 // rows per warp step
+    static constexpr int RPS = RPW * (kThreads / 32);    // rows per CTA step
+};
+
 template <int D, int G>
 struct GMap {
-    static constexpr int CPT = G < 64 ? G : 64;   // channels per thread
+    static constexpr int CPT = G < 32 ? G : 32;   // channels per thread
     static constexpr int TPG = G / CPT;           // threads per group (1 or 2)
     static constexpr int TPR = D / CPT;           // threads per row
     static constexpr int RPW = 32 / TPR;          // rows per warp
@@ -59,7 +72,7 @@ __device__ __forceinline__ void load_words(const uint32_t* p, uint32_t* w) {
 }
 
 template <int D, int G, bool HAS_C>
-__global__ void __launch_bounds__(kThreads, 2) prq_encode_kernel(EncodeArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) prq_encode_kernel(EncodeArgs a) {
     using M = GMap<D, G>;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t = lane % M::TPR;
@@ -70,11 +83,13 @@ __global__ void __launch_bounds__(kThreads, 2) prq_encode_kernel(EncodeArgs a) {
     float r[M::CPT];
     {
         uint4 xv[M::NV], cv[M::NV];
+        // the cluster id first: the centroid loads depend on it and then
+        // overlap the token loads
+        const int id = (HAS_C && valid) ? min((int)a.ids[(int64_t)h * a.cap + a.tok_offset + n], a.C - 1) : 0;
         const uint16_t* xp = a.x + (int64_t)h * a.head_stride + (valid ? n : 0) * a.token_stride + t * M::CPT;
 #pragma unroll
         for (int k = 0; k < M::NV; ++k) xv[k] = valid ? ldg_v4(xp + 8 * k) : make_uint4(0, 0, 0, 0);
         if (HAS_C) {
-            const int id = valid ? min((int)a.ids[(int64_t)h * a.cap + a.tok_offset + n], a.C - 1) : 0;
             const uint16_t* cp = a.cent + ((int64_t)h * a.C + id) * D + t * M::CPT;
 #pragma unroll
             for (int k = 0; k < M::NV; ++k) cv[k] = valid ? __ldg(reinterpret_cast<const uint4*>(cp + 8 * k)) : make_uint4(0, 0, 0, 0);
@@ -113,8 +128,9 @@ __device__ __forceinline__ int chunk_of(const int64_t* offs, int n_chunks, int64
 }
 
 template <int D, int G, bool HAS_C, bool VERSIONED>
-__global__ void __launch_bounds__(kThreads, 2) prq_decode_kernel(DecodeArgs a) {
-    using M = GMap<D, G>;
+__global__ void __launch_bounds__(kThreads, 4) prq_decode_kernel(DecodeArgs a) {
+    using M = Map16<D>;
+    constexpr int NR = kDecRowsPerThread;
     extern __shared__ int64_t chunk_smem[];   // VERSIONED: offsets[n_chunks + 1], versions[n_chunks]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t = lane % M::TPR;
@@ -125,61 +141,61 @@ __global__ void __launch_bounds__(kThreads, 2) prq_decode_kernel(DecodeArgs a) {
         for (int i = threadIdx.x; i < a.n_chunks; i += kThreads) vers[i] = a.chunk_version[i];
         __syncthreads();
     }
-    const int64_t i = (int64_t)blockIdx.x * M::RPC + (int64_t)warp * M::RPW + lane / M::TPR;
-    if (i >= a.tok_end - a.tok_begin) return;
-    const int64_t n = a.tok_begin + i;
-    const int64_t row = (int64_t)h * a.cap + n;
+    const int64_t n_rows = a.tok_end - a.tok_begin;
+    const int64_t base = (int64_t)blockIdx.x * M::RPS * NR + (int64_t)warp * M::RPW + lane / M::TPR;
     const int64_t stage_rows = (int64_t)a.H * a.cap;
-    // codes and scale/zero words of every stage, then the centroid
-    uint32_t code[kMaxStages][M::NW], meta[kMaxStages];
+    constexpr int WPR = D / 16, MPR = D / G;
+    const int mi = (t * 16) / G;
+
+    int64_t ii[NR];
+    bool ok[NR];
+    int id[NR];
+    uint32_t code[NR][kMaxStages], meta[NR][kMaxStages];
 #pragma unroll
-    for (int s = 0; s < kMaxStages; ++s) {
-        if (s < a.S) {
-            const int64_t srow = (int64_t)s * stage_rows + row;
-            load_words<M::NW>(a.codes + srow * (D / 16) + t * M::NW, code[s]);
-            meta[s] = __ldg(a.meta + srow * (D / G) + t / M::TPG);
+    for (int k = 0; k < NR; ++k) {
+        ii[k] = base + (int64_t)k * M::RPS;
+        ok[k] = ii[k] < n_rows;
+        const int64_t row = (int64_t)h * a.cap + a.tok_begin + ii[k];
+        id[k] = 0;
+        if (HAS_C && ok[k]) id[k] = a.ids[row];
+#pragma unroll
+        for (int s = 0; s < kMaxStages; ++s) {
+            code[k][s] = 0;
+            meta[k][s] = 0;
+            if (s < a.S && ok[k]) {
+                const int64_t srow = (int64_t)s * stage_rows + row;
+                code[k][s] = __ldg(a.codes + srow * WPR + t);
+                meta[k][s] = __ldg(a.meta + srow * MPR + mi);
+            }
         }
     }
-    // centroid row, then the output in runs of up to 32 channels (keeps the
-    // live registers down)
-    constexpr int HC = M::CPT < 32 ? M::CPT : 32;   // channels per run
-    const uint16_t* cp = nullptr;
-    if (HAS_C) {
-        const uint16_t* cbase = a.cent;
-        if (VERSIONED) {
-            const int32_t* vers = reinterpret_cast<const int32_t*>(chunk_smem + a.n_chunks + 1);
-            cbase += (int64_t)vers[chunk_of(chunk_smem, a.n_chunks, n)] * a.H * a.C * D;
-        }
-        const int id = min((int)a.ids[row], a.C - 1);
-        cp = cbase + ((int64_t)h * a.C + id) * D + t * M::CPT;
-    }
-    uint16_t* op = a.out + (int64_t)h * a.out_head_stride + i * a.out_token_stride + t * M::CPT;
 #pragma unroll
-    for (int hc = 0; hc < M::CPT; hc += HC) {
-        float acc[HC];
+    for (int k = 0; k < NR; ++k) {
+        if (!ok[k]) continue;
+        float acc[16];
         if (HAS_C) {
-            uint4 cv[HC / 8];
-#pragma unroll
-            for (int k = 0; k < HC / 8; ++k) cv[k] = __ldg(reinterpret_cast<const uint4*>(cp + hc + 8 * k));
-#pragma unroll
-            for (int k = 0; k < HC / 8; k += 2) unpack16(cv[k], cv[k + 1], acc + 8 * k);
+            const uint16_t* cbase = a.cent;
+            if (VERSIONED) {
+                const int32_t* vers = reinterpret_cast<const int32_t*>(chunk_smem + a.n_chunks + 1);
+                const int c = chunk_of(chunk_smem, a.n_chunks, a.tok_begin + ii[k]);
+                cbase += (int64_t)vers[c] * a.H * a.C * D;
+            }
+            const uint16_t* cr = cbase + ((int64_t)h * a.C + min(id[k], a.C - 1)) * D + t * 16;
+            const uint4 c0 = __ldg(reinterpret_cast<const uint4*>(cr));
+            const uint4 c1 = __ldg(reinterpret_cast<const uint4*>(cr + 8));
+            unpack16(c0, c1, acc);
         } else {
 #pragma unroll
-            for (int k = 0; k < HC; ++k) acc[k] = 0.0f;
+            for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
         }
 #pragma unroll
         for (int s = 0; s < kMaxStages; ++s)
-            if (s < a.S) {
-#pragma unroll
-                for (int w = 0; w < HC / 16; ++w) dequant_add16(acc + 16 * w, code[s][hc / 16 + w], meta[s]);
-            }
-#pragma unroll
-        for (int k = 0; k < HC / 8; k += 2) {
-            uint4 o0, o1;
-            pack16_bf16(acc + 8 * k, o0, o1);
-            stg_v4_stream(op + hc + 8 * k, o0);
-            stg_v4_stream(op + hc + 8 * k + 8, o1);
-        }
+            if (s < a.S) dequant_add16(acc, code[k][s], meta[k][s]);
+        uint4 o0, o1;
+        pack16_bf16(acc, o0, o1);
+        uint16_t* op = a.out + (int64_t)h * a.out_head_stride + ii[k] * a.out_token_stride + t * 16;
+        stg_v4_stream(op, o0);
+        stg_v4_stream(op + 8, o1);
     }
 }
 
@@ -195,10 +211,11 @@ cudaError_t encode_dg(const EncodeArgs& a, cudaStream_t s) {
 
 template <int D, int G>
 cudaError_t decode_dg(const DecodeArgs& a, cudaStream_t s) {
-    using M = GMap<D, G>;
+    using M = Map16<D>;
     const int64_t rows = a.tok_end - a.tok_begin;
     if (rows <= 0) return cudaSuccess;
-    dim3 grid((unsigned)((rows + M::RPC - 1) / M::RPC), (unsigned)a.H);
+    const int64_t rows_per_cta = (int64_t)M::RPS * kDecRowsPerThread;
+    dim3 grid((unsigned)((rows + rows_per_cta - 1) / rows_per_cta), (unsigned)a.H);
     if (a.C > 0 && a.chunk_offset) {
         const size_t smem = sizeof(int64_t) * (a.n_chunks + 1) + sizeof(int32_t) * a.n_chunks;
         prq_decode_kernel<D, G, true, true><<<grid, kThreads, smem, s>>>(a);

@@ -42,6 +42,7 @@ def gpu_layer(qvg, cfg, pred, xprev_dev, xnext_dev, N, encode=True, codes=None, 
     else:
         qvg.coral_predict_decode(cfg, pred, xprev_dev, N, codes, meta, xh, pout, ws)
     torch.cuda.synchronize()
+    assert qvg.qvg_fit_stats(cfg, N, ws)[3] == 0      # no bounded wait expired
     return codes, meta, xh, pout
 
 
@@ -51,10 +52,14 @@ def predictor(qvg, B, U, W):
     return p, dev
 
 
-@pytest.mark.parametrize("N,R", [(300, 32), (64, 16), (129, 0)])
-def test_coral_chain_staged_parity(qvg, oracle, N, R):
+# (tokens, rank, heads, group size): rank 32 runs the tcgen05 path (token
+# tiles of 128 with a ragged last tile), the other ranks the general one
+@pytest.mark.parametrize("N,R,H,G", [(300, 32, 4, None), (64, 16, 4, None), (129, 0, 4, None),
+                                     (300, 32, 4, 16), (300, 32, 4, 64), (1100, 32, 8, None)])
+def test_coral_chain_staged_parity(qvg, oracle, N, R, H, G):
     wl = WL.CORAL
-    H, D, S, G, L = 4, wl.head_dim, wl.stages, wl.group_size, 4
+    S, D, L = wl.stages, wl.head_dim, 4
+    G = G or wl.group_size
     small = WL.Workload(**{**wl.__dict__, "heads": H, "tokens": N, "layers": L, "rank": max(R, 16)})
     xs = SY.coral_layers(small, SY.K_TENSOR, 0, N)              # [L][N][H*D]
     cfg = qvg.config(H, D, 0, 0, S, G)
