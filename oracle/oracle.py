@@ -49,9 +49,9 @@ def lib():
         L.or_assign.argtypes = [P, I64, I32, P, I32, P, P]
         L.or_update.argtypes = [P, I64, I32, P, I32, P, P]
         L.or_fit.argtypes = [P, I64, I32, I32, I32, P, P, P]
-        L.or_prq_encode.argtypes = [P, I64, I32, P, P, I32, I32, P, P]
-        L.or_decode.argtypes = [P, P, P, P, I64, I32, I32, I32, P]
-        L.or_stream.argtypes = [P, I64, I32, I32, I32, I32, I32, I32, I32, P, P, P, P, P]
+        L.or_prq_encode.argtypes = [P, I64, I32, P, P, I32, I32, I32, P, P]
+        L.or_decode.argtypes = [P, P, P, P, I64, I32, I32, I32, I32, P]
+        L.or_stream.argtypes = [P, I64, I32, I32, I32, I32, I32, I32, I32, I32, P, P, P, P, P]
         L.or_stream.restype = I32
         L.or_coral_predict.argtypes = [P, I64, I32, I32, P, P, P, I32, P]
         L.or_coral_encode_layer.argtypes = [P, P, I64, I32, I32, P, P, P, I32, P, I32, I32, P, P, P, P]
@@ -126,41 +126,42 @@ def fit(x, C, T, warm=None):
 
 # --------------------------------------------------------------------- PRQ --
 
-def prq_encode(x, cent, ids, S, G):
-    """codes [S][N][D/16] uint32, meta [S][N][D/G] uint32 (lo = fp16 scale,
-    hi = fp16 zero)."""
+def prq_encode(x, cent, ids, S, G, b=2):
+    """codes [S][N][D*b/32] uint32 (element e at bits b*e of its row, least
+    significant first), meta [S][N][D/G] uint32 (lo = fp16 scale, hi = fp16
+    zero).  b = 2 (QVG) or 4 (the PRQ_INT4 variant)."""
     x = _c(x, np.uint16)
     N, D = x.shape
-    codes = np.empty((S, N, D // 16), np.uint32)
+    codes = np.empty((S, N, D * b // 32), np.uint32)
     meta = np.empty((S, N, D // G), np.uint32)
     c = None if cent is None else _c(cent, np.uint16)
     i = None if ids is None else _c(ids, np.int32)
-    lib().or_prq_encode(_p(x), N, D, _p(c), _p(i), S, G, _p(codes), _p(meta))
+    lib().or_prq_encode(_p(x), N, D, _p(c), _p(i), S, G, b, _p(codes), _p(meta))
     return codes, meta
 
 
-def decode(codes, meta, ids, cent, G):
+def decode(codes, meta, ids, cent, G, b=2):
     codes = _c(codes, np.uint32)
     meta = _c(meta, np.uint32)
     S, N, W = codes.shape
-    D = W * 16
+    D = W * 32 // b
     out = np.empty((N, D), np.uint16)
     c = None if cent is None else _c(cent, np.uint16)
     i = None if ids is None else _c(ids, np.int32)
-    lib().or_decode(_p(codes), _p(meta), _p(i), _p(c), N, D, S, G, _p(out))
+    lib().or_decode(_p(codes), _p(meta), _p(i), _p(c), N, D, S, G, b, _p(out))
     return out
 
 
-def stream(x, chunk, steps, refit_every, C, T, S, G):
+def stream(x, chunk, steps, refit_every, C, T, S, G, b=2):
     x = _c(x, np.uint16)
     D = x.shape[1]
     Ntot = chunk * steps
     versions = np.zeros((steps, C, D), np.uint16)
     cver = np.empty(steps, np.int32)
     ids = np.empty(Ntot, np.int32)
-    codes = np.empty((S, Ntot, D // 16), np.uint32)
+    codes = np.empty((S, Ntot, D * b // 32), np.uint32)
     meta = np.empty((S, Ntot, D // G), np.uint32)
-    nv = lib().or_stream(_p(x), chunk, steps, refit_every, D, C, T, S, G, _p(versions),
+    nv = lib().or_stream(_p(x), chunk, steps, refit_every, D, C, T, S, G, b, _p(versions),
                          _p(cver), _p(ids), _p(codes), _p(meta))
     return versions[:nv], cver, ids, codes, meta
 

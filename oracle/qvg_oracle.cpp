@@ -189,11 +189,16 @@ void or_fit(const uint16_t* x, int64_t N, int D, int C, int T, const uint16_t* w
 
 // ---------------------------------------------------- PRQ: the encoder -----
 
-// One stage of 2-bit asymmetric group quantisation of the fp32 residual r
-// (length D, groups of G), in place: r <- r - deq.  Writes D/16 code words and
-// D/G meta words (low half = fp16 scale, high half = fp16 zero-point).
-static void quantize_stage(float* r, int D, int G, uint32_t* codes, uint32_t* meta) {
-    for (int w = 0; w < D / 16; ++w) codes[w] = 0;
+// One stage of b-bit asymmetric group quantisation of the fp32 residual r
+// (length D, groups of G), in place: r <- r - deq.  L = 2^b - 1 levels above
+// the zero-point: s = fp16(range / L), q = clamp(rint((r - z) / s), 0, L).
+// b = 2 is the QVG codec (sec. 2B); b = 4 is the Study's PRQ_INT4 variant,
+// read as the same scheme with 15 steps.  Writes D*b/32 code words (element e
+// at bits b*e of the row, least significant first) and D/G meta words (low
+// half = fp16 scale, high half = fp16 zero-point).
+static void quantize_stage(float* r, int D, int G, int b, uint32_t* codes, uint32_t* meta) {
+    const int L = (1 << b) - 1;
+    for (int w = 0; w < D * b / 32; ++w) codes[w] = 0;
     for (int g = 0; g < D / G; ++g) {
         float mn = r[g * G], mx = r[g * G];
         for (int j = 1; j < G; ++j) {
@@ -206,7 +211,7 @@ static void quantize_stage(float* r, int D, int G, uint32_t* codes, uint32_t* me
         mn = mn + 0.0f;
         mx = mx + 0.0f;
         float range = mx - mn;
-        float s32 = range / 3.0f;
+        float s32 = range / (float)L;
         uint16_t sh = to_f16(s32), zh = to_f16(mn);
         float s = f16_float(sh), z = f16_float(zh);
         float inv = (s != 0.0f) ? 1.0f / s : 0.0f;
@@ -215,19 +220,20 @@ static void quantize_stage(float* r, int D, int G, uint32_t* codes, uint32_t* me
             int e = g * G + j;
             float t = (r[e] - z) * inv;
             float qf = std::nearbyint(t);
-            int q = qf < 0.0f ? 0 : (qf > 3.0f ? 3 : (int)qf);
+            int q = qf < 0.0f ? 0 : (qf > (float)L ? L : (int)qf);
             float deq = (float)q * s + z;          // q*s is exact: one rounding
             r[e] = r[e] - deq;
-            codes[e / 16] |= (uint32_t)q << (2 * (e % 16));
+            codes[(e * b) / 32] |= (uint32_t)q << ((e * b) % 32);
         }
     }
 }
 
-// QVG encode of one head: r0 = x - c[id] (fp32), then S stages (PRQ items
-// 1-2).  cent/ids may be null (no smoothing, C = 0).
-// codes: [S][N][D/16]; meta: [S][N][D/G].
+// QVG encode of one head: r0 = x - c[id] (fp32), then S stages of b-bit
+// codes (PRQ items 1-2).  cent/ids may be null (no smoothing, C = 0).
+// codes: [S][N][D*b/32]; meta: [S][N][D/G].
 void or_prq_encode(const uint16_t* x, int64_t N, int D, const uint16_t* cent,
-                   const int32_t* ids, int S, int G, uint32_t* codes, uint32_t* meta) {
+                   const int32_t* ids, int S, int G, int b, uint32_t* codes, uint32_t* meta) {
+    const int W = D * b / 32;
     std::vector<float> r(D);
     for (int64_t n = 0; n < N; ++n) {
         for (int i = 0; i < D; ++i) {
@@ -236,14 +242,14 @@ void or_prq_encode(const uint16_t* x, int64_t N, int D, const uint16_t* cent,
             r[i] = xv - cv;
         }
         for (int s = 0; s < S; ++s)
-            quantize_stage(r.data(), D, G, codes + ((int64_t)s * N + n) * (D / 16),
+            quantize_stage(r.data(), D, G, b, codes + ((int64_t)s * N + n) * W,
                            meta + ((int64_t)s * N + n) * (D / G));
     }
 }
 
-// Dequantised contribution of one stage for element e of a row.
-static float stage_value(const uint32_t* codes, const uint32_t* meta, int e, int G) {
-    uint32_t q = (codes[e / 16] >> (2 * (e % 16))) & 3u;
+// Dequantised contribution of one stage for element e of a row (b-bit codes).
+static float stage_value(const uint32_t* codes, const uint32_t* meta, int e, int G, int b) {
+    uint32_t q = (codes[(e * b) / 32] >> ((e * b) % 32)) & ((1u << b) - 1u);
     uint32_t m = meta[e / G];
     float s = f16_float((uint16_t)(m & 0xFFFF));
     float z = f16_float((uint16_t)(m >> 16));
@@ -252,13 +258,14 @@ static float stage_value(const uint32_t* codes, const uint32_t* meta, int e, int
 
 // QVG decode of one head (PRQ item 3): x_hat = bf16(((c + d1) + d2) + ...).
 void or_decode(const uint32_t* codes, const uint32_t* meta, const int32_t* ids,
-               const uint16_t* cent, int64_t N, int D, int S, int G, uint16_t* out) {
+               const uint16_t* cent, int64_t N, int D, int S, int G, int b, uint16_t* out) {
+    const int W = D * b / 32;
     for (int64_t n = 0; n < N; ++n) {
         for (int i = 0; i < D; ++i) {
             float acc = cent ? bf16_float(cent[(int64_t)ids[n] * D + i]) : 0.0f;
             for (int s = 0; s < S; ++s)
-                acc = acc + stage_value(codes + ((int64_t)s * N + n) * (D / 16),
-                                        meta + ((int64_t)s * N + n) * (D / G), i, G);
+                acc = acc + stage_value(codes + ((int64_t)s * N + n) * W,
+                                        meta + ((int64_t)s * N + n) * (D / G), i, G, b);
             out[n * D + i] = to_bf16((double)acc);
         }
     }
@@ -270,13 +277,14 @@ void or_decode(const uint32_t* codes, const uint32_t* meta, const int32_t* ids,
 // table version is pushed; otherwise its tokens are assigned to the latest
 // table.  Then the chunk is encoded against its version.
 // versions: [steps][C][D] (only the first n_versions used); chunk_version:
-// [steps]; codes [S][steps*chunk][D/16], meta [S][steps*chunk][D/G].
+// [steps]; codes [S][steps*chunk][D*b/32], meta [S][steps*chunk][D/G].
 int or_stream(const uint16_t* x, int64_t chunk, int steps, int refit_every, int D, int C,
-              int T, int S, int G, uint16_t* versions, int32_t* chunk_version,
+              int T, int S, int G, int b, uint16_t* versions, int32_t* chunk_version,
               int32_t* ids, uint32_t* codes, uint32_t* meta) {
     int64_t Ntot = chunk * steps;
+    const int W = D * b / 32;
     int nv = 0;
-    std::vector<uint32_t> cbuf((size_t)S * chunk * (D / 16)), mbuf((size_t)S * chunk * (D / G));
+    std::vector<uint32_t> cbuf((size_t)S * chunk * W), mbuf((size_t)S * chunk * (D / G));
     for (int t = 0; t < steps; ++t) {
         const uint16_t* xc = x + (int64_t)t * chunk * D;
         int32_t* idc = ids + (int64_t)t * chunk;
@@ -288,11 +296,11 @@ int or_stream(const uint16_t* x, int64_t chunk, int steps, int refit_every, int 
             or_assign(xc, chunk, D, versions + (size_t)(nv - 1) * C * D, C, idc, nullptr);
         }
         chunk_version[t] = nv - 1;
-        or_prq_encode(xc, chunk, D, versions + (size_t)(nv - 1) * C * D, idc, S, G,
+        or_prq_encode(xc, chunk, D, versions + (size_t)(nv - 1) * C * D, idc, S, G, b,
                       cbuf.data(), mbuf.data());
         for (int s = 0; s < S; ++s) {
-            std::memcpy(codes + ((int64_t)s * Ntot + (int64_t)t * chunk) * (D / 16),
-                        cbuf.data() + (size_t)s * chunk * (D / 16), sizeof(uint32_t) * chunk * (D / 16));
+            std::memcpy(codes + ((int64_t)s * Ntot + (int64_t)t * chunk) * W,
+                        cbuf.data() + (size_t)s * chunk * W, sizeof(uint32_t) * chunk * W);
             std::memcpy(meta + ((int64_t)s * Ntot + (int64_t)t * chunk) * (D / G),
                         mbuf.data() + (size_t)s * chunk * (D / G), sizeof(uint32_t) * chunk * (D / G));
         }
@@ -360,7 +368,7 @@ void or_coral_encode_layer(const uint16_t* xh_prev, const uint16_t* x_next, int6
                 r[i] = bf16_float(x_next[e]) - pv;
             }
             for (int s = 0; s < S; ++s)
-                quantize_stage(r.data(), D, G, cw.data() + (size_t)s * (D / 16), mw.data() + (size_t)s * (D / G));
+                quantize_stage(r.data(), D, G, 2, cw.data() + (size_t)s * (D / 16), mw.data() + (size_t)s * (D / G));
             for (int s = 0; s < S; ++s) {
                 std::memcpy(codes + (((int64_t)s * H + h) * N + n) * (D / 16), cw.data() + (size_t)s * (D / 16),
                             sizeof(uint32_t) * (D / 16));
@@ -370,7 +378,7 @@ void or_coral_encode_layer(const uint16_t* xh_prev, const uint16_t* x_next, int6
             for (int i = 0; i < D; ++i) {
                 float acc = p[i];
                 for (int s = 0; s < S; ++s) acc = acc + stage_value(cw.data() + (size_t)s * (D / 16),
-                                                                    mw.data() + (size_t)s * (D / G), i, G);
+                                                                    mw.data() + (size_t)s * (D / G), i, G, 2);
                 xh_next[n * HD + h * D + i] = to_bf16((double)acc);
             }
         }
@@ -395,7 +403,7 @@ void or_coral_decode_layer(const uint16_t* xh_prev, int64_t N, int H, int D, con
                 float acc = pred_in ? pred_in[e] : (xh_prev ? (float)pred64[e] : 0.0f);
                 for (int s = 0; s < S; ++s)
                     acc = acc + stage_value(codes + (((int64_t)s * H + h) * N + n) * (D / 16),
-                                            meta + (((int64_t)s * H + h) * N + n) * (D / G), i, G);
+                                            meta + (((int64_t)s * H + h) * N + n) * (D / G), i, G, 2);
                 xh_next[e] = to_bf16((double)acc);
             }
 }

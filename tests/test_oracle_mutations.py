@@ -15,9 +15,12 @@ PY = os.path.join(ROOT, "oracle", "oracle.py")
 
 MUTATIONS = {
     "residual sign": ("r[e] = r[e] - deq;", "r[e] = r[e] + deq;"),
-    "packing stride": ("codes[e / 16] |= (uint32_t)q << (2 * (e % 16));",
-                       "codes[e / 16] |= (uint32_t)q << (2 * (e % 8));"),
-    "scale divisor": ("float s32 = range / 3.0f;", "float s32 = range / 4.0f;"),
+    "packing stride": ("codes[(e * b) / 32] |= (uint32_t)q << ((e * b) % 32);",
+                       "codes[(e * b) / 32] |= (uint32_t)q << ((e * b) % 16);"),
+    "scale divisor": ("float s32 = range / (float)L;", "float s32 = range / (float)(L + 1);"),
+    "clamp at 3 for every width": ("int q = qf < 0.0f ? 0 : (qf > (float)L ? L : (int)qf);",
+                                   "int q = qf < 0.0f ? 0 : (qf > 3.0f ? 3 : (int)qf);"),
+    "4-bit field mask": ("& ((1u << b) - 1u);", "& 3u;"),
     "zero from max": ("uint16_t sh = to_f16(s32), zh = to_f16(mn);",
                       "uint16_t sh = to_f16(s32), zh = to_f16(mx);"),
     "rounding floor": ("float qf = std::nearbyint(t);", "float qf = std::floor(t);"),
@@ -51,11 +54,16 @@ MUTATIONS = {
 PIN_CALLS = [
     (PINS.test_bf16_rounding_is_exact_nearest_even, {}),
     (PINS.test_f16_rounding_matches_ieee, {}),
-    (PINS.test_single_stage_no_smoothing_is_rtn, {"D": 128, "G": 64}),
+    (PINS.test_single_stage_no_smoothing_is_rtn, {"D": 128, "G": 64, "b": 2}),
+    (PINS.test_single_stage_no_smoothing_is_rtn, {"D": 128, "G": 16, "b": 4}),
     (PINS.test_pack_example_golden, {}),
-    (PINS.test_on_grid_values_round_trip, {}),
-    (PINS.test_constant_group, {}),
-    (PINS.test_stage_error_bound_and_monotonicity, {}),
+    (PINS.test_pack_example_4bit_golden, {}),
+    (PINS.test_on_grid_values_round_trip, {"b": 2}),
+    (PINS.test_on_grid_values_round_trip, {"b": 4}),
+    (PINS.test_constant_group, {"b": 2}),
+    (PINS.test_constant_group, {"b": 4}),
+    (PINS.test_stage_error_bound_and_monotonicity, {"b": 2}),
+    (PINS.test_stage_error_bound_and_monotonicity, {"b": 4}),
     (PINS.test_decode_inverts_encode_within_last_stage_bound, {}),
     (PINS.test_decode_stage_sum_order, {}),
     (PINS.test_init_indices_golden, {}),

@@ -72,10 +72,12 @@ def decode_meta(meta):
     return s, z
 
 
-def unpack(codes, D):
-    """codes [..., D/16] uint32 -> [..., D] ints (least significant first)."""
-    sh = (2 * np.arange(16, dtype=np.uint32))
-    q = (codes[..., :, None] >> sh) & np.uint32(3)
+def unpack(codes, D, b=2):
+    """codes [..., D*b/32] uint32 -> [..., D] ints (b-bit fields, least
+    significant first)."""
+    per = 32 // b
+    sh = (b * np.arange(per, dtype=np.uint32))
+    q = (codes[..., :, None] >> sh) & np.uint32((1 << b) - 1)
     return q.reshape(codes.shape[:-1] + (D,)).astype(np.int64)
 
 
@@ -108,31 +110,34 @@ def test_f16_rounding_matches_ieee(oracle):
 
 # ------------------------------------------------- PRQ / group quantiser ---
 
-def rtn_reference(xb, G):
-    """Plain 2-bit asymmetric group round-to-nearest (the RTN baseline), one
+def rtn_reference(xb, G, b=2):
+    """Plain b-bit asymmetric group round-to-nearest (the RTN baseline), one
     stage, no smoothing; vectorised numpy fp32."""
+    L = (1 << b) - 1
     x = f32(xb)
     N, D = x.shape
     g = x.reshape(N, D // G, G)
     mn, mx = g.min(-1), g.max(-1)
-    s16 = ((mx - mn) / np.float32(3)).astype(np.float16)
+    s16 = ((mx - mn) / np.float32(L)).astype(np.float16)
     z16 = mn.astype(np.float16)
     s, z = s16.astype(np.float32), z16.astype(np.float32)
     with np.errstate(divide="ignore"):
         inv = np.where(s != 0, np.float32(1) / s, np.float32(0)).astype(np.float32)
-    q = np.clip(np.rint((g - z[..., None]) * inv[..., None]), 0, 3).astype(np.uint32)
-    q = q.reshape(N, D // 16, 16)
-    codes = (q << (2 * np.arange(16, dtype=np.uint32))).sum(-1, dtype=np.uint64).astype(np.uint32)
+    q = np.clip(np.rint((g - z[..., None]) * inv[..., None]), 0, L).astype(np.uint32)
+    per = 32 // b
+    q = q.reshape(N, D // per, per)
+    codes = (q << (b * np.arange(per, dtype=np.uint32))).sum(-1, dtype=np.uint64).astype(np.uint32)
     meta = s16.view(np.uint16).astype(np.uint32) | (z16.view(np.uint16).astype(np.uint32) << 16)
     return codes, meta
 
 
-@pytest.mark.parametrize("D,G", [(64, 64), (128, 64), (128, 128), (128, 32)])
-def test_single_stage_no_smoothing_is_rtn(oracle, D, G):
-    rng = np.random.default_rng(D + G)
+@pytest.mark.parametrize("D,G,b", [(64, 64, 2), (128, 64, 2), (128, 128, 2), (128, 32, 2),
+                                   (64, 64, 4), (128, 64, 4), (128, 16, 4)])
+def test_single_stage_no_smoothing_is_rtn(oracle, D, G, b):
+    rng = np.random.default_rng(D + G + b)
     x = rand_bf16(rng, (300, D), 2.0)
-    codes, meta = oracle.prq_encode(x, None, None, 1, G)
-    rc, rm = rtn_reference(x, G)
+    codes, meta = oracle.prq_encode(x, None, None, 1, G, b)
+    rc, rm = rtn_reference(x, G, b)
     assert np.array_equal(codes[0], rc)
     assert np.array_equal(meta[0], rm)
 
@@ -154,19 +159,40 @@ def test_pack_example_golden(oracle):
     assert np.array_equal(out, row)
 
 
-def test_on_grid_values_round_trip(oracle):
-    """Groups whose values are exactly z + k*s (s, z fp16, k in 0..3, all four
-    levels present) decode exactly and give codes k."""
-    rng = np.random.default_rng(3)
-    D, G = 128, 64
+def test_pack_example_4bit_golden(oracle):
+    """The hand-worked 4-bit row of tests/golden/pack_example_4bit.txt."""
+    fx = {}
+    for line in open(os.path.join(GOLD, "pack_example_4bit.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        k, *v = line.split()
+        fx[k] = v
+    pat = [int(h, 16) for h in fx["row_bf16"]]
+    row = np.array([pat[j % 16] for j in range(64)], np.uint16)[None, :]
+    codes, meta = oracle.prq_encode(row, None, None, 1, 64, 4)
+    assert codes.shape == (1, 1, int(fx["words_per_row"][0]))
+    want = [int(w, 16) for w in fx["codes_words"]]
+    assert [int(w) for w in codes[0, 0]] == want * 4
+    assert int(meta[0, 0, 0]) == int(fx["meta_word"][0], 16)
+    assert np.array_equal(oracle.decode(codes, meta, None, None, 64, 4), row)
+
+
+@pytest.mark.parametrize("b", [2, 4])
+def test_on_grid_values_round_trip(oracle, b):
+    """Groups whose values are exactly z + k*s (s, z fp16, k in 0..L with
+    L = 2^b - 1, every level present) decode exactly and give codes k."""
+    rng = np.random.default_rng(3 if b == 2 else 7)
+    D, G, L = 128, 64, (1 << b) - 1
     rows, ks = [], []
     for _ in range(50):
         row, krow = [], []
         for g in range(D // G):
             s = float(np.float16(2.0 ** rng.integers(-6, 2)))
-            z = float(np.float16(rng.integers(-64, 64) * 2.0 ** -4))
-            k = rng.integers(0, 4, G)
-            k[:4] = [0, 1, 2, 3]
+            # b = 4: z a multiple of s, so that every z + k*s = (m + k)*s,
+            # |m + k| < 256, is exact in bf16
+            z = float(np.float16(rng.integers(-64, 64) * (2.0 ** -4 if b == 2 else s)))
+            k = rng.integers(0, L + 1, G)
+            k[:L + 1] = np.arange(L + 1)
             rng.shuffle(k)
             row += [z + kk * s for kk in k]
             krow += list(k)
@@ -174,27 +200,29 @@ def test_on_grid_values_round_trip(oracle):
         ks.append(krow)
     x = SY.f64_to_bf16_bits(np.array(rows))
     assert np.array_equal(f32(x).astype(np.float64), np.array(rows))   # exact in bf16
-    codes, meta = oracle.prq_encode(x, None, None, 1, G)
-    assert np.array_equal(unpack(codes[0], D), np.array(ks))
-    assert np.array_equal(oracle.decode(codes, meta, None, None, G), x)
+    codes, meta = oracle.prq_encode(x, None, None, 1, G, b)
+    assert np.array_equal(unpack(codes[0], D, b), np.array(ks))
+    assert np.array_equal(oracle.decode(codes, meta, None, None, G, b), x)
 
 
-def test_constant_group(oracle):
+@pytest.mark.parametrize("b", [2, 4])
+def test_constant_group(oracle, b):
     x = np.full((4, 64), 0x3FC0, np.uint16)    # 1.5 everywhere
-    codes, meta = oracle.prq_encode(x, None, None, 2, 64)
+    codes, meta = oracle.prq_encode(x, None, None, 2, 64, b)
+    assert codes.shape == (2, 4, 64 * b // 32)
     s, z = decode_meta(meta)
     assert np.all(s == 0) and np.all(z[0] == 1.5) and np.all(z[1] == 0)
     assert np.all(codes == 0)
-    assert np.array_equal(oracle.decode(codes, meta, None, None, 64), x)
+    assert np.array_equal(oracle.decode(codes, meta, None, None, 64, b), x)
 
 
-def per_stage_residuals(x, S, G, oracle):
+def per_stage_residuals(x, S, G, oracle, b=2):
     """Residual after each number of stages, rebuilt from the stored codes
     (fp64 arithmetic of the dequantised values)."""
-    codes, meta = oracle.prq_encode(x, None, None, S, G)
+    codes, meta = oracle.prq_encode(x, None, None, S, G, b)
     N, D = x.shape
     s, z = decode_meta(meta)
-    q = unpack(codes, D).astype(np.float64)
+    q = unpack(codes, D, b).astype(np.float64)
     rng_s = np.repeat(s.astype(np.float64), G, axis=-1)
     rng_z = np.repeat(z.astype(np.float64), G, axis=-1)
     deq = q * rng_s + rng_z
@@ -206,24 +234,25 @@ def per_stage_residuals(x, S, G, oracle):
     return out, s, z
 
 
-def test_stage_error_bound_and_monotonicity(oracle):
+@pytest.mark.parametrize("b", [2, 4])
+def test_stage_error_bound_and_monotonicity(oracle, b):
     """|r_s - deq_s| <= s/2 + fp16 slack per element, and the per-group max-abs
-    error after a stage is at most (max-min of its input)/6 + slack, so it does
-    not grow as stages are added (PRQ items 1-2)."""
-    rng = np.random.default_rng(4)
-    G, S = 64, 4
+    error after a stage is at most (max-min of its input)/(2L) + slack with
+    L = 2^b - 1, so it does not grow as stages are added (PRQ items 1-2)."""
+    rng = np.random.default_rng(4 + b)
+    G, S, L = 64, 4, (1 << b) - 1
     x = rand_bf16(rng, (400, 128), 3.0)
-    res, s, z = per_stage_residuals(x, S, G, oracle)
+    res, s, z = per_stage_residuals(x, S, G, oracle, b)
     N = x.shape[0]
     for k in range(S):
         rin = res[k].reshape(N, -1, G)
         rout = res[k + 1].reshape(N, -1, G)
         span = rin.max(-1) - rin.min(-1)
-        exact_s = span / 3
-        slack = np.abs(rin.min(-1) - z[k]) + 3 * np.abs(exact_s - s[k]) + 1e-6 * (np.abs(rin).max(-1) + 1e-30)
+        exact_s = span / L
+        slack = np.abs(rin.min(-1) - z[k]) + L * np.abs(exact_s - s[k]) + 1e-6 * (np.abs(rin).max(-1) + 1e-30)
         err = np.abs(rout).max(-1)
         assert np.all(err <= s[k] / 2 + slack + 1e-12), k
-        assert np.all(err <= span / 6 + slack + 1e-12), k
+        assert np.all(err <= span / (2 * L) + slack + 1e-12), k
     mse = [np.mean(r ** 2) for r in res]
     assert all(mse[k + 1] <= mse[k] for k in range(S)), mse
 
