@@ -43,6 +43,18 @@ def source_hash(*files):
     return h.hexdigest()[:16]
 
 
+# The files each timed kernel is built from; a stored ncu traffic figure is
+# used only while all of them are unchanged.
+_CS = "kv_cache_quantization_means_b300/csrc/"
+KERNEL_SOURCES = {
+    "assign": [_CS + "assign_tc.cu", _CS + "tc_common.cuh", _CS + "common.cuh", _CS + "kernels.h"],
+    "encode": [_CS + "prq.cu", _CS + "prq16.cuh", _CS + "common.cuh", _CS + "kernels.h"],
+    "decode": [_CS + "prq.cu", _CS + "prq16.cuh", _CS + "common.cuh", _CS + "kernels.h"],
+    "coral_predict": [_CS + "coral_tc.cu", _CS + "prq16.cuh", _CS + "tc_common.cuh", _CS + "common.cuh",
+                      _CS + "kernels.h"],
+}
+
+
 def traffic_for(kernel, src_files):
     """DRAM bytes per launch from the committed ncu summary, if the kernel's
     source has not changed since it was captured; else None."""
@@ -194,7 +206,8 @@ class CoralStep:
         self.dec = [torch.empty((layers, N, H * D), dtype=torch.int16, device="cuda") for _ in (0, 1)]
         self.ws = Q.alloc_workspace(self.cfg, N)
         self.bytes_per_step = 2 * layers * N * H * D * 2
-        self.launches_per_step = 2 * (1 + 2 * (layers - 1)) * 2
+        # per tensor and direction: layer 0 (one kernel), then prep + low-rank + predict per layer
+        self.launches_per_step = 2 * (1 + 3 * (layers - 1)) * 2
 
     def encode(self, t, l):
         prev = None if l == 0 else self.xh[t][l - 1]
@@ -237,10 +250,10 @@ class StreamStep:
         self.ws = Q.alloc_workspace(self.cfg, self.chunk)
         self.out = torch.empty((N, H, D), dtype=torch.int16, device="cuda")
         per_tok = H * D * 2
-        # per (layer, tensor) and step: refit (init + T x 5 kernels) or assign, encode, chunk-table
+        # per (layer, tensor) and step: refit (init + T x 4 kernels) or assign, encode, chunk-table
         # update, then the history decode
         T = wl.lloyd_iters
-        self.launches_per_step = 2 * layers * sum((1 + 5 * T if k % self.every == 0 else 1) + 2 + 1
+        self.launches_per_step = 2 * layers * sum((1 + 4 * T if k % self.every == 0 else 1) + 2 + 1
                                                   for k in range(self.steps))
         self.enc_bytes = 2 * layers * N * per_tok
         self.dec_bytes = 2 * layers * per_tok * self.chunk * sum(range(1, self.steps + 1))
@@ -527,44 +540,61 @@ def main():
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         t = tt.item()
     value = st.bytes_per_step * world / t / 1e9
-    # per (layer, tensor): init + T x (assign, histogram, scatter, exact sum, mean) + encode + decode
-    launches_per_step = 2 * layers * (1 + wl.lloyd_iters * 5 + 2)
+    # per (layer, tensor): init + T x (assign, histogram, scatter, exact sum) + encode + decode
+    launches_per_step = 2 * layers * (1 + wl.lloyd_iters * 4 + 2)
 
     roof = kernel_rooflines(st, peaks)
 
     # end to end through the C ABI with host buffers: pinned H2D of every
-    # layer's K/V, fit + encode + decode, D2H of the compressed stream
+    # layer's K/V, fit + encode + decode, D2H of the compressed stream.  The
+    # three are pipelined over (layer, tensor) units on their own streams:
+    # unit u is uploaded while earlier units compute, and its compressed
+    # buffers are read back as soon as it is encoded.
     e2e = None
     if not args.no_e2e:
-        host_x = [[st.x[l][t].cpu().pin_memory() for t in (0, 1)] for l in range(layers)]
-        host_out = [torch.empty(st.compressed_bytes(), dtype=torch.uint8).pin_memory() for _ in (0, 1)]
+        units = [(l, t) for l in range(layers) for t in (0, 1)]
+        host_x = {u: st.x[u[0]][u[1]].cpu().pin_memory() for u in units}
+        host_out = {u: torch.empty(st.compressed_bytes(), dtype=torch.uint8).pin_memory() for u in units}
+        comp = torch.cuda.current_stream()
+        up, down = torch.cuda.Stream(), torch.cuda.Stream()
+        ev_in = {u: torch.cuda.Event() for u in units}
+        ev_done = {u: torch.cuda.Event() for u in units}
 
         def e2e_step():
-            for l in range(layers):
-                for t in (0, 1):
-                    st.x[l][t].copy_(host_x[l][t], non_blocking=True)
-                    st.fit(l, t)
-                    st.encode(l, t)
-                    st.decode(l, t)
-                    e = st.enc[l][t]
-                    o = 0
+            up.wait_stream(comp)                      # nothing starts before the timed region
+            down.wait_stream(comp)
+            with torch.cuda.stream(up):
+                for u in units:
+                    st.x[u[0]][u[1]].copy_(host_x[u], non_blocking=True)
+                    ev_in[u].record(up)
+            for u in units:
+                l, t = u
+                comp.wait_event(ev_in[u])
+                st.fit(l, t)
+                st.encode(l, t)
+                st.decode(l, t)
+                ev_done[u].record(comp)
+                with torch.cuda.stream(down):
+                    down.wait_event(ev_done[u])
+                    e, o = st.enc[l][t], 0
                     for k in ("codes", "meta", "ids", "centroids"):
                         nb = e[k].numel() * e[k].element_size()
-                        host_out[t][o:o + nb].copy_(e[k].view(torch.uint8), non_blocking=True)
+                        host_out[u][o:o + nb].copy_(e[k].view(torch.uint8), non_blocking=True)
                         o += nb
+            comp.wait_stream(down)                    # the timed region ends after the last read-back
+            comp.wait_stream(up)
         e2e_step()
         te = time_fn(e2e_step, max(1, min(args.steps, 3)))
         e2e = {"value": st.bytes_per_step * world / te / 1e9, "unit": "GB/s",
-               "h2d_bytes_per_step": st.bytes_per_step, "d2h_bytes_per_step": 2 * layers * st.compressed_bytes()}
+               "h2d_bytes_per_step": st.bytes_per_step, "d2h_bytes_per_step": 2 * layers * st.compressed_bytes(),
+               "pipelined": "upload / compute / read-back on three streams, per (layer, tensor)"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_baseline(args.config)
 
     dom = max(("assign", "decode", "encode"), key=lambda k: roof[k]["time_us"])
-    src = {"assign": ["kv_cache_quantization_means_b300/csrc/kmeans.cu"],
-           "decode": ["kv_cache_quantization_means_b300/csrc/prq.cu"],
-           "encode": ["kv_cache_quantization_means_b300/csrc/prq.cu"]}
+    src = {k: KERNEL_SOURCES[k] for k in ("assign", "decode", "encode")}
     rl = {k: roof[dom][k] for k in ("bound", "achieved", "peak", "unit", "frac")}
     rl["kernel"] = dom
     rl["traffic"] = traffic_for(dom, src[dom])

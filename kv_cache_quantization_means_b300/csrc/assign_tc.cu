@@ -180,13 +180,77 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(x));
 }
 
+// Rows whose fp32 re-rank left several survivors (a few per ten thousand):
+// exact squared distances decide (ties -> lowest j); candidates within 2^-40
+// of the best, or any value outside the exact range, are settled by the
+// channel-order fp64 sum of the plain definition.  Survivor list: lanes of sb
+// (lane k holds candidate myj), or -- more than 32 candidates -- every
+// candidate of the mask m, re-filtered.  Kept out of line so that the
+// epilogue's hot loop stays small.  All 32 lanes call it together.
+template <int D, int CP>
+__device__ __noinline__ int rerank_exact(const uint8_t* xs, int r, const uint8_t* Bs, uint32_t cslab, int lane,
+                                         const uint32_t* m, unsigned sb, int myj, int ncand, float dmin, float emin,
+                                         unsigned long long& n_seq) {
+    int best = -1;
+    const bool listed = ncand <= 32;
+    const int nlist = listed ? 32 : CP;
+    i128 dbest = 0;
+    bool exact = true, near = false;
+    for (int k = 0; k < nlist && exact; ++k) {
+        int j;
+        if (listed) {
+            if (!((sb >> k) & 1u)) continue;
+            j = __shfl_sync(0xffffffffu, myj, k);
+        } else {
+            j = k;
+            if (!((m[j >> 5] >> (j & 31)) & 1u)) continue;
+            const float d = warp_dist<D>(xs, r, Bs, j, cslab, lane);
+            if (d - (kDirectRel * d + kDirectAbs) > dmin + emin) continue;
+        }
+        bool ok;
+        const i128 de = warp_dist_exact<D>(xs, r, Bs, j, cslab, lane, ok);
+        if (!ok) { exact = false; break; }
+        if (best < 0 || de < dbest) {
+            if (best >= 0 && dbest - de <= (dbest >> 40)) near = true;
+            dbest = de;
+            best = j;
+        } else if (de - dbest <= (de >> 40)) {
+            near = true;
+        }
+    }
+    if (!exact || near) {
+        best = -1;
+        double cbest = INFINITY;
+        for (int k = 0; k < nlist; ++k) {
+            int j;
+            if (listed) {
+                if (!((sb >> k) & 1u)) continue;
+                j = __shfl_sync(0xffffffffu, myj, k);
+            } else {
+                j = k;
+                if (!((m[j >> 5] >> (j & 31)) & 1u)) continue;
+                const float d = warp_dist<D>(xs, r, Bs, j, cslab, lane);
+                if (d - (kDirectRel * d + kDirectAbs) > dmin + emin) continue;
+            }
+            double cd = 0.0;
+            if (lane == 0) cd = canonical_dist_smem<D>(xs, r, Bs, j, cslab);
+            cd = __shfl_sync(0xffffffffu, cd, 0);
+            if (cd < cbest) { cbest = cd; best = j; }
+        }
+        ++n_seq;
+    }
+    return best;
+}
+
 template <int D, int CP>
 __global__ void __launch_bounds__(kTcThreads, 1)
     kmeans_assign_tc_kernel(const __grid_constant__ CUtensorMap tmap, TcArgs a) {
     constexpr int nA = D / 64;
     constexpr int Cpad = CP;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    // 1024-byte aligned, derived from the shared array so that accesses stay in
+    // the shared window
+    uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int C = a.C, NS = a.stages;
     const Layout L = make_layout(D, Cpad, NS);
     uint8_t* Bs = base + L.b_off;     // centroids c_j
@@ -370,6 +434,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc_fence_after();
             const uint8_t* xs = Xs + (size_t)st * nA * kAtomBytes;
             const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)g * acc_cols;
+            // The row's 2*NW chunk reads (pass A, then pass B) form one
+            // stream: chunk k+1 is loaded while chunk k is used, and the
+            // first load overlaps ||x||^2.
+            uint32_t v[2][32];
+            tmem_ld32(taddr, v[0]);
             // ||x||^2 of this row (error bound of the screen)
             float xnt;
             {
@@ -386,56 +455,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 xnt = (s2.x + s2.y) + (t2.x + t2.y);
             }
+            tmem_wait_ld_regs(v[0]);
             // pass A: the largest score of the row
-            float b1;
-            {
-                uint32_t v[2][32];
-                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int c0 = 0; c0 < NW; c0 += 2) {
-                    tmem_ld32(taddr + 32u * c0, v[0]);
-                    if (c0 + 1 < NW) tmem_ld32(taddr + 32u * (c0 + 1), v[1]);
-                    tmem_wait_ld();
+            for (int c = 0; c < NW; ++c) {
+                // next: chunk c+1 of pass A, or chunk 0 of pass B
+                tmem_ld32(taddr + 32u * ((c + 1) % NW), v[(c + 1) & 1]);
+                const uint32_t* u = v[c & 1];
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        if (c0 + c < NW) {
-#pragma unroll
-                            for (int jj = 0; jj < 32; jj += 8) {
-                                m4[0] = fmax3(m4[0], __uint_as_float(v[c][jj]), __uint_as_float(v[c][jj + 1]));
-                                m4[1] = fmax3(m4[1], __uint_as_float(v[c][jj + 2]), __uint_as_float(v[c][jj + 3]));
-                                m4[2] = fmax3(m4[2], __uint_as_float(v[c][jj + 4]), __uint_as_float(v[c][jj + 5]));
-                                m4[3] = fmax3(m4[3], __uint_as_float(v[c][jj + 6]), __uint_as_float(v[c][jj + 7]));
-                            }
-                        }
-                    }
+                for (int jj = 0; jj < 32; jj += 8) {
+                    m4[0] = fmax3(m4[0], __uint_as_float(u[jj]), __uint_as_float(u[jj + 1]));
+                    m4[1] = fmax3(m4[1], __uint_as_float(u[jj + 2]), __uint_as_float(u[jj + 3]));
+                    m4[2] = fmax3(m4[2], __uint_as_float(u[jj + 4]), __uint_as_float(u[jj + 5]));
+                    m4[3] = fmax3(m4[3], __uint_as_float(u[jj + 6]), __uint_as_float(u[jj + 7]));
                 }
-                b1 = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                tmem_wait_ld_regs(v[(c + 1) & 1]);
             }
+            const float b1 = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
             // bound on the error of a score (half the bound on ||c||^2 - 2<x, c>)
             const float E = 0.5f * (1.01f * (kScreenXC * sqrtf(xnt) * cm + kScreenCC * cm2) + 1e-30f);
             const float thr = b1 - 2.0f * E;
             // pass B: candidates within 2E of the largest score
             uint32_t mw[NW];
-            {
-                uint32_t v[2][32];
 #pragma unroll
-                for (int c0 = 0; c0 < NW; c0 += 2) {
-                    tmem_ld32(taddr + 32u * c0, v[0]);
-                    if (c0 + 1 < NW) tmem_ld32(taddr + 32u * (c0 + 1), v[1]);
-                    tmem_wait_ld();
+            for (int c = 0; c < NW; ++c) {
+                const int b = (NW + c) & 1;              // buffer of pass-B chunk c
+                if (c + 1 < NW) tmem_ld32(taddr + 32u * (c + 1), v[b ^ 1]);
+                const uint32_t* u = v[b];
+                uint32_t m4[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        if (c0 + c < NW) {
-                            uint32_t me = 0, mo = 0;
-#pragma unroll
-                            for (int jj = 0; jj < 32; jj += 2) {
-                                if (__uint_as_float(v[c][jj]) >= thr) me |= 1u << jj;
-                                if (__uint_as_float(v[c][jj + 1]) >= thr) mo |= 2u << jj;
-                            }
-                            mw[c0 + c] = me | mo;
-                        }
-                    }
-                }
+                for (int jj = 0; jj < 32; ++jj)
+                    if (__uint_as_float(u[jj]) >= thr) m4[jj & 3] |= 1u << jj;
+                mw[c] = (m4[0] | m4[1]) | (m4[2] | m4[3]);
+                if (c + 1 < NW) tmem_wait_ld_regs(v[b ^ 1]);
             }
             // accumulator drained: hand it back to the MMA issuer
             tc_fence_before();
@@ -479,59 +532,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (__popc(sb) == 1) best = __shfl_sync(0xffffffffu, myj, __ffs(sb) - 1);
                 }
                 if (best < 0) {
-                    // several survivors: exact squared distances decide (ties ->
-                    // lowest j).  Candidates within 2^-40 of the best -- or any
-                    // value outside the exact range -- are settled by the
-                    // channel-order fp64 sum of the plain definition.
-                    // Survivor list: lanes of sb, or (more than 32 candidates)
-                    // every candidate, re-filtered.
-                    const bool listed = ncand <= 32;
-                    const int nlist = listed ? 32 : CP;
-                    i128 dbest = 0;
-                    bool exact = true, near = false;
-                    for (int k = 0; k < nlist && exact; ++k) {
-                        int j;
-                        if (listed) {
-                            if (!((sb >> k) & 1u)) continue;
-                            j = __shfl_sync(0xffffffffu, myj, k);
-                        } else {
-                            j = k;
-                            if (!((m[j >> 5] >> (j & 31)) & 1u)) continue;
-                            const float d = warp_dist<D>(xs, r, Bs, j, cslab, lane);
-                            if (d - (kDirectRel * d + kDirectAbs) > dmin + emin) continue;
-                        }
-                        bool ok;
-                        const i128 de = warp_dist_exact<D>(xs, r, Bs, j, cslab, lane, ok);
-                        if (!ok) { exact = false; break; }
-                        if (best < 0 || de < dbest) {
-                            if (best >= 0 && dbest - de <= (dbest >> 40)) near = true;
-                            dbest = de;
-                            best = j;
-                        } else if (de - dbest <= (de >> 40)) {
-                            near = true;
-                        }
-                    }
-                    if (!exact || near) {
-                        best = -1;
-                        double cbest = INFINITY;
-                        for (int k = 0; k < nlist; ++k) {
-                            int j;
-                            if (listed) {
-                                if (!((sb >> k) & 1u)) continue;
-                                j = __shfl_sync(0xffffffffu, myj, k);
-                            } else {
-                                j = k;
-                                if (!((m[j >> 5] >> (j & 31)) & 1u)) continue;
-                                const float d = warp_dist<D>(xs, r, Bs, j, cslab, lane);
-                                if (d - (kDirectRel * d + kDirectAbs) > dmin + emin) continue;
-                            }
-                            double cd = 0.0;
-                            if (lane == 0) cd = canonical_dist_smem<D>(xs, r, Bs, j, cslab);
-                            cd = __shfl_sync(0xffffffffu, cd, 0);
-                            if (cd < cbest) { cbest = cd; best = j; }
-                        }
-                        ++n_seq;
-                    }
+                    best = rerank_exact<D, CP>(xs, r, Bs, cslab, lane, m, sb, myj, ncand, dmin, emin, n_seq);
                     ++n_exact;
                 }
                 if (lane == 0 && best >= 0) idrow[(int64_t)(t_begin + i) * kTile + r] = (uint8_t)best;

@@ -79,6 +79,11 @@ __device__ __forceinline__ float dequant(uint32_t q, float s, float z) {
 // fma(b, -1, a): b * -1 is exact, so the single rounding is that of a - b.
 
 __device__ __forceinline__ float2 f2_add(float2 a, float2 b) { return __fadd2_rn(a, b); }
+// Caution: the code generator may fuse a packed product with a following
+// packed addition into one FFMA2 -- even when both are written with explicit
+// round-to-nearest -- so a product whose rounding matters must not feed an
+// addition directly.  In the quantiser the clamp of t = (r - z) * inv sits
+// between the product and the rounding addition.
 __device__ __forceinline__ float2 f2_mul(float2 a, float2 b) { return __fmul2_rn(a, b); }
 __device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 __device__ __forceinline__ float2 f2_sub(float2 a, float2 b) {

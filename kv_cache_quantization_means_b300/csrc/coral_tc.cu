@@ -78,7 +78,9 @@ __global__ void __launch_bounds__(kLrThreads, 1)
     coral_lowrank_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                             LrArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    // 1024-byte aligned, derived from the shared array so that accesses stay in
+    // the shared window
+    uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     constexpr int kWBytes = kR * 128;                   // Wt slab [32 x 64]
     uint8_t* Xs = base;                                  // kLrStages x [128 x 64]
     uint8_t* Ws = base + kLrStages * kSlab;              // kLrStages x [32 x 64]
@@ -209,7 +211,9 @@ __global__ void __launch_bounds__(kPrThreads, 1)
                             const __grid_constant__ CUtensorMap tm_t, const __grid_constant__ CUtensorMap tm_u,
                             PrArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    // 1024-byte aligned, derived from the shared array so that accesses stay in
+    // the shared window
+    uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t bar0 = smem_u32(base + kPrStages * kStageBytes);
     const uint32_t full_bar = bar0, empty_bar = bar0 + 8 * kPrStages, tfull_bar = bar0 + 16 * kPrStages,
                    tempty_bar = tfull_bar + 16;

@@ -1,0 +1,106 @@
+"""Small fixed cases of the codec's kernels, for timing and for profilers.
+
+    python -m kv_cache_quantization_means_b300.profile_case unit [time]
+    python -m kv_cache_quantization_means_b300.profile_case coral [time]
+
+`unit` runs one (layer, tensor) of the Wan2.1-shaped cache (12 heads x 32760
+tokens x 128, C = 256, T = 4, S = 2, G = 64): a fit, then one more assign,
+update, encode and decode.  `coral` runs one cross-layer layer (16 heads x
+16384 tokens x 128, rank 32, S = 2, G = 64): encode then decode, and checks
+that both rebuild the same x_hat.  Without `time` each kernel runs once (the
+form to put under a profiler); with `time` each call is replayed from a CUDA
+graph and its mean device time printed.  Inputs come from the seeded
+synthetic generators.
+"""
+import sys
+
+import torch
+
+from . import qvg as Q
+from synth import gpu as SG
+from synth import workloads as WL
+
+
+def _graph_time_us(f, reps=20, inner=10):
+    f()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(inner):
+            f()
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps / inner * 1e3
+
+
+def unit_case(timed):
+    wl = WL.WAN
+    H, D, N = wl.heads, wl.head_dim, wl.tokens
+    cfg = Q.config(H, D, wl.clusters, wl.lloyd_iters, wl.stages, wl.group_size)
+    x = SG.mixture_layer_gpu(wl, 0, 1, layout="nhd")
+    e = Q.alloc_encoded(cfg, N)
+    ws = Q.alloc_workspace(cfg, N)
+    out = torch.empty((N, H, D), dtype=torch.int16, device="cuda")
+    calls = {
+        "fit": lambda: Q.qvg_fit_centroids(cfg, x, N, D, H * D, None, e["centroids"], e["ids"], N, 0, ws),
+        "assign": lambda: Q.qvg_assign(cfg, x, N, D, H * D, e["centroids"], e["ids"], N, 0, ws),
+        "update": lambda: Q.qvg_update(cfg, x, N, D, H * D, e["ids"], N, 0, e["centroids"], ws),
+        "encode": lambda: Q.qvg_encode(cfg, x, N, D, H * D, e["centroids"], 0, e["codes"], e["meta"], e["ids"],
+                                       N, 0, ws),
+        "decode": lambda: Q.qvg_decode(cfg, e["codes"], e["meta"], e["ids"], e["centroids"], N, 0, N, out, D,
+                                       H * D),
+    }
+    for f in calls.values():
+        f()
+    torch.cuda.synchronize()
+    stats = Q.qvg_fit_stats(cfg, N, ws)
+    assert stats[3] == 0, stats
+    print("re-rank stats (rows re-ranked, exact, channel-order fp64, error word):", stats)
+    if timed:
+        for name in ("assign", "update", "encode", "decode", "fit"):
+            print(f"{name:8s} {_graph_time_us(calls[name]):9.1f} us")
+
+
+def coral_case(timed):
+    wl = WL.CORAL
+    H, D, N, S, G = wl.heads, wl.head_dim, wl.tokens, wl.stages, wl.group_size
+    cfg = Q.config(H, D, 0, 0, S, G)
+    xs = SG.coral_chain_gpu(wl, 0, n_layers=2)
+    B, U, W = SG.coral_predictor_device(wl, 0)
+    pred = Q.coral_predictor(B=B.data_ptr(), U=U.data_ptr(), W=W.data_ptr(), rank=wl.rank)
+    codes = torch.empty(S * H * N * D // 16, dtype=torch.int32, device="cuda")
+    meta = torch.empty(S * H * N * D // G, dtype=torch.int32, device="cuda")
+    xh = torch.empty((N, H * D), dtype=torch.int16, device="cuda")
+    dec = torch.empty((N, H * D), dtype=torch.int16, device="cuda")
+    ws = Q.alloc_workspace(cfg, N)
+    enc = lambda: Q.coral_predict_encode(cfg, pred, xs[0], xs[1], N, codes, meta, xh, None, ws)
+    dcd = lambda: Q.coral_predict_decode(cfg, pred, xs[0], N, codes, meta, dec, None, ws)
+    enc()
+    dcd()
+    torch.cuda.synchronize()
+    assert torch.equal(xh, dec), "encoder and decoder reconstructions differ"
+    assert Q.qvg_fit_stats(cfg, N, ws)[3] == 0
+    if timed:
+        el = N * H * D
+        # algorithmic bytes per element: encode reads x_hat_l and x_{l+1},
+        # writes x_hat_{l+1}, S stages of 2-bit codes and one 4-byte scale/zero
+        # word per G elements and stage
+        for name, f, byt in (("encode", enc, 6.0 + S * (0.25 + 4.0 / G)), ("decode", dcd, 4.0 + S * (0.25 + 4.0 / G))):
+            t = _graph_time_us(f)
+            print(f"{name:8s} {t:9.1f} us   {el * byt / t / 1e3:8.1f} GB/s algorithmic")
+
+
+def main(argv):
+    case = argv[1] if len(argv) > 1 else "unit"
+    timed = len(argv) > 2 and argv[2] == "time"
+    {"unit": unit_case, "coral": coral_case}[case](timed)
+
+
+if __name__ == "__main__":
+    main(sys.argv)

@@ -190,3 +190,21 @@ def test_repeated_calls_are_deterministic(qvg):
         assert np.array_equal(enc.codes(), runs[0][0].codes())
         assert np.array_equal(enc.centroids(), runs[0][0].centroids())
         assert np.array_equal(dec, runs[0][1])
+
+
+@pytest.mark.parametrize("G", [16, 32, 64, 128])
+def test_quantiser_half_integer_ties(qvg, oracle, G):
+    """Values on a coarse grid make t = (r - z) / s land exactly on k + 1/2
+    (or within half an ulp of it) for many elements, so rint(t) is decided by
+    the rounding of the product alone: any fusion of the multiply with the
+    rounding addition, or any skipped clamp that matters, changes codes here."""
+    rng = np.random.default_rng(4242 + G)
+    H, N, D, S = 2, 513, 128, 3
+    grid = rng.integers(-24, 25, size=(H, N, D)).astype(np.float64) / 16.0
+    # a few groups with a far outlier, so the clamp path is taken as well
+    grid[:, ::37, 5] = 900.0
+    xb = SY.f64_to_bf16_bits(grid)
+    cfg = qvg.config(H, D, 0, 0, S, G)
+    enc, dec = run_fit_encode_decode(qvg, cfg, to_dev(xb), N, N * D, D)
+    for h in range(H):
+        check_unit(oracle, xb[h], enc, dec, h, 0, 0, S, G)
