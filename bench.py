@@ -125,9 +125,11 @@ class ClockSampler:
 
 # --------------------------------------------------------------- workload --
 
-def workload(name):
+def workload(name, bits=None):
+    import dataclasses
     from synth import workloads as WL
-    return WL.SHORT[name]
+    wl = WL.SHORT[name]
+    return wl if bits is None else dataclasses.replace(wl, bits=bits)
 
 
 class QvgStep:
@@ -138,7 +140,7 @@ class QvgStep:
         from synth import gpu as SG
         self.Q, self.wl, self.L = Q, wl, layers
         H, D, N = wl.heads, wl.head_dim, wl.tokens
-        self.cfg = Q.config(H, D, wl.clusters, wl.lloyd_iters, wl.stages, wl.group_size)
+        self.cfg = Q.config(H, D, wl.clusters, wl.lloyd_iters, wl.stages, wl.group_size, wl.bits)
         self.x = [[SG.mixture_layer_gpu(wl, l, t, layout="nhd") for t in (0, 1)] for l in range(layers)]
         self.enc = [[Q.alloc_encoded(self.cfg, N) for _ in (0, 1)] for _ in range(layers)]
         self.ws = Q.alloc_workspace(self.cfg, N)
@@ -241,7 +243,7 @@ class StreamStep:
         from synth import gpu as SG
         self.Q, self.wl, self.L = Q, wl, layers
         H, D, N = wl.heads, wl.head_dim, wl.tokens
-        self.cfg = Q.config(H, D, wl.clusters, wl.lloyd_iters, wl.stages, wl.group_size)
+        self.cfg = Q.config(H, D, wl.clusters, wl.lloyd_iters, wl.stages, wl.group_size, wl.bits)
         self.N, self.H, self.D = N, H, D
         self.chunk, self.steps, self.every = wl.chunk_tokens, wl.steps, wl.refit_every
         self.x = [[SG.mixture_layer_gpu(wl, l, t, layout="nhd") for t in (0, 1)] for l in range(layers)]
@@ -312,7 +314,7 @@ def kernel_rooflines(st, peaks, reps=3):
     wl, L = st.wl, st.L
     elems = st.N * st.H * st.D                      # one tensor of one layer
     S, G, C, D = wl.stages, wl.group_size, wl.clusters, wl.head_dim
-    code_b = S * (2 / 8 + 4 / G)                    # code + meta bytes per element
+    code_b = S * (wl.bits / 8 + 4 / G)              # code + meta bytes per element
     id_b = 1 / D
     units = [(l, t) for l in range(L) for t in (0, 1)]
 
@@ -351,30 +353,30 @@ def kernel_rooflines(st, peaks, reps=3):
 # ------------------------------------------------------------ CPU oracle --
 
 def _oracle_unit(args):
-    name, layer, tensor, head = args
+    name, bits, layer, tensor, head = args
     import time as _t
     from oracle import oracle as O
     from synth import synth as SY
-    wl = workload(name)
+    wl = workload(name, bits)
     x = SY.mixture_unit(wl, layer, tensor, head)
     t0 = _t.perf_counter()
     cent, ids = O.fit(x, wl.clusters, wl.lloyd_iters)
-    codes, meta = O.prq_encode(x, cent, ids, wl.stages, wl.group_size)
-    O.decode(codes, meta, ids, cent, wl.group_size)
+    codes, meta = O.prq_encode(x, cent, ids, wl.stages, wl.group_size, wl.bits)
+    O.decode(codes, meta, ids, cent, wl.group_size, wl.bits)
     return _t.perf_counter() - t0, x.size * 2
 
 
-def cpu_baseline(name, max_units=None):
+def cpu_baseline(name, max_units=None, bits=None):
     """The oracle as it stands on this host's cores: one (layer, tensor, head)
     unit per worker process, all units in parallel; throughput = bf16 bytes of
     the units / wall time."""
     import multiprocessing as mp
     from oracle import oracle as O
     O.build()
-    wl = workload(name)
+    wl = workload(name, bits)
     cores = os.cpu_count() or 1
     n = min(cores, 8 if max_units is None else max_units)
-    units = [(name, (i * 7) % wl.layers, i % 2, (i * 5) % wl.heads) for i in range(n)]
+    units = [(name, bits, (i * 7) % wl.layers, i % 2, (i * 5) % wl.heads) for i in range(n)]
     ctx = mp.get_context("spawn")
     with ctx.Pool(n) as pool:
         res = pool.map(_oracle_unit, units)
@@ -393,13 +395,13 @@ def run_reference(args):
     if rank != 0:
         return 0
     name = args.config
-    wl = workload(name)
+    wl = workload(name, args.bits)
     t0 = time.perf_counter()
     per_step = []
     for _ in range(args.warmup):
-        cpu_baseline(name, max_units=2)
+        cpu_baseline(name, max_units=2, bits=args.bits)
     for _ in range(args.steps):
-        per_step.append(cpu_baseline(name, max_units=2))
+        per_step.append(cpu_baseline(name, max_units=2, bits=args.bits))
     wall = time.perf_counter() - t0
     v = statistics.median(p["value"] for p in per_step)
     cb = dict(per_step[-1])
@@ -416,9 +418,10 @@ def run_reference(args):
 def config_block(wl, args):
     return {"workload": f"{wl.name}: {wl.layers} layers x {wl.heads} heads x head_dim {wl.head_dim} x {wl.tokens} "
                         f"tokens, K and V bf16 token-major; C={wl.clusters} T={wl.lloyd_iters} S={wl.stages} "
-                        f"b=2 G={wl.group_size}",
+                        f"b={wl.bits} G={wl.group_size}",
             "layers": wl.layers, "heads": wl.heads, "head_dim": wl.head_dim, "tokens": wl.tokens,
             "clusters": wl.clusters, "lloyd_iters": wl.lloyd_iters, "stages": wl.stages, "group_size": wl.group_size,
+            "bits": wl.bits,
             "l2": "inputs larger than L2 (one layer's K or V is %.0f MB)" % (wl.tokens * wl.heads * wl.head_dim * 2 / 1e6),
             "parallelism": f"replicas x{args.gpus}"}
 
@@ -450,7 +453,7 @@ def run_aux(args, Q, wl, peaks, world, rank, local):
         lens = [st.chunk * (k + 1) for k in range(st.steps)]
         t_dec = graph_time(lambda: [Q.qvg_decode_cache(st.cfg, c, 0, n, st.out, st.D, st.H * st.D) for n in lens], 3)
         el = sum(lens) * st.H * st.D
-        b = el * (wl.stages * (2 / 8 + 4 / wl.group_size) + 1 / wl.head_dim + 2)
+        b = el * (wl.stages * (wl.bits / 8 + 4 / wl.group_size) + 1 / wl.head_dim + 2)
         dom = {"kernel": "prq_decode (versioned history decode)", "bound": "hbm", "achieved": b / t_dec / 1e9,
                "peak": hbm, "unit": "GB/s", "time_us": t_dec / st.steps * 1e6}
         cfgb = {"workload": f"{wl.name}: {wl.layers} layers x {wl.heads} heads x head_dim {wl.head_dim}; {wl.steps} steps "
@@ -480,7 +483,11 @@ def main():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--bits", type=int, default=None, choices=[2, 4],
+                    help="code width of the QVG workloads (default: the workload's, 2)")
     args = ap.parse_args()
+    if args.bits is not None and args.config == "coral" and args.bits != 2:
+        ap.error("the cross-layer codec uses 2-bit codes")
     if args.impl == "reference":
         return run_reference(args)
 
@@ -501,7 +508,7 @@ def main():
     GE.build()
     import kv_cache_quantization_means_b300 as Q
     Q.load()
-    wl = workload(args.config)
+    wl = workload(args.config, args.bits)
     peaks = load_peaks()
     if args.config in ("coral", "stream"):
         return run_aux(args, Q, wl, peaks, world, rank, local)
@@ -591,7 +598,7 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        cpu = cpu_baseline(args.config)
+        cpu = cpu_baseline(args.config, bits=args.bits)
 
     dom = max(("assign", "decode", "encode"), key=lambda k: roof[k]["time_us"])
     src = {k: KERNEL_SOURCES[k] for k in ("assign", "decode", "encode")}

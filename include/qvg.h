@@ -34,18 +34,23 @@
  *
  * Supported shapes: head_dim D in {32, 64, 128, 256} (k-means: D <= 128);
  * group_size G in {16, 32, 64, 128} dividing D; num_stages S in 1..4;
- * bits = 2; num_clusters C in 0..256 (0 = no smoothing).  Pointers must be
- * 16-byte aligned and strides multiples of 8 elements.
+ * bits b = 2 (the QVG codec) or 4 (the PRQ_INT4 variant named by the KV
+ * Cache Quantization for Self-Forcing Video Generation study, read as the same
+ * group scheme with 15 steps; the cross-layer codec is 2-bit only);
+ * num_clusters C in 0..256 (0 = no smoothing).  Pointers must be 16-byte
+ * aligned and strides multiples of 8 elements.
  *
  * Encoded layout of one (layer, tensor) with `capacity` token rows per head:
- *   codes : uint32 [S][H][capacity][D/16]; element j of a row sits in word
- *           j/16, bits 2*(j%16) .. 2*(j%16)+1 (least significant first).
- *   meta  : uint32 [S][H][capacity][D/G]; low half = fp16 scale s, high half
- *           = fp16 zero-point z of the group; a code q decodes to q*s + z.
+ *   codes : uint32 [S][H][capacity][D*b/32]; element j of a row sits in word
+ *           j/(32/b), bits b*(j%(32/b)) .. b*(j%(32/b))+b-1 (least
+ *           significant first).
+ *   meta  : uint32 [S][H][capacity][D/G]; low half = fp16 scale s =
+ *           fp16((max - min) / (2^b - 1)), high half = fp16 zero-point z of
+ *           the group; a code q decodes to q*s + z.
  *   ids   : uint8  [H][capacity] cluster of each token row (C > 0 only).
  *   centroids : bf16 [V][H][C][D], V centroid-table versions (V = 1 unless
  *           streaming).
- * Compressed bits per element = S*2 + 32*S/G + [C > 0]*(8/D + 16*C*V/N).
+ * Compressed bits per element = S*b + 32*S/G + [C > 0]*(8/D + 16*C*V/N).
  */
 #ifndef QVG_H
 #define QVG_H
@@ -81,7 +86,7 @@ typedef struct {
     int32_t num_clusters;  /* C, 0 = no smoothing */
     int32_t lloyd_iters;   /* T, Lloyd iterations of qvg_fit_centroids */
     int32_t num_stages;    /* S */
-    int32_t bits;          /* bits per code, must be 2 */
+    int32_t bits;          /* bits per code: 2 or 4 (cross-layer codec: 2) */
     int32_t group_size;    /* G, elements per (scale, zero) along D */
 } qvg_config;
 

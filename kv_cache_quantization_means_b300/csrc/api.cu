@@ -37,7 +37,7 @@ constexpr int kMaxChunks = 4096;   // chunk table is staged in shared memory by 
 qvg_status check_config(const qvg_config* c, bool need_clusters) {
     if (!c) return fail(QVG_ERR_INVALID_ARG, "config is NULL");
     if (c->num_heads < 1) return fail(QVG_ERR_INVALID_ARG, "num_heads must be >= 1");
-    if (c->bits != 2) return fail(QVG_ERR_UNSUPPORTED, "bits must be 2 (got %d)", c->bits);
+    if (c->bits != 2 && c->bits != 4) return fail(QVG_ERR_UNSUPPORTED, "bits must be 2 or 4 (got %d)", c->bits);
     const int D = c->head_dim, G = c->group_size;
     if (D != 32 && D != 64 && D != 128 && D != 256)
         return fail(QVG_ERR_UNSUPPORTED, "head_dim must be 32, 64, 128 or 256 (got %d)", D);
@@ -190,7 +190,7 @@ qvg_status qvg_encoded_bytes(const qvg_config* cfg, int64_t capacity, int32_t n_
     if (capacity < 0 || n_versions < 0) return fail(QVG_ERR_INVALID_ARG, "negative capacity or versions");
     const size_t S = cfg->num_stages, H = cfg->num_heads, D = cfg->head_dim, G = cfg->group_size,
                  C = cfg->num_clusters, N = (size_t)capacity;
-    if (codes_bytes) *codes_bytes = S * H * N * (D / 16) * 4;
+    if (codes_bytes) *codes_bytes = S * H * N * (D * (size_t)cfg->bits / 32) * 4;
     if (meta_bytes) *meta_bytes = S * H * N * (D / G) * 4;
     if (ids_bytes) *ids_bytes = C ? H * N : 0;
     if (centroid_bytes) *centroid_bytes = C ? (size_t)n_versions * H * C * D * 2 : 0;
@@ -333,7 +333,7 @@ qvg_status qvg_encode(const qvg_config* cfg, const qvg_bf16* x, int64_t n_tokens
     a.cent = C > 0 ? centroids : nullptr;
     a.ids = C > 0 ? ids : nullptr;
     a.codes = codes; a.meta = meta; a.cap = capacity; a.tok_offset = tok_offset;
-    a.H = cfg->num_heads; a.C = C; a.S = cfg->num_stages;
+    a.H = cfg->num_heads; a.C = C; a.S = cfg->num_stages; a.bits = cfg->bits;
     return cuda_status(qvg::launch_encode(cfg->head_dim, cfg->group_size, a, s), "encode launch");
 }
 
@@ -356,7 +356,7 @@ static qvg_status decode_impl(const qvg_config* cfg, const uint32_t* codes, cons
     a.chunk_offset = chunk_offset; a.chunk_version = chunk_version; a.n_chunks = n_chunks;
     a.cap = capacity; a.tok_begin = tok_begin; a.tok_end = tok_end;
     a.out = out; a.out_head_stride = ohs; a.out_token_stride = ots;
-    a.H = cfg->num_heads; a.C = cfg->num_clusters; a.S = cfg->num_stages;
+    a.H = cfg->num_heads; a.C = cfg->num_clusters; a.S = cfg->num_stages; a.bits = cfg->bits;
     return cuda_status(qvg::launch_decode(cfg->head_dim, cfg->group_size, a, s), "decode launch");
 }
 
@@ -448,6 +448,7 @@ static qvg_status coral_common(const qvg_config* cfg, const coral_predictor* pre
     qvg_status st = check_config(cfg, false);
     if (st) return st;
     if (cfg->num_clusters != 0) return fail(QVG_ERR_INVALID_ARG, "cross-layer codec needs num_clusters == 0");
+    if (cfg->bits != 2) return fail(QVG_ERR_UNSUPPORTED, "cross-layer codec uses 2-bit codes (got %d)", cfg->bits);
     if (cfg->head_dim != 64 && cfg->head_dim != 128)
         return fail(QVG_ERR_UNSUPPORTED, "cross-layer codec supports head_dim 64 or 128");
     if (n_tokens < 0) return fail(QVG_ERR_INVALID_ARG, "negative token count");

@@ -48,10 +48,11 @@ struct GroupParams {
 };
 
 // Scale / zero / reciprocal of one group from its fp32 min and max.
-__device__ __forceinline__ GroupParams group_params(float mn, float mx) {
+// levels = 2^b - 1: 3 for 2-bit codes, 15 for 4-bit codes.
+__device__ __forceinline__ GroupParams group_params(float mn, float mx, float levels = 3.0f) {
     GroupParams p;
     float range = __fsub_rn(mx, mn);
-    float s32 = __fdiv_rn(range, 3.0f);
+    float s32 = __fdiv_rn(range, levels);
     __half sh = __float2half_rn(s32);
     __half zh = __float2half_rn(mn);
     p.s = __half2float(sh);
@@ -59,17 +60,6 @@ __device__ __forceinline__ GroupParams group_params(float mn, float mx) {
     p.inv = (p.s != 0.0f) ? __frcp_rn(p.s) : 0.0f;
     p.meta = (uint32_t)__half_as_ushort(sh) | ((uint32_t)__half_as_ushort(zh) << 16);
     return p;
-}
-
-__device__ __forceinline__ uint32_t quant_code(float r, const GroupParams& p) {
-    float t = __fmul_rn(__fsub_rn(r, p.z), p.inv);
-    float q = rintf(t);
-    q = fminf(fmaxf(q, 0.0f), 3.0f);
-    return (uint32_t)q;
-}
-
-__device__ __forceinline__ float dequant(uint32_t q, float s, float z) {
-    return __fmaf_rn((float)q, s, z);
 }
 
 // --------------------------------------------- Blackwell packed fp32 pairs --
@@ -85,6 +75,7 @@ __device__ __forceinline__ float2 f2_add(float2 a, float2 b) { return __fadd2_rn
 // addition directly.  In the quantiser the clamp of t = (r - z) * inv sits
 // between the product and the rounding addition.
 __device__ __forceinline__ float2 f2_mul(float2 a, float2 b) { return __fmul2_rn(a, b); }
+
 __device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 __device__ __forceinline__ float2 f2_sub(float2 a, float2 b) {
     return __ffma2_rn(b, make_float2(-1.0f, -1.0f), a);

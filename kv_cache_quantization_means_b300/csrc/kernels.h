@@ -11,10 +11,11 @@ struct EncodeArgs {
     int64_t head_stride, token_stride, n_tokens;
     const uint16_t* cent;   // [H][C][D] or nullptr
     const uint8_t* ids;     // [H][cap], rows tok_offset.. (C > 0)
-    uint32_t* codes;        // [S][H][cap][D/16]
+    uint32_t* codes;        // [S][H][cap][D*bits/32]
     uint32_t* meta;         // [S][H][cap][D/G]
     int64_t cap, tok_offset;
     int H, C, S;
+    int bits;               // code width: 2 or 4
 };
 
 struct DecodeArgs {
@@ -29,6 +30,7 @@ struct DecodeArgs {
     uint16_t* out;
     int64_t out_head_stride, out_token_stride;
     int H, C, S;
+    int bits;                     // code width: 2 or 4
 };
 
 struct AssignArgs {

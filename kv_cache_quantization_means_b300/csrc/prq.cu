@@ -4,14 +4,17 @@
 // token's centroid) and sec. 2B items 1-3 (re-quantise the residual stage by
 // stage; decode = dequantise, sum the stages, add the centroid back).
 //
-// Both kernels stream HBM.  In the encoder a thread owns one quantisation
-// group of a token row (G channels; two threads share a group of 128), so the
-// group's min/max, scale, zero-point and reciprocal are formed once per
-// group; its CPT = min(G, 64) channels arrive as 16-byte bf16 vectors and its
-// codes leave as one vector store per stage.  In the write-heavy decoder a
-// thread owns 16 consecutive channels, so a warp's stores cover whole
-// contiguous row segments.  Every load of a row is issued before any of its
-// arithmetic.
+// Both kernels stream HBM.  In the encoder a thread owns CPT = min(G, 32)
+// consecutive channels of a token row -- a whole group, or a 1/TPG share of a
+// 64- or 128-channel group whose extremes are combined with shuffles -- so
+// the group's scale, zero-point and reciprocal are formed once; its channels
+// arrive as 16-byte bf16 vectors and its codes leave as one vector store per
+// stage.  In the write-heavy decoder a thread owns 16 consecutive channels,
+// so a warp's stores cover whole contiguous row segments.  Every load of a
+// row is issued before any of its arithmetic.  Codes are 2-bit (the QVG
+// codec) or 4-bit (the PRQ_INT4 variant of the KV Cache Quantization for
+// Self-Forcing Video Generation study, read as the same scheme with 15
+// steps); B is a template parameter of both kernels.
 #include "common.cuh"
 #include "kernels.h"
 #include "prq16.cuh"
@@ -33,7 +36,7 @@ struct Map16 {
     static constexpr int RPS = RPW * (kThreads / 32);    // rows per CTA step
 };
 
-template <int D, int G>
+template <int D, int G, int B>
 struct GMap {
     static constexpr int CPT = G < 32 ? G : 32;   // channels per thread
     static constexpr int TPG = G / CPT;           // threads per group (1 or 2)
@@ -41,7 +44,8 @@ struct GMap {
     static constexpr int RPW = 32 / TPR;          // rows per warp
     static constexpr int RPC = RPW * (kThreads / 32);
     static constexpr int NV = CPT / 8;            // 16-byte bf16 vectors per thread
-    static constexpr int NW = CPT / 16;           // code words per thread and stage
+    static constexpr int NW = CPT * B / 32;       // code words per thread and stage
+    static constexpr int WPR = D * B / 32;        // code words per row and stage
 };
 
 // 16-byte load through L1 (a thread's consecutive vectors share sectors).
@@ -71,9 +75,9 @@ __device__ __forceinline__ void load_words(const uint32_t* p, uint32_t* w) {
     }
 }
 
-template <int D, int G, bool HAS_C>
+template <int D, int G, bool HAS_C, int B>
 __global__ void __launch_bounds__(kThreads, 4) prq_encode_kernel(EncodeArgs a) {
-    using M = GMap<D, G>;
+    using M = GMap<D, G, B>;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t = lane % M::TPR;
     const int h = blockIdx.y;
@@ -108,10 +112,10 @@ __global__ void __launch_bounds__(kThreads, 4) prq_encode_kernel(EncodeArgs a) {
     const int64_t stage_rows = (int64_t)a.H * a.cap;
     for (int s = 0; s < a.S; ++s) {
         uint32_t code[M::NW], meta;
-        quant_stage<M::CPT, M::TPG>(r, s + 1 < a.S, nullptr, code, meta);
+        quant_stage<M::CPT, M::TPG, B>(r, s + 1 < a.S, nullptr, code, meta);
         if (valid) {
             const int64_t srow = (int64_t)s * stage_rows + row;
-            store_words<M::NW>(a.codes + srow * (D / 16) + t * M::NW, code);
+            store_words<M::NW>(a.codes + srow * M::WPR + t * M::NW, code);
             if (t % M::TPG == 0) a.meta[srow * (D / G) + t / M::TPG] = meta;
         }
     }
@@ -127,7 +131,7 @@ __device__ __forceinline__ int chunk_of(const int64_t* offs, int n_chunks, int64
     return lo;
 }
 
-template <int D, int G, bool HAS_C, bool VERSIONED>
+template <int D, int G, bool HAS_C, bool VERSIONED, int B>
 __global__ void __launch_bounds__(kThreads, 4) prq_decode_kernel(DecodeArgs a) {
     using M = Map16<D>;
     constexpr int NR = kDecRowsPerThread;
@@ -144,13 +148,14 @@ __global__ void __launch_bounds__(kThreads, 4) prq_decode_kernel(DecodeArgs a) {
     const int64_t n_rows = a.tok_end - a.tok_begin;
     const int64_t base = (int64_t)blockIdx.x * M::RPS * NR + (int64_t)warp * M::RPW + lane / M::TPR;
     const int64_t stage_rows = (int64_t)a.H * a.cap;
-    constexpr int WPR = D / 16, MPR = D / G;
+    constexpr int WPT = 16 * B / 32;          // code words per thread and stage (1 or 2)
+    constexpr int WPR = D * B / 32, MPR = D / G;
     const int mi = (t * 16) / G;
 
     int64_t ii[NR];
     bool ok[NR];
     int id[NR];
-    uint32_t code[NR][kMaxStages], meta[NR][kMaxStages];
+    uint32_t code[NR][kMaxStages][WPT], meta[NR][kMaxStages];
 #pragma unroll
     for (int k = 0; k < NR; ++k) {
         ii[k] = base + (int64_t)k * M::RPS;
@@ -160,11 +165,12 @@ __global__ void __launch_bounds__(kThreads, 4) prq_decode_kernel(DecodeArgs a) {
         if (HAS_C && ok[k]) id[k] = a.ids[row];
 #pragma unroll
         for (int s = 0; s < kMaxStages; ++s) {
-            code[k][s] = 0;
+#pragma unroll
+            for (int w = 0; w < WPT; ++w) code[k][s][w] = 0;
             meta[k][s] = 0;
             if (s < a.S && ok[k]) {
                 const int64_t srow = (int64_t)s * stage_rows + row;
-                code[k][s] = __ldg(a.codes + srow * WPR + t);
+                load_words<WPT>(a.codes + srow * WPR + t * WPT, code[k][s]);
                 meta[k][s] = __ldg(a.meta + srow * MPR + mi);
             }
         }
@@ -189,8 +195,15 @@ __global__ void __launch_bounds__(kThreads, 4) prq_decode_kernel(DecodeArgs a) {
             for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
         }
 #pragma unroll
-        for (int s = 0; s < kMaxStages; ++s)
-            if (s < a.S) dequant_add16(acc, code[k][s], meta[k][s]);
+        for (int s = 0; s < kMaxStages; ++s) {
+            if (s >= a.S) continue;
+            if constexpr (B == 2) {
+                dequant_add16(acc, code[k][s][0], meta[k][s]);
+            } else {
+                dequant_add8x4(acc, code[k][s][0], meta[k][s]);
+                dequant_add8x4(acc + 8, code[k][s][1], meta[k][s]);
+            }
+        }
         uint4 o0, o1;
         pack16_bf16(acc, o0, o1);
         uint16_t* op = a.out + (int64_t)h * a.out_head_stride + ii[k] * a.out_token_stride + t * 16;
@@ -199,32 +212,46 @@ __global__ void __launch_bounds__(kThreads, 4) prq_decode_kernel(DecodeArgs a) {
     }
 }
 
+template <int D, int G, int B>
+cudaError_t encode_dgb(const EncodeArgs& a, cudaStream_t s) {
+    using M = GMap<D, G, B>;
+    dim3 grid((unsigned)((a.n_tokens + M::RPC - 1) / M::RPC), (unsigned)a.H);
+    if (a.C > 0) prq_encode_kernel<D, G, true, B><<<grid, kThreads, 0, s>>>(a);
+    else prq_encode_kernel<D, G, false, B><<<grid, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
 template <int D, int G>
 cudaError_t encode_dg(const EncodeArgs& a, cudaStream_t s) {
-    using M = GMap<D, G>;
     if (a.n_tokens == 0) return cudaSuccess;
-    dim3 grid((unsigned)((a.n_tokens + M::RPC - 1) / M::RPC), (unsigned)a.H);
-    if (a.C > 0) prq_encode_kernel<D, G, true><<<grid, kThreads, 0, s>>>(a);
-    else prq_encode_kernel<D, G, false><<<grid, kThreads, 0, s>>>(a);
+    if (a.bits == 4) return encode_dgb<D, G, 4>(a, s);
+    if (a.bits == 2) return encode_dgb<D, G, 2>(a, s);
+    return cudaErrorInvalidValue;
+}
+
+template <int D, int G, int B>
+cudaError_t decode_dgb(const DecodeArgs& a, cudaStream_t s) {
+    using M = Map16<D>;
+    const int64_t rows = a.tok_end - a.tok_begin;
+    const int64_t rows_per_cta = (int64_t)M::RPS * kDecRowsPerThread;
+    dim3 grid((unsigned)((rows + rows_per_cta - 1) / rows_per_cta), (unsigned)a.H);
+    if (a.C > 0 && a.chunk_offset) {
+        const size_t smem = sizeof(int64_t) * (a.n_chunks + 1) + sizeof(int32_t) * a.n_chunks;
+        prq_decode_kernel<D, G, true, true, B><<<grid, kThreads, smem, s>>>(a);
+    } else if (a.C > 0) {
+        prq_decode_kernel<D, G, true, false, B><<<grid, kThreads, 0, s>>>(a);
+    } else {
+        prq_decode_kernel<D, G, false, false, B><<<grid, kThreads, 0, s>>>(a);
+    }
     return cudaGetLastError();
 }
 
 template <int D, int G>
 cudaError_t decode_dg(const DecodeArgs& a, cudaStream_t s) {
-    using M = Map16<D>;
-    const int64_t rows = a.tok_end - a.tok_begin;
-    if (rows <= 0) return cudaSuccess;
-    const int64_t rows_per_cta = (int64_t)M::RPS * kDecRowsPerThread;
-    dim3 grid((unsigned)((rows + rows_per_cta - 1) / rows_per_cta), (unsigned)a.H);
-    if (a.C > 0 && a.chunk_offset) {
-        const size_t smem = sizeof(int64_t) * (a.n_chunks + 1) + sizeof(int32_t) * a.n_chunks;
-        prq_decode_kernel<D, G, true, true><<<grid, kThreads, smem, s>>>(a);
-    } else if (a.C > 0) {
-        prq_decode_kernel<D, G, true, false><<<grid, kThreads, 0, s>>>(a);
-    } else {
-        prq_decode_kernel<D, G, false, false><<<grid, kThreads, 0, s>>>(a);
-    }
-    return cudaGetLastError();
+    if (a.tok_end - a.tok_begin <= 0) return cudaSuccess;
+    if (a.bits == 4) return decode_dgb<D, G, 4>(a, s);
+    if (a.bits == 2) return decode_dgb<D, G, 2>(a, s);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace

@@ -13,7 +13,9 @@
 //                                integer with ties to even
 //   d = fma(q, s, z)             q*s is exact, so this is q*s + z rounded once
 //   r = r - d
-// Every 16 2-bit codes go to one 32-bit word, element k at bits 2k, 2k+1.
+// Every 16 2-bit codes go to one 32-bit word, element k at bits 2k, 2k+1;
+// with 4-bit codes (levels 0..15, s = range / 15) every 8 codes go to one
+// word, element k at bits 4k .. 4k+3.
 #pragma once
 
 #include "common.cuh"
@@ -65,14 +67,26 @@ __device__ __forceinline__ uint32_t pack_codes16(const uint32_t* vb) {
     return w[0] | (w[1] << 2) | (w[2] << 4) | (w[3] << 6);
 }
 
+// Packs the low bytes of vb[0..7] (each a code q_k < 16) into one word,
+// element k at bits 4k: bytes {q0, q2, q4, q6} and {q1, q3, q5, q7} are
+// gathered, then interleaved four bits apart.
+__device__ __forceinline__ uint32_t pack_codes8x4(const uint32_t* vb) {
+    const uint32_t e = prmt(prmt(vb[0], vb[2], 0x0040u), prmt(vb[4], vb[6], 0x0040u), 0x5410u);
+    const uint32_t o = prmt(prmt(vb[1], vb[3], 0x0040u), prmt(vb[5], vb[7], 0x0040u), 0x5410u);
+    return e | (o << 4);
+}
+
 // One stage over the thread's CPT channels (a multiple of 16); the group of
 // G = CPT * TPG channels spans TPG consecutive lanes (TPG > 1: all 32 lanes
-// must call this together).  Writes CPT/16 code words to `codes`; `meta`
-// receives the group's (scale, zero) word.  When `update` the residual is
-// replaced by what the stage leaves; `acc` (may be null) gets the
-// dequantised values added.
-template <int CPT, int TPG>
+// must call this together).  B-bit codes (B = 2 or 4): writes CPT*B/32 code
+// words to `codes`; `meta` receives the group's (scale, zero) word.  When
+// `update` the residual is replaced by what the stage leaves; `acc` (may be
+// null) gets the dequantised values added.
+template <int CPT, int TPG, int B = 2>
 __device__ __forceinline__ void quant_stage(float* r, bool update, float* acc, uint32_t* codes, uint32_t& meta) {
+    static_assert(B == 2 || B == 4, "2- or 4-bit codes");
+    constexpr float L = (float)((1 << B) - 1);
+    constexpr int PER = 32 / B;                      // codes per word
     float m0 = fmin3(r[0], r[1], r[2]), M0 = fmax3(r[0], r[1], r[2]);
     float m1 = fmin3(r[3], r[4], r[5]), M1 = fmax3(r[3], r[4], r[5]);
 #pragma unroll
@@ -94,19 +108,19 @@ __device__ __forceinline__ void quant_stage(float* r, bool update, float* acc, u
     // order in which equal extremes are met
     mn = __fadd_rn(mn, 0.0f);
     mx = __fadd_rn(mx, 0.0f);
-    const GroupParams p = group_params(mn, mx);
+    const GroupParams p = group_params(mn, mx, L);
     meta = p.meta;
     const float2 z2 = make_float2(p.z, p.z), inv2 = make_float2(p.inv, p.inv);
     const float2 s2 = make_float2(p.s, p.s), m2 = make_float2(kRintMagic, kRintMagic);
 #pragma unroll
-    for (int w = 0; w < CPT / 16; ++w) {
-        uint32_t vb[16];
+    for (int w = 0; w < CPT / PER; ++w) {
+        uint32_t vb[PER];
 #pragma unroll
-        for (int k = 0; k < 16; k += 2) {
-            const int i = 16 * w + k;
+        for (int k = 0; k < PER; k += 2) {
+            const int i = PER * w + k;
             float2 t = f2_mul(f2_sub(make_float2(r[i], r[i + 1]), z2), inv2);
-            t.x = fminf(fmaxf(t.x, 0.0f), 3.0f);
-            t.y = fminf(fmaxf(t.y, 0.0f), 3.0f);
+            t.x = fminf(fmaxf(t.x, 0.0f), L);
+            t.y = fminf(fmaxf(t.y, 0.0f), L);
             const float2 v = f2_add(t, m2);             // 1.5*2^23 + q exactly
             vb[k] = __float_as_uint(v.x);
             vb[k + 1] = __float_as_uint(v.y);
@@ -123,7 +137,8 @@ __device__ __forceinline__ void quant_stage(float* r, bool update, float* acc, u
                 }
             }
         }
-        codes[w] = pack_codes16(vb);
+        if constexpr (B == 2) codes[w] = pack_codes16(vb);
+        else codes[w] = pack_codes8x4(vb);
     }
 }
 
@@ -147,6 +162,23 @@ __device__ __forceinline__ void dequant_add16(float* acc, uint32_t code, uint32_
     for (int k = 0; k < 16; k += 2) {
         const uint32_t ba = prmt(t[k & 3], kQMagicBits, 0x7650u | (uint32_t)(k >> 2));
         const uint32_t bb = prmt(t[(k + 1) & 3], kQMagicBits, 0x7650u | (uint32_t)((k + 1) >> 2));
+        const float2 q = f2_sub(make_float2(__uint_as_float(ba), __uint_as_float(bb)), b2);
+        const float2 d = f2_fma(q, s2, z2);
+        const float2 na = f2_add(make_float2(acc[k], acc[k + 1]), d);
+        acc[k] = na.x; acc[k + 1] = na.y;
+    }
+}
+
+// acc[k] += q_k * s + z for the 8 four-bit codes of `code` (element k at bits 4k).
+__device__ __forceinline__ void dequant_add8x4(float* acc, uint32_t code, uint32_t meta) {
+    const float s = f16_bits_to_f32(meta), z = f16_bits_to_f32(meta >> 16);
+    const float2 s2 = make_float2(s, s), z2 = make_float2(z, z);
+    const float2 b2 = make_float2(8388608.0f, 8388608.0f);
+    const uint32_t t[2] = {code & 0x0F0F0F0Fu, (code >> 4) & 0x0F0F0F0Fu};   // byte j of t[i] = q_{2j+i}
+#pragma unroll
+    for (int k = 0; k < 8; k += 2) {
+        const uint32_t ba = prmt(t[0], kQMagicBits, 0x7650u | (uint32_t)(k >> 1));
+        const uint32_t bb = prmt(t[1], kQMagicBits, 0x7650u | (uint32_t)(k >> 1));
         const float2 q = f2_sub(make_float2(__uint_as_float(ba), __uint_as_float(bb)), b2);
         const float2 d = f2_fma(q, s2, z2);
         const float2 na = f2_add(make_float2(acc[k], acc[k + 1]), d);

@@ -40,7 +40,7 @@ class Encoded:
 
     def codes(self):
         c = self.cfg
-        return u32(self.bufs["codes"]).reshape(c.num_stages, c.num_heads, self.cap, c.head_dim // 16)
+        return u32(self.bufs["codes"]).reshape(c.num_stages, c.num_heads, self.cap, c.head_dim * c.bits // 32)
 
     def meta(self):
         c = self.cfg

@@ -47,7 +47,7 @@ def cfg(Q, H=2, D=64, C=16, T=3, S=2, G=64, bits=2):
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(bits=4), 2), (dict(D=48), 2), (dict(G=48), 2), (dict(D=64, G=128), 1), (dict(S=0), 2),
+    (dict(bits=3), 2), (dict(bits=8), 2), (dict(D=48), 2), (dict(G=48), 2), (dict(D=64, G=128), 1), (dict(S=0), 2),
     (dict(S=5), 2), (dict(C=300), 2), (dict(C=-1), 2), (dict(D=256, C=16), 2), (dict(H=0), 1),
 ])
 def test_bad_configs_rejected(Q, kw, status):
@@ -59,14 +59,24 @@ def test_bad_configs_rejected(Q, kw, status):
 def test_encoded_bytes_closed_form(Q):
     """Buffer sizes from the ABI equal the closed form S*b + 32*S/G + 8/D +
     16*C*V/N bits per element."""
-    for (H, D, C, S, G, N, V) in [(2, 64, 16, 2, 64, 1560, 1), (12, 128, 256, 2, 64, 32760, 1),
-                                  (12, 128, 256, 2, 64, 187200, 5), (40, 128, 256, 3, 128, 81920, 1),
-                                  (16, 128, 0, 2, 64, 16384, 1)]:
-        c = Q.config(H, D, C, 1, S, G)
+    for (H, D, C, S, G, N, V, b) in [(2, 64, 16, 2, 64, 1560, 1, 2), (12, 128, 256, 2, 64, 32760, 1, 2),
+                                     (12, 128, 256, 2, 64, 187200, 5, 2), (40, 128, 256, 3, 128, 81920, 1, 2),
+                                     (16, 128, 0, 2, 64, 16384, 1, 2), (12, 128, 256, 1, 128, 32760, 1, 4),
+                                     (2, 32, 0, 4, 16, 777, 1, 4)]:
+        c = Q.config(H, D, C, 1, S, G, b)
         cb, mb, ib, xb = Q.qvg_encoded_bytes(c, N, V)
         bits = Fraction(8 * (cb + mb + ib + xb), H * N * D)
-        want = Fraction(2 * S) + Fraction(32 * S, G) + ((Fraction(8, D) + Fraction(16 * C * V, N)) if C else 0)
+        want = Fraction(b * S) + Fraction(32 * S, G) + ((Fraction(8, D) + Fraction(16 * C * V, N)) if C else 0)
         assert bits == want
+
+
+def test_cross_layer_codec_is_two_bit(Q):
+    """4-bit codes are a QVG option; the cross-layer codec refuses them on
+    the host, before any launch."""
+    c = Q.config(2, 128, 0, 0, 2, 64, 4)
+    with pytest.raises(Q.QvgError) as e:
+        Q.coral_predict_encode(c, None, None, None, 0, None, None, None, stream=0)
+    assert e.value.status == 2
 
 
 def test_workspace_bytes_monotone(Q):

@@ -22,7 +22,7 @@ def mixture(rng, N, D, M=8, spread=1.0, noise=0.1):
     return SY.f64_to_bf16_bits(centres[lab] + noise * rng.standard_normal((N, D)))
 
 
-def check_unit(oracle, xh, enc, dec, h, C, T, S, G, offset=0, n=None, warm=None):
+def check_unit(oracle, xh, enc, dec, h, C, T, S, G, offset=0, n=None, warm=None, b=2):
     n = xh.shape[0] if n is None else n
     sl = slice(offset, offset + n)
     if C > 0:
@@ -31,10 +31,10 @@ def check_unit(oracle, xh, enc, dec, h, C, T, S, G, offset=0, n=None, warm=None)
         np.testing.assert_array_equal(enc.ids()[h, sl], oi, err_msg=f"ids head {h}")
     else:
         oc, oi = None, None
-    rc, rm = oracle.prq_encode(xh, oc, oi, S, G)
+    rc, rm = oracle.prq_encode(xh, oc, oi, S, G, b)
     np.testing.assert_array_equal(enc.codes()[:, h, sl], rc, err_msg=f"codes head {h}")
     np.testing.assert_array_equal(enc.meta()[:, h, sl], rm, err_msg=f"meta head {h}")
-    np.testing.assert_array_equal(dec[h], oracle.decode(rc, rm, oi, oc, G), err_msg=f"decode head {h}")
+    np.testing.assert_array_equal(dec[h], oracle.decode(rc, rm, oi, oc, G, b), err_msg=f"decode head {h}")
 
 
 @pytest.mark.parametrize("tensor", [SY.K_TENSOR, SY.V_TENSOR])
@@ -208,3 +208,33 @@ def test_quantiser_half_integer_ties(qvg, oracle, G):
     enc, dec = run_fit_encode_decode(qvg, cfg, to_dev(xb), N, N * D, D)
     for h in range(H):
         check_unit(oracle, xb[h], enc, dec, h, 0, 0, S, G)
+
+
+@pytest.mark.parametrize("D,G,S,C", [
+    (128, 64, 2, 0), (128, 128, 1, 0), (128, 16, 3, 0), (64, 32, 2, 16), (32, 16, 4, 0), (256, 64, 2, 0),
+    (128, 64, 2, 256), (128, 128, 3, 100),
+])
+def test_four_bit_codes_bit_exact(qvg, oracle, D, G, S, C):
+    """4-bit codes (the PRQ_INT4 variant): fit, encode and decode match the
+    oracle bit for bit on ragged shapes (777 tokens)."""
+    rng = np.random.default_rng(D * 3 + G + S + C + 4)
+    H, N, T = 3, 777, 2
+    xb = np.stack([mixture(rng, N, D, M=12, spread=1.5, noise=0.2) for _ in range(H)])
+    cfg = qvg.config(H, D, C, T, S, G, 4)
+    enc, dec = run_fit_encode_decode(qvg, cfg, to_dev(xb), N, N * D, D)
+    for h in range(H):
+        check_unit(oracle, xb[h], enc, dec, h, C, T, S, G, b=4)
+
+
+@pytest.mark.parametrize("G", [16, 64, 128])
+def test_four_bit_half_integer_ties(qvg, oracle, G):
+    """The coarse-grid tie case of the quantiser, with 15 steps."""
+    rng = np.random.default_rng(99 + G)
+    H, N, D, S = 2, 300, 128, 2
+    grid = rng.integers(-40, 41, size=(H, N, D)).astype(np.float64) / 8.0
+    grid[:, ::29, 7] = -700.0
+    xb = SY.f64_to_bf16_bits(grid)
+    cfg = qvg.config(H, D, 0, 0, S, G, 4)
+    enc, dec = run_fit_encode_decode(qvg, cfg, to_dev(xb), N, N * D, D)
+    for h in range(H):
+        check_unit(oracle, xb[h], enc, dec, h, 0, 0, S, G, b=4)

@@ -33,8 +33,8 @@ def run_stream(qvg, cfg, xb, chunk, steps, every, layout="hnd"):
     return cache, bufs, u16(out), u16(out2)
 
 
-@pytest.mark.parametrize("layout", ["hnd", "nhd"])
-def test_stream_matches_oracle(qvg, oracle, layout):
+@pytest.mark.parametrize("layout,b", [("hnd", 2), ("nhd", 2), ("nhd", 4)])
+def test_stream_matches_oracle(qvg, oracle, layout, b):
     wl = WL.STREAM
     H, D, C, T, S, G = 2, 64, 32, 2, 2, 64
     chunk, steps, every = 390, 6, 3
@@ -44,11 +44,11 @@ def test_stream_matches_oracle(qvg, oracle, layout):
     xb = np.stack([SY.mixture_unit(WL.TINY, 0, 0, h, 0, n) for h in range(H)])
     xb = SY.f64_to_bf16_bits(SY.bf16_bits_to_f32(xb).astype(np.float64)
                              + np.linspace(0, 1, n)[None, :, None] * rng.standard_normal((H, 1, D)))
-    cfg = qvg.config(H, D, C, T, S, G)
+    cfg = qvg.config(H, D, C, T, S, G, b)
     cache, bufs, dec, dec2 = run_stream(qvg, cfg, xb, chunk, steps, every, layout)
     V = cache.n_versions
     assert V == 2
-    codes = u32(bufs["codes"]).reshape(S, H, n, D // 16)
+    codes = u32(bufs["codes"]).reshape(S, H, n, D * b // 32)
     meta = u32(bufs["meta"]).reshape(S, H, n, D // G)
     ids = bufs["ids"].cpu().numpy()[: H * n].reshape(H, n).astype(np.int32)
     cents = u16(bufs["centroids"])[: V * H * C * D].reshape(V, H, C, D)
@@ -56,7 +56,7 @@ def test_stream_matches_oracle(qvg, oracle, layout):
     coff = bufs["chunk_offset"].cpu().numpy()[: steps + 1]
     assert list(coff) == [chunk * t for t in range(steps + 1)]
     for h in range(H):
-        vers, ov, oi, oc, om = oracle.stream(xb[h], chunk, steps, every, C, T, S, G)
+        vers, ov, oi, oc, om = oracle.stream(xb[h], chunk, steps, every, C, T, S, G, b)
         assert list(cver) == list(ov)
         for v in range(V):
             np.testing.assert_array_equal(cents[v, h], vers[v])
@@ -64,7 +64,7 @@ def test_stream_matches_oracle(qvg, oracle, layout):
         np.testing.assert_array_equal(codes[:, h], oc)
         np.testing.assert_array_equal(meta[:, h], om)
         want = np.concatenate([oracle.decode(oc[:, t * chunk:(t + 1) * chunk], om[:, t * chunk:(t + 1) * chunk],
-                                             oi[t * chunk:(t + 1) * chunk], vers[ov[t]], G) for t in range(steps)])
+                                             oi[t * chunk:(t + 1) * chunk], vers[ov[t]], G, b) for t in range(steps)])
         np.testing.assert_array_equal(dec[h], want)
         np.testing.assert_array_equal(dec2[h], want[chunk - 9:min(2 * chunk + 8, n)])
 
