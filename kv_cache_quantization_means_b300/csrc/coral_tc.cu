@@ -57,7 +57,7 @@ __global__ void coral_prep_kernel(const uint16_t* W, const uint16_t* U, int HD, 
 
 // --------------------------------------------------------------- lowrank
 
-constexpr int kLrStages = 4;
+constexpr int kLrStages = 8;
 constexpr int kLrThreads = 64 + 128;    // TMA warp, MMA warp, 4 epilogue warps
 
 struct LrArgs {
@@ -205,7 +205,7 @@ __device__ __forceinline__ uint4 ldg_v4_l1(const void* p) {
     return v;
 }
 
-template <int G, bool ENCODE>
+template <int G, bool ENCODE, int SM>
 __global__ void __launch_bounds__(kPrThreads, 1)
     coral_predict_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                             const __grid_constant__ CUtensorMap tm_t, const __grid_constant__ CUtensorMap tm_u,
@@ -304,23 +304,42 @@ __global__ void __launch_bounds__(kPrThreads, 1)
         // ---------------------------------------------------- epilogue
         constexpr int CPT = G < 32 ? 32 : G;      // channels per pass (whole groups, whole TMEM loads)
         constexpr int GPP = CPT / G;              // groups per pass
+        constexpr int NP = kDh / CPT;             // passes per row
+        constexpr int WPR = kDh / 16, MPR = kDh / G;
         const int e = warp - 2, g = e >> 2, q = warp & 3;
         const int row = q * 32 + lane;
         const int64_t stage_rows = (int64_t)H * a.n_tokens;
         for (int i = g; i < my_items; i += 2) {
             const int item = (int)blockIdx.x + i * (int)gridDim.x;
             const int tile = item / H, h = item % H;
-            if (!mbar_wait(tfull_bar + 8 * g, (uint32_t)(i >> 1) & 1u)) { misc[1] = 1; break; }
-            tc_fence_after();
             const int64_t n = (int64_t)tile * kT + row;
             const bool valid = n < a.n_tokens;
             const int64_t elem0 = n * HD + (int64_t)h * kDh;
             const int64_t rowoff = (int64_t)h * a.n_tokens + n;
-#pragma unroll 1
-            for (int c = 0; c < kDh / CPT; ++c) {
+            // The decoder's loads do not depend on the MMA: the codes and
+            // scale/zero words of the whole row are issued before waiting for it.
+            uint32_t code[ENCODE ? 1 : SM][WPR], meta[ENCODE ? 1 : SM][MPR];
+            if (!ENCODE) {
+#pragma unroll
+                for (int s = 0; s < SM; ++s) {
+                    const bool on = valid && s < a.S;
+                    const int64_t srow = (int64_t)s * stage_rows + rowoff;
+#pragma unroll
+                    for (int w = 0; w < WPR; w += 4) {
+                        const uint4 cw = on ? ldg_v4_l1(a.codes + srow * WPR + w) : make_uint4(0, 0, 0, 0);
+                        code[s][w] = cw.x; code[s][w + 1] = cw.y; code[s][w + 2] = cw.z; code[s][w + 3] = cw.w;
+                    }
+#pragma unroll
+                    for (int m = 0; m < MPR; ++m) meta[s][m] = on ? __ldg(a.meta + srow * MPR + m) : 0u;
+                }
+            }
+            if (!mbar_wait(tfull_bar + 8 * g, (uint32_t)(i >> 1) & 1u)) { misc[1] = 1; break; }
+            tc_fence_after();
+            // one pass of CPT channels
+            auto pass = [&](const int c) {
                 const uint32_t tcol = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)g * kDh + (uint32_t)(c * CPT);
-                // this pass's codes and scale/zero words of every stage
-                uint32_t code[kMaxStages][CPT / 16], meta[kMaxStages][GPP];
+                // the encoder's codes and scale/zero words of this pass
+                uint32_t ec[ENCODE ? SM : 1][CPT / 16], em[ENCODE ? SM : 1][GPP];
                 if (ENCODE) {
                     // residual r = x_{l+1} - pred, quantised stage by stage
                     float r[CPT];
@@ -347,38 +366,23 @@ __global__ void __launch_bounds__(kPrThreads, 1)
                         sub16(r + 32 * k, pk);
                         sub16(r + 32 * k + 16, pk + 16);
                     }
+#pragma unroll 1
                     for (int s = 0; s < a.S; ++s) {
 #pragma unroll
                         for (int gi = 0; gi < GPP; ++gi) {
                             uint32_t cw[G / 16], m;
                             quant_stage<G, 1>(r + gi * G, s + 1 < a.S, nullptr, cw, m);
 #pragma unroll
-                            for (int w = 0; w < G / 16; ++w) code[s][gi * (G / 16) + w] = cw[w];
-                            meta[s][gi] = m;
+                            for (int w = 0; w < G / 16; ++w) ec[s][(gi * G) / 16 + w] = cw[w];
+                            em[s][gi] = m;
                             if (valid) {
                                 const int64_t srow = (int64_t)s * stage_rows + rowoff;
-                                uint32_t* cp = a.codes + srow * (kDh / 16) + (c * CPT + gi * G) / 16;
+                                uint32_t* cp = a.codes + srow * WPR + (c * CPT + gi * G) / 16;
 #pragma unroll
                                 for (int w = 0; w < G / 16; ++w) cp[w] = cw[w];
-                                a.meta[srow * (kDh / G) + (c * CPT) / G + gi] = m;
+                                a.meta[srow * MPR + c * GPP + gi] = m;
                             }
                         }
-                    }
-                } else if (valid) {
-                    for (int s = 0; s < a.S; ++s) {
-                        const int64_t srow = (int64_t)s * stage_rows + rowoff;
-                        const uint32_t* cp = a.codes + srow * (kDh / 16) + (c * CPT) / 16;
-                        if constexpr (CPT == 64) {
-                            const uint4 cw = ldg_v4_l1(cp);
-                            code[s][0] = cw.x; code[s][1] = cw.y;
-                            code[s][2] = cw.z; code[s][3] = cw.w;
-                        } else {
-                            const uint2 cw = __ldg(reinterpret_cast<const uint2*>(cp));
-                            code[s][0] = cw.x; code[s][1] = cw.y;
-                        }
-#pragma unroll
-                        for (int gi = 0; gi < GPP; ++gi)
-                            meta[s][gi] = __ldg(a.meta + srow * (kDh / G) + (c * CPT) / G + gi);
                     }
                 }
                 // x_hat = ((pred + d_1) + d_2) + ..., identical in encoder and decoder
@@ -397,10 +401,20 @@ __global__ void __launch_bounds__(kPrThreads, 1)
                         *reinterpret_cast<float4*>(a.pred_out + elem0 + c * CPT + jj) =
                             make_float4(acc[jj], acc[jj + 1], acc[jj + 2], acc[jj + 3]);
                 }
-                for (int s = 0; s < a.S; ++s) {
+                if constexpr (ENCODE) {
+#pragma unroll 1
+                    for (int s = 0; s < a.S; ++s) {
 #pragma unroll
-                    for (int w = 0; w < CPT / 16; ++w)
-                        dequant_add16(acc + 16 * w, code[s][w], meta[s][(16 * w) / G]);
+                        for (int w = 0; w < CPT / 16; ++w) dequant_add16(acc + 16 * w, ec[s][w], em[s][(16 * w) / G]);
+                    }
+                } else {
+#pragma unroll
+                    for (int s = 0; s < SM; ++s) {
+                        if (s >= a.S) break;
+#pragma unroll
+                        for (int w = 0; w < CPT / 16; ++w)
+                            dequant_add16(acc + 16 * w, code[s][(c * CPT) / 16 + w], meta[s][(c * CPT + 16 * w) / G]);
+                    }
                 }
                 if (valid) {
                     uint16_t* op = a.xhat + elem0 + c * CPT;
@@ -412,6 +426,15 @@ __global__ void __launch_bounds__(kPrThreads, 1)
                         *reinterpret_cast<uint4*>(op + k + 8) = o1;
                     }
                 }
+            };
+            if constexpr (ENCODE) {
+                // rolled: a pass's residual and codes are all the encoder keeps
+#pragma unroll 1
+                for (int c = 0; c < NP; ++c) pass(c);
+            } else {
+                // unrolled: the prefetched codes are indexed with constants
+#pragma unroll
+                for (int c = 0; c < NP; ++c) pass(c);
             }
             // accumulator drained
             tc_fence_before();
@@ -464,7 +487,9 @@ cudaError_t coral_tc_g(bool encode, const CoralArgs& a, const CoralTcScratch& w,
     coral_lowrank_tc_kernel<<<(unsigned)tiles, kLrThreads, lr_req, s>>>(tx, tw, la);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const size_t pr_smem = (size_t)kPrStages * kStageBytes + 8 * (2 * kPrStages + 4) + 32 + 1024;
-    auto kern = encode ? coral_predict_tc_kernel<G, true> : coral_predict_tc_kernel<G, false>;
+    // SM: stages held in registers by the epilogue (2, or 4 when S > 2)
+    auto kern = a.S <= 2 ? (encode ? coral_predict_tc_kernel<G, true, 2> : coral_predict_tc_kernel<G, false, 2>)
+                         : (encode ? coral_predict_tc_kernel<G, true, 4> : coral_predict_tc_kernel<G, false, 4>);
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pr_smem);
     if (e != cudaSuccess) return e;
     PrArgs pa;
