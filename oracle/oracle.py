@@ -57,6 +57,7 @@ def lib():
         L.or_coral_encode_layer.argtypes = [P, P, I64, I32, I32, P, P, P, I32, P, I32, I32, P, P, P, P]
         L.or_coral_decode_layer.argtypes = [P, I64, I32, I32, P, P, P, I32, P, I32, I32, P, P, P]
         L.or_bits_per_element.argtypes = [I32, I32, I32, I32, I32, I64, I32]
+        L.or_coral_fit_block.argtypes = [P, P, I64, I32, I32, P, P, I32, P, P]
         L.or_bits_per_element.restype = ctypes.c_double
         _lib = L
     return _lib
@@ -206,6 +207,22 @@ def coral_decode_layer(xh_prev, codes, meta, B, U, W, H, D, G, pred_in=None):
     lib().or_coral_decode_layer(_p(xp), N, H, D, _p(cv(B)), _p(cv(U)), _p(cv(W)), R, _p(pi), S, G,
                                 _p(codes), _p(meta), _p(xh_next))
     return xh_next
+
+
+def coral_fit_block(xh, y, U, W, H, D):
+    """Adapted block predictors (Coral-KV adapted configuration): per head
+    the ridge-regularised least-squares B_h for y - U_h t = B_h x_hat.
+    Returns (B bf16 bits [H][D][D], Z = B^T before rounding, fp64 [H][D][D]
+    laid out as B[h][o][i])."""
+    xh = _c(xh, np.uint16)
+    y = _c(y, np.uint16)
+    N = xh.shape[0]
+    R = 0 if U is None else U.shape[1]
+    B = np.empty((H, D, D), np.uint16)
+    Z = np.empty((H, D, D), np.float64)
+    cv = (lambda a: None if a is None else _c(a, np.uint16))
+    lib().or_coral_fit_block(_p(xh), _p(y), N, H, D, _p(cv(U)), _p(cv(W)), R, _p(B), _p(Z))
+    return B, Z
 
 
 def bits_per_element(S, b, G, C, D, N, V=1):

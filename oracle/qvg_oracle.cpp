@@ -34,6 +34,7 @@
 //
 // Parity pins for every function live in tests/test_oracle_pins.py.
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -406,6 +407,92 @@ void or_coral_decode_layer(const uint16_t* xh_prev, int64_t N, int H, int D, con
                                             meta + (((int64_t)s * H + h) * N + n) * (D / G), i, G, 2);
                 xh_next[e] = to_bf16((double)acc);
             }
+}
+
+// -------------------------------- Coral-KV: adapted block predictors -----
+
+// Adapted configuration of the Coral-KV pages: the per-head block B_h of the
+// predictor is rebuilt for the current video while the offline low-rank part
+// (U, W) is kept.  Reading: per head h, B_h minimises
+//     sum_n || y_{n,h} - L_{n,h} - B x_{n,h} ||^2 + lambda_h ||B||_F^2,
+// with x = the reconstruction x_hat_l, y = x_{l+1}, L = U_h t_n the low-rank
+// part of the prediction (t_n = W^T x_hat_n) and a tiny ridge
+// lambda_h = 2^-20 * trace(G_h) / D that only matters for (near-)singular
+// G_h = X_h^T X_h.  Normal equations: (G_h + lambda_h I) Z = X_h^T (Y_h - L_h)
+// with Z = B_h^T, solved by Cholesky; B_h = 0 when X_h is all zero.  Every
+// sum is fp64 in token order; the result is rounded to bf16 (the predictor's
+// format).  z_out (optional, fp64 [H][D][D], Z before rounding) serves the
+// pins.  B_out: bf16 [H][D][D], B[h][o][i].
+void or_coral_fit_block(const uint16_t* xh, const uint16_t* y, int64_t N, int H, int D, const uint16_t* U,
+                        const uint16_t* W, int R, uint16_t* B_out, double* z_out) {
+    const int HD = H * D;
+    std::vector<double> t((size_t)N * (R > 0 ? R : 1), 0.0);
+    for (int64_t n = 0; n < N; ++n)
+        for (int r = 0; r < R; ++r) {
+            double acc = 0.0;
+            for (int j = 0; j < HD; ++j) acc = acc + bf16_value(W[(int64_t)j * R + r]) * bf16_value(xh[n * HD + j]);
+            t[(size_t)n * R + r] = acc;
+        }
+    std::vector<double> Gm((size_t)D * D), rhs((size_t)D * D), res(D);
+    for (int h = 0; h < H; ++h) {
+        std::fill(Gm.begin(), Gm.end(), 0.0);
+        std::fill(rhs.begin(), rhs.end(), 0.0);
+        for (int64_t n = 0; n < N; ++n) {
+            const uint16_t* xr = xh + n * HD + h * D;
+            // residual target y - L of this token
+            for (int o = 0; o < D; ++o) {
+                double low = 0.0;
+                for (int r = 0; r < R; ++r) low = low + bf16_value(U[((int64_t)h * D + o) * R + r]) * t[(size_t)n * R + r];
+                res[o] = bf16_value(y[n * HD + h * D + o]) - low;
+            }
+            for (int i = 0; i < D; ++i) {
+                const double xi = bf16_value(xr[i]);
+                for (int k = 0; k < D; ++k) Gm[(size_t)i * D + k] = Gm[(size_t)i * D + k] + xi * bf16_value(xr[k]);
+                for (int o = 0; o < D; ++o) rhs[(size_t)i * D + o] = rhs[(size_t)i * D + o] + xi * res[o];
+            }
+        }
+        double tr = 0.0;
+        for (int i = 0; i < D; ++i) tr = tr + Gm[(size_t)i * D + i];
+        uint16_t* Bh = B_out + (size_t)h * D * D;
+        if (tr == 0.0) {
+            for (int k = 0; k < D * D; ++k) Bh[k] = 0;
+            if (z_out) for (int k = 0; k < D * D; ++k) z_out[(size_t)h * D * D + k] = 0.0;
+            continue;
+        }
+        const double lambda = std::ldexp(tr / D, -20);
+        for (int i = 0; i < D; ++i) Gm[(size_t)i * D + i] = Gm[(size_t)i * D + i] + lambda;
+        // Cholesky: G = L L^T, L lower triangular, stored in place
+        for (int j = 0; j < D; ++j) {
+            double d = Gm[(size_t)j * D + j];
+            for (int k = 0; k < j; ++k) d = d - Gm[(size_t)j * D + k] * Gm[(size_t)j * D + k];
+            d = std::sqrt(d);
+            Gm[(size_t)j * D + j] = d;
+            for (int i = j + 1; i < D; ++i) {
+                double v = Gm[(size_t)i * D + j];
+                for (int k = 0; k < j; ++k) v = v - Gm[(size_t)i * D + k] * Gm[(size_t)j * D + k];
+                Gm[(size_t)i * D + j] = v / d;
+            }
+        }
+        // for each output channel o: L u = rhs[:, o], then L^T z = u
+        for (int o = 0; o < D; ++o) {
+            for (int i = 0; i < D; ++i) {
+                double v = rhs[(size_t)i * D + o];
+                for (int k = 0; k < i; ++k) v = v - Gm[(size_t)i * D + k] * res[k];
+                res[i] = v / Gm[(size_t)i * D + i];
+            }
+            for (int i = D - 1; i >= 0; --i) {
+                double v = res[i];
+                for (int k = i + 1; k < D; ++k) v = v - Gm[(size_t)k * D + i] * rhs[(size_t)k * D + o];
+                rhs[(size_t)i * D + o] = v / Gm[(size_t)i * D + i];   // column o now holds z
+            }
+        }
+        for (int o = 0; o < D; ++o)
+            for (int i = 0; i < D; ++i) {
+                const double z = rhs[(size_t)i * D + o];                // Z[i][o] = B[o][i]
+                Bh[(size_t)o * D + i] = to_bf16(z);
+                if (z_out) z_out[((size_t)h * D + o) * D + i] = z;
+            }
+    }
 }
 
 // ------------------------------------------------------------- sizes -------

@@ -46,6 +46,11 @@ MUTATIONS = {
     "coral residual sign": ("r[i] = bf16_float(x_next[e]) - pv;", "r[i] = bf16_float(x_next[e]) + pv;"),
     "stream ignores warm start": ("const uint16_t* warm = nv ? versions + (size_t)(nv - 1) * C * D : nullptr;",
                                   "const uint16_t* warm = nullptr;"),
+    "ridge sign": ("for (int i = 0; i < D; ++i) Gm[(size_t)i * D + i] = Gm[(size_t)i * D + i] + lambda;",
+                   "for (int i = 0; i < D; ++i) Gm[(size_t)i * D + i] = Gm[(size_t)i * D + i] - lambda;"),
+    "fit low-rank sign": ("res[o] = bf16_value(y[n * HD + h * D + o]) - low;",
+                          "res[o] = bf16_value(y[n * HD + h * D + o]) + low;"),
+    "fit output transposed": ("Bh[(size_t)o * D + i] = to_bf16(z);", "Bh[(size_t)i * D + o] = to_bf16(z);"),
     "size meta term": ("double bits = (double)S * b + 32.0 * S / G;", "double bits = (double)S * b + 16.0 * S / G;"),
     "bf16 rounding truncates": ("double r = std::nearbyint(n); // default rounding mode: ties to even",
                                 "double r = std::trunc(n);"),
@@ -78,6 +83,9 @@ PIN_CALLS = [
     (PINS.test_coral_identity_predictor_gives_exact_reconstruction, {}),
     (PINS.test_coral_zero_predictor_is_plain_prq, {}),
     (PINS.test_coral_decode_matches_encoder_reconstruction, {}),
+    (PINS.test_coral_fit_block_matches_library_solve, {}),
+    (PINS.test_coral_fit_block_recovers_an_exact_block, {}),
+    (PINS.test_coral_fit_block_zero_input, {}),
 ]
 
 

@@ -531,3 +531,62 @@ def test_splitmix64_reference_values():
     # SplitMix64 seeded with 0: first outputs of the published generator
     got = [int(v) for v in SY.draws(0, np.arange(3, dtype=np.uint64))]
     assert got == [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F]
+
+
+# ------------------------------------------------ Coral adapted predictors --
+
+def _fit_inputs(seed, N=400, H=2, D=16, R=4):
+    rng = np.random.default_rng(seed)
+    xh = SY.f64_to_bf16_bits(rng.standard_normal((N, H * D)))
+    y = SY.f64_to_bf16_bits(rng.standard_normal((N, H * D)))
+    U = SY.f64_to_bf16_bits(rng.standard_normal((H * D, R)) * 0.2)
+    W = SY.f64_to_bf16_bits(rng.standard_normal((H * D, R)) * 0.2)
+    return xh, y, U, W, H, D
+
+
+def test_coral_fit_block_matches_library_solve(oracle):
+    """The oracle's Cholesky solve of the ridge normal equations agrees with
+    numpy's LU solve (LAPACK) of the same equations, built here in fp64."""
+    xh, y, U, W, H, D = _fit_inputs(11)
+    B, Z = oracle.coral_fit_block(xh, y, U, W, H, D)
+    x = f32(xh).astype(np.float64)
+    t = x @ f32(W).astype(np.float64)
+    for h in range(H):
+        X = x[:, h * D:(h + 1) * D]
+        L = t @ f32(U[h * D:(h + 1) * D]).astype(np.float64).T
+        Rm = f32(y[:, h * D:(h + 1) * D]).astype(np.float64) - L
+        G = X.T @ X
+        lam = np.ldexp(np.trace(G) / D, -20)
+        Zref = np.linalg.solve(G + lam * np.eye(D), X.T @ Rm)       # [i][o] = B[o][i]
+        np.testing.assert_allclose(Z[h], Zref.T, rtol=1e-9, atol=1e-12)
+        # B is Z rounded to bf16
+        assert np.array_equal(B[h], SY.f64_to_bf16_bits(Zref.T)) or \
+            np.max(np.abs(f32(B[h]) - Zref.T) / np.maximum(np.abs(Zref.T), 1e-30)) <= 2.0 ** -8
+
+
+def test_coral_fit_block_recovers_an_exact_block(oracle):
+    """Tokens that are unit vectors e_i (k copies each) and targets y = B x
+    with a bf16 block B and no low-rank part: G = k I, so the ridge solution
+    is B / (1 + 2^-20), which rounds back to B exactly."""
+    rng = np.random.default_rng(12)
+    H, D, k = 2, 16, 5
+    B0 = SY.f64_to_bf16_bits(rng.standard_normal((H, D, D)))
+    N = k * D
+    x = np.zeros((N, H * D))
+    yv = np.zeros((N, H * D))
+    for n in range(N):
+        i = n % D
+        for h in range(H):
+            x[n, h * D + i] = 1.0
+            yv[n, h * D:(h + 1) * D] = f32(B0[h][:, i])
+    xh, y = SY.f64_to_bf16_bits(x), SY.f64_to_bf16_bits(yv)
+    B, Z = oracle.coral_fit_block(xh, y, None, None, H, D)
+    assert np.array_equal(B, B0)
+    np.testing.assert_allclose(Z, f32(B0).astype(np.float64) / (1 + 2.0 ** -20), rtol=1e-12)
+
+
+def test_coral_fit_block_zero_input(oracle):
+    xh, y, U, W, H, D = _fit_inputs(13)
+    xh = np.zeros_like(xh)
+    B, Z = oracle.coral_fit_block(xh, y, U, W, H, D)
+    assert np.all(B == 0) and np.all(Z == 0)
