@@ -188,18 +188,28 @@ class CoralStep:
     subtracted from layer l+1 and the residual PRQ-coded (encoder), and the
     chain is decoded back (decoder)."""
 
-    def __init__(self, Q, wl, layers):
+    def __init__(self, Q, wl, layers, adapted=False):
         import torch
         from synth import gpu as SG
-        self.Q, self.wl, self.L = Q, wl, layers
+        self.Q, self.wl, self.L, self.adapted = Q, wl, layers, adapted
         H, D, N, S, G = wl.heads, wl.head_dim, wl.tokens, wl.stages, wl.group_size
         self.cfg = Q.config(H, D, 0, 0, S, G)
         self.N, self.H, self.D, self.HD = N, H, D, H * D
         self.x = [SG.coral_chain_gpu(wl, t, n_layers=layers) for t in (0, 1)]        # [L][N][HD]
-        self.preds = []
+        self.preds, self.keep = [], []
         for l in range(layers - 1):
             B, U, W = SG.coral_predictor_device(wl, l)
+            self.keep.append((B, U, W))
             self.preds.append(Q.qvg.coral_predictor(B=B.data_ptr(), U=U.data_ptr(), W=W.data_ptr(), rank=wl.rank))
+        # adapted configuration: per tensor and layer a block refit into its own buffer
+        self.fit_B, self.fit_preds = [], []
+        if adapted:
+            for t in (0, 1):
+                bs = [torch.empty(H * D * D, dtype=torch.int16, device="cuda") for _ in range(layers - 1)]
+                self.fit_B.append(bs)
+                self.fit_preds.append([Q.qvg.coral_predictor(B=bs[l].data_ptr(), U=self.keep[l][1].data_ptr(),
+                                                             W=self.keep[l][2].data_ptr(), rank=wl.rank)
+                                       for l in range(layers - 1)])
         self.codes = [[torch.empty(S * H * N * D // 16, dtype=torch.int32, device="cuda") for _ in range(layers)]
                       for _ in (0, 1)]
         self.meta = [[torch.empty(S * H * N * D // G, dtype=torch.int32, device="cuda") for _ in range(layers)]
@@ -208,18 +218,24 @@ class CoralStep:
         self.dec = [torch.empty((layers, N, H * D), dtype=torch.int16, device="cuda") for _ in (0, 1)]
         self.ws = Q.alloc_workspace(self.cfg, N)
         self.bytes_per_step = 2 * layers * N * H * D * 2
-        # per tensor and direction: layer 0 (one kernel), then prep + low-rank + predict per layer
-        self.launches_per_step = 2 * (1 + 3 * (layers - 1)) * 2
+        # per tensor and direction: layer 0 (one kernel), then prep + low-rank + predict per layer;
+        # adapted: + prep + low-rank + Gram + reduce + solve per encoded layer
+        self.launches_per_step = 2 * (1 + 3 * (layers - 1)) * 2 + (2 * 5 * (layers - 1) if adapted else 0)
+
+    def pred(self, t, l):
+        return self.fit_preds[t][l - 1] if self.adapted else self.preds[l - 1]
 
     def encode(self, t, l):
         prev = None if l == 0 else self.xh[t][l - 1]
-        pred = None if l == 0 else self.preds[l - 1]
+        pred = None if l == 0 else self.pred(t, l)
+        if self.adapted and l > 0:
+            self.Q.coral_fit_block(self.cfg, pred, prev, self.x[t][l], self.N, self.fit_B[t][l - 1], self.ws)
         self.Q.coral_predict_encode(self.cfg, pred, prev, self.x[t][l], self.N, self.codes[t][l], self.meta[t][l],
                                     self.xh[t][l], None, self.ws)
 
     def decode(self, t, l):
         prev = None if l == 0 else self.dec[t][l - 1]
-        pred = None if l == 0 else self.preds[l - 1]
+        pred = None if l == 0 else self.pred(t, l)
         self.Q.coral_predict_decode(self.cfg, pred, prev, self.N, self.codes[t][l], self.meta[t][l],
                                     self.dec[t][l], None, self.ws)
 
@@ -433,7 +449,7 @@ def run_aux(args, Q, wl, peaks, world, rank, local):
     import torch
     hbm = peaks[0]
     if args.config == "coral":
-        st = CoralStep(Q, wl, wl.layers)
+        st = CoralStep(Q, wl, wl.layers, adapted=args.adapted)
     else:
         st = StreamStep(Q, wl, wl.layers)
     st.step()
@@ -447,7 +463,8 @@ def run_aux(args, Q, wl, peaks, world, rank, local):
                "achieved": dec_bytes / t_dec / 1e9, "peak": hbm, "unit": "GB/s", "time_us": t_dec * 1e6}
         cfgb = {"workload": f"{wl.name}: {wl.layers} layers x {wl.heads} heads x head_dim {wl.head_dim} x {wl.tokens} "
                             f"tokens, K and V, closed-loop block-DPLR (rank {wl.rank}) + PRQ S={wl.stages} G={wl.group_size}, "
-                            "encode chain + decode chain"}
+                            "encode chain + decode chain" + ("; adapted: each layer's block predictors refit "
+                                                              "(least squares) before it is encoded" if args.adapted else "")}
     else:
         c = st.caches[-1][-1][0]
         lens = [st.chunk * (k + 1) for k in range(st.steps)]
@@ -483,6 +500,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--adapted", action="store_true",
+                    help="coral: refit each layer's block predictors for the current video before encoding it")
     ap.add_argument("--bits", type=int, default=None, choices=[2, 4],
                     help="code width of the QVG workloads (default: the workload's, 2)")
     args = ap.parse_args()

@@ -249,6 +249,24 @@ QVG_API qvg_status coral_predict_encode_static(const qvg_config* cfg, const cora
                                        uint32_t* codes, uint32_t* meta, qvg_bf16* xhat_next, float* pred_out,
                                        qvg_stream stream);
 
+/* Adapted configuration of the cross-layer codec (Coral-KV pages: the light
+ * block-diagonal predictors are rebuilt for the current video, the low-rank
+ * part stays as calibrated).  Per head h, the ridge least-squares block
+ *   B_h = argmin_B sum_n ||y_{n,h} - U_h t_n - B xhat_{n,h}||^2 + lambda_h ||B||^2,
+ *   t_n = W^T xhat_n, lambda_h = 2^-20 trace(X_h^T X_h) / D,
+ * from xhat_prev (= xhat_l, bf16 [n_tokens][H*D]) and x_next (= x_{l+1}, same
+ * layout), written to B_out (bf16 [H][D][D], B[h][o][i]; device memory,
+ * caller-owned).  pred supplies U and W (rank 32; pred->B is not read).  The
+ * block is then used as the predictor's B for coral_predict_encode of this
+ * layer, and must be stored with the stream so that the decoder uses the same
+ * one.  Sums: bf16 products, fp32 accumulation per 1024-token chunk, chunks
+ * added in a fixed order, fp32 Cholesky solve; B_h = 0 when X_h is zero.
+ * Needs C = 0, D = 128, rank 32, n_tokens >= 1 and qvg_workspace_bytes of
+ * workspace (256-byte aligned); qvg_fit_stats reports its error word. */
+QVG_API qvg_status coral_fit_block(const qvg_config* cfg, const coral_predictor* pred, const qvg_bf16* xhat_prev,
+                                   const qvg_bf16* x_next, int64_t n_tokens, qvg_bf16* B_out, void* workspace,
+                                   size_t workspace_bytes, qvg_stream stream);
+
 /* Decoder twin of coral_predict_encode: rebuilds xhat_next from xhat_prev,
  * the predictor and the stored codes (bit-identical to the encoder's
  * xhat_next). */

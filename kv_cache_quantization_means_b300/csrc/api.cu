@@ -133,6 +133,12 @@ size_t coral_ws_bytes(const qvg_config* c, int64_t n_tokens) {
     return lr > tc ? lr : tc;
 }
 
+// coral_fit_block: the tensor-core scratch (t, W^T, [U|U], error word), then
+// the fp32 partial Gram sums.
+size_t coral_fit_ws_bytes(const qvg_config* c, int64_t n_tokens) {
+    return qvg::coral_tc_scratch_bytes(c->num_heads, n_tokens) + align256(qvg::coral_fit_part_bytes(c->num_heads, n_tokens));
+}
+
 qvg::AssignArgs assign_args(const qvg_config* c, const qvg_bf16* x, int64_t n, int64_t hs, int64_t ts,
                             const qvg_bf16* cent, uint8_t* ids, int64_t cap, int64_t off, int* counts,
                             unsigned long long* stats) {
@@ -205,6 +211,10 @@ qvg_status qvg_workspace_bytes(const qvg_config* cfg, int64_t n_tokens, size_t* 
     if (cfg->num_clusters == 0) {
         size_t coral = coral_ws_bytes(cfg, n_tokens);
         if (coral > b) b = coral;
+        if (cfg->head_dim == 128) {
+            const size_t fit = coral_fit_ws_bytes(cfg, n_tokens);
+            if (fit > b) b = fit;
+        }
     }
     *bytes = b;
     return ok();
@@ -489,6 +499,42 @@ qvg_status coral_predict_encode(const qvg_config* cfg, const coral_predictor* pr
     if (workspace) clear_coral_error(cfg, n_tokens, workspace, workspace_bytes, (cudaStream_t)stream);
     return cuda_status(qvg::launch_coral(cfg->head_dim, cfg->group_size, true, a, (cudaStream_t)stream),
                        "coral launch");
+}
+
+qvg_status coral_fit_block(const qvg_config* cfg, const coral_predictor* pred, const qvg_bf16* xhat_prev,
+                           const qvg_bf16* x_next, int64_t n_tokens, qvg_bf16* B_out, void* workspace,
+                           size_t workspace_bytes, qvg_stream stream) {
+    qvg_status st = check_config(cfg, false);
+    if (st) return st;
+    if (cfg->num_clusters != 0) return fail(QVG_ERR_INVALID_ARG, "cross-layer codec needs num_clusters == 0");
+    if (cfg->head_dim != 128) return fail(QVG_ERR_UNSUPPORTED, "block refit supports head_dim 128");
+    if (!pred || pred->rank != 32 || !pred->U || !pred->W)
+        return fail(QVG_ERR_UNSUPPORTED, "block refit needs the rank-32 low-rank part (U, W)");
+    if (n_tokens < 1) return fail(QVG_ERR_INVALID_ARG, "block refit needs n_tokens >= 1");
+    if (!xhat_prev || !x_next || !B_out) return fail(QVG_ERR_INVALID_ARG, "buffer is NULL");
+    if (!aligned16(xhat_prev) || !aligned16(x_next) || !aligned16(B_out) || !aligned16(pred->U) || !aligned16(pred->W))
+        return fail(QVG_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+    const size_t need = coral_fit_ws_bytes(cfg, n_tokens);
+    if (!workspace || workspace_bytes < need) return fail(QVG_ERR_INVALID_ARG, "workspace too small: need %zu bytes", need);
+    if (((uintptr_t)workspace & 255u) != 0) return fail(QVG_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    cudaStream_t s = (cudaStream_t)stream;
+    clear_coral_error(cfg, n_tokens, workspace, workspace_bytes, s);
+    const size_t N = (size_t)n_tokens, HD = (size_t)cfg->num_heads * 128;
+    const size_t tc = qvg::coral_tc_scratch_bytes(cfg->num_heads, n_tokens);
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    qvg::CoralTcScratch w;
+    w.t2 = reinterpret_cast<uint16_t*>(base);
+    w.wt = reinterpret_cast<uint16_t*>(base + align256(N * 64 * 2));
+    w.ud = reinterpret_cast<uint16_t*>(base + align256(N * 64 * 2) + align256(32 * HD * 2));
+    w.err = reinterpret_cast<uint32_t*>(base + tc - 256);
+    qvg::CoralArgs a{};
+    a.xprev = xhat_prev; a.U = pred->U; a.W = pred->W; a.R = 32;
+    a.n_tokens = n_tokens; a.H = cfg->num_heads; a.S = cfg->num_stages;
+    cudaError_t e = qvg::launch_coral_lowrank_tc(a, w, s);
+    if (e != cudaSuccess) return cuda_status(e, "low-rank launch");
+    e = qvg::launch_coral_fit(xhat_prev, x_next, w.t2, pred->U, n_tokens, cfg->num_heads,
+                              reinterpret_cast<float*>(base + tc), B_out, s);
+    return cuda_status(e, "block refit launch");
 }
 
 qvg_status coral_predict_decode(const qvg_config* cfg, const coral_predictor* pred, const qvg_bf16* xhat_prev,

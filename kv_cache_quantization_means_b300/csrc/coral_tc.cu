@@ -464,16 +464,11 @@ bool encode_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int G>
-cudaError_t coral_tc_g(bool encode, const CoralArgs& a, const CoralTcScratch& w, bool* launched, cudaStream_t s) {
-    const int H = a.H, HD = H * kDh;
+// prep + low-rank: t = x_hat W into w.t2 as (hi, lo) bf16 pairs
+cudaError_t lowrank_stage(const CoralArgs& a, const CoralTcScratch& w, const CUtensorMap& tx, const CUtensorMap& tw,
+                          cudaStream_t s) {
+    const int HD = a.H * kDh;
     const int64_t N = a.n_tokens;
-    CUtensorMap tx, tw, tb, tt, tu;
-    if (!encode_2d(&tx, a.xprev, (uint64_t)HD, (uint64_t)N, (uint64_t)HD * 2, 64, kT)) return cudaSuccess;
-    if (!encode_2d(&tw, w.wt, (uint64_t)HD, (uint64_t)kR, (uint64_t)HD * 2, 64, kR)) return cudaSuccess;
-    if (!encode_2d(&tb, a.B, (uint64_t)kDh, (uint64_t)HD, (uint64_t)kDh * 2, 64, kT)) return cudaSuccess;
-    if (!encode_2d(&tt, w.t2, (uint64_t)(2 * kR), (uint64_t)N, (uint64_t)(4 * kR), 64, kT)) return cudaSuccess;
-    if (!encode_2d(&tu, w.ud, (uint64_t)(2 * kR), (uint64_t)HD, (uint64_t)(4 * kR), 64, kT)) return cudaSuccess;
     coral_prep_kernel<<<(unsigned)((HD + 127) / 128), 128, 0, s>>>(a.W, a.U, HD, w.wt, w.ud);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -485,7 +480,22 @@ cudaError_t coral_tc_g(bool encode, const CoralArgs& a, const CoralTcScratch& w,
     if (e != cudaSuccess) return e;
     LrArgs la{N, HD, w.t2, w.err};
     coral_lowrank_tc_kernel<<<(unsigned)tiles, kLrThreads, lr_req, s>>>(tx, tw, la);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+template <int G>
+cudaError_t coral_tc_g(bool encode, const CoralArgs& a, const CoralTcScratch& w, bool* launched, cudaStream_t s) {
+    const int H = a.H, HD = H * kDh;
+    const int64_t N = a.n_tokens;
+    CUtensorMap tx, tw, tb, tt, tu;
+    if (!encode_2d(&tx, a.xprev, (uint64_t)HD, (uint64_t)N, (uint64_t)HD * 2, 64, kT)) return cudaSuccess;
+    if (!encode_2d(&tw, w.wt, (uint64_t)HD, (uint64_t)kR, (uint64_t)HD * 2, 64, kR)) return cudaSuccess;
+    if (!encode_2d(&tb, a.B, (uint64_t)kDh, (uint64_t)HD, (uint64_t)kDh * 2, 64, kT)) return cudaSuccess;
+    if (!encode_2d(&tt, w.t2, (uint64_t)(2 * kR), (uint64_t)N, (uint64_t)(4 * kR), 64, kT)) return cudaSuccess;
+    if (!encode_2d(&tu, w.ud, (uint64_t)(2 * kR), (uint64_t)HD, (uint64_t)(4 * kR), 64, kT)) return cudaSuccess;
+    cudaError_t e = lowrank_stage(a, w, tx, tw, s);
+    if (e != cudaSuccess) return e;
+    const int tiles = (int)((N + kT - 1) / kT);
     const size_t pr_smem = (size_t)kPrStages * kStageBytes + 8 * (2 * kPrStages + 4) + 32 + 1024;
     // SM: stages held in registers by the epilogue (2, or 4 when S > 2)
     auto kern = a.S <= 2 ? (encode ? coral_predict_tc_kernel<G, true, 2> : coral_predict_tc_kernel<G, false, 2>)
@@ -509,6 +519,15 @@ size_t coral_tc_scratch_bytes(int H, int64_t n_tokens) {
     const size_t HD = (size_t)H * kDh, N = (size_t)(n_tokens > 0 ? n_tokens : 1);
     auto a256 = [](size_t v) { return (v + 255) & ~(size_t)255; };
     return a256(N * 2 * kR * 2) + a256((size_t)kR * HD * 2) + a256(HD * 2 * kR * 2) + 256;
+}
+
+cudaError_t launch_coral_lowrank_tc(const CoralArgs& a, const CoralTcScratch& w, cudaStream_t s) {
+    const int HD = a.H * kDh;
+    CUtensorMap tx, tw;
+    if (!encode_2d(&tx, a.xprev, (uint64_t)HD, (uint64_t)a.n_tokens, (uint64_t)HD * 2, 64, kT) ||
+        !encode_2d(&tw, w.wt, (uint64_t)HD, (uint64_t)kR, (uint64_t)HD * 2, 64, kR))
+        return cudaErrorInvalidValue;
+    return lowrank_stage(a, w, tx, tw, s);
 }
 
 cudaError_t launch_coral_tc(int D, int G, bool encode, const CoralArgs& a, const CoralTcScratch& w, bool* launched,

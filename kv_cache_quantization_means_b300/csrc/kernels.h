@@ -116,4 +116,16 @@ cudaError_t launch_coral(int D, int G, bool encode, const CoralArgs& a, cudaStre
 cudaError_t launch_coral_tc(int D, int G, bool encode, const CoralArgs& a, const CoralTcScratch& w, bool* launched,
                             cudaStream_t s);
 
+// The low-rank stage alone (W^T / [U|U] layout and t = x_hat W as bf16
+// hi/lo pairs into w.t2); D = 128, R = 32, 128-byte aligned scratch.
+cudaError_t launch_coral_lowrank_tc(const CoralArgs& a, const CoralTcScratch& w, cudaStream_t s);
+
+// Adapted block predictors: per head the ridge least-squares block of
+// y - U t = B x_hat (D = 128, R = 32), from x_hat, y = x_{l+1} and t2
+// (launch_coral_lowrank_tc).  part: coral_fit_part_bytes scratch.
+constexpr int kFitChunkTokens = 1024;   // tokens per fp32 partial Gram sum
+size_t coral_fit_part_bytes(int H, int64_t n_tokens);
+cudaError_t launch_coral_fit(const uint16_t* xh, const uint16_t* y, const uint16_t* t2, const uint16_t* U,
+                             int64_t n_tokens, int H, float* part, uint16_t* B, cudaStream_t s);
+
 }  // namespace qvg

@@ -2,6 +2,7 @@
 
     python -m kv_cache_quantization_means_b300.profile_case unit [time]
     python -m kv_cache_quantization_means_b300.profile_case coral [time]
+    python -m kv_cache_quantization_means_b300.profile_case coral_fit [time]
 
 `unit` runs one (layer, tensor) of the Wan2.1-shaped cache (12 heads x 32760
 tokens x 128, C = 256, T = 4, S = 2, G = 64): a fit, then one more assign,
@@ -96,10 +97,28 @@ def coral_case(timed):
             print(f"{name:8s} {t:9.1f} us   {el * byt / t / 1e3:8.1f} GB/s algorithmic")
 
 
+def coral_fit_case(timed):
+    """The adapted configuration's block refit on one Coral layer pair."""
+    wl = WL.CORAL
+    H, D, N, S, G = wl.heads, wl.head_dim, wl.tokens, wl.stages, wl.group_size
+    cfg = Q.config(H, D, 0, 0, S, G)
+    xs = SG.coral_chain_gpu(wl, 0, n_layers=2)
+    _, U, W = SG.coral_predictor_device(wl, 0)
+    B = torch.empty(H * D * D, dtype=torch.int16, device="cuda")
+    pred = Q.coral_predictor(B=B.data_ptr(), U=U.data_ptr(), W=W.data_ptr(), rank=wl.rank)
+    ws = Q.alloc_workspace(cfg, N)
+    fit = lambda: Q.coral_fit_block(cfg, pred, xs[0], xs[1], N, B, ws)
+    fit()
+    torch.cuda.synchronize()
+    assert Q.qvg_fit_stats(cfg, N, ws)[3] == 0
+    if timed:
+        print(f"fit      {_graph_time_us(fit):9.1f} us")
+
+
 def main(argv):
     case = argv[1] if len(argv) > 1 else "unit"
     timed = len(argv) > 2 and argv[2] == "time"
-    {"unit": unit_case, "coral": coral_case}[case](timed)
+    {"unit": unit_case, "coral": coral_case, "coral_fit": coral_fit_case}[case](timed)
 
 
 if __name__ == "__main__":

@@ -18,7 +18,7 @@ EXPORTS = [
     "qvg_last_error", "qvg_version", "qvg_encoded_bytes", "qvg_workspace_bytes", "qvg_fit_stats",
     "qvg_fit_centroids",
     "qvg_assign", "qvg_update", "qvg_encode", "qvg_decode", "qvg_append_chunk", "qvg_decode_cache",
-    "coral_predict_encode", "coral_predict_decode", "coral_predict_encode_static",
+    "coral_predict_encode", "coral_predict_decode", "coral_predict_encode_static", "coral_fit_block",
 ]
 
 
@@ -77,6 +77,7 @@ def load(path=LIB_PATH):
     L.coral_predict_encode.argtypes = [PCFG, ctypes.POINTER(coral_predictor), P, P, I64, P, P, P, P, P, SZ, P]
     L.coral_predict_encode_static.argtypes = [PCFG, ctypes.POINTER(coral_predictor), P, P, I64, P, P, P, P, P]
     L.coral_predict_decode.argtypes = [PCFG, ctypes.POINTER(coral_predictor), P, I64, P, P, P, P, P, SZ, P]
+    L.coral_fit_block.argtypes = [PCFG, ctypes.POINTER(coral_predictor), P, P, I64, P, P, SZ, P]
     for name in EXPORTS[2:]:
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -193,6 +194,14 @@ def coral_predict_encode_static(cfg, pred, xhat_prev, x_next, n_tokens, codes, m
     _check(load().coral_predict_encode_static(ctypes.byref(cfg), ctypes.byref(pred) if pred is not None else None,
                                               _ptr(xhat_prev), _ptr(x_next), n_tokens, _ptr(codes), _ptr(meta),
                                               _ptr(xhat_next), _ptr(pred_out), _stream(stream)))
+
+
+def coral_fit_block(cfg, pred, xhat_prev, x_next, n_tokens, B_out, workspace, stream=None):
+    """Adapted block predictors: per head the ridge least-squares B_h (bf16
+    [H][D][D]) for this layer pair; pred supplies U and W."""
+    _check(load().coral_fit_block(ctypes.byref(cfg), ctypes.byref(pred) if pred is not None else None,
+                                  _ptr(xhat_prev), _ptr(x_next), n_tokens, _ptr(B_out), _ptr(workspace),
+                                  _nbytes(workspace), _stream(stream)))
 
 
 def coral_predict_decode(cfg, pred, xhat_prev, n_tokens, codes, meta, xhat_next, pred_out=None, workspace=None,

@@ -130,3 +130,68 @@ def test_coral_closed_loop_end_to_end(qvg, oracle):
         eo = np.mean((SY.bf16_bits_to_f32(o_prev) - x) ** 2)
         assert abs(eg - eo) <= 0.01 * eo, (l, eg, eo)
     assert diff <= 1e-3 * total, (diff, total)
+
+
+@pytest.mark.parametrize("N,H", [(1100, 4), (9000, 4)])
+def test_coral_fit_block_parity(qvg, oracle, N, H):
+    """Adapted block predictors: the GPU's least-squares B_h (fp32 sums and
+    fp32 Cholesky solve) against the oracle's fp64 solution Z.  Bound, from
+    the arithmetic: rounding to bf16 (8 significant bits) errs by at most
+    2^-8 |Z|; the fp32 solve by the first-order Cholesky bound
+    cond(G_h) * D * 2^-24 of the block's scale (taken twice), with cond(G_h)
+    computed here from the ridge-regularised Gram matrix.  The layer is then
+    encoded with the fitted block and checked bit-exactly given its
+    prediction (staged parity)."""
+    wl = WL.CORAL
+    S, D, G = wl.stages, wl.head_dim, wl.group_size
+    small = WL.Workload(**{**wl.__dict__, "heads": H, "tokens": N, "layers": 2})
+    xs = SY.coral_layers(small, SY.K_TENSOR, 0, N)
+    _, U, W = SY.coral_predictor(small, 0)
+    cfg = qvg.config(H, D, 0, 0, S, G)
+    ws = qvg.alloc_workspace(cfg, N)
+    Ud, Wd = to_dev(U), to_dev(W)
+    Bout = torch.full((H * D * D,), -1, dtype=torch.int16, device="cuda")
+    fitpred = qvg.qvg.coral_predictor(B=Bout.data_ptr(), U=Ud.data_ptr(), W=Wd.data_ptr(), rank=U.shape[1])
+    xprev, xnext = to_dev(xs[0]), to_dev(xs[1])
+    qvg.coral_fit_block(cfg, fitpred, xprev, xnext, N, Bout, ws)
+    torch.cuda.synchronize()
+    assert qvg.qvg_fit_stats(cfg, N, ws)[3] == 0
+    Bg = u16(Bout).reshape(H, D, D)
+    Bo, Z = oracle.coral_fit_block(xs[0], xs[1], U, W, H, D)
+    bg = SY.bf16_bits_to_f32(Bg).astype(np.float64)
+    scale = np.abs(Z).max(axis=(1, 2), keepdims=True)
+    x = SY.bf16_bits_to_f32(xs[0]).astype(np.float64)
+    kappa = np.empty((H, 1, 1))
+    for h in range(H):
+        Gh = x[:, h * D:(h + 1) * D].T @ x[:, h * D:(h + 1) * D]
+        ev = np.linalg.eigvalsh(Gh + np.ldexp(np.trace(Gh) / D, -20) * np.eye(D))
+        kappa[h] = ev[-1] / ev[0]
+    tol = 2.0 ** -8 * np.abs(Z) + 2 * kappa * D * 2.0 ** -24 * scale
+    assert np.all(np.abs(bg - Z) <= tol), np.max(np.abs(bg - Z) / tol)
+    assert np.mean(Bg == Bo) >= 0.5, np.mean(Bg == Bo)
+    # encode this layer with the fitted block; the oracle quantises with the GPU's prediction
+    codes, meta, xh, pout = gpu_layer(qvg, cfg, fitpred, xprev, xnext, N)
+    gp = pout.cpu().numpy()
+    oc, om, oxh, _ = oracle.coral_encode_layer(xs[0], xs[1], Bg, U, W, H, D, S, G, pred_in=gp)
+    np.testing.assert_array_equal(u32(codes).reshape(oc.shape), oc)
+    np.testing.assert_array_equal(u32(meta).reshape(om.shape), om)
+    np.testing.assert_array_equal(u16(xh), oxh)
+    p64 = oracle.coral_predict(xs[0], Bg, U, W, H, D)
+    assert np.all(np.abs(gp - p64) <= pred_bound(xs[0], Bg, U, W, H, D))
+
+
+def test_coral_fit_block_zero_input(qvg):
+    wl = WL.CORAL
+    H, D, N = 2, wl.head_dim, 500
+    small = WL.Workload(**{**wl.__dict__, "heads": H, "tokens": N, "layers": 2})
+    _, U, W = SY.coral_predictor(small, 0)
+    cfg = qvg.config(H, D, 0, 0, wl.stages, wl.group_size)
+    ws = qvg.alloc_workspace(cfg, N)
+    Ud, Wd = to_dev(U), to_dev(W)
+    Bout = torch.full((H * D * D,), -1, dtype=torch.int16, device="cuda")
+    pred = qvg.qvg.coral_predictor(B=Bout.data_ptr(), U=Ud.data_ptr(), W=Wd.data_ptr(), rank=U.shape[1])
+    zeros = torch.zeros((N, H * D), dtype=torch.int16, device="cuda")
+    y = to_dev(SY.coral_layers(small, SY.K_TENSOR, 0, N)[1])
+    qvg.coral_fit_block(cfg, pred, zeros, y, N, Bout, ws)
+    torch.cuda.synchronize()
+    assert np.all(u16(Bout) == 0)
