@@ -143,38 +143,48 @@ class QvgStep:
         self.cfg = Q.config(H, D, wl.clusters, wl.lloyd_iters, wl.stages, wl.group_size, wl.bits)
         self.x = [[SG.mixture_layer_gpu(wl, l, t, layout="nhd") for t in (0, 1)] for l in range(layers)]
         self.enc = [[Q.alloc_encoded(self.cfg, N) for _ in (0, 1)] for _ in range(layers)]
-        self.ws = Q.alloc_workspace(self.cfg, N)
+        # one workspace per tensor: K and V units run concurrently on two streams
+        self.ws = [Q.alloc_workspace(self.cfg, N) for _ in (0, 1)]
+        self.side = torch.cuda.Stream()
         self.out = [torch.empty((N, H, D), dtype=torch.int16, device="cuda") for _ in range(2)]
         self.N, self.H, self.D = N, H, D
         self.bytes_per_step = 2 * layers * N * H * D * 2
 
     def fit(self, l, t):
         e, N, D, H = self.enc[l][t], self.N, self.D, self.H
-        self.Q.qvg_fit_centroids(self.cfg, self.x[l][t], N, D, H * D, None, e["centroids"], e["ids"], N, 0, self.ws)
+        self.Q.qvg_fit_centroids(self.cfg, self.x[l][t], N, D, H * D, None, e["centroids"], e["ids"], N, 0,
+                                 self.ws[t])
 
     def assign(self, l, t):
         e, N, D, H = self.enc[l][t], self.N, self.D, self.H
-        self.Q.qvg_assign(self.cfg, self.x[l][t], N, D, H * D, e["centroids"], e["ids"], N, 0, self.ws)
+        self.Q.qvg_assign(self.cfg, self.x[l][t], N, D, H * D, e["centroids"], e["ids"], N, 0, self.ws[t])
 
     def encode(self, l, t):
         e, N, D, H = self.enc[l][t], self.N, self.D, self.H
         self.Q.qvg_encode(self.cfg, self.x[l][t], N, D, H * D, e["centroids"], 0, e["codes"], e["meta"], e["ids"],
-                          N, 0, self.ws)
+                          N, 0, self.ws[t])
 
     def update(self, l, t):
         e, N, D, H = self.enc[l][t], self.N, self.D, self.H
-        self.Q.qvg_update(self.cfg, self.x[l][t], N, D, H * D, e["ids"], N, 0, e["centroids"], self.ws)
+        self.Q.qvg_update(self.cfg, self.x[l][t], N, D, H * D, e["ids"], N, 0, e["centroids"], self.ws[t])
 
     def decode(self, l, t):
         e, N, D, H = self.enc[l][t], self.N, self.D, self.H
         self.Q.qvg_decode(self.cfg, e["codes"], e["meta"], e["ids"], e["centroids"], N, 0, N, self.out[t], D, H * D)
 
     def step(self):
+        """K units on the current stream, V units on a second one: the two are
+        independent, so one's small kernels run beside the other's."""
+        import torch
+        cur = torch.cuda.current_stream()
+        self.side.wait_stream(cur)
         for l in range(self.L):
             for t in (0, 1):
-                self.fit(l, t)
-                self.encode(l, t)
-                self.decode(l, t)
+                with torch.cuda.stream(cur if t == 0 else self.side):
+                    self.fit(l, t)
+                    self.encode(l, t)
+                    self.decode(l, t)
+        cur.wait_stream(self.side)
 
     def compressed_bytes(self):
         cb, mb, ib, xb = self.Q.qvg_encoded_bytes(self.cfg, self.N, 1)
@@ -216,7 +226,9 @@ class CoralStep:
                      for _ in (0, 1)]
         self.xh = [torch.empty((layers, N, H * D), dtype=torch.int16, device="cuda") for _ in (0, 1)]
         self.dec = [torch.empty((layers, N, H * D), dtype=torch.int16, device="cuda") for _ in (0, 1)]
-        self.ws = Q.alloc_workspace(self.cfg, N)
+        # one workspace per tensor: the K and V chains run concurrently on two streams
+        self.ws = [Q.alloc_workspace(self.cfg, N) for _ in (0, 1)]
+        self.side = torch.cuda.Stream()
         self.bytes_per_step = 2 * layers * N * H * D * 2
         # per tensor and direction: layer 0 (one kernel), then prep + low-rank + predict per layer;
         # adapted: + prep + low-rank + Gram + reduce + solve per encoded layer
@@ -229,22 +241,34 @@ class CoralStep:
         prev = None if l == 0 else self.xh[t][l - 1]
         pred = None if l == 0 else self.pred(t, l)
         if self.adapted and l > 0:
-            self.Q.coral_fit_block(self.cfg, pred, prev, self.x[t][l], self.N, self.fit_B[t][l - 1], self.ws)
+            self.Q.coral_fit_block(self.cfg, pred, prev, self.x[t][l], self.N, self.fit_B[t][l - 1], self.ws[t])
         self.Q.coral_predict_encode(self.cfg, pred, prev, self.x[t][l], self.N, self.codes[t][l], self.meta[t][l],
-                                    self.xh[t][l], None, self.ws)
+                                    self.xh[t][l], None, self.ws[t])
 
     def decode(self, t, l):
         prev = None if l == 0 else self.dec[t][l - 1]
         pred = None if l == 0 else self.pred(t, l)
         self.Q.coral_predict_decode(self.cfg, pred, prev, self.N, self.codes[t][l], self.meta[t][l],
-                                    self.dec[t][l], None, self.ws)
+                                    self.dec[t][l], None, self.ws[t])
 
     def step(self):
+        """The K chain, then the V chain.  In the adapted configuration the V
+        chain runs on a second stream beside the K chain: the block refit's
+        one-CTA-per-head solve leaves most SMs idle.  (The reusable
+        configuration's persistent predict kernels already fill every SM, and
+        two chains only compete.)"""
+        import torch
+        cur = torch.cuda.current_stream()
+        if self.adapted:
+            self.side.wait_stream(cur)
         for t in (0, 1):
-            for l in range(self.L):
-                self.encode(t, l)
-            for l in range(self.L):
-                self.decode(t, l)
+            with torch.cuda.stream(self.side if (self.adapted and t == 1) else cur):
+                for l in range(self.L):
+                    self.encode(t, l)
+                for l in range(self.L):
+                    self.decode(t, l)
+        if self.adapted:
+            cur.wait_stream(self.side)
 
 
 class StreamStep:
