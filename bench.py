@@ -135,7 +135,7 @@ def workload(name, bits=None):
 class QvgStep:
     """Device buffers and the launch sequence of one step of the QVG path."""
 
-    def __init__(self, Q, wl, layers):
+    def __init__(self, Q, wl, layers, streams=4):
         import torch
         from synth import gpu as SG
         self.Q, self.wl, self.L = Q, wl, layers
@@ -143,48 +143,58 @@ class QvgStep:
         self.cfg = Q.config(H, D, wl.clusters, wl.lloyd_iters, wl.stages, wl.group_size, wl.bits)
         self.x = [[SG.mixture_layer_gpu(wl, l, t, layout="nhd") for t in (0, 1)] for l in range(layers)]
         self.enc = [[Q.alloc_encoded(self.cfg, N) for _ in (0, 1)] for _ in range(layers)]
-        # one workspace per tensor: K and V units run concurrently on two streams
-        self.ws = [Q.alloc_workspace(self.cfg, N) for _ in (0, 1)]
-        self.side = torch.cuda.Stream()
-        self.out = [torch.empty((N, H, D), dtype=torch.int16, device="cuda") for _ in range(2)]
+        # units run concurrently on `streams` streams, each with its own
+        # workspace and decode-output buffer: unit (l, t) goes to stream
+        # (2 l + t) mod streams
+        self.nstreams = streams
+        self.ws = [Q.alloc_workspace(self.cfg, N) for _ in range(streams)]
+        self.sides = [torch.cuda.Stream() for _ in range(streams - 1)]
+        self.out = [torch.empty((N, H, D), dtype=torch.int16, device="cuda") for _ in range(streams)]
         self.N, self.H, self.D = N, H, D
         self.bytes_per_step = 2 * layers * N * H * D * 2
 
     def fit(self, l, t):
         e, N, D, H = self.enc[l][t], self.N, self.D, self.H
         self.Q.qvg_fit_centroids(self.cfg, self.x[l][t], N, D, H * D, None, e["centroids"], e["ids"], N, 0,
-                                 self.ws[t])
+                                 self.ws[self.slot(l, t)])
 
     def assign(self, l, t):
         e, N, D, H = self.enc[l][t], self.N, self.D, self.H
-        self.Q.qvg_assign(self.cfg, self.x[l][t], N, D, H * D, e["centroids"], e["ids"], N, 0, self.ws[t])
+        self.Q.qvg_assign(self.cfg, self.x[l][t], N, D, H * D, e["centroids"], e["ids"], N, 0, self.ws[self.slot(l, t)])
 
     def encode(self, l, t):
         e, N, D, H = self.enc[l][t], self.N, self.D, self.H
         self.Q.qvg_encode(self.cfg, self.x[l][t], N, D, H * D, e["centroids"], 0, e["codes"], e["meta"], e["ids"],
-                          N, 0, self.ws[t])
+                          N, 0, self.ws[self.slot(l, t)])
 
     def update(self, l, t):
         e, N, D, H = self.enc[l][t], self.N, self.D, self.H
-        self.Q.qvg_update(self.cfg, self.x[l][t], N, D, H * D, e["ids"], N, 0, e["centroids"], self.ws[t])
+        self.Q.qvg_update(self.cfg, self.x[l][t], N, D, H * D, e["ids"], N, 0, e["centroids"], self.ws[self.slot(l, t)])
 
     def decode(self, l, t):
         e, N, D, H = self.enc[l][t], self.N, self.D, self.H
-        self.Q.qvg_decode(self.cfg, e["codes"], e["meta"], e["ids"], e["centroids"], N, 0, N, self.out[t], D, H * D)
+        self.Q.qvg_decode(self.cfg, e["codes"], e["meta"], e["ids"], e["centroids"], N, 0, N,
+                          self.out[self.slot(l, t)], D, H * D)
+
+    def slot(self, l, t):
+        return (2 * l + t) % self.nstreams
 
     def step(self):
-        """K units on the current stream, V units on a second one: the two are
-        independent, so one's small kernels run beside the other's."""
+        """Units spread over the streams: they are independent, so the small
+        kernels of one run beside another's work."""
         import torch
         cur = torch.cuda.current_stream()
-        self.side.wait_stream(cur)
+        streams = [cur] + self.sides
+        for sd in self.sides:
+            sd.wait_stream(cur)
         for l in range(self.L):
             for t in (0, 1):
-                with torch.cuda.stream(cur if t == 0 else self.side):
+                with torch.cuda.stream(streams[self.slot(l, t)]):
                     self.fit(l, t)
                     self.encode(l, t)
                     self.decode(l, t)
-        cur.wait_stream(self.side)
+        for sd in self.sides:
+            cur.wait_stream(sd)
 
     def compressed_bytes(self):
         cb, mb, ib, xb = self.Q.qvg_encoded_bytes(self.cfg, self.N, 1)
@@ -461,7 +471,7 @@ def config_block(wl, args):
                         f"b={wl.bits} G={wl.group_size}",
             "layers": wl.layers, "heads": wl.heads, "head_dim": wl.head_dim, "tokens": wl.tokens,
             "clusters": wl.clusters, "lloyd_iters": wl.lloyd_iters, "stages": wl.stages, "group_size": wl.group_size,
-            "bits": wl.bits,
+            "bits": wl.bits, "streams": getattr(args, "streams", 1),
             "l2": "inputs larger than L2 (one layer's K or V is %.0f MB)" % (wl.tokens * wl.heads * wl.head_dim * 2 / 1e6),
             "parallelism": f"replicas x{args.gpus}"}
 
@@ -524,6 +534,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--streams", type=int, default=4,
+                    help="QVG workloads: (layer, tensor) units run concurrently on this many streams")
     ap.add_argument("--adapted", action="store_true",
                     help="coral: refit each layer's block predictors for the current video before encoding it")
     ap.add_argument("--bits", type=int, default=None, choices=[2, 4],
@@ -556,7 +568,7 @@ def main():
     if args.config in ("coral", "stream"):
         return run_aux(args, Q, wl, peaks, world, rank, local)
     layers = wl.layers if args.config == "wan" else 2
-    st = QvgStep(Q, wl, layers)
+    st = QvgStep(Q, wl, layers, streams=args.streams)
     torch.cuda.synchronize()
 
     graph = None
