@@ -185,12 +185,16 @@ __global__ void __launch_bounds__(kLrThreads, 1)
 
 constexpr int kPrStages = 2;
 constexpr int kPrThreads = 64 + 256;    // TMA warp, MMA warp, two groups of four epilogue warps
-constexpr int kStageBytes = 2 * kSlab + 2 * kSlab + kSlab + kSlab;   // xhat_h, B_h, t2, Ud_h
+constexpr int kResBytes = 3 * kSlab;    // resident per head: B_h (two slabs), [U_h | U_h]
+constexpr int kPrBars = 2 * kPrStages + 4 + 2;   // full, empty, tfull, tempty, block full / free
+
+// Stage bytes: x_hat tile (two slabs) and t2 (one slab); the encoder adds the
+// x_{l+1} tile (two slabs).
+__host__ __device__ constexpr int pr_stage_bytes(bool encode) { return (encode ? 5 : 3) * kSlab; }
 
 struct PrArgs {
     int64_t n_tokens;
     int H, S, tiles;
-    const uint16_t* xnext;   // [N][H*D] (encode) or null (decode)
     uint32_t* codes;         // [S][H][N][D/16]
     uint32_t* meta;          // [S][H][N][D/G]
     uint16_t* xhat;          // [N][H*D] out
@@ -205,33 +209,46 @@ __device__ __forceinline__ uint4 ldg_v4_l1(const void* p) {
     return v;
 }
 
+// Items are (head, 128-token tile) pairs in head-major order; each CTA takes a
+// contiguous run of them, so the head's B_h and [U_h | U_h] stay resident in
+// shared memory and are reloaded only when the run crosses into the next head
+// (the MMA warp signals "block free" once the MMAs that read the old ones are
+// done).  A stage carries the item's x_hat tile and t2 -- and, in the encoder,
+// its x_{l+1} tile, which the epilogue reads from shared memory; the encoder's
+// stage is released by the MMAs and by the four epilogue warps that read it.
 template <int G, bool ENCODE, int SM>
 __global__ void __launch_bounds__(kPrThreads, 1)
     coral_predict_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                             const __grid_constant__ CUtensorMap tm_t, const __grid_constant__ CUtensorMap tm_u,
-                            PrArgs a) {
+                            const __grid_constant__ CUtensorMap tm_xn, PrArgs a) {
+    constexpr int SB = pr_stage_bytes(ENCODE);
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned, derived from the shared array so that accesses stay in
     // the shared window
     uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const uint32_t bar0 = smem_u32(base + kPrStages * kStageBytes);
+    uint8_t* res = base;                                   // resident B_h, [U_h | U_h]
+    uint8_t* stages = base + kResBytes;
+    const uint32_t bar0 = smem_u32(stages + kPrStages * SB);
     const uint32_t full_bar = bar0, empty_bar = bar0 + 8 * kPrStages, tfull_bar = bar0 + 16 * kPrStages,
-                   tempty_bar = tfull_bar + 16;
-    uint32_t* misc = reinterpret_cast<uint32_t*>(base + kPrStages * kStageBytes + 8 * (2 * kPrStages + 4));
+                   tempty_bar = tfull_bar + 16, bfull_bar = tempty_bar + 16, bfree_bar = bfull_bar + 8;
+    uint32_t* misc = reinterpret_cast<uint32_t*>(stages + kPrStages * SB + 8 * kPrBars);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int H = a.H, HD = H * kDh;
     const int n_items = a.tiles * H;
-    // this CTA's items: blockIdx.x, blockIdx.x + gridDim.x, ...
-    const int my_items = n_items > (int)blockIdx.x ? (n_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int per = (n_items + (int)gridDim.x - 1) / (int)gridDim.x;
+    const int i0 = (int)blockIdx.x * per;
+    const int my_items = n_items - i0 < per ? (n_items - i0 > 0 ? n_items - i0 : 0) : per;
     if (tid == 0) {
         for (int s = 0; s < kPrStages; ++s) {
             mbar_init(full_bar + 8 * s, 1);
-            mbar_init(empty_bar + 8 * s, 1);
+            mbar_init(empty_bar + 8 * s, ENCODE ? 1 + 4 : 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar + 8 * b, 1);
             mbar_init(tempty_bar + 8 * b, 4);
         }
+        mbar_init(bfull_bar, 1);
+        mbar_init(bfree_bar, 1);
         misc[1] = 0;
         fence_mbar_init();
     }
@@ -249,25 +266,37 @@ __global__ void __launch_bounds__(kPrThreads, 1)
     if (warp == 0) {
         // ---------------------------------------------------- TMA producer
         if (lane == 0) {
-            int armed = 0;
+            int armed = 0, nb = 0, hres = -1;
             for (int i = 0; i < my_items; ++i) {
-                const int item = (int)blockIdx.x + i * (int)gridDim.x;
-                const int tile = item / H, h = item % H;
+                const int item = i0 + i;
+                const int h = item / a.tiles, tile = item % a.tiles;
+                if (h != hres) {
+                    // the previous head's block is free once its MMAs are done
+                    if (nb > 0 && !mbar_wait(bfree_bar, (uint32_t)(nb - 1) & 1u)) { misc[1] = 1; break; }
+                    mbar_arrive_tx(bfull_bar, (uint32_t)kResBytes);
+                    for (int at = 0; at < 2; ++at)
+                        tma_load_2d(smem_u32(res + at * kSlab), &tm_b, bfull_bar, at * 64, h * kDh);
+                    tma_load_2d(smem_u32(res + 2 * kSlab), &tm_u, bfull_bar, 0, h * kDh);
+                    hres = h;
+                    ++nb;
+                }
                 const int s = i % kPrStages;
                 if (!mbar_wait(empty_bar + 8 * s, ((uint32_t)(i / kPrStages) & 1u) ^ 1u)) { misc[1] = 1; break; }
-                uint8_t* st = base + (size_t)s * kStageBytes;
-                mbar_arrive_tx(full_bar + 8 * s, (uint32_t)kStageBytes);
+                uint8_t* st = stages + (size_t)s * SB;
                 const uint32_t fb = full_bar + 8 * s;
-                for (int at = 0; at < 2; ++at) {
+                mbar_arrive_tx(fb, (uint32_t)SB);
+                for (int at = 0; at < 2; ++at)
                     tma_load_2d(smem_u32(st + at * kSlab), &tm_x, fb, h * kDh + at * 64, tile * kT);
-                    tma_load_2d(smem_u32(st + (2 + at) * kSlab), &tm_b, fb, at * 64, h * kDh);
-                }
-                tma_load_2d(smem_u32(st + 4 * kSlab), &tm_t, fb, 0, tile * kT);
-                tma_load_2d(smem_u32(st + 5 * kSlab), &tm_u, fb, 0, h * kDh);
+                tma_load_2d(smem_u32(st + 2 * kSlab), &tm_t, fb, 0, tile * kT);
+                if (ENCODE)
+                    for (int at = 0; at < 2; ++at)
+                        tma_load_2d(smem_u32(st + (3 + at) * kSlab), &tm_xn, fb, h * kDh + at * 64, tile * kT);
                 armed = i + 1;
             }
+            // drain this warp's copies before the CTA exits
             for (int i = armed - kPrStages > 0 ? armed - kPrStages : 0; i < armed; ++i)
                 mbar_wait(full_bar + 8 * (i % kPrStages), (uint32_t)(i / kPrStages) & 1u);
+            if (nb > 0) mbar_wait(bfull_bar, (uint32_t)(nb - 1) & 1u);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -275,27 +304,37 @@ __global__ void __launch_bounds__(kPrThreads, 1)
         if (lane == 0) {
             const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kDh >> 3) << 17) |
                                    ((uint32_t)(kT >> 4) << 24);
-            int issued = 0;
-            for (int i = 0; i < my_items; ++i) {
+            const uint32_t rs = smem_u32(res);
+            int issued = 0, nb = 0, hres = -1;
+            bool ok = true;
+            for (int i = 0; i < my_items && ok; ++i) {
+                const int h = (i0 + i) / a.tiles;
+                if (h != hres) {
+                    if (nb > 0) umma_commit(bfree_bar);     // the old block is free once the MMAs so far are done
+                    if (!mbar_wait(bfull_bar, (uint32_t)nb & 1u)) { ok = false; break; }
+                    hres = h;
+                    ++nb;
+                }
                 const int s = i % kPrStages, acc = i & 1;
-                if (!mbar_wait(tempty_bar + 8 * acc, ((uint32_t)(i >> 1) & 1u) ^ 1u)) { misc[1] = 1; break; }
-                if (!mbar_wait(full_bar + 8 * s, (uint32_t)(i / kPrStages) & 1u)) { misc[1] = 1; break; }
+                if (!mbar_wait(tempty_bar + 8 * acc, ((uint32_t)(i >> 1) & 1u) ^ 1u)) { ok = false; break; }
+                if (!mbar_wait(full_bar + 8 * s, (uint32_t)(i / kPrStages) & 1u)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t st = smem_u32(base + (size_t)s * kStageBytes);
+                const uint32_t st = smem_u32(stages + (size_t)s * SB);
                 const uint32_t d = tmem + (uint32_t)acc * kDh;
 #pragma unroll
                 for (int at = 0; at < 2; ++at)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16(d, sw128_desc(st + at * kSlab + 32u * kk), sw128_desc(st + (2 + at) * kSlab + 32u * kk),
+                        umma_bf16(d, sw128_desc(st + at * kSlab + 32u * kk), sw128_desc(rs + at * kSlab + 32u * kk),
                                   idesc, (at | kk) != 0 ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    umma_bf16(d, sw128_desc(st + 4 * kSlab + 32u * kk), sw128_desc(st + 5 * kSlab + 32u * kk), idesc, 1u);
-                umma_commit(empty_bar + 8 * s);        // operands free once these MMAs are done
+                    umma_bf16(d, sw128_desc(st + 2 * kSlab + 32u * kk), sw128_desc(rs + 2 * kSlab + 32u * kk), idesc, 1u);
+                umma_commit(empty_bar + 8 * s);        // operands consumed once these MMAs are done
                 umma_commit(tfull_bar + 8 * acc);
                 issued = i + 1;
             }
+            if (!ok) misc[1] = 1;
             for (int i = issued - 2 > 0 ? issued - 2 : 0; i < issued; ++i)
                 mbar_wait(tfull_bar + 8 * (i & 1), (uint32_t)(i >> 1) & 1u);
         }
@@ -310,8 +349,8 @@ __global__ void __launch_bounds__(kPrThreads, 1)
         const int row = q * 32 + lane;
         const int64_t stage_rows = (int64_t)H * a.n_tokens;
         for (int i = g; i < my_items; i += 2) {
-            const int item = (int)blockIdx.x + i * (int)gridDim.x;
-            const int tile = item / H, h = item % H;
+            const int item = i0 + i;
+            const int h = item / a.tiles, tile = item % a.tiles;
             const int64_t n = (int64_t)tile * kT + row;
             const bool valid = n < a.n_tokens;
             const int64_t elem0 = n * HD + (int64_t)h * kDh;
@@ -334,6 +373,12 @@ __global__ void __launch_bounds__(kPrThreads, 1)
                 }
             }
             if (!mbar_wait(tfull_bar + 8 * g, (uint32_t)(i >> 1) & 1u)) { misc[1] = 1; break; }
+            // the encoder reads the stage's x_{l+1} tile: wait on the stage's own
+            // arrival too, so the copy's bytes are visible to these threads
+            const int si = i % kPrStages;
+            if (ENCODE && !mbar_wait(full_bar + 8 * si, (uint32_t)(i / kPrStages) & 1u)) { misc[1] = 1; break; }
+            // this thread's row of the x_{l+1} tile (two 128-byte-swizzled slabs)
+            const uint8_t* xrow = stages + (size_t)si * SB + 3 * kSlab + (size_t)row * 128;
             tc_fence_after();
             // one pass of CPT channels
             auto pass = [&](const int c) {
@@ -349,8 +394,13 @@ __global__ void __launch_bounds__(kPrThreads, 1)
                         tmem_ld32(tcol + 32u * k, v);
                         uint4 xv[4];
 #pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            xv[u] = valid ? ldg_v4_l1(a.xnext + elem0 + c * CPT + 32 * k + 8 * u) : make_uint4(0, 0, 0, 0);
+                        for (int u = 0; u < 4; ++u) {
+                            // channel ch sits in slab ch / 64, 16-byte chunk (ch % 64) / 8 of the row,
+                            // stored at chunk position chunk ^ (row % 8)
+                            const int ch = c * CPT + 32 * k + 8 * u;
+                            xv[u] = *reinterpret_cast<const uint4*>(xrow + (ch >> 6) * kSlab +
+                                                                    ((((ch & 63) >> 3) ^ (row & 7)) << 4));
+                        }
                         tmem_wait_ld();
                         float pk[32];
 #pragma unroll
@@ -436,10 +486,13 @@ __global__ void __launch_bounds__(kPrThreads, 1)
 #pragma unroll
                 for (int c = 0; c < NP; ++c) pass(c);
             }
-            // accumulator drained
+            // accumulator drained (and, in the encoder, the stage's x_{l+1} read)
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar + 8 * g);
+            if (lane == 0) {
+                mbar_arrive(tempty_bar + 8 * g);
+                if (ENCODE) mbar_arrive(empty_bar + 8 * si);
+            }
         }
     }
     tc_fence_before();
@@ -487,8 +540,9 @@ template <int G>
 cudaError_t coral_tc_g(bool encode, const CoralArgs& a, const CoralTcScratch& w, bool* launched, cudaStream_t s) {
     const int H = a.H, HD = H * kDh;
     const int64_t N = a.n_tokens;
-    CUtensorMap tx, tw, tb, tt, tu;
+    CUtensorMap tx, tw, tb, tt, tu, txn;
     if (!encode_2d(&tx, a.xprev, (uint64_t)HD, (uint64_t)N, (uint64_t)HD * 2, 64, kT)) return cudaSuccess;
+    if (encode && !encode_2d(&txn, a.xnext, (uint64_t)HD, (uint64_t)N, (uint64_t)HD * 2, 64, kT)) return cudaSuccess;
     if (!encode_2d(&tw, w.wt, (uint64_t)HD, (uint64_t)kR, (uint64_t)HD * 2, 64, kR)) return cudaSuccess;
     if (!encode_2d(&tb, a.B, (uint64_t)kDh, (uint64_t)HD, (uint64_t)kDh * 2, 64, kT)) return cudaSuccess;
     if (!encode_2d(&tt, w.t2, (uint64_t)(2 * kR), (uint64_t)N, (uint64_t)(4 * kR), 64, kT)) return cudaSuccess;
@@ -496,7 +550,7 @@ cudaError_t coral_tc_g(bool encode, const CoralArgs& a, const CoralTcScratch& w,
     cudaError_t e = lowrank_stage(a, w, tx, tw, s);
     if (e != cudaSuccess) return e;
     const int tiles = (int)((N + kT - 1) / kT);
-    const size_t pr_smem = (size_t)kPrStages * kStageBytes + 8 * (2 * kPrStages + 4) + 32 + 1024;
+    const size_t pr_smem = (size_t)kResBytes + (size_t)kPrStages * pr_stage_bytes(encode) + 8 * kPrBars + 32 + 1024;
     // SM: stages held in registers by the epilogue (2, or 4 when S > 2)
     auto kern = a.S <= 2 ? (encode ? coral_predict_tc_kernel<G, true, 2> : coral_predict_tc_kernel<G, false, 2>)
                          : (encode ? coral_predict_tc_kernel<G, true, 4> : coral_predict_tc_kernel<G, false, 4>);
@@ -504,11 +558,11 @@ cudaError_t coral_tc_g(bool encode, const CoralArgs& a, const CoralTcScratch& w,
     if (e != cudaSuccess) return e;
     PrArgs pa;
     pa.n_tokens = N; pa.H = H; pa.S = a.S; pa.tiles = tiles;
-    pa.xnext = a.xnext; pa.codes = a.codes; pa.meta = a.meta; pa.xhat = a.xhat; pa.pred_out = a.pred_out;
+    pa.codes = a.codes; pa.meta = a.meta; pa.xhat = a.xhat; pa.pred_out = a.pred_out;
     pa.err = w.err;
     const int items = tiles * H;
     const int grid = items < sm_count() ? items : sm_count();
-    kern<<<(unsigned)grid, kPrThreads, pr_smem, s>>>(tx, tb, tt, tu, pa);
+    kern<<<(unsigned)grid, kPrThreads, pr_smem, s>>>(tx, tb, tt, tu, encode ? txn : tx, pa);
     if ((e = cudaGetLastError()) == cudaSuccess) *launched = true;
     return e;
 }
