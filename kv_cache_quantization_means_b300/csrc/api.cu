@@ -87,6 +87,7 @@ struct FitWorkspace {
     void* partials;     // [H][max_pieces][D] 16-byte exact sums
     unsigned long long* stats;  // [4]
     int* blockhist;     // [H][n_blocks][C]
+    float* xnorm;       // [H][N] ||x||^2 per token, shared by a fit's assign steps
     int max_pieces, n_blocks;
     size_t bytes;
 };
@@ -111,6 +112,7 @@ FitWorkspace carve(const qvg_config* c, int64_t n, void* base) {
     w.stats = (unsigned long long*)take(sizeof(unsigned long long) * 4);
     w.n_blocks = (int)((N + qvg::kSortBlock - 1) / qvg::kSortBlock);
     w.blockhist = (int*)take(sizeof(int) * H * (size_t)w.n_blocks * C);
+    w.xnorm = (float*)take(sizeof(float) * H * N);
     w.bytes = o;
     return w;
 }
@@ -148,6 +150,8 @@ qvg::AssignArgs assign_args(const qvg_config* c, const qvg_bf16* x, int64_t n, i
     a.ids = ids; a.cap = cap; a.tok_offset = off;
     a.counts = counts; a.stats = stats;
     a.err = stats ? reinterpret_cast<uint32_t*>(stats + 3) : nullptr;
+    a.xnorm = nullptr;
+    a.xnorm_mode = qvg::kNormCompute;
     return a;
 }
 
@@ -172,8 +176,12 @@ qvg_status lloyd(const qvg_config* c, const qvg_bf16* x, int64_t n, int64_t hs, 
     cudaError_t e = cudaMemsetAsync(w.stats, 0, sizeof(unsigned long long) * 4, s);
     if (e != cudaSuccess) return cuda_status(e, "memset");
     for (int t = 0; t < c->lloyd_iters; ++t) {
-        e = qvg::launch_assign(c->head_dim, c->num_heads,
-                               assign_args(c, x, n, hs, ts, cent, ids, cap, off, nullptr, w.stats), s);
+        // x is the same in every step: the first assign stores ||x||^2 per
+        // token, the later ones read it
+        qvg::AssignArgs aa = assign_args(c, x, n, hs, ts, cent, ids, cap, off, nullptr, w.stats);
+        aa.xnorm = w.xnorm;
+        aa.xnorm_mode = t == 0 ? qvg::kNormStore : qvg::kNormLoad;
+        e = qvg::launch_assign(c->head_dim, c->num_heads, aa, s);
         if (e != cudaSuccess) return cuda_status(e, "assign launch");
         e = qvg::launch_update(c->head_dim, update_args(c, x, n, hs, ts, ids, cap, off, w, cent), s);
         if (e != cudaSuccess) return cuda_status(e, "update launch");

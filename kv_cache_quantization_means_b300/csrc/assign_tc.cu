@@ -13,22 +13,26 @@
 //   warp 1     MMA issuer: tcgen05.mma (M = 128, N = C rounded up to 64,
 //              K = 16 per instruction) into one of two TMEM accumulators;
 //              also owns the TMEM allocation;
-//   warps 2-9  epilogue, two groups of four: group g takes the tiles that use
-//              accumulator g; a thread owns one tile row (its TMEM lane) and
-//              reads all of that row's columns (tcgen05.ld), so the groups and
-//              their warps never wait on one another.
+//   warps 2-17 epilogue, two groups of eight: group g takes the tiles that
+//              use accumulator g.  The two warps of a group that share a TMEM
+//              lane quadrant split a row's columns (and the row's channels for
+//              ||x||^2) in halves; a thread owns one tile row and one half,
+//              and the pair trades its partial results through shared memory
+//              at a 64-thread named barrier.  Groups never wait on one another.
 // The GEMM computes the score  <x, c_j> - ||c_j||^2 / 2  directly: one more
 // K = 16 block multiplies a constant ones column of the token side by
 // -||c_j||^2 / 2 split into three bf16 parts on the centroid side.  The
 // nearest centroid is the largest score.  The epilogue makes two passes:
 //   A. the row's largest score,
 //   B. the bitmask of centroids whose score is within 2E of it, E being a
-//      bound on the screen's error.
-// A row with one candidate is decided; the warp then re-ranks each of its
-// other rows over the row's candidates with direct fp32 distances (relative
-// error bound), then with exact squared distances in 128-bit integers, and
-// for near-exact ties with the squared distance in fp64 summed in channel
-// order, exactly as the plain definition.  Centroids (K-major, 128-byte
+//      bound on the screen's error that grows with ||x|| (a fit's first
+//      assign stores ||x||^2 per token; its later ones, on the same x, read
+//      it back).
+// A row with one candidate is decided.  The pair splits its other rows (2-3%
+// on k-means data) by parity and re-ranks each over the row's candidates with
+// direct fp32 distances (relative error bound), then with exact squared
+// distances in 128-bit integers, and for near-exact ties with the squared
+// distance in fp64 summed in channel order, exactly as the plain definition.  Centroids (K-major, 128-byte
 // swizzle) stay in shared memory for the whole CTA.  Every wait is a bounded
 // wait on an mbarrier: on expiry the kernel records an error code, lets the
 // other roles drain and returns after freeing its tensor memory.
@@ -45,7 +49,7 @@ namespace {
 
 constexpr int kTile = 128;                 // tokens per tile = UMMA M
 constexpr int kMaxStages = 3;              // token tiles in flight (2 when shared memory is short)
-constexpr int kEpiWarps = 8;               // two groups of four
+constexpr int kEpiWarps = 16;              // two groups of eight (four pairs each)
 constexpr int kTcThreads = 64 + 32 * kEpiWarps;
 constexpr int kAtomBytes = kTile * 128;    // one 64-channel slab of a tile
 constexpr uint32_t kErrTimeout = 0x7E000000u;
@@ -71,17 +75,20 @@ struct TcArgs {
     int head_inner;              // tensor map dims are (D, H, N) rather than (D, N, H)
     unsigned long long* stats;   // [4] or null
     uint32_t* err;               // or null
+    float* xnorm;                // [H][n_tokens] ||x||^2, or null
+    int xnorm_mode;              // kNormCompute / kNormStore / kNormLoad
 };
 
 // ----------------------------------------------------- shared memory map
 
 struct Layout {
-    uint32_t b_off, bx_off, ax_off, x_off, bar_off, misc_off, total;
+    uint32_t b_off, bx_off, ax_off, x_off, xch_off, bar_off, misc_off, total;
 };
 
 // Centroids (nA slabs of Cpad rows), the extra K block of the centroid side
 // (one slab of Cpad rows) and of the token side (one slab of 128 rows), the
-// token stages, then the barriers.
+// token stages, the epilogue pairs' exchange words ([pair][half][word][lane],
+// 8 words), then the barriers.
 __host__ __device__ inline Layout make_layout(int D, int Cpad, int stages) {
     Layout L;
     const int nA = D / 64;
@@ -90,6 +97,7 @@ __host__ __device__ inline Layout make_layout(int D, int Cpad, int stages) {
     L.bx_off = o;   o += (uint32_t)Cpad * 128;
     L.ax_off = o;   o += (uint32_t)kAtomBytes;
     L.x_off = o;    o += (uint32_t)stages * nA * kAtomBytes;
+    L.xch_off = o;  o += (uint32_t)(kEpiWarps / 2) * 2 * 8 * 32 * 4;
     L.bar_off = o;  o += (uint32_t)(2 * kMaxStages + 4) * 8;
     L.misc_off = o; o += 32;
     L.total = o + 1024;            // slack for 1024-byte alignment of the base
@@ -418,105 +426,149 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------ epilogue
-        const int e = warp - 2;                 // 0..7
-        const int g = e >> 2;                   // group = accumulator it drains
+        const int e = warp - 2;                 // 0..15
+        const int g = e >> 3;                   // group = accumulator it drains
+        const int hf = (e >> 2) & 1;            // half of the row's columns and channels
         const int q = warp & 3;                 // TMEM lane quadrant of this warp
         const int row = q * 32 + lane;          // tile row = TMEM lane
+        const int pair = g * 4 + q;             // the two warps (halves) on these rows
         constexpr int NW = CP / 32;             // 32-column chunks = mask words
+        constexpr int NWH = NW / 2;             // chunks per half
+        constexpr int NSH = 2 * NWH;            // 16-column tensor-memory reads per half
+        constexpr int DH = D / 2;               // channels per half
+        uint32_t* xw = reinterpret_cast<uint32_t*>(base + L.xch_off) + (size_t)pair * 2 * 8 * 32 + lane;
+        auto xword = [&](int half, int w) -> uint32_t* { return xw + (half * 8 + w) * 32; };
+        auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(1 + pair) : "memory"); };
         unsigned long long n_flag = 0, n_exact = 0, n_seq = 0;
         for (int i = g; i < n_tiles; i += 2) {
             const int st = i % NS;
             const uint32_t ph = (uint32_t)(i / NS) & 1u, aph = (uint32_t)(i >> 1) & 1u;
-            if (!mbar_wait(tfull_bar + 8 * g, aph) || !mbar_wait(full_bar + 8 * st, ph)) {
+            const int64_t tok = (int64_t)(t_begin + i) * kTile + row;
+            const bool valid = tok < a.n_tokens;
+            // a stored ||x||^2 is fetched before the waits
+            const bool load_norm = a.xnorm_mode == kNormLoad;
+            const float xnt_in = load_norm && valid ? __ldg(a.xnorm + (int64_t)h * a.n_tokens + tok) : 0.0f;
+            const bool ok = mbar_wait(tfull_bar + 8 * g, aph) && mbar_wait(full_bar + 8 * st, ph);
+            const uint8_t* xs = Xs + (size_t)st * nA * kAtomBytes;
+            const uint32_t taddr =
+                tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)g * acc_cols + 32u * (uint32_t)(hf * NWH);
+            uint32_t v[2][16];
+            float pmax = -INFINITY, pxn = 0.0f;
+            if (ok) {
+                tc_fence_after();
+                // The half's 2*NSH 16-column reads (pass A, then pass B) form
+                // one stream: read k+1 is in flight while read k is used, and
+                // the first overlaps the half's share of ||x||^2.
+                tmem_ld16(taddr, v[0]);
+                if (!load_norm) {
+                    float2 s2 = make_float2(0.0f, 0.0f), t2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+                    for (int i8 = hf * (DH / 8); i8 < (hf + 1) * (DH / 8); ++i8) {
+                        const uint4 w = *reinterpret_cast<const uint4*>(xs + sw_off(row, i8 * 8, kAtomBytes));
+                        const float2 f0 = make_float2(bf16_lo(w.x), bf16_hi(w.x)), f1 = make_float2(bf16_lo(w.y), bf16_hi(w.y));
+                        const float2 f2v = make_float2(bf16_lo(w.z), bf16_hi(w.z)), f3 = make_float2(bf16_lo(w.w), bf16_hi(w.w));
+                        s2 = f2_fma(f0, f0, s2);
+                        t2 = f2_fma(f1, f1, t2);
+                        s2 = f2_fma(f2v, f2v, s2);
+                        t2 = f2_fma(f3, f3, t2);
+                    }
+                    pxn = (s2.x + s2.y) + (t2.x + t2.y);
+                }
+                tmem_wait_ld_regs16(v[0]);
+                // pass A: the largest score of the half
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int c = 0; c < NSH; ++c) {
+                    // next: read c+1 of pass A, or read 0 of pass B
+                    tmem_ld16(taddr + 16u * ((c + 1) % NSH), v[(c + 1) & 1]);
+                    const uint32_t* u = v[c & 1];
+#pragma unroll
+                    for (int jj = 0; jj < 16; jj += 8) {
+                        m4[0] = fmax3(m4[0], __uint_as_float(u[jj]), __uint_as_float(u[jj + 1]));
+                        m4[1] = fmax3(m4[1], __uint_as_float(u[jj + 2]), __uint_as_float(u[jj + 3]));
+                        m4[2] = fmax3(m4[2], __uint_as_float(u[jj + 4]), __uint_as_float(u[jj + 5]));
+                        m4[3] = fmax3(m4[3], __uint_as_float(u[jj + 6]), __uint_as_float(u[jj + 7]));
+                    }
+                    tmem_wait_ld_regs16(v[(c + 1) & 1]);
+                }
+                pmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            }
+            // trade the halves' maxima and norms; a failed wait on either side
+            // stops both warps of the pair together
+            *xword(hf, 0) = __float_as_uint(pmax);
+            *xword(hf, 1) = __float_as_uint(pxn);
+            *xword(hf, 2) = ok ? 1u : 0u;
+            pair_sync();
+            if (!ok || !*xword(hf ^ 1, 2)) {
                 atomicExch(misc + 3, 1u);
                 break;
             }
-            tc_fence_after();
-            const uint8_t* xs = Xs + (size_t)st * nA * kAtomBytes;
-            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)g * acc_cols;
-            // The row's 2*NW chunk reads (pass A, then pass B) form one
-            // stream: chunk k+1 is loaded while chunk k is used, and the
-            // first load overlaps ||x||^2.
-            uint32_t v[2][32];
-            tmem_ld32(taddr, v[0]);
-            // ||x||^2 of this row (error bound of the screen)
-            float xnt;
-            {
-                float2 s2 = make_float2(0.0f, 0.0f), t2 = make_float2(0.0f, 0.0f);
-#pragma unroll
-                for (int i8 = 0; i8 < D / 8; ++i8) {
-                    const uint4 w = *reinterpret_cast<const uint4*>(xs + sw_off(row, i8 * 8, kAtomBytes));
-                    const float2 f0 = make_float2(bf16_lo(w.x), bf16_hi(w.x)), f1 = make_float2(bf16_lo(w.y), bf16_hi(w.y));
-                    const float2 f2v = make_float2(bf16_lo(w.z), bf16_hi(w.z)), f3 = make_float2(bf16_lo(w.w), bf16_hi(w.w));
-                    s2 = f2_fma(f0, f0, s2);
-                    t2 = f2_fma(f1, f1, t2);
-                    s2 = f2_fma(f2v, f2v, s2);
-                    t2 = f2_fma(f3, f3, t2);
-                }
-                xnt = (s2.x + s2.y) + (t2.x + t2.y);
-            }
-            tmem_wait_ld_regs(v[0]);
-            // pass A: the largest score of the row
-            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-            for (int c = 0; c < NW; ++c) {
-                // next: chunk c+1 of pass A, or chunk 0 of pass B
-                tmem_ld32(taddr + 32u * ((c + 1) % NW), v[(c + 1) & 1]);
-                const uint32_t* u = v[c & 1];
-#pragma unroll
-                for (int jj = 0; jj < 32; jj += 8) {
-                    m4[0] = fmax3(m4[0], __uint_as_float(u[jj]), __uint_as_float(u[jj + 1]));
-                    m4[1] = fmax3(m4[1], __uint_as_float(u[jj + 2]), __uint_as_float(u[jj + 3]));
-                    m4[2] = fmax3(m4[2], __uint_as_float(u[jj + 4]), __uint_as_float(u[jj + 5]));
-                    m4[3] = fmax3(m4[3], __uint_as_float(u[jj + 6]), __uint_as_float(u[jj + 7]));
-                }
-                tmem_wait_ld_regs(v[(c + 1) & 1]);
-            }
-            const float b1 = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            const float b1 = fmaxf(pmax, __uint_as_float(*xword(hf ^ 1, 0)));
+            const float xnt = load_norm ? xnt_in : __uint_as_float(*xword(0, 1)) + __uint_as_float(*xword(1, 1));
+            if (a.xnorm_mode == kNormStore && hf == 0 && valid) a.xnorm[(int64_t)h * a.n_tokens + tok] = xnt;
             // bound on the error of a score (half the bound on ||c||^2 - 2<x, c>)
             const float E = 0.5f * (1.01f * (kScreenXC * sqrtf(xnt) * cm + kScreenCC * cm2) + 1e-30f);
             const float thr = b1 - 2.0f * E;
-            // pass B: candidates within 2E of the largest score
-            uint32_t mw[NW];
+            // pass B: the half's candidates, the scores above thr.  E holds a
+            // 1% margin over the error bound, so the nearest centroid's score
+            // lies strictly above thr and the sign of the exactly rounded
+            // thr - score decides.  The signs are shifted into a word in
+            // column order (first column in the top bit), then bit-reversed.
+            // (NSH is even, so read 0 of pass B sits in buffer 0.)
+            const float2 thr2 = make_float2(thr, thr);
+            uint32_t mw[NWH], mrev = 0u;
 #pragma unroll
-            for (int c = 0; c < NW; ++c) {
-                const int b = (NW + c) & 1;              // buffer of pass-B chunk c
-                if (c + 1 < NW) tmem_ld32(taddr + 32u * (c + 1), v[b ^ 1]);
+            for (int c = 0; c < NSH; ++c) {
+                const int b = c & 1;
+                if (c + 1 < NSH) tmem_ld16(taddr + 16u * (c + 1), v[b ^ 1]);
                 const uint32_t* u = v[b];
-                uint32_t m4[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj)
-                    if (__uint_as_float(u[jj]) >= thr) m4[jj & 3] |= 1u << jj;
-                mw[c] = (m4[0] | m4[1]) | (m4[2] | m4[3]);
-                if (c + 1 < NW) tmem_wait_ld_regs(v[b ^ 1]);
+                for (int jj = 0; jj < 16; jj += 2) {
+                    const float2 d = f2_sub(thr2, make_float2(__uint_as_float(u[jj]), __uint_as_float(u[jj + 1])));
+                    mrev = __funnelshift_l(__float_as_uint(d.x), mrev, 1);
+                    mrev = __funnelshift_l(__float_as_uint(d.y), mrev, 1);
+                }
+                if (b == 1) mw[c >> 1] = __brev(mrev);
+                if (c + 1 < NSH) tmem_wait_ld_regs16(v[b ^ 1]);
             }
             // accumulator drained: hand it back to the MMA issuer
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar + 8 * g);
+            // the row's whole candidate mask, low half first
+#pragma unroll
+            for (int w = 0; w < NWH; ++w) *xword(hf, 4 + w) = mw[w];
+            pair_sync();
+            uint32_t m[NW];
+#pragma unroll
+            for (int w = 0; w < NWH; ++w) {
+                m[hf * NWH + w] = mw[w];
+                m[(hf ^ 1) * NWH + w] = *xword(hf ^ 1, 4 + w);
+            }
             int cnt = 0, first = -1;
 #pragma unroll
             for (int w = 0; w < NW; ++w) {
-                if (mw[w] && first < 0) first = 32 * w + __ffs(mw[w]) - 1;
-                cnt += __popc(mw[w]);
+                if (m[w] && first < 0) first = 32 * w + __ffs(m[w]) - 1;
+                cnt += __popc(m[w]);
             }
-            const int64_t tok = (int64_t)(t_begin + i) * kTile + row;
-            const bool valid = tok < a.n_tokens;
             uint8_t* idrow = a.ids + (int64_t)h * a.cap + a.tok_offset;
-            if (valid && cnt == 1) idrow[tok] = (uint8_t)first;
-            // undecided rows of this warp, one at a time, all lanes on the row
-            for (unsigned und = __ballot_sync(0xffffffffu, valid && cnt != 1); und; und &= und - 1) {
+            if (valid && cnt == 1 && hf == 0) idrow[tok] = (uint8_t)first;
+            // undecided rows of the pair, alternately to the two halves, one at
+            // a time with all lanes on the row
+            int k = 0;
+            for (unsigned und = __ballot_sync(0xffffffffu, valid && cnt != 1); und; und &= und - 1, ++k) {
+                if ((k & 1) != hf) continue;
                 const int src = __ffs(und) - 1;
                 const int r = q * 32 + src;
-                uint32_t m[NW];
+                uint32_t mr[NW];
 #pragma unroll
-                for (int w = 0; w < NW; ++w) m[w] = __shfl_sync(0xffffffffu, mw[w], src);
+                for (int w = 0; w < NW; ++w) mr[w] = __shfl_sync(0xffffffffu, m[w], src);
                 // direct fp32 distances of every candidate; lane k keeps candidate k
                 float dmin = INFINITY, myd = INFINITY;
                 int ncand = 0, myj = -1;
 #pragma unroll
                 for (int w = 0; w < NW; ++w)
-                    for (uint32_t mm = m[w]; mm; mm &= mm - 1) {
+                    for (uint32_t mm = mr[w]; mm; mm &= mm - 1) {
                         const int j = 32 * w + __ffs(mm) - 1;
                         const float d = warp_dist<D>(xs, r, Bs, j, cslab, lane);
                         if (lane == (ncand & 31)) { myd = d; myj = j; }
@@ -532,7 +584,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (__popc(sb) == 1) best = __shfl_sync(0xffffffffu, myj, __ffs(sb) - 1);
                 }
                 if (best < 0) {
-                    best = rerank_exact<D, CP>(xs, r, Bs, cslab, lane, m, sb, myj, ncand, dmin, emin, n_seq);
+                    best = rerank_exact<D, CP>(xs, r, Bs, cslab, lane, mr, sb, myj, ncand, dmin, emin, n_seq);
                     ++n_exact;
                 }
                 if (lane == 0 && best >= 0) idrow[(int64_t)(t_begin + i) * kTile + r] = (uint8_t)best;
@@ -611,6 +663,8 @@ cudaError_t assign_tc_d(int H, const AssignArgs& a, bool* launched, cudaStream_t
     t.ctas_per_head = ctas_per_head(H, t.tiles_per_head);
     t.stats = a.stats;
     t.err = a.err;
+    t.xnorm = a.xnorm;
+    t.xnorm_mode = a.xnorm ? a.xnorm_mode : kNormCompute;
     // three token stages when they fit in shared memory, else two
     t.stages = kMaxStages;
     Layout L = make_layout(D, t.Cpad, t.stages);

@@ -43,7 +43,13 @@ struct AssignArgs {
     int* counts;            // [H][C] or nullptr
     unsigned long long* stats;  // [4] refinement counters or nullptr
     uint32_t* err;              // error code of a kernel that gave up a wait, or nullptr
+    // ||x_n||^2 per (head, token) [H][n_tokens], fp32 (tensor-core path only):
+    // kNormCompute ignores it, kNormStore computes and stores it, kNormLoad
+    // reads what an earlier kNormStore call wrote for the same x.
+    float* xnorm;
+    int xnorm_mode;
 };
+constexpr int kNormCompute = 0, kNormStore = 1, kNormLoad = 2;
 
 constexpr int kPieceTokens = 64;   // tokens per exact partial sum of the update
 constexpr int kSortBlock = 2048;   // tokens per block of the update's counting sort
