@@ -18,9 +18,10 @@
 //         chunk.
 //  reduce the partials added in chunk order, a thread per element
 //         (deterministic).
-//  solve  one CTA per head: forms the right-hand side C - P U_h^T (t as its bf16 hi + lo pair),
-//         adds the ridge, factors G = L L^T (fp32, right-looking) and solves
-//         the 128 right-hand sides in parallel.
+//  solve  eight CTAs per head, 16 right-hand sides each: forms those columns
+//         of C - P U_h^T (t as its bf16 hi + lo pair), adds the ridge,
+//         factors G = L L^T (fp32, right-looking; every CTA of the head
+//         factors the same G the same way) and solves its columns.
 // The low-rank projection t comes from the tensor-core low-rank kernel.
 #include "common.cuh"
 #include "kernels.h"
@@ -135,6 +136,8 @@ __global__ void __launch_bounds__(256) coral_gram_reduce_kernel(const float* par
 }
 
 constexpr int kLdS = kFD + 1;     // padded fp32 rows of the solve
+constexpr int kSolveCols = 16;    // right-hand sides (columns of B_h^T) per solve CTA
+constexpr int kLdR = kSolveCols + 1;
 
 struct SolveArgs {
     const float* red;     // [H][kFBlocks][128][128]: X^T X, X^T Y, X^T t
@@ -147,27 +150,30 @@ struct SolveArgs {
 __global__ void __launch_bounds__(256) coral_solve_kernel(SolveArgs a) {
     extern __shared__ float sm[];
     float* Gm = sm;                         // [128][kLdS]: G, then its Cholesky factor L (lower)
-    float* Rm = Gm + kFD * kLdS;            // [128][kLdS]: right-hand sides, then solutions
-    float* Pm = Rm + kFD * kLdS;            // [128][64]: X_h^T (t_hi | t_lo)
-    float* Us = Pm + kFD * 64;              // [128][32]: U_h
+    float* Rm = Gm + kFD * kLdS;            // [128][kLdR]: this CTA's right-hand sides, then solutions
+    float* Pm = Rm + kFD * kLdR;            // [128][64]: X_h^T (t_hi | t_lo)
+    float* Us = Pm + kFD * 64;              // [kSolveCols][32]: the rows of U_h for those columns
     __shared__ float trace_s;
-    const int tid = threadIdx.x, h = blockIdx.x;
+    const int tid = threadIdx.x, h = blockIdx.y, o0 = blockIdx.x * kSolveCols;
     const float* base = a.red + (int64_t)h * kFBlocks * (kFD * kFD);
     for (int e = tid; e < kFD * kFD; e += 256) {
         const int i = e >> 7, k = e & 127;
         Gm[i * kLdS + k] = base[e];
-        Rm[i * kLdS + k] = base[kFD * kFD + e];
         if (k < 64) Pm[i * 64 + k] = base[2 * kFD * kFD + e];
     }
-    for (int e = tid; e < kFD * kFR; e += 256) Us[e] = bf16f(a.U[(int64_t)h * kFD * kFR + e]);
+    for (int e = tid; e < kFD * kSolveCols; e += 256) {
+        const int i = e / kSolveCols, c = e % kSolveCols;
+        Rm[i * kLdR + c] = base[kFD * kFD + i * kFD + o0 + c];
+    }
+    for (int e = tid; e < kSolveCols * kFR; e += 256) Us[e] = bf16f(a.U[((int64_t)h * kFD + o0) * kFR + e]);
     __syncthreads();
-    // right-hand side C - P U_h^T, with P = X_h^T (t_hi + t_lo)
-    for (int e = tid; e < kFD * kFD; e += 256) {
-        const int i = e >> 7, o = e & 127;
+    // right-hand sides C - P U_h^T, with P = X_h^T (t_hi + t_lo)
+    for (int e = tid; e < kFD * kSolveCols; e += 256) {
+        const int i = e / kSolveCols, c = e % kSolveCols;
         float s = 0.0f;
 #pragma unroll 8
-        for (int r = 0; r < kFR; ++r) s = fmaf(Pm[i * 64 + r] + Pm[i * 64 + kFR + r], Us[o * kFR + r], s);
-        Rm[i * kLdS + o] -= s;
+        for (int r = 0; r < kFR; ++r) s = fmaf(Pm[i * 64 + r] + Pm[i * 64 + kFR + r], Us[c * kFR + r], s);
+        Rm[i * kLdR + c] -= s;
     }
     if (tid < 32) {
         float t = 0.0f;
@@ -180,60 +186,52 @@ __global__ void __launch_bounds__(256) coral_solve_kernel(SolveArgs a) {
     const float tr = trace_s;
     uint16_t* Bh = a.B + (int64_t)h * kFD * kFD;
     if (!(tr > 0.0f)) {
-        for (int e = tid; e < kFD * kFD; e += 256) Bh[e] = 0;
+        for (int e = tid; e < kSolveCols * kFD; e += 256) Bh[(int64_t)o0 * kFD + e] = 0;
         return;
     }
     const float lambda = ldexpf(tr / kFD, -20);
     if (tid < kFD) Gm[tid * kLdS + tid] += lambda;
     __syncthreads();
-    // right-looking Cholesky, G = L L^T in the lower triangle
+    // right-looking Cholesky, G = L L^T in the lower triangle; the trailing
+    // update of step j is spread over the threads element by element (16 x 16
+    // thread grid), each element updated once per step, steps in order
+    const int ty = tid >> 4, tx = tid & 15;
     for (int j = 0; j < kFD; ++j) {
         if (tid == 0) Gm[j * kLdS + j] = sqrtf(fmaxf(Gm[j * kLdS + j], 1e-30f));
         __syncthreads();
         const float d = Gm[j * kLdS + j];
         for (int i = j + 1 + tid; i < kFD; i += 256) Gm[i * kLdS + j] /= d;
         __syncthreads();
-        // trailing update of the lower triangle, a thread per row
-        for (int i = j + 1 + tid; i < kFD; i += 256) {
+        for (int i = j + 1 + ty; i < kFD; i += 16) {
             const float lij = Gm[i * kLdS + j];
-            for (int k = j + 1; k <= i; ++k) Gm[i * kLdS + k] -= lij * Gm[k * kLdS + j];
+            for (int k = j + 1 + tx; k <= i; k += 16) Gm[i * kLdS + k] -= lij * Gm[k * kLdS + j];
         }
         __syncthreads();
     }
-    // thread o solves L u = r_o, then L^T z = u, in its column of Rm; four
-    // partial sums per dot product keep the FMA chains short
-    if (tid < kFD) {
-        const int o = tid;
-        for (int i = 0; i < kFD; ++i) {
-            float v0 = Rm[i * kLdS + o], v1 = 0.0f, v2 = 0.0f, v3 = 0.0f;
-            int k = 0;
-            for (; k + 3 < i; k += 4) {
-                v0 -= Gm[i * kLdS + k] * Rm[k * kLdS + o];
-                v1 -= Gm[i * kLdS + k + 1] * Rm[(k + 1) * kLdS + o];
-                v2 -= Gm[i * kLdS + k + 2] * Rm[(k + 2) * kLdS + o];
-                v3 -= Gm[i * kLdS + k + 3] * Rm[(k + 3) * kLdS + o];
-            }
-            for (; k < i; ++k) v0 -= Gm[i * kLdS + k] * Rm[k * kLdS + o];
-            Rm[i * kLdS + o] = ((v0 + v1) + (v2 + v3)) / Gm[i * kLdS + i];
+    // L u = r, then L^T z = u, for the CTA's columns: right-looking, a row's
+    // value fixed by its division, then subtracted from the rows it feeds
+    for (int i = 0; i < kFD; ++i) {
+        if (tid < kSolveCols) Rm[i * kLdR + tid] /= Gm[i * kLdS + i];
+        __syncthreads();
+        for (int e = tid; e < (kFD - 1 - i) * kSolveCols; e += 256) {
+            const int k = i + 1 + e / kSolveCols, c = e % kSolveCols;
+            Rm[k * kLdR + c] -= Gm[k * kLdS + i] * Rm[i * kLdR + c];
         }
-        for (int i = kFD - 1; i >= 0; --i) {
-            float v0 = Rm[i * kLdS + o], v1 = 0.0f, v2 = 0.0f, v3 = 0.0f;
-            int k = i + 1;
-            for (; k + 3 < kFD; k += 4) {
-                v0 -= Gm[k * kLdS + i] * Rm[k * kLdS + o];
-                v1 -= Gm[(k + 1) * kLdS + i] * Rm[(k + 1) * kLdS + o];
-                v2 -= Gm[(k + 2) * kLdS + i] * Rm[(k + 2) * kLdS + o];
-                v3 -= Gm[(k + 3) * kLdS + i] * Rm[(k + 3) * kLdS + o];
-            }
-            for (; k < kFD; ++k) v0 -= Gm[k * kLdS + i] * Rm[k * kLdS + o];
-            Rm[i * kLdS + o] = ((v0 + v1) + (v2 + v3)) / Gm[i * kLdS + i];
-        }
+        __syncthreads();
     }
-    __syncthreads();
+    for (int i = kFD - 1; i >= 0; --i) {
+        if (tid < kSolveCols) Rm[i * kLdR + tid] /= Gm[i * kLdS + i];
+        __syncthreads();
+        for (int e = tid; e < i * kSolveCols; e += 256) {
+            const int k = e / kSolveCols, c = e % kSolveCols;
+            Rm[k * kLdR + c] -= Gm[i * kLdS + k] * Rm[i * kLdR + c];
+        }
+        __syncthreads();
+    }
     // B[o][i] = z_o[i]
-    for (int e = tid; e < kFD * kFD; e += 256) {
-        const int o = e >> 7, i = e & 127;
-        Bh[e] = __bfloat16_as_ushort(__float2bfloat16_rn(Rm[i * kLdS + o]));
+    for (int e = tid; e < kSolveCols * kFD; e += 256) {
+        const int c = e >> 7, i = e & 127;
+        Bh[(int64_t)(o0 + c) * kFD + i] = __bfloat16_as_ushort(__float2bfloat16_rn(Rm[i * kLdR + c]));
     }
 }
 
@@ -256,11 +254,11 @@ cudaError_t launch_coral_fit(const uint16_t* xh, const uint16_t* y, const uint16
     const int64_t total = (int64_t)H * kFBlocks * kFD * kFD;
     coral_gram_reduce_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(part, chunks, total, red);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const size_t smem = sizeof(float) * (2 * kFD * kLdS + kFD * 64 + kFD * kFR);
+    const size_t smem = sizeof(float) * (kFD * kLdS + kFD * kLdR + kFD * 64 + kSolveCols * kFR);
     e = cudaFuncSetAttribute(coral_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     SolveArgs sa{red, U, H, B};
-    coral_solve_kernel<<<(unsigned)H, 256, smem, s>>>(sa);
+    coral_solve_kernel<<<dim3(kFD / kSolveCols, (unsigned)H), 256, smem, s>>>(sa);
     return cudaGetLastError();
 }
 
