@@ -63,12 +63,26 @@ struct GramArgs {
     float* part;          // [H][kFBlocks][chunks][128][128]
 };
 
+// 16-byte asynchronous copy global -> shared; src_bytes = 0 fills zeros (the
+// source address must still be a valid one).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+constexpr int kGramStages = 3;    // token slices in flight
+
 // grid (chunks, kFBlocks, H), 256 threads.  Warp w owns rows i in
 // [16w, 16w + 16) of X_h^T B over the chunk's tokens, B = the column block
-// (128 columns; 64 for t).
+// (128 columns; 64 for t).  The 32-token slices of X_h and B stream through a
+// three-stage ring of asynchronous copies, so a slice's loads overlap the
+// MMAs of the two before it; the slices are summed in token order.
 __global__ void __launch_bounds__(256) coral_gram_kernel(GramArgs a) {
-    __shared__ __align__(16) uint16_t xs[kFStep][kLdX];
-    __shared__ __align__(16) uint16_t bs[kFStep][kLdX];
+    extern __shared__ __align__(16) uint16_t gram_smem[];
+    auto xs = reinterpret_cast<uint16_t(*)[kFStep][kLdX]>(gram_smem);                                  // [stage][32][kLdX]
+    auto bs = reinterpret_cast<uint16_t(*)[kFStep][kLdX]>(gram_smem + kGramStages * kFStep * kLdX);    // [stage][32][kLdX]
     const int chunk = blockIdx.x, cb = blockIdx.y, h = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t HD = (int64_t)a.H * kFD;
@@ -81,36 +95,50 @@ __global__ void __launch_bounds__(256) coral_gram_kernel(GramArgs a) {
 #pragma unroll
     for (int j = 0; j < 16; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
     const int mi = lane >> 3, rr = lane & 7;
-    for (int64_t nb = n0; nb < n1; nb += kFStep) {
-        // the slice's rows of X_h (32 x 128 bf16) and of the column block
+    const int nslices = (int)((n1 - n0 + kFStep - 1) / kFStep);
+    // slice sl's rows of X_h (32 x 128 bf16) and of the column block into stage st;
+    // rows past the chunk and columns past the block are zero-filled
+    auto load_slice = [&](int sl, int st) {
+        const int64_t nb = n0 + (int64_t)sl * kFStep;
         for (int v = tid; v < kFStep * 16; v += 256) {
             const int r = v >> 4, k = v & 15;
             const int64_t n = nb + r;
-            *reinterpret_cast<uint4*>(&xs[r][8 * k]) =
-                n < n1 ? ldg_nc_v4(a.xh + n * HD + h * kFD + 8 * k) : make_uint4(0, 0, 0, 0);
+            const bool in = n < n1;
+            const int64_t nn = in ? n : n0;
+            cp_async16(saddr(&xs[st][r][8 * k]), a.xh + nn * HD + h * kFD + 8 * k, in ? 16u : 0u);
             const bool col_ok = 8 * k < ncol;
-            *reinterpret_cast<uint4*>(&bs[r][8 * k]) =
-                (n < n1 && col_ok) ? ldg_nc_v4(bsrc + n * bstride + 8 * k) : make_uint4(0, 0, 0, 0);
+            cp_async16(saddr(&bs[st][r][8 * k]), bsrc + nn * bstride + (col_ok ? 8 * k : 0), (in && col_ok) ? 16u : 0u);
         }
-        __syncthreads();
+    };
+#pragma unroll
+    for (int sl = 0; sl < kGramStages - 1; ++sl) {
+        if (sl < nslices) load_slice(sl, sl);
+        cp_async_commit();
+    }
+    for (int sl = 0; sl < nslices; ++sl) {
+        const int st = sl % kGramStages;
+        cp_async_wait<kGramStages - 2>();       // this thread's copies of slice sl have landed
+        __syncthreads();                        // everyone's; and slice sl - 1 is no longer read
+        if (sl + kGramStages - 1 < nslices) load_slice(sl + kGramStages - 1, (sl + kGramStages - 1) % kGramStages);
+        cp_async_commit();
 #pragma unroll
         for (int kk = 0; kk < kFStep; kk += 16) {
             // A = X_h^T (rows i, columns = tokens): matrices (tok 0-7 | 8-15) x (i 0-7 | 8-15)
             uint32_t af[4];
-            ldsm_x4_t(saddr(&xs[kk + ((mi >> 1) << 3) + rr][16 * warp + ((mi & 1) << 3)]), af[0], af[1], af[2],
+            ldsm_x4_t(saddr(&xs[st][kk + ((mi >> 1) << 3) + rr][16 * warp + ((mi & 1) << 3)]), af[0], af[1], af[2],
                       af[3]);
 #pragma unroll
             for (int p = 0; p < 8; ++p) {
                 if (16 * p >= ncol) break;
                 // B = block columns j (as the n dimension), tokens as k
                 uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(saddr(&bs[kk + ((mi & 1) << 3) + rr][16 * p + ((mi >> 1) << 3)]), b0, b1, b2, b3);
+                ldsm_x4_t(saddr(&bs[st][kk + ((mi & 1) << 3) + rr][16 * p + ((mi >> 1) << 3)]), b0, b1, b2, b3);
                 mma_bf16(acc[2 * p], af, b0, b1);
                 mma_bf16(acc[2 * p + 1], af, b2, b3);
             }
         }
-        __syncthreads();
     }
+    cp_async_wait<0>();
     float* out = a.part + (((int64_t)h * kFBlocks + cb) * a.chunks + chunk) * (kFD * kFD);
     const int g = lane >> 2, q = lane & 3;
 #pragma unroll
@@ -247,7 +275,10 @@ cudaError_t launch_coral_fit(const uint16_t* xh, const uint16_t* y, const uint16
                              int64_t n_tokens, int H, float* part, uint16_t* B, cudaStream_t s) {
     const int chunks = (int)((n_tokens + kFitChunkTokens - 1) / kFitChunkTokens);
     GramArgs ga{xh, y, t2, n_tokens, H, chunks, part};
-    coral_gram_kernel<<<dim3((unsigned)chunks, kFBlocks, (unsigned)H), 256, 0, s>>>(ga);
+    const size_t gsmem = sizeof(uint16_t) * 2 * kGramStages * kFStep * kLdX;
+    cudaError_t ge = cudaFuncSetAttribute(coral_gram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gsmem);
+    if (ge != cudaSuccess) return ge;
+    coral_gram_kernel<<<dim3((unsigned)chunks, kFBlocks, (unsigned)H), 256, gsmem, s>>>(ga);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     float* red = part + (size_t)H * kFBlocks * chunks * kFD * kFD;
