@@ -238,3 +238,28 @@ def test_four_bit_half_integer_ties(qvg, oracle, G):
     enc, dec = run_fit_encode_decode(qvg, cfg, to_dev(xb), N, N * D, D)
     for h in range(H):
         check_unit(oracle, xb[h], enc, dec, h, 0, 0, S, G, b=4)
+
+
+def test_fit_reuses_workspace_without_stale_norms(qvg, oracle):
+    """A fit keeps ||x||^2 per token in the workspace for its later assign
+    steps; a second fit on other data in the same workspace must not use the
+    first fit's norms.  The first fit runs on x / 64 (exact in bf16), so stale
+    norms would shrink the screen's error bound on the second."""
+    rng = np.random.default_rng(31)
+    H, D, N, C, T = 2, 128, 3000, 64, 3
+    xb = np.stack([mixture(rng, N, D, M=48, spread=1.0, noise=0.2) for _ in range(H)])
+    small = SY.f64_to_bf16_bits(SY.bf16_bits_to_f32(xb).astype(np.float64) / 64.0)
+    cfg = qvg.config(H, D, C, T, 2, 64)
+    ws = qvg.alloc_workspace(cfg, N)
+    cent = torch.empty(H * C * D, dtype=torch.int16, device="cuda")
+    ids = torch.empty(H * N, dtype=torch.uint8, device="cuda")
+    qvg.qvg_fit_centroids(cfg, to_dev(small), N, N * D, D, None, cent, ids, N, 0, ws)
+    qvg.qvg_fit_centroids(cfg, to_dev(xb), N, N * D, D, None, cent, ids, N, 0, ws)
+    torch.cuda.synchronize()
+    got_c = u16(cent).reshape(H, C, D)
+    got_i = ids.cpu().numpy().reshape(H, N).astype(np.int32)
+    for h in range(H):
+        oc, oi = oracle.fit(xb[h], C, T)
+        np.testing.assert_array_equal(got_c[h], oc, err_msg=f"centroids head {h}")
+        np.testing.assert_array_equal(got_i[h], oi, err_msg=f"ids head {h}")
+    assert qvg.qvg_fit_stats(cfg, N, ws)[3] == 0
