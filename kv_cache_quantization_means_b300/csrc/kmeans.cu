@@ -486,13 +486,14 @@ __device__ __forceinline__ i128 shfl_xor_i128(i128 v, int mask) {
     return (i128)(((u128)ohi << 64) | (u128)olo);
 }
 
-// One warp per piece.  The warp first stages the piece's rows (at most
-// kPieceTokens, gathered in sorted order) into its slice of shared memory with
-// 16-byte asynchronous copies, all in flight at once, then sums them from
-// there.  A lane owns 8 consecutive channels of one row slot; D/8 lanes cover
-// a row and 32/(D/8) rows go per instruction.  Row slots are reduced at the
-// end (integer additions: exact, any order).
+// One warp per piece.  The warp stages the piece's rows (at most
+// kPieceTokens, gathered in sorted order) kSumRows at a time into its slice of
+// shared memory with 16-byte asynchronous copies, all of a round in flight at
+// once, then sums them from there.  A lane owns 8 consecutive channels of one
+// row slot; D/8 lanes cover a row and 32/(D/8) rows go per instruction.  Row
+// slots are reduced at the end (integer additions: exact, any order).
 constexpr int kSumWarps = 4;
+constexpr int kSumRows = 32;      // rows staged per round
 static_assert(kPieceTokens <= 64, "a warp holds a piece's token indices in two registers per lane");
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
@@ -500,15 +501,15 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(32 * kSumWarps, 3) kmeans_sum_kernel(UpdateArgs a) {
+__global__ void __launch_bounds__(32 * kSumWarps, 6) kmeans_sum_kernel(UpdateArgs a) {
     constexpr int LPR = D / 8, RPI = 32 / LPR;
-    extern __shared__ __align__(16) uint16_t sum_rows[];     // [warp][kPieceTokens][D]
+    extern __shared__ __align__(16) uint16_t sum_rows[];     // [warp][kSumRows][D]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int sub = lane % LPR, slot = lane / LPR;
     const int h = blockIdx.y;
     const int p = blockIdx.x * kSumWarps + warp;
     if (p >= a.npieces[h]) return;
-    uint16_t* rows = sum_rows + (size_t)warp * kPieceTokens * D;
+    uint16_t* rows = sum_rows + (size_t)warp * kSumRows * D;
     const int4 pc = a.pieces[(int64_t)h * a.max_pieces + p];
     const int start = pc.x, len = pc.y, j = pc.z;
     const int* ph = a.perm + (int64_t)h * a.n_tokens + start;
@@ -516,28 +517,36 @@ __global__ void __launch_bounds__(32 * kSumWarps, 3) kmeans_sum_kernel(UpdateArg
     // the piece's token indices (len <= kPieceTokens = 64): lane k holds
     // positions k and k + 32
     const int pa = lane < len ? ph[lane] : 0, pb = lane + 32 < len ? ph[lane + 32] : 0;
-    for (int k0 = 0; k0 < len; k0 += RPI) {
-        const int k = k0 + slot;
-        const int na = __shfl_sync(0xffffffffu, pa, k & 31), nb = __shfl_sync(0xffffffffu, pb, k & 31);
-        if (k < len) cp_async16(smem_u32(rows + k * D + sub * 8), xh + (int64_t)(k < 32 ? na : nb) * a.token_stride);
-    }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
-    __syncwarp();
+    // rows [r0, r0 + kSumRows) of the piece into the warp's slice
+    auto stage = [&](int r0) {
+        for (int k0 = 0; k0 < kSumRows; k0 += RPI) {
+            const int k = r0 + k0 + slot;
+            const int na = __shfl_sync(0xffffffffu, pa, k & 31), nb = __shfl_sync(0xffffffffu, pb, k & 31);
+            if (k < len)
+                cp_async16(smem_u32(rows + (k0 + slot) * D + sub * 8), xh + (int64_t)(k < 32 ? na : nb) * a.token_stride);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncwarp();
+    };
     int w1[8], w2[8], w3[8];
 #pragma unroll
     for (int d = 0; d < 8; ++d) w1[d] = w2[d] = w3[d] = 0;
     float amax = 0.0f;
-#pragma unroll 4
-    for (int k = slot; k < len; k += RPI) {
-        const uint4 v = *reinterpret_cast<const uint4*>(rows + k * D + sub * 8);
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+    for (int r0 = 0; r0 < len; r0 += kSumRows) {
+        stage(r0);
+#pragma unroll 2
+        for (int k = slot; k < kSumRows && r0 + k < len; k += RPI) {
+            const uint4 v = *reinterpret_cast<const uint4*>(rows + k * D + sub * 8);
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float lo = bf16_lo(wv[q]), hi = bf16_hi(wv[q]);
-            amax = fmax3(amax, fabsf(lo), fabsf(hi));
-            window_add2(make_float2(lo, hi), w1 + 2 * q, w2 + 2 * q, w3 + 2 * q);
+            for (int q = 0; q < 4; ++q) {
+                const float lo = bf16_lo(wv[q]), hi = bf16_hi(wv[q]);
+                amax = fmax3(amax, fabsf(lo), fabsf(hi));
+                window_add2(make_float2(lo, hi), w1 + 2 * q, w2 + 2 * q, w3 + 2 * q);
+            }
         }
+        __syncwarp();                      // the slice is read before the next round overwrites it
     }
     i128 tot[8];
     if (__any_sync(0xffffffffu, !(amax < kWinMax))) {
@@ -545,7 +554,7 @@ __global__ void __launch_bounds__(32 * kSumWarps, 3) kmeans_sum_kernel(UpdateArg
 #pragma unroll
         for (int d = 0; d < 8; ++d) tot[d] = 0;
         for (int k = slot; k < len; k += RPI) {
-            const uint4 v = *reinterpret_cast<const uint4*>(rows + k * D + sub * 8);
+            const uint4 v = ldg_nc_v4(xh + (int64_t)ph[k] * a.token_stride);
             const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -634,7 +643,7 @@ cudaError_t update_d(const UpdateArgs& a, cudaStream_t s) {
     kmeans_hist_kernel<<<g1, kThreads, 0, s>>>(a);
     kmeans_scatter_kernel<<<g1, kThreads, 0, s>>>(a);
     dim3 g2((unsigned)((a.max_pieces + kSumWarps - 1) / kSumWarps), (unsigned)a.H);
-    const size_t sum_smem = sizeof(uint16_t) * kSumWarps * kPieceTokens * D;
+    const size_t sum_smem = sizeof(uint16_t) * kSumWarps * kSumRows * D;
     cudaError_t e = cudaFuncSetAttribute(kmeans_sum_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)sum_smem);
     if (e != cudaSuccess) return e;
