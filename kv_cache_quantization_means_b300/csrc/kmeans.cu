@@ -493,7 +493,7 @@ __device__ __forceinline__ i128 shfl_xor_i128(i128 v, int mask) {
 // row slot; D/8 lanes cover a row and 32/(D/8) rows go per instruction.  Row
 // slots are reduced at the end (integer additions: exact, any order).
 constexpr int kSumWarps = 4;
-constexpr int kSumRows = 32;      // rows staged per round
+constexpr int kSumRows = 16;      // rows staged per round
 static_assert(kPieceTokens <= 64, "a warp holds a piece's token indices in two registers per lane");
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
@@ -501,7 +501,7 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(32 * kSumWarps, 6) kmeans_sum_kernel(UpdateArgs a) {
+__global__ void __launch_bounds__(32 * kSumWarps, 8) kmeans_sum_kernel(UpdateArgs a) {
     constexpr int LPR = D / 8, RPI = 32 / LPR;
     extern __shared__ __align__(16) uint16_t sum_rows[];     // [warp][kSumRows][D]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
