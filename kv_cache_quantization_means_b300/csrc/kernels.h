@@ -52,7 +52,7 @@ struct AssignArgs {
 constexpr int kNormCompute = 0, kNormStore = 1, kNormLoad = 2;
 
 constexpr int kPieceTokens = 64;   // tokens per exact partial sum of the update
-constexpr int kSortBlock = 2048;   // tokens per block of the update's counting sort
+constexpr int kSortBlock = 1024;   // tokens per block of the update's counting sort
 
 struct UpdateArgs {
     const uint16_t* x;
