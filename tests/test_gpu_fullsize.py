@@ -144,3 +144,35 @@ def test_coral_full_size_token_slices(qvg, oracle):
                 p64 = oracle.coral_predict(xprev, Bm, Um, Wm, H, D)
                 assert np.max(np.abs(gp[rows] - p64)) < 1e-3
         prev = xh
+
+
+def test_bench_step_on_four_streams_matches_one_stream(qvg, oracle):
+    """The bench times the Wan2.1 step with its (layer, tensor) units spread
+    over four streams, a workspace per stream.  Four layers of that step must
+    give, unit for unit, the bytes of the same units run in order on one
+    stream; one head of the last unit is checked against the oracle."""
+    import bench
+    wl = bench.workload("wan")
+    L, H, D, N = 4, wl.heads, wl.head_dim, wl.tokens
+    runs = []
+    for streams in (4, 1):
+        st = bench.QvgStep(qvg, wl, L, streams=streams)
+        st.step()
+        torch.cuda.synchronize()
+        res = {(l, t): {k: st.enc[l][t][k].cpu().clone() for k in ("codes", "meta", "ids", "centroids")}
+               for l in range(L) for t in (0, 1)}
+        last = st.out[st.slot(L - 1, 1)].cpu().clone()
+        runs.append((res, last))
+        del st
+        torch.cuda.empty_cache()
+    (a, la), (b, lb) = runs
+    for key in a:
+        for k in a[key]:
+            assert torch.equal(a[key][k], b[key][k]), f"unit {key}: {k} differs between four streams and one"
+    assert torch.equal(la, lb), "decoded output differs between four streams and one"
+    h = 3
+    xh = SY.mixture_unit(wl, L - 1, 1, h)
+    oc, oi = oracle.fit(xh, wl.clusters, wl.lloyd_iters)
+    got = a[(L - 1, 1)]
+    np.testing.assert_array_equal(got["centroids"].numpy().view(np.uint16).reshape(H, wl.clusters, D)[h], oc)
+    np.testing.assert_array_equal(got["ids"].numpy().reshape(H, N)[h].astype(np.int32), oi)
