@@ -275,6 +275,42 @@ QVG_API qvg_status coral_predict_decode(const qvg_config* cfg, const coral_predi
                                 const uint32_t* meta, qvg_bf16* xhat_next, float* pred_out,
                                 void* workspace, size_t workspace_bytes, qvg_stream stream);
 
+/* Coral-KV + SAS hybrid: the cross-layer prediction (Coral-KV pages, the
+ * block-diagonal plus low-rank predictor of layer l+1 from the reconstructed
+ * layer l) combined with the k-means smoothing of Quant VideoGen (Sommario
+ * tecnico sec. 2A), applied to the prediction residual.  The pages do not
+ * describe the combination; this library's reading, per layer:
+ *   pred  = block-DPLR(xhat_prev) in fp32 (0 when xhat_prev is NULL),
+ *   r     = bf16(x_next - pred)            (fp32 difference, then RN to bf16),
+ *   centroids, ids = k-means of r per head (init + T Lloyd steps, as
+ *                    qvg_fit_centroids), codes/meta = PRQ of r - c[id]
+ *                    (as qvg_encode),
+ *   r_hat = the decoded residual (as qvg_decode), xhat_next = bf16(pred + r_hat).
+ * cfg: num_clusters C >= 1, lloyd_iters >= 1, bits 2, head_dim 64 or 128.
+ * Buffers (device memory, caller-owned, 16-byte aligned): xhat_prev, x_next,
+ * xhat_next token-major bf16 [n_tokens][H*D]; codes [S][H][n_tokens][D/16],
+ * meta [S][H][n_tokens][D/G], ids [H][n_tokens], centroids bf16 [H][C][D];
+ * pred_out fp32 [n_tokens][H*D] or NULL (receives the prediction).
+ * workspace: coral_sas_workspace_bytes of it, 256-byte aligned; it begins
+ * with the k-means workspace, so qvg_fit_stats(cfg, n_tokens, workspace, ...)
+ * reports the re-rank counters and the error word of both the k-means and the
+ * cross-layer kernels.  Errors: invalid arguments return an error code and
+ * launch nothing; asynchronous. */
+QVG_API qvg_status coral_sas_workspace_bytes(const qvg_config* cfg, int64_t n_tokens, size_t* bytes);
+
+QVG_API qvg_status coral_sas_encode(const qvg_config* cfg, const coral_predictor* pred, const qvg_bf16* xhat_prev,
+                                    const qvg_bf16* x_next, int64_t n_tokens, uint32_t* codes, uint32_t* meta,
+                                    uint8_t* ids, qvg_bf16* centroids, qvg_bf16* xhat_next, float* pred_out,
+                                    void* workspace, size_t workspace_bytes, qvg_stream stream);
+
+/* Decoder twin of coral_sas_encode: xhat_next = bf16(pred + r_hat) from
+ * xhat_prev, the predictor and the stored codes, meta, ids and centroids
+ * (bit-identical to the encoder's xhat_next). */
+QVG_API qvg_status coral_sas_decode(const qvg_config* cfg, const coral_predictor* pred, const qvg_bf16* xhat_prev,
+                                    int64_t n_tokens, const uint32_t* codes, const uint32_t* meta, const uint8_t* ids,
+                                    const qvg_bf16* centroids, qvg_bf16* xhat_next, float* pred_out,
+                                    void* workspace, size_t workspace_bytes, qvg_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

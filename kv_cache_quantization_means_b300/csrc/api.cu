@@ -172,9 +172,10 @@ qvg::UpdateArgs update_args(const qvg_config* c, const qvg_bf16* x, int64_t n, i
 // T Lloyd iterations (init already in `cent`).
 qvg_status lloyd(const qvg_config* c, const qvg_bf16* x, int64_t n, int64_t hs, int64_t ts,
                  qvg_bf16* cent, uint8_t* ids, int64_t cap, int64_t off, const FitWorkspace& w,
-                 cudaStream_t s) {
-    cudaError_t e = cudaMemsetAsync(w.stats, 0, sizeof(unsigned long long) * 4, s);
-    if (e != cudaSuccess) return cuda_status(e, "memset");
+                 cudaStream_t s, bool clear_stats = true) {
+    cudaError_t e = cudaSuccess;
+    if (clear_stats && (e = cudaMemsetAsync(w.stats, 0, sizeof(unsigned long long) * 4, s)) != cudaSuccess)
+        return cuda_status(e, "memset");
     for (int t = 0; t < c->lloyd_iters; ++t) {
         // x is the same in every step: the first assign stores ||x||^2 per
         // token, the later ones read it
@@ -643,6 +644,152 @@ qvg_status coral_predict_encode_static(const qvg_config* cfg, const coral_predic
     if (scratch) clear_coral_error(cfg, n_tokens, scratch, a.workspace_bytes, (cudaStream_t)stream);
     return cuda_status(qvg::launch_coral(cfg->head_dim, cfg->group_size, true, a, (cudaStream_t)stream),
                        "coral launch");
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------ Coral-KV + SAS hybrid
+//
+// Workspace: [k-means fit workspace][cross-layer workspace][prediction, fp32
+// [N][H*D]][residual / decoded residual, bf16 [N][H*D]], each 256-byte aligned.
+
+namespace {
+
+struct SasLayout {
+    size_t fit, coral, pred, res, total;
+};
+
+SasLayout sas_layout(const qvg_config* cfg, int64_t n_tokens) {
+    SasLayout L;
+    const size_t N = (size_t)(n_tokens > 0 ? n_tokens : 1), HD = (size_t)cfg->num_heads * cfg->head_dim;
+    qvg_config cc = *cfg;
+    cc.num_clusters = 0;
+    L.fit = 0;
+    L.coral = align256(carve(cfg, n_tokens, nullptr).bytes);
+    L.pred = L.coral + align256(coral_ws_bytes(&cc, n_tokens));
+    L.res = L.pred + align256(N * HD * sizeof(float));
+    L.total = L.res + align256(N * HD * 2);
+    return L;
+}
+
+qvg_status sas_check(const qvg_config* cfg, const coral_predictor* pred, const qvg_bf16* xhat_prev,
+                     int64_t n_tokens, void* workspace, size_t workspace_bytes, SasLayout* L) {
+    qvg_status st = check_config(cfg, true);
+    if (st) return st;
+    if (cfg->bits != 2) return fail(QVG_ERR_UNSUPPORTED, "cross-layer codec uses 2-bit codes (got %d)", cfg->bits);
+    if (cfg->lloyd_iters < 1) return fail(QVG_ERR_INVALID_ARG, "lloyd_iters must be >= 1");
+    if (n_tokens < 1) return fail(QVG_ERR_INVALID_ARG, "the hybrid needs n_tokens >= 1");
+    *L = sas_layout(cfg, n_tokens);
+    if (!workspace) return fail(QVG_ERR_INVALID_ARG, "workspace is NULL (need %zu bytes)", L->total);
+    if (((uintptr_t)workspace & 255u) != 0) return fail(QVG_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    if (workspace_bytes < L->total)
+        return fail(QVG_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, L->total);
+    qvg_config cc = *cfg;
+    cc.num_clusters = 0;
+    return coral_common(&cc, pred, xhat_prev, n_tokens, static_cast<char*>(workspace) + L->coral, L->pred - L->coral);
+}
+
+// The fp32 prediction from x_hat_l (zero without it) into P: the cross-layer
+// kernels with no quantisation stage.  Their error word goes to the fit's.
+qvg_status sas_predict(const qvg_config* cfg, const coral_predictor* pred, const qvg_bf16* xhat_prev,
+                       int64_t n_tokens, const SasLayout& L, void* workspace, float* P, const FitWorkspace& w,
+                       cudaStream_t s) {
+    char* base = static_cast<char*>(workspace);
+    qvg::CoralArgs a{};
+    a.xprev = xhat_prev;
+    a.B = xhat_prev ? pred->B : nullptr; a.U = xhat_prev ? pred->U : nullptr; a.W = xhat_prev ? pred->W : nullptr;
+    a.R = xhat_prev ? pred->rank : 0;
+    a.n_tokens = n_tokens; a.H = cfg->num_heads; a.S = 0;
+    a.xhat = reinterpret_cast<qvg_bf16*>(base + L.res);     // scratch: overwritten by the residual
+    a.pred_out = P;
+    a.lowrank = reinterpret_cast<float*>(base + L.coral);
+    a.workspace = base + L.coral;
+    a.workspace_bytes = L.pred - L.coral;
+    a.err_out = reinterpret_cast<uint32_t*>(w.stats + 3);
+    return cuda_status(qvg::launch_coral(cfg->head_dim, cfg->group_size, false, a, s), "coral prediction launch");
+}
+
+qvg_status sas_decode_residual(const qvg_config* cfg, const uint32_t* codes, const uint32_t* meta, const uint8_t* ids,
+                               const qvg_bf16* centroids, int64_t n_tokens, qvg_bf16* out, cudaStream_t s) {
+    qvg::DecodeArgs d;
+    d.codes = codes; d.meta = meta; d.ids = ids; d.cent = centroids;
+    d.chunk_offset = nullptr; d.chunk_version = nullptr; d.n_chunks = 0;
+    d.cap = n_tokens; d.tok_begin = 0; d.tok_end = n_tokens;
+    d.out = out; d.out_head_stride = cfg->head_dim; d.out_token_stride = (int64_t)cfg->num_heads * cfg->head_dim;
+    d.H = cfg->num_heads; d.C = cfg->num_clusters; d.S = cfg->num_stages; d.bits = cfg->bits;
+    return cuda_status(qvg::launch_decode(cfg->head_dim, cfg->group_size, d, s), "decode launch");
+}
+
+}  // namespace
+
+extern "C" {
+
+qvg_status coral_sas_workspace_bytes(const qvg_config* cfg, int64_t n_tokens, size_t* bytes) {
+    qvg_status st = check_config(cfg, true);
+    if (st) return st;
+    if (!bytes || n_tokens < 0) return fail(QVG_ERR_INVALID_ARG, "bad arguments");
+    *bytes = sas_layout(cfg, n_tokens).total;
+    return ok();
+}
+
+qvg_status coral_sas_encode(const qvg_config* cfg, const coral_predictor* pred, const qvg_bf16* xhat_prev,
+                            const qvg_bf16* x_next, int64_t n_tokens, uint32_t* codes, uint32_t* meta, uint8_t* ids,
+                            qvg_bf16* centroids, qvg_bf16* xhat_next, float* pred_out, void* workspace,
+                            size_t workspace_bytes, qvg_stream stream) {
+    SasLayout L;
+    qvg_status st = sas_check(cfg, pred, xhat_prev, n_tokens, workspace, workspace_bytes, &L);
+    if (st) return st;
+    if (!x_next || !codes || !meta || !ids || !centroids || !xhat_next) return fail(QVG_ERR_INVALID_ARG, "buffer is NULL");
+    if (!aligned16(x_next) || !aligned16(codes) || !aligned16(meta) || !aligned16(centroids) || !aligned16(xhat_next) ||
+        !aligned16(pred_out))
+        return fail(QVG_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+    cudaStream_t s = (cudaStream_t)stream;
+    char* base = static_cast<char*>(workspace);
+    FitWorkspace w = carve(cfg, n_tokens, workspace);
+    float* P = pred_out ? pred_out : reinterpret_cast<float*>(base + L.pred);
+    qvg_bf16* R = reinterpret_cast<qvg_bf16*>(base + L.res);
+    const int64_t HD = (int64_t)cfg->num_heads * cfg->head_dim, count = n_tokens * HD;
+    cudaError_t e = cudaMemsetAsync(w.stats, 0, sizeof(unsigned long long) * 4, s);
+    if (e != cudaSuccess) return cuda_status(e, "memset");
+    if ((st = sas_predict(cfg, pred, xhat_prev, n_tokens, L, workspace, P, w, s))) return st;
+    // the residual r = bf16(x_{l+1} - pred), smoothed and quantised like a KV tensor
+    if ((e = qvg::launch_coral_residual(x_next, P, count, R, s)) != cudaSuccess) return cuda_status(e, "residual launch");
+    e = qvg::launch_kmeans_init(cfg->head_dim, R, cfg->head_dim, HD, n_tokens, nullptr, cfg->num_heads,
+                                cfg->num_clusters, centroids, s);
+    if (e != cudaSuccess) return cuda_status(e, "init launch");
+    if ((st = lloyd(cfg, R, n_tokens, cfg->head_dim, HD, centroids, ids, n_tokens, 0, w, s, false))) return st;
+    qvg::EncodeArgs a;
+    a.x = R; a.head_stride = cfg->head_dim; a.token_stride = HD; a.n_tokens = n_tokens;
+    a.cent = centroids; a.ids = ids;
+    a.codes = codes; a.meta = meta; a.cap = n_tokens; a.tok_offset = 0;
+    a.H = cfg->num_heads; a.C = cfg->num_clusters; a.S = cfg->num_stages; a.bits = cfg->bits;
+    if ((e = qvg::launch_encode(cfg->head_dim, cfg->group_size, a, s)) != cudaSuccess) return cuda_status(e, "encode launch");
+    // x_hat_{l+1} = bf16(pred + r_hat), exactly as the decoder forms it
+    if ((st = sas_decode_residual(cfg, codes, meta, ids, centroids, n_tokens, R, s))) return st;
+    return cuda_status(qvg::launch_coral_recon(P, R, count, xhat_next, s), "reconstruction launch");
+}
+
+qvg_status coral_sas_decode(const qvg_config* cfg, const coral_predictor* pred, const qvg_bf16* xhat_prev,
+                            int64_t n_tokens, const uint32_t* codes, const uint32_t* meta, const uint8_t* ids,
+                            const qvg_bf16* centroids, qvg_bf16* xhat_next, float* pred_out, void* workspace,
+                            size_t workspace_bytes, qvg_stream stream) {
+    SasLayout L;
+    qvg_status st = sas_check(cfg, pred, xhat_prev, n_tokens, workspace, workspace_bytes, &L);
+    if (st) return st;
+    if (!codes || !meta || !ids || !centroids || !xhat_next) return fail(QVG_ERR_INVALID_ARG, "buffer is NULL");
+    if (!aligned16(codes) || !aligned16(meta) || !aligned16(centroids) || !aligned16(xhat_next) || !aligned16(pred_out))
+        return fail(QVG_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+    cudaStream_t s = (cudaStream_t)stream;
+    char* base = static_cast<char*>(workspace);
+    FitWorkspace w = carve(cfg, n_tokens, workspace);
+    float* P = pred_out ? pred_out : reinterpret_cast<float*>(base + L.pred);
+    qvg_bf16* R = reinterpret_cast<qvg_bf16*>(base + L.res);
+    const int64_t count = n_tokens * (int64_t)cfg->num_heads * cfg->head_dim;
+    cudaError_t e = cudaMemsetAsync(w.stats, 0, sizeof(unsigned long long) * 4, s);
+    if (e != cudaSuccess) return cuda_status(e, "memset");
+    if ((st = sas_predict(cfg, pred, xhat_prev, n_tokens, L, workspace, P, w, s))) return st;
+    if ((st = sas_decode_residual(cfg, codes, meta, ids, centroids, n_tokens, R, s))) return st;
+    return cuda_status(qvg::launch_coral_recon(P, R, count, xhat_next, s), "reconstruction launch");
 }
 
 }  // extern "C"

@@ -278,7 +278,8 @@ cudaError_t coral_dg(bool encode, const CoralArgs& a, cudaStream_t s) {
         w.t2 = reinterpret_cast<uint16_t*>(base);
         w.wt = reinterpret_cast<uint16_t*>(base + a256(N * 64 * 2));
         w.ud = reinterpret_cast<uint16_t*>(base + a256(N * 64 * 2) + a256(32 * HD * 2));
-        w.err = reinterpret_cast<uint32_t*>(base + coral_tc_scratch_bytes(a.H, a.n_tokens) - 256);
+        w.err = a.err_out ? a.err_out
+                          : reinterpret_cast<uint32_t*>(base + coral_tc_scratch_bytes(a.H, a.n_tokens) - 256);
         bool launched = false;
         cudaError_t e = launch_coral_tc(D, G, encode, a, w, &launched, s);
         if (e != cudaSuccess || launched) return e;
@@ -305,7 +306,75 @@ cudaError_t coral_dg(bool encode, const CoralArgs& a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// Coral + SAS hybrid: the prediction residual rounded to bf16 (the input of
+// the k-means smoothing), and the reconstruction pred + r_hat rounded to bf16.
+// Eight elements a thread and step.
+__global__ void coral_residual_kernel(const uint16_t* __restrict__ xnext, const float* __restrict__ pred,
+                                      int64_t count, uint16_t* __restrict__ r) {
+    for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8; i < count;
+         i += (int64_t)gridDim.x * blockDim.x * 8) {
+        const uint4 xv = ldg_nc_v4(xnext + i);
+        const float4 p0 = *reinterpret_cast<const float4*>(pred + i), p1 = *reinterpret_cast<const float4*>(pred + i + 4);
+        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+        const float pp[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float lo = __fsub_rn(bf16_lo(xw[k]), pp[2 * k]), hi = __fsub_rn(bf16_hi(xw[k]), pp[2 * k + 1]);
+            o[k] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+                   ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+        }
+        *reinterpret_cast<uint4*>(r + i) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+__global__ void coral_recon_kernel(const float* __restrict__ pred, const uint16_t* __restrict__ rhat, int64_t count,
+                                   uint16_t* __restrict__ xhat) {
+    for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8; i < count;
+         i += (int64_t)gridDim.x * blockDim.x * 8) {
+        const uint4 rv = ldg_nc_v4(rhat + i);
+        const float4 p0 = *reinterpret_cast<const float4*>(pred + i), p1 = *reinterpret_cast<const float4*>(pred + i + 4);
+        const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+        const float pp[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float lo = __fadd_rn(pp[2 * k], bf16_lo(rw[k])), hi = __fadd_rn(pp[2 * k + 1], bf16_hi(rw[k]));
+            o[k] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+                   ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+        }
+        *reinterpret_cast<uint4*>(xhat + i) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+unsigned elementwise_grid(int64_t count) {
+    static int sms = 0;
+    if (!sms) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0) sms = 148;
+    }
+    const int64_t blocks = (count / 8 + kThreads - 1) / kThreads;
+    const int64_t cap = (int64_t)sms * 8;
+    return (unsigned)(blocks < 1 ? 1 : (blocks < cap ? blocks : cap));
+}
+
 }  // namespace
+
+cudaError_t launch_coral_residual(const uint16_t* xnext, const float* pred, int64_t count, uint16_t* r,
+                                  cudaStream_t s) {
+    if (count <= 0) return cudaSuccess;
+    coral_residual_kernel<<<elementwise_grid(count), kThreads, 0, s>>>(xnext, pred, count, r);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_coral_recon(const float* pred, const uint16_t* rhat, int64_t count, uint16_t* xhat,
+                               cudaStream_t s) {
+    if (count <= 0) return cudaSuccess;
+    coral_recon_kernel<<<elementwise_grid(count), kThreads, 0, s>>>(pred, rhat, count, xhat);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_coral(int D, int G, bool encode, const CoralArgs& a, cudaStream_t s) {
     switch (D * 1000 + G) {

@@ -88,6 +88,7 @@ struct CoralArgs {
     float* lowrank;          // workspace [N][R]
     void* workspace;         // the whole workspace (tensor-core path)
     size_t workspace_bytes;
+    uint32_t* err_out;       // error word of the tensor-core path, or nullptr: the one in its scratch
 };
 
 // Scratch of the tensor-core cross-layer path, carved from the workspace.
@@ -117,6 +118,12 @@ cudaError_t launch_update(int D, const UpdateArgs& a, cudaStream_t s);
 cudaError_t launch_set_chunk(int64_t* chunk_offset, int32_t* chunk_version, int idx, int64_t begin,
                              int64_t end, int32_t version, cudaStream_t s);
 cudaError_t launch_coral(int D, int G, bool encode, const CoralArgs& a, cudaStream_t s);
+// Coral + SAS hybrid, element-wise over count (a multiple of 8) elements:
+// r = bf16(x_next - pred) and x_hat = bf16(pred + r_hat), fp32 arithmetic.
+cudaError_t launch_coral_residual(const uint16_t* xnext, const float* pred, int64_t count, uint16_t* r,
+                                  cudaStream_t s);
+cudaError_t launch_coral_recon(const float* pred, const uint16_t* rhat, int64_t count, uint16_t* xhat,
+                               cudaStream_t s);
 // tcgen05 cross-layer path (D = 128, rank 32, G <= 64, a previous layer);
 // *launched = false (cudaSuccess) when outside that set.
 cudaError_t launch_coral_tc(int D, int G, bool encode, const CoralArgs& a, const CoralTcScratch& w, bool* launched,

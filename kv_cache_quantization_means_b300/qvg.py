@@ -19,6 +19,7 @@ EXPORTS = [
     "qvg_fit_centroids",
     "qvg_assign", "qvg_update", "qvg_encode", "qvg_decode", "qvg_append_chunk", "qvg_decode_cache",
     "coral_predict_encode", "coral_predict_decode", "coral_predict_encode_static", "coral_fit_block",
+    "coral_sas_workspace_bytes", "coral_sas_encode", "coral_sas_decode",
 ]
 
 
@@ -78,6 +79,9 @@ def load(path=LIB_PATH):
     L.coral_predict_encode_static.argtypes = [PCFG, ctypes.POINTER(coral_predictor), P, P, I64, P, P, P, P, P]
     L.coral_predict_decode.argtypes = [PCFG, ctypes.POINTER(coral_predictor), P, I64, P, P, P, P, P, SZ, P]
     L.coral_fit_block.argtypes = [PCFG, ctypes.POINTER(coral_predictor), P, P, I64, P, P, SZ, P]
+    L.coral_sas_workspace_bytes.argtypes = [PCFG, I64, PSZ]
+    L.coral_sas_encode.argtypes = [PCFG, ctypes.POINTER(coral_predictor), P, P, I64, P, P, P, P, P, P, P, SZ, P]
+    L.coral_sas_decode.argtypes = [PCFG, ctypes.POINTER(coral_predictor), P, I64, P, P, P, P, P, P, P, SZ, P]
     for name in EXPORTS[2:]:
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -209,6 +213,30 @@ def coral_predict_decode(cfg, pred, xhat_prev, n_tokens, codes, meta, xhat_next,
     _check(load().coral_predict_decode(ctypes.byref(cfg), ctypes.byref(pred) if pred is not None else None,
                                        _ptr(xhat_prev), n_tokens, _ptr(codes), _ptr(meta), _ptr(xhat_next),
                                        _ptr(pred_out), _ptr(workspace), _nbytes(workspace), _stream(stream)))
+
+
+def coral_sas_workspace_bytes(cfg, n_tokens):
+    b = ctypes.c_size_t(0)
+    _check(load().coral_sas_workspace_bytes(ctypes.byref(cfg), n_tokens, ctypes.byref(b)))
+    return b.value
+
+
+def coral_sas_encode(cfg, pred, xhat_prev, x_next, n_tokens, codes, meta, ids, centroids, xhat_next, workspace,
+                     pred_out=None, stream=None):
+    """Coral-KV + SAS hybrid, one layer: k-means smoothing and PRQ of the
+    bf16 prediction residual; xhat_next = bf16(pred + decoded residual)."""
+    _check(load().coral_sas_encode(ctypes.byref(cfg), ctypes.byref(pred) if pred is not None else None,
+                                   _ptr(xhat_prev), _ptr(x_next), n_tokens, _ptr(codes), _ptr(meta), _ptr(ids),
+                                   _ptr(centroids), _ptr(xhat_next), _ptr(pred_out), _ptr(workspace),
+                                   _nbytes(workspace), _stream(stream)))
+
+
+def coral_sas_decode(cfg, pred, xhat_prev, n_tokens, codes, meta, ids, centroids, xhat_next, workspace,
+                     pred_out=None, stream=None):
+    _check(load().coral_sas_decode(ctypes.byref(cfg), ctypes.byref(pred) if pred is not None else None,
+                                   _ptr(xhat_prev), n_tokens, _ptr(codes), _ptr(meta), _ptr(ids), _ptr(centroids),
+                                   _ptr(xhat_next), _ptr(pred_out), _ptr(workspace), _nbytes(workspace),
+                                   _stream(stream)))
 
 
 # -------------------------------------------------- allocation conveniences --

@@ -227,3 +227,52 @@ def coral_fit_block(xh, y, U, W, H, D):
 
 def bits_per_element(S, b, G, C, D, N, V=1):
     return lib().or_bits_per_element(S, b, G, C, D, N, V)
+
+
+# ------------------------------------------------------ Coral + SAS hybrid --
+
+def f32_to_bf16_bits(a):
+    """bf16 bit patterns of finite float32 values, round to nearest even:
+    add 0x7FFF plus the lowest kept bit, then drop the low 16 bits."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def bf16_bits_to_f32(b):
+    return (np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def coral_sas_layer(xh_prev, x_next, B, U, W, H, D, C, T, S, G, pred_in=None):
+    """Coral-KV prediction with the k-means smoothing of its residual, one
+    layer.  The pages do not describe the combination; this is the plain
+    reading the library implements:
+      pred  = the block-DPLR prediction of layer l+1 from x_hat_l: fp32, taken
+              from pred_in when given (the GPU's own, for staged checks), else
+              the fp64 prediction rounded to fp32; zero without x_hat_l;
+      r     = bf16(fp32(x_next - pred));
+      per head: centroids, ids = fit(r_h, C, T); codes, meta = prq_encode of
+              r_h - c[id]; r_hat_h = decode of them;
+      x_hat = bf16(fp32(pred + r_hat)).
+    Returns (centroids [H][C][D], ids [H][N], codes [S][H][N][D/16],
+    meta [S][H][N][D/G], x_hat [N][H*D], pred fp32 [N][H*D])."""
+    x_next = _c(x_next, np.uint16)
+    N = x_next.shape[0]
+    if pred_in is not None:
+        pred = _c(pred_in, np.float32)
+    elif xh_prev is None:
+        pred = np.zeros((N, H * D), np.float32)
+    else:
+        pred = coral_predict(xh_prev, B, U, W, H, D).astype(np.float32)
+    r = f32_to_bf16_bits(bf16_bits_to_f32(x_next) - pred)
+    cent = np.empty((H, C, D), np.uint16)
+    ids = np.empty((H, N), np.int32)
+    codes = np.empty((S, H, N, D // 16), np.uint32)
+    meta = np.empty((S, H, N, D // G), np.uint32)
+    rhat = np.empty((N, H * D), np.uint16)
+    for h in range(H):
+        rh = np.ascontiguousarray(r[:, h * D:(h + 1) * D])
+        cent[h], ids[h] = fit(rh, C, T)
+        codes[:, h], meta[:, h] = prq_encode(rh, cent[h], ids[h], S, G)
+        rhat[:, h * D:(h + 1) * D] = decode(codes[:, h], meta[:, h], ids[h], cent[h], G)
+    x_hat = f32_to_bf16_bits(pred + bf16_bits_to_f32(rhat))
+    return cent, ids, codes, meta, x_hat, pred

@@ -195,3 +195,59 @@ def test_coral_fit_block_zero_input(qvg):
     qvg.coral_fit_block(cfg, pred, zeros, y, N, Bout, ws)
     torch.cuda.synchronize()
     assert np.all(u16(Bout) == 0)
+
+
+def sas_gpu_layer(qvg, cfg, pred, xprev_dev, xnext_dev, N, ws, bufs=None):
+    """One layer of the Coral-KV + SAS hybrid through the C ABI: encode when
+    bufs is None (fresh poisoned outputs), else decode from bufs."""
+    H, D, S, G, C = cfg.num_heads, cfg.head_dim, cfg.num_stages, cfg.group_size, cfg.num_clusters
+    xh = torch.full((N, H * D), -1, dtype=torch.int16, device="cuda")
+    pout = torch.empty((N, H * D), dtype=torch.float32, device="cuda")
+    if bufs is None:
+        bufs = {"codes": torch.full((S * H * N * D // 16,), -1, dtype=torch.int32, device="cuda"),
+                "meta": torch.full((S * H * N * D // G,), -1, dtype=torch.int32, device="cuda"),
+                "ids": torch.full((H * N,), 255, dtype=torch.uint8, device="cuda"),
+                "cent": torch.full((H * C * D,), -1, dtype=torch.int16, device="cuda")}
+        qvg.coral_sas_encode(cfg, pred, xprev_dev, xnext_dev, N, bufs["codes"], bufs["meta"], bufs["ids"],
+                             bufs["cent"], xh, ws, pred_out=pout)
+    else:
+        qvg.coral_sas_decode(cfg, pred, xprev_dev, N, bufs["codes"], bufs["meta"], bufs["ids"], bufs["cent"], xh,
+                             ws, pred_out=pout)
+    torch.cuda.synchronize()
+    assert qvg.qvg_fit_stats(cfg, N, ws)[3] == 0      # no bounded wait expired
+    return bufs, xh, pout
+
+
+# rank 32 runs the tensor-core prediction (ragged last token tile), rank 16 the general one
+@pytest.mark.parametrize("N,R,H", [(300, 32, 4), (129, 16, 4)])
+def test_coral_sas_hybrid_staged_parity(qvg, oracle, N, R, H):
+    """Coral-KV + SAS hybrid over three closed-loop layers: given the GPU's
+    fp32 prediction, the residual's centroids, ids, codes, meta and the
+    reconstruction are bit-exact against the oracle, and the decoder rebuilds
+    the encoder's reconstruction exactly.  Layer 0 has no prediction."""
+    wl = WL.CORAL
+    D, S, G, C, T, L = wl.head_dim, wl.stages, wl.group_size, 16, 3, 3
+    small = WL.Workload(**{**wl.__dict__, "heads": H, "tokens": N, "layers": L, "rank": R})
+    xs = SY.coral_layers(small, SY.K_TENSOR, 0, N)
+    cfg = qvg.config(H, D, C, T, S, G)
+    ws = torch.empty(qvg.coral_sas_workspace_bytes(cfg, N), dtype=torch.uint8, device="cuda")
+    prev = pred = keep = B = U = W = None
+    for l in range(L):
+        if l > 0:
+            B, U, W = SY.coral_predictor(small, l - 1)
+            pred, keep = predictor(qvg, B, U, W)
+        bufs, xh, pout = sas_gpu_layer(qvg, cfg, pred, None if prev is None else to_dev(prev), to_dev(xs[l]), N, ws)
+        gp = pout.cpu().numpy()
+        if l == 0:
+            assert np.all(gp == 0)
+        oc, oi, ocodes, ometa, oxh, _ = oracle.coral_sas_layer(prev, xs[l], B, U, W, H, D, C, T, S, G, pred_in=gp)
+        np.testing.assert_array_equal(u16(bufs["cent"]).reshape(H, C, D), oc, err_msg=f"centroids layer {l}")
+        np.testing.assert_array_equal(bufs["ids"].cpu().numpy().reshape(H, N).astype(np.int32), oi,
+                                      err_msg=f"ids layer {l}")
+        np.testing.assert_array_equal(u32(bufs["codes"]).reshape(ocodes.shape), ocodes, err_msg=f"codes layer {l}")
+        np.testing.assert_array_equal(u32(bufs["meta"]).reshape(ometa.shape), ometa, err_msg=f"meta layer {l}")
+        np.testing.assert_array_equal(u16(xh), oxh, err_msg=f"reconstruction layer {l}")
+        _, dxh, dp = sas_gpu_layer(qvg, cfg, pred, None if prev is None else to_dev(prev), None, N, ws, bufs=bufs)
+        np.testing.assert_array_equal(u16(dxh), u16(xh))
+        np.testing.assert_array_equal(dp.cpu().numpy(), gp)
+        prev = u16(xh)

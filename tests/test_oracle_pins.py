@@ -590,3 +590,87 @@ def test_coral_fit_block_zero_input(oracle):
     xh = np.zeros_like(xh)
     B, Z = oracle.coral_fit_block(xh, y, U, W, H, D)
     assert np.all(B == 0) and np.all(Z == 0)
+
+
+# ------------------------------------------------ Coral-KV + SAS hybrid ---
+
+def test_f32_to_bf16_rounding_matches_exact_rationals(oracle):
+    """The hybrid's vectorised bf16 rounding is round-to-nearest-even: each
+    result is the nearest bf16 to the exact fp32 value (ties to an even
+    mantissa), checked against exact rationals on random values and on every
+    exact tie of one binade."""
+    rng = np.random.default_rng(5)
+    v = (rng.standard_normal(3000) * np.exp2(rng.integers(-20, 20, 3000))).astype(np.float32)
+    ties = (np.float32(1.0) + np.arange(128, dtype=np.float32) * np.float32(2.0 ** -7) + np.float32(2.0 ** -8))
+    v = np.concatenate([v, ties, -ties]).astype(np.float32)
+    got = oracle.f32_to_bf16_bits(v)
+    for x, b in zip(v, got):
+        fx = Fraction(float(x))
+        # the two bf16 neighbours of x, from truncation and one ulp further from zero
+        t = int(np.float32(x).view(np.uint32)) >> 16
+        lo, hi = bf16_fraction(t), bf16_fraction(t + 1)
+        dl, dh = abs(fx - lo), abs(hi - fx)
+        want = t if dl < dh else (t + 1 if dh < dl else (t if t % 2 == 0 else t + 1))
+        assert int(b) == want, (x, int(b), want)
+    assert np.array_equal(oracle.bf16_bits_to_f32(got[:10]).view(np.uint32) >> 16, got[:10].astype(np.uint32))
+
+
+def test_coral_sas_zero_prediction_is_plain_qvg(oracle):
+    """With no previous layer the prediction is 0, so the residual is x_next
+    itself (exact in bf16), and the hybrid must reduce to the plain SAS + PRQ
+    path of every head: same centroids, ids, codes, meta, and x_hat equal to
+    the plain decode (0 + r_hat is exact)."""
+    rng = np.random.default_rng(8)
+    H, D, N, C, T, S, G = 2, 128, 300, 8, 3, 2, 64
+    x = SY.f64_to_bf16_bits(rng.standard_normal((N, H * D)))
+    cent, ids, codes, meta, xh, pred = oracle.coral_sas_layer(None, x, None, None, None, H, D, C, T, S, G)
+    assert np.all(pred == 0)
+    for h in range(H):
+        xh_h = np.ascontiguousarray(x[:, h * D:(h + 1) * D])
+        oc, oi = oracle.fit(xh_h, C, T)
+        rc, rm = oracle.prq_encode(xh_h, oc, oi, S, G)
+        np.testing.assert_array_equal(cent[h], oc)
+        np.testing.assert_array_equal(ids[h], oi)
+        np.testing.assert_array_equal(codes[:, h], rc)
+        np.testing.assert_array_equal(meta[:, h], rm)
+        np.testing.assert_array_equal(xh[:, h * D:(h + 1) * D], oracle.decode(rc, rm, oi, oc, G))
+
+
+def test_coral_sas_perfect_prediction_reconstructs_exactly(oracle):
+    """A prediction equal to x_next leaves a zero residual: every group is
+    constant (scale 0), the decoded residual is 0, and x_hat = bf16(pred + 0)
+    = x_next exactly."""
+    rng = np.random.default_rng(9)
+    H, D, N, C, T, S, G = 2, 128, 200, 4, 2, 2, 64
+    x = SY.f64_to_bf16_bits(rng.standard_normal((N, H * D)))
+    pred = oracle.bf16_bits_to_f32(x)
+    cent, ids, codes, meta, xh, _ = oracle.coral_sas_layer(None, x, None, None, None, H, D, C, T, S, G, pred_in=pred)
+    np.testing.assert_array_equal(xh, x)
+    assert np.all(cent == 0)
+    assert np.all(meta & 0xFFFF == 0)                     # every stage scale is 0
+
+
+def test_coral_sas_residual_and_reconstruction_arithmetic(oracle):
+    """The residual is the fp32 difference rounded once to bf16, and the
+    reconstruction adds the decoded residual to the fp32 prediction: checked
+    element by element against exact rationals for a random prediction."""
+    rng = np.random.default_rng(10)
+    H, D, N, C, T, S, G = 1, 128, 64, 4, 2, 2, 64
+    x = SY.f64_to_bf16_bits(rng.standard_normal((N, H * D)))
+    pred = (rng.standard_normal((N, H * D)) * 0.5).astype(np.float32)
+    cent, ids, codes, meta, xh, _ = oracle.coral_sas_layer(None, x, None, None, None, H, D, C, T, S, G, pred_in=pred)
+    rhat = oracle.decode(codes[:, 0], meta[:, 0], ids[0], cent[0], G)
+    for n in range(0, N, 7):
+        for i in range(0, D, 11):
+            # reconstruction: RN_bf16(RN_f32(pred + r_hat)) from exact rationals
+            s = np.float32(Fraction(float(pred[n, i])) + bf16_fraction(rhat[n, i]))
+            t = int(np.float32(s).view(np.uint32)) >> 16
+            lo, hi = bf16_fraction(t), bf16_fraction(t + 1)
+            fs = Fraction(float(s))
+            want = t if abs(fs - lo) < abs(hi - fs) else (t + 1 if abs(hi - fs) < abs(fs - lo) else (t if t % 2 == 0 else t + 1))
+            assert int(xh[n, i]) == want
+    # the residual enters with its sign and scale: two 2-bit stages leave at
+    # most span/18 of a group's residual, so the reconstruction error is far
+    # below the prediction error (a flipped or rescaled residual is not)
+    xf, hf = oracle.bf16_bits_to_f32(x).astype(np.float64), oracle.bf16_bits_to_f32(xh).astype(np.float64)
+    assert np.max(np.abs(hf - xf)) <= 0.25 * np.max(np.abs(xf - pred)) + 2.0 ** -6
