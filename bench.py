@@ -208,10 +208,10 @@ class CoralStep:
     subtracted from layer l+1 and the residual PRQ-coded (encoder), and the
     chain is decoded back (decoder)."""
 
-    def __init__(self, Q, wl, layers, adapted=False):
+    def __init__(self, Q, wl, layers, adapted=False, sas=False, sas_clusters=256, sas_iters=4):
         import torch
         from synth import gpu as SG
-        self.Q, self.wl, self.L, self.adapted = Q, wl, layers, adapted
+        self.Q, self.wl, self.L, self.adapted, self.sas = Q, wl, layers, adapted, sas
         H, D, N, S, G = wl.heads, wl.head_dim, wl.tokens, wl.stages, wl.group_size
         self.cfg = Q.config(H, D, 0, 0, S, G)
         self.N, self.H, self.D, self.HD = N, H, D, H * D
@@ -243,6 +243,21 @@ class CoralStep:
         # per tensor and direction: layer 0 (one kernel), then prep + low-rank + predict per layer;
         # adapted: + prep + low-rank + Gram + reduce + solve per encoded layer
         self.launches_per_step = 2 * (1 + 3 * (layers - 1)) * 2 + (2 * 5 * (layers - 1) if adapted else 0)
+        if sas:
+            # Coral-KV + SAS hybrid: the residual of every layer is k-means smoothed (C, T) and PRQ-coded
+            C, T = sas_clusters, sas_iters
+            self.cfg_s = Q.config(H, D, C, T, S, G)
+            self.ws_s = [torch.empty(Q.coral_sas_workspace_bytes(self.cfg_s, N), dtype=torch.uint8, device="cuda")
+                         for _ in (0, 1)]
+            self.ids = [[torch.empty(H * N, dtype=torch.uint8, device="cuda") for _ in range(layers)] for _ in (0, 1)]
+            self.cents = [[torch.empty(H * C * D, dtype=torch.int16, device="cuda") for _ in range(layers)]
+                          for _ in (0, 1)]
+            # encode per layer: prediction (1 kernel at layer 0, else prep + low-rank + predict), residual,
+            # k-means init + T x (assign + hist + scatter + sum + mean), PRQ encode, decode, reconstruction;
+            # decode per layer: prediction, decode, reconstruction
+            enc = (1 + 5 + 5 * T) + (layers - 1) * (3 + 5 + 5 * T)
+            dec = (1 + 2) + (layers - 1) * (3 + 2)
+            self.launches_per_step = 2 * (enc + dec)
 
     def pred(self, t, l):
         return self.fit_preds[t][l - 1] if self.adapted else self.preds[l - 1]
@@ -250,6 +265,10 @@ class CoralStep:
     def encode(self, t, l):
         prev = None if l == 0 else self.xh[t][l - 1]
         pred = None if l == 0 else self.pred(t, l)
+        if self.sas:
+            self.Q.coral_sas_encode(self.cfg_s, pred, prev, self.x[t][l], self.N, self.codes[t][l], self.meta[t][l],
+                                    self.ids[t][l], self.cents[t][l], self.xh[t][l], self.ws_s[t])
+            return
         if self.adapted and l > 0:
             self.Q.coral_fit_block(self.cfg, pred, prev, self.x[t][l], self.N, self.fit_B[t][l - 1], self.ws[t])
         self.Q.coral_predict_encode(self.cfg, pred, prev, self.x[t][l], self.N, self.codes[t][l], self.meta[t][l],
@@ -258,6 +277,10 @@ class CoralStep:
     def decode(self, t, l):
         prev = None if l == 0 else self.dec[t][l - 1]
         pred = None if l == 0 else self.pred(t, l)
+        if self.sas:
+            self.Q.coral_sas_decode(self.cfg_s, pred, prev, self.N, self.codes[t][l], self.meta[t][l],
+                                    self.ids[t][l], self.cents[t][l], self.dec[t][l], self.ws_s[t])
+            return
         self.Q.coral_predict_decode(self.cfg, pred, prev, self.N, self.codes[t][l], self.meta[t][l],
                                     self.dec[t][l], None, self.ws[t])
 
@@ -269,15 +292,16 @@ class CoralStep:
         two chains only compete.)"""
         import torch
         cur = torch.cuda.current_stream()
-        if self.adapted:
+        two = self.adapted or self.sas
+        if two:
             self.side.wait_stream(cur)
         for t in (0, 1):
-            with torch.cuda.stream(self.side if (self.adapted and t == 1) else cur):
+            with torch.cuda.stream(self.side if (two and t == 1) else cur):
                 for l in range(self.L):
                     self.encode(t, l)
                 for l in range(self.L):
                     self.decode(t, l)
-        if self.adapted:
+        if two:
             cur.wait_stream(self.side)
 
 
@@ -483,7 +507,7 @@ def run_aux(args, Q, wl, peaks, world, rank, local):
     import torch
     hbm = peaks[0]
     if args.config == "coral":
-        st = CoralStep(Q, wl, wl.layers, adapted=args.adapted)
+        st = CoralStep(Q, wl, wl.layers, adapted=args.adapted, sas=args.sas)
     else:
         st = StreamStep(Q, wl, wl.layers)
     st.step()
@@ -493,12 +517,17 @@ def run_aux(args, Q, wl, peaks, world, rank, local):
         L, n = st.L, st.N * st.HD
         t_dec = graph_time(lambda: [st.decode(t, l) for t in (0, 1) for l in range(L)], 3) / (2 * L)
         dec_bytes = n * (2 + wl.stages * (2 / 8 + 4 / wl.group_size) + 2)   # read x_hat_l, codes+meta; write x_hat_l+1
-        dom = {"kernel": "coral decode (low-rank + predict/decode per layer)", "bound": "hbm",
+        if args.sas:
+            dec_bytes += n / wl.head_dim                                      # + the residual's cluster ids
+        dom = {"kernel": ("coral+sas decode (prediction + residual decode + reconstruction per layer)" if args.sas
+                          else "coral decode (low-rank + predict/decode per layer)"), "bound": "hbm",
                "achieved": dec_bytes / t_dec / 1e9, "peak": hbm, "unit": "GB/s", "time_us": t_dec * 1e6}
         cfgb = {"workload": f"{wl.name}: {wl.layers} layers x {wl.heads} heads x head_dim {wl.head_dim} x {wl.tokens} "
                             f"tokens, K and V, closed-loop block-DPLR (rank {wl.rank}) + PRQ S={wl.stages} G={wl.group_size}, "
                             "encode chain + decode chain" + ("; adapted: each layer's block predictors refit "
-                                                              "(least squares) before it is encoded" if args.adapted else "")}
+                                                              "(least squares) before it is encoded" if args.adapted else "")
+                            + ("; hybrid: each layer's bf16 prediction residual k-means smoothed (C=256 T=4) before "
+                               "its PRQ" if args.sas else "")}
     else:
         c = st.caches[-1][-1][0]
         lens = [st.chunk * (k + 1) for k in range(st.steps)]
@@ -538,11 +567,15 @@ def main():
                     help="QVG workloads: (layer, tensor) units run concurrently on this many streams")
     ap.add_argument("--adapted", action="store_true",
                     help="coral: refit each layer's block predictors for the current video before encoding it")
+    ap.add_argument("--sas", action="store_true",
+                    help="coral: Coral-KV + SAS hybrid, k-means smoothing of each layer's prediction residual")
     ap.add_argument("--bits", type=int, default=None, choices=[2, 4],
                     help="code width of the QVG workloads (default: the workload's, 2)")
     args = ap.parse_args()
     if args.bits is not None and args.config == "coral" and args.bits != 2:
         ap.error("the cross-layer codec uses 2-bit codes")
+    if args.sas and (args.config != "coral" or args.adapted):
+        ap.error("--sas is a mode of the coral workload (and not combined with --adapted)")
     if args.impl == "reference":
         return run_reference(args)
 
