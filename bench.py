@@ -125,6 +125,23 @@ class ClockSampler:
 
 # --------------------------------------------------------------- workload --
 
+def max_over_ranks(t, world, device):
+    """The slowest rank's step time: each rank times its own GPU's step, and
+    the job is done when the last one is."""
+    if world <= 1:
+        return t
+    import torch
+    import torch.distributed as dist
+    tt = torch.tensor([t], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_throughput(bytes_per_rank_step, world, t):
+    """Whole-job GB/s: every rank processes its own replica of the step."""
+    return bytes_per_rank_step * world / t / 1e9
+
+
 def workload(name, bits=None):
     import dataclasses
     from synth import workloads as WL
@@ -326,10 +343,10 @@ class StreamStep:
         self.ws = Q.alloc_workspace(self.cfg, self.chunk)
         self.out = torch.empty((N, H, D), dtype=torch.int16, device="cuda")
         per_tok = H * D * 2
-        # per (layer, tensor) and step: refit (init + T x 4 kernels) or assign, encode, chunk-table
+        # per (layer, tensor) and step: refit (init + T x 5 kernels) or assign, encode, chunk-table
         # update, then the history decode
         T = wl.lloyd_iters
-        self.launches_per_step = 2 * layers * sum((1 + 4 * T if k % self.every == 0 else 1) + 2 + 1
+        self.launches_per_step = 2 * layers * sum((1 + 5 * T if k % self.every == 0 else 1) + 2 + 1
                                                   for k in range(self.steps))
         self.enc_bytes = 2 * layers * N * per_tok
         self.dec_bytes = 2 * layers * per_tok * self.chunk * sum(range(1, self.steps + 1))
@@ -512,7 +529,12 @@ def run_aux(args, Q, wl, peaks, world, rank, local):
         st = StreamStep(Q, wl, wl.layers)
     st.step()
     torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
     t_step = graph_time(st.step, max(1, args.steps))
+    if world > 1:
+        dist.barrier()
     if args.config == "coral":
         L, n = st.L, st.N * st.HD
         t_dec = graph_time(lambda: [st.decode(t, l) for t in (0, 1) for l in range(L)], 3) / (2 * L)
@@ -543,7 +565,8 @@ def run_aux(args, Q, wl, peaks, world, rank, local):
     dom["frac"] = dom["achieved"] / dom["peak"]
     dom["traffic"] = None
     dom["peak_kind"] = peaks[3]
-    value = st.bytes_per_step * world / t_step / 1e9
+    t_step = max_over_ranks(t_step, world, "cuda")
+    value = job_throughput(st.bytes_per_step, world, t_step)
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": cfgb, "roofline": dom,
@@ -629,14 +652,10 @@ def main():
         b.record(s)
         torch.cuda.synchronize()
         barrier()
-    t = a.elapsed_time(b) / 1e3 / args.steps
-    if world > 1:
-        tt = torch.tensor([t], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t = tt.item()
-    value = st.bytes_per_step * world / t / 1e9
-    # per (layer, tensor): init + T x (assign, histogram, scatter, exact sum) + encode + decode
-    launches_per_step = 2 * layers * (1 + wl.lloyd_iters * 4 + 2)
+    t = max_over_ranks(a.elapsed_time(b) / 1e3 / args.steps, world, "cuda")
+    value = job_throughput(st.bytes_per_step, world, t)
+    # per (layer, tensor): init + T x (assign, histogram, scatter, exact sum, mean) + encode + decode
+    launches_per_step = 2 * layers * (1 + wl.lloyd_iters * 5 + 2)
 
     roof = kernel_rooflines(st, peaks)
 
@@ -680,7 +699,8 @@ def main():
             comp.wait_stream(up)
         e2e_step()
         te = time_fn(e2e_step, max(1, min(args.steps, 3)))
-        e2e = {"value": st.bytes_per_step * world / te / 1e9, "unit": "GB/s",
+        te = max_over_ranks(te, world, "cuda")
+        e2e = {"value": job_throughput(st.bytes_per_step, world, te), "unit": "GB/s",
                "h2d_bytes_per_step": st.bytes_per_step, "d2h_bytes_per_step": 2 * layers * st.compressed_bytes(),
                "pipelined": "upload / compute / read-back on three streams, per (layer, tensor)"}
 
