@@ -116,3 +116,45 @@ def test_pins_catch_planted_mistake(tmp_path, name):
         except Exception:          # an assertion (or a crash of the check) = caught
             caught.append(fn.__name__)
     assert caught, f"no pin caught the planted mistake '{name}'"
+
+
+# Mistakes planted in the oracle's Python side (the Coral + SAS hybrid
+# composition and its bf16 rounding), run against the same compiled oracle.
+PY_MUTATIONS = {
+    "hybrid residual sign": ("r = f32_to_bf16_bits(bf16_bits_to_f32(x_next) - pred)",
+                             "r = f32_to_bf16_bits(bf16_bits_to_f32(x_next) + pred)"),
+    "hybrid reconstruction drops the prediction": ("x_hat = f32_to_bf16_bits(pred + bf16_bits_to_f32(rhat))",
+                                                   "x_hat = rhat.copy()"),
+    "hybrid bf16 rounding truncates": ("return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)",
+                                       "return (u >> 16).astype(np.uint16)"),
+    "hybrid head slice": ("rh = np.ascontiguousarray(r[:, h * D:(h + 1) * D])",
+                          "rh = np.ascontiguousarray(r[:, 0:D])"),
+}
+
+PY_PIN_CALLS = [
+    (PINS.test_f32_to_bf16_rounding_matches_exact_rationals, {}),
+    (PINS.test_coral_sas_zero_prediction_is_plain_qvg, {}),
+    (PINS.test_coral_sas_perfect_prediction_reconstructs_exactly, {}),
+    (PINS.test_coral_sas_residual_and_reconstruction_arithmetic, {}),
+]
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTATIONS))
+def test_pins_catch_planted_python_mistake(tmp_path, name):
+    old, new = PY_MUTATIONS[name]
+    text = open(PY).read()
+    assert text.count(old) == 1, f"mutation anchor not unique/absent: {name}"
+    path = tmp_path / "oracle_mut.py"
+    path.write_text(text.replace(old, new))
+    spec = importlib.util.spec_from_file_location("oracle_py_mutant_" + str(abs(hash(name))), str(path))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod._SRC, mod._LIB, mod._lib = SRC, os.path.join(ROOT, "oracle", "liboracle.so"), None
+    mod.lib()
+    caught = []
+    for fn, kw in PY_PIN_CALLS:
+        try:
+            fn(mod, **kw)
+        except Exception:
+            caught.append(fn.__name__)
+    assert caught, f"no pin caught the planted mistake '{name}'"
