@@ -43,15 +43,29 @@ constexpr uint32_t kErrTimeout = 0x7E000000u;
 
 // ------------------------------------------------------------------ prep
 
-__global__ void coral_prep_kernel(const uint16_t* W, const uint16_t* U, int HD, uint16_t* Wt, uint16_t* Ud) {
-    const int j = blockIdx.x * blockDim.x + threadIdx.x;
-    if (j >= HD) return;
-#pragma unroll 4
-    for (int r = 0; r < kR; ++r) {
-        Wt[(int64_t)r * HD + j] = W[(int64_t)j * kR + r];
-        const uint16_t u = U[(int64_t)j * kR + r];
-        Ud[(int64_t)j * 2 * kR + r] = u;
-        Ud[(int64_t)j * 2 * kR + kR + r] = u;
+// W [H*D][32] -> Wt [32][H*D] and U [H*D][32] -> Ud [H*D][64] = [U | U].  A
+// CTA takes kPrepRows channel rows: W and U are read along their rows and Ud
+// written along its rows (coalesced); Wt, the transpose, goes out through a
+// shared tile so that its rows are written along too.
+constexpr int kPrepRows = 32;
+
+__global__ void __launch_bounds__(256) coral_prep_kernel(const uint16_t* W, const uint16_t* U, int HD, uint16_t* Wt,
+                                                         uint16_t* Ud) {
+    __shared__ uint16_t tile[kR][kPrepRows + 2];
+    const int j0 = blockIdx.x * kPrepRows, tid = threadIdx.x;
+    for (int e = tid; e < kPrepRows * kR; e += 256) {
+        const int jr = e / kR, r = e % kR, j = j0 + jr;
+        if (j < HD) {
+            tile[r][jr] = W[(int64_t)j * kR + r];
+            const uint16_t u = U[(int64_t)j * kR + r];
+            Ud[(int64_t)j * 2 * kR + r] = u;
+            Ud[(int64_t)j * 2 * kR + kR + r] = u;
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e < kR * kPrepRows; e += 256) {
+        const int r = e / kPrepRows, jr = e % kPrepRows, j = j0 + jr;
+        if (j < HD) Wt[(int64_t)r * HD + j] = tile[r][jr];
     }
 }
 
@@ -522,7 +536,7 @@ cudaError_t lowrank_stage(const CoralArgs& a, const CoralTcScratch& w, const CUt
                           cudaStream_t s) {
     const int HD = a.H * kDh;
     const int64_t N = a.n_tokens;
-    coral_prep_kernel<<<(unsigned)((HD + 127) / 128), 128, 0, s>>>(a.W, a.U, HD, w.wt, w.ud);
+    coral_prep_kernel<<<(unsigned)((HD + kPrepRows - 1) / kPrepRows), 256, 0, s>>>(a.W, a.U, HD, w.wt, w.ud);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int tiles = (int)((N + kT - 1) / kT);
