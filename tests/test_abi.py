@@ -158,3 +158,38 @@ def test_coral_argument_checks(Q):
                                   None) == 1         # workspace too small
     cq = Q.config(4, 128, 16, 1, 2, 64)
     assert L.coral_predict_encode(ctypes.byref(cq), *args[1:]) == 1   # clusters must be 0
+
+
+def test_coral_sas_argument_checks(Q):
+    """The Coral + SAS hybrid validates its configuration, buffers and
+    workspace on the host and launches nothing when they are wrong."""
+    L = Q.load()
+    sz = ctypes.c_size_t(0)
+    c0 = Q.config(4, 128, 0, 4, 2, 64)              # no clusters: the hybrid needs some
+    assert L.coral_sas_workspace_bytes(ctypes.byref(c0), 100, ctypes.byref(sz)) == 1
+    c = Q.config(4, 128, 16, 3, 2, 64)
+    assert L.coral_sas_workspace_bytes(ctypes.byref(c), 100, ctypes.byref(sz)) == 0
+    need = sz.value
+    assert need >= Q.qvg_workspace_bytes(c, 100) + 100 * 4 * 128 * (4 + 2)    # fit + prediction + residual
+    assert Q.coral_sas_workspace_bytes(c, 10000) > need                      # grows with the tokens
+    ws = 1 << 20                                                             # a 256-byte aligned address
+
+    def enc(cfg, n=100, wbytes=None, x_next=16, codes=16, ids=16, ws_ptr=ws):
+        return L.coral_sas_encode(ctypes.byref(cfg), None, None, x_next, n, codes, 16, ids, 16, 16, None, ws_ptr,
+                                  need if wbytes is None else wbytes, None)
+
+    assert enc(c0) == 1                                  # no clusters
+    c4 = Q.config(4, 128, 16, 3, 2, 64, 4)
+    assert enc(c4) == 2                                  # 2-bit codes only
+    cT = Q.config(4, 128, 16, 0, 2, 64)
+    assert enc(cT) == 1                                  # lloyd_iters must be >= 1
+    assert enc(c, n=0) == 1                              # needs tokens
+    assert enc(c, wbytes=need - 1) == 1                  # workspace too small
+    assert enc(c, ws_ptr=ws + 16) == 1                   # workspace not 256-byte aligned
+    assert enc(c, x_next=None) == 1                      # buffer missing
+    assert enc(c, ids=None) == 1
+    assert enc(c, codes=24) == 1                         # codes not 16-byte aligned
+    assert L.coral_sas_decode(ctypes.byref(c), None, None, 100, None, 16, 16, 16, 16, None, ws, need, None) == 1
+    assert "NULL" in L.qvg_last_error().decode() or "null" in L.qvg_last_error().decode().lower()
+    # a predicted layer needs a predictor
+    assert L.coral_sas_encode(ctypes.byref(c), None, 16, 16, 100, 16, 16, 16, 16, 16, None, ws, need, None) == 1
