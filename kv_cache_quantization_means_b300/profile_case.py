@@ -3,6 +3,7 @@
     python -m kv_cache_quantization_means_b300.profile_case unit [time]
     python -m kv_cache_quantization_means_b300.profile_case coral [time]
     python -m kv_cache_quantization_means_b300.profile_case coral_fit [time]
+    python -m kv_cache_quantization_means_b300.profile_case coral_sas [time]
 
 `unit` runs one (layer, tensor) of the Wan2.1-shaped cache (12 heads x 32760
 tokens x 128, C = 256, T = 4, S = 2, G = 64): a fit, then one more assign,
@@ -115,10 +116,38 @@ def coral_fit_case(timed):
         print(f"fit      {_graph_time_us(fit):9.1f} us")
 
 
+def coral_sas_case(timed):
+    """One layer of the Coral-KV + SAS hybrid (C = 256, T = 4 on the residual):
+    encode then decode, checking that both rebuild the same x_hat."""
+    wl = WL.CORAL
+    H, D, N, S, G = wl.heads, wl.head_dim, wl.tokens, wl.stages, wl.group_size
+    cfg = Q.config(H, D, 256, 4, S, G)
+    xs = SG.coral_chain_gpu(wl, 0, n_layers=2)
+    B, U, W = SG.coral_predictor_device(wl, 0)
+    pred = Q.coral_predictor(B=B.data_ptr(), U=U.data_ptr(), W=W.data_ptr(), rank=wl.rank)
+    codes = torch.empty(S * H * N * D // 16, dtype=torch.int32, device="cuda")
+    meta = torch.empty(S * H * N * D // G, dtype=torch.int32, device="cuda")
+    ids = torch.empty(H * N, dtype=torch.uint8, device="cuda")
+    cent = torch.empty(H * 256 * D, dtype=torch.int16, device="cuda")
+    xh = torch.empty((N, H * D), dtype=torch.int16, device="cuda")
+    dec = torch.empty((N, H * D), dtype=torch.int16, device="cuda")
+    ws = torch.empty(Q.coral_sas_workspace_bytes(cfg, N), dtype=torch.uint8, device="cuda")
+    enc = lambda: Q.coral_sas_encode(cfg, pred, xs[0], xs[1], N, codes, meta, ids, cent, xh, ws)
+    dcd = lambda: Q.coral_sas_decode(cfg, pred, xs[0], N, codes, meta, ids, cent, dec, ws)
+    enc()
+    dcd()
+    torch.cuda.synchronize()
+    assert torch.equal(xh, dec), "encoder and decoder reconstructions differ"
+    assert Q.qvg_fit_stats(cfg, N, ws)[3] == 0
+    if timed:
+        for name, f in (("encode", enc), ("decode", dcd)):
+            print(f"{name:8s} {_graph_time_us(f):9.1f} us")
+
+
 def main(argv):
     case = argv[1] if len(argv) > 1 else "unit"
     timed = len(argv) > 2 and argv[2] == "time"
-    {"unit": unit_case, "coral": coral_case, "coral_fit": coral_fit_case}[case](timed)
+    {"unit": unit_case, "coral": coral_case, "coral_fit": coral_fit_case, "coral_sas": coral_sas_case}[case](timed)
 
 
 if __name__ == "__main__":
