@@ -48,7 +48,7 @@ namespace qvg {
 namespace {
 
 constexpr int kTile = 128;                 // tokens per tile = UMMA M
-constexpr int kMaxStages = 3;              // token tiles in flight (2 when shared memory is short)
+constexpr int kMaxStages = 4;              // token tiles in flight (fewer when shared memory is short)
 constexpr int kEpiWarps = 16;              // two groups of eight (four pairs each)
 constexpr int kTcThreads = 64 + 32 * kEpiWarps;
 constexpr int kAtomBytes = kTile * 128;    // one 64-channel slab of a tile
@@ -85,8 +85,9 @@ struct Layout {
     uint32_t b_off, bx_off, ax_off, x_off, xch_off, bar_off, misc_off, total;
 };
 
-// Centroids (nA slabs of Cpad rows), the extra K block of the centroid side
-// (one slab of Cpad rows) and of the token side (one slab of 128 rows), the
+// Centroids (nA slabs of Cpad rows), the extra K = 16 block of the centroid
+// side (Cpad rows) and of the token side (128 rows) -- 32 bytes a row, as
+// unswizzled core matrices (kx_off) -- the
 // token stages, the epilogue pairs' exchange words ([pair][half][word][lane],
 // 8 words), then the barriers.
 __host__ __device__ inline Layout make_layout(int D, int Cpad, int stages) {
@@ -94,14 +95,21 @@ __host__ __device__ inline Layout make_layout(int D, int Cpad, int stages) {
     const int nA = D / 64;
     uint32_t o = 0;
     L.b_off = o;    o += (uint32_t)nA * Cpad * 128;
-    L.bx_off = o;   o += (uint32_t)Cpad * 128;
-    L.ax_off = o;   o += (uint32_t)kAtomBytes;
+    L.bx_off = o;   o += (uint32_t)Cpad * 32;
+    L.ax_off = o;   o += (uint32_t)kTile * 32;
     L.x_off = o;    o += (uint32_t)stages * nA * kAtomBytes;
     L.xch_off = o;  o += (uint32_t)(kEpiWarps / 2) * 2 * 8 * 32 * 4;
     L.bar_off = o;  o += (uint32_t)(2 * kMaxStages + 4) * 8;
     L.misc_off = o; o += 32;
     L.total = o + 1024;            // slack for 1024-byte alignment of the base
     return L;
+}
+
+// Byte offset of 16-byte chunk k (channels 8k..8k+7, k = 0, 1) of row r in
+// an extra K = 16 block: 8-row core matrices of 16-byte rows, the two chunks
+// of a group 128 bytes apart, groups 256 bytes apart.
+__device__ __forceinline__ uint32_t kx_off(int r, int k) {
+    return (uint32_t)(r >> 3) * 256u + (uint32_t)k * 128u + (uint32_t)(r & 7) * 16u;
 }
 
 template <int D>
@@ -324,11 +332,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
         }
         // the token side's extra block: 1 in channels 0..2, 0 elsewhere
-        for (int v = tid; v < kTile * 8; v += kTcThreads) {
-            const int r = v >> 3, k = v & 7;
+        for (int v = tid; v < kTile * 2; v += kTcThreads) {
+            const int r = v >> 1, k = v & 1;
             uint4 w = make_uint4(0, 0, 0, 0);
             if (k == 0) { w.x = 0x3F803F80u; w.y = 0x00003F80u; }
-            *reinterpret_cast<uint4*>(Ax + sw_off(r, k * 8, kAtomBytes)) = w;
+            *reinterpret_cast<uint4*>(Ax + kx_off(r, k)) = w;
         }
     }
     __syncthreads();
@@ -343,7 +351,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-        if (lane < 8) {
+        if (lane < 2) {
             uint4 w = make_uint4(0, 0, 0, 0);
             if (lane == 0) {
                 if (j < C) {
@@ -358,7 +366,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     w.x = 0xFB80u;                           // -2^120: never the largest score
                 }
             }
-            *reinterpret_cast<uint4*>(Bx + sw_off(j, lane * 8, cslab)) = w;
+            *reinterpret_cast<uint4*>(Bx + kx_off(j, lane)) = w;
             if (lane == 0 && j < C) atomicMax(misc + 2, __float_as_uint(sq));
         }
     }
@@ -398,7 +406,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
             const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(Cpad >> 3) << 17) |
                                    ((uint32_t)(kTile >> 4) << 24);
-            const uint64_t dax = sw128_desc(smem_u32(Ax)), dbx = sw128_desc(smem_u32(Bx));
+            const uint64_t dax = kmajor_plain_desc(smem_u32(Ax), 128u, 256u),
+                           dbx = kmajor_plain_desc(smem_u32(Bx), 128u, 256u);
             int issued = 0;
             for (int i = 0; i < n_tiles; ++i) {
                 const int st = i % NS, acc = i & 1;
@@ -668,7 +677,7 @@ cudaError_t assign_tc_d(int H, const AssignArgs& a, bool* launched, cudaStream_t
     // three token stages when they fit in shared memory, else two
     t.stages = kMaxStages;
     Layout L = make_layout(D, t.Cpad, t.stages);
-    if (L.total > 232448u) { t.stages = 2; L = make_layout(D, t.Cpad, t.stages); }
+    while (L.total > 232448u && t.stages > 2) L = make_layout(D, t.Cpad, --t.stages);
     if (L.total > 232448u) return cudaSuccess;
     // at least 116 KB so that one CTA (and one TMEM allocation) lives per SM
     const size_t smem = L.total < 118784u ? 118784u : L.total;

@@ -91,6 +91,17 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
     return d;
 }
 
+// K-major operand without swizzle: core matrices of 8 rows x 16 bytes, `lbo`
+// bytes apart along K and `sbo` bytes apart along M / N.
+__device__ __forceinline__ uint64_t kmajor_plain_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFFu);          // start address
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;     // leading byte offset: next core matrix along K
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;     // stride byte offset: next 8 rows
+    d |= (uint64_t)1u << 46;                         // descriptor version; layout type 0 = no swizzle
+    return d;
+}
+
 __device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t idesc, uint32_t acc) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
