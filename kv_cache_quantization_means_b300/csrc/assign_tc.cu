@@ -674,7 +674,7 @@ cudaError_t assign_tc_d(int H, const AssignArgs& a, bool* launched, cudaStream_t
     t.err = a.err;
     t.xnorm = a.xnorm;
     t.xnorm_mode = a.xnorm ? a.xnorm_mode : kNormCompute;
-    // three token stages when they fit in shared memory, else two
+    // as many token stages (up to four) as fit in shared memory, at least two
     t.stages = kMaxStages;
     Layout L = make_layout(D, t.Cpad, t.stages);
     while (L.total > 232448u && t.stages > 2) L = make_layout(D, t.Cpad, --t.stages);
