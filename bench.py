@@ -145,7 +145,7 @@ def job_throughput(bytes_per_rank_step, world, t):
 def workload(name, bits=None):
     import dataclasses
     from synth import workloads as WL
-    wl = WL.SHORT[name]
+    wl = WL.SHORT["wan" if name == "attn" else name]
     return wl if bits is None else dataclasses.replace(wl, bits=bits)
 
 
@@ -371,6 +371,110 @@ class StreamStep:
                     self.Q.qvg_decode_cache(self.cfg, c, 0, c.n_used, self.out, D, H * D)
 
 
+class AttnStep:
+    """Attention of one 3-frame chunk's queries over the compressed history,
+    Wan2.1 shape: per layer, 12 heads x 4680 queries x 32760 keys x 128, with
+    K and V of every layer fitted (C = 256, T = 4) and encoded (S = 2, G = 64)
+    by the library once, outside the timed region.  A step is one
+    qvg_attention_decode per layer: keys and values decoded tile by tile in
+    shared memory, never written out as bf16."""
+
+    def __init__(self, Q, wl, layers):
+        import numpy as np
+        import torch
+        from synth import gpu as SG
+        from synth import synth as SY
+        self.Q, self.wl, self.L = Q, wl, layers
+        H, D, N = wl.heads, wl.head_dim, wl.tokens
+        self.H, self.D, self.N, self.Nq = H, D, N, 3 * wl.frame_tokens
+        self.cfg = Q.config(H, D, wl.clusters, wl.lloyd_iters, wl.stages, wl.group_size, wl.bits)
+        ws = Q.alloc_workspace(self.cfg, N)
+        self.enc = []
+        for l in range(layers):
+            pair = []
+            for t in (SY.K_TENSOR, SY.V_TENSOR):
+                x = SG.mixture_layer_gpu(wl, l, t, layout="nhd")
+                e = Q.alloc_encoded(self.cfg, N)
+                Q.qvg_fit_centroids(self.cfg, x, N, D, H * D, None, e["centroids"], e["ids"], N, 0, ws)
+                Q.qvg_encode(self.cfg, x, N, D, H * D, e["centroids"], 0, e["codes"], e["meta"], e["ids"], N, 0, ws)
+                pair.append((e, Q.encoded_view(e)))
+            self.enc.append(pair)
+        torch.cuda.synchronize()
+        del ws
+        q = np.stack([SY.mixture_unit(wl, 0, SY.Q_TENSOR, h, 0, self.Nq) for h in range(H)], axis=1)
+        self.q = torch.from_numpy(np.ascontiguousarray(q).view(np.int16)).cuda()
+        self.out = torch.empty((self.Nq, H, D), dtype=torch.float32, device="cuda")
+        self.scale = float(np.float32(D ** -0.5))
+        self.launches_per_step = layers
+        self.kv_bytes = 2 * H * N * D * 2                   # bf16 K + V of one layer
+        self.bytes_per_step = layers * self.kv_bytes
+        self.flops_per_launch = 4.0 * H * self.Nq * N * D   # Q K^T and P V
+
+    def layer(self, l):
+        (_, kv), (_, vv) = self.enc[l]
+        self.Q.qvg_attention_decode(self.cfg, self.q, self.Nq, self.D, self.H * self.D, kv, vv, self.N, self.N,
+                                    self.scale, self.out, self.D, self.H * self.D)
+
+    def step(self):
+        for l in range(self.L):
+            self.layer(l)
+
+
+def attn_config_block(wl):
+    return {"workload": f"attention over the compressed {wl.name} cache: {wl.layers} layers x {wl.heads} heads, "
+                        f"{3 * wl.frame_tokens} queries (one 3-frame chunk) x {wl.tokens} keys x head_dim "
+                        f"{wl.head_dim}, K and V encoded with C={wl.clusters} T={wl.lloyd_iters} S={wl.stages} "
+                        f"b={wl.bits} G={wl.group_size}; value counts the bf16 K+V bytes attended per second"}
+
+
+def _oracle_attn_sample(args):
+    """One head of the attention workload on the CPU: the oracle decodes the
+    head's 32760 K and V rows and attends `nq` queries over them."""
+    seed, head, nq = args
+    import time as _t
+    from oracle import oracle as O
+    from synth import synth as SY
+    wl = workload("wan")
+    H, D, N, S, G, C = 1, wl.head_dim, wl.tokens, wl.stages, wl.group_size, wl.clusters
+    kc, km, ki, kx = SY.random_encoding(seed + head, SY.K_TENSOR, H, N, D, S, G, C)
+    vc, vm, vi, vx = SY.random_encoding(seed + head, SY.V_TENSOR, H, N, D, S, G, C)
+    q = SY.mixture_unit(wl, 0, SY.Q_TENSOR, head, 0, nq)
+    t0 = _t.perf_counter()
+    kd = O.decode(kc[:, 0], km[:, 0], ki[0].astype("int32"), kx[0], G)
+    vd = O.decode(vc[:, 0], vm[:, 0], vi[0].astype("int32"), vx[0], G)
+    O.attention(q, kd, vd, D ** -0.5)
+    return _t.perf_counter() - t0
+
+
+def cpu_baseline_attn(nq=512):
+    """The oracle on this host's cores: one head per process (decode of the
+    head's K and V, then attention of nq of the chunk's 4680 queries), all in
+    parallel; the bytes credited are the head's bf16 K + V times nq / 4680."""
+    import multiprocessing as mp
+    from oracle import oracle as O
+    O.build()
+    wl = workload("wan")
+    n = min(os.cpu_count() or 1, 8)
+    ctx = mp.get_context("spawn")
+    # one BLAS thread per worker, so that `cores` counts the threads used
+    saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    os.environ.update({k: "1" for k in saved})
+    try:
+        with ctx.Pool(n) as pool:
+            walls = pool.map(_oracle_attn_sample, [(wl.seed, h, nq) for h in range(n)])
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    wall = max(walls)
+    nbytes = n * 2 * wl.tokens * wl.head_dim * 2 * nq / (3 * wl.frame_tokens)
+    return {"value": nbytes / wall / 1e9, "unit": "GB/s", "cores": n, "kind": "oracle",
+            "sample": f"{n} heads, each: oracle decode of {wl.tokens} K and V rows + fp64 attention of {nq} of the "
+                      f"{3 * wl.frame_tokens} queries; one head per process, all concurrent; slowest {wall:.1f} s"}
+
+
 def time_fn(fn, reps, stream=None):
     import torch
     s = torch.cuda.current_stream() if stream is None else stream
@@ -489,10 +593,12 @@ def run_reference(args):
     wl = workload(name, args.bits)
     t0 = time.perf_counter()
     per_step = []
+    base = (lambda: cpu_baseline_attn(nq=128)) if name == "attn" else \
+        (lambda: cpu_baseline(name, max_units=2, bits=args.bits))
     for _ in range(args.warmup):
-        cpu_baseline(name, max_units=2, bits=args.bits)
+        base()
     for _ in range(args.steps):
-        per_step.append(cpu_baseline(name, max_units=2, bits=args.bits))
+        per_step.append(base())
     wall = time.perf_counter() - t0
     v = statistics.median(p["value"] for p in per_step)
     cb = dict(per_step[-1])
@@ -500,7 +606,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall / max(1, args.steps + args.warmup) * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64/f32",
-            "data": "synthetic", "config": config_block(wl, args),
+            "data": "synthetic", "config": attn_config_block(wl) if name == "attn" else config_block(wl, args),
             "cpu_baseline": cb, "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
@@ -525,6 +631,8 @@ def run_aux(args, Q, wl, peaks, world, rank, local):
     hbm = peaks[0]
     if args.config == "coral":
         st = CoralStep(Q, wl, wl.layers, adapted=args.adapted, sas=args.sas)
+    elif args.config == "attn":
+        st = AttnStep(Q, wl, wl.layers)
     else:
         st = StreamStep(Q, wl, wl.layers)
     st.step()
@@ -532,7 +640,8 @@ def run_aux(args, Q, wl, peaks, world, rank, local):
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
-    t_step = graph_time(st.step, max(1, args.steps))
+    with ClockSampler(local) as clk:
+        t_step = graph_time(st.step, max(1, args.steps))
     if world > 1:
         dist.barrier()
     if args.config == "coral":
@@ -550,6 +659,12 @@ def run_aux(args, Q, wl, peaks, world, rank, local):
                                                               "(least squares) before it is encoded" if args.adapted else "")
                             + ("; hybrid: each layer's bf16 prediction residual k-means smoothed (C=256 T=4) before "
                                "its PRQ" if args.sas else "")}
+    elif args.config == "attn":
+        t_att = graph_time(lambda: st.layer(0), 3)
+        dom = {"kernel": "attention_decode_kernel (K/V tiles decoded in shared memory, mma.sync bf16)",
+               "bound": "tensor", "achieved": st.flops_per_launch / t_att / 1e12, "peak": peaks[1],
+               "unit": "TFLOP/s", "time_us": t_att * 1e6}
+        cfgb = attn_config_block(wl)
     else:
         c = st.caches[-1][-1][0]
         lens = [st.chunk * (k + 1) for k in range(st.steps)]
@@ -570,7 +685,12 @@ def run_aux(args, Q, wl, peaks, world, rank, local):
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": cfgb, "roofline": dom,
-            "cpu_baseline": None, "e2e": None, "gpu_launches": st.launches_per_step * args.steps, "cuda_graph": True}
+            "cpu_baseline": None, "e2e": None, "gpu_launches": st.launches_per_step * args.steps, "cuda_graph": True,
+            "clocks": clk.summary()}
+    if args.config == "attn":
+        line["dtype"] = "bf16 x bf16 -> f32"
+        if rank == 0 and not args.no_cpu:
+            line["cpu_baseline"] = cpu_baseline_attn()
     if rank == 0:
         print(json.dumps(line))
     return 0
@@ -582,7 +702,7 @@ def main():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="wan", choices=["wan", "large", "coral", "stream"])
+    ap.add_argument("--config", default="wan", choices=["wan", "large", "coral", "stream", "attn"])
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -621,7 +741,7 @@ def main():
     Q.load()
     wl = workload(args.config, args.bits)
     peaks = load_peaks()
-    if args.config in ("coral", "stream"):
+    if args.config in ("coral", "stream", "attn"):
         return run_aux(args, Q, wl, peaks, world, rank, local)
     layers = wl.layers if args.config == "wan" else 2
     st = QvgStep(Q, wl, layers, streams=args.streams)

@@ -311,6 +311,40 @@ QVG_API qvg_status coral_sas_decode(const qvg_config* cfg, const coral_predictor
                                     const qvg_bf16* centroids, qvg_bf16* xhat_next, float* pred_out,
                                     void* workspace, size_t workspace_bytes, qvg_stream stream);
 
+/* One encoded (layer, tensor) as qvg_encode writes it (single centroid
+ * version); device pointers, caller-owned. */
+typedef struct {
+    const uint32_t* codes;       /* [S][H][capacity][D*b/32] */
+    const uint32_t* meta;        /* [S][H][capacity][D/G] */
+    const uint8_t* ids;          /* [H][capacity]; NULL when C == 0 */
+    const qvg_bf16* centroids;   /* [H][C][D]; NULL when C == 0 */
+} qvg_encoded_view;
+
+/* Attention over a compressed K/V history with the decode fused in (Quant
+ * VideoGen explainer, sec. 3: fused dequantisation kernels; the 33-method
+ * Self-Forcing KV-cache study, abstract: rebuilt BF16 K/V buffers around
+ * attention undo the memory saving).  No bf16 K or V buffer is written.
+ * For every head h and query i < n_queries (non-causal: every query sees
+ * keys 0 .. n_keys-1 of the head):
+ *   s_n = scale * <q_i, k_hat_n>,
+ *   out_i = sum_n exp(s_n) v_hat_n / sum_n exp(s_n),
+ * where k_hat and v_hat are, bit for bit, the bf16 rows that qvg_decode
+ * writes for rows 0 .. n_keys-1 of the encodings k and v (both with cfg's
+ * S, b, G, C).  Arithmetic: bf16 products of q and k_hat with fp32 sums,
+ * fp32 online softmax, probabilities rounded to bf16 for the product with
+ * v_hat, fp32 sums; out is fp32.
+ * q: bf16 at q + h*q_head_stride + i*q_token_stride (strides multiples of 8
+ * elements, 16-byte aligned).  out: fp32 at out + h*out_head_stride +
+ * i*out_token_stride (strides multiples of 4 elements, 16-byte aligned).
+ * Needs head_dim 64 or 128 (QVG_ERR_UNSUPPORTED otherwise), 1 <= n_keys <=
+ * capacity, a finite scale.  n_queries == 0 launches nothing.  Errors:
+ * invalid arguments return an error code and launch nothing; asynchronous. */
+QVG_API qvg_status qvg_attention_decode(const qvg_config* cfg, const qvg_bf16* q, int64_t n_queries,
+                                        int64_t q_head_stride, int64_t q_token_stride, const qvg_encoded_view* k,
+                                        const qvg_encoded_view* v, int64_t capacity, int64_t n_keys, float scale,
+                                        float* out, int64_t out_head_stride, int64_t out_token_stride,
+                                        qvg_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -5,6 +5,9 @@
 #include <cstring>
 #include <mutex>
 
+#include <cmath>
+
+#include "attn.h"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -790,6 +793,44 @@ qvg_status coral_sas_decode(const qvg_config* cfg, const coral_predictor* pred, 
     if ((st = sas_predict(cfg, pred, xhat_prev, n_tokens, L, workspace, P, w, s))) return st;
     if ((st = sas_decode_residual(cfg, codes, meta, ids, centroids, n_tokens, R, s))) return st;
     return cuda_status(qvg::launch_coral_recon(P, R, count, xhat_next, s), "reconstruction launch");
+}
+
+qvg_status qvg_attention_decode(const qvg_config* cfg, const qvg_bf16* q, int64_t n_queries, int64_t q_head_stride,
+                                int64_t q_token_stride, const qvg_encoded_view* k, const qvg_encoded_view* v,
+                                int64_t capacity, int64_t n_keys, float scale, float* out, int64_t out_head_stride,
+                                int64_t out_token_stride, qvg_stream stream) {
+    qvg_status st = check_config(cfg, false);
+    if (st) return st;
+    if (cfg->head_dim != 64 && cfg->head_dim != 128)
+        return fail(QVG_ERR_UNSUPPORTED, "fused attention supports head_dim 64 or 128 (got %d)", cfg->head_dim);
+    if (n_queries < 0) return fail(QVG_ERR_INVALID_ARG, "negative query count");
+    if (capacity < 0 || n_keys < 1 || n_keys > capacity)
+        return fail(QVG_ERR_INVALID_ARG, "n_keys %lld must be in 1..capacity (%lld)", (long long)n_keys,
+                    (long long)capacity);
+    if (!std::isfinite(scale)) return fail(QVG_ERR_INVALID_ARG, "scale must be finite");
+    if (!k || !v) return fail(QVG_ERR_INVALID_ARG, "k/v encoding is NULL");
+    const bool has_c = cfg->num_clusters > 0;
+    for (const qvg_encoded_view* e : {k, v}) {
+        if (!e->codes || !e->meta) return fail(QVG_ERR_INVALID_ARG, "codes/meta is NULL");
+        if (!aligned16(e->codes) || !aligned16(e->meta))
+            return fail(QVG_ERR_INVALID_ARG, "codes/meta must be 16-byte aligned");
+        if (has_c && (!e->ids || !e->centroids || !aligned16(e->centroids)))
+            return fail(QVG_ERR_INVALID_ARG, "ids/centroids missing or centroids not 16-byte aligned");
+    }
+    if (n_queries == 0) return ok();
+    if ((st = check_input(cfg, q, n_queries, q_head_stride, q_token_stride, "q"))) return st;
+    if (!out || !aligned16(out)) return fail(QVG_ERR_INVALID_ARG, "out must be non-NULL and 16-byte aligned");
+    if (out_head_stride % 4 || out_token_stride % 4 || out_head_stride < 0 || out_token_stride < 0)
+        return fail(QVG_ERR_INVALID_ARG, "out strides must be non-negative multiples of 4");
+    qvg::AttnArgs a;
+    a.q = q; a.q_head_stride = q_head_stride; a.q_token_stride = q_token_stride; a.n_queries = n_queries;
+    a.k_codes = k->codes; a.k_meta = k->meta; a.k_ids = k->ids; a.k_cent = k->centroids;
+    a.v_codes = v->codes; a.v_meta = v->meta; a.v_ids = v->ids; a.v_cent = v->centroids;
+    a.cap = capacity; a.n_keys = n_keys;
+    a.out = out; a.out_head_stride = out_head_stride; a.out_token_stride = out_token_stride;
+    a.H = cfg->num_heads; a.C = cfg->num_clusters; a.S = cfg->num_stages; a.G = cfg->group_size; a.bits = cfg->bits;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    return cuda_status(qvg::launch_attention_decode(cfg->head_dim, a, (cudaStream_t)stream), "attention launch");
 }
 
 }  // extern "C"

@@ -4,6 +4,7 @@
     python -m kv_cache_quantization_means_b300.profile_case coral [time]
     python -m kv_cache_quantization_means_b300.profile_case coral_fit [time]
     python -m kv_cache_quantization_means_b300.profile_case coral_sas [time]
+    python -m kv_cache_quantization_means_b300.profile_case attn [time]
 
 `unit` runs one (layer, tensor) of the Wan2.1-shaped cache (12 heads x 32760
 tokens x 128, C = 256, T = 4, S = 2, G = 64): a fit, then one more assign,
@@ -144,10 +145,43 @@ def coral_sas_case(timed):
             print(f"{name:8s} {_graph_time_us(f):9.1f} us")
 
 
+def attn_case(timed):
+    """One layer of attention over the compressed Wan2.1 cache: 12 heads, a
+    3-frame chunk of 4680 queries over 32760 keys (K and V fitted with C = 256,
+    T = 4 and encoded with S = 2, G = 64 by the library first)."""
+    import numpy as np
+    from synth import synth as SY
+    wl = WL.WAN
+    H, D, N, Nq = wl.heads, wl.head_dim, wl.tokens, 3 * wl.frame_tokens
+    cfg = Q.config(H, D, wl.clusters, wl.lloyd_iters, wl.stages, wl.group_size)
+    ws = Q.alloc_workspace(cfg, N)
+    views, keep = [], []
+    for t in (SY.K_TENSOR, SY.V_TENSOR):
+        x = SG.mixture_layer_gpu(wl, 0, t, layout="nhd")
+        e = Q.alloc_encoded(cfg, N)
+        Q.qvg_fit_centroids(cfg, x, N, D, H * D, None, e["centroids"], e["ids"], N, 0, ws)
+        Q.qvg_encode(cfg, x, N, D, H * D, e["centroids"], 0, e["codes"], e["meta"], e["ids"], N, 0, ws)
+        keep.append(e)
+        views.append(Q.encoded_view(e))
+    q = np.stack([SY.mixture_unit(wl, 0, SY.Q_TENSOR, h, 0, Nq) for h in range(H)], axis=1)
+    qd = torch.from_numpy(np.ascontiguousarray(q).view(np.int16)).cuda()
+    out = torch.empty((Nq, H, D), dtype=torch.float32, device="cuda")
+    scale = float(np.float32(D ** -0.5))
+    f = lambda: Q.qvg_attention_decode(cfg, qd, Nq, D, H * D, views[0], views[1], N, N, scale, out, D, H * D)
+    f()
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    if timed:
+        t = _graph_time(f, reps=5, inner=3)
+        print(f"attention {t:9.1f} us   {4.0 * H * Nq * N * D / t / 1e6:8.1f} TFLOP/s   "
+              f"{2 * H * N * D * 2 / t / 1e3:8.1f} GB/s of bf16 K+V attended")
+
+
 def main(argv):
     case = argv[1] if len(argv) > 1 else "unit"
     timed = len(argv) > 2 and argv[2] == "time"
-    {"unit": unit_case, "coral": coral_case, "coral_fit": coral_fit_case, "coral_sas": coral_sas_case}[case](timed)
+    {"unit": unit_case, "coral": coral_case, "coral_fit": coral_fit_case, "coral_sas": coral_sas_case,
+     "attn": attn_case}[case](timed)
 
 
 if __name__ == "__main__":

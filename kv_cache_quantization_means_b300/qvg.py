@@ -19,7 +19,7 @@ EXPORTS = [
     "qvg_fit_centroids",
     "qvg_assign", "qvg_update", "qvg_encode", "qvg_decode", "qvg_append_chunk", "qvg_decode_cache",
     "coral_predict_encode", "coral_predict_decode", "coral_predict_encode_static", "coral_fit_block",
-    "coral_sas_workspace_bytes", "coral_sas_encode", "coral_sas_decode",
+    "coral_sas_workspace_bytes", "coral_sas_encode", "coral_sas_decode", "qvg_attention_decode",
 ]
 
 
@@ -47,6 +47,11 @@ class qvg_cache(ctypes.Structure):
 class coral_predictor(ctypes.Structure):
     _fields_ = [("B", ctypes.c_void_p), ("U", ctypes.c_void_p), ("W", ctypes.c_void_p),
                 ("rank", ctypes.c_int32)]
+
+
+class qvg_encoded_view(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("meta", ctypes.c_void_p), ("ids", ctypes.c_void_p),
+                ("centroids", ctypes.c_void_p)]
 
 
 _lib = None
@@ -82,6 +87,8 @@ def load(path=LIB_PATH):
     L.coral_sas_workspace_bytes.argtypes = [PCFG, I64, PSZ]
     L.coral_sas_encode.argtypes = [PCFG, ctypes.POINTER(coral_predictor), P, P, I64, P, P, P, P, P, P, P, SZ, P]
     L.coral_sas_decode.argtypes = [PCFG, ctypes.POINTER(coral_predictor), P, I64, P, P, P, P, P, P, P, SZ, P]
+    L.qvg_attention_decode.argtypes = [PCFG, P, I64, I64, I64, ctypes.POINTER(qvg_encoded_view),
+                                       ctypes.POINTER(qvg_encoded_view), I64, I64, ctypes.c_float, P, I64, I64, P]
     for name in EXPORTS[2:]:
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -237,6 +244,21 @@ def coral_sas_decode(cfg, pred, xhat_prev, n_tokens, codes, meta, ids, centroids
                                    _ptr(xhat_prev), n_tokens, _ptr(codes), _ptr(meta), _ptr(ids), _ptr(centroids),
                                    _ptr(xhat_next), _ptr(pred_out), _ptr(workspace), _nbytes(workspace),
                                    _stream(stream)))
+
+
+def encoded_view(bufs):
+    """qvg_encoded_view of a dict with "codes", "meta" and optionally "ids" and
+    "centroids" device tensors (as alloc_encoded returns)."""
+    return qvg_encoded_view(codes=_ptr(bufs["codes"]), meta=_ptr(bufs["meta"]), ids=_ptr(bufs.get("ids")),
+                            centroids=_ptr(bufs.get("centroids")))
+
+
+def qvg_attention_decode(cfg, q, n_queries, q_head_stride, q_token_stride, k, v, capacity, n_keys, scale, out,
+                         out_head_stride, out_token_stride, stream=None):
+    """k, v: qvg_encoded_view structs (see encoded_view)."""
+    _check(load().qvg_attention_decode(ctypes.byref(cfg), _ptr(q), n_queries, q_head_stride, q_token_stride,
+                                       ctypes.byref(k), ctypes.byref(v), capacity, n_keys, float(scale), _ptr(out),
+                                       out_head_stride, out_token_stride, _stream(stream)))
 
 
 # -------------------------------------------------- allocation conveniences --

@@ -276,3 +276,25 @@ def coral_sas_layer(xh_prev, x_next, B, U, W, H, D, C, T, S, G, pred_in=None):
         rhat[:, h * D:(h + 1) * D] = decode(codes[:, h], meta[:, h], ids[h], cent[h], G)
     x_hat = f32_to_bf16_bits(pred + bf16_bits_to_f32(rhat))
     return cent, ids, codes, meta, x_hat, pred
+
+
+# ------------------------------------------- attention over the decoded cache --
+
+def attention(q, k_hat, v_hat, scale):
+    """Softmax attention of one head over decoded K/V rows, in fp64: the plain
+    definition of what a consumer of the cache computes (Quant VideoGen
+    explainer, sec. 3: dequantisation fused into the kernels that use the
+    cache; the 33-method Self-Forcing KV-cache study, abstract: attention over
+    the rebuilt BF16 keys and values).  Non-causal: every query sees every key.
+      s[i, n] = scale * <q_i, k_n>,
+      o_i     = sum_n exp(s[i, n]) v_n / sum_n exp(s[i, n]).
+    Subtracting each row's largest score before the exponential leaves o
+    unchanged and keeps exp from overflowing.
+    q [Nq][D], k_hat and v_hat [N][D] as bf16 bits (uint16), N >= 1; scale is
+    used as given (a float32 value converts exactly).  Returns fp64 [Nq][D]."""
+    Qf = bf16_bits_to_f32(q).astype(np.float64)
+    Kf = bf16_bits_to_f32(k_hat).astype(np.float64)
+    Vf = bf16_bits_to_f32(v_hat).astype(np.float64)
+    s = float(scale) * (Qf @ Kf.T)
+    p = np.exp(s - s.max(axis=1, keepdims=True))
+    return (p @ Vf) / p.sum(axis=1, keepdims=True)

@@ -37,6 +37,8 @@ P_CENTERS, P_ASSIGN, P_DRIFT, P_NOISE, P_OUTLIER = 1, 2, 3, 4, 5
 P_CORAL_B, P_CORAL_U, P_CORAL_W, P_CORAL_NOISE = 6, 7, 8, 9
 
 K_TENSOR, V_TENSOR = 0, 1
+Q_TENSOR = 2        # queries of an attention consumer, drawn like K and V (no outliers)
+P_ENC_CODES, P_ENC_META, P_ENC_IDS, P_ENC_CENT = 10, 11, 12, 13
 
 
 def mix64_int(z):
@@ -210,3 +212,36 @@ def coral_layers(wl, tensor, tok_begin=0, tok_end=None, n_layers=None):
         z = normals(kz, idx)
         out[l + 1] = f64_to_bf16_bits(blk + low + wl.next_noise_std * z)
     return out
+
+
+# ---------------------------------------------------------------------------
+# Arbitrary encoded caches: every bit pattern of this form is a legal
+# encoding, so these stand in for a compressed history without running any
+# encoder.  Inputs only.
+# ---------------------------------------------------------------------------
+
+def random_encoding(seed, tensor, H, cap, D, S, G, C, bits=2):
+    """Bit patterns of one encoded (layer, tensor) with ``cap`` rows per head:
+    codes uint32 [S][H][cap][D*bits/32], uniform words; meta uint32
+    [S][H][cap][D/G], low half an fp16 scale in [2^-6, 2^-5) (exponent field
+    9, uniform mantissa), high half an fp16 zero-point of magnitude in
+    [2^-4, 2^-3) (exponent field 11) with a uniform sign; ids uint8 [H][cap]
+    uniform in [0, C); centroids bf16 [H][C][D] from the approximate normals.
+    ids and centroids are None when C == 0."""
+    W = D * bits // 32
+    kc = stream_key(seed, tensor, P_ENC_CODES)
+    codes = (draws(kc, np.arange(S * H * cap * W, dtype=np.uint64)) & np.uint64(0xFFFFFFFF)).astype(np.uint32)
+    km = stream_key(seed, tensor, P_ENC_META)
+    d = draws(km, np.arange(S * H * cap * (D // G), dtype=np.uint64))
+    scale = np.uint64(0x2400) | (d & np.uint64(0x3FF))
+    zero = (((d >> np.uint64(10)) & np.uint64(1)) << np.uint64(15)) | np.uint64(0x2C00) | ((d >> np.uint64(11)) & np.uint64(0x3FF))
+    meta = (scale | (zero << np.uint64(16))).astype(np.uint32)
+    codes = codes.reshape(S, H, cap, W)
+    meta = meta.reshape(S, H, cap, D // G)
+    if C == 0:
+        return codes, meta, None, None
+    ki = stream_key(seed, tensor, P_ENC_IDS)
+    ids = (draws(ki, np.arange(H * cap, dtype=np.uint64)) % np.uint64(C)).astype(np.uint8).reshape(H, cap)
+    kx = stream_key(seed, tensor, P_ENC_CENT)
+    cent = f64_to_bf16_bits(normals(kx, np.arange(H * C * D, dtype=np.uint64))).reshape(H, C, D)
+    return codes, meta, ids, cent

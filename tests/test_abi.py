@@ -193,3 +193,46 @@ def test_coral_sas_argument_checks(Q):
     assert "NULL" in L.qvg_last_error().decode() or "null" in L.qvg_last_error().decode().lower()
     # a predicted layer needs a predictor
     assert L.coral_sas_encode(ctypes.byref(c), None, 16, 16, 100, 16, 16, 16, 16, 16, None, ws, need, None) == 1
+
+
+def test_attention_argument_checks(Q):
+    """The fused attention call validates shapes, buffers, strides and the
+    key range on the host; every case here fails validation (or is the empty
+    no-op) and launches nothing."""
+    L = Q.load()
+    V = Q.qvg.qvg_encoded_view
+    kv = V(codes=16, meta=16, ids=16, centroids=16)
+    c = Q.config(2, 128, 16, 1, 2, 64)
+
+    def call(cfg=c, q=16, nq=10, qhs=1280, qts=128, k=kv, v=kv, cap=100, nk=50, scale=0.088, out=16, ohs=1280,
+             ots=128):
+        kp = None if k is None else ctypes.byref(k)
+        vp = None if v is None else ctypes.byref(v)
+        return L.qvg_attention_decode(ctypes.byref(cfg), q, nq, qhs, qts, kp, vp, cap, nk, ctypes.c_float(scale),
+                                      out, ohs, ots, None)
+
+    assert call(cfg=Q.config(2, 256, 0, 1, 2, 64)) == 2            # head_dim 256 not supported
+    assert call(cfg=Q.config(2, 32, 0, 1, 2, 16)) == 2             # nor 32
+    assert call(nk=0) == 1                                         # needs a key
+    assert call(nk=101) == 1                                       # beyond capacity
+    assert b"n_keys" in L.qvg_last_error()
+    assert call(nq=-1) == 1
+    assert call(scale=float("inf")) == 1
+    assert call(scale=float("nan")) == 1
+    assert call(k=None) == 1
+    assert call(v=V(codes=None, meta=16, ids=16, centroids=16)) == 1
+    assert call(k=V(codes=16, meta=24, ids=16, centroids=16)) == 1  # meta not 16-byte aligned
+    assert call(k=V(codes=16, meta=16, ids=None, centroids=16)) == 1  # C > 0 needs ids
+    assert call(v=V(codes=16, meta=16, ids=16, centroids=None)) == 1
+    assert call(q=None) == 1
+    assert call(q=24) == 1                                         # q not 16-byte aligned
+    assert call(qts=132) == 1                                      # q stride not a multiple of 8
+    assert call(out=None) == 1
+    assert call(out=8) == 1                                        # out not 16-byte aligned
+    assert call(ots=130) == 1                                      # out stride not a multiple of 4
+    assert call(cfg=Q.config(2, 128, 16, 1, 2, 48)) == 2           # group size outside 16, 32, 64, 128
+    # no clusters: ids and centroids may be NULL; still fails on the key range
+    c0 = Q.config(2, 128, 0, 0, 2, 64)
+    assert call(cfg=c0, k=V(codes=16, meta=16, ids=None, centroids=None), nk=0) == 1
+    # no queries: nothing to do, and nothing launched
+    assert call(nq=0, q=None, out=None) == 0

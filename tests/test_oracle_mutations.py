@@ -129,6 +129,12 @@ PY_MUTATIONS = {
                                        "return (u >> 16).astype(np.uint16)"),
     "hybrid head slice": ("rh = np.ascontiguousarray(r[:, h * D:(h + 1) * D])",
                           "rh = np.ascontiguousarray(r[:, 0:D])"),
+    "attention drops the scale": ("s = float(scale) * (Qf @ Kf.T)", "s = Qf @ Kf.T"),
+    "attention weighs the keys": ("return (p @ Vf) / p.sum(axis=1, keepdims=True)",
+                                  "return (p @ Kf) / p.sum(axis=1, keepdims=True)"),
+    "attention max over queries": ("p = np.exp(s - s.max(axis=1, keepdims=True))",
+                                   "p = np.exp(s - s.max(axis=0, keepdims=True))"),
+    "attention unnormalised": ("return (p @ Vf) / p.sum(axis=1, keepdims=True)", "return p @ Vf"),
 }
 
 PY_PIN_CALLS = [
@@ -136,6 +142,9 @@ PY_PIN_CALLS = [
     (PINS.test_coral_sas_zero_prediction_is_plain_qvg, {}),
     (PINS.test_coral_sas_perfect_prediction_reconstructs_exactly, {}),
     (PINS.test_coral_sas_residual_and_reconstruction_arithmetic, {}),
+    (PINS.test_attention_matches_torch_sdpa_in_fp64, {}),
+    (PINS.test_attention_closed_forms, {}),
+    (PINS.test_attention_invariances, {}),
 ]
 
 

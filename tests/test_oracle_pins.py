@@ -674,3 +674,68 @@ def test_coral_sas_residual_and_reconstruction_arithmetic(oracle):
     # below the prediction error (a flipped or rescaled residual is not)
     xf, hf = oracle.bf16_bits_to_f32(x).astype(np.float64), oracle.bf16_bits_to_f32(xh).astype(np.float64)
     assert np.max(np.abs(hf - xf)) <= 0.25 * np.max(np.abs(xf - pred)) + 2.0 ** -6
+
+
+# ------------------------------------------- attention over the decoded cache --
+# Pins of oracle.attention (Quant VideoGen explainer, sec. 3: dequantisation
+# fused into the consumer; 33-method Self-Forcing KV-cache study, abstract:
+# attention over the rebuilt keys and values).
+
+def _bf16_rows(rng, n, d, scale=1.0):
+    return SY.f64_to_bf16_bits(scale * rng.standard_normal((n, d)))
+
+
+def test_attention_matches_torch_sdpa_in_fp64(oracle):
+    """Against torch's scaled-dot-product attention (a library routine) run in
+    fp64 on the CPU, with the scale passed explicitly."""
+    import torch
+    rng = np.random.default_rng(21)
+    for nq, n, d, scale in ((5, 7, 64, 0.125), (33, 300, 128, 128 ** -0.5), (1, 1, 64, 2.0)):
+        q, k, v = _bf16_rows(rng, nq, d), _bf16_rows(rng, n, d), _bf16_rows(rng, n, d)
+        o = oracle.attention(q, k, v, np.float32(scale))
+        t = [torch.from_numpy(SY.bf16_bits_to_f32(a).astype(np.float64))[None] for a in (q, k, v)]
+        ref = torch.nn.functional.scaled_dot_product_attention(*t, scale=float(np.float32(scale)))[0].numpy()
+        np.testing.assert_allclose(o, ref, rtol=0, atol=1e-12)
+
+
+def test_attention_closed_forms(oracle):
+    """q = 0 gives equal weights, so every output row is the mean of the
+    value rows; one key gives that key's value row exactly; two keys whose
+    scores differ by ln 3 weigh their values 1/4 and 3/4."""
+    rng = np.random.default_rng(22)
+    n, d = 40, 64
+    k, v = _bf16_rows(rng, n, d), _bf16_rows(rng, n, d)
+    vf = SY.bf16_bits_to_f32(v).astype(np.float64)
+    o = oracle.attention(np.zeros((3, d), np.uint16), k, v, 0.5)
+    np.testing.assert_allclose(o, np.broadcast_to(vf.mean(axis=0), o.shape), rtol=0, atol=1e-13)
+    o1 = oracle.attention(_bf16_rows(rng, 4, d), k[:1], v[:1], 0.3)
+    np.testing.assert_array_equal(o1, np.broadcast_to(vf[0], o1.shape))
+    # q = e_0, k_0 = 0, k_1 = e_0: scores 0 and `scale`, with scale = ln 3 in fp32
+    q = np.zeros((1, d), np.uint16); q[0, 0] = 0x3F80          # 1.0
+    k2 = np.zeros((2, d), np.uint16); k2[1, 0] = 0x3F80
+    sc = np.float32(np.log(3.0))
+    w1 = 3.0 * np.exp(float(sc) - np.log(3.0))                  # 3 up to the fp32 rounding of ln 3
+    expect = (vf[0] + w1 * vf[1]) / (1.0 + w1)
+    np.testing.assert_allclose(oracle.attention(q, k2, v[:2], sc)[0], expect, rtol=0, atol=1e-14)
+    assert abs(w1 - 3.0) < 1e-6
+
+
+def test_attention_invariances(oracle):
+    """Permuting the (key, value) rows together leaves the output unchanged;
+    adding the same vector to every value row adds it to every output row
+    (the weights sum to 1); a key whose score leads by 800 takes all weight."""
+    rng = np.random.default_rng(23)
+    nq, n, d = 6, 50, 64
+    q, k, v = _bf16_rows(rng, nq, d), _bf16_rows(rng, n, d), _bf16_rows(rng, n, d)
+    o = oracle.attention(q, k, v, 0.125)
+    perm = rng.permutation(n)
+    np.testing.assert_allclose(oracle.attention(q, k[perm], v[perm], 0.125), o, rtol=0, atol=1e-13)
+    # multiples of 1/8 below 2 stay exact in bf16 after adding 2.0
+    vs = SY.f64_to_bf16_bits(rng.integers(0, 16, (n, d)) / 8.0)
+    v2 = SY.f64_to_bf16_bits(SY.bf16_bits_to_f32(vs).astype(np.float64) + 2.0)
+    np.testing.assert_allclose(oracle.attention(q, k, v2, 0.125), oracle.attention(q, k, vs, 0.125) + 2.0,
+                               rtol=0, atol=1e-12)
+    qd = np.zeros((1, d), np.uint16); qd[0, 3] = 0x3F80
+    kd = np.zeros((n, d), np.uint16); kd[17, 3] = 0x4448         # 800.0
+    vf = SY.bf16_bits_to_f32(v).astype(np.float64)
+    np.testing.assert_allclose(oracle.attention(qd, kd, v, 1.0)[0], vf[17], rtol=0, atol=1e-300)
