@@ -172,7 +172,7 @@ def attn_case(timed):
     torch.cuda.synchronize()
     assert torch.isfinite(out).all()
     if timed:
-        t = _graph_time(f, reps=5, inner=3)
+        t = _graph_time_us(f, reps=5, inner=3)
         print(f"attention {t:9.1f} us   {4.0 * H * Nq * N * D / t / 1e6:8.1f} TFLOP/s   "
               f"{2 * H * N * D * 2 / t / 1e3:8.1f} GB/s of bf16 K+V attended")
 
