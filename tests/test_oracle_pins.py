@@ -5,7 +5,9 @@ exact (rational / integer) computation, a textbook special case, a hand-worked
 fixture under tests/golden/, or an invariant of the method.  Sources: Quant
 VideoGen explainer (Sommario tecnico sec. 2A SAS, sec. 2B PRQ, sec. 3 centroid
 caching, sec. 4 "up to 7x", baselines RTN/KIVI), Coral-KV news items
-("cross-layer prediction": block-diagonal per head plus global low rank).
+("cross-layer prediction": block-diagonal per head plus global low rank), and
+for the attention that consumes the cache the explainer's sec. 3 (fused
+dequantisation) with the 33-method Self-Forcing KV-cache study's abstract.
 """
 import os
 from fractions import Fraction
