@@ -15,7 +15,9 @@
 // One CTA = 64 queries of one head, four warps of 16 query rows.  Per key tile:
 //  1. all 128 threads decode 64 rows of K and of V, 16 channels per item,
 //     into padded shared memory (row stride D + 8 bf16: conflict-free
-//     ldmatrix);
+//     ldmatrix); with at most two code and meta words per item, the raw
+//     words of the next tile are loaded into registers while this tile's
+//     products run, and decoded after them;
 //  2. each warp computes S = Q K^T (16 x 64) with bf16 mma.sync m16n8k16,
 //     fp32 accumulation, Q held in registers for the whole kernel;
 //  3. online softmax in fp32 with base-2 exponentials (scale * log2 e folded
@@ -96,11 +98,18 @@ __device__ __forceinline__ void decode_chunk(const uint32_t* codes, const uint32
     pack16_bf16(acc, o0, o1);
 }
 
-template <int D, int B>
+// PF: the next key tile's ids, code words and meta words are loaded into
+// registers before the current tile's products, so that their latency is
+// spent under the tensor work (needs S * B / 2 <= 2 code words and S <= 2
+// meta words per item); otherwise each tile is loaded and decoded in turn.
+template <int D, int B, bool PF>
 __global__ void __launch_bounds__(kAttnThreads) attention_decode_kernel(AttnArgs a) {
     constexpr int LD = D + 8;             // bf16 row stride in shared memory
     constexpr int CPR = D / 16;           // 16-channel items per row
     constexpr int ITEMS = 2 * kKTile * CPR;
+    constexpr int IPT = ITEMS / kAttnThreads;
+    constexpr int WPT = B / 2;            // code words per item and stage
+    constexpr int WPR = D * B / 32;       // code words per row and stage
     static_assert(ITEMS % kAttnThreads == 0, "whole items per thread");
     __shared__ __align__(16) uint16_t ks[kKTile * LD];
     __shared__ __align__(16) uint16_t vs[kKTile * LD];
@@ -134,16 +143,88 @@ __global__ void __launch_bounds__(kAttnThreads) attention_decode_kernel(AttnArgs
     const int brow = (lane & 7) + ((lane >> 4) << 3), bk = ((lane >> 3) & 1) * 8;
     const int64_t stage_rows = (int64_t)a.H * a.cap;
 
-    for (int64_t n0 = 0; n0 < a.n_keys; n0 += kKTile) {
-        // 1. decode 64 rows of K (items 0 .. ITEMS/2-1) and V (the rest)
+    // item k of this thread: v = tid + k * kAttnThreads; K for v < ITEMS / 2, V after
+    uint32_t pid[IPT], pcode[IPT][2], pmeta[IPT][2];
+    uint32_t pvalid = 0;
+    const int mpr = D / a.G;
+
+    // raw words of the tile starting at n (PF)
+    auto prefetch = [&](int64_t n) {
+        pvalid = 0;
+#pragma unroll
+        for (int k = 0; k < IPT; ++k) {
+            const int v = tid + k * kAttnThreads;
+            const bool is_v = v >= ITEMS / 2;
+            const int rem = is_v ? v - ITEMS / 2 : v;
+            const int r = rem / CPR, c = rem % CPR;
+            pid[k] = 0;
+            pcode[k][0] = pcode[k][1] = 0;
+            pmeta[k][0] = pmeta[k][1] = 0;
+            if (n + r < a.n_keys) {
+                pvalid |= 1u << k;
+                const int64_t row = (int64_t)h * a.cap + n + r;
+                const uint32_t* codes = is_v ? a.v_codes : a.k_codes;
+                const uint32_t* meta = is_v ? a.v_meta : a.k_meta;
+                if (a.C > 0) pid[k] = (is_v ? a.v_ids : a.k_ids)[row];
+#pragma unroll
+                for (int s2 = 0; s2 < 2; ++s2) {
+                    if (s2 >= a.S) continue;
+                    const int64_t srow = (int64_t)s2 * stage_rows + row;
+                    if constexpr (B == 2) pcode[k][s2] = __ldg(codes + srow * WPR + c * WPT);
+                    else if (s2 == 0) {
+                        pcode[k][0] = __ldg(codes + srow * WPR + c * WPT);
+                        pcode[k][1] = __ldg(codes + srow * WPR + c * WPT + 1);
+                    }
+                    pmeta[k][s2] = __ldg(meta + srow * mpr + (c * 16) / a.G);
+                }
+            }
+        }
+    };
+    // centroid rows, dequantisation and the stores to shared memory (PF)
+    auto finish = [&]() {
+#pragma unroll
+        for (int k = 0; k < IPT; ++k) {
+            const int v = tid + k * kAttnThreads;
+            const bool is_v = v >= ITEMS / 2;
+            const int rem = is_v ? v - ITEMS / 2 : v;
+            const int r = rem / CPR, c = rem % CPR;
+            uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
+            if (pvalid & (1u << k)) {
+                float acc[16];
+                if (a.C > 0) {
+                    const uint16_t* cr = (is_v ? a.v_cent : a.k_cent) +
+                                         ((int64_t)h * a.C + min((int)pid[k], a.C - 1)) * D + c * 16;
+                    unpack16(__ldg(reinterpret_cast<const uint4*>(cr)), __ldg(reinterpret_cast<const uint4*>(cr + 8)),
+                             acc);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+                }
+                if constexpr (B == 2) {
+#pragma unroll
+                    for (int s2 = 0; s2 < 2; ++s2)
+                        if (s2 < a.S) dequant_add16(acc, pcode[k][s2], pmeta[k][s2]);
+                } else {
+                    dequant_add8x4(acc, pcode[k][0], pmeta[k][0]);
+                    dequant_add8x4(acc + 8, pcode[k][1], pmeta[k][0]);
+                }
+                pack16_bf16(acc, o0, o1);
+            }
+            uint16_t* dst = (is_v ? vs : ks) + r * LD + c * 16;
+            *reinterpret_cast<uint4*>(dst) = o0;
+            *reinterpret_cast<uint4*>(dst + 8) = o1;
+        }
+    };
+    // load and decode the tile starting at n in one pass (not PF)
+    auto decode_tile = [&](int64_t n) {
 #pragma unroll 2
         for (int v = tid; v < ITEMS; v += kAttnThreads) {
             const bool is_v = v >= ITEMS / 2;
             const int rem = is_v ? v - ITEMS / 2 : v;
             const int r = rem / CPR, c = rem % CPR;
             uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
-            if (n0 + r < a.n_keys) {
-                const int64_t row = (int64_t)h * a.cap + n0 + r;
+            if (n + r < a.n_keys) {
+                const int64_t row = (int64_t)h * a.cap + n + r;
                 if (is_v)
                     decode_chunk<D, B>(a.v_codes, a.v_meta, a.v_ids, a.v_cent, row, h, c, stage_rows, a.C, a.S, a.G,
                                        o0, o1);
@@ -155,7 +236,22 @@ __global__ void __launch_bounds__(kAttnThreads) attention_decode_kernel(AttnArgs
             *reinterpret_cast<uint4*>(dst) = o0;
             *reinterpret_cast<uint4*>(dst + 8) = o1;
         }
-        __syncthreads();
+    };
+
+    // 1. the first tile of K (items 0 .. ITEMS/2-1) and V (the rest)
+    if constexpr (PF) {
+        prefetch(0);
+        finish();
+    } else {
+        decode_tile(0);
+    }
+    __syncthreads();
+
+    for (int64_t n0 = 0; n0 < a.n_keys; n0 += kKTile) {
+        const int64_t next = n0 + kKTile;
+        if constexpr (PF) {
+            if (next < a.n_keys) prefetch(next);   // in flight during the products below
+        }
 
         // 2. S = Q K^T: n-tile j holds keys n0 + 8j .. n0 + 8j + 7
         float sc[kKTile / 8][4];
@@ -228,6 +324,11 @@ __global__ void __launch_bounds__(kAttnThreads) attention_decode_kernel(AttnArgs
             }
         }
         __syncthreads();   // the next tile's decode overwrites ks / vs
+        if (next < a.n_keys) {
+            if constexpr (PF) finish();
+            else decode_tile(next);
+            __syncthreads();
+        }
     }
 
     // O / l, rows g and g + 8 of the warp
@@ -252,8 +353,10 @@ __global__ void __launch_bounds__(kAttnThreads) attention_decode_kernel(AttnArgs
 template <int D>
 cudaError_t launch_d(const AttnArgs& a, cudaStream_t s) {
     dim3 grid((unsigned)((a.n_queries + kQTile - 1) / kQTile), (unsigned)a.H);
-    if (a.bits == 2) attention_decode_kernel<D, 2><<<grid, kAttnThreads, 0, s>>>(a);
-    else if (a.bits == 4) attention_decode_kernel<D, 4><<<grid, kAttnThreads, 0, s>>>(a);
+    if (a.bits == 2 && a.S <= 2) attention_decode_kernel<D, 2, true><<<grid, kAttnThreads, 0, s>>>(a);
+    else if (a.bits == 2) attention_decode_kernel<D, 2, false><<<grid, kAttnThreads, 0, s>>>(a);
+    else if (a.bits == 4 && a.S == 1) attention_decode_kernel<D, 4, true><<<grid, kAttnThreads, 0, s>>>(a);
+    else if (a.bits == 4) attention_decode_kernel<D, 4, false><<<grid, kAttnThreads, 0, s>>>(a);
     else return cudaErrorInvalidValue;
     return cudaGetLastError();
 }
