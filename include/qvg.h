@@ -180,7 +180,8 @@ QVG_API qvg_status qvg_update(const qvg_config* cfg, const qvg_bf16* x, int64_t 
 /* QVG encode (sec. 2A item 3 and sec. 2B items 1-2): per token row,
  * r = x - c[id] in fp32 (r = x when C = 0), then for each stage and group of G
  * channels s = fp16((max r - min r)/3), z = fp16(min r),
- * q = clamp(rint((r - z) * fp32(1/s)), 0, 3) (0 when s = 0), r <- r - (q*s + z).
+ * q = clamp(rint((r - z) / s), 0, 3) with IEEE single-precision division (0 when
+ * s = 0), r <- r - (q*s + z).
  * Rows go to rows tok_offset .. tok_offset+n_tokens-1 of codes/meta/ids.
  * assign = 0: ids are read from `ids` (e.g. written by qvg_fit_centroids);
  * assign = 1: ids are first computed against `centroids` and written there. */

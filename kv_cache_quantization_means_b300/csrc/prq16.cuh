@@ -5,17 +5,29 @@
 //
 // Arithmetic per element and stage (identical, operation for operation, to
 // the plain statement of the quantiser):
-//   t = (r - z) * inv            two IEEE single operations
-//   q = clamp(rint(t), 0, 3)     computed as rint(clamp(t, 0, 3)), which is
-//                                the same integer because 0 and 3 are
-//                                integers; rint by adding and subtracting
-//                                1.5 * 2^23, whose IEEE sum rounds to an
-//                                integer with ties to even
+//   t = r - z                    one IEEE single subtraction
+//   y = t / s                    IEEE single division, correctly rounded
+//   q = clamp(rint(y), 0, L)     rint by adding and subtracting 1.5 * 2^23,
+//                                whose IEEE sum rounds to an integer with
+//                                ties to even
 //   d = fma(q, s, z)             q*s is exact, so this is q*s + z rounded once
 //   r = r - d
+// The division: with inv = RN(1/s), q0 = RN(t * inv) is within one ulp of
+// t/s, the remainder t - q0*s is exact in one fma, and RN(q0 + rem * inv) is
+// the correctly rounded quotient (Markstein's correction step: P. Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Develop. 34(1), 1990).  That holds while nothing
+// overflows or underflows near a rounding boundary.  A group whose extreme
+// quotients (min r - z)/s and (max r - z)/s lie in [-1/2, L + 1/2) has every
+// rint(y) in [0, L] already (rounding is monotone), so it needs neither the
+// clamp nor any other range care; any other group -- in practice one whose
+// zero-point rounded far from its minimum, or non-finite values -- takes
+// __fdiv_rn and the clamp.
 // Every 16 2-bit codes go to one 32-bit word, element k at bits 2k, 2k+1;
 // with 4-bit codes (levels 0..15, s = range / 15) every 8 codes go to one
-// word, element k at bits 4k .. 4k+3.
+// word, element k at bits 4k .. 4k+3.  The words are assembled in fp32: each
+// half-word is sum q_k * 2^(b k) accumulated exactly onto 2^23 by fmas, whose
+// low 16 bits are then spliced together.
 #pragma once
 
 #include "common.cuh"
@@ -53,27 +65,35 @@ __device__ __forceinline__ void sub16(float* r, const float* c) {
     }
 }
 
-// Packs the low bytes of vb[0..15] (each a code q_k < 4) into one word,
-// element k at bits 2k: bytes {q_j, q_j+4, q_j+8, q_j+12} are gathered into
-// W_j, then the four words are interleaved two bits apart.
-__device__ __forceinline__ uint32_t pack_codes16(const uint32_t* vb) {
-    uint32_t w[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const uint32_t lo = prmt(vb[j], vb[j + 4], 0x0040u);
-        const uint32_t hi = prmt(vb[j + 8], vb[j + 12], 0x0040u);
-        w[j] = prmt(lo, hi, 0x5410u);
-    }
-    return w[0] | (w[1] << 2) | (w[2] << 4) | (w[3] << 6);
+// Correctly rounded t / s from inv = RN(1/s) and ns = -s, two lanes at a
+// time (Markstein's correction step, see the top of this file).
+__device__ __forceinline__ float2 div2_rn(float2 t, float2 inv, float2 ns) {
+    const float2 q0 = f2_mul(t, inv);
+    const float2 rem = f2_fma(q0, ns, t);
+    return f2_fma(rem, inv, q0);
 }
 
-// Packs the low bytes of vb[0..7] (each a code q_k < 16) into one word,
-// element k at bits 4k: bytes {q0, q2, q4, q6} and {q1, q3, q5, q7} are
-// gathered, then interleaved four bits apart.
-__device__ __forceinline__ uint32_t pack_codes8x4(const uint32_t* vb) {
-    const uint32_t e = prmt(prmt(vb[0], vb[2], 0x0040u), prmt(vb[4], vb[6], 0x0040u), 0x5410u);
-    const uint32_t o = prmt(prmt(vb[1], vb[3], 0x0040u), prmt(vb[5], vb[7], 0x0040u), 0x5410u);
-    return e | (o << 4);
+__device__ __forceinline__ float div_rn_markstein(float t, float inv, float ns) {
+    const float q0 = __fmul_rn(t, inv);
+    const float rem = __fmaf_rn(q0, ns, t);
+    return __fmaf_rn(rem, inv, q0);
+}
+
+// One code word from PER = 32/B codes held as exact small floats, pairs
+// (q_2j, q_2j+1): each 16-bit half is sum q_k 2^(B k) accumulated exactly onto
+// 2^23 (whose low mantissa bits then hold it), the two halves spliced.
+template <int B>
+__device__ __forceinline__ uint32_t pack_word(const float2* qv) {
+    constexpr int PER = 32 / B, HALF = PER / 2;
+    float2 lo = make_float2(8388608.0f, 0.0f), hi = make_float2(8388608.0f, 0.0f);
+#pragma unroll
+    for (int j = 0; j < HALF / 2; ++j) {
+        const float2 w = make_float2((float)(1u << (B * 2 * j)), (float)(1u << (B * (2 * j + 1))));
+        lo = f2_fma(qv[j], w, lo);
+        hi = f2_fma(qv[j + HALF / 2], w, hi);
+    }
+    const float l = __fadd_rn(lo.x, lo.y), h = __fadd_rn(hi.x, hi.y);
+    return prmt(__float_as_uint(l), __float_as_uint(h), 0x5410u);
 }
 
 // One stage over the thread's CPT channels (a multiple of 16); the group of
@@ -110,23 +130,40 @@ __device__ __forceinline__ void quant_stage(float* r, bool update, float* acc, u
     mx = __fadd_rn(mx, 0.0f);
     const GroupParams p = group_params(mn, mx, L);
     meta = p.meta;
-    const float2 z2 = make_float2(p.z, p.z), inv2 = make_float2(p.inv, p.inv);
+    const float ns = -p.s;
+    // every quotient of the group lies between those of its extremes
+    const float ylo = div_rn_markstein(__fsub_rn(mn, p.z), p.inv, ns);
+    const float yhi = div_rn_markstein(__fsub_rn(mx, p.z), p.inv, ns);
+    const bool plain = ylo >= -0.5f && yhi < L + 0.5f;
+    const float2 z2 = make_float2(p.z, p.z), inv2 = make_float2(p.inv, p.inv), ns2 = make_float2(ns, ns);
     const float2 s2 = make_float2(p.s, p.s), m2 = make_float2(kRintMagic, kRintMagic);
 #pragma unroll
     for (int w = 0; w < CPT / PER; ++w) {
-        uint32_t vb[PER];
+        float2 qv[PER / 2];
+        if (plain) {
 #pragma unroll
-        for (int k = 0; k < PER; k += 2) {
-            const int i = PER * w + k;
-            float2 t = f2_mul(f2_sub(make_float2(r[i], r[i + 1]), z2), inv2);
-            t.x = fminf(fmaxf(t.x, 0.0f), L);
-            t.y = fminf(fmaxf(t.y, 0.0f), L);
-            const float2 v = f2_add(t, m2);             // 1.5*2^23 + q exactly
-            vb[k] = __float_as_uint(v.x);
-            vb[k + 1] = __float_as_uint(v.y);
-            if (update || acc) {
-                const float2 q = f2_sub(v, m2);
-                const float2 d = f2_fma(q, s2, z2);
+            for (int k = 0; k < PER; k += 2) {
+                const int i = PER * w + k;
+                const float2 y = div2_rn(f2_sub(make_float2(r[i], r[i + 1]), z2), inv2, ns2);
+                qv[k / 2] = f2_sub(f2_add(y, m2), m2);       // rint(y), in [0, L] here
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                const int i = PER * w + k;
+                const float t = __fsub_rn(r[i], p.z);
+                float y = p.s != 0.0f ? __fdiv_rn(t, p.s) : 0.0f;
+                y = fminf(fmaxf(y, 0.0f), L);                  // NaN -> 0
+                const float q = __fsub_rn(__fadd_rn(y, kRintMagic), kRintMagic);
+                if (k & 1) qv[k / 2].y = q; else qv[k / 2].x = q;
+            }
+        }
+        codes[w] = pack_word<B>(qv);
+        if (update || acc) {
+#pragma unroll
+            for (int k = 0; k < PER; k += 2) {
+                const int i = PER * w + k;
+                const float2 d = f2_fma(qv[k / 2], s2, z2);
                 if (update) {
                     const float2 nr = f2_sub(make_float2(r[i], r[i + 1]), d);
                     r[i] = nr.x; r[i + 1] = nr.y;
@@ -137,8 +174,6 @@ __device__ __forceinline__ void quant_stage(float* r, bool update, float* acc, u
                 }
             }
         }
-        if constexpr (B == 2) codes[w] = pack_codes16(vb);
-        else codes[w] = pack_codes8x4(vb);
     }
 }
 

@@ -28,7 +28,8 @@
 // the last update; argmin ties go to the lowest index; an empty cluster keeps
 // its centroid; centroids are bf16; asymmetric 2-bit group quantiser with an
 // fp16 scale s = fp16((max-min)/3) and an fp16 float zero-point z = fp16(min),
-// q = clamp(rint((r - z) * fp32(1/s)), 0, 3) (q = 0 when s = 0), stage
+// q = clamp(rint((r - z) / s), 0, 3) with IEEE single-precision division
+// (q = 0 when s = 0), stage
 // residual r <- r - (q*s + z); decoding sums ((c + d1) + d2) + ... in fp32 and
 // rounds once to bf16; 16 codes per 32-bit word, least significant first.
 //
@@ -215,13 +216,12 @@ static void quantize_stage(float* r, int D, int G, int b, uint32_t* codes, uint3
         float s32 = range / (float)L;
         uint16_t sh = to_f16(s32), zh = to_f16(mn);
         float s = f16_float(sh), z = f16_float(zh);
-        float inv = (s != 0.0f) ? 1.0f / s : 0.0f;
         meta[g] = (uint32_t)sh | ((uint32_t)zh << 16);
         for (int j = 0; j < G; ++j) {
             int e = g * G + j;
-            float t = (r[e] - z) * inv;
+            float t = (s != 0.0f) ? (r[e] - z) / s : 0.0f;
             float qf = std::nearbyint(t);
-            int q = qf < 0.0f ? 0 : (qf > (float)L ? L : (int)qf);
+            int q = qf > 0.0f ? (qf > (float)L ? L : (int)qf) : 0;   // NaN -> 0
             float deq = (float)q * s + z;          // q*s is exact: one rounding
             r[e] = r[e] - deq;
             codes[(e * b) / 32] |= (uint32_t)q << ((e * b) % 32);

@@ -18,8 +18,10 @@ MUTATIONS = {
     "packing stride": ("codes[(e * b) / 32] |= (uint32_t)q << ((e * b) % 32);",
                        "codes[(e * b) / 32] |= (uint32_t)q << ((e * b) % 16);"),
     "scale divisor": ("float s32 = range / (float)L;", "float s32 = range / (float)(L + 1);"),
-    "clamp at 3 for every width": ("int q = qf < 0.0f ? 0 : (qf > (float)L ? L : (int)qf);",
-                                   "int q = qf < 0.0f ? 0 : (qf > 3.0f ? 3 : (int)qf);"),
+    "clamp at 3 for every width": ("int q = qf > 0.0f ? (qf > (float)L ? L : (int)qf) : 0;",
+                                   "int q = qf > 0.0f ? (qf > 3.0f ? 3 : (int)qf) : 0;"),
+    "quantiser multiplies by the reciprocal": ("float t = (s != 0.0f) ? (r[e] - z) / s : 0.0f;",
+                                               "float t = (s != 0.0f) ? (r[e] - z) * (1.0f / s) : 0.0f;"),
     "4-bit field mask": ("& ((1u << b) - 1u);", "& 3u;"),
     "zero from max": ("uint16_t sh = to_f16(s32), zh = to_f16(mn);",
                       "uint16_t sh = to_f16(s32), zh = to_f16(mx);"),
@@ -61,6 +63,8 @@ PIN_CALLS = [
     (PINS.test_f16_rounding_matches_ieee, {}),
     (PINS.test_single_stage_no_smoothing_is_rtn, {"D": 128, "G": 64, "b": 2}),
     (PINS.test_single_stage_no_smoothing_is_rtn, {"D": 128, "G": 16, "b": 4}),
+    (PINS.test_exact_midpoints_round_to_even_level, {"b": 2}),
+    (PINS.test_exact_midpoints_round_to_even_level, {"b": 4}),
     (PINS.test_pack_example_golden, {}),
     (PINS.test_pack_example_4bit_golden, {}),
     (PINS.test_on_grid_values_round_trip, {"b": 2}),

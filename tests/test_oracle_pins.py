@@ -114,7 +114,8 @@ def test_f16_rounding_matches_ieee(oracle):
 
 def rtn_reference(xb, G, b=2):
     """Plain b-bit asymmetric group round-to-nearest (the RTN baseline), one
-    stage, no smoothing; vectorised numpy fp32."""
+    stage, no smoothing; vectorised numpy fp32: q = clip(rint((x - z) / s)),
+    numpy's float32 division being IEEE division."""
     L = (1 << b) - 1
     x = f32(xb)
     N, D = x.shape
@@ -123,9 +124,9 @@ def rtn_reference(xb, G, b=2):
     s16 = ((mx - mn) / np.float32(L)).astype(np.float16)
     z16 = mn.astype(np.float16)
     s, z = s16.astype(np.float32), z16.astype(np.float32)
-    with np.errstate(divide="ignore"):
-        inv = np.where(s != 0, np.float32(1) / s, np.float32(0)).astype(np.float32)
-    q = np.clip(np.rint((g - z[..., None]) * inv[..., None]), 0, L).astype(np.uint32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        t = np.where(s[..., None] != 0, (g - z[..., None]) / s[..., None], np.float32(0)).astype(np.float32)
+    q = np.clip(np.rint(t), 0, L).astype(np.uint32)
     per = 32 // b
     q = q.reshape(N, D // per, per)
     codes = (q << (b * np.arange(per, dtype=np.uint32))).sum(-1, dtype=np.uint64).astype(np.uint32)
@@ -142,6 +143,51 @@ def test_single_stage_no_smoothing_is_rtn(oracle, D, G, b):
     rc, rm = rtn_reference(x, G, b)
     assert np.array_equal(codes[0], rc)
     assert np.array_equal(meta[0], rm)
+
+
+def _midpoint_scales(bits, L, kmax):
+    """Every fp16 scale s = m * 2^e with a `bits`-bit significand m, over 20
+    binades, for which 0, L*s and the midpoints (k + 1/2)*s, k <= kmax, are all
+    exact in bf16."""
+    out = []
+    for e in range(-14, 6):
+        for m in range(1 << (bits - 1), 1 << bits):
+            s = m * 2.0 ** (e - bits + 1)
+            vals = np.array([0.0, L * s] + [(k + 0.5) * s for k in range(kmax + 1)])
+            if float(np.float16(s)) == s and np.array_equal(
+                    f32(SY.f64_to_bf16_bits(vals)).astype(np.float64), vals):
+                out.append(s)
+    return out
+
+
+@pytest.mark.parametrize("b", [2, 4])
+def test_exact_midpoints_round_to_even_level(oracle, b):
+    """An element exactly halfway between levels k and k+1 ((r - z)/s = k + 1/2
+    as an exact quotient) is coded to the even one of the two, for every scale
+    of a given width -- the rint-to-even rule applied to the exact quotient.
+    Groups are [0, L*s, midpoints...]: min 0 gives z = 0, and L*s / L = s
+    exactly.  A quantiser that rounds (r - z) * fp32(1/s) instead misses some of
+    these (at about one scale in five the product lands one float below or
+    above the midpoint)."""
+    L = (1 << b) - 1
+    kmax = 2 if b == 2 else 7          # midpoints (k + 1/2) s still exact in bf16
+    scales = _midpoint_scales(6 if b == 2 else 5, L, kmax)
+    assert len(scales) >= 150
+    D = G = 64
+    mids = [(k + 0.5) for k in range(kmax + 1)]
+    rows, want = [], []
+    for s in scales:
+        vals = [0.0, L * s] + [m * s for m in mids]
+        codes = [0, L] + [int(k + 1) if (k + 1) % 2 == 0 else int(k) for k in range(kmax + 1)]
+        reps = D // len(vals) + 1
+        rows.append((vals * reps)[:D])
+        want.append((codes * reps)[:D])
+    x = SY.f64_to_bf16_bits(np.array(rows))
+    assert np.array_equal(f32(x).astype(np.float64), np.array(rows))      # the values are exact
+    got_codes, meta = oracle.prq_encode(x, None, None, 1, G, b)
+    s_got, z_got = decode_meta(meta[0][:, 0])
+    assert np.array_equal(s_got.astype(np.float64), np.array(scales)) and np.all(z_got == 0)
+    assert np.array_equal(unpack(got_codes[0], D, b), np.array(want))
 
 
 def test_pack_example_golden(oracle):
