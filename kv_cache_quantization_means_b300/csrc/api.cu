@@ -262,6 +262,20 @@ qvg_status qvg_fit_stats(const qvg_config* cfg, int64_t n_tokens, const void* wo
     return ok();
 }
 
+qvg_status qvg_device_error(uint32_t* out, int32_t clear, qvg_stream stream) {
+    if (!out) return fail(QVG_ERR_INVALID_ARG, "out is NULL");
+    qvg_status st = cuda_status(qvg::read_codec_error(out, clear != 0, (cudaStream_t)stream), "device error word");
+    if (st) return st;
+    if (*out) return fail(QVG_ERR_TIMEOUT, "a kernel gave up a bounded wait (error word 0x%08x)", *out);
+    return ok();
+}
+
+qvg_status qvg_debug_set_wait(uint64_t wait_limit_ns, uint32_t flags, qvg_stream stream) {
+    if (flags > 1u) return fail(QVG_ERR_INVALID_ARG, "unknown debug flags 0x%x", flags);
+    const unsigned long long limit = wait_limit_ns ? (unsigned long long)wait_limit_ns : 2000000000ull;
+    return cuda_status(qvg::set_codec_debug(limit, flags, (cudaStream_t)stream), "debug settings");
+}
+
 qvg_status qvg_fit_centroids(const qvg_config* cfg, const qvg_bf16* x, int64_t n_tokens, int64_t head_stride,
                              int64_t token_stride, const qvg_bf16* warm_start, qvg_bf16* centroids, uint8_t* ids,
                              int64_t capacity, int64_t tok_offset, void* workspace, size_t workspace_bytes,

@@ -107,6 +107,15 @@ size_t coral_tc_scratch_bytes(int H, int64_t n_tokens);
 // validated by the caller.
 cudaError_t launch_encode(int D, int G, const EncodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode(int D, int G, const DecodeArgs& a, cudaStream_t s);
+// Persistent TMA-fed encoder / decoder (D = 64 or 128, G >= 16); *launched =
+// false (cudaSuccess) when the shape or layout is outside what they handle.
+cudaError_t launch_encode_tma(int D, int G, const EncodeArgs& a, bool* launched, cudaStream_t s);
+cudaError_t launch_decode_tma(int D, int G, const DecodeArgs& a, bool* launched, cudaStream_t s);
+// The device error word of the kernels that take no workspace (read, and
+// cleared when `clear`), and the bounded-wait limit / test flags; both
+// synchronise `s`.
+cudaError_t read_codec_error(uint32_t* out, bool clear, cudaStream_t s);
+cudaError_t set_codec_debug(unsigned long long wait_limit_ns, uint32_t flags, cudaStream_t s);
 cudaError_t launch_kmeans_init(int D, const uint16_t* x, int64_t head_stride, int64_t token_stride,
                                int64_t n_tokens, const uint16_t* warm, int H, int C, uint16_t* cent,
                                cudaStream_t s);

@@ -7,7 +7,7 @@
 // Both kernels stream HBM.  In the encoder a thread owns CPT = min(G, 32)
 // consecutive channels of a token row -- a whole group, or a 1/TPG share of a
 // 64- or 128-channel group whose extremes are combined with shuffles -- so
-// the group's scale, zero-point and reciprocal are formed once; its channels
+// the group's scale and zero-point are formed once; its channels
 // arrive as 16-byte bf16 vectors and its codes leave as one vector store per
 // stage.  In the write-heavy decoder a thread owns 16 consecutive channels,
 // so a warp's stores cover whole contiguous row segments.  Every load of a
@@ -275,10 +275,16 @@ cudaError_t decode_dg(const DecodeArgs& a, cudaStream_t s) {
     }
 
 cudaError_t launch_encode(int D, int G, const EncodeArgs& a, cudaStream_t s) {
+    bool launched = false;
+    cudaError_t e = launch_encode_tma(D, G, a, &launched, s);
+    if (e != cudaSuccess || launched) return e;
     QVG_DG_SWITCH(encode_dg, D, G, a, s)
 }
 
 cudaError_t launch_decode(int D, int G, const DecodeArgs& a, cudaStream_t s) {
+    bool launched = false;
+    cudaError_t e = launch_decode_tma(D, G, a, &launched, s);
+    if (e != cudaSuccess || launched) return e;
     QVG_DG_SWITCH(decode_dg, D, G, a, s)
 }
 

@@ -20,6 +20,7 @@ EXPORTS = [
     "qvg_assign", "qvg_update", "qvg_encode", "qvg_decode", "qvg_append_chunk", "qvg_decode_cache",
     "coral_predict_encode", "coral_predict_decode", "coral_predict_encode_static", "coral_fit_block",
     "coral_sas_workspace_bytes", "coral_sas_encode", "coral_sas_decode", "qvg_attention_decode",
+    "qvg_device_error", "qvg_debug_set_wait",
 ]
 
 
@@ -89,6 +90,8 @@ def load(path=LIB_PATH):
     L.coral_sas_decode.argtypes = [PCFG, ctypes.POINTER(coral_predictor), P, I64, P, P, P, P, P, P, P, SZ, P]
     L.qvg_attention_decode.argtypes = [PCFG, P, I64, I64, I64, ctypes.POINTER(qvg_encoded_view),
                                        ctypes.POINTER(qvg_encoded_view), I64, I64, ctypes.c_float, P, I64, I64, P]
+    L.qvg_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), I32, P]
+    L.qvg_debug_set_wait.argtypes = [ctypes.c_uint64, ctypes.c_uint32, P]
     for name in EXPORTS[2:]:
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -147,6 +150,19 @@ def qvg_fit_stats(cfg, n_tokens, workspace, stream=None):
     _check(load().qvg_fit_stats(ctypes.byref(cfg), n_tokens, _ptr(workspace), _nbytes(workspace), out,
                                 _stream(stream)))
     return tuple(int(v) for v in out)
+
+
+def qvg_device_error(clear=False, stream=None):
+    """(status, error word): QVG_ERR_TIMEOUT with the word when it was set."""
+    out = ctypes.c_uint32(0)
+    st = load().qvg_device_error(ctypes.byref(out), 1 if clear else 0, _stream(stream))
+    if st not in (QVG_OK, QVG_ERR_TIMEOUT):
+        _check(st)
+    return st, out.value
+
+
+def qvg_debug_set_wait(wait_limit_ns, flags=0, stream=None):
+    _check(load().qvg_debug_set_wait(wait_limit_ns, flags, _stream(stream)))
 
 
 def qvg_fit_centroids(cfg, x, n_tokens, head_stride, token_stride, warm_start, centroids, ids, capacity,
