@@ -48,8 +48,10 @@ def source_hash(*files):
 _CS = "kv_cache_quantization_means_b300/csrc/"
 KERNEL_SOURCES = {
     "assign": [_CS + "assign_tc.cu", _CS + "tc_common.cuh", _CS + "common.cuh", _CS + "kernels.h"],
-    "encode": [_CS + "prq.cu", _CS + "prq16.cuh", _CS + "common.cuh", _CS + "kernels.h"],
-    "decode": [_CS + "prq.cu", _CS + "prq16.cuh", _CS + "common.cuh", _CS + "kernels.h"],
+    "encode": [_CS + "prq.cu", _CS + "prq16.cuh", _CS + "common.cuh",
+               _CS + "tc_common.cuh", _CS + "kernels.h"],
+    "decode": [_CS + "prq_decode_tma.cu", _CS + "prq16.cuh", _CS + "common.cuh",
+               _CS + "tc_common.cuh", _CS + "kernels.h"],
     "coral_predict": [_CS + "coral_tc.cu", _CS + "prq16.cuh", _CS + "tc_common.cuh", _CS + "common.cuh",
                       _CS + "kernels.h"],
 }

@@ -149,10 +149,9 @@ QVG_API qvg_status qvg_fit_stats(const qvg_config* cfg, int64_t n_tokens, const 
                          size_t workspace_bytes, uint64_t* out, qvg_stream stream);
 
 /* Error word of the kernels that take no workspace -- the persistent PRQ
- * encoder and decoder behind qvg_encode, qvg_decode, qvg_decode_cache and
- * qvg_append_chunk: 0 = none, 0x7E000000 = a kernel gave up one of its
- * bounded waits (about 2 s by default) and the outputs of that call are not
- * valid.  The word is shared by every call on the current device and keeps
+ * decoder behind qvg_decode, qvg_decode_cache and coral_sas_*: 0 = none,
+ * 0x7E000000 = a kernel gave up one of its bounded waits (about 2 s by
+ * default) and the outputs of that call are not valid.  The word is shared by every call on the current device and keeps
  * its value until cleared; clear != 0 resets it to 0 after reading.  Returns
  * QVG_ERR_TIMEOUT (with *out filled) when the word was set, QVG_OK when it
  * was 0.  Waits for `stream`; out is host memory. */
@@ -163,8 +162,8 @@ QVG_API qvg_status qvg_device_error(uint32_t* out, int32_t clear, qvg_stream str
  * flags bit 0 makes each CTA's copy producer withhold its first copy, so that
  * the first wait of that CTA's consumers runs out (and the call records
  * 0x7E000000 in the error word, drains its other copies and returns).  For
- * failure-path tests only; applies to every later call on the current
- * device.  Waits for `stream`. */
+ * failure-path tests only; waits for `stream`, then applies to every call
+ * the process makes afterwards. */
 QVG_API qvg_status qvg_debug_set_wait(uint64_t wait_limit_ns, uint32_t flags, qvg_stream stream);
 
 /* SAS k-means (QVG sec. 2A items 1-2 and sec. 3): per head, T Lloyd iterations

@@ -1,4 +1,5 @@
 """Builds libqvg.so in-tree with nvcc for sm_103a (B300)."""
+import concurrent.futures
 import os
 import subprocess
 import sys
@@ -6,7 +7,7 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
-SOURCES = ["api.cu", "prq.cu", "prq_tma.cu", "kmeans.cu", "assign_tc.cu", "coral.cu", "coral_tc.cu", "coral_fit.cu", "attn.cu"]
+SOURCES = ["api.cu", "prq.cu", "prq_decode_tma.cu", "kmeans.cu", "assign_tc.cu", "coral.cu", "coral_tc.cu", "coral_fit.cu", "attn.cu"]
 LIB = os.path.join(HERE, "libqvg.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -29,17 +30,21 @@ def _stale():
 def build(force=False, verbose=False, extra=()):
     if not force and not _stale():
         return LIB
-    objs = []
     bdir = os.path.join(HERE, "_build")
     os.makedirs(bdir, exist_ok=True)
-    for src in SOURCES:
-        obj = os.path.join(bdir, src.replace(".cu", ".o"))
+    objs = [os.path.join(bdir, src.replace(".cu", ".o")) for src in SOURCES]
+
+    def compile_one(src, obj):
         cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
                "-I", os.path.join(ROOT, "include"), "-c", os.path.join(CSRC, src), "-o", obj, *extra]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
         subprocess.check_call(cmd)
-        objs.append(obj)
+
+    # the translation units are independent: compile them side by side
+    with concurrent.futures.ThreadPoolExecutor(max_workers=min(len(SOURCES), os.cpu_count() or 1)) as ex:
+        for f in [ex.submit(compile_one, src, obj) for src, obj in zip(SOURCES, objs)]:
+            f.result()
     tmp = LIB + ".tmp"
     subprocess.check_call([nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-lcudart_static", "-lrt", "-ldl", "-lpthread"])
     os.replace(tmp, LIB)

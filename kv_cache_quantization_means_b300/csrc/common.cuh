@@ -47,18 +47,28 @@ struct GroupParams {
     uint32_t meta;   // low half fp16 scale, high half fp16 zero
 };
 
-// Scale / zero / reciprocal of one group from its fp32 min and max.
-// levels = 2^b - 1: 3 for 2-bit codes, 15 for 4-bit codes.
-__device__ __forceinline__ GroupParams group_params(float mn, float mx, float levels = 3.0f) {
+// Scale / zero / reciprocal of one group from its fp32 min and max, with
+// L = 2^b - 1 levels above the zero-point (3 for 2-bit codes, 15 for 4-bit).
+// s = fp16(range / L) needs the correctly rounded quotient: with y = RN(1/L),
+// q0 = RN(range*y), rem = range - q0*L (exact in one fma) and RN(q0 + rem*y)
+// is it (Markstein's correction step; for L = 3 and 15 it was checked
+// against IEEE division for every finite non-negative fp32 range, subnormals
+// included).  An infinite range is passed through, as division would.
+template <int L>
+__device__ __forceinline__ GroupParams group_params(float mn, float mx) {
+    constexpr float Lf = (float)L, y = 1.0f / (float)L;
     GroupParams p;
-    float range = __fsub_rn(mx, mn);
-    float s32 = __fdiv_rn(range, levels);
-    __half sh = __float2half_rn(s32);
-    __half zh = __float2half_rn(mn);
-    p.s = __half2float(sh);
-    p.z = __half2float(zh);
+    const float range = __fsub_rn(mx, mn);
+    const float q0 = __fmul_rn(range, y);
+    const float rem = __fmaf_rn(q0, -Lf, range);
+    float s32 = __fmaf_rn(rem, y, q0);
+    if (!(range < INFINITY)) s32 = range;
+    const __half2 sz = __floats2half2_rn(s32, mn);    // low half: scale, high half: zero-point
+    const float2 f = __half22float2(sz);
+    p.s = f.x;
+    p.z = f.y;
     p.inv = (p.s != 0.0f) ? __frcp_rn(p.s) : 0.0f;
-    p.meta = (uint32_t)__half_as_ushort(sh) | ((uint32_t)__half_as_ushort(zh) << 16);
+    p.meta = *reinterpret_cast<const uint32_t*>(&sz);
     return p;
 }
 

@@ -107,9 +107,8 @@ size_t coral_tc_scratch_bytes(int H, int64_t n_tokens);
 // validated by the caller.
 cudaError_t launch_encode(int D, int G, const EncodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode(int D, int G, const DecodeArgs& a, cudaStream_t s);
-// Persistent TMA-fed encoder / decoder (D = 64 or 128, G >= 16); *launched =
-// false (cudaSuccess) when the shape or layout is outside what they handle.
-cudaError_t launch_encode_tma(int D, int G, const EncodeArgs& a, bool* launched, cudaStream_t s);
+// Persistent decoder fed by bulk copies (D = 64 or 128, G >= 16); *launched
+// = false (cudaSuccess) when the shape or layout is outside what it handles.
 cudaError_t launch_decode_tma(int D, int G, const DecodeArgs& a, bool* launched, cudaStream_t s);
 // The device error word of the kernels that take no workspace (read, and
 // cleared when `clear`), and the bounded-wait limit / test flags; both

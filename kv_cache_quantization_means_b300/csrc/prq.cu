@@ -75,7 +75,9 @@ __device__ __forceinline__ void load_words(const uint32_t* p, uint32_t* w) {
     }
 }
 
-template <int D, int G, bool HAS_C, int B>
+// SC: the stage count when it is a compile-time constant (the loop over
+// stages then unrolls), 0 when it is read from the arguments.
+template <int D, int G, bool HAS_C, int B, int SC>
 __global__ void __launch_bounds__(kThreads, 4) prq_encode_kernel(EncodeArgs a) {
     using M = GMap<D, G, B>;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -110,9 +112,12 @@ __global__ void __launch_bounds__(kThreads, 4) prq_encode_kernel(EncodeArgs a) {
     }
     const int64_t row = (int64_t)h * a.cap + a.tok_offset + n;
     const int64_t stage_rows = (int64_t)a.H * a.cap;
-    for (int s = 0; s < a.S; ++s) {
+    const int S = SC ? SC : a.S;
+#pragma unroll
+    for (int s = 0; s < (SC ? SC : kMaxStages); ++s) {
+        if (!SC && s >= S) break;
         uint32_t code[M::NW], meta;
-        quant_stage<M::CPT, M::TPG, B>(r, s + 1 < a.S, nullptr, code, meta);
+        quant_stage<M::CPT, M::TPG, B>(r, s + 1 < S, nullptr, code, meta);
         if (valid) {
             const int64_t srow = (int64_t)s * stage_rows + row;
             store_words<M::NW>(a.codes + srow * M::WPR + t * M::NW, code);
@@ -216,8 +221,18 @@ template <int D, int G, int B>
 cudaError_t encode_dgb(const EncodeArgs& a, cudaStream_t s) {
     using M = GMap<D, G, B>;
     dim3 grid((unsigned)((a.n_tokens + M::RPC - 1) / M::RPC), (unsigned)a.H);
-    if (a.C > 0) prq_encode_kernel<D, G, true, B><<<grid, kThreads, 0, s>>>(a);
-    else prq_encode_kernel<D, G, false, B><<<grid, kThreads, 0, s>>>(a);
+    auto kern = a.C > 0 ? prq_encode_kernel<D, G, true, B, 0> : prq_encode_kernel<D, G, false, B, 0>;
+    if constexpr (D == 64 || D == 128) {
+        // the head dims of the measured workloads get the unrolled stage loop
+        switch (a.S) {
+#define QVG_ENC_SC(SV) \
+            case SV: kern = a.C > 0 ? prq_encode_kernel<D, G, true, B, SV> : prq_encode_kernel<D, G, false, B, SV>; break;
+            QVG_ENC_SC(1) QVG_ENC_SC(2) QVG_ENC_SC(3) QVG_ENC_SC(4)
+#undef QVG_ENC_SC
+            default: break;
+        }
+    }
+    kern<<<grid, kThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -275,9 +290,6 @@ cudaError_t decode_dg(const DecodeArgs& a, cudaStream_t s) {
     }
 
 cudaError_t launch_encode(int D, int G, const EncodeArgs& a, cudaStream_t s) {
-    bool launched = false;
-    cudaError_t e = launch_encode_tma(D, G, a, &launched, s);
-    if (e != cudaSuccess || launched) return e;
     QVG_DG_SWITCH(encode_dg, D, G, a, s)
 }
 

@@ -17,12 +17,14 @@
 // the correctly rounded quotient (Markstein's correction step: P. Markstein,
 // "Computation of elementary functions on the IBM RISC System/6000
 // processor", IBM J. Res. Develop. 34(1), 1990).  That holds while nothing
-// overflows or underflows near a rounding boundary.  A group whose extreme
-// quotients (min r - z)/s and (max r - z)/s lie in [-1/2, L + 1/2) has every
-// rint(y) in [0, L] already (rounding is monotone), so it needs neither the
-// clamp nor any other range care; any other group -- in practice one whose
-// zero-point rounded far from its minimum, or non-finite values -- takes
-// __fdiv_rn and the clamp.
+// overflows or underflows near a rounding boundary.  A group whose extremes
+// satisfy min r - z >= -s/2 and max r - z <= (L + 1/4) s has every quotient
+// in [-1/2, L + 1/4] and so every rint(y) in [0, L] already (rounding is
+// monotone): it needs neither the clamp nor any other range care.  When any
+// group of the warp is not of that kind -- in practice one whose zero-point
+// rounded far from its minimum, or non-finite values -- the whole warp clamps
+// t to [-s, (L+1) s] before dividing and the quotient to [0, L] after, which
+// is exact for every group.  All 32 lanes must call the stage together.
 // Every 16 2-bit codes go to one 32-bit word, element k at bits 2k, 2k+1;
 // with 4-bit codes (levels 0..15, s = range / 15) every 8 codes go to one
 // word, element k at bits 4k .. 4k+3.  The words are assembled in fp32: each
@@ -102,61 +104,32 @@ __device__ __forceinline__ uint32_t pack_word(const float2* qv) {
 // words to `codes`; `meta` receives the group's (scale, zero) word.  When
 // `update` the residual is replaced by what the stage leaves; `acc` (may be
 // null) gets the dequantised values added.
-template <int CPT, int TPG, int B = 2>
-__device__ __forceinline__ void quant_stage(float* r, bool update, float* acc, uint32_t* codes, uint32_t& meta) {
-    static_assert(B == 2 || B == 4, "2- or 4-bit codes");
+// The element work of one stage, given the group's parameters (see
+// quant_stage); CLAMP selects the clamped form.
+template <int CPT, int B, bool CLAMP>
+__device__ __forceinline__ void quant_words(float* r, bool update, float* acc, uint32_t* codes, const GroupParams& p) {
     constexpr float L = (float)((1 << B) - 1);
     constexpr int PER = 32 / B;                      // codes per word
-    float m0 = fmin3(r[0], r[1], r[2]), M0 = fmax3(r[0], r[1], r[2]);
-    float m1 = fmin3(r[3], r[4], r[5]), M1 = fmax3(r[3], r[4], r[5]);
-#pragma unroll
-    for (int i = 6; i + 3 < CPT; i += 4) {
-        m0 = fmin3(m0, r[i], r[i + 1]);
-        M0 = fmax3(M0, r[i], r[i + 1]);
-        m1 = fmin3(m1, r[i + 2], r[i + 3]);
-        M1 = fmax3(M1, r[i + 2], r[i + 3]);
-    }
-    // CPT % 4 == 0: the loop stops with r[CPT-2], r[CPT-1] left
-    float mn = fmin3(m0, m1, fminf(r[CPT - 2], r[CPT - 1]));
-    float mx = fmax3(M0, M1, fmaxf(r[CPT - 2], r[CPT - 1]));
-#pragma unroll
-    for (int off = 1; off < TPG; off <<= 1) {
-        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    }
-    // a zero extreme is taken as +0 so the stored bits do not depend on the
-    // order in which equal extremes are met
-    mn = __fadd_rn(mn, 0.0f);
-    mx = __fadd_rn(mx, 0.0f);
-    const GroupParams p = group_params(mn, mx, L);
-    meta = p.meta;
-    const float ns = -p.s;
-    // every quotient of the group lies between those of its extremes
-    const float ylo = div_rn_markstein(__fsub_rn(mn, p.z), p.inv, ns);
-    const float yhi = div_rn_markstein(__fsub_rn(mx, p.z), p.inv, ns);
-    const bool plain = ylo >= -0.5f && yhi < L + 0.5f;
-    const float2 z2 = make_float2(p.z, p.z), inv2 = make_float2(p.inv, p.inv), ns2 = make_float2(ns, ns);
+    const float lo = -p.s, hi = (L + 1.0f) * p.s;
+    const float2 z2 = make_float2(p.z, p.z), inv2 = make_float2(p.inv, p.inv), ns2 = make_float2(-p.s, -p.s);
     const float2 s2 = make_float2(p.s, p.s), m2 = make_float2(kRintMagic, kRintMagic);
 #pragma unroll
     for (int w = 0; w < CPT / PER; ++w) {
         float2 qv[PER / 2];
-        if (plain) {
 #pragma unroll
-            for (int k = 0; k < PER; k += 2) {
-                const int i = PER * w + k;
-                const float2 y = div2_rn(f2_sub(make_float2(r[i], r[i + 1]), z2), inv2, ns2);
-                qv[k / 2] = f2_sub(f2_add(y, m2), m2);       // rint(y), in [0, L] here
+        for (int k = 0; k < PER; k += 2) {
+            const int i = PER * w + k;
+            float2 t = f2_sub(make_float2(r[i], r[i + 1]), z2);
+            if (CLAMP) {
+                t.x = fminf(fmaxf(t.x, lo), hi);
+                t.y = fminf(fmaxf(t.y, lo), hi);
             }
-        } else {
-#pragma unroll
-            for (int k = 0; k < PER; ++k) {
-                const int i = PER * w + k;
-                const float t = __fsub_rn(r[i], p.z);
-                float y = p.s != 0.0f ? __fdiv_rn(t, p.s) : 0.0f;
-                y = fminf(fmaxf(y, 0.0f), L);                  // NaN -> 0
-                const float q = __fsub_rn(__fadd_rn(y, kRintMagic), kRintMagic);
-                if (k & 1) qv[k / 2].y = q; else qv[k / 2].x = q;
+            float2 y = div2_rn(t, inv2, ns2);
+            if (CLAMP) {
+                y.x = fminf(fmaxf(y.x, 0.0f), L);              // NaN -> 0
+                y.y = fminf(fmaxf(y.y, 0.0f), L);
             }
+            qv[k / 2] = f2_sub(f2_add(y, m2), m2);           // rint(y), in [0, L]
         }
         codes[w] = pack_word<B>(qv);
         if (update || acc) {
@@ -175,6 +148,56 @@ __device__ __forceinline__ void quant_stage(float* r, bool update, float* acc, u
             }
         }
     }
+}
+
+template <int CPT, int TPG, int B = 2, int OFF1 = 1, int OFF2 = 2, int OFF3 = 4>
+__device__ __forceinline__ void quant_stage(float* r, bool update, float* acc, uint32_t* codes, uint32_t& meta) {
+    static_assert(B == 2 || B == 4, "2- or 4-bit codes");
+    constexpr float L = (float)((1 << B) - 1);
+    float m0 = fmin3(r[0], r[1], r[2]), M0 = fmax3(r[0], r[1], r[2]);
+    float m1 = fmin3(r[3], r[4], r[5]), M1 = fmax3(r[3], r[4], r[5]);
+#pragma unroll
+    for (int i = 6; i + 3 < CPT; i += 4) {
+        m0 = fmin3(m0, r[i], r[i + 1]);
+        M0 = fmax3(M0, r[i], r[i + 1]);
+        m1 = fmin3(m1, r[i + 2], r[i + 3]);
+        M1 = fmax3(M1, r[i + 2], r[i + 3]);
+    }
+    // CPT % 4 == 0: the loop stops with r[CPT-2], r[CPT-1] left
+    float mn = fmin3(m0, m1, fminf(r[CPT - 2], r[CPT - 1]));
+    float mx = fmax3(M0, M1, fmaxf(r[CPT - 2], r[CPT - 1]));
+    // the lanes of a group: OFF1, OFF2, OFF3 apart (up to TPG = 8)
+    if (TPG > 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, OFF1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, OFF1));
+    }
+    if (TPG > 2) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, OFF2));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, OFF2));
+    }
+    if (TPG > 4) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, OFF3));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, OFF3));
+    }
+    // a zero extreme is taken as +0 so the stored bits do not depend on the
+    // order in which equal extremes are met
+    mn = __fadd_rn(mn, 0.0f);
+    mx = __fadd_rn(mx, 0.0f);
+    const GroupParams p = group_params<(1 << B) - 1>(mn, mx);
+    meta = p.meta;
+    // Every quotient of the group lies between those of its extremes.  With
+    // (min - z) >= -s/2 and (max - z) <= (L + 1/4) s (both products exact: s
+    // is an fp16 value) every rint(y) is already in [0, L].
+    const bool plain = __fsub_rn(mn, p.z) >= -0.5f * p.s && __fsub_rn(mx, p.z) <= (L + 0.25f) * p.s;
+    // Otherwise (any lane of the warp, so that the branch is uniform) t is
+    // clamped to [-s, (L+1) s] first (exact bounds): inside, the quotient is
+    // unchanged and stays in [-1, L+1], where the division is exact; outside,
+    // the clamped and the true quotient both give code 0 or L.  s = 0 gives
+    // t = 0 and y = 0; a NaN goes to a bound, then to 0.  The clamped form is
+    // exact for every group, so lanes whose own group is plain may take it too.
+    const bool clamp = !__all_sync(0xffffffffu, plain);
+    if (clamp) quant_words<CPT, B, true>(r, update, acc, codes, p);
+    else quant_words<CPT, B, false>(r, update, acc, codes, p);
 }
 
 // 16-channel form (one code word).

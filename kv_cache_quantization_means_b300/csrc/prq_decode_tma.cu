@@ -1,38 +1,36 @@
-// Progressive residual quantisation, persistent TMA-fed encoder and decoder
-// for head_dim 64 and 128 (sm_103a).
+// Progressive residual quantisation: the persistent decoder fed by the copy
+// engine, for head_dim 64 and 128 (sm_103a).
 //
-// Quant VideoGen explainer, Sommario tecnico sec. 2A item 3 (each token's
-// centroid is subtracted) and sec. 2B items 1-3 (the residual is re-quantised
-// stage by stage; decoding dequantises, sums the stages and adds the centroid
-// back); sec. 3 (centroid caching: each streaming chunk decodes against its
-// own centroid version).
+// Quant VideoGen explainer, Sommario tecnico sec. 2B item 3 (decoding
+// dequantises every stage, sums them and adds the centroid back) and sec. 3
+// (centroid caching: each streaming chunk decodes against its own centroid
+// version).
 //
-// One CTA per SM walks a contiguous run of (head, token tile) units.  Warp 16
-// is the producer: one lane moves each tile's inputs into a ring of shared
-// memory stages with the copy engine --
-//   encoder: the bf16 token tile, one cp.async.bulk.tensor copy (rows of D
-//            channels, no swizzle);
-//   decoder: the tile's code rows, scale/zero words and cluster ids, one
-//            cp.async.bulk copy per stage and array (the scale/zero and id
-//            copies take the 16-byte-aligned window around the tile's bytes)
-// -- and the head's centroid table (C x D bf16, up to 64 KB) into its own
-// buffer whenever the run enters another head (or, streaming, another
-// centroid version).  Warps 0-15 compute: lane l owns 16 consecutive channels
-// of one tile row (8 lanes a row at D = 128, 4 at D = 64), so a warp covers 4
-// (8) rows and the 16 warps one tile.  Consumers release a stage as soon as
-// its words are in registers.
+// One CTA per SM walks a contiguous run of (head, token tile) units.  Warp 15
+// is the producer: one lane moves each tile's code rows, scale/zero words and
+// cluster ids into a ring of shared-memory stages with cp.async.bulk (one copy
+// per stage and array; the scale/zero and id copies take the 16-byte-aligned
+// window around the tile's bytes, and a window that would run past the end of
+// its buffer is left to plain loads), and the head's centroid table (C x D
+// bf16, up to 64 KB) into its own buffer whenever the run enters another head
+// or, streaming, another centroid version.  Warps 0-14 compute: lane l owns 16
+// consecutive channels of R rows of the tile (8 lanes a row at D = 128, 4 at
+// D = 64).  Consumers release a stage as soon as its words are in registers.
 //
-// Bank conflicts: a row of x, of the table or of the output is D*2 bytes of
-// 16-byte chunks; a lane reads its two chunks 2t, 2t+1 in the order that puts
-// the eight lanes of a quarter-warp on eight different bank groups (lanes of
-// the upper half of a row, and at D = 64 those of the second row of the
+// Bank conflicts: a row of the table or of the output is D*2 bytes of 16-byte
+// chunks; a lane reads its two chunks 2t, 2t+1 in the order that puts the
+// eight lanes of a quarter-warp on eight different bank groups (lanes of the
+// upper half of a row, and at D = 64 those of the second row of the
 // quarter-warp, take the odd chunk first).  Registers then hold the channels
-// in that order; the code words, meta index and output addresses follow it.
+// in that order; the code words and output addresses follow it.
 //
-// Every wait is bounded (qvg_debug_set changes the limit); a wait that runs
-// out records kErrTimeout in the library's device error word (read with
+// Every wait is bounded (qvg_debug_set_wait changes the limit); a wait that
+// runs out records kErrTimeout in the library's device error word (read with
 // qvg_device_error), every role drains the copies it issued and the CTA
 // returns.
+#include <atomic>
+#include <mutex>
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -43,16 +41,26 @@
 
 namespace qvg {
 
-// Library-wide device error word of the kernels without a workspace, the
-// bounded-wait limit (ns) and the test flags (bit 0: the producer withholds
-// its first copy, so that the first consumer wait runs out).
-__device__ uint32_t g_codec_err = 0;
-__device__ unsigned long long g_wait_limit_ns = 2000000000ull;
-__device__ uint32_t g_debug_flags = 0;
+// What the persistent decoder needs for its bounded waits: the
+// device error word of the current device (0x7E000000 once a wait ran out),
+// the wait limit in ns and the test flags (bit 0: each CTA's producer
+// withholds its first copy, so that the first consumer wait runs out).
+struct CodecCtl {
+    uint32_t* err;
+    unsigned long long limit;
+    uint32_t flags;
+};
+
+// The current device's control block (the error word's address is looked up
+// once per device); false when the lookup fails.
+bool codec_ctl(CodecCtl* ctl);
 
 namespace {
 
-constexpr int kCWarps = 16;                     // consumer warps
+// 15 consumer warps + the producer = 16 warps, four per scheduler, which
+// leaves each thread up to 128 registers (a scheduler's file holds 16,384; a
+// fifth warp on one of them would cap every thread at 96).
+constexpr int kCWarps = 15;                     // decoder consumer warps
 constexpr int kPThreads = 32 * (kCWarps + 1);   // + the producer warp
 constexpr int kMaxRing = 8;
 constexpr uint32_t kErrTimeout = 0x7E000000u;
@@ -77,7 +85,7 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         : "memory");
 }
 
-__device__ __forceinline__ void record_timeout() { atomicExch(&g_codec_err, kErrTimeout); }
+__device__ __forceinline__ void record_timeout(uint32_t* err) { atomicExch(err, kErrTimeout); }
 
 // Before a producer whose consumers may have given up returns: waits (bounded)
 // until the copies of the last `nst` stages it issued have landed, so that no
@@ -138,175 +146,32 @@ struct Cursor {
     }
 };
 
-// --------------------------------------------------------------- encoder --
 
-struct EncTma {
-    const uint16_t* cent;   // [H][C][D] or null
-    const uint8_t* ids;     // [H][cap]
-    uint32_t* codes;        // [S][H][cap][D*B/32]
-    uint32_t* meta;         // [S][H][cap][D/G]
-    int64_t cap, tok_offset, n_tokens;
-    int H, C, S, tiles, nst;
-    int head_inner;         // the tensor map's dims are (D, H, N)
-    uint32_t table_off, ring_off, bar_off;
-};
+constexpr uint32_t kSmemLimit = 232448u;
 
-template <int D, int G, int B, int R, bool HAS_C>
-__global__ void __launch_bounds__(kPThreads, 1) prq_encode_tma_kernel(const __grid_constant__ CUtensorMap xmap, EncTma a) {
-    using M = RowMap<D, R>;
-    constexpr int TILE = M::TILE, TPR = M::TPR, BLOCK = M::BLOCK;
-    constexpr int TPG = G / 16;                    // lanes per quantisation group
-    constexpr int WPT = B / 2;                     // code words per lane and stage (16 channels)
-    constexpr uint32_t kBoxBytes = BLOCK * D * 2, kTileBytes = kBoxBytes * R;
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    // the launch adds 1024 bytes of slack: the map is laid out from a 1024-byte boundary
-    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t bars = smem_u32(sm + a.bar_off);
-    auto full_bar = [&](int st) { return bars + 8u * st; };
-    auto empty_bar = [&](int st) { return bars + 8u * (kMaxRing + st); };
-    const uint32_t tab_full = bars + 8u * (2 * kMaxRing), tab_empty = tab_full + 8u;
-    const unsigned long long limit = g_wait_limit_ns;
-    if (threadIdx.x == 0) {
-        for (int st = 0; st < a.nst; ++st) {
-            mbar_init(full_bar(st), 1);
-            mbar_init(empty_bar(st), kCWarps);
-        }
-        mbar_init(tab_full, 1);
-        mbar_init(tab_empty, kCWarps);
-        fence_mbar_init();
-    }
-    __syncthreads();
-    const UnitRun run = unit_run(a.H, a.tiles);
-    const uint32_t ring = smem_u32(sm + a.ring_off);
+inline uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
-    if (warp == kCWarps) {
-        // ---------------- producer
-        if (lane != 0) return;
-        const bool withhold = (g_debug_flags & 1u) != 0;
-        bool ok = true;
-        int head = -1;
-        uint32_t tab_ph = 0;
-        int64_t issued = 0;
-        Cursor c{run.h0, run.t0, 0, 0u};
-        for (int64_t k = 0; k < run.count; ++k, c.next(a.tiles, a.nst)) {
-            if (HAS_C && c.h != head) {
-                if (head >= 0) {
-                    if (!wait_bounded(tab_empty, tab_ph, limit)) { ok = false; break; }
-                    tab_ph ^= 1u;
-                }
-                const uint32_t tb = (uint32_t)a.C * D * 2;
-                mbar_arrive_tx(tab_full, tb);
-                bulk_g2s(smem_u32(sm + a.table_off), a.cent + (int64_t)c.h * a.C * D, tb, tab_full);
-                head = c.h;
-            }
-            if (k >= a.nst && !wait_bounded(empty_bar(c.st), c.ph ^ 1u, limit)) { ok = false; break; }
-            if (withhold && k == 0) { ++issued; continue; }   // test flag: the first stage never fills
-            mbar_arrive_tx(full_bar(c.st), kTileBytes);
-            const uint32_t dst = ring + (uint32_t)c.st * kTileBytes;
-#pragma unroll
-            for (int j = 0; j < R; ++j) {
-                const int y = c.tile * TILE + j * BLOCK;
-                if (a.head_inner) tma_load_3d(dst + j * kBoxBytes, &xmap, full_bar(c.st), 0, c.h, y);
-                else tma_load_3d(dst + j * kBoxBytes, &xmap, full_bar(c.st), 0, y, c.h);
-            }
-            ++issued;
-        }
-        if (!ok) record_timeout();
-        if (!ok || withhold) drain(issued, a.nst, withhold, full_bar, limit);
-        if (withhold && HAS_C && head >= 0) wait_bounded(tab_full, tab_ph, limit);
-        return;
-    }
+}  // namespace
 
-    // ---------------- consumers: lane owns 16 channels of rows j * BLOCK + rb, j < R
-    const int rb = warp * M::RPW + lane / TPR;     // row within each block
-    const int t = lane % TPR;                      // 16-channel slice of the row
-    const int sw = chunk_swap<D>(lane);
-    const int c0 = 2 * t + sw, c1 = 2 * t + 1 - sw;   // chunk of register slots 0-7 and 8-15
-    int head = -1;
-    uint32_t tab_ph = 0;
-    const int64_t stage_rows = (int64_t)a.H * a.cap;
-    // the cluster ids of a unit's rows, loaded one unit ahead
-    auto load_ids = [&](int h, int tile, bool live, int* id) {
-#pragma unroll
-        for (int j = 0; j < R; ++j) {
-            const int64_t n = (int64_t)tile * TILE + j * BLOCK + rb;
-            id[j] = 0;
-            if (HAS_C && live && n < a.n_tokens)
-                id[j] = min((int)__ldg(a.ids + (int64_t)h * a.cap + a.tok_offset + n), a.C - 1);
-        }
-    };
-    int id_next[R];
-    load_ids(run.h0, run.t0, run.count > 0, id_next);
-    bool ok = true;
-    Cursor c{run.h0, run.t0, 0, 0u};
-    for (int64_t k = 0; k < run.count; ++k, c.next(a.tiles, a.nst)) {
-        int id[R];
-#pragma unroll
-        for (int j = 0; j < R; ++j) id[j] = id_next[j];
-        {
-            Cursor nx = c;
-            nx.next(a.tiles, a.nst);
-            load_ids(nx.h, nx.tile, k + 1 < run.count, id_next);
-        }
-        if (HAS_C && c.h != head) {
-            if (head >= 0) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(tab_empty);
-            }
-            if (!wait_bounded(tab_full, tab_ph, limit)) { ok = false; break; }
-            tab_ph ^= 1u;
-            head = c.h;
-        }
-        if (!wait_bounded(full_bar(c.st), c.ph, limit)) { ok = false; break; }
-        uint4 xv[R][2];
-        const uint8_t* tile_s = sm + a.ring_off + (size_t)c.st * kTileBytes;
-#pragma unroll
-        for (int j = 0; j < R; ++j) {
-            const uint8_t* xrow = tile_s + (size_t)(j * BLOCK + rb) * D * 2;
-            xv[j][0] = *reinterpret_cast<const uint4*>(xrow + 16 * c0);
-            xv[j][1] = *reinterpret_cast<const uint4*>(xrow + 16 * c1);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty_bar(c.st));
-#pragma unroll
-        for (int j = 0; j < R; ++j) {
-            float r[16];
-            unpack16(xv[j][0], xv[j][1], r);
-            if (HAS_C) {
-                const uint8_t* crow = sm + a.table_off + (size_t)id[j] * D * 2;
-                const uint4 k0 = *reinterpret_cast<const uint4*>(crow + 16 * c0);
-                const uint4 k1 = *reinterpret_cast<const uint4*>(crow + 16 * c1);
-                float cc[16];
-                unpack16(k0, k1, cc);
-                sub16(r, cc);
-            }
-            const int64_t n = (int64_t)c.tile * TILE + j * BLOCK + rb;
-            const bool valid = n < a.n_tokens;
-            const int64_t row = (int64_t)c.h * a.cap + a.tok_offset + n;
-            for (int s = 0; s < a.S; ++s) {
-                uint32_t w[WPT], m;
-                quant_stage<16, TPG, B>(r, s + 1 < a.S, nullptr, w, m);
-                if (valid) {
-                    const int64_t srow = (int64_t)s * stage_rows + row;
-                    if constexpr (B == 2) {
-                        // register slots 0-7 are chunk c0: halves of the word follow it
-                        a.codes[srow * (D / 16) + t] = sw ? ((w[0] >> 16) | (w[0] << 16)) : w[0];
-                    } else {
-                        uint32_t* cp = a.codes + srow * (D / 8) + 2 * t;
-                        *reinterpret_cast<uint2*>(cp) = sw ? make_uint2(w[1], w[0]) : make_uint2(w[0], w[1]);
-                    }
-                    if (t % TPG == 0) a.meta[srow * (D / G) + t / TPG] = m;
-                }
-            }
-        }
-    }
-    if (!ok) record_timeout();
-}
+// The error word of the kernels that take no workspace, one per device.
+__device__ uint32_t g_codec_err = 0;
+
+namespace {
+
+std::atomic<unsigned long long> g_limit_ns{2000000000ull};
+std::atomic<uint32_t> g_flags{0u};
+std::mutex g_err_mu;
+constexpr int kMaxDev = 64;
+uint32_t* g_err_ptr[kMaxDev] = {};
+
+}  // namespace
+
+namespace {
 
 // --------------------------------------------------------------- decoder --
 
 struct DecTma {
+    CodecCtl ctl;
     const uint32_t* codes;
     const uint32_t* meta;
     const uint8_t* ids;
@@ -330,7 +195,7 @@ __device__ __forceinline__ bool window16(int64_t start, int64_t len, int64_t ext
     return we <= extent;
 }
 
-template <int D, int G, int B, int R, bool HAS_C, bool VERSIONED>
+template <int D, int G, int B, int S, int R, bool HAS_C, bool VERSIONED>
 __global__ void __launch_bounds__(kPThreads, 1) prq_decode_tma_kernel(DecTma a) {
     using M = RowMap<D, R>;
     constexpr int TILE = M::TILE, TPR = M::TPR, BLOCK = M::BLOCK;
@@ -343,7 +208,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prq_decode_tma_kernel(DecTma a) 
     auto full_bar = [&](int st) { return bars + 8u * st; };
     auto empty_bar = [&](int st) { return bars + 8u * (kMaxRing + st); };
     const uint32_t tab_full = bars + 8u * (2 * kMaxRing), tab_empty = tab_full + 8u;
-    const unsigned long long limit = g_wait_limit_ns;
+    const unsigned long long limit = a.ctl.limit;
     int64_t* offs = reinterpret_cast<int64_t*>(sm + a.chunk_off);
     int32_t* vers = reinterpret_cast<int32_t*>(sm + a.chunk_off + 8 * (a.n_chunks + 1));
     if (threadIdx.x == 0) {
@@ -373,12 +238,12 @@ __global__ void __launch_bounds__(kPThreads, 1) prq_decode_tma_kernel(DecTma a) 
     const UnitRun run = unit_run(a.H, a.tiles);
     const int64_t stage_rows = (int64_t)a.H * a.cap;
     const size_t table_elems = (size_t)a.C * D;
-    const uint32_t ids_off = a.codes_bytes + (uint32_t)a.S * a.meta_slot;
+    const uint32_t ids_off = a.codes_bytes + (uint32_t)S * a.meta_slot;
 
     if (warp == kCWarps) {
         // ---------------- producer
         if (lane != 0) return;
-        const bool withhold = (g_debug_flags & 1u) != 0;
+        const bool withhold = (a.ctl.flags & 1u) != 0;
         bool ok = true;
         int head = -1, ver = -1;
         uint32_t tab_ph = 0;
@@ -393,15 +258,15 @@ __global__ void __launch_bounds__(kPThreads, 1) prq_decode_tma_kernel(DecTma a) 
                 ++issued;   // test flag: the first stage never fills
             } else {
                 // the bytes first (the barrier must expect them before any copy lands)
-                uint32_t bytes = (uint32_t)a.S * rows * WPR * 4;
+                uint32_t bytes = (uint32_t)S * rows * WPR * 4;
                 int64_t ws, we;
                 const int64_t row0 = (int64_t)c.h * a.cap + a.tok_begin + n0;
-                for (int s = 0; s < a.S; ++s)
+                for (int s = 0; s < S; ++s)
                     if (window16((s * stage_rows + row0) * MPR * 4, (int64_t)rows * MPR * 4, a.meta_words * 4, ws, we))
                         bytes += (uint32_t)(we - ws);
                 if (HAS_C && window16(row0, rows, a.id_bytes, ws, we)) bytes += (uint32_t)(we - ws);
                 mbar_arrive_tx(full_bar(c.st), bytes);
-                for (int s = 0; s < a.S; ++s) {
+                for (int s = 0; s < S; ++s) {
                     const int64_t srow = s * stage_rows + row0;
                     bulk_g2s(slot + (uint32_t)s * TILE * WPR * 4, a.codes + srow * WPR, (uint32_t)rows * WPR * 4,
                              full_bar(c.st));
@@ -429,7 +294,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prq_decode_tma_kernel(DecTma a) 
                 }
             }
         }
-        if (!ok) record_timeout();
+        if (!ok) record_timeout(a.ctl.err);
         if (!ok || withhold) drain(issued, a.nst, withhold, full_bar, limit);
         if (withhold && HAS_C && head >= 0) wait_bounded(tab_full, tab_ph, limit);
         return;
@@ -450,13 +315,12 @@ __global__ void __launch_bounds__(kPThreads, 1) prq_decode_tma_kernel(DecTma a) 
         const int rows = (int)min((int64_t)TILE, a.n_rows - n0);
         if (!wait_bounded(full_bar(c.st), c.ph, limit)) { ok = false; break; }
         const uint8_t* slot = sm + a.ring_off + (size_t)c.st * a.slot_bytes;
-        uint32_t code[R][kMaxStages][WPT], meta[R][kMaxStages];
+        uint32_t code[R][S][WPT], meta[R][S];
         int id[R];
         const int64_t row0 = (int64_t)c.h * a.cap + a.tok_begin + n0;
         int64_t ws, we;
 #pragma unroll
-        for (int s = 0; s < kMaxStages; ++s) {
-            if (s >= a.S) break;
+        for (int s = 0; s < S; ++s) {
             const int64_t srow = s * stage_rows + row0;
             // scale/zero words: from the stage, or (a window that would pass the end of
             // the buffer, which the producer did not copy) straight from global memory
@@ -526,8 +390,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prq_decode_tma_kernel(DecTma a) 
                 for (int e = 0; e < 16; ++e) acc[e] = 0.0f;
             }
 #pragma unroll
-            for (int s = 0; s < kMaxStages; ++s) {
-                if (s >= a.S) break;
+            for (int s = 0; s < S; ++s) {
                 if constexpr (B == 2) {
                     // register slots 0-7 hold chunk c0: bring its codes to the low half
                     const uint32_t cw = sw ? ((code[j][s][0] >> 16) | (code[j][s][0] << 16)) : code[j][s][0];
@@ -548,67 +411,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prq_decode_tma_kernel(DecTma a) 
             }
         }
     }
-    if (!ok) record_timeout();
-}
-
-// ------------------------------------------------------------- host side --
-
-constexpr uint32_t kSmemLimit = 232448u;
-
-uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
-
-constexpr int kEncRows = 2;   // encoder: rows per lane and tile
-
-template <int D, int G, int B>
-cudaError_t encode_tma_dgb(const EncodeArgs& a, bool* launched, cudaStream_t s) {
-    using M = RowMap<D, kEncRows>;
-    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
-    if (!enc) return cudaSuccess;
-    const bool head_inner = a.head_stride <= a.token_stride;
-    cuuint64_t dims[3], strides[2];
-    cuuint32_t box[3], estr[3] = {1, 1, 1};
-    dims[0] = (cuuint64_t)D;
-    if (head_inner) {
-        dims[1] = (cuuint64_t)a.H; dims[2] = (cuuint64_t)a.n_tokens;
-        strides[0] = (cuuint64_t)a.head_stride * 2; strides[1] = (cuuint64_t)a.token_stride * 2;
-        box[0] = D; box[1] = 1; box[2] = M::BLOCK;
-    } else {
-        dims[1] = (cuuint64_t)a.n_tokens; dims[2] = (cuuint64_t)a.H;
-        strides[0] = (cuuint64_t)a.token_stride * 2; strides[1] = (cuuint64_t)a.head_stride * 2;
-        box[0] = D; box[1] = M::BLOCK; box[2] = 1;
-    }
-    if (a.H == 1) {
-        if (head_inner) strides[0] = (cuuint64_t)D * 2;
-        else strides[1] = strides[0] * (cuuint64_t)a.n_tokens;
-    }
-    CUtensorMap map;
-    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(a.x), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return cudaSuccess;   // layout not expressible: the caller falls back
-    EncTma t;
-    t.cent = a.cent; t.ids = a.ids; t.codes = a.codes; t.meta = a.meta;
-    t.cap = a.cap; t.tok_offset = a.tok_offset; t.n_tokens = a.n_tokens;
-    t.H = a.H; t.C = a.C; t.S = a.S;
-    t.tiles = (int)((a.n_tokens + M::TILE - 1) / M::TILE);
-    t.head_inner = head_inner ? 1 : 0;
-    const uint32_t tile_bytes = (uint32_t)M::TILE * D * 2;
-    t.table_off = 0;
-    t.ring_off = align_up(a.C > 0 ? (uint32_t)a.C * D * 2 : 0u, 1024u);
-    t.nst = kMaxRing;
-    while (t.nst > 2 && t.ring_off + (uint32_t)t.nst * tile_bytes + 256u + 1024u > kSmemLimit) --t.nst;
-    t.bar_off = t.ring_off + (uint32_t)t.nst * tile_bytes;
-    const uint32_t smem = t.bar_off + 8u * (2 * kMaxRing + 2) + 1024u;
-    if (smem > kSmemLimit) return cudaSuccess;
-    const int64_t units = (int64_t)a.H * t.tiles;
-    const int grid = (int)(units < sm_count() ? units : sm_count());
-    auto kern = a.C > 0 ? prq_encode_tma_kernel<D, G, B, kEncRows, true> : prq_encode_tma_kernel<D, G, B, kEncRows, false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    kern<<<grid, kPThreads, smem, s>>>(map, t);
-    e = cudaGetLastError();
-    if (e == cudaSuccess) *launched = true;
-    return e;
+    if (!ok) record_timeout(a.ctl.err);
 }
 
 // Shared-memory layout of the decoder for R rows per lane; false when it
@@ -633,14 +436,14 @@ bool decode_layout(const DecodeArgs& a, DecTma& t) {
     return t.bar_off + 8u * (2 * kMaxRing + 2) + 1024u <= kSmemLimit;
 }
 
-template <int D, int G, int B, int R>
+template <int D, int G, int B, int S, int R>
 cudaError_t decode_tma_launch(const DecodeArgs& a, DecTma& t, bool* launched, cudaStream_t s) {
     const uint32_t smem = t.bar_off + 8u * (2 * kMaxRing + 2) + 1024u;
     const int64_t units = (int64_t)a.H * t.tiles;
     const int grid = (int)(units < sm_count() ? units : sm_count());
-    auto kern = prq_decode_tma_kernel<D, G, B, R, false, false>;
-    if (a.C > 0 && a.chunk_offset) kern = prq_decode_tma_kernel<D, G, B, R, true, true>;
-    else if (a.C > 0) kern = prq_decode_tma_kernel<D, G, B, R, true, false>;
+    auto kern = prq_decode_tma_kernel<D, G, B, S, R, false, false>;
+    if (a.C > 0 && a.chunk_offset) kern = prq_decode_tma_kernel<D, G, B, S, R, true, true>;
+    else if (a.C > 0) kern = prq_decode_tma_kernel<D, G, B, S, R, true, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, kPThreads, smem, s>>>(t);
@@ -649,10 +452,19 @@ cudaError_t decode_tma_launch(const DecodeArgs& a, DecTma& t, bool* launched, cu
     return e;
 }
 
+// Rows per lane: four while the stages' code words are small, else two.
+template <int D, int G, int B, int S>
+cudaError_t decode_tma_dgbs(const DecodeArgs& a, DecTma& t, bool* launched, cudaStream_t s) {
+    constexpr int R = S * B <= 8 ? 4 : 2;
+    if (!decode_layout<D, G, B, R>(a, t)) return cudaSuccess;
+    return decode_tma_launch<D, G, B, S, R>(a, t, launched, s);
+}
+
 template <int D, int G, int B>
 cudaError_t decode_tma_dgb(const DecodeArgs& a, bool* launched, cudaStream_t s) {
     constexpr int MPR = D / G;
     DecTma t;
+    if (!codec_ctl(&t.ctl)) return cudaSuccess;
     t.codes = a.codes; t.meta = a.meta; t.ids = a.ids; t.cent = a.cent;
     t.chunk_offset = a.chunk_offset; t.chunk_version = a.chunk_version; t.n_chunks = a.n_chunks;
     t.cap = a.cap; t.tok_begin = a.tok_begin; t.n_rows = a.tok_end - a.tok_begin;
@@ -660,17 +472,13 @@ cudaError_t decode_tma_dgb(const DecodeArgs& a, bool* launched, cudaStream_t s) 
     t.H = a.H; t.C = a.C; t.S = a.S;
     t.meta_words = (int64_t)a.S * a.H * a.cap * MPR;
     t.id_bytes = (int64_t)a.H * a.cap;
-    // four rows per lane where the stages fit, else two
-    if (decode_layout<D, G, B, 4>(a, t)) return decode_tma_launch<D, G, B, 4>(a, t, launched, s);
-    if (decode_layout<D, G, B, 2>(a, t)) return decode_tma_launch<D, G, B, 2>(a, t, launched, s);
-    return cudaSuccess;
-}
-
-template <int D, int G>
-cudaError_t encode_tma_dg(const EncodeArgs& a, bool* launched, cudaStream_t s) {
-    if (a.bits == 2) return encode_tma_dgb<D, G, 2>(a, launched, s);
-    if (a.bits == 4) return encode_tma_dgb<D, G, 4>(a, launched, s);
-    return cudaSuccess;
+    switch (a.S) {
+        case 1: return decode_tma_dgbs<D, G, B, 1>(a, t, launched, s);
+        case 2: return decode_tma_dgbs<D, G, B, 2>(a, t, launched, s);
+        case 3: return decode_tma_dgbs<D, G, B, 3>(a, t, launched, s);
+        case 4: return decode_tma_dgbs<D, G, B, 4>(a, t, launched, s);
+        default: return cudaSuccess;
+    }
 }
 
 template <int D, int G>
@@ -694,14 +502,6 @@ cudaError_t decode_tma_dg(const DecodeArgs& a, bool* launched, cudaStream_t s) {
         default: return cudaSuccess;                       \
     }
 
-cudaError_t launch_encode_tma(int D, int G, const EncodeArgs& a, bool* launched, cudaStream_t s) {
-    *launched = false;
-    if (a.n_tokens <= 0 || a.C > kMaxClusters) return cudaSuccess;
-    if ((reinterpret_cast<uintptr_t>(a.x) & 15u) || (a.head_stride % 8) || (a.token_stride % 8)) return cudaSuccess;
-    if (a.n_tokens > (int64_t)INT32_MAX / 2) return cudaSuccess;
-    QVG_TMA_SWITCH(encode_tma_dg, D, G, a, launched, s)
-}
-
 cudaError_t launch_decode_tma(int D, int G, const DecodeArgs& a, bool* launched, cudaStream_t s) {
     *launched = false;
     const int64_t rows = a.tok_end - a.tok_begin;
@@ -709,6 +509,23 @@ cudaError_t launch_decode_tma(int D, int G, const DecodeArgs& a, bool* launched,
     if (a.C > 0 && a.chunk_offset && a.n_chunks > 1024) return cudaSuccess;
     if (rows > (int64_t)INT32_MAX / 2) return cudaSuccess;
     QVG_TMA_SWITCH(decode_tma_dg, D, G, a, launched, s)
+}
+
+bool codec_ctl(CodecCtl* ctl) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return false;
+    {
+        std::lock_guard<std::mutex> lock(g_err_mu);
+        if (!g_err_ptr[dev]) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_codec_err) != cudaSuccess) return false;
+            g_err_ptr[dev] = static_cast<uint32_t*>(p);
+        }
+        ctl->err = g_err_ptr[dev];
+    }
+    ctl->limit = g_limit_ns.load();
+    ctl->flags = g_flags.load();
+    return true;
 }
 
 cudaError_t read_codec_error(uint32_t* out, bool clear, cudaStream_t s) {
@@ -722,10 +539,9 @@ cudaError_t read_codec_error(uint32_t* out, bool clear, cudaStream_t s) {
 }
 
 cudaError_t set_codec_debug(unsigned long long wait_limit_ns, uint32_t flags, cudaStream_t s) {
-    cudaError_t e = cudaMemcpyToSymbolAsync(g_wait_limit_ns, &wait_limit_ns, sizeof(wait_limit_ns), 0,
-                                            cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess) e = cudaMemcpyToSymbolAsync(g_debug_flags, &flags, sizeof(flags), 0, cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    cudaError_t e = cudaStreamSynchronize(s);   // calls already enqueued keep the old settings
+    g_limit_ns.store(wait_limit_ns);
+    g_flags.store(flags);
     return e;
 }
 

@@ -1,10 +1,9 @@
-"""Failure path of the bounded waits in the persistent encoder and decoder,
-exercised without a GPU fault: a test flag makes each CTA's copy producer
-withhold its first copy, so the consumers' first wait runs out after a short
-limit.  The kernels must then record the error word (0x7E000000), drain the
-copies they did issue and return, leaving the context usable; the library
-reports the word as QVG_ERR_TIMEOUT.  Nothing here traps, faults or waits
-without a limit."""
+"""Failure path of the bounded waits in the persistent decoder, exercised
+without a GPU fault: a test flag makes each CTA's copy producer withhold its
+first copy, so the consumers' first wait runs out after a short limit.  The
+kernel must then record the error word (0x7E000000), drain the copies it did
+issue and return, leaving the context usable; the library reports the word as
+QVG_ERR_TIMEOUT.  Nothing here traps, faults or waits without a limit."""
 import numpy as np
 import pytest
 import torch
@@ -42,9 +41,6 @@ def test_withheld_copy_expires_the_wait_and_reports_timeout(qvg, C):
     codes_ref = enc["codes"].clone()
     try:
         qvg.qvg_debug_set_wait(20_000_000, 1)      # 20 ms, first copy withheld
-        qvg.qvg_encode(cfg, x, N, N * D, D, enc["centroids"], 0, enc["codes"], enc["meta"], enc["ids"], N, 0, ws)
-        torch.cuda.synchronize()
-        assert qvg.qvg_device_error(clear=True) == (qvg.QVG_ERR_TIMEOUT, ERR_TIMEOUT_WORD)
         out = torch.empty_like(ref)
         qvg.qvg_decode(cfg, enc["codes"], enc["meta"], enc["ids"], enc["centroids"], N, 0, N, out, N * D, D)
         torch.cuda.synchronize()
@@ -52,6 +48,7 @@ def test_withheld_copy_expires_the_wait_and_reports_timeout(qvg, C):
     finally:
         qvg.qvg_debug_set_wait(0, 0)
     # the context still works: a normal encode and decode reproduce the clean run
+    # (the encoder has no waits: the flag leaves it unchanged)
     qvg.qvg_encode(cfg, x, N, N * D, D, enc["centroids"], 0, enc["codes"], enc["meta"], enc["ids"], N, 0, ws)
     out = torch.empty_like(ref)
     qvg.qvg_decode(cfg, enc["codes"], enc["meta"], enc["ids"], enc["centroids"], N, 0, N, out, N * D, D)
