@@ -456,14 +456,14 @@ def cpu_baseline_attn(nq=512):
     from oracle import oracle as O
     O.build()
     wl = workload("wan")
-    n = min(os.cpu_count() or 1, 8)
+    n = host_workers()
     ctx = mp.get_context("spawn")
     # one BLAS thread per worker, so that `cores` counts the threads used
     saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
     os.environ.update({k: "1" for k in saved})
     try:
         with ctx.Pool(n) as pool:
-            walls = pool.map(_oracle_attn_sample, [(wl.seed, h, nq) for h in range(n)])
+            walls = pool.map(_oracle_attn_sample, [(wl.seed, h % wl.heads, nq) for h in range(n)])
     finally:
         for k, v in saved.items():
             if v is None:
@@ -563,16 +563,24 @@ def _oracle_unit(args):
     return _t.perf_counter() - t0, x.size * 2
 
 
-def cpu_baseline(name, max_units=None, bits=None):
+def host_workers():
+    """Worker processes of the CPU oracle: one per core this process may run
+    on (both the cpu_baseline leg and --impl reference use this count)."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(name, bits=None):
     """The oracle as it stands on this host's cores: one (layer, tensor, head)
-    unit per worker process, all units in parallel; throughput = bf16 bytes of
-    the units / wall time."""
+    unit per worker process, one process per core, all units in parallel;
+    throughput = bf16 bytes of the units / wall time."""
     import multiprocessing as mp
     from oracle import oracle as O
     O.build()
     wl = workload(name, bits)
-    cores = os.cpu_count() or 1
-    n = min(cores, 8 if max_units is None else max_units)
+    n = host_workers()
     units = [(name, bits, (i * 7) % wl.layers, i % 2, (i * 5) % wl.heads) for i in range(n)]
     ctx = mp.get_context("spawn")
     with ctx.Pool(n) as pool:
@@ -595,8 +603,8 @@ def run_reference(args):
     wl = workload(name, args.bits)
     t0 = time.perf_counter()
     per_step = []
-    base = (lambda: cpu_baseline_attn(nq=128)) if name == "attn" else \
-        (lambda: cpu_baseline(name, max_units=2, bits=args.bits))
+    # the same sample, on the same number of cores, as the cpu_baseline leg
+    base = (lambda: cpu_baseline_attn()) if name == "attn" else (lambda: cpu_baseline(name, bits=args.bits))
     for _ in range(args.warmup):
         base()
     for _ in range(args.steps):

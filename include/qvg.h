@@ -149,7 +149,8 @@ QVG_API qvg_status qvg_fit_stats(const qvg_config* cfg, int64_t n_tokens, const 
                          size_t workspace_bytes, uint64_t* out, qvg_stream stream);
 
 /* Error word of the kernels that take no workspace -- the persistent PRQ
- * decoder behind qvg_decode, qvg_decode_cache and coral_sas_*: 0 = none,
+ * decoder behind qvg_decode, qvg_decode_cache and coral_sas_*, and the
+ * tensor-core kernels of coral_predict_encode_static: 0 = none,
  * 0x7E000000 = a kernel gave up one of its bounded waits (about 2 s by
  * default) and the outputs of that call are not valid.  The word is shared by every call on the current device and keeps
  * its value until cleared; clear != 0 resets it to 0 after reading.  Returns
@@ -254,15 +255,21 @@ QVG_API qvg_status coral_predict_encode(const qvg_config* cfg, const coral_predi
  * of coral_predict_encode without the workspace: the low-rank scratch is a
  * fixed 4 MiB device array inside this library (64 floats per token), which
  * every GPU that loads the library keeps until the process exits.
- *  - n_tokens must be <= 16384; larger returns QVG_ERR_CAPACITY, launching
+ *  - n_tokens must be <= 16384, and the call's scratch (the low-rank
+ *    projection or, with head_dim 128 and rank 32, the tensor-core path's
+ *    128*n_tokens + 192*H*D bytes and a little alignment, whichever is
+ *    larger) must fit the 4 MiB; otherwise QVG_ERR_CAPACITY, launching
  *    nothing.  The call allocates and frees nothing.
  *  - The first call on a device (with a previous layer) looks up the array's
- *    device address on the current device; make that first call before any
- *    stream capture.
+ *    device address, and that of the library's device error word, on the
+ *    current device; make that first call before any stream capture.
  *  - All calls share the one array: calls whose work can overlap on the GPU
  *    (other streams, other host threads) race and must be serialised by the
- *    caller.  The array needs no clearing: each call writes every value it
- *    reads before reading it. */
+ *    caller.  The array's contents carry nothing from one call to the next:
+ *    each call writes every value it reads before reading it.
+ *  - A tensor-core wait that runs out (its outputs are then not valid) is
+ *    recorded in the library's device error word: read it with
+ *    qvg_device_error. */
 QVG_API qvg_status coral_predict_encode_static(const qvg_config* cfg, const coral_predictor* pred,
                                        const qvg_bf16* xhat_prev, const qvg_bf16* x_next, int64_t n_tokens,
                                        uint32_t* codes, uint32_t* meta, qvg_bf16* xhat_next, float* pred_out,

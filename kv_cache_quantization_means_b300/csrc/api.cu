@@ -637,6 +637,11 @@ qvg_status coral_predict_encode_static(const qvg_config* cfg, const coral_predic
     if (n_tokens > kStaticMaxTokens)
         return fail(QVG_ERR_CAPACITY, "n_tokens %lld exceeds the %lld tokens the built-in scratch holds",
                     (long long)n_tokens, (long long)kStaticMaxTokens);
+    if (cfg && cfg->num_heads > 0 && xhat_prev && n_tokens > 0 &&
+        coral_ws_bytes(cfg, n_tokens) > kStaticScratchFloats * sizeof(float))
+        return fail(QVG_ERR_CAPACITY, "%d heads x %lld tokens need %zu bytes of scratch; the built-in array holds %zu",
+                    cfg->num_heads, (long long)n_tokens, coral_ws_bytes(cfg, n_tokens),
+                    kStaticScratchFloats * sizeof(float));
     float* scratch = nullptr;
     qvg_status st = QVG_OK;
     if (n_tokens > 0 && xhat_prev) {
@@ -658,7 +663,10 @@ qvg_status coral_predict_encode_static(const qvg_config* cfg, const coral_predic
     a.lowrank = scratch;
     a.workspace = scratch;
     a.workspace_bytes = kStaticScratchFloats * sizeof(float);
-    if (scratch) clear_coral_error(cfg, n_tokens, scratch, a.workspace_bytes, (cudaStream_t)stream);
+    // a tensor-core wait that runs out is recorded in the library's device
+    // error word (qvg_device_error), the only word this call can report through
+    a.err_out = qvg::codec_error_word();
+    if (scratch && !a.err_out) return fail(QVG_ERR_CUDA, "device error word lookup failed");
     return cuda_status(qvg::launch_coral(cfg->head_dim, cfg->group_size, true, a, (cudaStream_t)stream),
                        "coral launch");
 }

@@ -114,6 +114,9 @@ cudaError_t launch_decode_tma(int D, int G, const DecodeArgs& a, bool* launched,
 // cleared when `clear`), and the bounded-wait limit / test flags; both
 // synchronise `s`.
 cudaError_t read_codec_error(uint32_t* out, bool clear, cudaStream_t s);
+// That error word's device address on the current device (looked up once per
+// device), or nullptr when the lookup fails.
+uint32_t* codec_error_word();
 cudaError_t set_codec_debug(unsigned long long wait_limit_ns, uint32_t flags, cudaStream_t s);
 cudaError_t launch_kmeans_init(int D, const uint16_t* x, int64_t head_stride, int64_t token_stride,
                                int64_t n_tokens, const uint16_t* warm, int H, int C, uint16_t* cent,

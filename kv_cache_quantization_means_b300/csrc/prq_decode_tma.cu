@@ -528,6 +528,11 @@ bool codec_ctl(CodecCtl* ctl) {
     return true;
 }
 
+uint32_t* codec_error_word() {
+    CodecCtl c;
+    return codec_ctl(&c) ? c.err : nullptr;
+}
+
 cudaError_t read_codec_error(uint32_t* out, bool clear, cudaStream_t s) {
     cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_codec_err, sizeof(uint32_t), 0, cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess && clear) {

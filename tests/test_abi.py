@@ -236,3 +236,17 @@ def test_attention_argument_checks(Q):
     assert call(cfg=c0, k=V(codes=16, meta=16, ids=None, centroids=None), nk=0) == 1
     # no queries: nothing to do, and nothing launched
     assert call(nq=0, q=None, out=None) == 0
+
+
+def test_static_coral_encode_refuses_scratch_beyond_its_array(Q):
+    """The allocation-free Coral encode checks on the host that its scratch
+    fits the built-in 4 MiB array: 128 heads of 128 channels at 16,384 tokens
+    need 128*N + 192*H*D bytes > 4 MiB for the tensor-core path, so the call
+    returns QVG_ERR_CAPACITY before touching the GPU (the pointers are never
+    dereferenced)."""
+    c = Q.config(128, 128, 0, 0, 2, 64)
+    fake = 1 << 20
+    pred = Q.qvg.coral_predictor(B=fake, U=fake, W=fake, rank=32)
+    with pytest.raises(Q.QvgError) as e:
+        Q.coral_predict_encode_static(c, pred, fake, fake, 16384, fake, fake, fake, None, stream=0)
+    assert e.value.status == 3

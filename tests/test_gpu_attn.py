@@ -124,6 +124,9 @@ CASES = [  # D, bits, S, G, C, token-major
     (64, 2, 1, 32, 0, True),
     (64, 4, 3, 16, 8, False),
     (128, 2, 4, 128, 0, True),
+    # 4-bit, one stage: the kernel's prefetching specialisation
+    (128, 4, 1, 64, 16, True),
+    (64, 4, 1, 16, 0, False),
 ]
 
 

@@ -87,3 +87,42 @@ def test_stream_wan_shape_first_chunks(qvg, oracle):
         np.testing.assert_array_equal(codes[:, h], oc)
         want = oracle.decode(oc, om, oi, vers[0], G)
         np.testing.assert_array_equal(dec[h], want)
+
+
+def test_stream_wan_shape_through_a_warm_refit(qvg, oracle):
+    """Ten real 4680-token chunks of the streaming workload (Wan2.1 shape,
+    C = 256, T = 4, refit every 8th chunk): chunk 0 refits cold, chunks 1-7
+    assign to that table, chunk 8 refits warm-started from it (a second
+    version), chunk 9 assigns to the new one.  Centroid versions, ids, codes,
+    scale/zero words and the decode of the whole history -- and of a window
+    across the version change -- are compared with the oracle bit for bit on
+    head 0 (two heads run on the GPU)."""
+    wl = WL.STREAM
+    H, D, chunk, steps = 2, wl.head_dim, wl.chunk_tokens, 10
+    n = chunk * steps
+    S, G, C, T = wl.stages, wl.group_size, wl.clusters, wl.lloyd_iters
+    xb = np.stack([SY.mixture_unit(wl, 0, SY.K_TENSOR, h, 0, n) for h in range(H)])
+    cfg = qvg.config(H, D, C, T, S, G)
+    cache, bufs, dec, _ = run_stream(qvg, cfg, xb, chunk, steps, wl.refit_every)
+    assert cache.n_versions == 2
+    w0, w1 = 7 * chunk + 100, 9 * chunk + 50          # chunk 7 (version 0) .. chunk 9 (version 1)
+    win = torch.full((H, w1 - w0, D), -1, dtype=torch.int16, device="cuda")
+    qvg.qvg_decode_cache(cfg, cache, w0, w1, win, (w1 - w0) * D, D)
+    torch.cuda.synchronize()
+    win = u16(win)
+    codes = u32(bufs["codes"]).reshape(S, H, n, D // 16)
+    meta = u32(bufs["meta"]).reshape(S, H, n, D // G)
+    ids = bufs["ids"].cpu().numpy()[: H * n].reshape(H, n).astype(np.int32)
+    cents = u16(bufs["centroids"])[: 2 * H * C * D].reshape(2, H, C, D)
+    h = 0
+    vers, ov, oi, oc, om = oracle.stream(xb[h], chunk, steps, wl.refit_every, C, T, S, G)
+    assert list(ov) == [0] * 8 + [1] * 2
+    for v in range(2):
+        np.testing.assert_array_equal(cents[v, h], vers[v], err_msg=f"version {v}")
+    np.testing.assert_array_equal(ids[h], oi)
+    np.testing.assert_array_equal(codes[:, h], oc)
+    np.testing.assert_array_equal(meta[:, h], om)
+    want = np.concatenate([oracle.decode(oc[:, t * chunk:(t + 1) * chunk], om[:, t * chunk:(t + 1) * chunk],
+                                         oi[t * chunk:(t + 1) * chunk], vers[ov[t]], G) for t in range(steps)])
+    np.testing.assert_array_equal(dec[h], want)
+    np.testing.assert_array_equal(win[h], want[w0:w1])

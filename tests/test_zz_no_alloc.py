@@ -74,3 +74,32 @@ def test_static_scratch_rejects_oversized_calls(qvg):
     with pytest.raises(qvg.QvgError) as ei:
         qvg.coral_predict_encode_static(cfg, pred, dummy, dummy, N, dummy, dummy, dummy, None)
     assert ei.value.status == qvg.QVG_ERR_CAPACITY
+
+
+def test_static_scratch_encode_at_its_token_limit(qvg):
+    """At the cross-layer workload's own shape -- 16 heads of 128 channels and
+    16,384 tokens, the most the built-in scratch takes -- the allocation-free
+    encode still gives exactly what the workspace entry point gives, on two
+    layers in a row, and leaves the device error word clear."""
+    from synth import gpu as SG
+    wl = WL.CORAL
+    H, D, S, G, N = wl.heads, wl.head_dim, wl.stages, wl.group_size, wl.tokens
+    assert N == 16384
+    cfg = qvg.config(H, D, 0, 0, S, G)
+    xs = SG.coral_chain_gpu(wl, SY.V_TENSOR, n_layers=3)     # [3][N][H*D] bf16 bits, on the device
+    ws = qvg.alloc_workspace(cfg, N)
+    qvg.qvg_device_error(clear=True)
+    prev = xs[0]
+    for layer in (1, 2):
+        B, U, W = SG.coral_predictor_device(wl, layer - 1)
+        pred = qvg.qvg.coral_predictor(B=B.data_ptr(), U=U.data_ptr(), W=W.data_ptr(), rank=wl.rank)
+        ref = _outputs(cfg, N)
+        qvg.coral_predict_encode(cfg, pred, prev, xs[layer], N, ref[0], ref[1], ref[2], None, ws)
+        got = _outputs(cfg, N)
+        qvg.coral_predict_encode_static(cfg, pred, prev, xs[layer], N, got[0], got[1], got[2], None)
+        torch.cuda.synchronize()
+        assert torch.equal(got[0], ref[0]), f"codes, layer {layer}"
+        assert torch.equal(got[1], ref[1]), f"meta, layer {layer}"
+        assert torch.equal(got[2], ref[2]), f"reconstruction, layer {layer}"
+        prev = ref[2]
+    assert qvg.qvg_device_error() == (qvg.QVG_OK, 0)
