@@ -198,7 +198,10 @@ __global__ void __launch_bounds__(kLrThreads, 1)
 // --------------------------------------------------------------- predict
 
 constexpr int kPrStages = 2;
-constexpr int kPrThreads = 64 + 256;    // TMA warp, MMA warp, two groups of four epilogue warps
+// TMA warp, MMA warp, two groups of eight epilogue warps: in a group the two
+// warps on one TMEM lane quadrant take the two 64-channel halves of its rows
+constexpr int kPrEpi = 16;
+constexpr int kPrThreads = 64 + 32 * kPrEpi;
 constexpr int kResBytes = 3 * kSlab;    // resident per head: B_h (two slabs), [U_h | U_h]
 constexpr int kPrBars = 2 * kPrStages + 4 + 2;   // full, empty, tfull, tempty, block full / free
 
@@ -230,7 +233,7 @@ __device__ __forceinline__ uint4 ldg_v4_l1(const void* p) {
 // done).  A stage carries the item's x_hat tile and t2 -- and, in the encoder,
 // its x_{l+1} tile, which the epilogue reads from shared memory; the encoder's
 // stage is released by the MMAs and by the four epilogue warps that read it.
-template <int G, bool ENCODE, int SM>
+template <int G, bool ENCODE, int S>
 __global__ void __launch_bounds__(kPrThreads, 1)
     coral_predict_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_b,
                             const __grid_constant__ CUtensorMap tm_t, const __grid_constant__ CUtensorMap tm_u,
@@ -255,11 +258,11 @@ __global__ void __launch_bounds__(kPrThreads, 1)
     if (tid == 0) {
         for (int s = 0; s < kPrStages; ++s) {
             mbar_init(full_bar + 8 * s, 1);
-            mbar_init(empty_bar + 8 * s, ENCODE ? 1 + 4 : 1);
+            mbar_init(empty_bar + 8 * s, ENCODE ? 1 + kPrEpi / 2 : 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar + 8 * b, 1);
-            mbar_init(tempty_bar + 8 * b, 4);
+            mbar_init(tempty_bar + 8 * b, kPrEpi / 2);
         }
         mbar_init(bfull_bar, 1);
         mbar_init(bfree_bar, 1);
@@ -355,11 +358,15 @@ __global__ void __launch_bounds__(kPrThreads, 1)
         __syncwarp();
     } else {
         // ---------------------------------------------------- epilogue
-        constexpr int CPT = G < 32 ? 32 : G;      // channels per pass (whole groups, whole TMEM loads)
+        // A thread owns one token row's half: 64 channels = one TMEM lane,
+        // 64 accumulator columns; it works through them in passes of CPT.
+        constexpr int CPT = G < 32 ? 32 : G;      // channels per pass (whole groups)
         constexpr int GPP = CPT / G;              // groups per pass
-        constexpr int NP = kDh / CPT;             // passes per row
+        constexpr int HALF = kDh / 2;
+        constexpr int NP = HALF / CPT;            // passes per half row
         constexpr int WPR = kDh / 16, MPR = kDh / G;
-        const int e = warp - 2, g = e >> 2, q = warp & 3;
+        constexpr int WPH = HALF / 16, MPH = HALF / G > 0 ? HALF / G : 1;
+        const int e = warp - 2, g = e >> 3, hf = (e >> 2) & 1, q = warp & 3;
         const int row = q * 32 + lane;
         const int64_t stage_rows = (int64_t)H * a.n_tokens;
         for (int i = g; i < my_items; i += 2) {
@@ -367,23 +374,22 @@ __global__ void __launch_bounds__(kPrThreads, 1)
             const int h = item / a.tiles, tile = item % a.tiles;
             const int64_t n = (int64_t)tile * kT + row;
             const bool valid = n < a.n_tokens;
-            const int64_t elem0 = n * HD + (int64_t)h * kDh;
+            const int64_t elem0 = n * HD + (int64_t)h * kDh + hf * HALF;
             const int64_t rowoff = (int64_t)h * a.n_tokens + n;
             // The decoder's loads do not depend on the MMA: the codes and
-            // scale/zero words of the whole row are issued before waiting for it.
-            uint32_t code[ENCODE ? 1 : SM][WPR], meta[ENCODE ? 1 : SM][MPR];
+            // scale/zero words of the half row are issued before waiting for it.
+            uint32_t code[ENCODE ? 1 : S][WPH], meta[ENCODE ? 1 : S][MPH];
             if (!ENCODE) {
 #pragma unroll
-                for (int s = 0; s < SM; ++s) {
-                    const bool on = valid && s < a.S;
+                for (int s = 0; s < S; ++s) {
                     const int64_t srow = (int64_t)s * stage_rows + rowoff;
 #pragma unroll
-                    for (int w = 0; w < WPR; w += 4) {
-                        const uint4 cw = on ? ldg_v4_l1(a.codes + srow * WPR + w) : make_uint4(0, 0, 0, 0);
+                    for (int w = 0; w < WPH; w += 4) {
+                        const uint4 cw = valid ? ldg_v4_l1(a.codes + srow * WPR + hf * WPH + w) : make_uint4(0, 0, 0, 0);
                         code[s][w] = cw.x; code[s][w + 1] = cw.y; code[s][w + 2] = cw.z; code[s][w + 3] = cw.w;
                     }
 #pragma unroll
-                    for (int m = 0; m < MPR; ++m) meta[s][m] = on ? __ldg(a.meta + srow * MPR + m) : 0u;
+                    for (int m = 0; m < MPH; ++m) meta[s][m] = valid ? __ldg(a.meta + srow * MPR + hf * MPH + m) : 0u;
                 }
             }
             if (!mbar_wait(tfull_bar + 8 * g, (uint32_t)(i >> 1) & 1u)) { misc[1] = 1; break; }
@@ -391,114 +397,89 @@ __global__ void __launch_bounds__(kPrThreads, 1)
             // arrival too, so the copy's bytes are visible to these threads
             const int si = i % kPrStages;
             if (ENCODE && !mbar_wait(full_bar + 8 * si, (uint32_t)(i / kPrStages) & 1u)) { misc[1] = 1; break; }
-            // this thread's row of the x_{l+1} tile (two 128-byte-swizzled slabs)
-            const uint8_t* xrow = stages + (size_t)si * SB + 3 * kSlab + (size_t)row * 128;
+            // this thread's half row of the x_{l+1} tile: slab hf, 128-byte swizzled
+            const uint8_t* xrow = stages + (size_t)si * SB + (3 + hf) * kSlab + (size_t)row * 128;
             tc_fence_after();
-            // one pass of CPT channels
-            auto pass = [&](const int c) {
-                const uint32_t tcol = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)g * kDh + (uint32_t)(c * CPT);
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)g * kDh + (uint32_t)(hf * HALF);
+#pragma unroll
+            for (int c = 0; c < NP; ++c) {
+                const uint32_t tcol = tbase + (uint32_t)(c * CPT);
                 // the encoder's codes and scale/zero words of this pass
-                uint32_t ec[ENCODE ? SM : 1][CPT / 16], em[ENCODE ? SM : 1][GPP];
+                uint32_t ec[ENCODE ? S : 1][CPT / 16], em[ENCODE ? S : 1][GPP];
                 if (ENCODE) {
-                    // residual r = x_{l+1} - pred, quantised stage by stage
+                    // residual r = x_{l+1} - pred, 16 channels at a time
                     float r[CPT];
 #pragma unroll
-                    for (int k = 0; k < CPT / 32; ++k) {
-                        uint32_t v[32];
-                        tmem_ld32(tcol + 32u * k, v);
-                        uint4 xv[4];
+                    for (int k = 0; k < CPT / 16; ++k) {
+                        uint32_t v[16];
+                        tmem_ld16(tcol + 16u * k, v);
+                        // channel ch of the half sits in 16-byte chunk ch / 8 of the
+                        // row, stored at chunk position chunk ^ (row % 8)
+                        const int ch = c * CPT + 16 * k;
+                        const uint4 x0 = *reinterpret_cast<const uint4*>(xrow + ((((ch >> 3)) ^ (row & 7)) << 4));
+                        const uint4 x1 = *reinterpret_cast<const uint4*>(xrow + ((((ch >> 3) + 1) ^ (row & 7)) << 4));
+                        tmem_wait_ld_regs16(v);
+                        float pk[16];
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            // channel ch sits in slab ch / 64, 16-byte chunk (ch % 64) / 8 of the row,
-                            // stored at chunk position chunk ^ (row % 8)
-                            const int ch = c * CPT + 32 * k + 8 * u;
-                            xv[u] = *reinterpret_cast<const uint4*>(xrow + (ch >> 6) * kSlab +
-                                                                    ((((ch & 63) >> 3) ^ (row & 7)) << 4));
-                        }
-                        tmem_wait_ld();
-                        float pk[32];
-#pragma unroll
-                        for (int jj = 0; jj < 32; ++jj) pk[jj] = __uint_as_float(v[jj]);
+                        for (int jj = 0; jj < 16; ++jj) pk[jj] = __uint_as_float(v[jj]);
                         if (valid && a.pred_out) {
 #pragma unroll
-                            for (int jj = 0; jj < 32; jj += 4)
-                                *reinterpret_cast<float4*>(a.pred_out + elem0 + c * CPT + 32 * k + jj) =
+                            for (int jj = 0; jj < 16; jj += 4)
+                                *reinterpret_cast<float4*>(a.pred_out + elem0 + c * CPT + 16 * k + jj) =
                                     make_float4(pk[jj], pk[jj + 1], pk[jj + 2], pk[jj + 3]);
                         }
-                        unpack16(xv[0], xv[1], r + 32 * k);
-                        unpack16(xv[2], xv[3], r + 32 * k + 16);
-                        sub16(r + 32 * k, pk);
-                        sub16(r + 32 * k + 16, pk + 16);
+                        unpack16(x0, x1, r + 16 * k);
+                        sub16(r + 16 * k, pk);
                     }
-#pragma unroll 1
-                    for (int s = 0; s < a.S; ++s) {
+#pragma unroll
+                    for (int s = 0; s < S; ++s) {
 #pragma unroll
                         for (int gi = 0; gi < GPP; ++gi) {
                             uint32_t cw[G / 16], m;
-                            quant_stage<G, 1>(r + gi * G, s + 1 < a.S, nullptr, cw, m);
+                            quant_stage<G, 1>(r + gi * G, s + 1 < S, nullptr, cw, m);
 #pragma unroll
                             for (int w = 0; w < G / 16; ++w) ec[s][(gi * G) / 16 + w] = cw[w];
                             em[s][gi] = m;
-                            if (valid) {
-                                const int64_t srow = (int64_t)s * stage_rows + rowoff;
-                                uint32_t* cp = a.codes + srow * WPR + (c * CPT + gi * G) / 16;
+                        }
+                        if (valid) {
+                            const int64_t srow = (int64_t)s * stage_rows + rowoff;
+                            uint32_t* cp = a.codes + srow * WPR + (hf * HALF + c * CPT) / 16;
+                            if constexpr (CPT / 16 == 4) *reinterpret_cast<uint4*>(cp) = make_uint4(ec[s][0], ec[s][1], ec[s][2], ec[s][3]);
+                            else *reinterpret_cast<uint2*>(cp) = make_uint2(ec[s][0], ec[s][1]);
 #pragma unroll
-                                for (int w = 0; w < G / 16; ++w) cp[w] = cw[w];
-                                a.meta[srow * MPR + c * GPP + gi] = m;
-                            }
+                            for (int gi = 0; gi < GPP; ++gi) a.meta[srow * MPR + (hf * HALF + c * CPT) / G + gi] = em[s][gi];
                         }
                     }
                 }
                 // x_hat = ((pred + d_1) + d_2) + ..., identical in encoder and decoder
-                float acc[CPT];
 #pragma unroll
-                for (int k = 0; k < CPT / 32; ++k) {
-                    uint32_t v[32];
-                    tmem_ld32(tcol + 32u * k, v);
-                    tmem_wait_ld();
+                for (int k = 0; k < CPT / 16; ++k) {
+                    uint32_t v[16];
+                    tmem_ld16(tcol + 16u * k, v);
+                    tmem_wait_ld_regs16(v);
+                    float acc[16];
 #pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) acc[32 * k + jj] = __uint_as_float(v[jj]);
-                }
-                if (!ENCODE && valid && a.pred_out) {
+                    for (int jj = 0; jj < 16; ++jj) acc[jj] = __uint_as_float(v[jj]);
+                    const int ch = c * CPT + 16 * k;                 // channel within the half
+                    if (!ENCODE && valid && a.pred_out) {
 #pragma unroll
-                    for (int jj = 0; jj < CPT; jj += 4)
-                        *reinterpret_cast<float4*>(a.pred_out + elem0 + c * CPT + jj) =
-                            make_float4(acc[jj], acc[jj + 1], acc[jj + 2], acc[jj + 3]);
-                }
-                if constexpr (ENCODE) {
-#pragma unroll 1
-                    for (int s = 0; s < a.S; ++s) {
-#pragma unroll
-                        for (int w = 0; w < CPT / 16; ++w) dequant_add16(acc + 16 * w, ec[s][w], em[s][(16 * w) / G]);
+                        for (int jj = 0; jj < 16; jj += 4)
+                            *reinterpret_cast<float4*>(a.pred_out + elem0 + ch + jj) =
+                                make_float4(acc[jj], acc[jj + 1], acc[jj + 2], acc[jj + 3]);
                     }
-                } else {
 #pragma unroll
-                    for (int s = 0; s < SM; ++s) {
-                        if (s >= a.S) break;
-#pragma unroll
-                        for (int w = 0; w < CPT / 16; ++w)
-                            dequant_add16(acc + 16 * w, code[s][(c * CPT) / 16 + w], meta[s][(c * CPT + 16 * w) / G]);
+                    for (int s = 0; s < S; ++s) {
+                        if constexpr (ENCODE) dequant_add16(acc, ec[s][(16 * k) / 16], em[s][(16 * k) / G]);
+                        else dequant_add16(acc, code[s][ch / 16], meta[s][ch / G]);
                     }
-                }
-                if (valid) {
-                    uint16_t* op = a.xhat + elem0 + c * CPT;
-#pragma unroll
-                    for (int k = 0; k < CPT; k += 16) {
+                    if (valid) {
                         uint4 o0, o1;
-                        pack16_bf16(acc + k, o0, o1);
-                        *reinterpret_cast<uint4*>(op + k) = o0;
-                        *reinterpret_cast<uint4*>(op + k + 8) = o1;
+                        pack16_bf16(acc, o0, o1);
+                        uint16_t* op = a.xhat + elem0 + ch;
+                        *reinterpret_cast<uint4*>(op) = o0;
+                        *reinterpret_cast<uint4*>(op + 8) = o1;
                     }
                 }
-            };
-            if constexpr (ENCODE) {
-                // rolled: a pass's residual and codes are all the encoder keeps
-#pragma unroll 1
-                for (int c = 0; c < NP; ++c) pass(c);
-            } else {
-                // unrolled: the prefetched codes are indexed with constants
-#pragma unroll
-                for (int c = 0; c < NP; ++c) pass(c);
             }
             // accumulator drained (and, in the encoder, the stage's x_{l+1} read)
             tc_fence_before();
@@ -565,9 +546,15 @@ cudaError_t coral_tc_g(bool encode, const CoralArgs& a, const CoralTcScratch& w,
     if (e != cudaSuccess) return e;
     const int tiles = (int)((N + kT - 1) / kT);
     const size_t pr_smem = (size_t)kResBytes + (size_t)kPrStages * pr_stage_bytes(encode) + 8 * kPrBars + 32 + 1024;
-    // SM: stages held in registers by the epilogue (2, or 4 when S > 2)
-    auto kern = a.S <= 2 ? (encode ? coral_predict_tc_kernel<G, true, 2> : coral_predict_tc_kernel<G, false, 2>)
-                         : (encode ? coral_predict_tc_kernel<G, true, 4> : coral_predict_tc_kernel<G, false, 4>);
+    // the stage count is a template parameter: the epilogue's stage loops unroll
+    auto kern = encode ? coral_predict_tc_kernel<G, true, 2> : coral_predict_tc_kernel<G, false, 2>;
+    switch (a.S) {
+        case 1: kern = encode ? coral_predict_tc_kernel<G, true, 1> : coral_predict_tc_kernel<G, false, 1>; break;
+        case 2: break;
+        case 3: kern = encode ? coral_predict_tc_kernel<G, true, 3> : coral_predict_tc_kernel<G, false, 3>; break;
+        case 4: kern = encode ? coral_predict_tc_kernel<G, true, 4> : coral_predict_tc_kernel<G, false, 4>; break;
+        default: return cudaSuccess;
+    }
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pr_smem);
     if (e != cudaSuccess) return e;
     PrArgs pa;
