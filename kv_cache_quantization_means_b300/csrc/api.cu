@@ -82,16 +82,15 @@ qvg_status check_rows(int64_t cap, int64_t off, int64_t n) {
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 struct FitWorkspace {
-    int* counts;        // [H][C]
-    int* first_piece;   // [H][C]
-    int* npieces;       // [H]
-    int* perm;          // [H][N]
-    int4* pieces;       // [H][max_pieces]
-    void* partials;     // [H][max_pieces][D] 16-byte exact sums
     unsigned long long* stats;  // [4]
-    int* blockhist;     // [H][n_blocks][C]
     float* xnorm;       // [H][N] ||x||^2 per token, shared by a fit's assign steps
-    int max_pieces, n_blocks;
+    long long* ksum;    // [H][C][3][D] exact window sums of each cluster's members
+    int* kcount;        // [H][C]
+    int* kbig;          // [H][C]
+    int* chg_tok;       // [H][chg_stride] ids changed by the last assign
+    uint16_t* chg_on;   // [H][chg_stride]
+    int2* chg_parts;    // [H][kChgParts]
+    int64_t chg_stride; // head stride of chg_tok / chg_on
     size_t bytes;
 };
 
@@ -99,23 +98,21 @@ FitWorkspace carve(const qvg_config* c, int64_t n, void* base) {
     const size_t H = c->num_heads, C = c->num_clusters > 0 ? c->num_clusters : 1, D = c->head_dim;
     const size_t N = (size_t)(n > 0 ? n : 1);
     FitWorkspace w{};
-    w.max_pieces = (int)((N + qvg::kPieceTokens - 1) / qvg::kPieceTokens + C);
     size_t o = 0;
     auto take = [&](size_t bytes) {
         size_t at = o;
         o += align256(bytes);
         return base ? (void*)((char*)base + at) : nullptr;
     };
-    w.counts = (int*)take(sizeof(int) * H * C);
-    w.first_piece = (int*)take(sizeof(int) * H * C);
-    w.npieces = (int*)take(sizeof(int) * H);
-    w.perm = (int*)take(sizeof(int) * H * N);
-    w.pieces = (int4*)take(sizeof(int4) * H * (size_t)w.max_pieces);
-    w.partials = take((size_t)16 * H * (size_t)w.max_pieces * D);
     w.stats = (unsigned long long*)take(sizeof(unsigned long long) * 4);
-    w.n_blocks = (int)((N + qvg::kSortBlock - 1) / qvg::kSortBlock);
-    w.blockhist = (int*)take(sizeof(int) * H * (size_t)w.n_blocks * C);
     w.xnorm = (float*)take(sizeof(float) * H * N);
+    w.ksum = (long long*)take(sizeof(long long) * H * C * 3 * D);
+    w.kcount = (int*)take(sizeof(int) * H * C);
+    w.kbig = (int*)take(sizeof(int) * H * C);
+    w.chg_stride = (int64_t)((N + 7) / 8 * 8);
+    w.chg_tok = (int*)take(sizeof(int) * H * (size_t)w.chg_stride);
+    w.chg_on = (uint16_t*)take(sizeof(uint16_t) * H * (size_t)w.chg_stride);
+    w.chg_parts = (int2*)take(sizeof(int2) * H * qvg::kChgParts);
     w.bytes = o;
     return w;
 }
@@ -155,40 +152,53 @@ qvg::AssignArgs assign_args(const qvg_config* c, const qvg_bf16* x, int64_t n, i
     a.err = stats ? reinterpret_cast<uint32_t*>(stats + 3) : nullptr;
     a.xnorm = nullptr;
     a.xnorm_mode = qvg::kNormCompute;
+    a.chg_tok = nullptr; a.chg_on = nullptr; a.chg_parts = nullptr; a.chg_stride = 0;
     return a;
 }
 
 qvg::UpdateArgs update_args(const qvg_config* c, const qvg_bf16* x, int64_t n, int64_t hs, int64_t ts,
-                            const uint8_t* ids, int64_t cap, int64_t off, const FitWorkspace& w,
-                            qvg_bf16* cent) {
+                            const uint8_t* ids, int64_t cap, int64_t off, const FitWorkspace& w, qvg_bf16* cent) {
     qvg::UpdateArgs u;
     u.x = x; u.head_stride = hs; u.token_stride = ts; u.n_tokens = n;
     u.ids = ids; u.cap = cap; u.tok_offset = off;
     u.H = c->num_heads; u.C = c->num_clusters;
-    u.max_pieces = w.max_pieces;
-    u.n_blocks = w.n_blocks; u.blockhist = w.blockhist;
-    u.counts = w.counts; u.first_piece = w.first_piece; u.npieces = w.npieces;
-    u.perm = w.perm; u.pieces = w.pieces; u.partials = w.partials; u.cent = cent;
+    u.group_log2 = -1;
+    u.cent = cent;
+    u.ksum = w.ksum; u.kcount = w.kcount; u.kbig = w.kbig;
+    u.chg_tok = w.chg_tok; u.chg_on = w.chg_on; u.chg_parts = w.chg_parts; u.chg_stride = w.chg_stride;
+    u.mode = qvg::kUpdFull;
     return u;
 }
 
-// T Lloyd iterations (init already in `cent`).
+// T Lloyd iterations (init already in `cent`).  The first update sums every
+// cluster; each later one applies only the ids that the assign before it
+// changed, to the exact sums the previous update stored in the workspace.
 qvg_status lloyd(const qvg_config* c, const qvg_bf16* x, int64_t n, int64_t hs, int64_t ts,
                  qvg_bf16* cent, uint8_t* ids, int64_t cap, int64_t off, const FitWorkspace& w,
                  cudaStream_t s, bool clear_stats = true) {
     cudaError_t e = cudaSuccess;
     if (clear_stats && (e = cudaMemsetAsync(w.stats, 0, sizeof(unsigned long long) * 4, s)) != cudaSuccess)
         return cuda_status(e, "memset");
+    bool have_sums = false;    // the workspace holds the exact sums of the current ids
     for (int t = 0; t < c->lloyd_iters; ++t) {
         // x is the same in every step: the first assign stores ||x||^2 per
         // token, the later ones read it
         qvg::AssignArgs aa = assign_args(c, x, n, hs, ts, cent, ids, cap, off, nullptr, w.stats);
         aa.xnorm = w.xnorm;
         aa.xnorm_mode = t == 0 ? qvg::kNormStore : qvg::kNormLoad;
-        e = qvg::launch_assign(c->head_dim, c->num_heads, aa, s);
+        if (have_sums) {
+            if ((e = cudaMemsetAsync(w.chg_parts, 0, sizeof(int2) * c->num_heads * qvg::kChgParts, s)) != cudaSuccess)
+                return cuda_status(e, "memset");
+            aa.chg_tok = w.chg_tok; aa.chg_on = w.chg_on; aa.chg_parts = w.chg_parts; aa.chg_stride = w.chg_stride;
+        }
+        bool recorded = false;
+        e = qvg::launch_assign(c->head_dim, c->num_heads, aa, s, &recorded);
         if (e != cudaSuccess) return cuda_status(e, "assign launch");
-        e = qvg::launch_update(c->head_dim, update_args(c, x, n, hs, ts, ids, cap, off, w, cent), s);
+        qvg::UpdateArgs u = update_args(c, x, n, hs, ts, ids, cap, off, w, cent);
+        u.mode = have_sums && recorded ? qvg::kUpdIncremental : qvg::kUpdFull;
+        e = qvg::launch_update(c->head_dim, u, s);
         if (e != cudaSuccess) return cuda_status(e, "update launch");
+        have_sums = true;
     }
     return ok();
 }
@@ -331,8 +341,7 @@ qvg_status qvg_update(const qvg_config* cfg, const qvg_bf16* x, int64_t n_tokens
     FitWorkspace w;
     if ((st = check_workspace(cfg, n_tokens, workspace, workspace_bytes, &w))) return st;
     cudaStream_t s = (cudaStream_t)stream;
-    qvg::UpdateArgs u = update_args(cfg, x, n_tokens, head_stride, token_stride, ids, capacity, tok_offset, w,
-                                    centroids);
+    qvg::UpdateArgs u = update_args(cfg, x, n_tokens, head_stride, token_stride, ids, capacity, tok_offset, w, centroids);
     cudaError_t e = qvg::launch_update(cfg->head_dim, u, s);
     return cuda_status(e, "update launch");
 }

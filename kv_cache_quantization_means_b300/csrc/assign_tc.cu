@@ -77,6 +77,10 @@ struct TcArgs {
     uint32_t* err;               // or null
     float* xnorm;                // [H][n_tokens] ||x||^2, or null
     int xnorm_mode;              // kNormCompute / kNormStore / kNormLoad
+    int* chg_tok;                // changed ids: tokens, (old | new << 8), (start, count) per CTA; or null
+    uint16_t* chg_on;
+    int2* chg_parts;
+    int64_t chg_stride;
 };
 
 // ----------------------------------------------------- shared memory map
@@ -302,6 +306,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         misc[1] = 0;
         misc[2] = 0;
         misc[3] = 0;
+        misc[4] = 0;              // changed ids recorded
         fence_mbar_init();
     }
     __syncthreads();
@@ -457,6 +462,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // a stored ||x||^2 is fetched before the waits
             const bool load_norm = a.xnorm_mode == kNormLoad;
             const float xnt_in = load_norm && valid ? __ldg(a.xnorm + (int64_t)h * a.n_tokens + tok) : 0.0f;
+            // so is the row's previous id, when changes are recorded
+            const uint32_t old_id = a.chg_parts && valid ? a.ids[(int64_t)h * a.cap + a.tok_offset + tok] : 0u;
             const bool ok = mbar_wait(tfull_bar + 8 * g, aph) && mbar_wait(full_bar + 8 * st, ph);
             const uint8_t* xs = Xs + (size_t)st * nA * kAtomBytes;
             const uint32_t taddr =
@@ -561,6 +568,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 cnt += __popc(m[w]);
             }
             uint8_t* idrow = a.ids + (int64_t)h * a.cap + a.tok_offset;
+            if (a.chg_parts) {
+                // record the decided rows whose id changes: slots of the CTA's
+                // range, one run per warp from a shared counter
+                const bool dec = valid && cnt == 1 && hf == 0;
+                const uint32_t old = old_id;
+                const bool chg = dec && old != (uint32_t)first;
+                const unsigned bal = __ballot_sync(0xffffffffu, chg);
+                if (bal) {
+                    const int lead = __ffs(bal) - 1;
+                    int base = 0;
+                    if (lane == lead) base = (int)atomicAdd(misc + 4, (uint32_t)__popc(bal));
+                    base = __shfl_sync(0xffffffffu, base, lead);
+                    if (chg) {
+                        const int64_t at = (int64_t)h * a.chg_stride + (int64_t)t_begin * kTile + base +
+                                           __popc(bal & ((1u << lane) - 1u));
+                        a.chg_tok[at] = (int)tok;
+                        a.chg_on[at] = (uint16_t)(old | ((uint32_t)first << 8));
+                    }
+                }
+            }
             if (valid && cnt == 1 && hf == 0) idrow[tok] = (uint8_t)first;
             // undecided rows of the pair, alternately to the two halves, one at
             // a time with all lanes on the row
@@ -569,6 +596,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if ((k & 1) != hf) continue;
                 const int src = __ffs(und) - 1;
                 const int r = q * 32 + src;
+                const uint32_t old_r = __shfl_sync(0xffffffffu, old_id, src);
                 uint32_t mr[NW];
 #pragma unroll
                 for (int w = 0; w < NW; ++w) mr[w] = __shfl_sync(0xffffffffu, m[w], src);
@@ -596,7 +624,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     best = rerank_exact<D, CP>(xs, r, Bs, cslab, lane, mr, sb, myj, ncand, dmin, emin, n_seq);
                     ++n_exact;
                 }
-                if (lane == 0 && best >= 0) idrow[(int64_t)(t_begin + i) * kTile + r] = (uint8_t)best;
+                if (lane == 0 && best >= 0) {
+                    const int64_t rt = (int64_t)(t_begin + i) * kTile + r;
+                    if (a.chg_parts) {
+                        const uint32_t old = old_r;
+                        if (old != (uint32_t)best) {
+                            const int64_t at = (int64_t)h * a.chg_stride + (int64_t)t_begin * kTile + atomicAdd(misc + 4, 1u);
+                            a.chg_tok[at] = (int)rt;
+                            a.chg_on[at] = (uint16_t)(old | ((uint32_t)best << 8));
+                        }
+                    }
+                    idrow[rt] = (uint8_t)best;
+                }
                 ++n_flag;
             }
             // the token tile is no longer read by this warp
@@ -614,6 +653,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_before();
     __syncthreads();
     if (tid == 0 && (misc[1] | misc[3]) && a.err) atomicExch(a.err, kErrTimeout);
+    if (tid == 0 && a.chg_parts) a.chg_parts[(int64_t)h * kChgParts + part] = make_int2(t_begin * kTile, (int)misc[4]);
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(alloc_cols) : "memory");
@@ -674,6 +714,8 @@ cudaError_t assign_tc_d(int H, const AssignArgs& a, bool* launched, cudaStream_t
     t.err = a.err;
     t.xnorm = a.xnorm;
     t.xnorm_mode = a.xnorm ? a.xnorm_mode : kNormCompute;
+    t.chg_tok = a.chg_tok; t.chg_on = a.chg_on; t.chg_parts = a.chg_parts; t.chg_stride = a.chg_stride;
+    if (a.chg_parts && t.ctas_per_head > kChgParts) t.ctas_per_head = kChgParts;   // one record range per CTA
     // as many token stages (up to four) as fit in shared memory, at least two
     t.stages = kMaxStages;
     Layout L = make_layout(D, t.Cpad, t.stages);

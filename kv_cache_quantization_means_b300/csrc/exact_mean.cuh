@@ -139,4 +139,32 @@ __device__ __forceinline__ uint16_t mean_bf16_bits(i128 I, uint32_t cnt) {
     return (uint16_t)(bits | (neg ? 0x8000u : 0u));
 }
 
+// The same result, taken from the fp32 estimate alone when no bf16 rounding
+// midpoint can lie between it and q.  The estimate U' / cnt with U' = U >> sh
+// (24 significant bits) is within 2^-22 of q relative (truncation < 2^-23,
+// the correctly rounded quotient 2^-24; cnt < 2^24 is exact in fp32), that is
+// within 4 units in the last place of the estimate qf.  The bits of qf below
+// the bf16 mantissa (r) are at least 16 units from the midpoint 0x8000, so q,
+// RN_f64(q) and qf lie on the same side of every midpoint and round to the
+// same bf16 value; the rounding carries into the exponent where it must
+// (also when qf and q lie on either side of a power of two).  Otherwise, and
+// near the ends of the bf16 range, the exact comparisons decide.
+__device__ __forceinline__ uint16_t mean_bf16_bits_fast(i128 I, uint32_t cnt) {
+    if (I == 0) return 0;
+    const bool neg = I < 0;
+    const u128 U = neg ? (u128)(-I) : (u128)I;
+    const int bl = 128 - clz128(U);
+    const int sh = bl > 24 ? bl - 24 : 0;
+    const float qf = __fdiv_rn((float)(uint32_t)(U >> sh), (float)cnt);
+    const uint32_t b = __float_as_uint(qf);
+    const uint32_t r = b & 0xFFFFu;
+    const int e = (int)(b >> 23) - 127 + sh - 52;           // q ~ 1.m * 2^e
+    if (cnt < (1u << 24) && (r > 0x8000u + 16u || r + 16u < 0x8000u) && e > -126 && e < 126) {
+        uint32_t bits = ((uint32_t)(e + 127) << 7) | ((b >> 16) & 0x7Fu);
+        if (r > 0x8000u) ++bits;
+        return (uint16_t)(bits | (neg ? 0x8000u : 0u));
+    }
+    return mean_bf16_bits(I, cnt);
+}
+
 }  // namespace qvg

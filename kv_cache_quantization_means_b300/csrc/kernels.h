@@ -48,28 +48,44 @@ struct AssignArgs {
     // reads what an earlier kNormStore call wrote for the same x.
     float* xnorm;
     int xnorm_mode;
+    // ids that this assign changes, recorded when chg_parts is not null (the
+    // tensor-core path only).  Each CTA records the rows of its token range
+    // [start, start + ...) in that range of chg_tok (token) and chg_on (old
+    // id | new id << 8), [H][chg_stride] each, and sets chg_parts[h][part] =
+    // (start, count); the caller zeroes chg_parts ([H][kChgParts]) first.
+    int* chg_tok;
+    uint16_t* chg_on;
+    int2* chg_parts;
+    int64_t chg_stride;     // head stride of chg_tok / chg_on: n_tokens rounded up to a multiple of 8
 };
+constexpr int kChgParts = 160;   // token ranges (assign CTAs) per head, at most
 constexpr int kNormCompute = 0, kNormStore = 1, kNormLoad = 2;
 
-constexpr int kPieceTokens = 64;   // tokens per exact partial sum of the update
-constexpr int kSortBlock = 1024;   // tokens per block of the update's counting sort
+constexpr int kUpdFull = 0, kUpdIncremental = 1;
 
 struct UpdateArgs {
     const uint16_t* x;
     int64_t head_stride, token_stride, n_tokens;
-    const uint8_t* ids;
+    const uint8_t* ids;     // [H][cap], rows tok_offset..; an id >= C is in no cluster
     int64_t cap, tok_offset;
     int H, C;
-    int max_pieces;         // per head: ceil(n_tokens / kPieceTokens) + C
-    int n_blocks;           // per head: ceil(n_tokens / kSortBlock) sort blocks
-    int* blockhist;         // [H][n_blocks][C] ids per cluster and sort block
-    int* counts;            // [H][C] tokens per cluster
-    int* first_piece;       // [H][C] index of the cluster's first piece
-    int* npieces;           // [H]
-    int* perm;              // [H][n_tokens] token indices sorted by cluster
-    int4* pieces;           // [H][max_pieces]: first sorted position, length, cluster, only piece?
-    void* partials;         // [H][max_pieces][D] exact 128-bit sums (units 2^-52)
+    int group_log2;         // clusters per CTA = 2^group_log2 (<= 16), or -1: chosen from H, C and n_tokens
     uint16_t* cent;         // [H][C][D] in/out
+    // Exact state that one update leaves for the next: per cluster the
+    // fixed-point window sums of its members ([H][C][3][D]) and their count,
+    // and per group of clusters a flag that its window sums are not valid (a
+    // member value of magnitude >= 2^14).  kUpdFull recomputes and stores
+    // all of it; kUpdIncremental applies the changes an assign recorded since
+    // the previous update (AssignArgs::chg_*), then rounds the means of the
+    // clusters those changes touched.
+    long long* ksum;
+    int* kcount;
+    int* kbig;              // [H][C] (groups of a head use its first entries)
+    const int* chg_tok;     // [H][chg_stride]
+    const uint16_t* chg_on; // [H][chg_stride]
+    const int2* chg_parts;  // [H][kChgParts]
+    int64_t chg_stride;
+    int mode;
 };
 
 struct CoralArgs {
@@ -121,7 +137,9 @@ cudaError_t set_codec_debug(unsigned long long wait_limit_ns, uint32_t flags, cu
 cudaError_t launch_kmeans_init(int D, const uint16_t* x, int64_t head_stride, int64_t token_stride,
                                int64_t n_tokens, const uint16_t* warm, int H, int C, uint16_t* cent,
                                cudaStream_t s);
-cudaError_t launch_assign(int D, int H, const AssignArgs& a, cudaStream_t s);
+// *recorded (if not null) says whether the launched kernel records id
+// changes (AssignArgs::chg_parts).
+cudaError_t launch_assign(int D, int H, const AssignArgs& a, cudaStream_t s, bool* recorded = nullptr);
 // tcgen05 assign; sets *launched = false (and returns cudaSuccess) when the
 // shape or layout is outside what it handles, so the caller can fall back.
 cudaError_t launch_assign_tc(int D, int H, const AssignArgs& a, bool* launched, cudaStream_t s);

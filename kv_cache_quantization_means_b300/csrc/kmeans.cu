@@ -357,258 +357,458 @@ __global__ void kmeans_init_kernel(const uint16_t* x, int64_t head_stride, int64
 
 // ------------------------------------------------------------- update ---
 //
-// 1. sort: per block of kSortBlock tokens a histogram of ids, then a stable
-//    counting sort of the tokens by cluster (perm), the cluster sizes and a
-//    table of pieces: runs of at most kPieceTokens sorted positions of one
-//    cluster.  Offsets come from the block histograms in a fixed order and
-//    ranks from __match_any_sync, so neither the counts nor the order depend
-//    on scheduling.
-// 2. sum: one warp per piece gathers its rows and forms their exact sum
-//    (fixed-point windows); the only piece of a cluster is turned into the
-//    centroid directly, other pieces store their exact partial.
-// 3. mean: clusters with several pieces add their partials in piece order
-//    and round the mean.  Integer sums make the result independent of any
-//    order; no atomic operation is used.
+// One CTA per (head, group of 2^k consecutive clusters), one launch per
+// update.  Cluster sums are exact integers (three fixed-point windows per
+// value), so they do not depend on the order in which tokens are listed or
+// added, and shared-memory atomics may place and add them in any order.
+//
+// Full update: the CTA finds its clusters' tokens in the id array itself --
+// one scan counts them and lists their token indices in shared memory in
+// arrival order, and a counting sort in shared memory groups that list by
+// cluster.  Each unit of D/8 lanes takes a contiguous run of the sorted list,
+// gathers those rows and adds them into per-lane windows, which it flushes
+// into the cluster's shared sums when its run reaches the next cluster.  The
+// sums and counts are stored for the next update, and the means rounded.  A
+// group whose tokens overflow the list is taken in token segments (a
+// counting scan and a placing scan each); a group holding a value of
+// magnitude >= 2^14 is summed again with 128-bit integers and marked, so that
+// its next update is a full one too.
+//
+// Incremental update: the stored sums already hold the members under the
+// previous ids, and the assign in between recorded the ids it changed.  The
+// CTA lists the changes that touch its clusters (a token leaving is
+// subtracted from the old cluster, one arriving added to the new), sums those
+// rows the same way, adds the result to the stored sums and counts, and
+// rounds again the means of the clusters that changed; the others keep their
+// centroid, which is already the mean of the same members.  A changed row
+// with a value of magnitude >= 2^14 sends the group to a full update.
 
-constexpr int kSortWarps = kThreads / 32;
-constexpr int kSortPerWarp = kSortBlock / kSortWarps;
+constexpr int kUpdThreads = 256;
+constexpr int kListCap = 4096;                         // rows listed at once
+constexpr int kMaxGroup = 16;                          // clusters per CTA
+constexpr int kFlushTerms = 255;                       // window terms a lane adds between flushes (|sum| < 2^30)
+constexpr int64_t kPackLimit = (int64_t)1 << 26;       // token index packed above a 5-bit bucket
+constexpr int kMaxGroupChannels = 1024;                // G * D: the group's int64 sums fit over the two lists
+static_assert(3 * kMaxGroupChannels * 8 <= 2 * 4 * kListCap, "sums copy over the lists");
+static_assert(kChgParts % 32 == 0, "change ranges are scanned 32 lanes wide");
 
-// Exclusive scan of v over threads 0..kMaxClusters-1 of a 256-thread block;
-// returns the prefix, *total receives the sum.
-__device__ __forceinline__ int block_scan256(int v, int* warp_tot, int* total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int inc = v;
+// Calls f(i, byte) for the bytes i in [t0, t1) of p whose value v has
+// (v & keep) == want: 16-byte loads in the aligned middle, four bytes per
+// word tested at once (a byte of (w & mask) ^ want is zero exactly for a
+// member).
+template <class F>
+__device__ __forceinline__ void for_matching_bytes(const uint8_t* p, int64_t t0, int64_t t1, uint32_t keep,
+                                                   uint32_t want, F&& f) {
+    const uint32_t mask4 = keep * 0x01010101u, want4 = want * 0x01010101u;
+    auto one = [&](int64_t n, uint32_t v) {
+        if ((v & keep) == want) f(n, v);
+    };
+    const uint8_t* p0 = p + t0;
+    int64_t pre = (int64_t)((16u - ((uint32_t)(uintptr_t)p0 & 15u)) & 15u);
+    if (pre > t1 - t0) pre = t1 - t0;
+    const int64_t body = (t1 - t0 - pre) >> 4;
+    for (int64_t i = threadIdx.x; i < pre; i += kUpdThreads) one(t0 + i, p0[i]);
+    const uint4* pb = reinterpret_cast<const uint4*>(p0 + pre);
+    for (int64_t i0 = threadIdx.x; i0 < body; i0 += 4 * kUpdThreads) {
+        uint4 v[4];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int u = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += u;
-    }
-    if (lane == 31) warp_tot[warp] = inc;
-    __syncthreads();
-    int before = 0, all = 0;
-    for (int w = 0; w < kThreads / 32; ++w) {
-        if (w < warp) before += warp_tot[w];
-        all += warp_tot[w];
-    }
-    __syncthreads();
-    *total = all;
-    return before + inc - v;
-}
-
-// Histogram of the ids of one block of kSortBlock tokens.
-__global__ void __launch_bounds__(kThreads) kmeans_hist_kernel(UpdateArgs a) {
-    __shared__ int hist[kMaxClusters];
-    const int h = blockIdx.y, b = blockIdx.x, C = a.C;
-    for (int j = threadIdx.x; j < kMaxClusters; j += kThreads) hist[j] = 0;
-    __syncthreads();
-    const uint8_t* idh = a.ids + (int64_t)h * a.cap + a.tok_offset;
-    const int64_t n0 = (int64_t)b * kSortBlock, n1 = min(n0 + kSortBlock, a.n_tokens);
-    for (int64_t n = n0 + threadIdx.x; n < n1; n += kThreads) atomicAdd(&hist[min((int)idh[n], C - 1)], 1);
-    __syncthreads();
-    int* bh = a.blockhist + ((int64_t)h * a.n_blocks + b) * C;
-    for (int j = threadIdx.x; j < C; j += kThreads) bh[j] = hist[j];
-}
-
-// Stable counting sort, one block of kSortBlock tokens per CTA: the block's
-// first position for cluster j is (tokens of clusters < j) + (tokens of j in
-// earlier blocks), both from the block histograms in a fixed order; inside the
-// block, warp w's slice follows warps < w and a warp ranks equal ids with
-// __match_any_sync.  Block 0 of each head also writes the counts and the
-// table of pieces.
-__global__ void __launch_bounds__(kThreads) kmeans_scatter_kernel(UpdateArgs a) {
-    __shared__ int cur[kSortWarps][kMaxClusters];
-    __shared__ int warp_tot[kThreads / 32];
-    __shared__ __align__(16) uint8_t ids_s[kSortBlock];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int h = blockIdx.y, b = blockIdx.x, C = a.C;
-    const uint8_t* idh = a.ids + (int64_t)h * a.cap + a.tok_offset;
-    const int64_t n0 = (int64_t)b * kSortBlock;
-    const int nb = (int)min((int64_t)kSortBlock, a.n_tokens - n0);
-    for (int i = tid; i < nb; i += kThreads) ids_s[i] = idh[n0 + i];
-    for (int i = tid; i < kSortWarps * kMaxClusters; i += kThreads) (&cur[0][0])[i] = 0;
-    // totals and the part before this block, per cluster (thread j)
-    const int* bh = a.blockhist + (int64_t)h * a.n_blocks * C;
-    int total = 0, before = 0;
-    if (tid < C)
-        for (int bb = 0; bb < a.n_blocks; ++bb) {
-            const int v = bh[(int64_t)bb * C + tid];
-            total += v;
-            if (bb < b) before += v;
-        }
-    int all;
-    const int off = block_scan256(tid < C ? total : 0, warp_tot, &all);   // also syncs ids_s / cur
-    const int np = (total + kPieceTokens - 1) / kPieceTokens;
-    int np_all;
-    const int pfirst = block_scan256(tid < C ? np : 0, warp_tot, &np_all);
-    if (b == 0 && tid < C) {
-        a.counts[(int64_t)h * C + tid] = total;
-        a.first_piece[(int64_t)h * C + tid] = pfirst;
-        int4* ph = a.pieces + (int64_t)h * a.max_pieces;
-        for (int p = 0; p < np; ++p)
-            ph[pfirst + p] = make_int4(off + p * kPieceTokens, min(kPieceTokens, total - p * kPieceTokens), tid,
-                                       np == 1 ? 1 : 0);
-    }
-    if (b == 0 && tid == 0) a.npieces[h] = np_all;
-    // per-warp histograms of this block
-    const int w0 = warp * kSortPerWarp, w1 = min(w0 + kSortPerWarp, nb);
-    for (int bs = w0; bs < w1; bs += 32) {
-        const int n = bs + lane;
-        const int id = n < w1 ? min((int)ids_s[n], C - 1) : -1;
-        const unsigned m = __match_any_sync(0xffffffffu, id);
-        if (id >= 0 && lane == __ffs(m) - 1) cur[warp][id] += __popc(m);
-    }
-    __syncthreads();
-    if (tid < C) {
-        int run = off + before;
-        for (int w = 0; w < kSortWarps; ++w) {
-            const int t = cur[w][tid];
-            cur[w][tid] = run;
-            run += t;
+        for (int r = 0; r < 4; ++r)
+            if (i0 + r * kUpdThreads < body) v[r] = __ldg(pb + i0 + r * kUpdThreads);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            if (i0 + r * kUpdThreads >= body) break;
+            const uint32_t w[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
+            uint32_t hit[4], any = 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t t = (w[q] & mask4) ^ want4;            // zero byte <=> member
+                hit[q] = (t - 0x01010101u) & ~t & 0x80808080u;        // nonzero iff t has a zero byte
+                any |= hit[q];
+            }
+            if (any) {
+                const int64_t n = t0 + pre + 16 * (i0 + r * kUpdThreads);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (hit[q])
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) one(n + 4 * q + j, (w[q] >> (8 * j)) & 0xFFu);
+            }
         }
     }
-    __syncthreads();
-    int* perm = a.perm + (int64_t)h * a.n_tokens;
-    const unsigned lt = (1u << lane) - 1u;
-    for (int bs = w0; bs < w1; bs += 32) {
-        const int n = bs + lane;
-        const int id = n < w1 ? min((int)ids_s[n], C - 1) : -1;
-        const unsigned m = __match_any_sync(0xffffffffu, id);
-        if (id >= 0) perm[cur[warp][id] + __popc(m & lt)] = (int)(n0 + n);
-        __syncwarp();
-        if (id >= 0 && lane == __ffs(m) - 1) cur[warp][id] += __popc(m);
-        __syncwarp();
-    }
+    for (int64_t n = t0 + pre + 16 * body + threadIdx.x; n < t1; n += kUpdThreads) one(n, p[n]);
 }
 
-__device__ __forceinline__ i128 shfl_xor_i128(i128 v, int mask) {
-    const uint64_t lo = (uint64_t)v, hi = (uint64_t)((u128)v >> 64);
-    const uint64_t olo = __shfl_xor_sync(0xffffffffu, lo, mask), ohi = __shfl_xor_sync(0xffffffffu, hi, mask);
-    return (i128)(((u128)ohi << 64) | (u128)olo);
-}
-
-// One warp per piece.  The warp stages the piece's rows (at most
-// kPieceTokens, gathered in sorted order) kSumRows at a time into its slice of
-// shared memory with 16-byte asynchronous copies, all of a round in flight at
-// once, then sums them from there.  A lane owns 8 consecutive channels of one
-// row slot; D/8 lanes cover a row and 32/(D/8) rows go per instruction.  Row
-// slots are reduced at the end (integer additions: exact, any order).
-constexpr int kSumWarps = 4;
-constexpr int kSumRows = 16;      // rows staged per round
-static_assert(kPieceTokens <= 64, "a warp holds a piece's token indices in two registers per lane");
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+// Shared memory: the sorted list and the arrival-order list (int[kListCap]
+// each), then the window sums of the group split at bit 15 (int lo, hi
+// [G][3][D], the layout of the stored sums), which the 128-bit sums reuse.
+__host__ __device__ inline size_t update_smem(int D, int lg) {
+    return 2 * sizeof(int) * kListCap + 2 * sizeof(int) * ((size_t)3 * D << lg);
 }
 
 template <int D>
-__global__ void __launch_bounds__(32 * kSumWarps, 8) kmeans_sum_kernel(UpdateArgs a) {
-    constexpr int LPR = D / 8, RPI = 32 / LPR;
-    extern __shared__ __align__(16) uint16_t sum_rows[];     // [warp][kSumRows][D]
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int sub = lane % LPR, slot = lane / LPR;
-    const int h = blockIdx.y;
-    const int p = blockIdx.x * kSumWarps + warp;
-    if (p >= a.npieces[h]) return;
-    uint16_t* rows = sum_rows + (size_t)warp * kSumRows * D;
-    const int4 pc = a.pieces[(int64_t)h * a.max_pieces + p];
-    const int start = pc.x, len = pc.y, j = pc.z;
-    const int* ph = a.perm + (int64_t)h * a.n_tokens + start;
-    const uint16_t* xh = a.x + (int64_t)h * a.head_stride + sub * 8;
-    // the piece's token indices (len <= kPieceTokens = 64): lane k holds
-    // positions k and k + 32
-    const int pa = lane < len ? ph[lane] : 0, pb = lane + 32 < len ? ph[lane + 32] : 0;
-    // rows [r0, r0 + kSumRows) of the piece into the warp's slice
-    auto stage = [&](int r0) {
-        for (int k0 = 0; k0 < kSumRows; k0 += RPI) {
-            const int k = r0 + k0 + slot;
-            const int na = __shfl_sync(0xffffffffu, pa, k & 31), nb = __shfl_sync(0xffffffffu, pb, k & 31);
-            if (k < len)
-                cp_async16(smem_u32(rows + (k0 + slot) * D + sub * 8), xh + (int64_t)(k < 32 ? na : nb) * a.token_stride);
+__global__ void __launch_bounds__(kUpdThreads, 3) kmeans_update_kernel(UpdateArgs a) {
+    constexpr int LPR = D / 8, RPW = 32 / LPR, UNITS = (kUpdThreads / 32) * RPW;
+    extern __shared__ __align__(16) unsigned char upd_smem[];
+    const int lg = a.group_log2, G = 1 << lg, GD3 = 3 * (D << lg);
+    int* list = reinterpret_cast<int*>(upd_smem);
+    int* raw = list + kListCap;
+    int* lo = raw + kListCap;
+    int* hi = lo + GD3;
+    __shared__ int cnt[kMaxGroup], dcnt[kMaxGroup], bcnt[2 * kMaxGroup], off[2 * kMaxGroup + 1], cur[2 * kMaxGroup];
+    __shared__ int touched[kMaxGroup];
+    __shared__ int n_raw, big, ibig;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int h = blockIdx.y, c0 = blockIdx.x << lg;
+    const int ng = min(G, a.C - c0);
+    const int64_t N = a.n_tokens;
+    const uint8_t* idh = a.ids + (int64_t)h * a.cap + a.tok_offset;
+    const uint16_t* xh = a.x + (int64_t)h * a.head_stride;
+    long long* ks = a.ksum + ((int64_t)h * a.C + c0) * 3 * D;        // [k][w][d], k < ng
+    int* kc = a.kcount + (int64_t)h * a.C + c0;
+    int* kb = a.kbig + (int64_t)h * a.C + blockIdx.x;
+    const uint32_t keep = (0xFFu << lg) & 0xFFu;
+
+    // offsets of nb buckets from their counts c[] (cur becomes the cursors)
+    auto set_offsets = [&](const int* c, int nb) {
+        __syncthreads();
+        if (tid == 0) {
+            int run = 0;
+            for (int b = 0; b < nb; ++b) {
+                const int v = c[b];
+                off[b] = run;
+                cur[b] = run;
+                run += v;
+            }
+            for (int b = nb; b <= 2 * kMaxGroup; ++b) off[b] = run;
         }
-        asm volatile("cp.async.commit_group;" ::: "memory");
-        asm volatile("cp.async.wait_group 0;" ::: "memory");
-        __syncwarp();
+        __syncthreads();
     };
-    int w1[8], w2[8], w3[8];
-#pragma unroll
-    for (int d = 0; d < 8; ++d) w1[d] = w2[d] = w3[d] = 0;
+    // the arrival-order list of n_raw (n << 5 | bucket) entries, sorted
+    auto sort_raw = [&](const int* c, int nb) {
+        set_offsets(c, nb);
+        for (int i = tid; i < n_raw; i += kUpdThreads) {
+            const int v = raw[i];
+            list[atomicAdd(&cur[v & 31], 1)] = v >> 5;
+        }
+        __syncthreads();
+    };
+    auto clear_sums = [&]() {
+        for (int i = tid; i < GD3; i += kUpdThreads) lo[i] = hi[i] = 0;
+    };
+
+    // window sums of the listed rows into lo/hi: unit u takes the contiguous
+    // run [u T / UNITS, (u + 1) T / UNITS) of the list.  In an incremental
+    // list bucket 2k adds rows to cluster k and bucket 2k + 1 subtracts them.
     float amax = 0.0f;
-    for (int r0 = 0; r0 < len; r0 += kSumRows) {
-        stage(r0);
-#pragma unroll 2
-        for (int k = slot; k < kSumRows && r0 + k < len; k += RPI) {
-            const uint4 v = *reinterpret_cast<const uint4*>(rows + k * D + sub * 8);
-            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+    auto sum_list = [&](bool signed_buckets) {
+        const int T = off[2 * kMaxGroup];
+        const int unit = warp * RPW + lane / LPR, sub = lane % LPR;
+        const int pb = (int)((int64_t)unit * T / UNITS), pe = (int)((int64_t)(unit + 1) * T / UNITS);
+        if (pb >= pe) return;
+        const uint16_t* xs = xh + sub * 8;
+        int w1[8], w2[8], w3[8];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float lo = bf16_lo(wv[q]), hi = bf16_hi(wv[q]);
-                amax = fmax3(amax, fabsf(lo), fabsf(hi));
-                window_add2(make_float2(lo, hi), w1 + 2 * q, w2 + 2 * q, w3 + 2 * q);
-            }
-        }
-        __syncwarp();                      // the slice is read before the next round overwrites it
-    }
-    i128 tot[8];
-    if (__any_sync(0xffffffffu, !(amax < kWinMax))) {
-        // a value outside the first window: redo the piece with 128-bit sums
-#pragma unroll
-        for (int d = 0; d < 8; ++d) tot[d] = 0;
-        for (int k = slot; k < len; k += RPI) {
-            const uint4 v = ldg_nc_v4(xh + (int64_t)ph[k] * a.token_stride);
-            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                tot[2 * q] += bf16_to_i128_units(wv[q] & 0xFFFFu);
-                tot[2 * q + 1] += bf16_to_i128_units(wv[q] >> 16);
-            }
-        }
-#pragma unroll
-        for (int o = LPR; o < 32; o <<= 1)
-#pragma unroll
-            for (int d = 0; d < 8; ++d) tot[d] += shfl_xor_i128(tot[d], o);
-    } else {
-        // row slots first, in int32 (at most kPieceTokens terms of <= 2^22 each)
-#pragma unroll
-        for (int o = LPR; o < 32; o <<= 1)
+        for (int d = 0; d < 8; ++d) w1[d] = w2[d] = w3[d] = 0;
+        int b = 0, terms = 0;
+        while (pb >= off[b + 1]) ++b;
+        auto flush = [&]() {
+            const int k = signed_buckets ? b >> 1 : b;
+            const bool neg = signed_buckets && (b & 1);
+            int* l0 = lo + k * 3 * D + 8 * sub;
+            int* h0 = hi + k * 3 * D + 8 * sub;
 #pragma unroll
             for (int d = 0; d < 8; ++d) {
-                w1[d] += __shfl_xor_sync(0xffffffffu, w1[d], o);
-                w2[d] += __shfl_xor_sync(0xffffffffu, w2[d], o);
-                w3[d] += __shfl_xor_sync(0xffffffffu, w3[d], o);
+                const int v1 = neg ? -w1[d] : w1[d], v2 = neg ? -w2[d] : w2[d], v3 = neg ? -w3[d] : w3[d];
+                atomicAdd(l0 + d, v1 & 0x7FFF);         atomicAdd(h0 + d, v1 >> 15);
+                atomicAdd(l0 + D + d, v2 & 0x7FFF);     atomicAdd(h0 + D + d, v2 >> 15);
+                atomicAdd(l0 + 2 * D + d, v3 & 0x7FFF); atomicAdd(h0 + 2 * D + d, v3 >> 15);
+                w1[d] = w2[d] = w3[d] = 0;
+            }
+            terms = 0;
+        };
+        for (int p0 = pb; p0 < pe; p0 += 4) {
+            uint4 v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (p0 + j < pe) v[j] = ldg_nc_v4(xs + (int64_t)list[p0 + j] * a.token_stride);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int p = p0 + j;
+                if (p >= pe) break;
+                if (p >= off[b + 1] || terms == kFlushTerms) {
+                    if (terms) flush();
+                    while (p >= off[b + 1]) ++b;
+                }
+                const uint32_t wv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float l = bf16_lo(wv[q]), u = bf16_hi(wv[q]);
+                    amax = fmax3(amax, fabsf(l), fabsf(u));
+                    window_add2(make_float2(l, u), w1 + 2 * q, w2 + 2 * q, w3 + 2 * q);
+                }
+                ++terms;
+            }
+        }
+        if (terms) flush();
+    };
+    // lo/hi into the stored sums (= when first, else +=), then cleared
+    // ... and a copy in shared memory (ksm, over the lists) for the means;
+    // the stored sums are read four at a time so that their loads overlap
+    long long* ksm = reinterpret_cast<long long*>(list);
+    auto fold = [&](bool first) {
+        __syncthreads();
+        const int n3 = ng * 3 * D;
+        for (int i0 = tid; i0 < n3; i0 += 4 * kUpdThreads) {
+            long long old[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int i = i0 + r * kUpdThreads;
+                old[r] = (!first && i < n3) ? ks[i] : 0;
             }
 #pragma unroll
-        for (int d = 0; d < 8; ++d) tot[d] = windows_to_i128(w1[d], w2[d], w3[d]);
+            for (int r = 0; r < 4; ++r) {
+                const int i = i0 + r * kUpdThreads;
+                if (i < n3) {
+                    const long long v = old[r] + (long long)hi[i] * 32768 + lo[i];
+                    ks[i] = v;
+                    ksm[i] = v;
+                    lo[i] = hi[i] = 0;
+                }
+            }
+        }
+        __syncthreads();
+    };
+    auto mean_of = [&](int k, int d, bool from_lohi, int count) -> uint16_t {
+        long long w[3];
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+            const int j = (k * 3 + q) * D + d;
+            w[q] = from_lohi ? (long long)hi[j] * 32768 + lo[j] : ksm[j];
+        }
+        return mean_bf16_bits_fast(((i128)w[0] << 44) + ((i128)w[1] << 22) + (i128)w[2], (uint32_t)count);
+    };
+    uint16_t* ch = a.cent + ((int64_t)h * a.C + c0) * D;
+
+    if (a.mode == kUpdIncremental && *kb == 0 && N < kPackLimit) {
+        // The changes lie in the ranges chg_parts[h][p] = (start, count) of
+        // the head's chg_tok / chg_on rows (stride chg_stride, a multiple of
+        // 8; every start a multiple of 128), bytes 2i and 2i + 1 of chg_on
+        // being the old and the new id of change i.  The ranges' 16-byte
+        // chunks are numbered consecutively so that all threads share one scan.
+        __shared__ int2 parts[kChgParts];
+        __shared__ int pchunk[kChgParts + 1];
+        const uint8_t* onb = reinterpret_cast<const uint8_t*>(a.chg_on + (int64_t)h * a.chg_stride);
+        const int* tk = a.chg_tok + (int64_t)h * a.chg_stride;
+        for (int p = tid; p < kChgParts; p += kUpdThreads) parts[p] = a.chg_parts[(int64_t)h * kChgParts + p];
+        if (tid < kMaxGroup) dcnt[tid] = touched[tid] = 0;
+        if (tid < 2 * kMaxGroup) bcnt[tid] = 0;
+        if (tid == 0) { ibig = 0; n_raw = 0; }
+        clear_sums();
+        __syncthreads();
+        if (warp == 0) {
+            // exclusive prefix of the ranges' chunk counts, kChgParts / 32 per lane
+            constexpr int PL = kChgParts / 32;
+            int c[PL], sum = 0;
+#pragma unroll
+            for (int r = 0; r < PL; ++r) {
+                c[r] = (2 * parts[lane * PL + r].y + 15) >> 4;
+                sum += c[r];
+            }
+            int inc = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += u;
+            }
+            int run = inc - sum;
+#pragma unroll
+            for (int r = 0; r < PL; ++r) {
+                pchunk[lane * PL + r] = run;
+                run += c[r];
+            }
+            if (lane == 31) pchunk[kChgParts] = run;
+        }
+        __syncthreads();
+        const int n_chunks = pchunk[kChgParts];
+        // f(j, v) for the bytes v of the group in chunks [cb, ce) (j: byte index in the head's rows)
+        auto scan_changes = [&](int cb, int ce, auto&& f) {
+            for (int q0 = cb + tid; q0 < ce; q0 += 4 * kUpdThreads) {
+                uint4 v[4];
+                int64_t at[4], lim[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int q = q0 + r * kUpdThreads;
+                    if (q >= ce) break;
+                    int lo_p = 0, hi_p = kChgParts - 1;           // the part holding chunk q
+                    while (lo_p < hi_p) {
+                        const int mid = (lo_p + hi_p + 1) >> 1;
+                        if (pchunk[mid] <= q) lo_p = mid; else hi_p = mid - 1;
+                    }
+                    at[r] = 2 * (int64_t)parts[lo_p].x + 16 * (int64_t)(q - pchunk[lo_p]);
+                    lim[r] = 2 * ((int64_t)parts[lo_p].x + parts[lo_p].y);
+                    v[r] = __ldg(reinterpret_cast<const uint4*>(onb + at[r]));
+                }
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    if (q0 + r * kUpdThreads >= ce) break;
+                    const uint32_t w[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq)
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) {
+                            const int64_t j = at[r] + 4 * qq + jj;
+                            const uint32_t byte = (w[qq] >> (8 * jj)) & 0xFFu;
+                            if (j < lim[r] && (byte & keep) == (uint32_t)c0) f(j, byte);
+                        }
+                }
+            }
+        };
+        // one scan: counts, and the rows while the list has room
+        scan_changes(0, n_chunks, [&](int64_t j, uint32_t v) {
+            const int k = (int)v - c0, leaving = (int)(~j & 1);
+            atomicAdd(&dcnt[k], leaving ? -1 : 1);
+            touched[k] = 1;
+            atomicAdd(&bcnt[2 * k + leaving], 1);
+            const int pos = atomicAdd(&n_raw, 1);
+            if (pos < kListCap) raw[pos] = (tk[j >> 1] << 5) | (2 * k + leaving);
+        });
+        __syncthreads();
+        if (n_raw <= kListCap) {
+            sort_raw(bcnt, 2 * G);
+            sum_list(true);
+            fold(false);
+        } else {
+            // more rows than the list holds: runs of chunks holding at most
+            // kListCap / 2 changes
+            for (int cb = 0; cb < n_chunks; cb += kListCap / 16) {
+                __syncthreads();
+                if (tid < 2 * kMaxGroup) bcnt[tid] = 0;
+                if (tid == 0) n_raw = 0;
+                __syncthreads();
+                scan_changes(cb, min(n_chunks, cb + kListCap / 16), [&](int64_t j, uint32_t v) {
+                    const int k = (int)v - c0, leaving = (int)(~j & 1);
+                    atomicAdd(&bcnt[2 * k + leaving], 1);
+                    raw[atomicAdd(&n_raw, 1)] = (tk[j >> 1] << 5) | (2 * k + leaving);
+                });
+                __syncthreads();
+                sort_raw(bcnt, 2 * G);
+                sum_list(true);
+                fold(false);
+            }
+        }
+        if (!(amax < kWinMax)) ibig = 1;
+        __syncthreads();
+        if (!ibig) {
+            if (tid < ng) {
+                dcnt[tid] += kc[tid];                  // the new counts
+                kc[tid] = dcnt[tid];
+            }
+            __syncthreads();
+            // clusters that a change touched are rounded again (a token leaving
+            // and another arriving may leave the count as it was); an emptied
+            // one keeps its centroid
+            for (int i = tid; i < ng * D; i += kUpdThreads) {
+                const int k = i / D, d = i % D;
+                if (touched[k] && dcnt[k] != 0) ch[i] = mean_of(k, d, false, dcnt[k]);
+            }
+            return;
+        }
+        // a changed row holds a value >= 2^14: the full update below redoes the group
+        __syncthreads();
     }
-    if (slot != 0) return;
-    if (pc.w) {
-        uint16_t r[8];
-#pragma unroll
-        for (int d = 0; d < 8; ++d) r[d] = mean_bf16_bits(tot[d], (uint32_t)len);
-        uint4 o;
-        o.x = r[0] | ((uint32_t)r[1] << 16); o.y = r[2] | ((uint32_t)r[3] << 16);
-        o.z = r[4] | ((uint32_t)r[5] << 16); o.w = r[6] | ((uint32_t)r[7] << 16);
-        *reinterpret_cast<uint4*>(a.cent + ((int64_t)h * a.C + j) * D + sub * 8) = o;
+
+    // ---- full update
+    if (tid < kMaxGroup) cnt[tid] = 0;
+    if (tid == 0) { n_raw = 0; big = 0; }
+    clear_sums();
+    __syncthreads();
+    const bool packable = N < kPackLimit;
+    for_matching_bytes(idh, 0, N, keep, (uint32_t)c0, [&](int64_t n, uint32_t v) {
+        const int k = (int)v - c0;
+        atomicAdd(&cnt[k], 1);
+        if (packable) {
+            const int pos = atomicAdd(&n_raw, 1);
+            if (pos < kListCap) raw[pos] = ((int)n << 5) | k;
+        }
+    });
+    __syncthreads();
+    int total = 0;
+    for (int k = 0; k < G; ++k) total += cnt[k];
+    const bool one = packable && total <= kListCap;
+    amax = 0.0f;
+    if (one) {
+        sort_raw(cnt, G);
+        sum_list(false);
+        __syncthreads();
+        for (int i = tid; i < ng * 3 * D; i += kUpdThreads) ks[i] = (long long)hi[i] * 32768 + lo[i];
     } else {
-        i128* pr = reinterpret_cast<i128*>(a.partials) + ((int64_t)h * a.max_pieces + p) * D + sub * 8;
-#pragma unroll
-        for (int d = 0; d < 8; ++d) pr[d] = tot[d];
+        for (int64_t t0 = 0; t0 < N; t0 += kListCap) {
+            const int64_t t1 = min(N, t0 + kListCap);
+            if (tid < 2 * kMaxGroup) bcnt[tid] = 0;
+            __syncthreads();
+            for_matching_bytes(idh, t0, t1, keep, (uint32_t)c0, [&](int64_t, uint32_t v) { atomicAdd(&bcnt[(int)v - c0], 1); });
+            set_offsets(bcnt, G);
+            for_matching_bytes(idh, t0, t1, keep, (uint32_t)c0,
+                               [&](int64_t n, uint32_t v) { list[atomicAdd(&cur[(int)v - c0], 1)] = (int)n; });
+            __syncthreads();
+            sum_list(false);
+            fold(t0 == 0);
+        }
+    }
+    if (!(amax < kWinMax)) big = 1;
+    if (tid < ng) kc[tid] = cnt[tid];
+    __syncthreads();
+    if (tid == 0) *kb = big;
+    if (!big) {
+        for (int i = tid; i < ng * D; i += kUpdThreads) {
+            const int k = i / D, d = i % D;
+            if (cnt[k] != 0) ch[i] = mean_of(k, d, one, cnt[k]);   // an empty cluster keeps its centroid
+        }
+        return;
+    }
+    // a value outside the first window: sum the group again with 128-bit
+    // integers, one thread per (slot, channel)
+    i128* s128 = reinterpret_cast<i128*>(lo);
+    for (int i = tid; i < G * D; i += kUpdThreads) s128[i] = 0;
+    __syncthreads();
+    auto exact_list = [&]() {
+        for (int i = tid; i < ng * D; i += kUpdThreads) {
+            const int k = i / D, d = i % D;
+            i128 t = 0;
+            for (int p = off[k]; p < off[k + 1]; ++p) t += bf16_to_i128_units(xh[(int64_t)list[p] * a.token_stride + d]);
+            s128[i] += t;
+        }
+        __syncthreads();
+    };
+    if (one) {
+        exact_list();                                // the sorted list is still in place
+    } else {
+        for (int64_t t0 = 0; t0 < N; t0 += kListCap) {
+            const int64_t t1 = min(N, t0 + kListCap);
+            if (tid < 2 * kMaxGroup) bcnt[tid] = 0;
+            __syncthreads();
+            for_matching_bytes(idh, t0, t1, keep, (uint32_t)c0, [&](int64_t, uint32_t v) { atomicAdd(&bcnt[(int)v - c0], 1); });
+            set_offsets(bcnt, G);
+            for_matching_bytes(idh, t0, t1, keep, (uint32_t)c0,
+                               [&](int64_t n, uint32_t v) { list[atomicAdd(&cur[(int)v - c0], 1)] = (int)n; });
+            __syncthreads();
+            exact_list();
+        }
+    }
+    for (int i = tid; i < ng * D; i += kUpdThreads) {
+        const int k = i / D;
+        if (cnt[k] != 0) ch[i] = mean_bf16_bits_fast(s128[i], (uint32_t)cnt[k]);
     }
 }
 
-// Clusters made of several pieces: add the partials in piece order, round.
-template <int D>
-__global__ void kmeans_mean_kernel(UpdateArgs a) {
-    const int j = blockIdx.x, h = blockIdx.y;
-    const int cnt = a.counts[(int64_t)h * a.C + j];
-    const int np = (cnt + kPieceTokens - 1) / kPieceTokens;
-    if (np <= 1) return;
-    const int first = a.first_piece[(int64_t)h * a.C + j];
-    const i128* pr = reinterpret_cast<const i128*>(a.partials) + ((int64_t)h * a.max_pieces + first) * D;
-    for (int d = threadIdx.x; d < D; d += blockDim.x) {
-        i128 s = 0;
-        for (int p = 0; p < np; ++p) s += pr[(int64_t)p * D + d];
-        a.cent[((int64_t)h * a.C + j) * D + d] = mean_bf16_bits(s, (uint32_t)cnt);
-    }
+// Clusters per CTA: the largest power of two up to kMaxGroup that still
+// gives two CTAs per SM and lists a group's tokens at once on average.
+int update_group_log2(int D, int H, int C, int64_t N) {
+    int lg = 0;
+    while ((1 << (lg + 1)) <= kMaxGroup && (int64_t)H * ((C + (2 << lg) - 1) >> (lg + 1)) >= 2 * 148 &&
+           N * (2 << lg) <= (int64_t)C * (kListCap / 2) && (D << (lg + 1)) <= kMaxGroupChannels)
+        ++lg;
+    return lg;
 }
 
 __global__ void set_chunk_kernel(int64_t* off, int32_t* ver, int idx, int64_t begin, int64_t end,
@@ -637,18 +837,17 @@ cudaError_t assign_d(int H, const AssignArgs& a, cudaStream_t s) {
 }
 
 template <int D>
-cudaError_t update_d(const UpdateArgs& a, cudaStream_t s) {
-    if (a.n_tokens == 0) return cudaSuccess;
-    dim3 g1((unsigned)a.n_blocks, (unsigned)a.H);
-    kmeans_hist_kernel<<<g1, kThreads, 0, s>>>(a);
-    kmeans_scatter_kernel<<<g1, kThreads, 0, s>>>(a);
-    dim3 g2((unsigned)((a.max_pieces + kSumWarps - 1) / kSumWarps), (unsigned)a.H);
-    const size_t sum_smem = sizeof(uint16_t) * kSumWarps * kSumRows * D;
-    cudaError_t e = cudaFuncSetAttribute(kmeans_sum_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)sum_smem);
+cudaError_t update_d(const UpdateArgs& a0, cudaStream_t s) {
+    if (a0.n_tokens == 0) return cudaSuccess;
+    UpdateArgs a = a0;
+    if (a.group_log2 < 0) a.group_log2 = update_group_log2(D, a.H, a.C, a.n_tokens);
+    if ((1 << a.group_log2) > kMaxGroup || (D << a.group_log2) > kMaxGroupChannels) return cudaErrorInvalidValue;
+    const size_t smem = update_smem(D, a.group_log2);
+    cudaError_t e = cudaFuncSetAttribute(kmeans_update_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
     if (e != cudaSuccess) return e;
-    kmeans_sum_kernel<D><<<g2, 32 * kSumWarps, sum_smem, s>>>(a);
-    kmeans_mean_kernel<D><<<dim3((unsigned)a.C, (unsigned)a.H), D, 0, s>>>(a);
+    dim3 grid((unsigned)((a.C + (1 << a.group_log2) - 1) >> a.group_log2), (unsigned)a.H);
+    kmeans_update_kernel<D><<<grid, kUpdThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -662,9 +861,10 @@ cudaError_t launch_kmeans_init(int D, const uint16_t* x, int64_t head_stride, in
     return cudaGetLastError();
 }
 
-cudaError_t launch_assign(int D, int H, const AssignArgs& a, cudaStream_t s) {
+cudaError_t launch_assign(int D, int H, const AssignArgs& a, cudaStream_t s, bool* recorded) {
     bool launched = false;
     const cudaError_t e = launch_assign_tc(D, H, a, &launched, s);
+    if (recorded) *recorded = launched && a.chg_parts != nullptr;
     if (e != cudaSuccess || launched) return e;
     switch (D) {
         case 32: return assign_d<32>(H, a, s);

@@ -112,6 +112,99 @@ def test_staged_assign_and_update(qvg, oracle):
         np.testing.assert_array_equal(got[h], want)
 
 
+@pytest.mark.parametrize("D,C,N,big", [
+    (128, 2, 9000, False),     # one cluster of ~6300 tokens: more than one shared-memory list
+    (128, 2, 9000, True),      # the same with values >= 2^14 (128-bit sums over several lists)
+    (64, 3, 7001, False),
+    (32, 1, 5003, True),
+    (128, 40, 3001, True),     # values >= 2^14 in short clusters (one list)
+])
+def test_update_long_clusters_and_large_values(qvg, oracle, D, C, N, big):
+    """The update alone, given ids with clusters longer than one list of
+    tokens, values of magnitude >= 2^14, and id rows that start off a 16-byte
+    boundary (capacity and offset not multiples of 16)."""
+    rng = np.random.default_rng(D + 10 * C + N + big)
+    H, cap, off = 2, N + 37, 5
+    x = rng.standard_normal((H, N, D))
+    if big:
+        m = rng.random((H, N, D)) < 0.002
+        x[m] = rng.choice([-1.0, 1.0], m.sum()) * 2.0 ** rng.integers(14, 18, m.sum())
+    xb = SY.f64_to_bf16_bits(x)
+    p = rng.random(C) + 0.1
+    p[0] += 4.0                                    # cluster 0 holds most tokens
+    oids = np.stack([rng.choice(C, N, p=p / p.sum()) for _ in range(H)]).astype(np.int32)
+    cent = SY.f64_to_bf16_bits(rng.standard_normal((H, C, D)))
+    ids = np.full((H, cap), 255, np.uint8)
+    ids[:, off:off + N] = oids
+    cfg = qvg.config(H, D, C, 1, 2, 32)
+    c_dev = to_dev(cent)
+    ws = qvg.alloc_workspace(cfg, N)
+    qvg.qvg_update(cfg, to_dev(xb), N, N * D, D, to_dev(ids.reshape(-1)), cap, off, c_dev, ws)
+    torch.cuda.synchronize()
+    got = u16(c_dev).reshape(H, C, D)
+    for h in range(H):
+        want, counts = oracle.update(xb[h], oids[h], cent[h])
+        if C <= 3:
+            assert counts.max() > 4096
+        np.testing.assert_array_equal(got[h], want)
+
+
+@pytest.mark.parametrize("D,C", [(128, 16), (64, 40)])
+def test_fit_with_values_beyond_the_first_window(qvg, oracle, D, C):
+    """A fit whose later updates apply only the changed ids to the stored
+    exact sums: head 0 has a few values of magnitude 2^14..2^16 (those groups
+    take 128-bit sums and full updates), head 1 has none."""
+    rng = np.random.default_rng(D + C)
+    H, N, T, S, G = 2, 2500, 4, 2, 64
+    xb = np.stack([mixture(rng, N, D, M=24, spread=1.5, noise=0.3) for _ in range(H)])
+    xf = SY.bf16_bits_to_f32(xb).astype(np.float64)
+    m = rng.random((N, D)) < 0.0005
+    xf[0][m] = rng.choice([-1.0, 1.0], m.sum()) * 2.0 ** rng.integers(14, 17, m.sum())
+    xb = SY.f64_to_bf16_bits(xf)
+    cfg = qvg.config(H, D, C, T, S, G)
+    enc, dec = run_fit_encode_decode(qvg, cfg, to_dev(xb), N, N * D, D)
+    for h in range(H):
+        check_unit(oracle, xb[h], enc, dec, h, C, T, S, G)
+
+
+def test_update_means_at_rounding_midpoints(qvg, oracle):
+    """Cluster means that are exact bf16 rounding midpoints (ties to even),
+    or lie just off them, or next to a power of two, next to ordinary
+    clusters and an empty one: the rounding is decided exactly there."""
+    rng = np.random.default_rng(77)
+    D, C = 64, 8
+    def nxt(b, k=1):                       # the k-th bf16 pattern above b (positive values)
+        return (b.astype(np.int64) + k).astype(np.uint16)
+    a = SY.f64_to_bf16_bits(np.abs(rng.standard_normal((6, D))) + 0.1)
+    edge = np.full(D, 0x3FFF, np.uint16)   # 1.9921875, the last bf16 below 2
+    rows, lab = [], []
+    def add(k, *vals):
+        for v in vals:
+            rows.append(v); lab.append(k)
+    add(0, a[0], nxt(a[0]))                          # mean = midpoint
+    add(1, a[1], a[1], nxt(a[1]), nxt(a[1]))         # midpoint from four tokens
+    add(2, a[2], a[2], nxt(a[2], 2))                 # a + 2/3 ulp
+    add(3, *([a[3]] * 3 + [nxt(a[3])] * 3))          # midpoint from six
+    for v in SY.f64_to_bf16_bits(rng.standard_normal((1000, D))):
+        add(4, v)                                    # an ordinary cluster
+    add(5, a[5], a[5] ^ np.uint16(0x8000))           # mean 0
+    add(6, edge, nxt(edge))                          # midpoint below 2.0
+    x = np.stack(rows).astype(np.uint16)
+    ids = np.array(lab, np.int32)
+    perm = rng.permutation(len(ids))
+    x, ids = x[perm], ids[perm]
+    N = len(ids)
+    cent = SY.f64_to_bf16_bits(rng.standard_normal((C, D)))
+    cfg = qvg.config(1, D, C, 1, 2, 32)
+    c_dev = to_dev(cent[None])
+    ws = qvg.alloc_workspace(cfg, N)
+    qvg.qvg_update(cfg, to_dev(x[None]), N, N * D, D, to_dev(ids.astype(np.uint8)), N, 0, c_dev, ws)
+    torch.cuda.synchronize()
+    want, counts = oracle.update(x, ids, cent)
+    assert counts[7] == 0
+    np.testing.assert_array_equal(u16(c_dev).reshape(C, D), want)
+
+
 def test_ties_and_degenerate_inputs(qvg, oracle):
     """Exact duplicate tokens (ties at distance 0 between equal centroids),
     fewer tokens than clusters (duplicate initial centroids), constant rows
