@@ -143,8 +143,9 @@ QVG_API qvg_status qvg_workspace_bytes(const qvg_config* cfg, int64_t n_tokens, 
  * internal barrier and its ids are not valid).  With C = 0 (a Coral-KV
  * configuration) out[0..2] are 0 and out[3] is the error word of the last
  * coral_* call that used `workspace` (0x7E000000 = a tensor-core kernel gave
- * up waiting and its outputs are not valid).  Copies from the device and
- * waits for `stream`; out is host memory. */
+ * up waiting and its outputs are not valid).  Returns QVG_ERR_TIMEOUT (with
+ * out filled) when the error word is set, QVG_OK otherwise.  Copies from the
+ * device and waits for `stream`; out is host memory. */
 QVG_API qvg_status qvg_fit_stats(const qvg_config* cfg, int64_t n_tokens, const void* workspace,
                          size_t workspace_bytes, uint64_t* out, qvg_stream stream);
 
@@ -158,13 +159,15 @@ QVG_API qvg_status qvg_fit_stats(const qvg_config* cfg, int64_t n_tokens, const 
  * was 0.  Waits for `stream`; out is host memory. */
 QVG_API qvg_status qvg_device_error(uint32_t* out, int32_t clear, qvg_stream stream);
 
-/* Test hook of the bounded waits of the kernels above: wait_limit_ns is the
- * limit after which a waiting role gives up (0 restores the default, 2 s);
- * flags bit 0 makes each CTA's copy producer withhold its first copy, so that
- * the first wait of that CTA's consumers runs out (and the call records
- * 0x7E000000 in the error word, drains its other copies and returns).  For
- * failure-path tests only; waits for `stream`, then applies to every call
- * the process makes afterwards. */
+/* Test hook of the bounded waits of the kernels above and of the
+ * tensor-core k-means assign: wait_limit_ns is the limit after which a
+ * waiting role gives up (0 restores the default, 2 s); flags bit 0 makes each
+ * CTA's copy producer withhold its first copy, so that the first wait of that
+ * CTA's consumers runs out (and the call records 0x7E000000 -- in the device
+ * error word, or for the assign in the workspace word that qvg_fit_stats
+ * reads -- drains its other copies and returns).  For failure-path tests
+ * only; waits for `stream`, then applies to every call the process makes
+ * afterwards. */
 QVG_API qvg_status qvg_debug_set_wait(uint64_t wait_limit_ns, uint32_t flags, qvg_stream stream);
 
 /* SAS k-means (QVG sec. 2A items 1-2 and sec. 3): per head, T Lloyd iterations

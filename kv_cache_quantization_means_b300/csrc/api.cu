@@ -260,6 +260,7 @@ qvg_status qvg_fit_stats(const qvg_config* cfg, int64_t n_tokens, const void* wo
         if (e == cudaSuccess) e = cudaStreamSynchronize(s);
         if (e != cudaSuccess) return cuda_status(e, "stats copy");
         out[3] = w;
+        if (w) return fail(QVG_ERR_TIMEOUT, "a kernel gave up a bounded wait (error word 0x%08x)", w);
         return ok();
     }
     FitWorkspace w;
@@ -269,6 +270,7 @@ qvg_status qvg_fit_stats(const qvg_config* cfg, int64_t n_tokens, const void* wo
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_status(e, "stats copy");
     out[3] &= 0xFFFFFFFFull;
+    if (out[3]) return fail(QVG_ERR_TIMEOUT, "a kernel gave up a bounded wait (error word 0x%08x)", (unsigned)out[3]);
     return ok();
 }
 

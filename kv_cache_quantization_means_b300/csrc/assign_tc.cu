@@ -81,6 +81,8 @@ struct TcArgs {
     uint16_t* chg_on;
     int2* chg_parts;
     int64_t chg_stride;
+    unsigned long long limit;    // bounded waits give up after this many ns
+    uint32_t dbg;                // bit 0: the producer withholds each CTA's first tile (tests)
 };
 
 // ----------------------------------------------------- shared memory map
@@ -386,12 +388,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
+            const bool withhold = (a.dbg & 1u) != 0;
             int armed = 0;
             for (int i = 0; i < n_tiles; ++i) {
                 const int st = i % NS;
                 const uint32_t ph = (uint32_t)(i / NS) & 1u;
-                if (!mbar_wait(empty_bar + 8 * st, ph ^ 1u)) { atomicExch(misc + 1, 1u); break; }
+                if (!mbar_wait(empty_bar + 8 * st, ph ^ 1u, a.limit)) { atomicExch(misc + 1, 1u); break; }
                 if (*(volatile uint32_t*)(misc + 1)) break;
+                if (withhold && i == 0) continue;     // test: tile 0 never arrives
                 mbar_arrive_tx(full_bar + 8 * st, (uint32_t)(nA * kAtomBytes));
                 const int tok0 = (t_begin + i) * kTile;
                 for (int at = 0; at < nA; ++at) {
@@ -403,7 +407,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             // drain: every copy this thread issued has landed before exit
             for (int i = armed - NS > 0 ? armed - NS : 0; i < armed; ++i)
-                mbar_wait(full_bar + 8 * (i % NS), (uint32_t)(i / NS) & 1u);
+                if (!(withhold && i == 0)) mbar_wait(full_bar + 8 * (i % NS), (uint32_t)(i / NS) & 1u, a.limit);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -417,8 +421,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int i = 0; i < n_tiles; ++i) {
                 const int st = i % NS, acc = i & 1;
                 const uint32_t ph = (uint32_t)(i / NS) & 1u, aph = (uint32_t)(i >> 1) & 1u;
-                if (!mbar_wait(tempty_bar + 8 * acc, aph ^ 1u)) { atomicExch(misc + 1, 1u); break; }
-                if (!mbar_wait(full_bar + 8 * st, ph)) { atomicExch(misc + 1, 1u); break; }
+                if (!mbar_wait(tempty_bar + 8 * acc, aph ^ 1u, a.limit)) { atomicExch(misc + 1, 1u); break; }
+                if (!mbar_wait(full_bar + 8 * st, ph, a.limit)) { atomicExch(misc + 1, 1u); break; }
                 if (*(volatile uint32_t*)(misc + 1)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + (uint32_t)acc * acc_cols;
@@ -435,7 +439,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             // drain: the last accumulators are complete before tensor memory is freed
             for (int i = issued - 2 > 0 ? issued - 2 : 0; i < issued; ++i)
-                mbar_wait(tfull_bar + 8 * (i & 1), (uint32_t)(i >> 1) & 1u);
+                mbar_wait(tfull_bar + 8 * (i & 1), (uint32_t)(i >> 1) & 1u, a.limit);
         }
         __syncwarp();
     } else {
@@ -464,7 +468,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const float xnt_in = load_norm && valid ? __ldg(a.xnorm + (int64_t)h * a.n_tokens + tok) : 0.0f;
             // so is the row's previous id, when changes are recorded
             const uint32_t old_id = a.chg_parts && valid ? a.ids[(int64_t)h * a.cap + a.tok_offset + tok] : 0u;
-            const bool ok = mbar_wait(tfull_bar + 8 * g, aph) && mbar_wait(full_bar + 8 * st, ph);
+            const bool ok = mbar_wait(tfull_bar + 8 * g, aph, a.limit) && mbar_wait(full_bar + 8 * st, ph, a.limit);
             const uint8_t* xs = Xs + (size_t)st * nA * kAtomBytes;
             const uint32_t taddr =
                 tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)g * acc_cols + 32u * (uint32_t)(hf * NWH);
@@ -715,6 +719,10 @@ cudaError_t assign_tc_d(int H, const AssignArgs& a, bool* launched, cudaStream_t
     t.xnorm = a.xnorm;
     t.xnorm_mode = a.xnorm ? a.xnorm_mode : kNormCompute;
     t.chg_tok = a.chg_tok; t.chg_on = a.chg_on; t.chg_parts = a.chg_parts; t.chg_stride = a.chg_stride;
+    CodecCtl ctl;
+    if (!codec_ctl(&ctl)) return cudaSuccess;
+    t.limit = ctl.limit;
+    t.dbg = ctl.flags;
     if (a.chg_parts && t.ctas_per_head > kChgParts) t.ctas_per_head = kChgParts;   // one record range per CTA
     // as many token stages (up to four) as fit in shared memory, at least two
     t.stages = kMaxStages;

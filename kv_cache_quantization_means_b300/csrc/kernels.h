@@ -134,6 +134,19 @@ cudaError_t read_codec_error(uint32_t* out, bool clear, cudaStream_t s);
 // device), or nullptr when the lookup fails.
 uint32_t* codec_error_word();
 cudaError_t set_codec_debug(unsigned long long wait_limit_ns, uint32_t flags, cudaStream_t s);
+// What the kernels with bounded waits read at launch: the device error word
+// of the current device (0x7E000000 once a wait ran out, for the kernels
+// without a workspace), the wait limit in ns and the test flags (bit 0: each
+// CTA's copy producer withholds its first copy, so that the first wait on it
+// runs out).
+struct CodecCtl {
+    uint32_t* err;
+    unsigned long long limit;
+    uint32_t flags;
+};
+// The current device's control block (the error word's address is looked up
+// once per device); false when the lookup fails.
+bool codec_ctl(CodecCtl* ctl);
 cudaError_t launch_kmeans_init(int D, const uint16_t* x, int64_t head_stride, int64_t token_stride,
                                int64_t n_tokens, const uint16_t* warm, int H, int C, uint16_t* cent,
                                cudaStream_t s);

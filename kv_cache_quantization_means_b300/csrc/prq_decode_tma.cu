@@ -41,20 +41,6 @@
 
 namespace qvg {
 
-// What the persistent decoder needs for its bounded waits: the
-// device error word of the current device (0x7E000000 once a wait ran out),
-// the wait limit in ns and the test flags (bit 0: each CTA's producer
-// withholds its first copy, so that the first consumer wait runs out).
-struct CodecCtl {
-    uint32_t* err;
-    unsigned long long limit;
-    uint32_t flags;
-};
-
-// The current device's control block (the error word's address is looked up
-// once per device); false when the lookup fails.
-bool codec_ctl(CodecCtl* ctl);
-
 namespace {
 
 // 15 consumer warps + the producer = 16 warps, four per scheduler, which

@@ -53,14 +53,14 @@ __device__ __forceinline__ uint64_t global_ns() {
     return t;
 }
 
-// Waits for the phase of parity `parity` to complete; gives up after about
-// two seconds and returns false.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Waits for the phase of parity `parity` to complete; gives up after
+// limit_ns (about two seconds by default) and returns false.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned long long limit_ns = 2000000000ull) {
     if (mbar_try(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try(bar, parity)) return true;
-        if ((it & 15u) == 0 && global_ns() - t0 > 2000000000ull) return false;
+        if ((it & 15u) == 0 && global_ns() - t0 > limit_ns) return false;
     }
 }
 

@@ -145,11 +145,16 @@ def qvg_workspace_bytes(cfg, n_tokens):
     return b.value
 
 
-def qvg_fit_stats(cfg, n_tokens, workspace, stream=None):
+def qvg_fit_stats(cfg, n_tokens, workspace, stream=None, with_status=False):
+    """The four counters; with_status=True returns (status, counters) and
+    accepts QVG_ERR_TIMEOUT (error word set) instead of raising."""
     out = (ctypes.c_uint64 * 4)()
-    _check(load().qvg_fit_stats(ctypes.byref(cfg), n_tokens, _ptr(workspace), _nbytes(workspace), out,
-                                _stream(stream)))
-    return tuple(int(v) for v in out)
+    st = load().qvg_fit_stats(ctypes.byref(cfg), n_tokens, _ptr(workspace), _nbytes(workspace), out,
+                              _stream(stream))
+    if not (with_status and st == QVG_ERR_TIMEOUT):
+        _check(st)
+    stats = tuple(int(v) for v in out)
+    return (st, stats) if with_status else stats
 
 
 def qvg_device_error(clear=False, stream=None):
