@@ -374,6 +374,33 @@ QVG_API qvg_status qvg_attention_decode(const qvg_config* cfg, const qvg_bf16* q
                                         float* out, int64_t out_head_stride, int64_t out_token_stride,
                                         qvg_stream stream);
 
+/* Bytes of the working buffer of qvg_attention_decode_staged for n_keys keys
+ * (0 when the tensor-core path does not apply: head_dim != 128).  Host only. */
+QVG_API qvg_status qvg_attention_workspace_bytes(const qvg_config* cfg, int64_t n_keys, size_t* bytes);
+
+/* The attention of qvg_attention_decode, same arguments and result
+ * definition, on the tensor cores (tcgen05) for head_dim 128: each group of
+ * up to four heads is first decoded into the caller's working buffer (K as
+ * rows, V transposed: 2 * min(H, 4) * n_keys * 128 bf16, sized by
+ * qvg_attention_workspace_bytes, 256-byte aligned) -- one decode of every key
+ * row per head, with a buffer small enough to stay in L2 rather than a bf16
+ * K/V of the whole history -- then 128-query tiles attend to it: S = QK^T and
+ * O += PV accumulate in tensor memory, the online softmax in fp32 runs one
+ * query row per thread, and its probabilities are rounded to bf16 for the
+ * product with v_hat.  The running maximum is raised only when a tile's
+ * exceeds it by more than a factor 2^8 (O is then rescaled); the stale
+ * maximum scales numerator and denominator alike.  Other head dims, and
+ * layouts the bulk copies cannot express, run qvg_attention_decode's kernel.
+ * A bounded wait that runs out records 0x7E000000 in the device error word
+ * (qvg_device_error).  Asynchronous; the buffer is reused group after group
+ * in stream order. */
+QVG_API qvg_status qvg_attention_decode_staged(const qvg_config* cfg, const qvg_bf16* q, int64_t n_queries,
+                                               int64_t q_head_stride, int64_t q_token_stride,
+                                               const qvg_encoded_view* k, const qvg_encoded_view* v,
+                                               int64_t capacity, int64_t n_keys, float scale, float* out,
+                                               int64_t out_head_stride, int64_t out_token_stride, void* workspace,
+                                               size_t workspace_bytes, qvg_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

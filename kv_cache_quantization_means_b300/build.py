@@ -7,7 +7,7 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
-SOURCES = ["api.cu", "prq.cu", "prq_decode_tma.cu", "kmeans.cu", "assign_tc.cu", "coral.cu", "coral_tc.cu", "coral_fit.cu", "attn.cu"]
+SOURCES = ["api.cu", "prq.cu", "prq_decode_tma.cu", "kmeans.cu", "assign_tc.cu", "coral.cu", "coral_tc.cu", "coral_fit.cu", "attn.cu", "attn_tc.cu"]
 LIB = os.path.join(HERE, "libqvg.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -828,10 +828,17 @@ qvg_status coral_sas_decode(const qvg_config* cfg, const coral_predictor* pred, 
     return cuda_status(qvg::launch_coral_recon(P, R, count, xhat_next, s), "reconstruction launch");
 }
 
-qvg_status qvg_attention_decode(const qvg_config* cfg, const qvg_bf16* q, int64_t n_queries, int64_t q_head_stride,
-                                int64_t q_token_stride, const qvg_encoded_view* k, const qvg_encoded_view* v,
-                                int64_t capacity, int64_t n_keys, float scale, float* out, int64_t out_head_stride,
-                                int64_t out_token_stride, qvg_stream stream) {
+}  // extern "C"
+
+namespace {
+
+// Validates an attention call and fills its arguments; *skip = true when
+// there is nothing to launch.
+qvg_status attention_args(const qvg_config* cfg, const qvg_bf16* q, int64_t n_queries, int64_t q_head_stride,
+                          int64_t q_token_stride, const qvg_encoded_view* k, const qvg_encoded_view* v,
+                          int64_t capacity, int64_t n_keys, float scale, float* out, int64_t out_head_stride,
+                          int64_t out_token_stride, qvg::AttnArgs* ap, bool* skip) {
+    *skip = false;
     qvg_status st = check_config(cfg, false);
     if (st) return st;
     if (cfg->head_dim != 64 && cfg->head_dim != 128)
@@ -850,7 +857,10 @@ qvg_status qvg_attention_decode(const qvg_config* cfg, const qvg_bf16* q, int64_
         if (has_c && (!e->ids || !e->centroids || !aligned16(e->centroids)))
             return fail(QVG_ERR_INVALID_ARG, "ids/centroids missing or centroids not 16-byte aligned");
     }
-    if (n_queries == 0) return ok();
+    if (n_queries == 0) {
+        *skip = true;
+        return ok();
+    }
     if ((st = check_input(cfg, q, n_queries, q_head_stride, q_token_stride, "q"))) return st;
     if (!out || !aligned16(out)) return fail(QVG_ERR_INVALID_ARG, "out must be non-NULL and 16-byte aligned");
     if (out_head_stride % 4 || out_token_stride % 4 || out_head_stride < 0 || out_token_stride < 0)
@@ -863,7 +873,53 @@ qvg_status qvg_attention_decode(const qvg_config* cfg, const qvg_bf16* q, int64_
     a.out = out; a.out_head_stride = out_head_stride; a.out_token_stride = out_token_stride;
     a.H = cfg->num_heads; a.C = cfg->num_clusters; a.S = cfg->num_stages; a.G = cfg->group_size; a.bits = cfg->bits;
     a.scale_log2 = scale * 1.4426950408889634f;
+    *ap = a;
+    return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+qvg_status qvg_attention_decode(const qvg_config* cfg, const qvg_bf16* q, int64_t n_queries, int64_t q_head_stride,
+                                int64_t q_token_stride, const qvg_encoded_view* k, const qvg_encoded_view* v,
+                                int64_t capacity, int64_t n_keys, float scale, float* out, int64_t out_head_stride,
+                                int64_t out_token_stride, qvg_stream stream) {
+    qvg::AttnArgs a;
+    bool skip = false;
+    qvg_status st = attention_args(cfg, q, n_queries, q_head_stride, q_token_stride, k, v, capacity, n_keys, scale,
+                                   out, out_head_stride, out_token_stride, &a, &skip);
+    if (st || skip) return st;
     return cuda_status(qvg::launch_attention_decode(cfg->head_dim, a, (cudaStream_t)stream), "attention launch");
+}
+
+qvg_status qvg_attention_workspace_bytes(const qvg_config* cfg, int64_t n_keys, size_t* bytes) {
+    qvg_status st = check_config(cfg, false);
+    if (st) return st;
+    if (!bytes) return fail(QVG_ERR_INVALID_ARG, "bytes is NULL");
+    if (n_keys < 0) return fail(QVG_ERR_INVALID_ARG, "negative key count");
+    *bytes = cfg->head_dim == 128 ? qvg::attention_staged_bytes(cfg->head_dim, cfg->num_heads, n_keys) : 0;
+    return ok();
+}
+
+qvg_status qvg_attention_decode_staged(const qvg_config* cfg, const qvg_bf16* q, int64_t n_queries,
+                                       int64_t q_head_stride, int64_t q_token_stride, const qvg_encoded_view* k,
+                                       const qvg_encoded_view* v, int64_t capacity, int64_t n_keys, float scale,
+                                       float* out, int64_t out_head_stride, int64_t out_token_stride,
+                                       void* workspace, size_t workspace_bytes, qvg_stream stream) {
+    qvg::AttnArgs a;
+    bool skip = false;
+    qvg_status st = attention_args(cfg, q, n_queries, q_head_stride, q_token_stride, k, v, capacity, n_keys, scale,
+                                   out, out_head_stride, out_token_stride, &a, &skip);
+    if (st || skip) return st;
+    const size_t need = cfg->head_dim == 128 ? qvg::attention_staged_bytes(cfg->head_dim, cfg->num_heads, n_keys) : 0;
+    if (need && (!workspace || ((uintptr_t)workspace & 255u)))
+        return fail(QVG_ERR_INVALID_ARG, "workspace NULL or not 256-byte aligned (need %zu bytes)", need);
+    if (workspace_bytes < need) return fail(QVG_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
+    bool launched = false;
+    cudaError_t e = qvg::launch_attention_staged(cfg->head_dim, a, workspace, workspace_bytes, &launched, (cudaStream_t)stream);
+    if (e == cudaSuccess && !launched) e = qvg::launch_attention_decode(cfg->head_dim, a, (cudaStream_t)stream);
+    return cuda_status(e, "attention launch");
 }
 
 }  // extern "C"

@@ -65,39 +65,6 @@ __device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Decodes channels 16c .. 16c+15 of row n of one encoded tensor to bf16.
-template <int D, int B>
-__device__ __forceinline__ void decode_chunk(const uint32_t* codes, const uint32_t* meta, const uint8_t* ids,
-                                             const uint16_t* cent, int64_t row, int h, int c, int64_t stage_rows,
-                                             int C, int S, int G, uint4& o0, uint4& o1) {
-    constexpr int WPT = B / 2;          // code words per 16 channels and stage
-    constexpr int WPR = D * B / 32;     // code words per row and stage
-    const int mpr = D / G;
-    float acc[16];
-    if (C > 0) {
-        const int id = ids[row];
-        const uint16_t* cr = cent + ((int64_t)h * C + min(id, C - 1)) * D + c * 16;
-        const uint4 c0 = __ldg(reinterpret_cast<const uint4*>(cr));
-        const uint4 c1 = __ldg(reinterpret_cast<const uint4*>(cr + 8));
-        unpack16(c0, c1, acc);
-    } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
-    }
-    for (int s = 0; s < S; ++s) {
-        const int64_t srow = (int64_t)s * stage_rows + row;
-        const uint32_t* cw = codes + srow * WPR + c * WPT;
-        const uint32_t mw = __ldg(meta + srow * mpr + (c * 16) / G);
-        if constexpr (B == 2) {
-            dequant_add16(acc, __ldg(cw), mw);
-        } else {
-            dequant_add8x4(acc, __ldg(cw), mw);
-            dequant_add8x4(acc + 8, __ldg(cw + 1), mw);
-        }
-    }
-    pack16_bf16(acc, o0, o1);
-}
-
 // PF: the next key tile's ids, code words and meta words are loaded into
 // registers before the current tile's products, so that their latency is
 // spent under the tensor work (needs S * B / 2 <= 2 code words and S <= 2

@@ -24,4 +24,13 @@ struct AttnArgs {
 // cudaErrorInvalidValue for any other head dimension or code width.
 cudaError_t launch_attention_decode(int D, const AttnArgs& a, cudaStream_t s);
 
+// The tensor-core path (attn_tc.cu): groups of kAttnGroupHeads heads decoded
+// into a working buffer of attention_staged_bytes, then attended.  D = 128;
+// *launched = false (cudaSuccess) when the shape, layout or buffer is outside
+// what it handles.
+constexpr int kAttnGroupHeads = 4;
+size_t attention_staged_bytes(int D, int H, int64_t n_keys);
+cudaError_t launch_attention_staged(int D, const AttnArgs& a, void* ws, size_t ws_bytes, bool* launched,
+                                    cudaStream_t s);
+
 }  // namespace qvg

@@ -8,7 +8,8 @@
 
 `unit` runs one (layer, tensor) of the Wan2.1-shaped cache (12 heads x 32760
 tokens x 128, C = 256, T = 4, S = 2, G = 64): a fit, then one more assign,
-update, encode and decode.  `coral` runs one cross-layer layer (16 heads x
+update, encode and decode.  `attn` runs the attention over a compressed history, the tensor-core
+(staged) entry point and the in-CTA fused one.  `coral` runs one cross-layer layer (16 heads x
 16384 tokens x 128, rank 32, S = 2, G = 64): encode then decode, and checks
 that both rebuild the same x_hat.  Without `time` each kernel runs once (the
 form to put under a profiler); with `time` each call is replayed from a CUDA
@@ -167,14 +168,21 @@ def attn_case(timed):
     qd = torch.from_numpy(np.ascontiguousarray(q).view(np.int16)).cuda()
     out = torch.empty((Nq, H, D), dtype=torch.float32, device="cuda")
     scale = float(np.float32(D ** -0.5))
-    f = lambda: Q.qvg_attention_decode(cfg, qd, Nq, D, H * D, views[0], views[1], N, N, scale, out, D, H * D)
-    f()
+    aws = torch.empty(Q.qvg_attention_workspace_bytes(cfg, N), dtype=torch.uint8, device="cuda")
+    calls = {
+        "staged": lambda: Q.qvg_attention_decode_staged(cfg, qd, Nq, D, H * D, views[0], views[1], N, N, scale, out,
+                                                        D, H * D, aws),
+        "fused": lambda: Q.qvg_attention_decode(cfg, qd, Nq, D, H * D, views[0], views[1], N, N, scale, out, D, H * D),
+    }
+    for f in calls.values():
+        f()
     torch.cuda.synchronize()
     assert torch.isfinite(out).all()
     if timed:
-        t = _graph_time_us(f, reps=5, inner=3)
-        print(f"attention {t:9.1f} us   {4.0 * H * Nq * N * D / t / 1e6:8.1f} TFLOP/s   "
-              f"{2 * H * N * D * 2 / t / 1e3:8.1f} GB/s of bf16 K+V attended")
+        for name, f in calls.items():
+            t = _graph_time_us(f, reps=5, inner=3)
+            print(f"attention ({name}) {t:9.1f} us   {4.0 * H * Nq * N * D / t / 1e6:8.1f} TFLOP/s   "
+                  f"{2 * H * N * D * 2 / t / 1e3:8.1f} GB/s of bf16 K+V attended")
 
 
 def main(argv):

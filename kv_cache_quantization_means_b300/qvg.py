@@ -20,6 +20,7 @@ EXPORTS = [
     "qvg_assign", "qvg_update", "qvg_encode", "qvg_decode", "qvg_append_chunk", "qvg_decode_cache",
     "coral_predict_encode", "coral_predict_decode", "coral_predict_encode_static", "coral_fit_block",
     "coral_sas_workspace_bytes", "coral_sas_encode", "coral_sas_decode", "qvg_attention_decode",
+    "qvg_attention_workspace_bytes", "qvg_attention_decode_staged",
     "qvg_device_error", "qvg_debug_set_wait",
 ]
 
@@ -90,6 +91,10 @@ def load(path=LIB_PATH):
     L.coral_sas_decode.argtypes = [PCFG, ctypes.POINTER(coral_predictor), P, I64, P, P, P, P, P, P, P, SZ, P]
     L.qvg_attention_decode.argtypes = [PCFG, P, I64, I64, I64, ctypes.POINTER(qvg_encoded_view),
                                        ctypes.POINTER(qvg_encoded_view), I64, I64, ctypes.c_float, P, I64, I64, P]
+    L.qvg_attention_workspace_bytes.argtypes = [PCFG, I64, PSZ]
+    L.qvg_attention_decode_staged.argtypes = [PCFG, P, I64, I64, I64, ctypes.POINTER(qvg_encoded_view),
+                                              ctypes.POINTER(qvg_encoded_view), I64, I64, ctypes.c_float, P, I64,
+                                              I64, P, ctypes.c_size_t, P]
     L.qvg_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), I32, P]
     L.qvg_debug_set_wait.argtypes = [ctypes.c_uint64, ctypes.c_uint32, P]
     for name in EXPORTS[2:]:
@@ -280,6 +285,22 @@ def qvg_attention_decode(cfg, q, n_queries, q_head_stride, q_token_stride, k, v,
     _check(load().qvg_attention_decode(ctypes.byref(cfg), _ptr(q), n_queries, q_head_stride, q_token_stride,
                                        ctypes.byref(k), ctypes.byref(v), capacity, n_keys, float(scale), _ptr(out),
                                        out_head_stride, out_token_stride, _stream(stream)))
+
+
+def qvg_attention_workspace_bytes(cfg, n_keys):
+    b = ctypes.c_size_t(0)
+    _check(load().qvg_attention_workspace_bytes(ctypes.byref(cfg), n_keys, ctypes.byref(b)))
+    return b.value
+
+
+def qvg_attention_decode_staged(cfg, q, n_queries, q_head_stride, q_token_stride, k, v, capacity, n_keys, scale,
+                                out, out_head_stride, out_token_stride, workspace, stream=None):
+    """k, v: qvg_encoded_view structs; workspace: a device buffer of at least
+    qvg_attention_workspace_bytes (or None when that is 0)."""
+    _check(load().qvg_attention_decode_staged(ctypes.byref(cfg), _ptr(q), n_queries, q_head_stride, q_token_stride,
+                                              ctypes.byref(k), ctypes.byref(v), capacity, n_keys, float(scale),
+                                              _ptr(out), out_head_stride, out_token_stride, _ptr(workspace),
+                                              _nbytes(workspace), _stream(stream)))
 
 
 # -------------------------------------------------- allocation conveniences --

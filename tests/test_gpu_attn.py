@@ -19,7 +19,13 @@ arithmetic (its decoded K/V rows are the decoder's, bit for bit):
              at most 2^-9 * Ew|v_d|.
   sums       fp32 accumulation of P V and of the denominator: four MMA
              accumulations and one rescale per 64-key tile, plus exp2f's
-             2 ulps: (5 * tiles + 16) * 2^-23 * Ew|v_d|.
+             2 ulps: (5 * tiles + 16) * 2^-23 * Ew|v_d|, tiles = n_keys / 64
+             rounded up.  The tensor-core path accumulates eight K = 16
+             products and at most one rescale per 128-key tile (9 roundings
+             per 128 keys, within the 10 allowed) and sums each tile's
+             probabilities in four partial sums of 32 before adding them to
+             the denominator ((34 + n_keys / 128) * 2^-24 relative, within
+             the same allowance).
 """
 import numpy as np
 import pytest
@@ -94,7 +100,18 @@ def device_views(Q, codes, meta, ids, cent):
     return bufs, Q.encoded_view(bufs)
 
 
-def run_attention(Q, cfg, q_nhd, kb, vb, cap, n_keys, scale, token_major=True, out_pad=0):
+def attend(Q, cfg, q, Nq, qhs, qts, kb, vb, cap, n_keys, scale, out, ohs, ots, staged):
+    """qvg_attention_decode, or qvg_attention_decode_staged with a working
+    buffer of the size the library asks for."""
+    if not staged:
+        Q.qvg_attention_decode(cfg, q, Nq, qhs, qts, kb[1], vb[1], cap, n_keys, scale, out, ohs, ots)
+        return
+    nb = Q.qvg_attention_workspace_bytes(cfg, n_keys)
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda") if nb else None
+    Q.qvg_attention_decode_staged(cfg, q, Nq, qhs, qts, kb[1], vb[1], cap, n_keys, scale, out, ohs, ots, ws)
+
+
+def run_attention(Q, cfg, q_nhd, kb, vb, cap, n_keys, scale, token_major=True, out_pad=0, staged=False):
     """q_nhd: bf16 bits [Nq][H][D].  Returns fp32 [H][Nq][D]."""
     Nq, H, D = q_nhd.shape
     if token_major:
@@ -108,7 +125,7 @@ def run_attention(Q, cfg, q_nhd, kb, vb, cap, n_keys, scale, token_major=True, o
         qhs, qts = Nq * D, D
         ohs, ots = Nq * D + out_pad, D
         out = torch.full((H * ohs + 4,), float("nan"), dtype=torch.float32, device="cuda")
-    Q.qvg_attention_decode(cfg, q, Nq, qhs, qts, kb[1], vb[1], cap, n_keys, scale, out, ohs, ots)
+    attend(Q, cfg, q, Nq, qhs, qts, kb, vb, cap, n_keys, scale, out, ohs, ots, staged)
     torch.cuda.synchronize()
     o = out.cpu().numpy()
     res = np.empty((H, Nq, D))
@@ -130,11 +147,14 @@ CASES = [  # D, bits, S, G, C, token-major
 ]
 
 
+@pytest.mark.parametrize("staged", [False, True])
 @pytest.mark.parametrize("D,bits,S,G,C,token_major", CASES)
-def test_attention_matches_oracle(qvg, oracle, D, bits, S, G, C, token_major):
-    """Two heads, 300 keys (four full 64-key tiles and a ragged one) inside a
-    320-row encoding whose last 20 rows hold random words, 100 queries (one
-    full 64-query tile and a ragged one)."""
+def test_attention_matches_oracle(qvg, oracle, D, bits, S, G, C, token_major, staged):
+    """Two heads, 300 keys (four full 64-key tiles and a ragged one; two full
+    128-key tiles and a ragged one) inside a 320-row encoding whose last 20
+    rows hold random words, 100 queries (one full 64-query tile and a ragged
+    one; one ragged 128-query tile).  staged: the tensor-core entry point
+    (head_dim 64 takes its fallback to the fused kernel)."""
     rng = np.random.default_rng(1000 + D + 10 * bits + S + G + C)
     H, N, cap, Nq = 2, 300, 320, 100
     cfg = qvg.config(H, D, C, 2, S, G, bits)
@@ -148,7 +168,7 @@ def test_attention_matches_oracle(qvg, oracle, D, bits, S, G, C, token_major):
                       None if vi is None else pad_rows(vi, cap, rng, 1), vx)
     q = np.stack([mixture(rng, Nq, D) for _ in range(H)], axis=1)     # [Nq][H][D]
     scale = float(np.float32(D ** -0.5))
-    got, raw, (ohs, ots) = run_attention(qvg, cfg, q, kb, vb, cap, N, scale, token_major, out_pad=4)
+    got, raw, (ohs, ots) = run_attention(qvg, cfg, q, kb, vb, cap, N, scale, token_major, out_pad=4, staged=staged)
     for h in range(H):
         ref = oracle.attention(q[:, h], kdec[h], vdec[h], scale)
         tol = tolerance(q[:, h], kdec[h], vdec[h], ref, scale, N)
@@ -162,7 +182,8 @@ def test_attention_matches_oracle(qvg, oracle, D, bits, S, G, C, token_major):
     assert np.all(np.isnan(raw[~written]))
 
 
-def test_attention_single_key_is_exact(qvg, oracle):
+@pytest.mark.parametrize("staged", [False, True])
+def test_attention_single_key_is_exact(qvg, oracle, staged):
     """With one key every weight is exactly 1 (exp2(0) = 1, bf16(1) = 1), so
     every output row is the decoded value row, bit for bit in fp32."""
     rng = np.random.default_rng(5)
@@ -174,7 +195,7 @@ def test_attention_single_key_is_exact(qvg, oracle):
     vc, vm, vi, vx, vdec = oracle_encoding(oracle, xv, C, S, G, 2)
     kb, vb = device_views(qvg, kc, km, ki, kx), device_views(qvg, vc, vm, vi, vx)
     q = np.stack([mixture(rng, 70, D) for _ in range(H)], axis=1)
-    got, _, _ = run_attention(qvg, cfg, q, kb, vb, cap, 1, 0.3)
+    got, _, _ = run_attention(qvg, cfg, q, kb, vb, cap, 1, 0.3, staged=staged)
     for h in range(H):
         np.testing.assert_array_equal(got[h], np.broadcast_to(SY.bf16_bits_to_f32(vdec[h, 0]), got[h].shape))
 
@@ -203,7 +224,8 @@ def test_attention_zero_queries_and_mean(qvg, oracle):
         assert np.all(np.abs(got[h] - ref) <= tolerance(q[:, h], kdec[h], vdec[h], ref, 0.125, N))
 
 
-def test_attention_full_size_sampled_rows(qvg, oracle):
+@pytest.mark.parametrize("staged", [False, True])
+def test_attention_full_size_sampled_rows(qvg, oracle, staged):
     """The Wan2.1 shape in the bench's launch configuration: 12 heads, a chunk
     of 4680 queries (token-major) over 32760 compressed keys (C = 256, S = 2,
     G = 64), random but legal encodings.  Sampled query rows of every head are
@@ -231,7 +253,7 @@ def test_attention_full_size_sampled_rows(qvg, oracle):
     scale = float(np.float32(D ** -0.5))
     qd = to_dev(np.ascontiguousarray(q).reshape(-1))
     out = torch.empty((Nq, H, D), dtype=torch.float32, device="cuda")
-    qvg.qvg_attention_decode(cfg, qd, Nq, D, H * D, kb[1], vb[1], N, N, scale, out, D, H * D)
+    attend(qvg, cfg, qd, Nq, D, H * D, kb, vb, N, N, scale, out, D, H * D, staged)
     torch.cuda.synchronize()
     got = out.cpu().numpy()
     rows = sorted({0, 63, 64, 2345, 4607, 4608} | {row for _, row, _ in probes})
