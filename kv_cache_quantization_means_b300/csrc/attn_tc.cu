@@ -19,20 +19,25 @@
 // tiles from there; then the next group reuses the buffer.  No bf16 K/V of the
 // whole history is ever formed.
 //
-// Attention kernel: one CTA per (head, 128 queries), 6 warps.
+// Attention kernel: one CTA per (head, 128 queries), 2 + 4 kFaNG warps.
 //   warp 0   bulk tensor copies: the query tile once, then per 128-key tile
-//            the K tile and the V^T tile into a ring of two stages;
+//            the K tile (one lane, a ring of three) and the V^T tile (another
+//            lane, a ring of two); a K tile is released when its scores are
+//            computed, a V^T tile when its product is;
 //   warp 1   tcgen05.mma issuer: S_j = Q K_j^T into one of two tensor-memory
 //            score buffers (128 x 128 fp32), then O += P_{j-1} V_{j-1} into
 //            the output accumulator (128 x D fp32), P from shared memory;
-//   warps 2-5 softmax, one query row per thread (its tensor-memory lane):
-//            scores scaled to base-2 units, the running maximum m and sum l,
-//            p = exp2(t - m) rounded to bf16 into P.  The maximum is only
-//            raised when a tile's exceeds it by more than 8 (a factor 2^8),
-//            and then O is rescaled in tensor memory; otherwise the stale m
-//            keeps every p below 2^8, which changes no rounding (powers of
-//            two) and cannot overflow.  The tile's p are summed in four
-//            partial sums and then added to l.
+//   the other warps softmax: the kFaNG warps on a tensor-memory lane quadrant
+//            take 128 / kFaNG of each row's columns each and trade the row maximum
+//            through shared memory.  Scores in base-2 units t = RN(s c),
+//            c = scale log2(e); the running maximum m and sum l; p =
+//            exp2(t - m) (ex2.approx, subnormals flushed) rounded to bf16
+//            into P.  The maximum is only raised when a tile's exceeds it by
+//            more than 8 (a factor 2^8), and then O is rescaled in tensor
+//            memory; otherwise the stale m keeps every p below 2^8, which
+//            changes no rounding (powers of two) and cannot overflow.  Each
+//            group sums its p in four partial sums into its own l; the
+//            groups' l are added at the end.
 // Every wait is bounded; a wait that runs out records 0x7E000000 in the
 // library's device error word, the roles drain what they issued and return.
 #include <math.h>
@@ -49,19 +54,26 @@ namespace {
 
 constexpr int kFaQ = 128;                 // queries per CTA
 constexpr int kFaK = 128;                 // keys per tile
-constexpr int kFaNS = 2;                  // K/V stages
-constexpr int kFaThreads = 192;
+constexpr int kFaNG = 2;                  // softmax column groups: each row's S and O columns split in kFaNG parts
+constexpr int kFaSoftWarps = 4 * kFaNG;
+constexpr int kFaThreads = 32 * (2 + kFaSoftWarps);   // warp 0 copies, warp 1 MMA, the rest softmax
 constexpr uint32_t kFaAtom = 128u * 128u; // one 64-element slab of 128 rows, 128-byte swizzle
 constexpr uint32_t kFaErrTimeout = 0x7E000000u;
 constexpr int kStageRows = 64;            // rows per CTA of the staging decode
 
-// shared memory map (offsets from the 1024-byte aligned base)
+// shared memory map (offsets from the 1024-byte aligned base): Q, a ring of
+// kFaKS K tiles and one of kFaVS V^T tiles (K_j is released as soon as S_j
+// has been computed, V_j after O += P_j V_j), P, barriers, exchange words
+constexpr int kFaKS = 3, kFaVS = 2;
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffKV = 2 * kFaAtom;                       // stage st: K at +0, V^T at +2 atoms
-constexpr uint32_t kOffP = kOffKV + kFaNS * 4 * kFaAtom;
+constexpr uint32_t kOffK = 2 * kFaAtom;
+constexpr uint32_t kOffV = kOffK + kFaKS * 2 * kFaAtom;
+constexpr uint32_t kOffP = kOffV + kFaVS * 2 * kFaAtom;
 constexpr uint32_t kOffBar = kOffP + 2 * kFaAtom;
-constexpr uint32_t kOffMisc = kOffBar + 128;
-constexpr uint32_t kFaSmem = kOffMisc + 16 + 1024;             // + alignment slack
+constexpr uint32_t kOffMisc = kOffBar + 160;
+constexpr uint32_t kOffX = kOffMisc + 16;                      // row maxima / sums / flags traded by the groups
+constexpr uint32_t kFaSmem = kOffX + kFaNG * 128 * 4 + 2 * kFaNG * 128 + 1024;   // + alignment slack
+static_assert(kFaSmem <= 232448, "shared memory of one CTA");
 
 struct FaArgs {
     int64_t n_queries, n_keys;
@@ -86,9 +98,20 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* v) {
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
-           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+// 2^x by the hardware approximation (ex2.approx, subnormal results flushed
+// to zero: a probability below 2^-126 weighs nothing next to the row's
+// largest, which is at least 1).
+__device__ __forceinline__ float ex2_ftz(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// bf16 of lo in the low half, of hi in the high half (round to nearest even)
+__device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
 }
 
 // ------------------------------------------------------- staging decode
@@ -152,12 +175,13 @@ __global__ void __launch_bounds__(kFaThreads, 1)
                    const __grid_constant__ CUtensorMap vmap, FaArgs a) {
     extern __shared__ __align__(1024) uint8_t fa_smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(fa_smem_raw) + 1023) & ~(uintptr_t)1023);
-    const uint32_t sQ = smem_u32(base + kOffQ), sKV = smem_u32(base + kOffKV), sP = smem_u32(base + kOffP);
+    const uint32_t sQ = smem_u32(base + kOffQ), sK = smem_u32(base + kOffK), sV = smem_u32(base + kOffV),
+                   sP = smem_u32(base + kOffP);
     uint8_t* P = base + kOffP;
     const uint32_t bar0 = smem_u32(base + kOffBar);
-    const uint32_t q_full = bar0, kv_full = bar0 + 8, kv_empty = bar0 + 8 * (1 + kFaNS),
-                   s_full = bar0 + 8 * (1 + 2 * kFaNS), s_free = s_full + 16, p_full = s_free + 16,
-                   pv_done = p_full + 8;
+    const uint32_t q_full = bar0, k_full = bar0 + 8, k_empty = k_full + 8 * kFaKS, v_full = k_empty + 8 * kFaKS,
+                   v_empty = v_full + 8 * kFaVS, s_full = v_empty + 8 * kFaVS, s_free = s_full + 16,
+                   p_full = s_free + 16, pv_done = p_full + 8;
     uint32_t* misc = reinterpret_cast<uint32_t*>(base + kOffMisc);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -168,15 +192,19 @@ __global__ void __launch_bounds__(kFaThreads, 1)
 
     if (tid == 0) {
         mbar_init(q_full, 1);
-        for (int st = 0; st < kFaNS; ++st) {
-            mbar_init(kv_full + 8 * st, 1);
-            mbar_init(kv_empty + 8 * st, 1);
+        for (int st = 0; st < kFaKS; ++st) {
+            mbar_init(k_full + 8 * st, 1);
+            mbar_init(k_empty + 8 * st, 1);
+        }
+        for (int st = 0; st < kFaVS; ++st) {
+            mbar_init(v_full + 8 * st, 1);
+            mbar_init(v_empty + 8 * st, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(s_full + 8 * b, 1);
-            mbar_init(s_free + 8 * b, 4);
+            mbar_init(s_free + 8 * b, kFaSoftWarps);
         }
-        mbar_init(p_full, 4);
+        mbar_init(p_full, kFaSoftWarps);
         mbar_init(pv_done, 1);
         misc[1] = 0;
         fence_mbar_init();
@@ -193,7 +221,7 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     const uint32_t tmem = misc[0];
 
     if (warp == 0) {
-        // ------------------------------------------------ copies
+        // ------------------------------------------------ copies: lane 0 Q and K, lane 1 V^T
         if (lane == 0) {
             mbar_arrive_tx(q_full, 2 * kFaAtom);
             for (int at = 0; at < 2; ++at) {
@@ -202,22 +230,32 @@ __global__ void __launch_bounds__(kFaThreads, 1)
             }
             int armed = 0;
             for (int j = 0; j < nkt; ++j) {
-                const int st = j % kFaNS;
-                const uint32_t ph = (uint32_t)(j / kFaNS) & 1u;
-                if (!mbar_wait(kv_empty + 8 * st, ph ^ 1u, lim)) { atomicExch(misc + 1, 1u); break; }
+                const int st = j % kFaKS;
+                if (!mbar_wait(k_empty + 8 * st, ((uint32_t)(j / kFaKS) & 1u) ^ 1u, lim)) { atomicExch(misc + 1, 1u); break; }
                 if (*(volatile uint32_t*)(misc + 1)) break;
-                const uint32_t dst = sKV + (uint32_t)st * 4 * kFaAtom;
-                mbar_arrive_tx(kv_full + 8 * st, 4 * kFaAtom);
-                for (int at = 0; at < 2; ++at) {
-                    tma_load_3d(dst + at * kFaAtom, &kmap, kv_full + 8 * st, 64 * at, j * kFaK, hh);
-                    tma_load_3d(dst + (2 + at) * kFaAtom, &vmap, kv_full + 8 * st, j * kFaK + 64 * at, 0, hh);
-                }
+                const uint32_t dst = sK + (uint32_t)st * 2 * kFaAtom;
+                mbar_arrive_tx(k_full + 8 * st, 2 * kFaAtom);
+                for (int at = 0; at < 2; ++at) tma_load_3d(dst + at * kFaAtom, &kmap, k_full + 8 * st, 64 * at, j * kFaK, hh);
                 armed = j + 1;
             }
             // drain: every copy issued has landed before exit
             mbar_wait(q_full, 0u, lim);
-            for (int j = armed - kFaNS > 0 ? armed - kFaNS : 0; j < armed; ++j)
-                mbar_wait(kv_full + 8 * (j % kFaNS), (uint32_t)(j / kFaNS) & 1u, lim);
+            for (int j = armed - kFaKS > 0 ? armed - kFaKS : 0; j < armed; ++j)
+                mbar_wait(k_full + 8 * (j % kFaKS), (uint32_t)(j / kFaKS) & 1u, lim);
+        } else if (lane == 1) {
+            int armed = 0;
+            for (int j = 0; j < nkt; ++j) {
+                const int st = j % kFaVS;
+                if (!mbar_wait(v_empty + 8 * st, ((uint32_t)(j / kFaVS) & 1u) ^ 1u, lim)) { atomicExch(misc + 1, 1u); break; }
+                if (*(volatile uint32_t*)(misc + 1)) break;
+                const uint32_t dst = sV + (uint32_t)st * 2 * kFaAtom;
+                mbar_arrive_tx(v_full + 8 * st, 2 * kFaAtom);
+                for (int at = 0; at < 2; ++at)
+                    tma_load_3d(dst + at * kFaAtom, &vmap, v_full + 8 * st, j * kFaK + 64 * at, 0, hh);
+                armed = j + 1;
+            }
+            for (int j = armed - kFaVS > 0 ? armed - kFaVS : 0; j < armed; ++j)
+                mbar_wait(v_full + 8 * (j % kFaVS), (uint32_t)(j / kFaVS) & 1u, lim);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -229,12 +267,12 @@ __global__ void __launch_bounds__(kFaThreads, 1)
             bool ok = mbar_wait(q_full, 0u, lim);
             for (int j = 0; ok && j <= nkt; ++j) {
                 if (j < nkt) {
-                    const int st = j % kFaNS, b = j & 1;
-                    if (!(ok = mbar_wait(kv_full + 8 * st, (uint32_t)(j / kFaNS) & 1u, lim))) break;
+                    const int st = j % kFaKS, b = j & 1;
+                    if (!(ok = mbar_wait(k_full + 8 * st, (uint32_t)(j / kFaKS) & 1u, lim))) break;
                     if (!(ok = mbar_wait(s_free + 8 * b, ((uint32_t)(j >> 1) & 1u) ^ 1u, lim))) break;
                     if (*(volatile uint32_t*)(misc + 1)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t kb = sKV + (uint32_t)st * 4 * kFaAtom;
+                    const uint32_t kb = sK + (uint32_t)st * 2 * kFaAtom;
 #pragma unroll
                     for (int at = 0; at < 2; ++at)
 #pragma unroll
@@ -242,15 +280,17 @@ __global__ void __launch_bounds__(kFaThreads, 1)
                             umma_bf16(tmem + 128u * b, sw128_desc(sQ + at * kFaAtom + 32u * k),
                                       sw128_desc(kb + at * kFaAtom + 32u * k), idesc, (at | k) ? 1u : 0u);
                     umma_commit(s_full + 8 * b);
+                    umma_commit(k_empty + 8 * st);
                     last_bar = s_full + 8 * b;
                     last_ph = (uint32_t)(j >> 1) & 1u;
                 }
                 if (j >= 1) {
-                    const int jj = j - 1, st = jj % kFaNS;
+                    const int jj = j - 1, st = jj % kFaVS;
+                    if (!(ok = mbar_wait(v_full + 8 * st, (uint32_t)(jj / kFaVS) & 1u, lim))) break;
                     if (!(ok = mbar_wait(p_full, (uint32_t)jj & 1u, lim))) break;
                     if (*(volatile uint32_t*)(misc + 1)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t vb = sKV + (uint32_t)st * 4 * kFaAtom + 2 * kFaAtom;
+                    const uint32_t vb = sV + (uint32_t)st * 2 * kFaAtom;
 #pragma unroll
                     for (int at = 0; at < 2; ++at)
 #pragma unroll
@@ -258,7 +298,7 @@ __global__ void __launch_bounds__(kFaThreads, 1)
                             umma_bf16(tmem + 256u, sw128_desc(sP + at * kFaAtom + 32u * k),
                                       sw128_desc(vb + at * kFaAtom + 32u * k), idesc, (jj | at | k) ? 1u : 0u);
                     umma_commit(pv_done);
-                    umma_commit(kv_empty + 8 * st);
+                    umma_commit(v_empty + 8 * st);
                     last_bar = pv_done;
                     last_ph = (uint32_t)jj & 1u;
                 }
@@ -269,91 +309,166 @@ __global__ void __launch_bounds__(kFaThreads, 1)
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------ softmax, row = tensor-memory lane
-        const int row = 32 * (warp & 3) + lane;
-        const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+        // ------------------------------------------------ softmax
+        // row = tensor-memory lane; the kFaNG warps on a row's quadrant take
+        // CW of its S columns (keys) and of its O columns (channels) each.
+        // They trade their maxima (at the end their sums) through shared
+        // memory, so all keep the same m, and with them whether their waits
+        // succeeded, so that all leave the loop at the same point.
+        constexpr int CW = kFaK / kFaNG;
+        static_assert(CW % 32 == 0, "whole 32-column tensor-memory loads per group");
+        const int grp = (warp - 2) >> 2, quad = warp & 3;
+        const int row = 32 * quad + lane;
+        const uint32_t trow = tmem + ((uint32_t)(32 * quad) << 16);
+        float* xch = reinterpret_cast<float*>(base + kOffX);                    // [grp][row]
+        uint8_t* xok1 = base + kOffX + kFaNG * 128 * 4;                         // [grp][row]
+        uint8_t* xok2 = xok1 + kFaNG * 128;
+        auto group_sync = [&]() { asm volatile("bar.sync %0, %1;" ::"r"(1 + quad), "r"(32 * kFaNG) : "memory"); };
+        auto all_ok = [&](const uint8_t* f) {
+            bool r = true;
+#pragma unroll
+            for (int g = 0; g < kFaNG; ++g) r = r && f[g * 128 + row];
+            return r;
+        };
+        // one lane probes the barrier, the warp follows (__syncwarp orders the
+        // other lanes' reads after that lane's acquiring wait)
+        auto warp_wait = [&](uint32_t bar, uint32_t parity) -> bool {
+            uint32_t r = 0;
+            if (lane == 0) r = mbar_wait(bar, parity, lim) ? 1u : 0u;
+            r = __shfl_sync(0xffffffffu, r, 0);
+            __syncwarp();
+            return r != 0;
+        };
+        const float c2 = a.scale_log2;
         float m = -INFINITY, l = 0.0f;
         bool ok = true;
         for (int j = 0; j < nkt; ++j) {
             const int b = j & 1;
-            ok = __all_sync(0xffffffffu, mbar_wait(s_full + 8 * b, (uint32_t)(j >> 1) & 1u, lim));
-            if (!ok) break;
-            tc_fence_after();
-            uint32_t s[kFaK];
-#pragma unroll
-            for (int c = 0; c < kFaK / 32; ++c) tmem_ld32(trow + 128u * b + 32u * c, s + 32 * c);
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(s_free + 8 * b);
-            // scores in base-2 units; keys past n_keys are masked
-            const int64_t k0 = (int64_t)j * kFaK;
-            float mx = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < kFaK; ++c) {
-                float t = __uint_as_float(s[c]) * a.scale_log2;
-                if (k0 + c >= a.n_keys) t = -INFINITY;
-                s[c] = __float_as_uint(t);
-                mx = fmaxf(mx, t);
-            }
-            // P and O are free once the previous product has completed
-            if (j >= 1) {
-                ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (uint32_t)(j - 1) & 1u, lim));
-                if (!ok) break;
+            uint32_t s[CW];
+            float e0 = 0.0f;
+            bool okw = warp_wait(s_full + 8 * b, (uint32_t)(j >> 1) & 1u);
+            if (okw) {
                 tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < CW / 32; ++c) tmem_ld32(trow + 128u * b + (uint32_t)(CW * grp + 32 * c), s + 32 * c);
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s_free + 8 * b);
+                // keys past n_keys (last tile only) take the score that maps to -inf
+                if (j == nkt - 1) {
+                    const int64_t k0 = (int64_t)j * kFaK + CW * grp;
+#pragma unroll
+                    for (int c = 0; c < CW; ++c)
+                        if (k0 + c >= a.n_keys) s[c] = __float_as_uint(c2 >= 0.0f ? -INFINITY : INFINITY);
+                }
+                // the group's extreme raw score (four chains), then in base-2 units
+                float x4[4] = {__uint_as_float(s[0]), __uint_as_float(s[1]), __uint_as_float(s[2]),
+                               __uint_as_float(s[3])};
+                if (c2 >= 0.0f) {
+#pragma unroll
+                    for (int c = 4; c < CW; c += 8)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            x4[q] = c + 2 * q + 1 < CW ? fmax3(x4[q], __uint_as_float(s[c + 2 * q]), __uint_as_float(s[c + 2 * q + 1]))
+                                                       : x4[q];
+                    e0 = fmaxf(fmaxf(x4[0], x4[1]), fmaxf(x4[2], x4[3]));
+                } else {
+#pragma unroll
+                    for (int c = 4; c < CW; c += 8)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            x4[q] = c + 2 * q + 1 < CW ? fmin3(x4[q], __uint_as_float(s[c + 2 * q]), __uint_as_float(s[c + 2 * q + 1]))
+                                                       : x4[q];
+                    e0 = fminf(fminf(x4[0], x4[1]), fminf(x4[2], x4[3]));
+                }
             }
+            xch[grp * 128 + row] = e0 * c2;
+            xok1[grp * 128 + row] = okw ? 1 : 0;
+            group_sync();
+            if (!all_ok(xok1)) { ok = false; break; }
+            float mx = xch[row];
+#pragma unroll
+            for (int g = 1; g < kFaNG; ++g) mx = fmaxf(mx, xch[g * 128 + row]);
             const float m_new = fmaxf(m, mx);
-            if (__any_sync(0xffffffffu, m_new > m + 8.0f)) {
-                const bool raise = m_new > m + 8.0f;
-                const float alpha = raise ? exp2f(m - m_new) : 1.0f;
-                if (j >= 1) {
-                    uint32_t o[32];
+            // P and O are free once the previous product has completed
+            okw = j == 0 || warp_wait(pv_done, (uint32_t)(j - 1) & 1u);
+            if (okw) {
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, m_new > m + 8.0f)) {
+                    const bool raise = m_new > m + 8.0f;
+                    const float alpha = raise ? exp2f(m - m_new) : 1.0f;
+                    if (j >= 1) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        tmem_ld32(trow + 256u + 32u * c, o);
-                        tmem_wait_ld_regs(o);
+                        for (int c = 0; c < CW / 32; ++c) {
+                            uint32_t o[32];
+                            tmem_ld32(trow + 256u + (uint32_t)(CW * grp + 32 * c), o);
+                            tmem_wait_ld_regs(o);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tmem_st32(trow + 256u + 32u * c, o);
+                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                            tmem_st32(trow + 256u + (uint32_t)(CW * grp + 32 * c), o);
+                        }
+                        tmem_wait_st();
                     }
-                    tmem_wait_st();
+                    if (raise) {
+                        l *= alpha;
+                        m = m_new;
+                    }
                 }
-                if (raise) {
-                    l *= alpha;
-                    m = m_new;
-                }
-            }
-            float ps[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                // p = exp2(RN(s * c2) - m) (the row's largest score gives exactly
+                // 1), summed in four partial sums, rounded to bf16 into P
+                // (packed pairs: each lane of an fp32x2 operation rounds as the scalar one)
+                const float2 c22 = make_float2(c2, c2), m2 = make_float2(m, m);
+                float2 ps2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
-            for (int c8 = 0; c8 < kFaK / 8; ++c8) {
-                float p[8];
+                for (int c8 = 0; c8 < CW / 8; ++c8) {
+                    uint32_t w[4];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    p[e] = exp2f(__uint_as_float(s[8 * c8 + e]) - m);
-                    ps[e & 3] += p[e];
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 t = f2_sub(f2_mul(make_float2(__uint_as_float(s[8 * c8 + 2 * e]),
+                                                                   __uint_as_float(s[8 * c8 + 2 * e + 1])),
+                                                       c22),
+                                                m2);
+                        const float2 p = make_float2(ex2_ftz(t.x), ex2_ftz(t.y));
+                        ps2[e & 1] = f2_add(ps2[e & 1], p);
+                        w[e] = cvt_bf16x2(p.x, p.y);
+                    }
+                    *reinterpret_cast<uint4*>(P + sw_off(row, CW * grp + 8 * c8, kFaAtom)) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
                 }
-                const uint4 w = make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]), pack_bf16x2(p[4], p[5]),
-                                           pack_bf16x2(p[6], p[7]));
-                *reinterpret_cast<uint4*>(P + sw_off(row, 8 * c8, kFaAtom)) = w;
+                l += (ps2[0].x + ps2[1].x) + (ps2[0].y + ps2[1].y);
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_full);
             }
-            l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-            fence_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
+            xok2[grp * 128 + row] = okw ? 1 : 0;
+            group_sync();                     // also: the maxima are read before the next tile overwrites them
+            if (!all_ok(xok2)) { ok = false; break; }
         }
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (uint32_t)(nkt - 1) & 1u, lim));
-        if (!ok) {
+        if (ok) ok = warp_wait(pv_done, (uint32_t)(nkt - 1) & 1u);
+        // every group of a row reaches this trade (they leave the loop together)
+        xch[grp * 128 + row] = ok ? l : -1.0f;
+        group_sync();
+        float lsum = 0.0f;
+        bool good = ok;
+#pragma unroll
+        for (int g = 0; g < kFaNG; ++g) {
+            const float v = xch[g * 128 + row];
+            good = good && v >= 0.0f;
+            lsum += v;
+        }
+        if (!good) {
             if (lane == 0) atomicExch(misc + 1, 1u);
         } else {
             tc_fence_after();
             const int64_t qi = q0 + row;
-            const float inv = 1.0f / l;
-            float* orow = a.out + (int64_t)h * a.out_head_stride + qi * a.out_token_stride;
+            const float inv = 1.0f / lsum;
+            float* orow = a.out + (int64_t)h * a.out_head_stride + qi * a.out_token_stride + CW * grp;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < CW / 32; ++c) {
                 uint32_t o[32];
-                tmem_ld32(trow + 256u + 32u * c, o);
+                tmem_ld32(trow + 256u + (uint32_t)(CW * grp + 32 * c), o);
                 tmem_wait_ld_regs(o);
                 if (qi < a.n_queries)
 #pragma unroll
