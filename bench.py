@@ -272,9 +272,9 @@ class CoralStep:
             self.cents = [[torch.empty(H * C * D, dtype=torch.int16, device="cuda") for _ in range(layers)]
                           for _ in (0, 1)]
             # encode per layer: prediction (1 kernel at layer 0, else prep + low-rank + predict), residual,
-            # k-means init + T x (assign + hist + scatter + sum + mean), PRQ encode, decode, reconstruction;
+            # k-means init + T x (assign + update), PRQ encode, decode, reconstruction;
             # decode per layer: prediction, decode, reconstruction
-            enc = (1 + 5 + 5 * T) + (layers - 1) * (3 + 5 + 5 * T)
+            enc = (1 + 5 + 2 * T) + (layers - 1) * (3 + 5 + 2 * T)
             dec = (1 + 2) + (layers - 1) * (3 + 2)
             self.launches_per_step = 2 * (enc + dec)
 
@@ -345,10 +345,10 @@ class StreamStep:
         self.ws = Q.alloc_workspace(self.cfg, self.chunk)
         self.out = torch.empty((N, H, D), dtype=torch.int16, device="cuda")
         per_tok = H * D * 2
-        # per (layer, tensor) and step: refit (init + T x 5 kernels) or assign, encode, chunk-table
+        # per (layer, tensor) and step: refit (init + T x (assign + update)) or assign, encode, chunk-table
         # update, then the history decode
         T = wl.lloyd_iters
-        self.launches_per_step = 2 * layers * sum((1 + 5 * T if k % self.every == 0 else 1) + 2 + 1
+        self.launches_per_step = 2 * layers * sum((1 + 2 * T if k % self.every == 0 else 1) + 2 + 1
                                                   for k in range(self.steps))
         self.enc_bytes = 2 * layers * N * per_tok
         self.dec_bytes = 2 * layers * per_tok * self.chunk * sum(range(1, self.steps + 1))
@@ -378,8 +378,10 @@ class AttnStep:
     Wan2.1 shape: per layer, 12 heads x 4680 queries x 32760 keys x 128, with
     K and V of every layer fitted (C = 256, T = 4) and encoded (S = 2, G = 64)
     by the library once, outside the timed region.  A step is one
-    qvg_attention_decode per layer: keys and values decoded tile by tile in
-    shared memory, never written out as bf16."""
+    qvg_attention_decode_staged per layer: per group of four heads the keys
+    and values are decoded once into an L2-sized working buffer, then 128-query
+    tiles attend to it on the tensor cores; no bf16 K/V of the layer is
+    formed."""
 
     def __init__(self, Q, wl, layers):
         import numpy as np
@@ -407,15 +409,17 @@ class AttnStep:
         self.q = torch.from_numpy(np.ascontiguousarray(q).view(np.int16)).cuda()
         self.out = torch.empty((self.Nq, H, D), dtype=torch.float32, device="cuda")
         self.scale = float(np.float32(D ** -0.5))
-        self.launches_per_step = layers
+        self.aws = torch.empty(Q.qvg_attention_workspace_bytes(self.cfg, N), dtype=torch.uint8, device="cuda")
+        groups = (H + 3) // 4
+        self.launches_per_step = layers * 2 * groups        # a staging decode and an attention kernel per group
         self.kv_bytes = 2 * H * N * D * 2                   # bf16 K + V of one layer
         self.bytes_per_step = layers * self.kv_bytes
         self.flops_per_launch = 4.0 * H * self.Nq * N * D   # Q K^T and P V
 
     def layer(self, l):
         (_, kv), (_, vv) = self.enc[l]
-        self.Q.qvg_attention_decode(self.cfg, self.q, self.Nq, self.D, self.H * self.D, kv, vv, self.N, self.N,
-                                    self.scale, self.out, self.D, self.H * self.D)
+        self.Q.qvg_attention_decode_staged(self.cfg, self.q, self.Nq, self.D, self.H * self.D, kv, vv, self.N,
+                                           self.N, self.scale, self.out, self.D, self.H * self.D, self.aws)
 
     def step(self):
         for l in range(self.L):
@@ -671,7 +675,8 @@ def run_aux(args, Q, wl, peaks, world, rank, local):
                                "its PRQ" if args.sas else "")}
     elif args.config == "attn":
         t_att = graph_time(lambda: st.layer(0), 3)
-        dom = {"kernel": "attention_decode_kernel (K/V tiles decoded in shared memory, mma.sync bf16)",
+        dom = {"kernel": "attn_stage_kernel + attn_fa_kernel (per 4-head group: K/V decoded once into an L2-sized "
+                         "buffer; tcgen05 S=QK^T and O+=PV in tensor memory)",
                "bound": "tensor", "achieved": st.flops_per_launch / t_att / 1e12, "peak": peaks[1],
                "unit": "TFLOP/s", "time_us": t_att * 1e6}
         cfgb = attn_config_block(wl)
@@ -784,8 +789,8 @@ def main():
         barrier()
     t = max_over_ranks(a.elapsed_time(b) / 1e3 / args.steps, world, "cuda")
     value = job_throughput(st.bytes_per_step, world, t)
-    # per (layer, tensor): init + T x (assign, histogram, scatter, exact sum, mean) + encode + decode
-    launches_per_step = 2 * layers * (1 + wl.lloyd_iters * 5 + 2)
+    # per (layer, tensor): init + T x (assign, update) + encode + decode
+    launches_per_step = 2 * layers * (1 + wl.lloyd_iters * 2 + 2)
 
     roof = kernel_rooflines(st, peaks)
 
