@@ -802,11 +802,13 @@ __global__ void __launch_bounds__(kUpdThreads, 3) kmeans_update_kernel(UpdateArg
 }
 
 // Clusters per CTA: the largest power of two up to kMaxGroup that still
-// gives two CTAs per SM and lists a group's tokens at once on average.
+// gives two CTAs per SM and, on average, fills at most three quarters of the
+// list.  Every CTA scans all N ids of its head, so larger groups scan less in
+// all (H * C / G * N bytes).
 int update_group_log2(int D, int H, int C, int64_t N) {
     int lg = 0;
     while ((1 << (lg + 1)) <= kMaxGroup && (int64_t)H * ((C + (2 << lg) - 1) >> (lg + 1)) >= 2 * 148 &&
-           N * (2 << lg) <= (int64_t)C * (kListCap / 2) && (D << (lg + 1)) <= kMaxGroupChannels)
+           4 * N * (2 << lg) <= 3 * (int64_t)C * kListCap && (D << (lg + 1)) <= kMaxGroupChannels)
         ++lg;
     return lg;
 }
