@@ -386,6 +386,7 @@ __global__ void kmeans_init_kernel(const uint16_t* x, int64_t head_stride, int64
 constexpr int kUpdThreads = 256;
 constexpr int kListCap = 4096;                         // rows listed at once
 constexpr int kMaxGroup = 16;                          // clusters per CTA
+constexpr int kScanR = 2;                              // 16-byte chunks per lane and round of an id scan
 constexpr int kFlushTerms = 255;                       // window terms a lane adds between flushes (|sum| < 2^30)
 constexpr int64_t kPackLimit = (int64_t)1 << 26;       // token index packed above a 5-bit bucket
 constexpr int kMaxGroupChannels = 1024;                // G * D: the group's int64 sums fit over the two lists
@@ -438,6 +439,27 @@ __device__ __forceinline__ void for_matching_bytes(const uint8_t* p, int64_t t0,
     for (int64_t n = t0 + pre + 16 * body + threadIdx.x; n < t1; n += kUpdThreads) one(n, p[n]);
 }
 
+// 0x80 in every byte of t that is zero, nothing in the others (exact, unlike
+// the borrow-based test, which can also mark a 0x01 byte above a zero one).
+__device__ __forceinline__ uint32_t zero_bytes(uint32_t t) {
+    return ~(((t & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | t | 0x7F7F7F7Fu);
+}
+
+// All 32 lanes: lane i reserves m_i consecutive slots of *counter; returns
+// its first slot (one shared atomic per warp instead of one per entry).
+__device__ __forceinline__ int warp_reserve(int m, int* counter, int lane) {
+    int inc = m;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += u;
+    }
+    int base = 0;
+    if (lane == 31 && inc) base = atomicAdd(counter, inc);
+    base = __shfl_sync(0xffffffffu, base, 31);
+    return base + inc - m;
+}
+
 // Shared memory: the sorted list and the arrival-order list (int[kListCap]
 // each), then the window sums of the group split at bit 15 (int lo, hi
 // [G][3][D], the layout of the stored sums), which the 128-bit sums reuse.
@@ -483,12 +505,35 @@ __global__ void __launch_bounds__(kUpdThreads, 3) kmeans_update_kernel(UpdateArg
         }
         __syncthreads();
     };
-    // the arrival-order list of n_raw (n << 5 | bucket) entries, sorted
+    // bucket counts of the arrival-order list of n_raw <= kListCap entries
+    // (n << 5 | bucket) into c[nb]; lanes on the same bucket add together
+    auto count_raw = [&](int* c, int nb) {
+        if (tid < nb) c[tid] = 0;
+        __syncthreads();
+        const int n = n_raw;
+        for (int i0 = warp * 32; i0 < n; i0 += kUpdThreads) {
+            const int i = i0 + lane;
+            const int b = i < n ? (raw[i] & 31) : -1;
+            const unsigned mm = __match_any_sync(0xffffffffu, b);
+            if (b >= 0 && lane == __ffs(mm) - 1) atomicAdd(&c[b], __popc(mm));
+        }
+        __syncthreads();
+    };
+    // that list, sorted by bucket (ranks within a warp from __match_any_sync)
     auto sort_raw = [&](const int* c, int nb) {
         set_offsets(c, nb);
-        for (int i = tid; i < n_raw; i += kUpdThreads) {
-            const int v = raw[i];
-            list[atomicAdd(&cur[v & 31], 1)] = v >> 5;
+        const int n = n_raw;
+        const unsigned lt = (1u << lane) - 1u;
+        for (int i0 = warp * 32; i0 < n; i0 += kUpdThreads) {
+            const int i = i0 + lane;
+            const int v = i < n ? raw[i] : -1;
+            const int b = v >= 0 ? (v & 31) : -1;
+            const unsigned mm = __match_any_sync(0xffffffffu, b);
+            const int leader = __ffs(mm) - 1;
+            int base = 0;
+            if (b >= 0 && lane == leader) base = atomicAdd(&cur[b], __popc(mm));
+            base = __shfl_sync(0xffffffffu, base, leader);
+            if (b >= 0) list[base + __popc(mm & lt)] = v >> 5;
         }
         __syncthreads();
     };
@@ -555,25 +600,24 @@ __global__ void __launch_bounds__(kUpdThreads, 3) kmeans_update_kernel(UpdateArg
     // ... and a copy in shared memory (ksm, over the lists) for the means;
     // the stored sums are read four at a time so that their loads overlap
     long long* ksm = reinterpret_cast<long long*>(list);
+    constexpr int kFoldPer = 3 * kMaxGroupChannels / kUpdThreads;       // entries per thread, at most
     auto fold = [&](bool first) {
         __syncthreads();
         const int n3 = ng * 3 * D;
-        for (int i0 = tid; i0 < n3; i0 += 4 * kUpdThreads) {
-            long long old[4];
+        long long old[kFoldPer];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int i = i0 + r * kUpdThreads;
-                old[r] = (!first && i < n3) ? ks[i] : 0;
-            }
+        for (int r = 0; r < kFoldPer; ++r) {
+            const int i = tid + r * kUpdThreads;
+            old[r] = (!first && i < n3) ? ks[i] : 0;
+        }
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int i = i0 + r * kUpdThreads;
-                if (i < n3) {
-                    const long long v = old[r] + (long long)hi[i] * 32768 + lo[i];
-                    ks[i] = v;
-                    ksm[i] = v;
-                    lo[i] = hi[i] = 0;
-                }
+        for (int r = 0; r < kFoldPer; ++r) {
+            const int i = tid + r * kUpdThreads;
+            if (i < n3) {
+                const long long v = old[r] + (long long)hi[i] * 32768 + lo[i];
+                ks[i] = v;
+                ksm[i] = v;
+                lo[i] = hi[i] = 0;
             }
         }
         __syncthreads();
@@ -630,67 +674,100 @@ __global__ void __launch_bounds__(kUpdThreads, 3) kmeans_update_kernel(UpdateArg
         }
         __syncthreads();
         const int n_chunks = pchunk[kChgParts];
-        // f(j, v) for the bytes v of the group in chunks [cb, ce) (j: byte index in the head's rows)
-        auto scan_changes = [&](int cb, int ce, auto&& f) {
-            for (int q0 = cb + tid; q0 < ce; q0 += 4 * kUpdThreads) {
-                uint4 v[4];
-                int64_t at[4], lim[4];
+        // the chunk q of the changes: its first byte and the end of its range
+        auto locate = [&](int q, int64_t& at, int64_t& lim) {
+            int lo_p = 0, hi_p = kChgParts - 1;                    // the range holding chunk q
+            while (lo_p < hi_p) {
+                const int mid = (lo_p + hi_p + 1) >> 1;
+                if (pchunk[mid] <= q) lo_p = mid; else hi_p = mid - 1;
+            }
+            at = 2 * (int64_t)parts[lo_p].x + 16 * (int64_t)(q - pchunk[lo_p]);
+            lim = 2 * ((int64_t)parts[lo_p].x + parts[lo_p].y);
+        };
+        // the entry of change byte j (old id at even j, new at odd)
+        auto entry = [&](int64_t j, uint32_t v) {
+            const int k = (int)v - c0, leaving = (int)(~j & 1);
+            return (tk[j >> 1] << 5) | (2 * k + leaving);
+        };
+        // one scan of all chunks: every member byte appended to raw while it
+        // has room (n_raw counts them all), one shared atomic per warp and round
+        {
+            const uint32_t mask4 = keep * 0x01010101u, want4 = (uint32_t)c0 * 0x01010101u;
+            for (int q0 = warp * 32 * kScanR; q0 < n_chunks; q0 += kScanR * kUpdThreads) {
+                uint32_t w[kScanR][4], z[kScanR][4];
+                int64_t at[kScanR];
+                int m = 0;
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int q = q0 + r * kUpdThreads;
-                    if (q >= ce) break;
-                    int lo_p = 0, hi_p = kChgParts - 1;           // the part holding chunk q
-                    while (lo_p < hi_p) {
-                        const int mid = (lo_p + hi_p + 1) >> 1;
-                        if (pchunk[mid] <= q) lo_p = mid; else hi_p = mid - 1;
+                for (int r = 0; r < kScanR; ++r) {
+                    const int q = q0 + 32 * r + lane;
+                    int64_t lim = 0;
+                    at[r] = 0;
+                    uint4 v = make_uint4(0, 0, 0, 0);
+                    if (q < n_chunks) {
+                        locate(q, at[r], lim);
+                        v = __ldg(reinterpret_cast<const uint4*>(onb + at[r]));
                     }
-                    at[r] = 2 * (int64_t)parts[lo_p].x + 16 * (int64_t)(q - pchunk[lo_p]);
-                    lim[r] = 2 * ((int64_t)parts[lo_p].x + parts[lo_p].y);
-                    v[r] = __ldg(reinterpret_cast<const uint4*>(onb + at[r]));
-                }
+                    w[r][0] = v.x; w[r][1] = v.y; w[r][2] = v.z; w[r][3] = v.w;
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    if (q0 + r * kUpdThreads >= ce) break;
-                    const uint32_t w[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
+                    for (int qq = 0; qq < 4; ++qq) {
+                        const int64_t rem = q < n_chunks ? lim - at[r] - 4 * qq : 0;   // valid bytes of the word
+                        uint32_t zz = zero_bytes((w[r][qq] & mask4) ^ want4);
+                        if (rem <= 0) zz = 0;
+                        else if (rem < 4) zz &= (1u << (8 * rem)) - 1u;
+                        z[r][qq] = zz;
+                        m += __popc(zz);
+                    }
+                }
+                int slot = warp_reserve(m, &n_raw, lane);
+#pragma unroll
+                for (int r = 0; r < kScanR; ++r)
 #pragma unroll
                     for (int qq = 0; qq < 4; ++qq)
-#pragma unroll
-                        for (int jj = 0; jj < 4; ++jj) {
-                            const int64_t j = at[r] + 4 * qq + jj;
-                            const uint32_t byte = (w[qq] >> (8 * jj)) & 0xFFu;
-                            if (j < lim[r] && (byte & keep) == (uint32_t)c0) f(j, byte);
+                        for (uint32_t zz = z[r][qq]; zz; zz &= zz - 1u) {
+                            const int byte = (__ffs(zz) - 1) >> 3;
+                            if (slot < kListCap) raw[slot] = entry(at[r] + 4 * qq + byte, (w[r][qq] >> (8 * byte)) & 0xFFu);
+                            ++slot;
                         }
-                }
             }
-        };
-        // one scan: counts, and the rows while the list has room
-        scan_changes(0, n_chunks, [&](int64_t j, uint32_t v) {
-            const int k = (int)v - c0, leaving = (int)(~j & 1);
-            atomicAdd(&dcnt[k], leaving ? -1 : 1);
-            touched[k] = 1;
-            atomicAdd(&bcnt[2 * k + leaving], 1);
-            const int pos = atomicAdd(&n_raw, 1);
-            if (pos < kListCap) raw[pos] = (tk[j >> 1] << 5) | (2 * k + leaving);
-        });
+        }
         __syncthreads();
         if (n_raw <= kListCap) {
+            count_raw(bcnt, 2 * G);
+            if (tid < G) {
+                dcnt[tid] = bcnt[2 * tid] - bcnt[2 * tid + 1];
+                touched[tid] = (bcnt[2 * tid] | bcnt[2 * tid + 1]) != 0;
+            }
             sort_raw(bcnt, 2 * G);
             sum_list(true);
             fold(false);
         } else {
             // more rows than the list holds: runs of chunks holding at most
-            // kListCap / 2 changes
+            // kListCap / 2 changes, each scanned again entry by entry
             for (int cb = 0; cb < n_chunks; cb += kListCap / 16) {
+                const int ce = min(n_chunks, cb + kListCap / 16);
                 __syncthreads();
                 if (tid < 2 * kMaxGroup) bcnt[tid] = 0;
                 if (tid == 0) n_raw = 0;
                 __syncthreads();
-                scan_changes(cb, min(n_chunks, cb + kListCap / 16), [&](int64_t j, uint32_t v) {
-                    const int k = (int)v - c0, leaving = (int)(~j & 1);
-                    atomicAdd(&bcnt[2 * k + leaving], 1);
-                    raw[atomicAdd(&n_raw, 1)] = (tk[j >> 1] << 5) | (2 * k + leaving);
-                });
+                for (int q = cb + tid; q < ce; q += kUpdThreads) {
+                    int64_t at, lim;
+                    locate(q, at, lim);
+                    const uint4 v = __ldg(reinterpret_cast<const uint4*>(onb + at));
+                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                    for (int b = 0; b < 16 && at + b < lim; ++b) {
+                        const uint32_t byte = (w[b >> 2] >> (8 * (b & 3))) & 0xFFu;
+                        if ((byte & keep) == (uint32_t)c0) {
+                            const int e = entry(at + b, byte);
+                            atomicAdd(&bcnt[e & 31], 1);
+                            raw[atomicAdd(&n_raw, 1)] = e;
+                        }
+                    }
+                }
                 __syncthreads();
+                if (tid < G) {
+                    dcnt[tid] += bcnt[2 * tid] - bcnt[2 * tid + 1];
+                    if (bcnt[2 * tid] | bcnt[2 * tid + 1]) touched[tid] = 1;
+                }
                 sort_raw(bcnt, 2 * G);
                 sum_list(true);
                 fold(false);
@@ -723,20 +800,56 @@ __global__ void __launch_bounds__(kUpdThreads, 3) kmeans_update_kernel(UpdateArg
     clear_sums();
     __syncthreads();
     const bool packable = N < kPackLimit;
-    for_matching_bytes(idh, 0, N, keep, (uint32_t)c0, [&](int64_t n, uint32_t v) {
-        const int k = (int)v - c0;
-        atomicAdd(&cnt[k], 1);
-        if (packable) {
-            const int pos = atomicAdd(&n_raw, 1);
-            if (pos < kListCap) raw[pos] = ((int)n << 5) | k;
+    if (packable) {
+        // one scan of the ids: every member appended to raw while it has room
+        // (n_raw counts them all), one shared atomic per warp and round; the
+        // unaligned head and tail (at most 30 bytes) one atomic per member
+        const uint32_t mask4 = keep * 0x01010101u, want4 = (uint32_t)c0 * 0x01010101u;
+        int64_t pre = (int64_t)((16u - ((uint32_t)(uintptr_t)idh & 15u)) & 15u);
+        if (pre > N) pre = N;
+        const int64_t body = (N - pre) >> 4;
+        const uint4* pb = reinterpret_cast<const uint4*>(idh + pre);
+        auto put1 = [&](int64_t n, uint32_t v) {
+            if ((v & keep) == (uint32_t)c0) {
+                const int pos = atomicAdd(&n_raw, 1);
+                if (pos < kListCap) raw[pos] = ((int)n << 5) | ((int)v - c0);
+            }
+        };
+        for (int64_t i = tid; i < pre; i += kUpdThreads) put1(i, idh[i]);
+        for (int64_t n = pre + 16 * body + tid; n < N; n += kUpdThreads) put1(n, idh[n]);
+        for (int64_t i0 = (int64_t)warp * 32 * kScanR; i0 < body; i0 += kScanR * kUpdThreads) {
+            uint32_t w[kScanR][4], z[kScanR][4];
+            int m = 0;
+#pragma unroll
+            for (int r = 0; r < kScanR; ++r) {
+                const int64_t i = i0 + 32 * r + lane;
+                const uint4 v = i < body ? __ldg(pb + i) : make_uint4(0, 0, 0, 0);
+                w[r][0] = v.x; w[r][1] = v.y; w[r][2] = v.z; w[r][3] = v.w;
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) {
+                    const uint32_t zz = i < body ? zero_bytes((w[r][qq] & mask4) ^ want4) : 0u;
+                    z[r][qq] = zz;
+                    m += __popc(zz);
+                }
+            }
+            int slot = warp_reserve(m, &n_raw, lane);
+#pragma unroll
+            for (int r = 0; r < kScanR; ++r)
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq)
+                    for (uint32_t zz = z[r][qq]; zz; zz &= zz - 1u) {
+                        const int byte = (__ffs(zz) - 1) >> 3;
+                        const int64_t n = pre + 16 * (i0 + 32 * r + lane) + 4 * qq + byte;
+                        if (slot < kListCap) raw[slot] = ((int)n << 5) | ((int)((w[r][qq] >> (8 * byte)) & 0xFFu) - c0);
+                        ++slot;
+                    }
         }
-    });
+    }
     __syncthreads();
-    int total = 0;
-    for (int k = 0; k < G; ++k) total += cnt[k];
-    const bool one = packable && total <= kListCap;
+    const bool one = packable && n_raw <= kListCap;
     amax = 0.0f;
     if (one) {
+        count_raw(cnt, G);
         sort_raw(cnt, G);
         sum_list(false);
         __syncthreads();
@@ -747,6 +860,8 @@ __global__ void __launch_bounds__(kUpdThreads, 3) kmeans_update_kernel(UpdateArg
             if (tid < 2 * kMaxGroup) bcnt[tid] = 0;
             __syncthreads();
             for_matching_bytes(idh, t0, t1, keep, (uint32_t)c0, [&](int64_t, uint32_t v) { atomicAdd(&bcnt[(int)v - c0], 1); });
+            __syncthreads();
+            if (tid < G) cnt[tid] += bcnt[tid];
             set_offsets(bcnt, G);
             for_matching_bytes(idh, t0, t1, keep, (uint32_t)c0,
                                [&](int64_t n, uint32_t v) { list[atomicAdd(&cur[(int)v - c0], 1)] = (int)n; });
