@@ -387,6 +387,7 @@ constexpr int kUpdThreads = 256;
 constexpr int kListCap = 4096;                         // rows listed at once
 constexpr int kMaxGroup = 16;                          // clusters per CTA
 constexpr int kScanR = 2;                              // 16-byte chunks per lane and round of an id scan
+constexpr int kSumRows = 4;                            // token rows a unit has in flight
 constexpr int kFlushTerms = 255;                       // window terms a lane adds between flushes (|sum| < 2^30)
 constexpr int64_t kPackLimit = (int64_t)1 << 26;       // token index packed above a 5-bit bucket
 constexpr int kMaxGroupChannels = 1024;                // G * D: the group's int64 sums fit over the two lists
@@ -571,13 +572,13 @@ __global__ void __launch_bounds__(kUpdThreads, 3) kmeans_update_kernel(UpdateArg
             }
             terms = 0;
         };
-        for (int p0 = pb; p0 < pe; p0 += 4) {
-            uint4 v[4];
+        for (int p0 = pb; p0 < pe; p0 += kSumRows) {
+            uint4 v[kSumRows];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
+            for (int j = 0; j < kSumRows; ++j)
                 if (p0 + j < pe) v[j] = ldg_nc_v4(xs + (int64_t)list[p0 + j] * a.token_stride);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < kSumRows; ++j) {
                 const int p = p0 + j;
                 if (p >= pe) break;
                 if (p >= off[b + 1] || terms == kFlushTerms) {
