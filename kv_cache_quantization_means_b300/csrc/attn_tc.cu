@@ -127,30 +127,87 @@ struct StageArgs {
     uint16_t *kscr, *vscr;
 };
 
-template <int D, int B>
+// A thread's four items (16 channels of a row: two of K, two of V) have all
+// their loads in flight at once: the ids first, then every centroid chunk,
+// code word and scale/zero word, then the arithmetic of decode_chunk.
+template <int D, int B, int S>
 __global__ void __launch_bounds__(256) attn_stage_kernel(StageArgs a) {
-    constexpr int CPR = D / 16, LD = D + 8;
+    constexpr int CPR = D / 16, LD = D + 8, WPT = B / 2, WPR = D * B / 32;
+    constexpr int PER = kStageRows * CPR;                 // items per tensor
+    constexpr int IT = 2 * PER / 256;                     // items per thread
+    static_assert(2 * PER % 256 == 0 && PER % 256 == 0, "whole items per thread, K before V");
     __shared__ __align__(16) uint16_t vt[kStageRows * LD];
     const int tid = threadIdx.x, hh = blockIdx.y, h = a.h0 + hh;
     const int64_t n0 = (int64_t)blockIdx.x * kStageRows;
     const int64_t stage_rows = (int64_t)a.H * a.cap;
-    for (int it = tid; it < 2 * kStageRows * CPR; it += 256) {
-        const bool is_v = it >= kStageRows * CPR;
-        const int j = is_v ? it - kStageRows * CPR : it;
-        const int r = j / CPR, c = j % CPR;
-        uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
-        if (n0 + r < a.n_keys) {
-            const int64_t row = (int64_t)h * a.cap + n0 + r;
-            if (is_v)
-                decode_chunk<D, B>(a.v_codes, a.v_meta, a.v_ids, a.v_cent, row, h, c, stage_rows, a.C, a.S, a.G, o0, o1);
-            else
-                decode_chunk<D, B>(a.k_codes, a.k_meta, a.k_ids, a.k_cent, row, h, c, stage_rows, a.C, a.S, a.G, o0, o1);
+    const int mpr = D / a.G;
+    int64_t row[IT];
+    int rr[IT], cc[IT], id[IT];
+    bool valid[IT];
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+        const bool is_v = it >= IT / 2;
+        const int j = tid + 256 * (is_v ? it - IT / 2 : it);
+        rr[it] = j / CPR;
+        cc[it] = j % CPR;
+        valid[it] = n0 + rr[it] < a.n_keys;
+        row[it] = (int64_t)h * a.cap + n0 + rr[it];
+        id[it] = (a.C > 0 && valid[it]) ? (is_v ? a.v_ids : a.k_ids)[row[it]] : 0;
+    }
+    uint4 c0[IT], c1[IT];
+    uint32_t cw[IT][S][WPT], mw[IT][S];
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+        const bool is_v = it >= IT / 2;
+        const uint32_t* codes = is_v ? a.v_codes : a.k_codes;
+        const uint32_t* meta = is_v ? a.v_meta : a.k_meta;
+        c0[it] = c1[it] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+#pragma unroll
+            for (int w = 0; w < WPT; ++w) cw[it][s][w] = 0;
+            mw[it][s] = 0;
         }
+        if (!valid[it]) continue;
+        if (a.C > 0) {
+            const uint16_t* cr = (is_v ? a.v_cent : a.k_cent) + ((int64_t)h * a.C + min(id[it], a.C - 1)) * D + cc[it] * 16;
+            c0[it] = __ldg(reinterpret_cast<const uint4*>(cr));
+            c1[it] = __ldg(reinterpret_cast<const uint4*>(cr + 8));
+        }
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            const int64_t srow = (int64_t)s * stage_rows + row[it];
+#pragma unroll
+            for (int w = 0; w < WPT; ++w) cw[it][s][w] = __ldg(codes + srow * WPR + cc[it] * WPT + w);
+            mw[it][s] = __ldg(meta + srow * mpr + (cc[it] * 16) / a.G);
+        }
+    }
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
+        const bool is_v = it >= IT / 2;
+        float acc[16];
+        if (a.C > 0) {
+            unpack16(c0[it], c1[it], acc);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+        }
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            if constexpr (B == 2) {
+                dequant_add16(acc, cw[it][s][0], mw[it][s]);
+            } else {
+                dequant_add8x4(acc, cw[it][s][0], mw[it][s]);
+                dequant_add8x4(acc + 8, cw[it][s][1], mw[it][s]);
+            }
+        }
+        uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
+        if (valid[it]) pack16_bf16(acc, o0, o1);
         if (is_v) {
-            *reinterpret_cast<uint4*>(vt + r * LD + 16 * c) = o0;
-            *reinterpret_cast<uint4*>(vt + r * LD + 16 * c + 8) = o1;
-        } else if (n0 + r < a.n_keys) {
-            uint16_t* kr = a.kscr + ((int64_t)hh * a.npad + n0 + r) * D + 16 * c;
+            *reinterpret_cast<uint4*>(vt + rr[it] * LD + 16 * cc[it]) = o0;
+            *reinterpret_cast<uint4*>(vt + rr[it] * LD + 16 * cc[it] + 8) = o1;
+        } else if (valid[it]) {
+            uint16_t* kr = a.kscr + ((int64_t)hh * a.npad + n0 + rr[it]) * D + 16 * cc[it];
             *reinterpret_cast<uint4*>(kr) = o0;
             *reinterpret_cast<uint4*>(kr + 8) = o1;
         }
@@ -166,6 +223,18 @@ __global__ void __launch_bounds__(256) attn_stage_kernel(StageArgs a) {
             w[k] = (uint32_t)vt[(8 * u + 2 * k) * LD + d] | ((uint32_t)vt[(8 * u + 2 * k + 1) * LD + d] << 16);
         *reinterpret_cast<uint4*>(a.vscr + ((int64_t)hh * D + d) * a.npad + n0 + 8 * u) = make_uint4(w[0], w[1], w[2], w[3]);
     }
+}
+
+template <int B>
+cudaError_t launch_stage(const StageArgs& sa, dim3 grid, cudaStream_t s) {
+    switch (sa.S) {
+        case 1: attn_stage_kernel<128, B, 1><<<grid, 256, 0, s>>>(sa); break;
+        case 2: attn_stage_kernel<128, B, 2><<<grid, 256, 0, s>>>(sa); break;
+        case 3: attn_stage_kernel<128, B, 3><<<grid, 256, 0, s>>>(sa); break;
+        case 4: attn_stage_kernel<128, B, 4><<<grid, 256, 0, s>>>(sa); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
 }
 
 // ------------------------------------------------------- attention kernel
@@ -512,7 +581,7 @@ cudaError_t launch_attention_staged(int D, const AttnArgs& a, void* ws, size_t w
                                     cudaStream_t s) {
     *launched = false;
     if (D != 128 || a.n_queries == 0 || !ws || ws_bytes < attention_staged_bytes(D, a.H, a.n_keys)) return cudaSuccess;
-    if (!(a.bits == 2 || a.bits == 4)) return cudaSuccess;
+    if (!(a.bits == 2 || a.bits == 4) || a.S < 1 || a.S > 4) return cudaSuccess;
     if (a.n_keys > (int64_t)INT32_MAX - kFaK || a.n_queries > (int64_t)INT32_MAX - kFaQ) return cudaSuccess;
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) || (reinterpret_cast<uintptr_t>(a.q) & 15u)) return cudaSuccess;
     CodecCtl ctl;
@@ -577,9 +646,8 @@ cudaError_t launch_attention_staged(int D, const AttnArgs& a, void* ws, size_t w
         const int hg = a.H - h0 < hg_max ? a.H - h0 : hg_max;
         sa.h0 = h0;
         const dim3 sgrid((unsigned)((a.n_keys + kStageRows - 1) / kStageRows), (unsigned)hg);
-        if (a.bits == 2) attn_stage_kernel<128, 2><<<sgrid, 256, 0, s>>>(sa);
-        else attn_stage_kernel<128, 4><<<sgrid, 256, 0, s>>>(sa);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        e = a.bits == 2 ? launch_stage<2>(sa, sgrid, s) : launch_stage<4>(sa, sgrid, s);
+        if (e != cudaSuccess) return e;
         fa.h0 = h0;
         const dim3 grid((unsigned)((a.n_queries + kFaQ - 1) / kFaQ), (unsigned)hg);
         attn_fa_kernel<<<grid, kFaThreads, kFaSmem, s>>>(qmap, kmap, vmap, fa);
