@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(kPrThreads, 1)
             const int64_t rowoff = (int64_t)h * a.n_tokens + n;
             // The decoder's loads do not depend on the MMA: the codes and
             // scale/zero words of the half row are issued before waiting for it.
-            uint32_t code[ENCODE ? 1 : S][WPH], meta[ENCODE ? 1 : S][MPH];
+            uint32_t code[ENCODE || S == 0 ? 1 : S][WPH], meta[ENCODE || S == 0 ? 1 : S][MPH];
             if (!ENCODE) {
 #pragma unroll
                 for (int s = 0; s < S; ++s) {
@@ -405,7 +405,7 @@ __global__ void __launch_bounds__(kPrThreads, 1)
             for (int c = 0; c < NP; ++c) {
                 const uint32_t tcol = tbase + (uint32_t)(c * CPT);
                 // the encoder's codes and scale/zero words of this pass
-                uint32_t ec[ENCODE ? S : 1][CPT / 16], em[ENCODE ? S : 1][GPP];
+                uint32_t ec[ENCODE && S > 0 ? S : 1][CPT / 16], em[ENCODE && S > 0 ? S : 1][GPP];
                 if (ENCODE) {
                     // residual r = x_{l+1} - pred, 16 channels at a time
                     float r[CPT];
@@ -549,6 +549,10 @@ cudaError_t coral_tc_g(bool encode, const CoralArgs& a, const CoralTcScratch& w,
     // the stage count is a template parameter: the epilogue's stage loops unroll
     auto kern = encode ? coral_predict_tc_kernel<G, true, 2> : coral_predict_tc_kernel<G, false, 2>;
     switch (a.S) {
+        case 0:                       // the prediction alone (the Coral + SAS hybrid)
+            if (encode) return cudaSuccess;
+            kern = coral_predict_tc_kernel<G, false, 0>;
+            break;
         case 1: kern = encode ? coral_predict_tc_kernel<G, true, 1> : coral_predict_tc_kernel<G, false, 1>; break;
         case 2: break;
         case 3: kern = encode ? coral_predict_tc_kernel<G, true, 3> : coral_predict_tc_kernel<G, false, 3>; break;
