@@ -794,50 +794,40 @@ def main():
 
     roof = kernel_rooflines(st, peaks)
 
-    # end to end through the C ABI with host buffers: pinned H2D of every
-    # layer's K/V, fit + encode + decode, D2H of the compressed stream.  The
-    # three are pipelined over (layer, tensor) units on their own streams:
-    # unit u is uploaded while earlier units compute, and its compressed
-    # buffers are read back as soon as it is encoded.
+    # end to end through the C ABI with host buffers: for every (layer,
+    # tensor), qvg_compress_host copies its K or V from pinned host memory,
+    # fits, encodes and decodes it, and copies the compressed stream back.
     e2e = None
     if not args.no_e2e:
         units = [(l, t) for l in range(layers) for t in (0, 1)]
         host_x = {u: st.x[u[0]][u[1]].cpu().pin_memory() for u in units}
         host_out = {u: torch.empty(st.compressed_bytes(), dtype=torch.uint8).pin_memory() for u in units}
         comp = torch.cuda.current_stream()
-        up, down = torch.cuda.Stream(), torch.cuda.Stream()
-        ev_in = {u: torch.cuda.Event() for u in units}
-        ev_done = {u: torch.cuda.Event() for u in units}
+        # one qvg_compress_host call per unit (host->device copy, fit, encode,
+        # decode, device->host copy of the encoding, all on the unit's stream),
+        # units dealt round-robin to three streams so that one unit's copies
+        # overlap another's kernels
+        lanes = [torch.cuda.Stream() for _ in range(3)]
+        N, D, H = st.N, st.D, st.H
 
         def e2e_step():
-            up.wait_stream(comp)                      # nothing starts before the timed region
-            down.wait_stream(comp)
-            with torch.cuda.stream(up):
-                for u in units:
-                    st.x[u[0]][u[1]].copy_(host_x[u], non_blocking=True)
-                    ev_in[u].record(up)
-            for u in units:
+            for ln in lanes:
+                ln.wait_stream(comp)                  # nothing starts before the timed region
+            for i, u in enumerate(units):
                 l, t = u
-                comp.wait_event(ev_in[u])
-                st.fit(l, t)
-                st.encode(l, t)
-                st.decode(l, t)
-                ev_done[u].record(comp)
-                with torch.cuda.stream(down):
-                    down.wait_event(ev_done[u])
-                    e, o = st.enc[l][t], 0
-                    for k in ("codes", "meta", "ids", "centroids"):
-                        nb = e[k].numel() * e[k].element_size()
-                        host_out[u][o:o + nb].copy_(e[k].view(torch.uint8), non_blocking=True)
-                        o += nb
-            comp.wait_stream(down)                    # the timed region ends after the last read-back
-            comp.wait_stream(up)
+                e, ln = st.enc[l][t], lanes[i % len(lanes)]
+                Q.qvg_compress_host(st.cfg, host_x[u], st.x[l][t], N, D, H * D, None, e["centroids"], e["ids"],
+                                    e["codes"], e["meta"], st.out[i % len(lanes)], host_out[u], st.ws[i % len(lanes)],
+                                    stream=ln)
+            for ln in lanes:
+                comp.wait_stream(ln)                  # the timed region ends after the last read-back
         e2e_step()
         te = time_fn(e2e_step, max(1, min(args.steps, 3)))
         te = max_over_ranks(te, world, "cuda")
         e2e = {"value": job_throughput(st.bytes_per_step, world, te), "unit": "GB/s",
                "h2d_bytes_per_step": st.bytes_per_step, "d2h_bytes_per_step": 2 * layers * st.compressed_bytes(),
-               "pipelined": "upload / compute / read-back on three streams, per (layer, tensor)"}
+               "pipelined": "qvg_compress_host per (layer, tensor): host->device copy, fit, encode, decode, "
+                            "device->host copy of the encoding; units round-robin on three streams"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:

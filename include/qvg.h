@@ -374,7 +374,24 @@ QVG_API qvg_status qvg_attention_decode(const qvg_config* cfg, const qvg_bf16* q
                                         float* out, int64_t out_head_stride, int64_t out_token_stride,
                                         qvg_stream stream);
 
-/* Bytes of the working buffer of qvg_attention_decode_staged for n_keys keys
+/* One (layer, tensor) end to end from host memory, all on `stream`: the copy
+ * of x from host to device (x_host holds the layout x_dev will have: the
+ * (n_tokens-1)*token_stride + (H-1)*head_stride + D elements from its start,
+ * ideally pinned), qvg_fit_centroids (C > 0; warm_start may be NULL), then
+ * qvg_encode with those ids, then (out_dev not NULL) qvg_decode of all rows
+ * into out_dev with x's strides, and the copy of the encoding to host_out:
+ * codes, meta, ids, centroids back to back, each sized as qvg_encoded_bytes
+ * gives for capacity = n_tokens and one version.  codes, meta, ids and
+ * centroids are device buffers of that size; the workspace is the fit's.
+ * Asynchronous: host_out is complete, and x_host free, when the stream
+ * reaches this point. */
+QVG_API qvg_status qvg_compress_host(const qvg_config* cfg, const qvg_bf16* x_host, qvg_bf16* x_dev, int64_t n_tokens,
+                                     int64_t head_stride, int64_t token_stride, const qvg_bf16* warm_start,
+                                     qvg_bf16* centroids, uint8_t* ids, uint32_t* codes, uint32_t* meta,
+                                     qvg_bf16* out_dev, void* host_out, size_t host_out_bytes, void* workspace,
+                                     size_t workspace_bytes, qvg_stream stream);
+
+/* Bytes of the working buffer of qvg_attention_decode_staged for n_keys keys/* Bytes of the working buffer of qvg_attention_decode_staged for n_keys keys
  * (0 when the tensor-core path does not apply: head_dim != 128).  Host only. */
 QVG_API qvg_status qvg_attention_workspace_bytes(const qvg_config* cfg, int64_t n_keys, size_t* bytes);
 

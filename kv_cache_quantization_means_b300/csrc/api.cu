@@ -416,6 +416,49 @@ qvg_status qvg_decode(const qvg_config* cfg, const uint32_t* codes, const uint32
                        out_head_stride, out_token_stride, (cudaStream_t)stream);
 }
 
+qvg_status qvg_compress_host(const qvg_config* cfg, const qvg_bf16* x_host, qvg_bf16* x_dev, int64_t n_tokens,
+                             int64_t head_stride, int64_t token_stride, const qvg_bf16* warm_start,
+                             qvg_bf16* centroids, uint8_t* ids, uint32_t* codes, uint32_t* meta, qvg_bf16* out_dev,
+                             void* host_out, size_t host_out_bytes, void* workspace, size_t workspace_bytes,
+                             qvg_stream stream) {
+    qvg_status st = check_config(cfg, false);
+    if (st) return st;
+    if (n_tokens < 1) return fail(QVG_ERR_INVALID_ARG, "n_tokens must be >= 1");
+    if (!x_host || !host_out) return fail(QVG_ERR_INVALID_ARG, "host buffers are NULL");
+    if ((st = check_input(cfg, x_dev, n_tokens, head_stride, token_stride, "x_dev"))) return st;
+    const int64_t span = (n_tokens - 1) * token_stride + (int64_t)(cfg->num_heads - 1) * head_stride + cfg->head_dim;
+    size_t cb = 0, mb = 0, ib = 0, xb = 0;
+    if ((st = qvg_encoded_bytes(cfg, n_tokens, 1, &cb, &mb, &ib, &xb))) return st;
+    if (host_out_bytes < cb + mb + ib + xb)
+        return fail(QVG_ERR_INVALID_ARG, "host_out too small: %zu < %zu bytes", host_out_bytes, cb + mb + ib + xb);
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaMemcpyAsync(x_dev, x_host, (size_t)span * sizeof(qvg_bf16), cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_status(e, "host-to-device copy");
+    if (cfg->num_clusters > 0) {
+        st = qvg_fit_centroids(cfg, x_dev, n_tokens, head_stride, token_stride, warm_start, centroids, ids, n_tokens,
+                               0, workspace, workspace_bytes, stream);
+        if (st) return st;
+    }
+    st = qvg_encode(cfg, x_dev, n_tokens, head_stride, token_stride, centroids, 0, codes, meta, ids, n_tokens, 0,
+                    workspace, workspace_bytes, stream);
+    if (st) return st;
+    if (out_dev) {
+        st = qvg_decode(cfg, codes, meta, ids, centroids, n_tokens, 0, n_tokens, out_dev, head_stride, token_stride,
+                        stream);
+        if (st) return st;
+    }
+    char* h = static_cast<char*>(host_out);
+    const void* src[4] = {codes, meta, ids, centroids};
+    const size_t nb[4] = {cb, mb, ib, xb};
+    for (int k = 0; k < 4; ++k) {
+        if (!nb[k]) continue;
+        if ((e = cudaMemcpyAsync(h, src[k], nb[k], cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+            return cuda_status(e, "device-to-host copy");
+        h += nb[k];
+    }
+    return ok();
+}
+
 qvg_status qvg_append_chunk(const qvg_config* cfg, qvg_cache* cache, const qvg_bf16* x, int64_t n_new,
                             int64_t head_stride, int64_t token_stride, int32_t refit, void* workspace,
                             size_t workspace_bytes, qvg_stream stream) {

@@ -20,7 +20,7 @@ EXPORTS = [
     "qvg_assign", "qvg_update", "qvg_encode", "qvg_decode", "qvg_append_chunk", "qvg_decode_cache",
     "coral_predict_encode", "coral_predict_decode", "coral_predict_encode_static", "coral_fit_block",
     "coral_sas_workspace_bytes", "coral_sas_encode", "coral_sas_decode", "qvg_attention_decode",
-    "qvg_attention_workspace_bytes", "qvg_attention_decode_staged",
+    "qvg_attention_workspace_bytes", "qvg_attention_decode_staged", "qvg_compress_host",
     "qvg_device_error", "qvg_debug_set_wait",
 ]
 
@@ -95,6 +95,7 @@ def load(path=LIB_PATH):
     L.qvg_attention_decode_staged.argtypes = [PCFG, P, I64, I64, I64, ctypes.POINTER(qvg_encoded_view),
                                               ctypes.POINTER(qvg_encoded_view), I64, I64, ctypes.c_float, P, I64,
                                               I64, P, ctypes.c_size_t, P]
+    L.qvg_compress_host.argtypes = [PCFG, P, P, I64, I64, I64, P, P, P, P, P, P, P, SZ, P, SZ, P]
     L.qvg_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), I32, P]
     L.qvg_debug_set_wait.argtypes = [ctypes.c_uint64, ctypes.c_uint32, P]
     for name in EXPORTS[2:]:
@@ -285,6 +286,15 @@ def qvg_attention_decode(cfg, q, n_queries, q_head_stride, q_token_stride, k, v,
     _check(load().qvg_attention_decode(ctypes.byref(cfg), _ptr(q), n_queries, q_head_stride, q_token_stride,
                                        ctypes.byref(k), ctypes.byref(v), capacity, n_keys, float(scale), _ptr(out),
                                        out_head_stride, out_token_stride, _stream(stream)))
+
+
+def qvg_compress_host(cfg, x_host, x_dev, n_tokens, head_stride, token_stride, warm_start, centroids, ids, codes,
+                      meta, out_dev, host_out, workspace, stream=None):
+    """x_host, host_out: (pinned) host tensors; the rest device tensors (out_dev may be None)."""
+    _check(load().qvg_compress_host(ctypes.byref(cfg), _ptr(x_host), _ptr(x_dev), n_tokens, head_stride, token_stride,
+                                    _ptr(warm_start), _ptr(centroids), _ptr(ids), _ptr(codes), _ptr(meta),
+                                    _ptr(out_dev), _ptr(host_out), _nbytes(host_out), _ptr(workspace),
+                                    _nbytes(workspace), _stream(stream)))
 
 
 def qvg_attention_workspace_bytes(cfg, n_keys):

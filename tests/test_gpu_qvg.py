@@ -205,6 +205,38 @@ def test_update_means_at_rounding_midpoints(qvg, oracle):
     np.testing.assert_array_equal(u16(c_dev).reshape(C, D), want)
 
 
+def test_compress_host_matches_device_calls(qvg):
+    """qvg_compress_host (host buffers in and out) gives the bytes of the
+    separate device calls: fit, encode, decode, then the encoding copied back."""
+    rng = np.random.default_rng(31)
+    H, D, N, C, T, S, G = 3, 128, 1111, 32, 3, 2, 64
+    xb = np.stack([mixture(rng, N, D, M=12) for _ in range(H)])          # [H][N][D]
+    xt = np.ascontiguousarray(xb.transpose(1, 0, 2))                    # token-major [N][H][D]
+    cfg = qvg.config(H, D, C, T, S, G)
+    x_dev = to_dev(xt.reshape(-1))
+    ref = Encoded(qvg, cfg, N)
+    ws = qvg.alloc_workspace(cfg, N)
+    ref_out = torch.empty((N, H, D), dtype=torch.int16, device="cuda")
+    qvg.qvg_fit_centroids(cfg, x_dev, N, D, H * D, None, ref["centroids"], ref["ids"], N, 0, ws)
+    qvg.qvg_encode(cfg, x_dev, N, D, H * D, ref["centroids"], 0, ref["codes"], ref["meta"], ref["ids"], N, 0, ws)
+    qvg.qvg_decode(cfg, ref["codes"], ref["meta"], ref["ids"], ref["centroids"], N, 0, N, ref_out, D, H * D)
+    torch.cuda.synchronize()
+    host_x = torch.from_numpy(xt.reshape(-1).view(np.int16)).pin_memory()
+    cb, mb, ib, xbytes = qvg.qvg_encoded_bytes(cfg, N, 1)
+    host_out = torch.full((cb + mb + ib + xbytes,), 0xAB, dtype=torch.uint8).pin_memory()
+    got = Encoded(qvg, cfg, N)
+    staging = torch.empty_like(x_dev)
+    out = torch.empty_like(ref_out)
+    qvg.qvg_compress_host(cfg, host_x, staging, N, D, H * D, None, got["centroids"], got["ids"], got["codes"],
+                          got["meta"], out, host_out, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(staging, x_dev)
+    assert torch.equal(out, ref_out)
+    want = b"".join(ref[k].cpu().numpy().tobytes()[:n] for k, n in
+                    (("codes", cb), ("meta", mb), ("ids", ib), ("centroids", xbytes)))
+    assert host_out.numpy().tobytes() == want
+
+
 def test_ties_and_degenerate_inputs(qvg, oracle):
     """Exact duplicate tokens (ties at distance 0 between equal centroids),
     fewer tokens than clusters (duplicate initial centroids), constant rows
