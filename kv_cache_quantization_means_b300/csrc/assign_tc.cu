@@ -452,7 +452,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int pair = g * 4 + q;             // the two warps (halves) on these rows
         constexpr int NW = CP / 32;             // 32-column chunks = mask words
         constexpr int NWH = NW / 2;             // chunks per half
-        constexpr int NSH = 2 * NWH;            // 16-column tensor-memory reads per half
+        constexpr int NR = NWH;                 // 32-column tensor-memory reads per half
         constexpr int DH = D / 2;               // channels per half
         uint32_t* xw = reinterpret_cast<uint32_t*>(base + L.xch_off) + (size_t)pair * 2 * 8 * 32 + lane;
         auto xword = [&](int half, int w) -> uint32_t* { return xw + (half * 8 + w) * 32; };
@@ -472,14 +472,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint8_t* xs = Xs + (size_t)st * nA * kAtomBytes;
             const uint32_t taddr =
                 tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)g * acc_cols + 32u * (uint32_t)(hf * NWH);
-            uint32_t v[2][16];
+            uint32_t v[32];
             float pmax = -INFINITY, pxn = 0.0f;
             if (ok) {
                 tc_fence_after();
-                // The half's 2*NSH 16-column reads (pass A, then pass B) form
-                // one stream: read k+1 is in flight while read k is used, and
-                // the first overlaps the half's share of ||x||^2.
-                tmem_ld16(taddr, v[0]);
+                // Pass A reads the half's NR 32-column chunks one at a time
+                // (tensor-memory latency, not arithmetic, sets the pace, so
+                // fewer and wider reads beat overlapping narrower ones).
                 if (!load_norm) {
                     float2 s2 = make_float2(0.0f, 0.0f), t2 = make_float2(0.0f, 0.0f);
 #pragma unroll
@@ -494,22 +493,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     pxn = (s2.x + s2.y) + (t2.x + t2.y);
                 }
-                tmem_wait_ld_regs16(v[0]);
-                // pass A: the largest score of the half
                 float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int c = 0; c < NSH; ++c) {
-                    // next: read c+1 of pass A, or read 0 of pass B
-                    tmem_ld16(taddr + 16u * ((c + 1) % NSH), v[(c + 1) & 1]);
-                    const uint32_t* u = v[c & 1];
+                for (int c = 0; c < NR; ++c) {
+                    tmem_ld32(taddr + 32u * c, v);
+                    tmem_wait_ld_regs(v);
 #pragma unroll
-                    for (int jj = 0; jj < 16; jj += 8) {
-                        m4[0] = fmax3(m4[0], __uint_as_float(u[jj]), __uint_as_float(u[jj + 1]));
-                        m4[1] = fmax3(m4[1], __uint_as_float(u[jj + 2]), __uint_as_float(u[jj + 3]));
-                        m4[2] = fmax3(m4[2], __uint_as_float(u[jj + 4]), __uint_as_float(u[jj + 5]));
-                        m4[3] = fmax3(m4[3], __uint_as_float(u[jj + 6]), __uint_as_float(u[jj + 7]));
+                    for (int jj = 0; jj < 32; jj += 8) {
+                        m4[0] = fmax3(m4[0], __uint_as_float(v[jj]), __uint_as_float(v[jj + 1]));
+                        m4[1] = fmax3(m4[1], __uint_as_float(v[jj + 2]), __uint_as_float(v[jj + 3]));
+                        m4[2] = fmax3(m4[2], __uint_as_float(v[jj + 4]), __uint_as_float(v[jj + 5]));
+                        m4[3] = fmax3(m4[3], __uint_as_float(v[jj + 6]), __uint_as_float(v[jj + 7]));
                     }
-                    tmem_wait_ld_regs16(v[(c + 1) & 1]);
                 }
                 pmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
             }
@@ -532,24 +527,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // pass B: the half's candidates, the scores above thr.  E holds a
             // 1% margin over the error bound, so the nearest centroid's score
             // lies strictly above thr and the sign of the exactly rounded
-            // thr - score decides.  The signs are shifted into a word in
+            // thr - score decides.  A chunk's signs are shifted into a word in
             // column order (first column in the top bit), then bit-reversed.
-            // (NSH is even, so read 0 of pass B sits in buffer 0.)
             const float2 thr2 = make_float2(thr, thr);
-            uint32_t mw[NWH], mrev = 0u;
+            uint32_t mw[NWH];
 #pragma unroll
-            for (int c = 0; c < NSH; ++c) {
-                const int b = c & 1;
-                if (c + 1 < NSH) tmem_ld16(taddr + 16u * (c + 1), v[b ^ 1]);
-                const uint32_t* u = v[b];
+            for (int c = 0; c < NR; ++c) {
+                tmem_ld32(taddr + 32u * c, v);
+                tmem_wait_ld_regs(v);
+                uint32_t mrev = 0u;
 #pragma unroll
-                for (int jj = 0; jj < 16; jj += 2) {
-                    const float2 d = f2_sub(thr2, make_float2(__uint_as_float(u[jj]), __uint_as_float(u[jj + 1])));
+                for (int jj = 0; jj < 32; jj += 2) {
+                    const float2 d = f2_sub(thr2, make_float2(__uint_as_float(v[jj]), __uint_as_float(v[jj + 1])));
                     mrev = __funnelshift_l(__float_as_uint(d.x), mrev, 1);
                     mrev = __funnelshift_l(__float_as_uint(d.y), mrev, 1);
                 }
-                if (b == 1) mw[c >> 1] = __brev(mrev);
-                if (c + 1 < NSH) tmem_wait_ld_regs16(v[b ^ 1]);
+                mw[c] = __brev(mrev);
             }
             // accumulator drained: hand it back to the MMA issuer
             tc_fence_before();
