@@ -312,6 +312,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         fence_mbar_init();
     }
     __syncthreads();
+    // the first ring of token tiles is requested now, so that its copies land
+    // while the centroids are staged (a stage's first use needs no empty wait)
+    const bool withhold = (a.dbg & 1u) != 0;      // test: tile 0 never arrives
+    auto issue_tile = [&](int i) {
+        const int st = i % NS;
+        mbar_arrive_tx(full_bar + 8 * st, (uint32_t)(nA * kAtomBytes));
+        const int tok0 = (t_begin + i) * kTile;
+        for (int at = 0; at < nA; ++at) {
+            const uint32_t dst = smem_u32(Xs + (size_t)(st * nA + at) * kAtomBytes);
+            if (a.head_inner) tma_load_3d(dst, &tmap, full_bar + 8 * st, at * 64, h, tok0);
+            else tma_load_3d(dst, &tmap, full_bar + 8 * st, at * 64, tok0, h);
+        }
+    };
+    const int pre = n_tiles < NS ? n_tiles : NS;
+    if (tid == 0)
+        for (int i = 0; i < pre; ++i)
+            if (!(withhold && i == 0)) issue_tile(i);
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(misc)),
                      "r"(alloc_cols)
@@ -347,35 +364,39 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     }
     __syncthreads();
-    // -||c_j||^2 / 2 into the centroid side's extra block, one warp per centroid
-    for (int j = warp; j < Cpad; j += kTcThreads / 32) {
-        float sq = 0.0f;
-        for (int i = lane * 2; i < D; i += 64) {
-            const uint32_t w = *reinterpret_cast<const uint32_t*>(Bs + sw_off(j, i, cslab));
-            const float c0 = bf16_lo(w), c1 = bf16_hi(w);
-            sq = __fmaf_rn(c0, c0, sq);
-            sq = __fmaf_rn(c1, c1, sq);
+    // -||c_j||^2 / 2 into the centroid side's extra block, one thread per
+    // centroid (two fp32 chains of exact bf16 squares; any order of the sum
+    // obeys the screen's bound on the norm's rounding)
+    for (int j = tid; j < Cpad; j += kTcThreads) {
+        float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll 4
+        for (int i = 0; i < D; i += 8) {
+            const uint4 w = *reinterpret_cast<const uint4*>(Bs + sw_off(j, i, cslab));
+            s0 = __fmaf_rn(bf16_lo(w.x), bf16_lo(w.x), s0);
+            s1 = __fmaf_rn(bf16_hi(w.x), bf16_hi(w.x), s1);
+            s0 = __fmaf_rn(bf16_lo(w.y), bf16_lo(w.y), s0);
+            s1 = __fmaf_rn(bf16_hi(w.y), bf16_hi(w.y), s1);
+            s0 = __fmaf_rn(bf16_lo(w.z), bf16_lo(w.z), s0);
+            s1 = __fmaf_rn(bf16_hi(w.z), bf16_hi(w.z), s1);
+            s0 = __fmaf_rn(bf16_lo(w.w), bf16_lo(w.w), s0);
+            s1 = __fmaf_rn(bf16_hi(w.w), bf16_hi(w.w), s1);
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-        if (lane < 2) {
-            uint4 w = make_uint4(0, 0, 0, 0);
-            if (lane == 0) {
-                if (j < C) {
-                    const float v = -0.5f * sq;              // exact scaling
-                    const uint16_t hi = f32_to_bf16_bits(v);
-                    const float r1 = __fsub_rn(v, bf16f(hi));
-                    const uint16_t mid = f32_to_bf16_bits(r1);
-                    const uint16_t lo = f32_to_bf16_bits(__fsub_rn(r1, bf16f(mid)));
-                    w.x = (uint32_t)hi | ((uint32_t)mid << 16);
-                    w.y = lo;
-                } else {
-                    w.x = 0xFB80u;                           // -2^120: never the largest score
-                }
-            }
-            *reinterpret_cast<uint4*>(Bx + kx_off(j, lane)) = w;
-            if (lane == 0 && j < C) atomicMax(misc + 2, __float_as_uint(sq));
+        const float sq = __fadd_rn(s0, s1);
+        uint4 w0 = make_uint4(0, 0, 0, 0);
+        if (j < C) {
+            const float v = -0.5f * sq;              // exact scaling
+            const uint16_t hi = f32_to_bf16_bits(v);
+            const float r1 = __fsub_rn(v, bf16f(hi));
+            const uint16_t mid = f32_to_bf16_bits(r1);
+            const uint16_t lo = f32_to_bf16_bits(__fsub_rn(r1, bf16f(mid)));
+            w0.x = (uint32_t)hi | ((uint32_t)mid << 16);
+            w0.y = lo;
+            atomicMax(misc + 2, __float_as_uint(sq));
+        } else {
+            w0.x = 0xFB80u;                           // -2^120: never the largest score
         }
+        *reinterpret_cast<uint4*>(Bx + kx_off(j, 0)) = w0;
+        *reinterpret_cast<uint4*>(Bx + kx_off(j, 1)) = make_uint4(0, 0, 0, 0);
     }
     fence_async_smem();
     tc_fence_before();
@@ -388,21 +409,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
-            const bool withhold = (a.dbg & 1u) != 0;
-            int armed = 0;
-            for (int i = 0; i < n_tiles; ++i) {
+            int armed = pre;
+            for (int i = pre; i < n_tiles; ++i) {
                 const int st = i % NS;
                 const uint32_t ph = (uint32_t)(i / NS) & 1u;
                 if (!mbar_wait(empty_bar + 8 * st, ph ^ 1u, a.limit)) { atomicExch(misc + 1, 1u); break; }
                 if (*(volatile uint32_t*)(misc + 1)) break;
-                if (withhold && i == 0) continue;     // test: tile 0 never arrives
-                mbar_arrive_tx(full_bar + 8 * st, (uint32_t)(nA * kAtomBytes));
-                const int tok0 = (t_begin + i) * kTile;
-                for (int at = 0; at < nA; ++at) {
-                    const uint32_t dst = smem_u32(Xs + (size_t)(st * nA + at) * kAtomBytes);
-                    if (a.head_inner) tma_load_3d(dst, &tmap, full_bar + 8 * st, at * 64, h, tok0);
-                    else tma_load_3d(dst, &tmap, full_bar + 8 * st, at * 64, tok0, h);
-                }
+                issue_tile(i);
                 armed = i + 1;
             }
             // drain: every copy this thread issued has landed before exit
