@@ -62,6 +62,22 @@ def test_shape_variants_bit_exact(qvg, oracle, D, G, S, C):
         check_unit(oracle, xb[h], enc, dec, h, C, T, S, G)
 
 
+@pytest.mark.parametrize("D,C", [(64, 120), (64, 200), (64, 256), (128, 150), (128, 192), (128, 65)])
+def test_assign_tile_widths_bit_exact(qvg, oracle, D, C):
+    """The tensor-core assign at each padded centroid count it is built for
+    (C rounded up to a multiple of 64: 128, 192 and 256 with D = 64; 192 with
+    D = 128; and 128 with 63 padding columns, whose scores must never win): a
+    fit's centroids and ids, the encode and the decode bit-exact against the
+    oracle on 1500 tokens per head (a ragged last tile)."""
+    rng = np.random.default_rng(D * 1000 + C)
+    H, N, T, S, G = 2, 1500, 2, 2, 64
+    xb = np.stack([mixture(rng, N, D, M=max(8, C // 2), spread=1.0, noise=0.15) for _ in range(H)])
+    cfg = qvg.config(H, D, C, T, S, G)
+    enc, dec = run_fit_encode_decode(qvg, cfg, to_dev(xb), N, N * D, D)
+    for h in range(H):
+        check_unit(oracle, xb[h], enc, dec, h, C, T, S, G)
+
+
 def test_token_major_layout_offsets_and_subrange_decode(qvg, oracle):
     """[N][H][D] input (head_stride = D, token_stride = H*D), rows written at an
     offset inside a larger buffer, and a decode of a sub-range."""
