@@ -144,6 +144,11 @@ CASES = [  # D, bits, S, G, C, token-major
     # 4-bit, one stage: the kernel's prefetching specialisation
     (128, 4, 1, 64, 16, True),
     (64, 4, 1, 16, 0, False),
+    # with the rows above, every (bits, S) form of the tensor-core path's staging decode
+    (128, 2, 1, 32, 8, False),
+    (128, 2, 3, 16, 16, True),
+    (128, 4, 3, 128, 0, False),
+    (128, 4, 4, 64, 8, True),
 ]
 
 
