@@ -52,13 +52,16 @@ def predictor(qvg, B, U, W):
     return p, dev
 
 
-# (tokens, rank, heads, group size): rank 32 runs the tcgen05 path (token
-# tiles of 128 with a ragged last tile), the other ranks the general one
-@pytest.mark.parametrize("N,R,H,G", [(300, 32, 4, None), (64, 16, 4, None), (129, 0, 4, None),
-                                     (300, 32, 4, 16), (300, 32, 4, 64), (1100, 32, 8, None)])
-def test_coral_chain_staged_parity(qvg, oracle, N, R, H, G):
+# (tokens, rank, heads, group size, stages): rank 32 runs the tcgen05 path
+# (token tiles of 128 with a ragged last tile), the other ranks the general
+# one; the last three rows give the tcgen05 path's other stage counts
+@pytest.mark.parametrize("N,R,H,G,S", [(300, 32, 4, None, None), (64, 16, 4, None, None), (129, 0, 4, None, None),
+                                       (300, 32, 4, 16, None), (300, 32, 4, 64, None), (1100, 32, 8, None, None),
+                                       (300, 32, 4, None, 1), (300, 32, 4, 16, 3), (129, 32, 4, 64, 4)])
+def test_coral_chain_staged_parity(qvg, oracle, N, R, H, G, S):
     wl = WL.CORAL
-    S, D, L = wl.stages, wl.head_dim, 4
+    D, L = wl.head_dim, 4
+    S = S or wl.stages
     G = G or wl.group_size
     small = WL.Workload(**{**wl.__dict__, "heads": H, "tokens": N, "layers": L, "rank": max(R, 16)})
     xs = SY.coral_layers(small, SY.K_TENSOR, 0, N)              # [L][N][H*D]
