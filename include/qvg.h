@@ -334,7 +334,9 @@ QVG_API qvg_status coral_sas_encode(const qvg_config* cfg, const coral_predictor
 
 /* Decoder twin of coral_sas_encode: xhat_next = bf16(pred + r_hat) from
  * xhat_prev, the predictor and the stored codes, meta, ids and centroids
- * (bit-identical to the encoder's xhat_next). */
+ * (bit-identical to the encoder's xhat_next).  r_hat is decoded first, into
+ * the workspace; the prediction kernel then adds it and rounds, so the fp32
+ * prediction is written only when pred_out is non-NULL. */
 QVG_API qvg_status coral_sas_decode(const qvg_config* cfg, const coral_predictor* pred, const qvg_bf16* xhat_prev,
                                     int64_t n_tokens, const uint32_t* codes, const uint32_t* meta, const uint8_t* ids,
                                     const qvg_bf16* centroids, qvg_bf16* xhat_next, float* pred_out,

@@ -247,8 +247,15 @@ __global__ void __launch_bounds__(kThreads, 2) coral_predict_kernel(CoralArgs a)
                 const int64_t srow = (int64_t)s * stage_stride + rowoff;
                 dequant_add16(acc, __ldg(a.codes + srow * (D / 16) + t), __ldg(a.meta + srow * (D / G) + (t * 16) / G));
             }
+            if (a.resid) {
+                // x_hat = bf16(... + r_hat): one fp32 addition, then the rounding
+                float rr[16];
+                unpack16(ldg_nc_v4(a.resid + elem), ldg_nc_v4(a.resid + elem + 8), rr);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) acc[i] = __fadd_rn(acc[i], rr[i]);
+            }
         }
-        if (valid) {
+        if (valid && a.xhat) {
             uint4 o0, o1;
             pack16_bf16(acc, o0, o1);
             *reinterpret_cast<uint4*>(a.xhat + elem) = o0;

@@ -214,8 +214,9 @@ struct PrArgs {
     int H, S, tiles;
     uint32_t* codes;         // [S][H][N][D/16]
     uint32_t* meta;          // [S][H][N][D/G]
-    uint16_t* xhat;          // [N][H*D] out
+    uint16_t* xhat;          // [N][H*D] out, or nullptr
     float* pred_out;         // optional [N][H*D]
+    const uint16_t* resid;   // optional [N][H*D] bf16, decoder with S = 0 only
     uint32_t* err;
 };
 
@@ -392,6 +393,14 @@ __global__ void __launch_bounds__(kPrThreads, 1)
                     for (int m = 0; m < MPH; ++m) meta[s][m] = valid ? __ldg(a.meta + srow * MPR + hf * MPH + m) : 0u;
                 }
             }
+            // the prediction-only decoder's residual rows, also ahead of the wait
+            constexpr bool RES = !ENCODE && S == 0;
+            uint4 rv[RES ? HALF / 8 : 1];
+            if constexpr (RES) {
+#pragma unroll
+                for (int v8 = 0; v8 < HALF / 8; ++v8)
+                    rv[v8] = valid && a.resid ? ldg_v4_l1(a.resid + elem0 + 8 * v8) : make_uint4(0, 0, 0, 0);
+            }
             if (!mbar_wait(tfull_bar + 8 * g, (uint32_t)(i >> 1) & 1u)) { misc[1] = 1; break; }
             // the encoder reads the stage's x_{l+1} tile: wait on the stage's own
             // arrival too, so the copy's bytes are visible to these threads
@@ -472,7 +481,16 @@ __global__ void __launch_bounds__(kPrThreads, 1)
                         if constexpr (ENCODE) dequant_add16(acc, ec[s][(16 * k) / 16], em[s][(16 * k) / G]);
                         else dequant_add16(acc, code[s][ch / 16], meta[s][ch / G]);
                     }
-                    if (valid) {
+                    if constexpr (RES) {
+                        // x_hat = bf16(pred + r_hat): one fp32 addition, then the rounding
+                        if (a.resid) {
+                            float rr[16];
+                            unpack16(rv[ch / 8], rv[ch / 8 + 1], rr);
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj) acc[jj] = __fadd_rn(acc[jj], rr[jj]);
+                        }
+                    }
+                    if (valid && a.xhat) {
                         uint4 o0, o1;
                         pack16_bf16(acc, o0, o1);
                         uint16_t* op = a.xhat + elem0 + ch;
@@ -564,6 +582,7 @@ cudaError_t coral_tc_g(bool encode, const CoralArgs& a, const CoralTcScratch& w,
     PrArgs pa;
     pa.n_tokens = N; pa.H = H; pa.S = a.S; pa.tiles = tiles;
     pa.codes = a.codes; pa.meta = a.meta; pa.xhat = a.xhat; pa.pred_out = a.pred_out;
+    pa.resid = a.S == 0 && !encode ? a.resid : nullptr;
     pa.err = w.err;
     const int items = tiles * H;
     const int grid = items < sm_count() ? items : sm_count();
@@ -596,7 +615,8 @@ cudaError_t launch_coral_tc(int D, int G, bool encode, const CoralArgs& a, const
     auto al = [](const void* p, uintptr_t m) { return (reinterpret_cast<uintptr_t>(p) & (m - 1)) == 0; };
     if (!al(a.xprev, 16) || !al(a.B, 16) || !al(w.t2, 128) || !al(w.wt, 128) || !al(w.ud, 128)) return cudaSuccess;
     // the epilogue moves 16-byte vectors of x_{l+1}, x_hat, codes and the prediction
-    if (!al(a.xnext, 16) || !al(a.xhat, 16) || !al(a.codes, 16) || !al(a.pred_out, 16)) return cudaSuccess;
+    if (!al(a.xnext, 16) || !al(a.xhat, 16) || !al(a.codes, 16) || !al(a.pred_out, 16) || !al(a.resid, 16))
+        return cudaSuccess;
     switch (G) {
         case 16: return coral_tc_g<16>(encode, a, w, launched, s);
         case 32: return coral_tc_g<32>(encode, a, w, launched, s);

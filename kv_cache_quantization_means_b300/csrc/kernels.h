@@ -99,8 +99,9 @@ struct CoralArgs {
     int H, S;
     uint32_t* codes;         // [S][H][N][D/16]
     uint32_t* meta;          // [S][H][N][D/G]
-    uint16_t* xhat;          // [N][H*D] out
+    uint16_t* xhat;          // [N][H*D] out, or nullptr: not stored
     float* pred_out;         // optional [N][H*D]
+    const uint16_t* resid;   // optional [N][H*D] bf16 (decode): added to the stage sum before the rounding
     float* lowrank;          // workspace [N][R]
     void* workspace;         // the whole workspace (tensor-core path)
     size_t workspace_bytes;
