@@ -388,6 +388,7 @@ constexpr int kListCap = 4096;                         // rows listed at once
 constexpr int kMaxGroup = 16;                          // clusters per CTA
 constexpr int kScanR = 2;                              // 16-byte chunks per lane and round of an id scan
 constexpr int kSumRows = 4;                            // token rows a unit has in flight
+constexpr int kSumAhead = 2 * kSumRows;                // rows ahead a unit asks into L2
 constexpr int kFlushTerms = 255;                       // window terms a lane adds between flushes (|sum| < 2^30)
 constexpr int64_t kPackLimit = (int64_t)1 << 26;       // token index packed above a 5-bit bucket
 constexpr int kMaxGroupChannels = 1024;                // G * D: the group's int64 sums fit over the two lists
@@ -573,6 +574,14 @@ __global__ void __launch_bounds__(kUpdThreads, 3) kmeans_update_kernel(UpdateArg
             terms = 0;
         };
         for (int p0 = pb; p0 < pe; p0 += kSumRows) {
+            // rows two rounds ahead are asked into L2 now, so that their loads
+            // there meet L2 latency rather than DRAM's (no registers held)
+#pragma unroll
+            for (int j = 0; j < kSumRows; ++j) {
+                const int pf = p0 + kSumAhead + j;
+                if (pf < pe)
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(xs + (int64_t)list[pf] * a.token_stride));
+            }
             uint4 v[kSumRows];
 #pragma unroll
             for (int j = 0; j < kSumRows; ++j)
