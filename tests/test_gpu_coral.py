@@ -200,9 +200,10 @@ def test_coral_fit_block_zero_input(qvg):
     assert np.all(u16(Bout) == 0)
 
 
-def sas_gpu_layer(qvg, cfg, pred, xprev_dev, xnext_dev, N, ws, bufs=None):
+def sas_gpu_layer(qvg, cfg, pred, xprev_dev, xnext_dev, N, ws, bufs=None, want_pred=True):
     """One layer of the Coral-KV + SAS hybrid through the C ABI: encode when
-    bufs is None (fresh poisoned outputs), else decode from bufs."""
+    bufs is None (fresh poisoned outputs), else decode from bufs.  want_pred
+    False passes no prediction buffer (the decoder then stores none)."""
     H, D, S, G, C = cfg.num_heads, cfg.head_dim, cfg.num_stages, cfg.group_size, cfg.num_clusters
     xh = torch.full((N, H * D), -1, dtype=torch.int16, device="cuda")
     pout = torch.empty((N, H * D), dtype=torch.float32, device="cuda")
@@ -215,7 +216,7 @@ def sas_gpu_layer(qvg, cfg, pred, xprev_dev, xnext_dev, N, ws, bufs=None):
                              bufs["cent"], xh, ws, pred_out=pout)
     else:
         qvg.coral_sas_decode(cfg, pred, xprev_dev, N, bufs["codes"], bufs["meta"], bufs["ids"], bufs["cent"], xh,
-                             ws, pred_out=pout)
+                             ws, pred_out=pout if want_pred else None)
     torch.cuda.synchronize()
     assert qvg.qvg_fit_stats(cfg, N, ws)[3] == 0      # no bounded wait expired
     return bufs, xh, pout
@@ -253,4 +254,8 @@ def test_coral_sas_hybrid_staged_parity(qvg, oracle, N, R, H):
         _, dxh, dp = sas_gpu_layer(qvg, cfg, pred, None if prev is None else to_dev(prev), None, N, ws, bufs=bufs)
         np.testing.assert_array_equal(u16(dxh), u16(xh))
         np.testing.assert_array_equal(dp.cpu().numpy(), gp)
+        # and without a prediction buffer (nothing but x_hat stored)
+        _, dxh2, _ = sas_gpu_layer(qvg, cfg, pred, None if prev is None else to_dev(prev), None, N, ws, bufs=bufs,
+                                   want_pred=False)
+        np.testing.assert_array_equal(u16(dxh2), u16(xh))
         prev = u16(xh)

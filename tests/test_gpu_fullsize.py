@@ -146,6 +146,45 @@ def test_coral_full_size_token_slices(qvg, oracle):
         prev = xh
 
 
+def test_coral_sas_full_size_decoder_rebuilds_encoder(qvg):
+    """The Coral-KV + SAS hybrid at the bench's layer size (16 heads x 16,384
+    tokens, C = 256, T = 4), two layers: the decoder, with and without a
+    prediction buffer, rebuilds the encoder's reconstruction bit for bit and
+    the same fp32 prediction, and the reconstruction is close to the input
+    (relative MSE below 1e-2)."""
+    wl = WL.CORAL
+    H, D, S, G, N = wl.heads, wl.head_dim, wl.stages, wl.group_size, wl.tokens
+    C, T, L = 256, 4, 2
+    xs = SG.coral_chain_gpu(wl, SY.K_TENSOR, n_layers=L)             # [L][N][HD] device
+    cfg = qvg.config(H, D, C, T, S, G)
+    ws = torch.empty(qvg.coral_sas_workspace_bytes(cfg, N), dtype=torch.uint8, device="cuda")
+    prev, pred = None, None
+    for l in range(L):
+        if l > 0:
+            Bd, Ud, Wd = SG.coral_predictor_device(wl, l - 1)
+            pred = qvg.qvg.coral_predictor(B=Bd.data_ptr(), U=Ud.data_ptr(), W=Wd.data_ptr(), rank=wl.rank)
+        codes = torch.empty(S * H * N * D // 16, dtype=torch.int32, device="cuda")
+        meta = torch.empty(S * H * N * D // G, dtype=torch.int32, device="cuda")
+        ids = torch.empty(H * N, dtype=torch.uint8, device="cuda")
+        cent = torch.empty(H * C * D, dtype=torch.int16, device="cuda")
+        xh = torch.empty((N, H * D), dtype=torch.int16, device="cuda")
+        pe = torch.empty((N, H * D), dtype=torch.float32, device="cuda")
+        qvg.coral_sas_encode(cfg, pred, prev, xs[l], N, codes, meta, ids, cent, xh, ws, pred_out=pe)
+        dx1 = torch.empty_like(xh)
+        pd = torch.empty_like(pe)
+        qvg.coral_sas_decode(cfg, pred, prev, N, codes, meta, ids, cent, dx1, ws, pred_out=pd)
+        dx2 = torch.empty_like(xh)
+        qvg.coral_sas_decode(cfg, pred, prev, N, codes, meta, ids, cent, dx2, ws)
+        torch.cuda.synchronize()
+        assert qvg.qvg_fit_stats(cfg, N, ws)[3] == 0
+        assert torch.equal(dx1, xh) and torch.equal(dx2, xh), f"layer {l}"
+        assert torch.equal(pd, pe), f"layer {l}"
+        x = SY.bf16_bits_to_f32(u16(xs[l])).astype(np.float64)
+        r = SY.bf16_bits_to_f32(u16(xh)).astype(np.float64)
+        assert np.mean((x - r) ** 2) / np.mean(x ** 2) < 1e-2, f"layer {l}"
+        prev = xh
+
+
 def test_bench_step_on_four_streams_matches_one_stream(qvg, oracle):
     """The bench times the Wan2.1 step with its (layer, tensor) units spread
     over four streams, a workspace per stream.  Four layers of that step must
