@@ -273,10 +273,10 @@ class CoralStep:
                           for _ in (0, 1)]
             # encode per layer: prediction (1 kernel at layer 0, else prep + low-rank + predict), residual,
             # k-means init + T x (assign + update), PRQ encode, decode, reconstruction;
-            # decode per layer: the residual's decode, then the prediction, whose kernel
-            # also forms x_hat = bf16(pred + r_hat)
+            # decode per layer: the prediction alone, whose kernel also decodes the residual
+            # and forms x_hat = bf16(pred + r_hat)
             enc = (1 + 5 + 2 * T) + (layers - 1) * (3 + 5 + 2 * T)
-            dec = (1 + 1) + (layers - 1) * (3 + 1)
+            dec = 1 + (layers - 1) * 3
             self.launches_per_step = 2 * (enc + dec)
 
     def pred(self, t, l):
@@ -665,8 +665,8 @@ def run_aux(args, Q, wl, peaks, world, rank, local):
         dec_bytes = n * (2 + wl.stages * (2 / 8 + 4 / wl.group_size) + 2)   # read x_hat_l, codes+meta; write x_hat_l+1
         if args.sas:
             dec_bytes += n / wl.head_dim                                      # + the residual's cluster ids
-        dom = {"kernel": ("coral+sas decode (residual decode, then prediction + reconstruction in one kernel, per "
-                          "layer)" if args.sas
+        dom = {"kernel": ("coral+sas decode (prediction, residual decode and reconstruction in one kernel per "
+                          "layer, after the low-rank projection)" if args.sas
                           else "coral decode (low-rank + predict/decode per layer)"), "bound": "hbm",
                "achieved": dec_bytes / t_dec / 1e9, "peak": hbm, "unit": "GB/s", "time_us": t_dec * 1e6}
         cfgb = {"workload": f"{wl.name}: {wl.layers} layers x {wl.heads} heads x head_dim {wl.head_dim} x {wl.tokens} "

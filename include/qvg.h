@@ -334,9 +334,11 @@ QVG_API qvg_status coral_sas_encode(const qvg_config* cfg, const coral_predictor
 
 /* Decoder twin of coral_sas_encode: xhat_next = bf16(pred + r_hat) from
  * xhat_prev, the predictor and the stored codes, meta, ids and centroids
- * (bit-identical to the encoder's xhat_next).  r_hat is decoded first, into
- * the workspace; the prediction kernel then adds it and rounds, so the fp32
- * prediction is written only when pred_out is non-NULL. */
+ * (bit-identical to the encoder's xhat_next).  One pass: the prediction
+ * kernel decodes r_hat itself (centroid row plus dequantised stages, rounded
+ * to bf16 as qvg_decode rounds it) and adds it to the prediction, so no
+ * residual buffer is written and the fp32 prediction only when pred_out is
+ * non-NULL. */
 QVG_API qvg_status coral_sas_decode(const qvg_config* cfg, const coral_predictor* pred, const qvg_bf16* xhat_prev,
                                     int64_t n_tokens, const uint32_t* codes, const uint32_t* meta, const uint8_t* ids,
                                     const qvg_bf16* centroids, qvg_bf16* xhat_next, float* pred_out,

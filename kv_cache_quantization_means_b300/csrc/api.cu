@@ -770,20 +770,33 @@ qvg_status sas_check(const qvg_config* cfg, const coral_predictor* pred, const q
 
 // The fp32 prediction from x_hat_l (zero without it) into P: the cross-layer
 // kernels with no quantisation stage.  Their error word goes to the fit's.
-// The layer's prediction (fp32) into P (may be NULL); with `resid` (the
-// decoded residual, bf16) also xhat = bf16(pred + resid), formed in the same
-// kernel, in the arithmetic of the separate reconstruction.
+// The residual's encoding, for the decoder (codes == NULL: none).
+struct SasResidual {
+    const uint32_t* codes = nullptr;
+    const uint32_t* meta = nullptr;
+    const uint8_t* ids = nullptr;
+    const qvg_bf16* centroids = nullptr;
+};
+
+// The layer's prediction (fp32) into P (may be NULL).  Given the residual's
+// encoding, the same kernel also forms xhat = bf16(pred + r_hat), r_hat being
+// the residual decoded exactly as qvg_decode decodes it.
 qvg_status sas_predict(const qvg_config* cfg, const coral_predictor* pred, const qvg_bf16* xhat_prev,
-                       int64_t n_tokens, const SasLayout& L, void* workspace, float* P, const qvg_bf16* resid,
+                       int64_t n_tokens, const SasLayout& L, void* workspace, float* P, const SasResidual& r,
                        qvg_bf16* xhat, const FitWorkspace& w, cudaStream_t s) {
     char* base = static_cast<char*>(workspace);
     qvg::CoralArgs a{};
     a.xprev = xhat_prev;
     a.B = xhat_prev ? pred->B : nullptr; a.U = xhat_prev ? pred->U : nullptr; a.W = xhat_prev ? pred->W : nullptr;
     a.R = xhat_prev ? pred->rank : 0;
-    a.n_tokens = n_tokens; a.H = cfg->num_heads; a.S = 0;
-    a.xhat = resid ? xhat : nullptr;
-    a.resid = resid;
+    a.n_tokens = n_tokens; a.H = cfg->num_heads;
+    a.S = r.codes ? cfg->num_stages : 0;
+    a.codes = const_cast<uint32_t*>(r.codes);
+    a.meta = const_cast<uint32_t*>(r.meta);
+    a.ids = r.ids;
+    a.cent = r.centroids;
+    a.C = cfg->num_clusters;
+    a.xhat = r.codes ? xhat : nullptr;
     a.pred_out = P;
     a.lowrank = reinterpret_cast<float*>(base + L.coral);
     a.workspace = base + L.coral;
@@ -834,7 +847,7 @@ qvg_status coral_sas_encode(const qvg_config* cfg, const coral_predictor* pred, 
     const int64_t HD = (int64_t)cfg->num_heads * cfg->head_dim, count = n_tokens * HD;
     cudaError_t e = cudaMemsetAsync(w.stats, 0, sizeof(unsigned long long) * 4, s);
     if (e != cudaSuccess) return cuda_status(e, "memset");
-    if ((st = sas_predict(cfg, pred, xhat_prev, n_tokens, L, workspace, P, nullptr, nullptr, w, s))) return st;
+    if ((st = sas_predict(cfg, pred, xhat_prev, n_tokens, L, workspace, P, SasResidual{}, nullptr, w, s))) return st;
     // the residual r = bf16(x_{l+1} - pred), smoothed and quantised like a KV tensor
     if ((e = qvg::launch_coral_residual(x_next, P, count, R, s)) != cudaSuccess) return cuda_status(e, "residual launch");
     e = qvg::launch_kmeans_init(cfg->head_dim, R, cfg->head_dim, HD, n_tokens, nullptr, cfg->num_heads,
@@ -863,15 +876,15 @@ qvg_status coral_sas_decode(const qvg_config* cfg, const coral_predictor* pred, 
     if (!aligned16(codes) || !aligned16(meta) || !aligned16(centroids) || !aligned16(xhat_next) || !aligned16(pred_out))
         return fail(QVG_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
     cudaStream_t s = (cudaStream_t)stream;
-    char* base = static_cast<char*>(workspace);
     FitWorkspace w = carve(cfg, n_tokens, workspace);
-    qvg_bf16* R = reinterpret_cast<qvg_bf16*>(base + L.res);
     cudaError_t e = cudaMemsetAsync(w.stats, 0, sizeof(unsigned long long) * 4, s);
     if (e != cudaSuccess) return cuda_status(e, "memset");
-    // the residual first, so that the prediction kernel forms x_hat itself
-    // (the fp32 prediction is stored only when the caller asks for it)
-    if ((st = sas_decode_residual(cfg, codes, meta, ids, centroids, n_tokens, R, s))) return st;
-    return sas_predict(cfg, pred, xhat_prev, n_tokens, L, workspace, pred_out, R, xhat_next, w, s);
+    // one pass: the prediction kernel decodes the residual (centroid row plus
+    // dequantised stages, rounded to bf16) and forms x_hat itself; the fp32
+    // prediction is stored only when the caller asks for it
+    SasResidual r;
+    r.codes = codes; r.meta = meta; r.ids = ids; r.centroids = centroids;
+    return sas_predict(cfg, pred, xhat_prev, n_tokens, L, workspace, pred_out, r, xhat_next, w, s);
 }
 
 }  // extern "C"

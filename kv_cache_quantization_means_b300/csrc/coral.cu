@@ -242,17 +242,22 @@ __global__ void __launch_bounds__(kThreads, 2) coral_predict_kernel(CoralArgs a)
                     if (t % TPG == 0) a.meta[srow * (D / G) + t / TPG] = meta;
                 }
             }
+        } else if (valid && a.cent) {
+            // a smoothed residual: r_hat = bf16(c[id] + d_1 + d_2 + ...), the QVG
+            // decoder's sum and rounding, then x_hat = bf16(pred + r_hat)
+            const uint16_t* cr = a.cent + ((int64_t)h * a.C + min((int)a.ids[rowoff], a.C - 1)) * D + t * 16;
+            float rr[16];
+            unpack16(ldg_nc_v4(cr), ldg_nc_v4(cr + 8), rr);
+            for (int s = 0; s < a.S; ++s) {
+                const int64_t srow = (int64_t)s * stage_stride + rowoff;
+                dequant_add16(rr, __ldg(a.codes + srow * (D / 16) + t), __ldg(a.meta + srow * (D / G) + (t * 16) / G));
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[i] = __fadd_rn(acc[i], __bfloat162float(__float2bfloat16_rn(rr[i])));
         } else if (valid) {
             for (int s = 0; s < a.S; ++s) {
                 const int64_t srow = (int64_t)s * stage_stride + rowoff;
                 dequant_add16(acc, __ldg(a.codes + srow * (D / 16) + t), __ldg(a.meta + srow * (D / G) + (t * 16) / G));
-            }
-            if (a.resid) {
-                // x_hat = bf16(... + r_hat): one fp32 addition, then the rounding
-                float rr[16];
-                unpack16(ldg_nc_v4(a.resid + elem), ldg_nc_v4(a.resid + elem + 8), rr);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) acc[i] = __fadd_rn(acc[i], rr[i]);
             }
         }
         if (valid && a.xhat) {

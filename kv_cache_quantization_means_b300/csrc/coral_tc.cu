@@ -216,7 +216,9 @@ struct PrArgs {
     uint32_t* meta;          // [S][H][N][D/G]
     uint16_t* xhat;          // [N][H*D] out, or nullptr
     float* pred_out;         // optional [N][H*D]
-    const uint16_t* resid;   // optional [N][H*D] bf16, decoder with S = 0 only
+    const uint8_t* ids;      // decoder, optional: the stages code a smoothed residual (ids [H][N],
+    const uint16_t* cent;    // centroids [H][C][D]); see CoralArgs
+    int C;
     uint32_t* err;
 };
 
@@ -393,13 +395,16 @@ __global__ void __launch_bounds__(kPrThreads, 1)
                     for (int m = 0; m < MPH; ++m) meta[s][m] = valid ? __ldg(a.meta + srow * MPR + hf * MPH + m) : 0u;
                 }
             }
-            // the prediction-only decoder's residual rows, also ahead of the wait
-            constexpr bool RES = !ENCODE && S == 0;
-            uint4 rv[RES ? HALF / 8 : 1];
-            if constexpr (RES) {
+            // a smoothed residual's centroid row (half of it), also ahead of the wait
+            constexpr bool HYB = !ENCODE && S > 0;
+            uint4 cv[HYB ? HALF / 8 : 1];
+            if constexpr (HYB) {
+                if (a.cent) {
+                    const int id = valid ? min((int)a.ids[rowoff], a.C - 1) : 0;
+                    const uint16_t* cr = a.cent + ((int64_t)h * a.C + id) * kDh + hf * HALF;
 #pragma unroll
-                for (int v8 = 0; v8 < HALF / 8; ++v8)
-                    rv[v8] = valid && a.resid ? ldg_v4_l1(a.resid + elem0 + 8 * v8) : make_uint4(0, 0, 0, 0);
+                    for (int v8 = 0; v8 < HALF / 8; ++v8) cv[v8] = valid ? ldg_v4_l1(cr + 8 * v8) : make_uint4(0, 0, 0, 0);
+                }
             }
             if (!mbar_wait(tfull_bar + 8 * g, (uint32_t)(i >> 1) & 1u)) { misc[1] = 1; break; }
             // the encoder reads the stage's x_{l+1} tile: wait on the stage's own
@@ -476,18 +481,23 @@ __global__ void __launch_bounds__(kPrThreads, 1)
                             *reinterpret_cast<float4*>(a.pred_out + elem0 + ch + jj) =
                                 make_float4(acc[jj], acc[jj + 1], acc[jj + 2], acc[jj + 3]);
                     }
+                    if constexpr (ENCODE) {
 #pragma unroll
-                    for (int s = 0; s < S; ++s) {
-                        if constexpr (ENCODE) dequant_add16(acc, ec[s][(16 * k) / 16], em[s][(16 * k) / G]);
-                        else dequant_add16(acc, code[s][ch / 16], meta[s][ch / G]);
-                    }
-                    if constexpr (RES) {
-                        // x_hat = bf16(pred + r_hat): one fp32 addition, then the rounding
-                        if (a.resid) {
+                        for (int s = 0; s < S; ++s) dequant_add16(acc, ec[s][(16 * k) / 16], em[s][(16 * k) / G]);
+                    } else if constexpr (HYB) {
+                        if (a.cent) {
+                            // r_hat = bf16(c[id] + d_1 + d_2 + ...), the QVG decoder's sum
+                            // and rounding, then x_hat = bf16(pred + r_hat): one fp32 addition
                             float rr[16];
-                            unpack16(rv[ch / 8], rv[ch / 8 + 1], rr);
+                            unpack16(cv[ch / 8], cv[ch / 8 + 1], rr);
 #pragma unroll
-                            for (int jj = 0; jj < 16; ++jj) acc[jj] = __fadd_rn(acc[jj], rr[jj]);
+                            for (int s = 0; s < S; ++s) dequant_add16(rr, code[s][ch / 16], meta[s][ch / G]);
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj)
+                                acc[jj] = __fadd_rn(acc[jj], __bfloat162float(__float2bfloat16_rn(rr[jj])));
+                        } else {
+#pragma unroll
+                            for (int s = 0; s < S; ++s) dequant_add16(acc, code[s][ch / 16], meta[s][ch / G]);
                         }
                     }
                     if (valid && a.xhat) {
@@ -582,7 +592,9 @@ cudaError_t coral_tc_g(bool encode, const CoralArgs& a, const CoralTcScratch& w,
     PrArgs pa;
     pa.n_tokens = N; pa.H = H; pa.S = a.S; pa.tiles = tiles;
     pa.codes = a.codes; pa.meta = a.meta; pa.xhat = a.xhat; pa.pred_out = a.pred_out;
-    pa.resid = a.S == 0 && !encode ? a.resid : nullptr;
+    pa.ids = encode ? nullptr : a.ids;
+    pa.cent = encode ? nullptr : a.cent;
+    pa.C = a.C;
     pa.err = w.err;
     const int items = tiles * H;
     const int grid = items < sm_count() ? items : sm_count();
@@ -615,7 +627,7 @@ cudaError_t launch_coral_tc(int D, int G, bool encode, const CoralArgs& a, const
     auto al = [](const void* p, uintptr_t m) { return (reinterpret_cast<uintptr_t>(p) & (m - 1)) == 0; };
     if (!al(a.xprev, 16) || !al(a.B, 16) || !al(w.t2, 128) || !al(w.wt, 128) || !al(w.ud, 128)) return cudaSuccess;
     // the epilogue moves 16-byte vectors of x_{l+1}, x_hat, codes and the prediction
-    if (!al(a.xnext, 16) || !al(a.xhat, 16) || !al(a.codes, 16) || !al(a.pred_out, 16) || !al(a.resid, 16))
+    if (!al(a.xnext, 16) || !al(a.xhat, 16) || !al(a.codes, 16) || !al(a.pred_out, 16) || !al(a.cent, 16))
         return cudaSuccess;
     switch (G) {
         case 16: return coral_tc_g<16>(encode, a, w, launched, s);

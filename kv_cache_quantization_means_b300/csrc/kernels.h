@@ -101,7 +101,11 @@ struct CoralArgs {
     uint32_t* meta;          // [S][H][N][D/G]
     uint16_t* xhat;          // [N][H*D] out, or nullptr: not stored
     float* pred_out;         // optional [N][H*D]
-    const uint16_t* resid;   // optional [N][H*D] bf16 (decode): added to the stage sum before the rounding
+    // decode, optional: the stages code a k-means-smoothed residual (ids [H][N], centroids [H][C][D]);
+    // xhat = bf16(pred + bf16(c[id] + stage sum)) instead of bf16(pred + stage sum)
+    const uint8_t* ids;
+    const uint16_t* cent;
+    int C;
     float* lowrank;          // workspace [N][R]
     void* workspace;         // the whole workspace (tensor-core path)
     size_t workspace_bytes;
