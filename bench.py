@@ -84,12 +84,19 @@ class ClockSampler:
         self.lines = []
 
     def __enter__(self):
+        self.first = 0
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            # the timed region starts once the sampler is running; samples taken
+            # before it (the first one) are not counted
+            deadline = time.monotonic() + 3.0
+            while not self.lines and time.monotonic() < deadline and self.proc.poll() is None:
+                time.sleep(0.005)
+            self.first = len(self.lines)
         except Exception:
             self.proc = None
         return self
@@ -109,7 +116,7 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in self.lines[self.first:]:
             p = [x.strip() for x in ln.split(",")]
             if len(p) < 8:
                 continue
