@@ -13,7 +13,9 @@
 //     shared memory and each token row is then PRQ-coded (encode) or
 //     rebuilt from its codes (decode).  Encode and decode run the identical
 //     prediction code, so the encoder's reconstruction equals the decoder's
-//     bit for bit.
+//     bit for bit.  Given a smoothed residual's ids and centroids the decode
+//     adds c[id] to the stages and rounds that residual to bf16 before adding
+//     it to the prediction (the Coral + SAS hybrid).
 #include "common.cuh"
 #include "kernels.h"
 #include "prq16.cuh"

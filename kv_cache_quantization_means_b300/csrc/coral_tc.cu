@@ -23,7 +23,10 @@
 //             scale/zero words and x_hat_{l+1} = bf16(((pred + d_1) + d_2)..);
 //             decode rebuilds x_hat_{l+1} from the codes.  Encoder and decoder
 //             run the identical prediction, so their reconstructions agree
-//             bit for bit.
+//             bit for bit.  Two decoder forms serve the Coral + SAS hybrid:
+//             S = 0 stores the prediction alone, and with the residual's ids
+//             and centroids the stages code a k-means-smoothed residual,
+//             x_hat_{l+1} = bf16(pred + bf16(c[id] + d_1 + d_2 ..)).
 // Every wait is a bounded mbarrier wait; on expiry the kernel records an
 // error code, drains its own copies and MMAs and frees its tensor memory.
 #include "common.cuh"
