@@ -9,7 +9,8 @@
 // One persistent CTA per SM works through a contiguous range of one head's
 // token tiles with warp-specialised roles:
 //   warp 0     TMA producer: token tiles (128 rows x 64 channels per copy,
-//              128-byte swizzle) into a ring of 2-3 shared-memory stages;
+//              128-byte swizzle) into a ring of 2-4 shared-memory stages,
+//              the first ring requested before the centroids are staged;
 //   warp 1     MMA issuer: tcgen05.mma (M = 128, N = C rounded up to 64,
 //              K = 16 per instruction) into one of two TMEM accumulators;
 //              also owns the TMEM allocation;
@@ -32,8 +33,9 @@
 // on k-means data) by parity and re-ranks each over the row's candidates with
 // direct fp32 distances (relative error bound), then with exact squared
 // distances in 128-bit integers, and for near-exact ties with the squared
-// distance in fp64 summed in channel order, exactly as the plain definition.  Centroids (K-major, 128-byte
-// swizzle) stay in shared memory for the whole CTA.  Every wait is a bounded
+// distance in fp64 summed in channel order, exactly as the plain definition.
+// Centroids (K-major, 128-byte swizzle) stay in shared memory for the whole
+// CTA.  Every wait is a bounded
 // wait on an mbarrier: on expiry the kernel records an error code, lets the
 // other roles drain and returns after freeing its tensor memory.
 #include <cuda.h>
