@@ -865,19 +865,37 @@ __global__ void __launch_bounds__(kUpdThreads, 3) kmeans_update_kernel(UpdateArg
         __syncthreads();
         for (int i = tid; i < ng * 3 * D; i += kUpdThreads) ks[i] = (long long)hi[i] * 32768 + lo[i];
     } else {
-        for (int64_t t0 = 0; t0 < N; t0 += kListCap) {
-            const int64_t t1 = min(N, t0 + kListCap);
+        // more members than the list holds: token spans sized from the
+        // member count to fill about three quarters of it (a span that still
+        // overflows is halved; kListCap tokens never can)
+        int64_t span = kListCap;
+        if (packable && n_raw > 0) {
+            const int64_t fit = (int64_t)((double)(3 * kListCap / 4) * (double)N / (double)n_raw);
+            if (fit > span) span = fit;
+        }
+        bool first = true;
+        for (int64_t t0 = 0; t0 < N;) {
+            const int64_t t1 = min(N, t0 + span);
             if (tid < 2 * kMaxGroup) bcnt[tid] = 0;
             __syncthreads();
             for_matching_bytes(idh, t0, t1, keep, (uint32_t)c0, [&](int64_t, uint32_t v) { atomicAdd(&bcnt[(int)v - c0], 1); });
             __syncthreads();
+            int members = 0;
+            for (int b = 0; b < G; ++b) members += bcnt[b];
+            __syncthreads();               // every thread has read the counts (the same decision) before they change
+            if (members > kListCap) {
+                span = span / 2 > kListCap ? span / 2 : kListCap;
+                continue;
+            }
             if (tid < G) cnt[tid] += bcnt[tid];
             set_offsets(bcnt, G);
             for_matching_bytes(idh, t0, t1, keep, (uint32_t)c0,
                                [&](int64_t n, uint32_t v) { list[atomicAdd(&cur[(int)v - c0], 1)] = (int)n; });
             __syncthreads();
             sum_list(false);
-            fold(t0 == 0);
+            fold(first);
+            first = false;
+            t0 = t1;
         }
     }
     if (!(amax < kWinMax)) big = 1;
