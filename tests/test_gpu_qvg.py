@@ -253,12 +253,13 @@ def test_compress_host_matches_device_calls(qvg):
     assert host_out.numpy().tobytes() == want
 
 
-def test_ties_and_degenerate_inputs(qvg, oracle):
+@pytest.mark.parametrize("D", [64, 128])
+def test_ties_and_degenerate_inputs(qvg, oracle, D):
     """Exact duplicate tokens (ties at distance 0 between equal centroids),
     fewer tokens than clusters (duplicate initial centroids), constant rows
-    (zero scale) and a single token."""
-    rng = np.random.default_rng(13)
-    D, G, S = 64, 32, 2
+    (zero scale) and a single token (one partial tile)."""
+    rng = np.random.default_rng(13 + D)
+    G, S = 32, 2
     base = mixture(rng, 40, D, M=3)
     cases = [
         np.concatenate([base, base, base[:7]]),                        # duplicates
@@ -404,3 +405,47 @@ def test_fit_reuses_workspace_without_stale_norms(qvg, oracle):
         np.testing.assert_array_equal(got_c[h], oc, err_msg=f"centroids head {h}")
         np.testing.assert_array_equal(got_i[h], oi, err_msg=f"ids head {h}")
     assert qvg.qvg_fit_stats(cfg, N, ws)[3] == 0
+
+
+def test_empty_inputs_write_nothing(qvg):
+    """Zero tokens: assign, update, encode, an empty decode range, the
+    cross-layer codec and attention with no queries return OK and write
+    nothing; the calls that need a token (fit, append, the hybrid) refuse
+    with an argument error and write nothing either."""
+    H, D, C, T, S, G = 2, 128, 16, 2, 2, 64
+    cap = 300
+    cfg = qvg.config(H, D, C, T, S, G)
+    enc = qvg.alloc_encoded(cfg, cap)
+    for k, t in enc.items():
+        t.fill_(0xFF if t.dtype == torch.uint8 else -1)
+    x = torch.zeros((cap, H, D), dtype=torch.int16, device="cuda")
+    ws = qvg.alloc_workspace(cfg, cap)
+    out = torch.full((cap, H, D), -1, dtype=torch.int16, device="cuda")
+    before = {k: t.clone() for k, t in enc.items()}
+    qvg.qvg_assign(cfg, x, 0, D, H * D, enc["centroids"], enc["ids"], cap, 0, ws)
+    qvg.qvg_update(cfg, x, 0, D, H * D, enc["ids"], cap, 0, enc["centroids"], ws)
+    qvg.qvg_encode(cfg, x, 0, D, H * D, enc["centroids"], 1, enc["codes"], enc["meta"], enc["ids"], cap, 0, ws)
+    qvg.qvg_decode(cfg, enc["codes"], enc["meta"], enc["ids"], enc["centroids"], cap, 7, 7, out, D, H * D)
+    with pytest.raises(qvg.QvgError):
+        qvg.qvg_fit_centroids(cfg, x, 0, D, H * D, None, enc["centroids"], enc["ids"], cap, 0, ws)
+    # cross-layer codec (no clusters) with no tokens
+    ccfg = qvg.config(H, D, 0, 0, S, G)
+    cws = qvg.alloc_workspace(ccfg, cap)
+    xh = torch.full((cap, H * D), -1, dtype=torch.int16, device="cuda")
+    qvg.coral_predict_encode(ccfg, None, None, x.view(cap, H * D), 0, enc["codes"], enc["meta"], xh, None, cws)
+    qvg.coral_predict_decode(ccfg, None, None, 0, enc["codes"], enc["meta"], xh, None, cws)
+    sws = torch.empty(qvg.coral_sas_workspace_bytes(cfg, cap), dtype=torch.uint8, device="cuda")
+    with pytest.raises(qvg.QvgError):
+        qvg.coral_sas_encode(cfg, None, None, x.view(cap, H * D), 0, enc["codes"], enc["meta"], enc["ids"],
+                             enc["centroids"], xh, sws)
+    # attention with no queries over a one-key history
+    q = torch.zeros((4, H, D), dtype=torch.int16, device="cuda")
+    ao = torch.full((4, H, D), float("nan"), dtype=torch.float32, device="cuda")
+    view = qvg.encoded_view(enc)
+    qvg.qvg_attention_decode(cfg, q, 0, D, H * D, view, view, cap, 1, 0.1, ao, D, H * D)
+    aws = torch.empty(max(1, qvg.qvg_attention_workspace_bytes(cfg, 1)), dtype=torch.uint8, device="cuda")
+    qvg.qvg_attention_decode_staged(cfg, q, 0, D, H * D, view, view, cap, 1, 0.1, ao, D, H * D, aws)
+    torch.cuda.synchronize()
+    for k, t in enc.items():
+        assert torch.equal(t, before[k]), k
+    assert bool((out == -1).all()) and bool((xh == -1).all()) and bool(torch.isnan(ao).all())
