@@ -242,11 +242,18 @@ class CoralStep:
         self.cfg = Q.config(H, D, 0, 0, S, G)
         self.N, self.H, self.D, self.HD = N, H, D, H * D
         self.x = [SG.coral_chain_gpu(wl, t, n_layers=layers) for t in (0, 1)]        # [L][N][HD]
-        self.preds, self.keep = [], []
+        self.preds, self.keep, self.layouts = [], [], []
         for l in range(layers - 1):
             B, U, W = SG.coral_predictor_device(wl, l)
             self.keep.append((B, U, W))
-            self.preds.append(Q.qvg.coral_predictor(B=B.data_ptr(), U=U.data_ptr(), W=W.data_ptr(), rank=wl.rank))
+            p = Q.qvg.coral_predictor(B=B.data_ptr(), U=U.data_ptr(), W=W.data_ptr(), rank=wl.rank)
+            # the predictor's U/W layout for the tensor cores, prepared once when it is loaded
+            lay = torch.empty(Q.coral_prepared_bytes(self.cfg, wl.rank), dtype=torch.uint8, device="cuda")
+            Q.coral_prepare_predictor(self.cfg, p, lay)
+            p.prepared = lay.data_ptr()
+            self.layouts.append(lay)
+            self.preds.append(p)
+        torch.cuda.synchronize()
         # adapted configuration: per tensor and layer a block refit into its own buffer
         self.fit_B, self.fit_preds = [], []
         if adapted:
@@ -254,7 +261,8 @@ class CoralStep:
                 bs = [torch.empty(H * D * D, dtype=torch.int16, device="cuda") for _ in range(layers - 1)]
                 self.fit_B.append(bs)
                 self.fit_preds.append([Q.qvg.coral_predictor(B=bs[l].data_ptr(), U=self.keep[l][1].data_ptr(),
-                                                             W=self.keep[l][2].data_ptr(), rank=wl.rank)
+                                                             W=self.keep[l][2].data_ptr(), rank=wl.rank,
+                                                             prepared=self.layouts[l].data_ptr())
                                        for l in range(layers - 1)])
         self.codes = [[torch.empty(S * H * N * D // 16, dtype=torch.int32, device="cuda") for _ in range(layers)]
                       for _ in (0, 1)]
@@ -266,9 +274,10 @@ class CoralStep:
         self.ws = [Q.alloc_workspace(self.cfg, N) for _ in (0, 1)]
         self.side = torch.cuda.Stream()
         self.bytes_per_step = 2 * layers * N * H * D * 2
-        # per tensor and direction: layer 0 (one kernel), then prep + low-rank + predict per layer;
-        # adapted: + prep + low-rank + Gram + reduce + solve per encoded layer
-        self.launches_per_step = 2 * (1 + 3 * (layers - 1)) * 2 + (2 * 5 * (layers - 1) if adapted else 0)
+        # per tensor and direction: layer 0 (one kernel), then low-rank + predict per layer (the
+        # predictors' layouts are prepared at load); adapted: + low-rank + Gram + reduce + solve per
+        # encoded layer
+        self.launches_per_step = 2 * (1 + 2 * (layers - 1)) * 2 + (2 * 4 * (layers - 1) if adapted else 0)
         if sas:
             # Coral-KV + SAS hybrid: the residual of every layer is k-means smoothed (C, T) and PRQ-coded
             C, T = sas_clusters, sas_iters
@@ -278,12 +287,12 @@ class CoralStep:
             self.ids = [[torch.empty(H * N, dtype=torch.uint8, device="cuda") for _ in range(layers)] for _ in (0, 1)]
             self.cents = [[torch.empty(H * C * D, dtype=torch.int16, device="cuda") for _ in range(layers)]
                           for _ in (0, 1)]
-            # encode per layer: prediction (1 kernel at layer 0, else prep + low-rank + predict), residual,
+            # encode per layer: prediction (1 kernel at layer 0, else low-rank + predict), residual,
             # k-means init + T x (assign + update), PRQ encode, decode, reconstruction;
             # decode per layer: the prediction alone, whose kernel also decodes the residual
             # and forms x_hat = bf16(pred + r_hat)
-            enc = (1 + 5 + 2 * T) + (layers - 1) * (3 + 5 + 2 * T)
-            dec = 1 + (layers - 1) * 3
+            enc = (1 + 5 + 2 * T) + (layers - 1) * (2 + 5 + 2 * T)
+            dec = 1 + (layers - 1) * 2
             self.launches_per_step = 2 * (enc + dec)
 
     def pred(self, t, l):
@@ -677,7 +686,7 @@ def run_aux(args, Q, wl, peaks, world, rank, local):
                           else "coral decode (low-rank + predict/decode per layer)"), "bound": "hbm",
                "achieved": dec_bytes / t_dec / 1e9, "peak": hbm, "unit": "GB/s", "time_us": t_dec * 1e6}
         cfgb = {"workload": f"{wl.name}: {wl.layers} layers x {wl.heads} heads x head_dim {wl.head_dim} x {wl.tokens} "
-                            f"tokens, K and V, closed-loop block-DPLR (rank {wl.rank}) + PRQ S={wl.stages} G={wl.group_size}, "
+                            f"tokens, K and V, closed-loop block-DPLR (rank {wl.rank}; U/W layouts prepared at load) + PRQ S={wl.stages} G={wl.group_size}, "
                             "encode chain + decode chain" + ("; adapted: each layer's block predictors refit "
                                                               "(least squares) before it is encoded" if args.adapted else "")
                             + ("; hybrid: each layer's bf16 prediction residual k-means smoothed (C=256 T=4) before "

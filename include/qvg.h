@@ -115,6 +115,10 @@ typedef struct {
     const qvg_bf16* U;   /* [H*D][R] */
     const qvg_bf16* W;   /* [H*D][R] */
     int32_t rank;        /* R, 0 = block-diagonal only; R % 16 == 0, R <= 64 */
+    /* Optional (NULL: none): U and W already laid out for the tensor-core
+     * path by coral_prepare_predictor, so that no call re-lays them out.  It
+     * depends on U and W only, so it stays valid when B is refit. */
+    const qvg_bf16* prepared;
 } coral_predictor;
 
 /* Message of the last failed call on this thread ("" if none). */
@@ -292,6 +296,18 @@ QVG_API qvg_status coral_predict_encode_static(const qvg_config* cfg, const cora
  * added in a fixed order, fp32 Cholesky solve; B_h = 0 when X_h is zero.
  * Needs C = 0, D = 128, rank 32, n_tokens >= 1 and qvg_workspace_bytes of
  * workspace (256-byte aligned); qvg_fit_stats reports its error word. */
+/* Bytes of the prepared layout of a rank-32 predictor's U and W for H heads
+ * of D = 128 (W transposed, then [U | U], each 256-byte aligned). */
+QVG_API qvg_status coral_prepared_bytes(const qvg_config* cfg, int32_t rank, size_t* bytes);
+
+/* Writes that layout of pred->U and pred->W (rank 32, head_dim 128) into
+ * `prepared` (device, caller-owned, 256-byte aligned, coral_prepared_bytes
+ * long).  Setting pred->prepared to it afterwards lets every call skip the
+ * re-layout (bit-identical results).  Errors: invalid arguments return an
+ * error code and launch nothing; asynchronous on `stream`. */
+QVG_API qvg_status coral_prepare_predictor(const qvg_config* cfg, const coral_predictor* pred, qvg_bf16* prepared,
+                                           size_t prepared_bytes, qvg_stream stream);
+
 QVG_API qvg_status coral_fit_block(const qvg_config* cfg, const coral_predictor* pred, const qvg_bf16* xhat_prev,
                                    const qvg_bf16* x_next, int64_t n_tokens, qvg_bf16* B_out, void* workspace,
                                    size_t workspace_bytes, qvg_stream stream);

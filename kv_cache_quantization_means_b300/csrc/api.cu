@@ -533,6 +533,16 @@ static void clear_coral_error(const qvg_config* cfg, int64_t n_tokens, void* ws,
     if (ws_bytes >= tc) cudaMemsetAsync(static_cast<char*>(ws) + tc - 256, 0, sizeof(uint32_t), s);
 }
 
+// A prepared layout (coral_prepare_predictor) is for the rank-32, D = 128
+// tensor-core path and must be 256-byte aligned.
+static qvg_status check_prepared(const qvg_config* cfg, const coral_predictor* pred) {
+    if (!pred->prepared) return QVG_OK;
+    if (pred->rank != 32 || cfg->head_dim != 128)
+        return fail(QVG_ERR_UNSUPPORTED, "a prepared predictor layout needs rank 32 and head_dim 128");
+    if (((uintptr_t)pred->prepared & 255u) != 0) return fail(QVG_ERR_INVALID_ARG, "prepared layout must be 256-byte aligned");
+    return QVG_OK;
+}
+
 static qvg_status coral_common(const qvg_config* cfg, const coral_predictor* pred, const qvg_bf16* xhat_prev,
                                int64_t n_tokens, void* workspace, size_t workspace_bytes) {
     qvg_status st = check_config(cfg, false);
@@ -552,6 +562,7 @@ static qvg_status coral_common(const qvg_config* cfg, const coral_predictor* pre
         const size_t need = coral_ws_bytes(cfg, n_tokens);
         if (pred->rank > 0 && (!workspace || workspace_bytes < need))
             return fail(QVG_ERR_INVALID_ARG, "workspace too small: need %zu bytes", need);
+        if ((st = check_prepared(cfg, pred))) return st;
     }
     return QVG_OK;
 }
@@ -571,6 +582,7 @@ qvg_status coral_predict_encode(const qvg_config* cfg, const coral_predictor* pr
     a.xprev = xhat_prev; a.xnext = x_next;
     a.B = xhat_prev ? pred->B : nullptr; a.U = xhat_prev ? pred->U : nullptr; a.W = xhat_prev ? pred->W : nullptr;
     a.R = xhat_prev ? pred->rank : 0;
+    a.prepared = xhat_prev ? pred->prepared : nullptr;
     a.n_tokens = n_tokens; a.H = cfg->num_heads; a.S = cfg->num_stages;
     a.codes = codes; a.meta = meta; a.xhat = xhat_next; a.pred_out = pred_out;
     a.lowrank = (float*)workspace;
@@ -579,6 +591,31 @@ qvg_status coral_predict_encode(const qvg_config* cfg, const coral_predictor* pr
     if (workspace) clear_coral_error(cfg, n_tokens, workspace, workspace_bytes, (cudaStream_t)stream);
     return cuda_status(qvg::launch_coral(cfg->head_dim, cfg->group_size, true, a, (cudaStream_t)stream),
                        "coral launch");
+}
+
+qvg_status coral_prepared_bytes(const qvg_config* cfg, int32_t rank, size_t* bytes) {
+    qvg_status st = check_config(cfg, false);
+    if (st) return st;
+    if (!bytes) return fail(QVG_ERR_INVALID_ARG, "bytes is NULL");
+    if (rank != 32 || cfg->head_dim != 128)
+        return fail(QVG_ERR_UNSUPPORTED, "a prepared predictor layout needs rank 32 and head_dim 128");
+    *bytes = qvg::coral_prepared_bytes(cfg->num_heads);
+    return ok();
+}
+
+qvg_status coral_prepare_predictor(const qvg_config* cfg, const coral_predictor* pred, qvg_bf16* prepared,
+                                   size_t prepared_bytes, qvg_stream stream) {
+    qvg_status st = check_config(cfg, false);
+    if (st) return st;
+    if (!pred || !pred->U || !pred->W || !prepared) return fail(QVG_ERR_INVALID_ARG, "predictor or buffer is NULL");
+    if (pred->rank != 32 || cfg->head_dim != 128)
+        return fail(QVG_ERR_UNSUPPORTED, "a prepared predictor layout needs rank 32 and head_dim 128");
+    if (!aligned16(pred->U) || !aligned16(pred->W)) return fail(QVG_ERR_INVALID_ARG, "U/W must be 16-byte aligned");
+    if (((uintptr_t)prepared & 255u) != 0) return fail(QVG_ERR_INVALID_ARG, "prepared layout must be 256-byte aligned");
+    const size_t need = qvg::coral_prepared_bytes(cfg->num_heads);
+    if (prepared_bytes < need) return fail(QVG_ERR_INVALID_ARG, "prepared buffer too small: need %zu bytes", need);
+    return cuda_status(qvg::launch_coral_prep(pred->W, pred->U, cfg->num_heads, prepared, (cudaStream_t)stream),
+                       "prep launch");
 }
 
 qvg_status coral_fit_block(const qvg_config* cfg, const coral_predictor* pred, const qvg_bf16* xhat_prev,
@@ -606,9 +643,12 @@ qvg_status coral_fit_block(const qvg_config* cfg, const coral_predictor* pred, c
     w.t2 = reinterpret_cast<uint16_t*>(base);
     w.wt = reinterpret_cast<uint16_t*>(base + align256(N * 64 * 2));
     w.ud = reinterpret_cast<uint16_t*>(base + align256(N * 64 * 2) + align256(32 * HD * 2));
+    if (pred->prepared) qvg::use_prepared(pred->prepared, cfg->num_heads, w);
     w.err = reinterpret_cast<uint32_t*>(base + tc - 256);
+    if ((st = check_prepared(cfg, pred))) return st;
     qvg::CoralArgs a{};
     a.xprev = xhat_prev; a.U = pred->U; a.W = pred->W; a.R = 32;
+    a.prepared = pred->prepared;
     a.n_tokens = n_tokens; a.H = cfg->num_heads; a.S = cfg->num_stages;
     cudaError_t e = qvg::launch_coral_lowrank_tc(a, w, s);
     if (e != cudaSuccess) return cuda_status(e, "low-rank launch");
@@ -630,6 +670,7 @@ qvg_status coral_predict_decode(const qvg_config* cfg, const coral_predictor* pr
     a.xprev = xhat_prev; a.xnext = nullptr;
     a.B = xhat_prev ? pred->B : nullptr; a.U = xhat_prev ? pred->U : nullptr; a.W = xhat_prev ? pred->W : nullptr;
     a.R = xhat_prev ? pred->rank : 0;
+    a.prepared = xhat_prev ? pred->prepared : nullptr;
     a.n_tokens = n_tokens; a.H = cfg->num_heads; a.S = cfg->num_stages;
     a.codes = const_cast<uint32_t*>(codes); a.meta = const_cast<uint32_t*>(meta);
     a.xhat = xhat_next; a.pred_out = pred_out;
@@ -712,6 +753,7 @@ qvg_status coral_predict_encode_static(const qvg_config* cfg, const coral_predic
     a.xprev = xhat_prev; a.xnext = x_next;
     a.B = xhat_prev ? pred->B : nullptr; a.U = xhat_prev ? pred->U : nullptr; a.W = xhat_prev ? pred->W : nullptr;
     a.R = xhat_prev ? pred->rank : 0;
+    a.prepared = xhat_prev ? pred->prepared : nullptr;
     a.n_tokens = n_tokens; a.H = cfg->num_heads; a.S = cfg->num_stages;
     a.codes = codes; a.meta = meta; a.xhat = xhat_next; a.pred_out = pred_out;
     a.lowrank = scratch;
@@ -789,6 +831,7 @@ qvg_status sas_predict(const qvg_config* cfg, const coral_predictor* pred, const
     a.xprev = xhat_prev;
     a.B = xhat_prev ? pred->B : nullptr; a.U = xhat_prev ? pred->U : nullptr; a.W = xhat_prev ? pred->W : nullptr;
     a.R = xhat_prev ? pred->rank : 0;
+    a.prepared = xhat_prev ? pred->prepared : nullptr;
     a.n_tokens = n_tokens; a.H = cfg->num_heads;
     a.S = r.codes ? cfg->num_stages : 0;
     a.codes = const_cast<uint32_t*>(r.codes);

@@ -292,6 +292,7 @@ cudaError_t coral_dg(bool encode, const CoralArgs& a, cudaStream_t s) {
         w.t2 = reinterpret_cast<uint16_t*>(base);
         w.wt = reinterpret_cast<uint16_t*>(base + a256(N * 64 * 2));
         w.ud = reinterpret_cast<uint16_t*>(base + a256(N * 64 * 2) + a256(32 * HD * 2));
+        if (a.prepared) use_prepared(a.prepared, a.H, w);
         w.err = a.err_out ? a.err_out
                           : reinterpret_cast<uint32_t*>(base + coral_tc_scratch_bytes(a.H, a.n_tokens) - 256);
         bool launched = false;

@@ -548,7 +548,9 @@ cudaError_t lowrank_stage(const CoralArgs& a, const CoralTcScratch& w, const CUt
                           cudaStream_t s) {
     const int HD = a.H * kDh;
     const int64_t N = a.n_tokens;
-    coral_prep_kernel<<<(unsigned)((HD + kPrepRows - 1) / kPrepRows), 256, 0, s>>>(a.W, a.U, HD, w.wt, w.ud);
+    // the re-layout of W and U, unless the caller prepared it once
+    if (!a.prepared)
+        coral_prep_kernel<<<(unsigned)((HD + kPrepRows - 1) / kPrepRows), 256, 0, s>>>(a.W, a.U, HD, w.wt, w.ud);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int tiles = (int)((N + kT - 1) / kT);
@@ -612,6 +614,27 @@ size_t coral_tc_scratch_bytes(int H, int64_t n_tokens) {
     const size_t HD = (size_t)H * kDh, N = (size_t)(n_tokens > 0 ? n_tokens : 1);
     auto a256 = [](size_t v) { return (v + 255) & ~(size_t)255; };
     return a256(N * 2 * kR * 2) + a256((size_t)kR * HD * 2) + a256(HD * 2 * kR * 2) + 256;
+}
+
+size_t coral_prepared_bytes(int H) {
+    const size_t HD = (size_t)H * kDh;
+    auto a256 = [](size_t v) { return (v + 255) & ~(size_t)255; };
+    return a256((size_t)kR * HD * 2) + a256(HD * 2 * kR * 2);
+}
+
+void use_prepared(const uint16_t* prepared, int H, CoralTcScratch& w) {
+    const size_t HD = (size_t)H * kDh;
+    const size_t wt_bytes = ((size_t)kR * HD * 2 + 255) & ~(size_t)255;
+    w.wt = const_cast<uint16_t*>(prepared);
+    w.ud = const_cast<uint16_t*>(prepared) + wt_bytes / 2;
+}
+
+cudaError_t launch_coral_prep(const uint16_t* W, const uint16_t* U, int H, uint16_t* prepared, cudaStream_t s) {
+    const int HD = H * kDh;
+    CoralTcScratch w{};
+    use_prepared(prepared, H, w);
+    coral_prep_kernel<<<(unsigned)((HD + kPrepRows - 1) / kPrepRows), 256, 0, s>>>(W, U, HD, w.wt, w.ud);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_coral_lowrank_tc(const CoralArgs& a, const CoralTcScratch& w, cudaStream_t s) {

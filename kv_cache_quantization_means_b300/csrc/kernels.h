@@ -106,6 +106,7 @@ struct CoralArgs {
     const uint8_t* ids;
     const uint16_t* cent;
     int C;
+    const uint16_t* prepared;  // optional: Wt, then [U | U], as coral_prepare_predictor lays them out
     float* lowrank;          // workspace [N][R]
     void* workspace;         // the whole workspace (tensor-core path)
     size_t workspace_bytes;
@@ -123,6 +124,12 @@ struct CoralTcScratch {
 // Bytes of CoralTcScratch for H heads of 128 and n_tokens tokens (including
 // the error word at the end).
 size_t coral_tc_scratch_bytes(int H, int64_t n_tokens);
+// The prepared layout of a rank-32 predictor's W and U (H heads of 128):
+// Wt [32][H*128], then Ud = [U | U] [H*128][64], each 256-byte aligned.
+size_t coral_prepared_bytes(int H);
+cudaError_t launch_coral_prep(const uint16_t* W, const uint16_t* U, int H, uint16_t* prepared, cudaStream_t s);
+// Points w's Wt and Ud at a prepared layout.
+void use_prepared(const uint16_t* prepared, int H, CoralTcScratch& w);
 
 // Each launcher returns cudaSuccess or the launch error; shapes are
 // validated by the caller.

@@ -19,6 +19,7 @@ EXPORTS = [
     "qvg_fit_centroids",
     "qvg_assign", "qvg_update", "qvg_encode", "qvg_decode", "qvg_append_chunk", "qvg_decode_cache",
     "coral_predict_encode", "coral_predict_decode", "coral_predict_encode_static", "coral_fit_block",
+    "coral_prepared_bytes", "coral_prepare_predictor",
     "coral_sas_workspace_bytes", "coral_sas_encode", "coral_sas_decode", "qvg_attention_decode",
     "qvg_attention_workspace_bytes", "qvg_attention_decode_staged", "qvg_compress_host",
     "qvg_device_error", "qvg_debug_set_wait",
@@ -48,7 +49,7 @@ class qvg_cache(ctypes.Structure):
 
 class coral_predictor(ctypes.Structure):
     _fields_ = [("B", ctypes.c_void_p), ("U", ctypes.c_void_p), ("W", ctypes.c_void_p),
-                ("rank", ctypes.c_int32)]
+                ("rank", ctypes.c_int32), ("prepared", ctypes.c_void_p)]
 
 
 class qvg_encoded_view(ctypes.Structure):
@@ -86,6 +87,8 @@ def load(path=LIB_PATH):
     L.coral_predict_encode_static.argtypes = [PCFG, ctypes.POINTER(coral_predictor), P, P, I64, P, P, P, P, P]
     L.coral_predict_decode.argtypes = [PCFG, ctypes.POINTER(coral_predictor), P, I64, P, P, P, P, P, SZ, P]
     L.coral_fit_block.argtypes = [PCFG, ctypes.POINTER(coral_predictor), P, P, I64, P, P, SZ, P]
+    L.coral_prepared_bytes.argtypes = [PCFG, I32, PSZ]
+    L.coral_prepare_predictor.argtypes = [PCFG, ctypes.POINTER(coral_predictor), P, SZ, P]
     L.coral_sas_workspace_bytes.argtypes = [PCFG, I64, PSZ]
     L.coral_sas_encode.argtypes = [PCFG, ctypes.POINTER(coral_predictor), P, P, I64, P, P, P, P, P, P, P, SZ, P]
     L.coral_sas_decode.argtypes = [PCFG, ctypes.POINTER(coral_predictor), P, I64, P, P, P, P, P, P, P, SZ, P]
@@ -232,6 +235,19 @@ def coral_predict_encode_static(cfg, pred, xhat_prev, x_next, n_tokens, codes, m
     _check(load().coral_predict_encode_static(ctypes.byref(cfg), ctypes.byref(pred) if pred is not None else None,
                                               _ptr(xhat_prev), _ptr(x_next), n_tokens, _ptr(codes), _ptr(meta),
                                               _ptr(xhat_next), _ptr(pred_out), _stream(stream)))
+
+
+def coral_prepared_bytes(cfg, rank=32):
+    b = ctypes.c_size_t()
+    _check(load().coral_prepared_bytes(ctypes.byref(cfg), rank, ctypes.byref(b)))
+    return b.value
+
+
+def coral_prepare_predictor(cfg, pred, prepared, stream=None):
+    """Lays pred's U and W out once into `prepared` (a device buffer of
+    coral_prepared_bytes); set pred.prepared to it afterwards."""
+    _check(load().coral_prepare_predictor(ctypes.byref(cfg), ctypes.byref(pred), _ptr(prepared), _nbytes(prepared),
+                                          _stream(stream)))
 
 
 def coral_fit_block(cfg, pred, xhat_prev, x_next, n_tokens, B_out, workspace, stream=None):

@@ -160,6 +160,39 @@ def test_coral_argument_checks(Q):
     assert L.coral_predict_encode(ctypes.byref(cq), *args[1:]) == 1   # clusters must be 0
 
 
+def test_coral_prepared_layout_checks(Q):
+    """The prepared predictor layout: its size, and the argument checks of
+    coral_prepare_predictor and of a predictor that carries one (all refused
+    on the host, nothing launched)."""
+    L = _raw(Q)
+    c = Q.config(4, 128, 0, 0, 2, 64)
+    sz = ctypes.c_size_t(0)
+    assert L.coral_prepared_bytes(ctypes.byref(c), 32, ctypes.byref(sz)) == 0
+    HD = 4 * 128
+    a256 = lambda v: (v + 255) // 256 * 256
+    assert sz.value == a256(32 * HD * 2) + a256(HD * 64 * 2)              # Wt, then [U | U]
+    assert L.coral_prepared_bytes(ctypes.byref(c), 16, ctypes.byref(sz)) == 2      # rank 32 only
+    c64 = Q.config(4, 64, 0, 0, 2, 64)
+    assert L.coral_prepared_bytes(ctypes.byref(c64), 32, ctypes.byref(sz)) == 2    # head_dim 128 only
+    need = Q.coral_prepared_bytes(c)
+    buf = 1 << 20                                                            # a 256-byte aligned address
+    pred = Q.qvg.coral_predictor(B=16, U=16, W=16, rank=32)
+    prep = lambda p, ptr=buf, n=need: L.coral_prepare_predictor(ctypes.byref(c), ctypes.byref(p), ptr, n, None)
+    assert prep(pred, ptr=None) == 1                                         # no buffer
+    assert prep(pred, ptr=buf + 16) == 1                                     # not 256-byte aligned
+    assert prep(pred, n=need - 1) == 1                                       # too small
+    assert prep(Q.qvg.coral_predictor(B=16, U=None, W=16, rank=32)) == 1     # U missing
+    assert prep(Q.qvg.coral_predictor(B=16, U=16, W=16, rank=16)) == 2       # rank 32 only
+    # a predictor carrying a layout it cannot use is refused by the codec calls
+    bad = Q.qvg.coral_predictor(B=16, U=16, W=16, rank=32, prepared=buf + 16)
+    ws = 1 << 24                                                             # workspace bytes claimed: enough
+    assert L.coral_predict_encode(ctypes.byref(c), ctypes.byref(bad), 16, 16, 10, 16, 16, 16, None, 256, ws,
+                                  None) == 1                                 # layout not 256-byte aligned
+    bad16 = Q.qvg.coral_predictor(B=16, U=16, W=16, rank=16, prepared=buf)
+    assert L.coral_predict_encode(ctypes.byref(c), ctypes.byref(bad16), 16, 16, 10, 16, 16, 16, None, 256, ws,
+                                  None) == 2                                 # layout with rank 16
+
+
 def test_coral_sas_argument_checks(Q):
     """The Coral + SAS hybrid validates its configuration, buffers and
     workspace on the host and launches nothing when they are wrong."""

@@ -183,6 +183,52 @@ def test_coral_fit_block_parity(qvg, oracle, N, H):
     assert np.all(np.abs(gp - p64) <= pred_bound(xs[0], Bg, U, W, H, D))
 
 
+def test_prepared_predictor_is_bit_identical(qvg):
+    """A predictor that carries its prepared U/W layout (coral_prepare_predictor)
+    gives, bit for bit, what one without it gives: codes, meta, reconstruction
+    and prediction of the encoder and the decoder, the refit block, and the
+    Coral + SAS hybrid's outputs."""
+    wl = WL.CORAL
+    H, D, S, G, N = 4, wl.head_dim, wl.stages, wl.group_size, 300
+    small = WL.Workload(**{**wl.__dict__, "heads": H, "tokens": N, "layers": 2, "rank": 32})
+    xs = SY.coral_layers(small, SY.K_TENSOR, 0, N)
+    cfg = qvg.config(H, D, 0, 0, S, G)
+    B, U, W = SY.coral_predictor(small, 0)
+    plain, keep = predictor(qvg, B, U, W)
+    lay = torch.empty(qvg.coral_prepared_bytes(cfg), dtype=torch.uint8, device="cuda")
+    qvg.coral_prepare_predictor(cfg, plain, lay)
+    prepared = qvg.qvg.coral_predictor(B=plain.B, U=plain.U, W=plain.W, rank=32, prepared=lay.data_ptr())
+    prev, nxt = to_dev(xs[0]), to_dev(xs[1])
+    e1 = gpu_layer(qvg, cfg, plain, prev, nxt, N)
+    e2 = gpu_layer(qvg, cfg, prepared, prev, nxt, N)
+    for u, v in zip(e1, e2):
+        assert torch.equal(u, v)
+    d1 = gpu_layer(qvg, cfg, plain, prev, None, N, encode=False, codes=e1[0], meta=e1[1])
+    d2 = gpu_layer(qvg, cfg, prepared, prev, None, N, encode=False, codes=e1[0], meta=e1[1])
+    assert torch.equal(d1[2], d2[2]) and torch.equal(d1[3], d2[3]) and torch.equal(d1[2], e1[2])
+    # the block refit (its low-rank projection uses the layout too)
+    ws = qvg.alloc_workspace(cfg, N)
+    outs = []
+    for p in (plain, prepared):
+        Bout = torch.full((H * D * D,), -1, dtype=torch.int16, device="cuda")
+        fp = qvg.qvg.coral_predictor(B=Bout.data_ptr(), U=p.U, W=p.W, rank=32, prepared=p.prepared)
+        qvg.coral_fit_block(cfg, fp, prev, nxt, N, Bout, ws)
+        torch.cuda.synchronize()
+        outs.append(Bout.clone())
+    assert torch.equal(outs[0], outs[1])
+    # the hybrid, both directions
+    scfg = qvg.config(H, D, 16, 2, S, G)
+    sws = torch.empty(qvg.coral_sas_workspace_bytes(scfg, N), dtype=torch.uint8, device="cuda")
+    r1 = sas_gpu_layer(qvg, scfg, plain, prev, nxt, N, sws)
+    r2 = sas_gpu_layer(qvg, scfg, prepared, prev, nxt, N, sws)
+    for k in r1[0]:
+        assert torch.equal(r1[0][k], r2[0][k]), k
+    assert torch.equal(r1[1], r2[1]) and torch.equal(r1[2], r2[2])
+    q1 = sas_gpu_layer(qvg, scfg, plain, prev, None, N, sws, bufs=r1[0])
+    q2 = sas_gpu_layer(qvg, scfg, prepared, prev, None, N, sws, bufs=r1[0])
+    assert torch.equal(q1[1], q2[1]) and torch.equal(q1[1], r1[1])
+
+
 def test_coral_fit_block_zero_input(qvg):
     wl = WL.CORAL
     H, D, N = 2, wl.head_dim, 500
